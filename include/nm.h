@@ -1,0 +1,226 @@
+/*
+ * nm.h - C ABI of the N:M structured-sparsity library for NVIDIA GB300 (sm_103a).
+ *
+ * The calls follow the workflow of the cuSPARSELt blog ("Exploiting NVIDIA
+ * Ampere Structured Sparsity with cuSPARSELt", the workflow list and the
+ * "Structured sparse matrix-matrix multiplication code example"): describe
+ * the product once (nm_spmm_plan), prune (nm_prune / nm_prune_transposable),
+ * check the pattern (nm_check), compress (nm_compress), then multiply
+ * (nm_spmm) as often as needed.
+ *
+ * Conventions shared by every call
+ *   - Matrices are dense row-major arrays with a leading dimension `ld`
+ *     counted in elements (ld >= cols).  Sizes are int64_t element counts.
+ *   - Every pointer argument that names matrix data is a DEVICE pointer owned
+ *     by the caller; the library never allocates, frees or keeps it.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream).  Arguments are validated on the host before anything is
+ *     enqueued; on an error nothing is launched and the stream is untouched.
+ *     No call synchronises the stream.
+ *   - A launch failure reported by the CUDA runtime returns NM_ERR_CUDA.
+ *     Results that depend on data (a violation count, a wait that gave up)
+ *     are written to caller-owned device int32 words.
+ *   - Element types: NM_F16 / NM_BF16 are IEEE binary16 / bfloat16 bit
+ *     patterns, NM_I8 is two's-complement int8.
+ *   - Magnitude order: |w| by value, NaN above every number (several NaNs
+ *     tie), int8 -128 has magnitude 128.  Equal magnitudes: lower position
+ *     wins.  Pruned slots of a dense output are written as +0.
+ *
+ * Storage formats
+ *   - 2:4 canonical metadata (NM_META_CANONICAL): per group of 4 consecutive
+ *     elements of a row one 4-bit code i0 | i1 << 2 (i0 < i1 the kept
+ *     positions).  Group g of a row is at bits 4*(g % 4) of uint16 word
+ *     g / 4; a row has ceil(cols/16) words; rows are packed back to back.
+ *   - 2:4 tensor-core metadata (NM_META_TC): the order in which the sparse
+ *     tensor core reads metadata for 128-row tiles of 16-bit operands, one
+ *     block per k-step of 32 columns.  It is a uint32 array of shape
+ *     [cols/32][S][4], S = ceil(rows/128)*128 slot rows of 16 bytes.  Word 0
+ *     of slot row 16b + 8h + i in block s holds, in its low 16 bits, the four
+ *     codes of row 16b+i for columns 32s+16h .. 32s+16h+15 and, in its high
+ *     16 bits, the same codes of row 16b+8+i.  Words 1..3 of every slot row
+ *     and the codes of rows past `rows` are 0x4 (positions 0 and 1), so the
+ *     tensor core only ever reads valid codes.  Needs cols % 32 == 0.
+ *   - N:M metadata for (n, m) != (2, 4): one uint8 position (0..m-1) per kept
+ *     value, in the same order as the values (NM_META_CANONICAL only).
+ *   - Compressed values: rows x (cols/m*n) elements, packed, kept entries in
+ *     ascending position order with their original bits.
+ *   - Bit masks: row-major, ceil(cols/32) uint32 words per row, bit c % 32 of
+ *     word c / 32 is element c.
+ */
+#ifndef NM_H_
+#define NM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* nm_stream_t;
+
+typedef enum {
+  NM_OK = 0,
+  NM_ERR_INVALID_ARG = 1, /* a size, pointer or enum is out of range            */
+  NM_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for         */
+  NM_ERR_MISALIGNED = 3,  /* a pointer or leading dimension breaks an alignment */
+  NM_ERR_CUDA = 4,        /* the CUDA runtime reported an error                  */
+  NM_ERR_TIMEOUT = 5      /* written to a status word: a bounded wait gave up    */
+} nm_status_t;
+
+typedef enum { NM_F16 = 0, NM_BF16 = 1, NM_I8 = 2, NM_F32 = 3, NM_I32 = 4 } nm_dtype_t;
+
+typedef enum { NM_META_CANONICAL = 0, NM_META_TC = 1 } nm_meta_layout_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nm_status_string(nm_status_t status);
+
+/* Library ABI version, currently 1. */
+int nm_version(void);
+
+/*
+ * nm_compressed_size - host-only size query (cuSPARSELt blog, code example,
+ * cusparseLtSpMMACompressedSize before the compressed buffer is allocated).
+ * Writes the byte sizes of the compressed values and of the metadata of a
+ * rows x cols matrix pruned n:m with the given metadata layout.
+ * Errors: NM_ERR_INVALID_ARG for bad sizes/NULL outputs, NM_ERR_UNSUPPORTED
+ * for NM_META_TC with (n,m) != (2,4) or a non-16-bit type or cols % 32 != 0.
+ */
+nm_status_t nm_compressed_size(int64_t rows, int64_t cols, nm_dtype_t dtype, int n, int m,
+                               nm_meta_layout_t layout, size_t* vals_bytes, size_t* meta_bytes);
+
+/*
+ * nm_prune - greedy N:M magnitude pruning along rows (apex PR #1631
+ * "[sparse] update support for arbitrary N:M settings sparse", extension 1,
+ * mn_1d_greedy; cuSPARSELt blog, cusparseLtSpMMAPrune in the code example).
+ * In every group of m consecutive elements of a row the n largest |w| are
+ * kept.  W: rows x cols, leading dimension ld.  W_out (nullable): pruned
+ * copy with leading dimension ld_out; it may be W itself (in-place, then
+ * ld_out == ld).  mask_bits (nullable): bit mask of the kept entries.
+ * Requires 1 <= n < m <= 32, cols % m == 0, dtype F16/BF16/I8.
+ */
+nm_status_t nm_prune(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int n, int m,
+                     void* W_out, int64_t ld_out, uint32_t* mask_bits, nm_stream_t stream);
+
+/*
+ * nm_compress - select and pack in one pass (cuSPARSELt blog, Figure 2 text
+ * and cusparseLtSpMMACompress).  The selection is nm_prune's rule applied to
+ * W itself, so an already pruned W keeps its nonzeros.  transpose = 0
+ * compresses W (groups along rows); transpose = 1 compresses W^T, i.e. the
+ * groups run down the columns of W and the outputs describe a cols x rows
+ * matrix.  vals and meta (either nullable) receive the compressed values and
+ * the metadata in `layout`.  Sizes come from nm_compressed_size for the
+ * compressed matrix's (rows, cols).
+ */
+nm_status_t nm_compress(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int n, int m,
+                        int transpose, nm_meta_layout_t layout, void* vals, void* meta, nm_stream_t stream);
+
+/*
+ * nm_decompress - inverse of nm_compress: scatter the values back to their
+ * positions, +0 everywhere else.  rows x cols is the dense shape; W_out has
+ * leading dimension ld_out.
+ */
+nm_status_t nm_decompress(const void* vals, const void* meta, int64_t rows, int64_t cols, nm_dtype_t dtype, int n,
+                          int m, nm_meta_layout_t layout, void* W_out, int64_t ld_out, nm_stream_t stream);
+
+/*
+ * nm_check - pattern check (cuSPARSELt blog, cusparseLtSpMMAPruneCheck):
+ * *d_violations (device int32, caller-owned) is set to the number of groups
+ * of m consecutive row elements holding more than n nonzeros (NaN counts as
+ * nonzero, -0 does not).  With transposable != 0 (2:4 only, rows % 4 == 0)
+ * the groups of 4 consecutive rows of every column, aligned to multiples of
+ * 4, are counted as well.  Zero means the matrix conforms.
+ */
+nm_status_t nm_check(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int n, int m,
+                     int transposable, int32_t* d_violations, nm_stream_t stream);
+
+/*
+ * nm_prune_transposable - 2:4 mask on 4x4 tiles that is 2:4 along rows and
+ * along columns (PyTorch issue #126420, maintainer reply: the forward W x
+ * and the backward W^T dL/dy both need 2:4), computed at run time.  Per tile
+ * the kept pattern is, among the 90 with two entries in every row and every
+ * column, the one with the largest float32 score ((p0+p1)+p2)+p3 where p_r
+ * is the float32 sum of row r's two kept magnitudes; ties go to the earliest
+ * pattern when row 0's pair is the outermost loop over the pairs
+ * (0,1),(0,2),(0,3),(1,2),(1,3),(2,3).  NaN magnitudes score +Inf.
+ * Outputs, each nullable: W_out (pruned copy, may alias W with ld_out == ld),
+ * mask_bits, vals/meta (compressed W, groups along rows, rows x cols/2) and
+ * valsT/metaT (compressed W^T, cols x rows/2), metadata in `layout`.
+ * Requires rows % 4 == 0 and cols % 4 == 0; NM_META_TC needs cols % 32 == 0
+ * for meta and rows % 32 == 0 for metaT.
+ */
+nm_status_t nm_prune_transposable(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype,
+                                  void* W_out, int64_t ld_out, uint32_t* mask_bits, void* vals, void* meta,
+                                  void* valsT, void* metaT, nm_meta_layout_t layout, nm_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The product D = alpha * op(A) * op(B) + beta * C  (cuSPARSELt blog, the
+ * GEMM paragraph: A is M x K, B is K x N, C and D are M x N; "N" layout =
+ * column-major, "T" = row-major; FP16/BF16 inputs accumulate in FP32, INT8
+ * inputs in INT32).
+ * ---------------------------------------------------------------------- */
+typedef enum {
+  NM_SPMM_SPARSE_A = 0,     /* A is N:M sparse, given compressed (values + metadata)                */
+  NM_SPMM_DENSE_MASKED = 1  /* A and B dense; the product is multiplied by a bit mask of D's shape  */
+} nm_spmm_mode_t;
+
+typedef enum {
+  NM_ROW = 0, /* row-major: the second index is contiguous */
+  NM_COL = 1  /* column-major: the first index is contiguous */
+} nm_order_t;
+
+typedef struct {
+  int64_t M, N, K;
+  nm_spmm_mode_t mode;
+  int n, m;                     /* sparsity of A (SPARSE_A)                                   */
+  nm_dtype_t ab_type;           /* F16, BF16 or I8                                            */
+  nm_dtype_t cd_type;           /* = ab_type for F16/BF16; I32 for I8                         */
+  nm_order_t order_a;           /* DENSE_MASKED: ROW = A stored M x K, COL = stored K x M     */
+  nm_order_t order_b;           /* ROW = B stored K x N, COL = B stored N x K                 */
+  nm_order_t order_cd;          /* ROW = C, D stored M x N, COL = stored N x M                */
+  int64_t lda, ldb, ldc, ldd;   /* leading dimensions in elements (lda: DENSE_MASKED only)    */
+  nm_meta_layout_t meta_layout; /* SPARSE_A 2:4 with F16/BF16 needs NM_META_TC                */
+} nm_spmm_desc_t;
+
+typedef struct nm_spmm_plan_s* nm_spmm_plan_t;
+
+/*
+ * nm_spmm_plan - validate a product description and choose its kernel and
+ * tile configuration once (cuSPARSELt blog, code example: matrix and matmul
+ * descriptors, algorithm selection, plan).  *plan is a host object owned by
+ * the caller until nm_spmm_plan_destroy; it is read-only afterwards and may
+ * be used from several host threads.
+ * Supported: SPARSE_A 2:4 F16/BF16 (tensor cores, B in NM_COL), SPARSE_A 2:4
+ * I8 -> I32 (canonical metadata, B in NM_COL), SPARSE_A n:m with m <= 32 and
+ * canonical metadata (CUDA-core gather, B in NM_COL), DENSE_MASKED F16/BF16
+ * (tensor cores, any orders).
+ */
+nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc);
+
+/* Device workspace bytes nm_spmm needs with this plan (may be 0). */
+nm_status_t nm_spmm_plan_workspace(nm_spmm_plan_t plan, size_t* bytes);
+
+nm_status_t nm_spmm_plan_destroy(nm_spmm_plan_t plan);
+
+/*
+ * nm_spmm - run a planned product (cuSPARSELt blog, cusparseLtMatmul).
+ * alpha, beta: HOST pointers to float (F16/BF16) or int32 (I8).  beta == 0
+ * means C is not read (it may be NULL).  A: compressed values (SPARSE_A) or
+ * dense A (DENSE_MASKED).  A_meta: metadata (SPARSE_A) or the bit mask of
+ * D's M x N shape in row-major order (DENSE_MASKED).  C may alias D.
+ * workspace: device buffer of at least nm_spmm_plan_workspace bytes (NULL if
+ * 0).  d_status (nullable, device int32): set to NM_ERR_TIMEOUT if a bounded
+ * pipeline wait gave up; it is not cleared by the call.
+ * Base pointers must be 16-byte aligned and leading dimensions multiples of
+ * 16 bytes (NM_ERR_MISALIGNED).
+ */
+nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const void* A_meta, const void* B,
+                    const void* beta, const void* C, void* D, void* workspace, size_t workspace_bytes,
+                    int32_t* d_status, nm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NM_H_ */

@@ -1,0 +1,322 @@
+// C ABI of the library (declared in include/nm.h): argument validation,
+// status codes, plans and dispatch to the kernels.  Nothing here allocates
+// device memory; every launch goes to the caller's stream.
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "nm_internal.h"
+
+namespace {
+
+bool is_elem(nm_dtype_t t) { return t == NM_F16 || t == NM_BF16 || t == NM_I8; }
+int64_t elem_size(nm_dtype_t t) {
+  switch (t) {
+    case NM_F16:
+    case NM_BF16: return 2;
+    case NM_I8: return 1;
+    case NM_F32:
+    case NM_I32: return 4;
+  }
+  return 0;
+}
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+nm_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? NM_OK : NM_ERR_CUDA; }
+
+nm_status_t check_nm(int n, int m) {
+  if (m < 2 || m > 32 || n < 1 || n >= m) return NM_ERR_INVALID_ARG;
+  return NM_OK;
+}
+
+// Validates a rows x cols matrix with leading dimension ld.
+nm_status_t check_matrix(const void* p, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t t, bool nullable) {
+  if (rows < 0 || cols < 0) return NM_ERR_INVALID_ARG;
+  if (p == nullptr) return (nullable || rows == 0 || cols == 0) ? NM_OK : NM_ERR_INVALID_ARG;
+  if (ld < cols || ld < 1) return NM_ERR_INVALID_ARG;
+  if (!aligned(p, (uintptr_t)elem_size(t))) return NM_ERR_MISALIGNED;
+  return NM_OK;
+}
+
+size_t tc_meta_bytes(int64_t rows, int64_t cols) {
+  return (size_t)((cols / 32) * (((rows + 127) / 128) * 128) * 16);
+}
+
+}  // namespace
+
+struct nm_spmm_plan_s {
+  nm_spmm_desc_t d;
+  int kind;  // 0 tc sparse, 1 tc dense masked, 2 gather n:m, 3 int8 mma.sp
+  int split_k;
+  size_t ws_bytes;
+};
+
+extern "C" {
+
+const char* nm_status_string(nm_status_t s) {
+  switch (s) {
+    case NM_OK: return "NM_OK";
+    case NM_ERR_INVALID_ARG: return "NM_ERR_INVALID_ARG";
+    case NM_ERR_UNSUPPORTED: return "NM_ERR_UNSUPPORTED";
+    case NM_ERR_MISALIGNED: return "NM_ERR_MISALIGNED";
+    case NM_ERR_CUDA: return "NM_ERR_CUDA";
+    case NM_ERR_TIMEOUT: return "NM_ERR_TIMEOUT";
+  }
+  return "NM_ERR_UNKNOWN";
+}
+
+int nm_version(void) { return 1; }
+
+nm_status_t nm_compressed_size(int64_t rows, int64_t cols, nm_dtype_t dtype, int n, int m, nm_meta_layout_t layout,
+                               size_t* vals_bytes, size_t* meta_bytes) {
+  if (vals_bytes == nullptr || meta_bytes == nullptr || rows < 0 || cols < 0 || !is_elem(dtype))
+    return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_nm(n, m)) return st;
+  if (cols % m) return NM_ERR_INVALID_ARG;
+  if (layout != NM_META_CANONICAL && layout != NM_META_TC) return NM_ERR_INVALID_ARG;
+  *vals_bytes = (size_t)(rows * (cols / m) * n * elem_size(dtype));
+  if (n == 2 && m == 4) {
+    if (layout == NM_META_TC) {
+      if (dtype == NM_I8 || cols % 32) return NM_ERR_UNSUPPORTED;
+      *meta_bytes = tc_meta_bytes(rows, cols);
+    } else {
+      *meta_bytes = (size_t)(rows * ((cols / 4 + 3) / 4) * 2);
+    }
+  } else {
+    if (layout == NM_META_TC) return NM_ERR_UNSUPPORTED;
+    *meta_bytes = (size_t)(rows * (cols / m) * n);
+  }
+  return NM_OK;
+}
+
+nm_status_t nm_prune(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int n, int m,
+                     void* W_out, int64_t ld_out, uint32_t* mask_bits, nm_stream_t stream) {
+  if (!is_elem(dtype)) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_nm(n, m)) return st;
+  if (cols % m) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_matrix(W, rows, cols, ld, dtype, false)) return st;
+  if (nm_status_t st = check_matrix(W_out, rows, cols, ld_out, dtype, true)) return st;
+  if (W_out == W && W != nullptr && ld_out != ld) return NM_ERR_INVALID_ARG;
+  if (mask_bits != nullptr && !aligned(mask_bits, 4)) return NM_ERR_MISALIGNED;
+  nmk::PruneLaunch a{};
+  a.dt = (int)dtype;
+  a.W = W;
+  a.rowsL = rows;
+  a.colsL = cols;
+  a.ld = ld;
+  a.trans = 0;
+  a.n = n;
+  a.m = m;
+  a.W_out = W_out;
+  a.ld_out = ld_out;
+  a.mask_bits = mask_bits;
+  return from_cuda(nmk::launch_prune(a, (cudaStream_t)stream));
+}
+
+nm_status_t nm_compress(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int n, int m,
+                        int transpose, nm_meta_layout_t layout, void* vals, void* meta, nm_stream_t stream) {
+  if (!is_elem(dtype) || (transpose != 0 && transpose != 1)) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_nm(n, m)) return st;
+  if (nm_status_t st = check_matrix(W, rows, cols, ld, dtype, false)) return st;
+  const int64_t rowsL = transpose ? cols : rows, colsL = transpose ? rows : cols;
+  size_t vb = 0, mb = 0;
+  if (nm_status_t st = nm_compressed_size(rowsL, colsL, dtype, n, m, layout, &vb, &mb)) return st;
+  if (vals != nullptr && !aligned(vals, (uintptr_t)elem_size(dtype))) return NM_ERR_MISALIGNED;
+  if (meta != nullptr && !aligned(meta, 4)) return NM_ERR_MISALIGNED;
+  nmk::PruneLaunch a{};
+  a.dt = (int)dtype;
+  a.W = W;
+  a.rowsL = rowsL;
+  a.colsL = colsL;
+  a.ld = ld;
+  a.trans = transpose;
+  a.n = n;
+  a.m = m;
+  a.vals = vals;
+  a.meta = meta;
+  a.meta_tc = layout == NM_META_TC;
+  return from_cuda(nmk::launch_prune(a, (cudaStream_t)stream));
+}
+
+nm_status_t nm_decompress(const void* vals, const void* meta, int64_t rows, int64_t cols, nm_dtype_t dtype, int n,
+                          int m, nm_meta_layout_t layout, void* W_out, int64_t ld_out, nm_stream_t stream) {
+  if (!is_elem(dtype)) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_nm(n, m)) return st;
+  size_t vb = 0, mb = 0;
+  if (nm_status_t st = nm_compressed_size(rows, cols, dtype, n, m, layout, &vb, &mb)) return st;
+  if (rows > 0 && cols > 0 && (vals == nullptr || meta == nullptr)) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_matrix(W_out, rows, cols, ld_out, dtype, false)) return st;
+  if (vals != nullptr && !aligned(vals, (uintptr_t)elem_size(dtype))) return NM_ERR_MISALIGNED;
+  if (meta != nullptr && !aligned(meta, 4)) return NM_ERR_MISALIGNED;
+  nmk::DecompressLaunch a{};
+  a.dt = (int)dtype;
+  a.vals = vals;
+  a.meta = meta;
+  a.rows = rows;
+  a.cols = cols;
+  a.n = n;
+  a.m = m;
+  a.meta_tc = layout == NM_META_TC;
+  a.W_out = W_out;
+  a.ld_out = ld_out;
+  return from_cuda(nmk::launch_decompress(a, (cudaStream_t)stream));
+}
+
+nm_status_t nm_check(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int n, int m,
+                     int transposable, int32_t* d_violations, nm_stream_t stream) {
+  if (!is_elem(dtype) || d_violations == nullptr) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_nm(n, m)) return st;
+  if (cols % m) return NM_ERR_INVALID_ARG;
+  if (transposable && (n != 2 || m != 4 || rows % 4)) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_matrix(W, rows, cols, ld, dtype, false)) return st;
+  if (!aligned(d_violations, 4)) return NM_ERR_MISALIGNED;
+  return from_cuda(nmk::launch_check((int)dtype, W, rows, cols, ld, n, m, transposable ? 1 : 0, d_violations,
+                                     (cudaStream_t)stream));
+}
+
+nm_status_t nm_prune_transposable(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype,
+                                  void* W_out, int64_t ld_out, uint32_t* mask_bits, void* vals, void* meta,
+                                  void* valsT, void* metaT, nm_meta_layout_t layout, nm_stream_t stream) {
+  if (!is_elem(dtype)) return NM_ERR_INVALID_ARG;
+  if (layout != NM_META_CANONICAL && layout != NM_META_TC) return NM_ERR_INVALID_ARG;
+  if (rows % 4 || cols % 4) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_matrix(W, rows, cols, ld, dtype, false)) return st;
+  if (nm_status_t st = check_matrix(W_out, rows, cols, ld_out, dtype, true)) return st;
+  if (W_out == W && W != nullptr && ld_out != ld) return NM_ERR_INVALID_ARG;
+  if (layout == NM_META_TC) {
+    if (dtype == NM_I8) return NM_ERR_UNSUPPORTED;
+    if (meta != nullptr && cols % 32) return NM_ERR_UNSUPPORTED;
+    if (metaT != nullptr && rows % 32) return NM_ERR_UNSUPPORTED;
+  }
+  const uintptr_t es = (uintptr_t)elem_size(dtype);
+  if ((vals && !aligned(vals, es)) || (valsT && !aligned(valsT, es)) || (meta && !aligned(meta, 4)) ||
+      (metaT && !aligned(metaT, 4)) || (mask_bits && !aligned(mask_bits, 4)))
+    return NM_ERR_MISALIGNED;
+  nmk::TransposableLaunch a{};
+  a.dt = (int)dtype;
+  a.W = W;
+  a.rows = rows;
+  a.cols = cols;
+  a.ld = ld;
+  a.W_out = W_out;
+  a.ld_out = ld_out;
+  a.mask_bits = mask_bits;
+  a.vals = vals;
+  a.meta = meta;
+  a.valsT = valsT;
+  a.metaT = metaT;
+  a.meta_tc = layout == NM_META_TC;
+  return from_cuda(nmk::launch_transposable(a, (cudaStream_t)stream));
+}
+
+// ------------------------------------------------------------------ products
+nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
+  if (plan == nullptr || desc == nullptr) return NM_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const nm_spmm_desc_t& d = *desc;
+  if (d.M < 0 || d.N < 0 || d.K < 0) return NM_ERR_INVALID_ARG;
+  if (!is_elem(d.ab_type)) return NM_ERR_INVALID_ARG;
+  const bool fp = d.ab_type != NM_I8;
+  if (fp ? d.cd_type != d.ab_type : d.cd_type != NM_I32) return NM_ERR_UNSUPPORTED;
+  if ((d.order_a != NM_ROW && d.order_a != NM_COL) || (d.order_b != NM_ROW && d.order_b != NM_COL) ||
+      (d.order_cd != NM_ROW && d.order_cd != NM_COL))
+    return NM_ERR_INVALID_ARG;
+  // leading dimensions
+  const int64_t es = elem_size(d.ab_type), eo = elem_size(d.cd_type);
+  const int64_t b_inner = d.order_b == NM_COL ? d.K : d.N;
+  const int64_t cd_inner = d.order_cd == NM_ROW ? d.N : d.M;
+  if (d.ldb < b_inner || d.ldb < 1 || d.ldc < 0 || d.ldd < cd_inner || d.ldd < 1) return NM_ERR_INVALID_ARG;
+  if (d.ldc != 0 && d.ldc < cd_inner) return NM_ERR_INVALID_ARG;
+  if ((d.ldb * es) % 16 || (d.ldd * eo) % 16 || (d.ldc * eo) % 16) return NM_ERR_MISALIGNED;
+  int kind = -1;
+  if (d.mode == NM_SPMM_SPARSE_A) {
+    if (nm_status_t st = check_nm(d.n, d.m)) return st;
+    if (d.K % d.m) return NM_ERR_INVALID_ARG;
+    if (d.order_b != NM_COL) return NM_ERR_UNSUPPORTED;
+    if (d.n == 2 && d.m == 4) {
+      if (fp) {
+        if (d.meta_layout != NM_META_TC) return NM_ERR_UNSUPPORTED;
+        if (d.K % 32) return NM_ERR_UNSUPPORTED;
+        kind = 0;
+      } else {
+        if (d.meta_layout != NM_META_CANONICAL) return NM_ERR_UNSUPPORTED;
+        if (d.K % 64) return NM_ERR_UNSUPPORTED;
+        return NM_ERR_UNSUPPORTED;  // int8 kernel not built yet
+      }
+    } else {
+      if (d.meta_layout != NM_META_CANONICAL || !fp) return NM_ERR_UNSUPPORTED;
+      kind = 2;
+    }
+  } else if (d.mode == NM_SPMM_DENSE_MASKED) {
+    if (!fp) return NM_ERR_UNSUPPORTED;
+    const int64_t a_inner = d.order_a == NM_ROW ? d.K : d.M;
+    if (d.lda < a_inner || d.lda < 1) return NM_ERR_INVALID_ARG;
+    if ((d.lda * es) % 16) return NM_ERR_MISALIGNED;
+    kind = 1;
+  } else {
+    return NM_ERR_INVALID_ARG;
+  }
+  nm_spmm_plan_s* p = new (std::nothrow) nm_spmm_plan_s;
+  if (p == nullptr) return NM_ERR_INVALID_ARG;
+  p->d = d;
+  p->kind = kind;
+  p->split_k = kind == 1 ? nmk::spmm_tc_dense_masked_split(d) : 1;
+  p->ws_bytes = kind == 1 ? nmk::spmm_tc_dense_masked_workspace(d, p->split_k) : 0;
+  *plan = p;
+  return NM_OK;
+}
+
+nm_status_t nm_spmm_plan_workspace(nm_spmm_plan_t plan, size_t* bytes) {
+  if (plan == nullptr || bytes == nullptr) return NM_ERR_INVALID_ARG;
+  *bytes = plan->ws_bytes;
+  return NM_OK;
+}
+
+nm_status_t nm_spmm_plan_destroy(nm_spmm_plan_t plan) {
+  delete plan;
+  return NM_OK;
+}
+
+nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const void* A_meta, const void* B,
+                    const void* beta, const void* C, void* D, void* workspace, size_t workspace_bytes,
+                    int32_t* d_status, nm_stream_t stream) {
+  if (plan == nullptr || alpha == nullptr || beta == nullptr) return NM_ERR_INVALID_ARG;
+  const nm_spmm_desc_t& d = plan->d;
+  nmk::SpmmLaunch a{};
+  a.d = d;
+  if (d.ab_type == NM_I8) {
+    std::memcpy(&a.alpha_i, alpha, 4);
+    std::memcpy(&a.beta_i, beta, 4);
+  } else {
+    std::memcpy(&a.alpha_f, alpha, 4);
+    std::memcpy(&a.beta_f, beta, 4);
+  }
+  const bool beta_zero = d.ab_type == NM_I8 ? a.beta_i == 0 : a.beta_f == 0.0f;
+  if (d.M == 0 || d.N == 0) return NM_OK;
+  if (A == nullptr || A_meta == nullptr || B == nullptr || D == nullptr) {
+    if (d.K > 0 || D == nullptr) return NM_ERR_INVALID_ARG;
+  }
+  if (!beta_zero && (C == nullptr || d.ldc == 0)) return NM_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(A_meta, 16) || !aligned(B, 16) || !aligned(D, 16) ||
+      (!beta_zero && !aligned(C, 16)) || (d_status && !aligned(d_status, 4)))
+    return NM_ERR_MISALIGNED;
+  if (workspace_bytes < plan->ws_bytes || (plan->ws_bytes > 0 && workspace == nullptr)) return NM_ERR_INVALID_ARG;
+  if (workspace != nullptr && !aligned(workspace, 16)) return NM_ERR_MISALIGNED;
+  a.A = A;
+  a.A_meta = A_meta;
+  a.B = B;
+  a.C = beta_zero ? nullptr : C;
+  a.D = D;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.d_status = d_status;
+  cudaStream_t s = (cudaStream_t)stream;
+  switch (plan->kind) {
+    case 0: return from_cuda(nmk::launch_spmm_tc_sparse(a, s));
+    case 1: return from_cuda(nmk::launch_spmm_tc_dense_masked(a, plan->split_k, s));
+    case 2: return from_cuda(nmk::launch_spmm_nm_gather(a, s));
+    case 3: return from_cuda(nmk::launch_spmm_i8(a, s));
+  }
+  return NM_ERR_INVALID_ARG;
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// Device-side helpers shared by the library's kernels: element traits and the
+// magnitude key that orders elements for N:M selection.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace nmk {
+
+// Element type tags, equal to nm_dtype_t values.
+constexpr int kF16 = 0, kBF16 = 1, kI8 = 2;
+
+template <int DT> struct Elem;
+template <> struct Elem<kF16> {
+  using T = uint16_t;
+  // |w| order on bit patterns: clear the sign; every NaN maps to one key above +Inf (0x7C00).
+  __device__ __forceinline__ static uint32_t key(T v) { return min((uint32_t)v & 0x7FFFu, 0x7C01u); }
+  __device__ __forceinline__ static bool nonzero(T v) { return (v & 0x7FFFu) != 0; }
+};
+template <> struct Elem<kBF16> {
+  using T = uint16_t;
+  __device__ __forceinline__ static uint32_t key(T v) { return min((uint32_t)v & 0x7FFFu, 0x7F81u); }
+  __device__ __forceinline__ static bool nonzero(T v) { return (v & 0x7FFFu) != 0; }
+};
+template <> struct Elem<kI8> {
+  using T = int8_t;
+  __device__ __forceinline__ static uint32_t key(T v) { return (uint32_t)abs((int)v); }  // |-128| = 128
+  __device__ __forceinline__ static bool nonzero(T v) { return v != 0; }
+};
+
+// Float32 magnitude used by the transposable tile score: exact for every
+// input type; NaN scores as +Inf.
+__device__ __forceinline__ float mag_f32(uint16_t v, int dt) {
+  float f;
+  if (dt == kF16) {
+    f = __half2float(__ushort_as_half(v));
+  } else {
+    f = __uint_as_float((uint32_t)v << 16);
+  }
+  f = fabsf(f);
+  return (f != f) ? __int_as_float(0x7F800000) : f;
+}
+
+// Tensor-core order of 2:4 metadata: for each k-step s (32 columns) a block of
+// `nslots` 16-byte slot rows; word 0 of slot row 16b + 8h + i holds the codes of
+// row 16b+i (low half) and row 16b+8+i (high half) for columns 32s+16h..+15,
+// words 1..3 are filler (code 0x4).  Byte offset of the 16-bit half that holds
+// 16-column segment k of row r:
+__host__ __device__ __forceinline__ int64_t tc_half_offset(int64_t r, int64_t k, int64_t nslots) {
+  const int64_t slot = (r & ~int64_t(15)) + 8 * (k & 1) + (r & 7);
+  return ((k >> 1) * nslots + slot) * 16 + ((r >> 3) & 1) * 2;
+}
+constexpr uint32_t kTcFiller = 0x44444444u;
+inline int64_t tc_slots(int64_t rows) { return ((rows + 127) / 128) * 128; }
+
+// Writes segment k of row r into the tensor-core metadata (and the slot row's
+// filler words when this row supplies the low half).
+__device__ __forceinline__ void tc_store(void* meta, int64_t r, int64_t k, int64_t nslots, uint32_t code16) {
+  const int64_t off = tc_half_offset(r, k, nslots);
+  char* base = reinterpret_cast<char*>(meta);
+  *reinterpret_cast<uint16_t*>(base + off) = (uint16_t)code16;
+  if (((r >> 3) & 1) == 0) {
+    uint32_t* f = reinterpret_cast<uint32_t*>(base + off + 4);
+    f[0] = kTcFiller;
+    f[1] = kTcFiller;
+    f[2] = kTcFiller;
+  }
+}
+
+// Grid size for grid-stride loops: enough CTAs to fill 152 SMs several times.
+inline unsigned grid_for(int64_t work_items, int threads, int max_ctas_per_sm = 8) {
+  int64_t g = (work_items + threads - 1) / threads;
+  int64_t cap = 152LL * max_ctas_per_sm;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return (unsigned)g;
+}
+
+}  // namespace nmk

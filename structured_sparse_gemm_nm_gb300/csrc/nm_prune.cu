@@ -1,0 +1,454 @@
+// N:M greedy magnitude pruning, compression, decompression and pattern check.
+//
+// Selection rule (apex PR #1631 "[sparse] update support for arbitrary N:M
+// settings sparse", extension 1, mn_1d_greedy): in every group of m
+// consecutive elements of a row keep the n largest |w|; equal magnitudes go
+// to the lower position; NaN ranks above every number.  Compression
+// (cuSPARSELt blog, Figure 2 text) stores the kept values at n/m of the size
+// plus position metadata.
+//
+// 2:4 kernels give each thread one 16-column segment of a row: four groups,
+// one uint16 of canonical metadata (or one 16-bit half of a tensor-core
+// metadata word), one 16-bit half of a mask word.  For aligned 16-bit data
+// the segment is two 128-bit loads and the eight kept values one 128-bit
+// store.  Other N:M shapes give each thread one group.
+#include <cuda_fp16.h>
+
+#include "nm_device.cuh"
+#include "nm_internal.h"
+
+namespace nmk {
+namespace {
+
+// Position of logical element (r, c) in the stored matrix.
+template <bool TRANS>
+__device__ __forceinline__ int64_t at(int64_t r, int64_t c, int64_t ld) {
+  return TRANS ? c * ld + r : r * ld + c;
+}
+
+// Selects the two kept positions of a group of four keys (lower position wins
+// ties) and returns the 4-bit keep mask.
+__device__ __forceinline__ uint32_t keep2of4(uint32_t k0, uint32_t k1, uint32_t k2, uint32_t k3) {
+  // cij (i < j): element i beats element j  <=>  k_i >= k_j
+  const uint32_t c01 = k0 >= k1, c02 = k0 >= k2, c03 = k0 >= k3;
+  const uint32_t c12 = k1 >= k2, c13 = k1 >= k3, c23 = k2 >= k3;
+  const uint32_t r0 = (c01 ^ 1) + (c02 ^ 1) + (c03 ^ 1);
+  const uint32_t r1 = c01 + (c12 ^ 1) + (c13 ^ 1);
+  const uint32_t r2 = c02 + c12 + (c23 ^ 1);
+  const uint32_t r3 = c03 + c13 + c23;
+  return (uint32_t)(r0 < 2) | ((uint32_t)(r1 < 2) << 1) | ((uint32_t)(r2 < 2) << 2) | ((uint32_t)(r3 < 2) << 3);
+}
+
+template <int DT, bool VEC, bool TRANS>
+__global__ void __launch_bounds__(256) prune24_kernel(const typename Elem<DT>::T* __restrict__ W, int64_t rowsL,
+                                                      int64_t colsL, int64_t ld, typename Elem<DT>::T* W_out,
+                                                      int64_t ld_out, uint32_t* __restrict__ mask_bits,
+                                                      typename Elem<DT>::T* __restrict__ vals, void* __restrict__ meta,
+                                                      int meta_tc) {
+  using T = typename Elem<DT>::T;
+  const int64_t segs = (colsL + 15) / 16;
+  const int64_t total = rowsL * segs;
+  const int64_t half_cols = colsL / 2;
+  const int64_t mask_halves = ((colsL + 31) / 32) * 2;
+  const int64_t nslots = ((rowsL + 127) / 128) * 128;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = idx / segs;
+    const int64_t k = idx - r * segs;
+    const int64_t c0 = k * 16;
+    const int ncol = (int)(colsL - c0 < 16 ? colsL - c0 : 16);
+    T v[16];
+    if constexpr (VEC) {
+      const uint4* p = reinterpret_cast<const uint4*>(W + r * ld + c0);
+      if constexpr (sizeof(T) == 2) {
+        const uint4 a = __ldg(p), b = __ldg(p + 1);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[2 * j] = (T)(w[j] & 0xFFFFu);
+          v[2 * j + 1] = (T)(w[j] >> 16);
+        }
+      } else {
+        const uint4 a = __ldg(p);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = (T)(int8_t)((w[j / 4] >> (8 * (j % 4))) & 0xFFu);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = (j < ncol) ? W[at<TRANS>(r, c0 + j, ld)] : (T)0;
+    }
+    uint32_t keep = 0, code = 0;
+    T kv[8];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const T* e = v + 4 * g;
+      const uint32_t km = keep2of4(Elem<DT>::key(e[0]), Elem<DT>::key(e[1]), Elem<DT>::key(e[2]), Elem<DT>::key(e[3]));
+      const uint32_t kmask = (4 * g < ncol) ? km : 0u;
+      const uint32_t i0 = (km & 1u) ? 0u : ((km & 2u) ? 1u : 2u);
+      const uint32_t i1 = (km & 8u) ? 3u : ((km & 4u) ? 2u : 1u);
+      kv[2 * g] = (4 * g < ncol) ? ((km & 1u) ? e[0] : ((km & 2u) ? e[1] : e[2])) : (T)0;
+      kv[2 * g + 1] = (4 * g < ncol) ? ((km & 8u) ? e[3] : ((km & 4u) ? e[2] : e[1])) : (T)0;
+      keep |= kmask << (4 * g);
+      code |= ((4 * g < ncol) ? (i0 | (i1 << 2)) : 0u) << (4 * g);
+    }
+    if (vals != nullptr) {
+      T* out = vals + r * half_cols + c0 / 2;
+      if constexpr (VEC) {
+        if constexpr (sizeof(T) == 2) {
+          uint4 o;
+          o.x = (uint32_t)kv[0] | ((uint32_t)kv[1] << 16);
+          o.y = (uint32_t)kv[2] | ((uint32_t)kv[3] << 16);
+          o.z = (uint32_t)kv[4] | ((uint32_t)kv[5] << 16);
+          o.w = (uint32_t)kv[6] | ((uint32_t)kv[7] << 16);
+          *reinterpret_cast<uint4*>(out) = o;
+        } else {
+          uint2 o;
+          o.x = 0;
+          o.y = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            o.x |= ((uint32_t)(uint8_t)kv[j]) << (8 * j);
+            o.y |= ((uint32_t)(uint8_t)kv[4 + j]) << (8 * j);
+          }
+          *reinterpret_cast<uint2*>(out) = o;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (2 * j < ncol) out[j] = kv[j];
+      }
+    }
+    if (meta != nullptr) {
+      if (meta_tc) {
+        tc_store(meta, r, k, nslots, code);
+      } else {
+        reinterpret_cast<uint16_t*>(meta)[r * segs + k] = (uint16_t)code;
+      }
+    }
+    if constexpr (!TRANS) {
+      if (mask_bits != nullptr) {
+        uint16_t* mh = reinterpret_cast<uint16_t*>(mask_bits) + r * mask_halves;
+        mh[k] = (uint16_t)keep;
+        if (k == segs - 1 && (segs & 1)) mh[k + 1] = 0;  // unused upper half of the row's last word
+      }
+      if (W_out != nullptr) {
+        T o[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[j] = ((keep >> j) & 1u) ? v[j] : (T)0;
+        T* q = W_out + r * ld_out + c0;
+        if constexpr (VEC) {
+          if constexpr (sizeof(T) == 2) {
+            uint4 a, b;
+            a.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
+            a.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
+            a.z = (uint32_t)o[4] | ((uint32_t)o[5] << 16);
+            a.w = (uint32_t)o[6] | ((uint32_t)o[7] << 16);
+            b.x = (uint32_t)o[8] | ((uint32_t)o[9] << 16);
+            b.y = (uint32_t)o[10] | ((uint32_t)o[11] << 16);
+            b.z = (uint32_t)o[12] | ((uint32_t)o[13] << 16);
+            b.w = (uint32_t)o[14] | ((uint32_t)o[15] << 16);
+            reinterpret_cast<uint4*>(q)[0] = a;
+            reinterpret_cast<uint4*>(q)[1] = b;
+          } else {
+            uint4 a;
+            uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j / 4] |= ((uint32_t)(uint8_t)o[j]) << (8 * (j % 4));
+            a.x = w[0];
+            a.y = w[1];
+            a.z = w[2];
+            a.w = w[3];
+            *reinterpret_cast<uint4*>(q) = a;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < ncol) q[j] = o[j];
+        }
+      }
+    }
+  }
+}
+
+// General n:m (m <= 32), one thread per group.  Composite keys (key << 5 |
+// (31 - position)) are all distinct; an element is kept when fewer than n
+// composite keys of its group exceed its own.
+template <int DT, bool TRANS>
+__global__ void __launch_bounds__(256) prune_nm_kernel(const typename Elem<DT>::T* __restrict__ W, int64_t rowsL,
+                                                       int64_t colsL, int64_t ld, int n, int m,
+                                                       typename Elem<DT>::T* W_out, int64_t ld_out,
+                                                       uint32_t* __restrict__ mask_bits,
+                                                       typename Elem<DT>::T* __restrict__ vals,
+                                                       uint8_t* __restrict__ meta) {
+  using T = typename Elem<DT>::T;
+  const int64_t gpr = colsL / m;
+  const int64_t total = rowsL * gpr;
+  const int64_t words = (colsL + 31) / 32;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = idx / gpr;
+    const int64_t g = idx - r * gpr;
+    const int64_t c0 = g * m;
+    T v[32];
+    uint32_t ck[32];
+    for (int j = 0; j < m; ++j) {
+      v[j] = W[at<TRANS>(r, c0 + j, ld)];
+      ck[j] = (Elem<DT>::key(v[j]) << 5) | (uint32_t)(31 - j);
+    }
+    uint32_t keep = 0;
+    for (int j = 0; j < m; ++j) {
+      int rank = 0;
+      for (int i = 0; i < m; ++i) rank += ck[i] > ck[j];
+      if (rank < n) keep |= 1u << j;
+    }
+    if (vals != nullptr || meta != nullptr) {
+      int o = 0;
+      const int64_t base = r * gpr * n + g * n;
+      for (int j = 0; j < m; ++j) {
+        if ((keep >> j) & 1u) {
+          if (vals != nullptr) vals[base + o] = v[j];
+          if (meta != nullptr) meta[base + o] = (uint8_t)j;
+          ++o;
+        }
+      }
+    }
+    if constexpr (!TRANS) {
+      if (W_out != nullptr) {
+        for (int j = 0; j < m; ++j) W_out[r * ld_out + c0 + j] = ((keep >> j) & 1u) ? v[j] : (T)0;
+      }
+      if (mask_bits != nullptr && keep != 0u) {  // buffer was zeroed by the launcher
+        const int64_t w0 = c0 / 32;
+        const int sh = (int)(c0 % 32);
+        atomicOr(mask_bits + r * words + w0, keep << sh);
+        if (sh + m > 32) atomicOr(mask_bits + r * words + w0 + 1, keep >> (32 - sh));
+      }
+    }
+  }
+}
+
+// ---- decompression -------------------------------------------------------
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(256) decompress24_kernel(const typename Elem<DT>::T* __restrict__ vals,
+                                                           const void* __restrict__ meta, int64_t rows, int64_t cols,
+                                                           int meta_tc, typename Elem<DT>::T* __restrict__ W_out,
+                                                           int64_t ld_out) {
+  using T = typename Elem<DT>::T;
+  const int64_t segs = (cols + 15) / 16;
+  const int64_t total = rows * segs;
+  const int64_t nslots = ((rows + 127) / 128) * 128;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = idx / segs;
+    const int64_t k = idx - r * segs;
+    const int64_t c0 = k * 16;
+    const int ncol = (int)(cols - c0 < 16 ? cols - c0 : 16);
+    const uint32_t code = meta_tc ? *reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(meta) +
+                                                                      tc_half_offset(r, k, nslots))
+                                  : reinterpret_cast<const uint16_t*>(meta)[r * segs + k];
+    T kv[8];
+    const T* in = vals + r * (cols / 2) + c0 / 2;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) kv[j] = (2 * j < ncol) ? in[j] : (T)0;
+    T o[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j] = (T)0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t c = (code >> (4 * g)) & 0xFu;
+      const uint32_t i0 = c & 3u, i1 = c >> 2;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (t == (int)i0) o[4 * g + t] = kv[2 * g];
+        if (t == (int)i1) o[4 * g + t] = kv[2 * g + 1];
+      }
+    }
+    T* q = W_out + r * ld_out + c0;
+    if constexpr (VEC && sizeof(T) == 2) {
+      uint4 a, b;
+      a.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
+      a.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
+      a.z = (uint32_t)o[4] | ((uint32_t)o[5] << 16);
+      a.w = (uint32_t)o[6] | ((uint32_t)o[7] << 16);
+      b.x = (uint32_t)o[8] | ((uint32_t)o[9] << 16);
+      b.y = (uint32_t)o[10] | ((uint32_t)o[11] << 16);
+      b.z = (uint32_t)o[12] | ((uint32_t)o[13] << 16);
+      b.w = (uint32_t)o[14] | ((uint32_t)o[15] << 16);
+      reinterpret_cast<uint4*>(q)[0] = a;
+      reinterpret_cast<uint4*>(q)[1] = b;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < ncol) q[j] = o[j];
+    }
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) decompress_nm_kernel(const typename Elem<DT>::T* __restrict__ vals,
+                                                            const uint8_t* __restrict__ meta, int64_t rows,
+                                                            int64_t cols, int n, int m,
+                                                            typename Elem<DT>::T* __restrict__ W_out, int64_t ld_out) {
+  using T = typename Elem<DT>::T;
+  const int64_t gpr = cols / m;
+  const int64_t total = rows * gpr;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = idx / gpr;
+    const int64_t g = idx - r * gpr;
+    T* q = W_out + r * ld_out + g * m;
+    for (int j = 0; j < m; ++j) q[j] = (T)0;
+    const int64_t base = r * gpr * n + g * n;
+    for (int t = 0; t < n; ++t) {
+      const int p = meta[base + t];
+      if (p < m) q[p] = vals[base + t];
+    }
+  }
+}
+
+// ---- pattern check ---------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(256) check_kernel(const typename Elem<DT>::T* __restrict__ W, int64_t rows,
+                                                    int64_t cols, int64_t ld, int n, int m, int transposable,
+                                                    int32_t* __restrict__ d_violations) {
+  const int64_t gpr = cols / m;
+  const int64_t row_groups = rows * gpr;
+  const int64_t col_groups = transposable ? (rows / 4) * cols : 0;
+  int count = 0;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < row_groups + col_groups;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    int nz = 0;
+    if (idx < row_groups) {
+      const int64_t r = idx / gpr;
+      const int64_t c0 = (idx - r * gpr) * m;
+      for (int j = 0; j < m; ++j) nz += Elem<DT>::nonzero(W[r * ld + c0 + j]);
+      count += nz > n;
+    } else {
+      const int64_t t = idx - row_groups;
+      const int64_t rg = t / cols;
+      const int64_t c = t - rg * cols;
+      for (int j = 0; j < 4; ++j) nz += Elem<DT>::nonzero(W[(4 * rg + j) * ld + c]);
+      count += nz > 2;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) count += __shfl_xor_sync(0xFFFFFFFFu, count, off);
+  if ((threadIdx.x & 31) == 0 && count) atomicAdd(d_violations, count);
+}
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <int DT>
+cudaError_t prune_dt(const PruneLaunch& a, cudaStream_t s) {
+  using T = typename Elem<DT>::T;
+  const int threads = 256;
+  const T* W = static_cast<const T*>(a.W);
+  T* W_out = static_cast<T*>(a.W_out);
+  T* vals = static_cast<T*>(a.vals);
+  if (a.n == 2 && a.m == 4) {
+    const int64_t segs = (a.colsL + 15) / 16;
+    const unsigned grid = grid_for(a.rowsL * segs, threads);
+    if (a.meta != nullptr && a.meta_tc) {
+      // slot rows of rows past the matrix hold the valid code 0x4 (positions 0 and 1)
+      const int64_t slots = tc_slots(a.rowsL);
+      if (slots != a.rowsL) {
+        cudaError_t e = cudaMemsetAsync(a.meta, 0x44, (size_t)((a.colsL / 32) * slots * 16), s);
+        if (e != cudaSuccess) return e;
+      }
+    }
+    const int64_t es = (int64_t)sizeof(T);
+    const bool vec = !a.trans && (a.colsL % 16 == 0) && (a.ld * es) % 16 == 0 && aligned16(W) &&
+                     (W_out == nullptr || ((a.ld_out * es) % 16 == 0 && aligned16(W_out))) && aligned16(vals);
+    if (vec)
+      prune24_kernel<DT, true, false><<<grid, threads, 0, s>>>(W, a.rowsL, a.colsL, a.ld, W_out, a.ld_out,
+                                                                a.mask_bits, vals, a.meta, a.meta_tc);
+    else if (!a.trans)
+      prune24_kernel<DT, false, false><<<grid, threads, 0, s>>>(W, a.rowsL, a.colsL, a.ld, W_out, a.ld_out,
+                                                                 a.mask_bits, vals, a.meta, a.meta_tc);
+    else
+      prune24_kernel<DT, false, true><<<grid, threads, 0, s>>>(W, a.rowsL, a.colsL, a.ld, nullptr, 0, nullptr,
+                                                                vals, a.meta, a.meta_tc);
+    return cudaGetLastError();
+  }
+  if (a.mask_bits != nullptr && !a.trans) {
+    const size_t bytes = (size_t)a.rowsL * (size_t)((a.colsL + 31) / 32) * 4;
+    cudaError_t e = cudaMemsetAsync(a.mask_bits, 0, bytes, s);
+    if (e != cudaSuccess) return e;
+  }
+  const unsigned grid = grid_for(a.rowsL * (a.colsL / a.m), threads);
+  uint8_t* meta = static_cast<uint8_t*>(a.meta);
+  if (!a.trans)
+    prune_nm_kernel<DT, false><<<grid, threads, 0, s>>>(W, a.rowsL, a.colsL, a.ld, a.n, a.m, W_out, a.ld_out,
+                                                         a.mask_bits, vals, meta);
+  else
+    prune_nm_kernel<DT, true><<<grid, threads, 0, s>>>(W, a.rowsL, a.colsL, a.ld, a.n, a.m, nullptr, 0, nullptr,
+                                                        vals, meta);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t decompress_dt(const DecompressLaunch& a, cudaStream_t s) {
+  using T = typename Elem<DT>::T;
+  const int threads = 256;
+  const T* vals = static_cast<const T*>(a.vals);
+  T* W_out = static_cast<T*>(a.W_out);
+  if (a.n == 2 && a.m == 4) {
+    const int64_t segs = (a.cols + 15) / 16;
+    const unsigned grid = grid_for(a.rows * segs, threads);
+    const bool vec = sizeof(T) == 2 && a.cols % 16 == 0 && (a.ld_out * 2) % 16 == 0 && aligned16(W_out);
+    if (vec)
+      decompress24_kernel<DT, true><<<grid, threads, 0, s>>>(vals, a.meta, a.rows, a.cols, a.meta_tc, W_out, a.ld_out);
+    else
+      decompress24_kernel<DT, false><<<grid, threads, 0, s>>>(vals, a.meta, a.rows, a.cols, a.meta_tc, W_out,
+                                                              a.ld_out);
+  } else {
+    const unsigned grid = grid_for(a.rows * (a.cols / a.m), threads);
+    decompress_nm_kernel<DT><<<grid, threads, 0, s>>>(vals, static_cast<const uint8_t*>(a.meta), a.rows, a.cols, a.n,
+                                                      a.m, W_out, a.ld_out);
+  }
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t check_dt(const void* W, int64_t rows, int64_t cols, int64_t ld, int n, int m, int transposable,
+                     int32_t* d_violations, cudaStream_t s) {
+  using T = typename Elem<DT>::T;
+  cudaError_t e = cudaMemsetAsync(d_violations, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
+  const int64_t work = rows * (cols / m) + (transposable ? (rows / 4) * cols : 0);
+  if (work == 0) return cudaSuccess;
+  check_kernel<DT><<<grid_for(work, 256), 256, 0, s>>>(static_cast<const T*>(W), rows, cols, ld, n, m, transposable,
+                                                       d_violations);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prune(const PruneLaunch& a, cudaStream_t s) {
+  if (a.rowsL == 0 || a.colsL == 0) return cudaSuccess;
+  switch (a.dt) {
+    case kF16: return prune_dt<kF16>(a, s);
+    case kBF16: return prune_dt<kBF16>(a, s);
+    default: return prune_dt<kI8>(a, s);
+  }
+}
+
+cudaError_t launch_decompress(const DecompressLaunch& a, cudaStream_t s) {
+  if (a.rows == 0 || a.cols == 0) return cudaSuccess;
+  switch (a.dt) {
+    case kF16: return decompress_dt<kF16>(a, s);
+    case kBF16: return decompress_dt<kBF16>(a, s);
+    default: return decompress_dt<kI8>(a, s);
+  }
+}
+
+cudaError_t launch_check(int dt, const void* W, int64_t rows, int64_t cols, int64_t ld, int n, int m,
+                         int transposable, int32_t* d_violations, cudaStream_t s) {
+  switch (dt) {
+    case kF16: return check_dt<kF16>(W, rows, cols, ld, n, m, transposable, d_violations, s);
+    case kBF16: return check_dt<kBF16>(W, rows, cols, ld, n, m, transposable, d_violations, s);
+    default: return check_dt<kI8>(W, rows, cols, ld, n, m, transposable, d_violations, s);
+  }
+}
+
+}  // namespace nmk

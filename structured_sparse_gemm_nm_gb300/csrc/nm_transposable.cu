@@ -1,0 +1,232 @@
+// Transposable 2:4 pruning on 4x4 tiles (PyTorch issue #126420, maintainer
+// reply: the forward product W x and the backward product W^T dL/dy both run
+// on 2:4 sparse hardware only if every 4x4 tile keeps two entries per row and
+// two per column).
+//
+// Per tile the kernel scores the 90 patterns with two kept entries in every
+// row and column, score = ((p0 + p1) + p2) + p3 in float32 where p_r is the
+// sum of row r's two kept magnitudes, and keeps the first pattern (row 0's
+// pair outermost, pairs in the order (0,1),(0,2),(0,3),(1,2),(1,3),(2,3))
+// with the largest score.
+//
+// Work layout: one warp per 16 x 32 block of W, lane l owns the tile in tile
+// row l/8 and tile column l%8 of the block.  Every packed output word (a
+// 32-bit mask word of one row, a 16-bit metadata word of four groups) then
+// comes from lanes of the same warp and is assembled with shuffles.
+#include <cuda_fp16.h>
+
+#include "nm_device.cuh"
+#include "nm_internal.h"
+
+namespace nmk {
+namespace {
+
+// Column bits of pair q in (0,1),(0,2),(0,3),(1,2),(1,3),(2,3).
+__host__ __device__ constexpr uint32_t pair_bits(int q) {
+  return q == 0 ? 0x3u : q == 1 ? 0x5u : q == 2 ? 0x9u : q == 3 ? 0x6u : q == 4 ? 0xAu : 0xCu;
+}
+__host__ __device__ constexpr int pair_of_bits(uint32_t b) {
+  return b == 0x3u ? 0 : b == 0x5u ? 1 : b == 0x9u ? 2 : b == 0x6u ? 3 : b == 0xAu ? 4 : b == 0xCu ? 5 : -1;
+}
+__host__ __device__ constexpr int col_count(int a, int b, int c, int j) {
+  return (int)((pair_bits(a) >> j) & 1u) + (int)((pair_bits(b) >> j) & 1u) + (int)((pair_bits(c) >> j) & 1u);
+}
+// Pair that row 3 must keep after rows 0..2 chose a, b, c, or -1 if none completes a valid tile.
+__host__ __device__ constexpr int completion(int a, int b, int c) {
+  uint32_t need = 0;
+  for (int j = 0; j < 4; ++j) {
+    const int k = col_count(a, b, c, j);
+    if (k < 1 || k > 2) return -1;
+    if (k == 1) need |= 1u << j;
+  }
+  return pair_of_bits(need);
+}
+__host__ __device__ constexpr uint32_t tile_mask(int a, int b, int c, int d) {
+  return pair_bits(a) | (pair_bits(b) << 4) | (pair_bits(c) << 8) | (pair_bits(d) << 12);
+}
+
+template <int DT>
+__device__ __forceinline__ float tile_mag(typename Elem<DT>::T v) {
+  if constexpr (DT == kI8) {
+    return fabsf((float)v);
+  } else {
+    return mag_f32((uint16_t)v, DT);
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) transposable_kernel(const typename Elem<DT>::T* __restrict__ W, int64_t rows,
+                                                           int64_t cols, int64_t ld, typename Elem<DT>::T* W_out,
+                                                           int64_t ld_out, uint32_t* __restrict__ mask_bits,
+                                                           typename Elem<DT>::T* __restrict__ vals,
+                                                           void* __restrict__ meta,
+                                                           typename Elem<DT>::T* __restrict__ valsT,
+                                                           void* __restrict__ metaT, int meta_tc) {
+  using T = typename Elem<DT>::T;
+  const int lane = threadIdx.x & 31;
+  const int tr = lane >> 3, tcol = lane & 7;
+  const int64_t nbr = (rows + 15) / 16, nbc = (cols + 31) / 32;
+  const int64_t nblocks = nbr * nbc;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int64_t mw = (cols + 15) / 16, mwT = (rows + 15) / 16;
+  const int64_t nslots = ((rows + 127) / 128) * 128, nslotsT = ((cols + 127) / 128) * 128;
+  const int64_t mask_words = (cols + 31) / 32;
+  for (int64_t blk = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5); blk < nblocks; blk += warps) {
+    const int64_t br = blk / nbc, bc = blk - br * nbc;
+    const int64_t R0 = br * 16 + tr * 4, C0 = bc * 32 + tcol * 4;
+    const bool valid = R0 < rows && C0 < cols;
+    T v[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[r][c] = valid ? W[(R0 + r) * ld + C0 + c] : (T)0;
+    float p[4][6];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float mg[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) mg[c] = tile_mag<DT>(v[r][c]);
+      p[r][0] = mg[0] + mg[1];
+      p[r][1] = mg[0] + mg[2];
+      p[r][2] = mg[0] + mg[3];
+      p[r][3] = mg[1] + mg[2];
+      p[r][4] = mg[1] + mg[3];
+      p[r][5] = mg[2] + mg[3];
+    }
+    float best = -1.0f;
+    uint32_t bmask = 0;
+#pragma unroll
+    for (int a = 0; a < 6; ++a) {
+#pragma unroll
+      for (int b = 0; b < 6; ++b) {
+        const float s01 = p[0][a] + p[1][b];
+#pragma unroll
+        for (int c = 0; c < 6; ++c) {
+          const int d = completion(a, b, c);
+          if (d >= 0) {
+            const float s = (s01 + p[2][c]) + p[3][d];
+            if (s > best) {
+              best = s;
+              bmask = tile_mask(a, b, c, d);
+            }
+          }
+        }
+      }
+    }
+    if (!valid) bmask = 0;
+
+    // ---- pruned copy
+    if (W_out != nullptr && valid) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) W_out[(R0 + r) * ld_out + C0 + c] = ((bmask >> (4 * r + c)) & 1u) ? v[r][c] : (T)0;
+    }
+    // ---- mask bits: 8 lanes of a tile row form one 32-bit word per row
+    if (mask_bits != nullptr) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        uint32_t w = ((bmask >> (4 * r)) & 0xFu) << (4 * tcol);
+        w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
+        w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+        w |= __shfl_xor_sync(0xFFFFFFFFu, w, 4);
+        if (tcol == 0 && R0 < rows) mask_bits[(R0 + r) * mask_words + bc] = w;
+      }
+    }
+    // ---- row-compressed W: per row two values and one 4-bit code
+    if (vals != nullptr || meta != nullptr) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t km = (bmask >> (4 * r)) & 0xFu;
+        const uint32_t i0 = (km & 1u) ? 0u : ((km & 2u) ? 1u : 2u);
+        const uint32_t i1 = (km & 8u) ? 3u : ((km & 4u) ? 2u : 1u);
+        if (vals != nullptr && valid) {
+          T* o = vals + (R0 + r) * (cols / 2) + C0 / 2;
+          o[0] = (km & 1u) ? v[r][0] : ((km & 2u) ? v[r][1] : v[r][2]);
+          o[1] = (km & 8u) ? v[r][3] : ((km & 4u) ? v[r][2] : v[r][1]);
+        }
+        if (meta != nullptr) {
+          uint32_t code = valid ? (i0 | (i1 << 2)) << (4 * (tcol & 3)) : 0u;
+          code |= __shfl_xor_sync(0xFFFFFFFFu, code, 1);
+          code |= __shfl_xor_sync(0xFFFFFFFFu, code, 2);
+          if ((tcol & 3) == 0 && valid) {
+            const int64_t row = R0 + r, k = C0 / 16;
+            if (meta_tc)
+              tc_store(meta, row, k, nslots, code);
+            else
+              reinterpret_cast<uint16_t*>(meta)[row * mw + k] = (uint16_t)code;
+          }
+        }
+      }
+    }
+    // ---- column-compressed (W^T): per tile column two values and one code
+    if (valsT != nullptr || metaT != nullptr) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t km = ((bmask >> c) & 1u) | (((bmask >> (4 + c)) & 1u) << 1) | (((bmask >> (8 + c)) & 1u) << 2) |
+                            (((bmask >> (12 + c)) & 1u) << 3);
+        const uint32_t i0 = (km & 1u) ? 0u : ((km & 2u) ? 1u : 2u);
+        const uint32_t i1 = (km & 8u) ? 3u : ((km & 4u) ? 2u : 1u);
+        if (valsT != nullptr && valid) {
+          T* o = valsT + (C0 + c) * (rows / 2) + R0 / 2;
+          o[0] = (km & 1u) ? v[0][c] : ((km & 2u) ? v[1][c] : v[2][c]);
+          o[1] = (km & 8u) ? v[3][c] : ((km & 4u) ? v[2][c] : v[1][c]);
+        }
+        if (metaT != nullptr) {
+          // four tile rows of the block share one 16-bit word: lanes tcol, tcol+8, tcol+16, tcol+24
+          uint32_t code = valid ? (i0 | (i1 << 2)) << (4 * tr) : 0u;
+          code |= __shfl_xor_sync(0xFFFFFFFFu, code, 8);
+          code |= __shfl_xor_sync(0xFFFFFFFFu, code, 16);
+          if (tr == 0 && C0 < cols) {
+            const int64_t row = C0 + c, k = br;
+            if (meta_tc)
+              tc_store(metaT, row, k, nslotsT, code);
+            else
+              reinterpret_cast<uint16_t*>(metaT)[row * mwT + k] = (uint16_t)code;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int DT>
+cudaError_t transposable_dt(const TransposableLaunch& a, cudaStream_t s) {
+  using T = typename Elem<DT>::T;
+  if (a.meta_tc) {
+    if (a.meta != nullptr) {
+      const int64_t slots = tc_slots(a.rows);
+      if (slots != a.rows) {
+        cudaError_t e = cudaMemsetAsync(a.meta, 0x44, (size_t)((a.cols / 32) * slots * 16), s);
+        if (e != cudaSuccess) return e;
+      }
+    }
+    if (a.metaT != nullptr) {
+      const int64_t slots = tc_slots(a.cols);
+      if (slots != a.cols) {
+        cudaError_t e = cudaMemsetAsync(a.metaT, 0x44, (size_t)((a.rows / 32) * slots * 16), s);
+        if (e != cudaSuccess) return e;
+      }
+    }
+  }
+  const int64_t nblocks = ((a.rows + 15) / 16) * ((a.cols + 31) / 32);
+  const unsigned grid = grid_for(nblocks * 32, 256);
+  transposable_kernel<DT><<<grid, 256, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
+                                               static_cast<T*>(a.W_out), a.ld_out, a.mask_bits,
+                                               static_cast<T*>(a.vals), a.meta, static_cast<T*>(a.valsT), a.metaT,
+                                               a.meta_tc);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_transposable(const TransposableLaunch& a, cudaStream_t s) {
+  if (a.rows == 0 || a.cols == 0) return cudaSuccess;
+  switch (a.dt) {
+    case kF16: return transposable_dt<kF16>(a, s);
+    case kBF16: return transposable_dt<kBF16>(a, s);
+    default: return transposable_dt<kI8>(a, s);
+  }
+}
+
+}  // namespace nmk

@@ -1,0 +1,150 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+entry point, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from structured_sparse_gemm_nm_gb300 import binding as nb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(nb.LIB_PATH):
+        from structured_sparse_gemm_nm_gb300.build import build
+
+        build()
+    return nb.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_binding_names():
+    assert declared_functions() == sorted(nb.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", nb.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (nm_[a-z0-9_]+)", out))
+    missing = [f for f in declared_functions() if f not in exported]
+    assert not missing, missing
+    for f in declared_functions():
+        assert hasattr(lib, f)
+
+
+def test_version_and_status_strings(lib):
+    assert nb.nm_version() == 1
+    for code, name in enumerate(["NM_OK", "NM_ERR_INVALID_ARG", "NM_ERR_UNSUPPORTED", "NM_ERR_MISALIGNED",
+                                 "NM_ERR_CUDA", "NM_ERR_TIMEOUT"]):
+        assert nb.status_string(code) == name
+
+
+def test_compressed_size(lib):
+    assert nb.nm_compressed_size(64, 128, "f16", 2, 4) == (64 * 64 * 2, 64 * 8 * 2)
+    # tensor-core order: slot rows padded to 128, words per row padded to 4
+    assert nb.nm_compressed_size(64, 128, "f16", 2, 4, nb.NM_META_TC) == (64 * 64 * 2, 4 * 128 * 16)
+    assert nb.nm_compressed_size(300, 96, "bf16", 2, 4, nb.NM_META_TC) == (300 * 48 * 2, 3 * 384 * 16)
+    assert nb.nm_compressed_size(4096, 4096, "f16", 8, 32) == (4096 * 1024 * 2, 4096 * 1024)
+    assert nb.nm_compressed_size(8, 64, "i8", 2, 4) == (8 * 32, 8 * 4 * 2)
+    assert nb.nm_compressed_size(8, 20, "f16", 2, 4)[1] == 8 * 2 * 2  # ceil(20/16) words per row
+    with pytest.raises(nb.NmError) as e:
+        nb.nm_compressed_size(8, 64, "i8", 2, 4, nb.NM_META_TC)
+    assert e.value.status == nb.NM_ERR_UNSUPPORTED
+    with pytest.raises(nb.NmError):
+        nb.nm_compressed_size(8, 48, "f16", 2, 4, nb.NM_META_TC)  # cols % 32
+    with pytest.raises(nb.NmError):
+        nb.nm_compressed_size(8, 64, "f16", 4, 32, nb.NM_META_TC)
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize(
+    "kwargs,status",
+    [
+        (dict(n=4, m=4), nb.NM_ERR_INVALID_ARG),
+        (dict(n=0, m=4), nb.NM_ERR_INVALID_ARG),
+        (dict(n=2, m=33), nb.NM_ERR_INVALID_ARG),
+        (dict(cols=30), nb.NM_ERR_INVALID_ARG),
+        (dict(ld=10), nb.NM_ERR_INVALID_ARG),
+        (dict(W=None), nb.NM_ERR_INVALID_ARG),
+        (dict(W=FAKE + 1), nb.NM_ERR_MISALIGNED),
+        (dict(dtype=nb.NM_F32), nb.NM_ERR_INVALID_ARG),
+        (dict(W_out=FAKE, ld_out=64), nb.NM_ERR_INVALID_ARG),  # aliasing W with another ld
+    ],
+)
+def test_prune_rejects_bad_arguments(lib, kwargs, status):
+    a = dict(W=FAKE, rows=8, cols=32, ld=32, dtype=nb.NM_F16, n=2, m=4, W_out=None, ld_out=0, mask_bits=None)
+    a.update(kwargs)
+    st = lib.nm_prune(a["W"], a["rows"], a["cols"], a["ld"], a["dtype"], a["n"], a["m"], a["W_out"], a["ld_out"],
+                      a["mask_bits"], None)
+    assert st == status
+
+
+def test_other_calls_reject_bad_arguments(lib):
+    L = lib
+    assert L.nm_compress(FAKE, 8, 32, 32, nb.NM_F16, 2, 4, 2, 0, None, None, None) == nb.NM_ERR_INVALID_ARG
+    assert L.nm_compress(FAKE, 8, 48, 48, nb.NM_F16, 2, 4, 0, nb.NM_META_TC, None, None, None) == nb.NM_ERR_UNSUPPORTED
+    assert L.nm_compress(FAKE, 8, 32, 32, nb.NM_F16, 2, 4, 0, 0, FAKE + 1, None, None) == nb.NM_ERR_MISALIGNED
+    assert L.nm_decompress(None, None, 8, 32, nb.NM_F16, 2, 4, 0, FAKE, 32, None) == nb.NM_ERR_INVALID_ARG
+    assert L.nm_check(FAKE, 8, 32, 32, nb.NM_F16, 2, 4, 0, None, None) == nb.NM_ERR_INVALID_ARG
+    assert L.nm_check(FAKE, 6, 32, 32, nb.NM_F16, 2, 4, 1, FAKE, None) == nb.NM_ERR_INVALID_ARG  # rows % 4
+    assert L.nm_check(FAKE, 8, 32, 32, nb.NM_F16, 8, 32, 1, FAKE, None) == nb.NM_ERR_INVALID_ARG  # not 2:4
+    assert (L.nm_prune_transposable(FAKE, 6, 32, 32, nb.NM_F16, None, 0, None, None, None, None, None, 0, None)
+            == nb.NM_ERR_INVALID_ARG)
+    assert (L.nm_prune_transposable(FAKE, 8, 48, 48, nb.NM_F16, None, 0, None, None, FAKE, None, None, nb.NM_META_TC,
+                                    None) == nb.NM_ERR_UNSUPPORTED)
+
+
+def plan_status(**kw):
+    d = nb.make_desc(**kw)
+    h = ctypes.c_void_p()
+    st = nb.lib().nm_spmm_plan(ctypes.byref(h), ctypes.byref(d))
+    if st == nb.NM_OK:
+        nb.lib().nm_spmm_plan_destroy(h)
+    return st
+
+
+def test_plan_validation(lib):
+    base = dict(M=256, N=512, K=1024, ab_type="f16", cd_type="f16", ldb=1024, ldd=256)
+    assert plan_status(**base) == nb.NM_OK
+    assert plan_status(**{**base, "cd_type": "bf16"}) == nb.NM_ERR_UNSUPPORTED
+    assert plan_status(**{**base, "order_b": nb.NM_ROW, "ldb": 512}) == nb.NM_ERR_UNSUPPORTED
+    assert plan_status(**{**base, "meta_layout": nb.NM_META_CANONICAL}) == nb.NM_ERR_UNSUPPORTED
+    assert plan_status(**{**base, "ldb": 1000}) == nb.NM_ERR_INVALID_ARG  # < K
+    assert plan_status(**{**base, "ldb": 1028}) == nb.NM_ERR_MISALIGNED   # not 16 bytes
+    assert plan_status(**{**base, "K": 1000, "ldb": 1024}) == nb.NM_ERR_UNSUPPORTED  # K % 32
+    assert plan_status(**{**base, "n": 8, "m": 32, "meta_layout": nb.NM_META_CANONICAL}) == nb.NM_OK
+    dense = dict(M=256, N=512, K=4096, mode=nb.NM_SPMM_DENSE_MASKED, ab_type="bf16", cd_type="bf16",
+                 order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_ROW, lda=256, ldb=512, ldd=512)
+    assert plan_status(**dense) == nb.NM_OK
+    assert plan_status(**{**dense, "lda": 100}) == nb.NM_ERR_INVALID_ARG
+    assert plan_status(**{**dense, "mode": 7}) == nb.NM_ERR_INVALID_ARG
+    assert plan_status(M=-1, N=1, K=32, ab_type="f16", cd_type="f16", ldb=32, ldd=8) == nb.NM_ERR_INVALID_ARG
+
+
+def test_spmm_rejects_bad_pointers(lib):
+    plan = nb.nm_spmm_plan(nb.make_desc(M=128, N=128, K=128, ab_type="f16", cd_type="f16", ldb=128, ldd=128))
+    with pytest.raises(nb.NmError) as e:
+        nb.nm_spmm(plan, 1.0, FAKE, FAKE, FAKE, 1.0, None, FAKE, stream=0)  # beta != 0 without C
+    assert e.value.status == nb.NM_ERR_INVALID_ARG
+    with pytest.raises(nb.NmError) as e:
+        nb.nm_spmm(plan, 1.0, FAKE + 8, FAKE, FAKE, 0.0, None, FAKE, stream=0)
+    assert e.value.status == nb.NM_ERR_MISALIGNED
+    plan.destroy()
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(nb, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(nb, "_lib", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        nb.lib()

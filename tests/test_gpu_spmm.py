@@ -1,0 +1,211 @@
+"""GPU parity of the products against the CPU oracle (float64 reference).
+
+Sparse 2:4 on tensor cores (forward and the transposed backward operand),
+the masked dense weight gradient, and the CUDA-core N:M gather.  Small shapes
+span several tiles with ragged tails and are compared in full; the workloads'
+full sizes run in the launch configuration the benchmark uses and are
+compared on sampled rows that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+from structured_sparse_gemm_nm_gb300 import binding as nb
+from structured_sparse_gemm_nm_gb300 import inputs
+
+from gpu_util import DEV, assert_gemm_close, bits_of, dev_bytes, ensure_lib, to_dev_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def compress_on_gpu(Wd, M, K, dtype, layout=nb.NM_META_TC, transpose=0):
+    rl, cl = (K, M) if transpose else (M, K)
+    vb, mb = nb.nm_compressed_size(rl, cl, dtype, 2, 4, layout)
+    vals, meta = dev_bytes(vb), dev_bytes(mb)
+    ld = Wd.shape[1] if Wd.dim() == 2 else K
+    nb.nm_compress(Wd, M, K, ld, dtype, 2, 4, transpose, layout, vals, meta)
+    return vals, meta
+
+
+def sample_rows(M, count, seed):
+    if M <= count:
+        return np.arange(M)
+    return np.sort(np.random.default_rng(seed).choice(M, size=count, replace=False))
+
+
+SPARSE_CASES = [
+    # M, N, K, dtype, order_cd, alpha, beta, sampled
+    (64, 32, 128, "f16", nb.NM_COL, 1.0, 0.0, False),      # tiny round trip
+    (256, 4096, 512, "f16", nb.NM_COL, 1.0, 0.0, False),   # SparseLinear forward
+    (512, 4096, 256, "f16", nb.NM_COL, 1.0, 0.0, False),   # its backward (W^T operand shape)
+    (200, 300, 224, "bf16", nb.NM_COL, 1.0, 0.0, False),   # ragged M, N and K % 128
+    (136, 72, 96, "f16", nb.NM_ROW, 2.0, 0.5, False),      # row-major D, alpha/beta
+    (384, 264, 640, "bf16", nb.NM_ROW, -0.5, 1.0, False),
+    (128, 128, 32, "f16", nb.NM_COL, 1.0, 0.25, False),    # a single MMA k-step
+    (1024, 4096, 1024, "f16", nb.NM_COL, 1.0, 0.0, True),  # BERT-Large shapes
+    (4096, 4096, 1024, "f16", nb.NM_COL, 1.0, 0.0, True),
+    (1024, 4096, 4096, "f16", nb.NM_COL, 1.0, 0.0, True),
+    (3072, 16384, 768, "bf16", nb.NM_COL, 1.0, 0.0, True),  # GPT-neo FC1 forward
+    (768, 16384, 3072, "bf16", nb.NM_COL, 1.0, 0.0, True),  # GPT-neo FC1 backward (dX)
+]
+
+
+@pytest.mark.parametrize("M,N,K,dtype,order_cd,alpha,beta,sampled", SPARSE_CASES)
+def test_sparse_tc_matches_oracle(M, N, K, dtype, order_cd, alpha, beta, sampled):
+    std = 0.02 if K >= 512 else 0.5
+    W = inputs.normal((M, K), std, inputs.SEED_W + M, dtype)
+    X = inputs.normal((N, K), 1.0, inputs.SEED_X + N, dtype)  # B stored N x K
+    Wd, Xd = W.to(DEV), X.to(DEV)
+    vals, meta = compress_on_gpu(Wd, M, K, dtype)
+    cd_shape = (M, N) if order_cd == nb.NM_ROW else (N, M)
+    ld = cd_shape[1]
+    C = inputs.normal(cd_shape, 1.0, inputs.SEED_C, dtype).to(DEV) if beta != 0 else None
+    D = torch.full(cd_shape, float("nan"), dtype=C.dtype if C is not None else Wd.dtype, device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type=dtype, cd_type=dtype, ldb=K,
+                                        ldc=ld if C is not None else 0, ldd=ld, order_cd=order_cd))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nb.nm_spmm(plan, alpha, vals, meta, Xd, beta, C, D, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    Wb = inputs.as_numpy_bits(W)
+    A = o.decode(o.nm_prune(Wb, dtype, 2, 4)[0], dtype)
+    Bm = o.decode(inputs.as_numpy_bits(X), dtype).T  # K x N
+    got = D.cpu().double().numpy()
+    got = got if order_cd == nb.NM_ROW else got.T  # M x N
+    Cm = None
+    if C is not None:
+        Cm = C.cpu().double().numpy()
+        Cm = Cm if order_cd == nb.NM_ROW else Cm.T
+    rows = sample_rows(M, 256, seed=M + N) if sampled else np.arange(M)
+    ref = o.spmm(alpha, A[rows], Bm, beta, Cm[rows] if Cm is not None else None)
+    assert_gemm_close(got[rows], ref, f"sparse {M}x{N}x{K} {dtype}")
+
+
+def test_sparse_backward_uses_transposable_compressed_wt():
+    """dX^T = W^T dY^T with the W^T operand from the transposable prune (MLP layer 512 -> 256)."""
+    out_f, in_f, T = 256, 512, 4096
+    W = inputs.normal((out_f, in_f), 0.05, inputs.SEED_W, "f16")
+    dY = inputs.normal((T, out_f), 0.01, inputs.SEED_DY, "f16")
+    Wd, dYd = W.to(DEV), dY.to(DEV)
+    vb, mb = nb.nm_compressed_size(in_f, out_f, "f16", 2, 4, nb.NM_META_TC)
+    valsT, metaT = dev_bytes(vb), dev_bytes(mb)
+    nb.nm_prune_transposable(Wd, out_f, in_f, in_f, "f16", valsT=valsT, metaT=metaT, layout=nb.NM_META_TC)
+    dX = torch.empty((T, in_f), dtype=torch.float16, device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=in_f, N=T, K=out_f, ab_type="f16", cd_type="f16", ldb=out_f, ldd=in_f))
+    nb.nm_spmm(plan, 1.0, valsT, metaT, dYd, 0.0, None, dX)
+    torch.cuda.synchronize()
+    pruned = o.nm_prune_transposable(inputs.as_numpy_bits(W), "f16")[0]
+    ref = o.spmm(1.0, o.decode(pruned, "f16").T, o.decode(inputs.as_numpy_bits(dY), "f16").T)  # in x T
+    assert_gemm_close(dX.cpu().double().numpy().T, ref, "dX")
+
+
+DENSE_CASES = [
+    # M (out), N (in), K (tokens), dtype, sampled
+    (256, 512, 4096, "f16", False),    # SparseLinear 512 -> 256 weight gradient
+    (104, 200, 96, "bf16", False),     # ragged
+    (136, 72, 1000, "f16", False),     # K not a multiple of the stage
+    (3072, 768, 16384, "bf16", True),  # GPT-neo FC1 dW
+    (768, 3072, 16384, "bf16", True),  # GPT-neo FC2 dW
+]
+
+
+@pytest.mark.parametrize("M,N,K,dtype,sampled", DENSE_CASES)
+def test_masked_weight_grad_matches_oracle(M, N, K, dtype, sampled):
+    dY = inputs.normal((K, M), 1.0, inputs.SEED_DY + K, dtype)   # tokens x out
+    X = inputs.normal((K, N), 1.0, inputs.SEED_X + K, dtype)     # tokens x in
+    W = inputs.normal((M, N), 0.02, inputs.SEED_W, dtype)
+    pruned, mask_ref = o.nm_prune(inputs.as_numpy_bits(W), dtype, 2, 4)
+    bits = torch.from_numpy(o.mask_to_bits(mask_ref).view(np.int32)).to(DEV)
+    dW = torch.empty((M, N), dtype=dY.dtype, device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, mode=nb.NM_SPMM_DENSE_MASKED, ab_type=dtype, cd_type=dtype,
+                                        order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_ROW, lda=M, ldb=N,
+                                        ldd=N, meta_layout=nb.NM_META_CANONICAL))
+    ws_bytes = nb.nm_spmm_plan_workspace(plan)
+    ws = dev_bytes(ws_bytes) if ws_bytes else None
+    nb.nm_spmm(plan, 1.0, dY.to(DEV), bits, X.to(DEV), 0.0, None, dW, ws, ws_bytes)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, 128, seed=K) if sampled else np.arange(M)
+    dYm = o.decode(inputs.as_numpy_bits(dY), dtype)
+    Xm = o.decode(inputs.as_numpy_bits(X), dtype)
+    ref = o.masked_weight_grad(dYm[:, rows], Xm, mask_ref[rows])
+    assert_gemm_close(dW.cpu().double().numpy()[rows], ref, f"dW {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("n", [4, 8, 16])
+@pytest.mark.parametrize("batch", [1, 8])
+def test_nm_gather_gemv_matches_oracle(n, batch):
+    M = K = 4096
+    W = inputs.normal((M, K), 0.02, inputs.SEED_W, "f16")
+    x = inputs.normal((batch, K), 1.0, inputs.SEED_VEC, "f16")
+    Wd = W.to(DEV)
+    vb, mb = nb.nm_compressed_size(M, K, "f16", n, 32)
+    vals, idx = dev_bytes(vb), dev_bytes(mb)
+    nb.nm_compress(Wd, M, K, K, "f16", n, 32, 0, nb.NM_META_CANONICAL, vals, idx)
+    y = torch.empty((batch, M), dtype=torch.float16, device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=batch, K=K, n=n, m=32, ab_type="f16", cd_type="f16", ldb=K, ldd=M,
+                                        meta_layout=nb.NM_META_CANONICAL))
+    nb.nm_spmm(plan, 1.0, vals, idx, x.to(DEV), 0.0, None, y)
+    torch.cuda.synchronize()
+    A = o.decode(o.nm_prune(inputs.as_numpy_bits(W), "f16", n, 32)[0], "f16")
+    ref = o.spmm(1.0, A, o.decode(inputs.as_numpy_bits(x), "f16").T)
+    assert_gemm_close(y.cpu().double().numpy().T, ref, f"gemv n={n} b={batch}")
+
+
+def test_gather_ragged_and_beta():
+    M, K, N, n, m = 77, 96, 11, 3, 8
+    W = inputs.normal((M, K), 0.5, 9, "bf16")
+    B = inputs.normal((N, K), 1.0, 10, "bf16")
+    C = inputs.normal((M, N), 1.0, 11, "bf16")
+    vb, mb = nb.nm_compressed_size(M, K, "bf16", n, m)
+    vals, idx = dev_bytes(vb), dev_bytes(mb)
+    nb.nm_compress(W.to(DEV), M, K, K, "bf16", n, m, 0, nb.NM_META_CANONICAL, vals, idx)
+    Cd = C.to(DEV)
+    D = torch.empty((M, 16), dtype=torch.bfloat16, device=DEV)  # ldd = 16 (row-major M x N, padded)
+    Cp = torch.zeros((M, 16), dtype=torch.bfloat16, device=DEV)
+    Cp[:, :N] = Cd
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, n=n, m=m, ab_type="bf16", cd_type="bf16", ldb=K, ldc=16,
+                                        ldd=16, order_cd=nb.NM_ROW, meta_layout=nb.NM_META_CANONICAL))
+    nb.nm_spmm(plan, 0.5, vals, idx, B.to(DEV), -2.0, Cp, D)
+    torch.cuda.synchronize()
+    A = o.decode(o.nm_prune(inputs.as_numpy_bits(W), "bf16", n, m)[0], "bf16")
+    ref = o.spmm(0.5, A, o.decode(inputs.as_numpy_bits(B), "bf16").T, -2.0, C.double().numpy())
+    assert_gemm_close(D.cpu().double().numpy()[:, :N], ref, "gather ragged")
+
+
+def test_k_zero_gives_beta_c():
+    M, N = 64, 48
+    C = inputs.normal((N, M), 1.0, 3, "f16").to(DEV)
+    D = torch.empty((N, M), dtype=torch.float16, device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=0, ab_type="f16", cd_type="f16", ldb=8, ldc=M, ldd=M))
+    nb.nm_spmm(plan, 1.0, None, None, None, 0.5, C, D)
+    torch.cuda.synchronize()
+    assert torch.equal(D, (C.float() * 0.5).half())
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait nothing completes gives up after its budget: NM_ERR_TIMEOUT, no hang, GPU still usable."""
+    M, N, K = 128, 128, 256
+    W = inputs.normal((M, K), 0.5, 1, "f16").to(DEV)
+    X = inputs.normal((N, K), 1.0, 2, "f16").to(DEV)
+    vals, meta = compress_on_gpu(W, M, K, "f16")
+    D = torch.zeros((N, M), dtype=torch.float16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    desc = nb.make_desc(M=M, N=N, K=K, ab_type="f16", cd_type="f16", ldb=K, ldd=M)
+    nb.nm_test_spmm_wait_timeout(desc, vals, meta, X, D, status, budget_cycles=1 << 22)
+    torch.cuda.synchronize()
+    assert int(status.item()) == nb.NM_ERR_TIMEOUT
+    # the context is intact: a normal product still runs and is right
+    status.zero_()
+    plan = nb.nm_spmm_plan(desc)
+    nb.nm_spmm(plan, 1.0, vals, meta, X, 0.0, None, D, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    A = o.decode(o.nm_prune(bits_of(W, "f16", (M, K)), "f16", 2, 4)[0], "f16")
+    ref = o.spmm(1.0, A, o.decode(bits_of(X, "f16", (N, K)), "f16").T)
+    assert_gemm_close(D.cpu().double().numpy().T, ref, "after timeout")

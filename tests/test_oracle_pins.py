@@ -378,14 +378,18 @@ def test_tc_layout_round_trip_and_grouping():
     W = f16_bits(rng.standard_normal((40, 96)))
     _, meta = o.nm_compress(W, "f16", 2, 4)
     tc = o.meta_to_tc_layout(meta, 40, 96)
-    assert tc.shape == (48, 4)
+    assert tc.shape == (3, 128, 4)
     assert (o.meta_from_tc_layout(tc, 40, 96) == meta).all()
+    assert (tc[:, :, 1:] == o.TC_PAD_CODE_WORD).all()
+    # rows 40..47 are the high halves of slots 32..47; slots 48.. are filler
+    assert (tc[:, 48:, 0] == o.TC_PAD_CODE_WORD).all()
+    assert ((tc[:, 32:48, 0] >> 16) == 0x4444).all()
     # each slot word pairs rows i and i+8 of its 16-row block at the same 16 columns
     for slot in range(40):
         b, j = divmod(slot, 16)
         h, i = divmod(j, 8)
         for s in range(3):
             lo_row, hi_row = 16 * b + i, 16 * b + 8 + i
-            assert int(tc[slot, s]) & 0xFFFF == int(meta[lo_row, 2 * s + h])
+            assert int(tc[s, slot, 0]) & 0xFFFF == int(meta[lo_row, 2 * s + h])
             if hi_row < 40:
-                assert int(tc[slot, s]) >> 16 == int(meta[hi_row, 2 * s + h])
+                assert int(tc[s, slot, 0]) >> 16 == int(meta[hi_row, 2 * s + h])
