@@ -1,0 +1,695 @@
+#!/usr/bin/env python3
+"""Benchmark of the N:M structured-sparsity hot path on GB300.
+
+One step is one training pass over the GPT-neo-125M-shaped linears (12
+layers of QKV 768->2304, O 768->768, FC1 768->3072, FC2 3072->768, 16384
+tokens, bf16, synthetic): for every weight a run-time transposable 2:4 prune
+and compression (W and W^T, tensor-core metadata, bit mask), the sparse
+forward Y = X W^T, the sparse backward dX = dY W (through the compressed
+W^T) and the masked weight gradient dW = mask * (dY^T X).  The step is
+captured once as a CUDA graph and replayed.
+
+``value`` is the step's dense-equivalent throughput: the 144 products' 2*M*N*K
+over the step time (prune included).  ``rows`` reports every hot-path row on
+its own: each product class against the 2:4-sparse or dense tensor peak,
+cuBLAS on the same shapes, prune/compress/decompress/check and the N:M GEMV
+in GB/s against HBM bandwidth.  ``cpu_baseline`` times the CPU oracle on a
+bounded sample of the same step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "2:4 SpMM dense-equiv TFLOPS & % of sparse TC peak; prune+compress GB/s"
+UNIT = "TFLOPS (dense-equivalent)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SPARSE_RATIO = 2.0  # nominal 2:4-sparse / dense tensor rate for 16-bit inputs
+WORKLOAD = ("gptneo125m_train_linears: 12 layers x {qkv 2304x768, o 768x768, fc1 3072x768, fc2 768x3072}, "
+            "16384 tokens (8x2048), bf16, run-time transposable 2:4 prune+compress, Y=X W^T, dX=dY W, "
+            "dW=mask*(dY^T X)")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+KERNEL_SOURCES = {
+    "spmm_tc_sparse": "structured_sparse_gemm_nm_gb300/csrc/nm_spmm_tc.cu",
+    "spmm_tc_dense_masked": "structured_sparse_gemm_nm_gb300/csrc/nm_spmm_tc.cu",
+    "transposable": "structured_sparse_gemm_nm_gb300/csrc/nm_transposable.cu",
+}
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {k: float(d.get(k, FALLBACK_PEAKS[k])) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(rel: str) -> str:
+    return hashlib.sha256(open(os.path.join(ROOT, rel), "rb").read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    want = source_hash(KERNEL_SOURCES[kernel])
+    for line in open(TRAFFIC_FILE):
+        parts = line.split()
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == want:
+            return {"bytes_per_launch": float(parts[2]), "workload": " ".join(parts[3:])}
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples taken while the timed regions run."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.windows = []
+
+    def start(self):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "50"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def mark(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.2)
+        self.proc.terminate()
+        self.proc.wait()
+        self.out.flush()
+        rows = []
+        for line in open(self.out.name):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.out.name)
+        inside = [r for r in rows if any(a - 0.06 <= r[0] <= b + 0.06 for a, b in self.windows)] or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[3][i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+                "sm_max_mhz": max([r[2] for r in inside]) if inside else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------------ workload
+class GptNeoTrain:
+    """Device buffers, plans and launch sequence of one training step."""
+
+    def __init__(self, torch, nb, inputs, dev, layers: int, tokens: int):
+        self.torch, self.nb = torch, nb
+        self.T = T = tokens
+        self.dtype = "bf16"
+        tdt = torch.bfloat16
+        TC = nb.NM_META_TC
+        self.linears = inputs.GPTNEO_LINEARS
+        self.layers = []
+        for l in range(layers):
+            lay = []
+            for j, (_, out_f, in_f) in enumerate(self.linears):
+                vb, mb = nb.nm_compressed_size(out_f, in_f, "bf16", 2, 4, TC)
+                vbT, mbT = nb.nm_compressed_size(in_f, out_f, "bf16", 2, 4, TC)
+                lay.append(dict(
+                    out=out_f, inp=in_f,
+                    W=inputs.normal((out_f, in_f), 0.02, inputs.gptneo_seed(l, j, 0), "bf16", device=dev),
+                    X=inputs.normal((T, in_f), 1.0, inputs.gptneo_seed(l, j, 1), "bf16", device=dev),
+                    dY=inputs.normal((T, out_f), 1.0, inputs.gptneo_seed(l, j, 2), "bf16", device=dev),
+                    vals=torch.empty(vb, dtype=torch.uint8, device=dev), meta=torch.empty(mb, dtype=torch.uint8, device=dev),
+                    valsT=torch.empty(vbT, dtype=torch.uint8, device=dev),
+                    metaT=torch.empty(mbT, dtype=torch.uint8, device=dev),
+                    mask=torch.empty(out_f * ((in_f + 31) // 32), dtype=torch.int32, device=dev),
+                    dW=torch.empty((out_f, in_f), dtype=tdt, device=dev),
+                    prune_bytes=out_f * in_f * 2 + vb + mb + vbT + mbT + out_f * ((in_f + 31) // 32) * 4,
+                ))
+            self.layers.append(lay)
+        self.Y = [torch.empty((T, o), dtype=tdt, device=dev) for (_, o, i) in self.linears]
+        self.dX = [torch.empty((T, i), dtype=tdt, device=dev) for (_, o, i) in self.linears]
+        self.p_fwd, self.p_dx, self.p_dw, self.ws = [], [], [], []
+        for (_, o, i) in self.linears:
+            self.p_fwd.append(nb.nm_spmm_plan(nb.make_desc(M=o, N=T, K=i, ab_type="bf16", cd_type="bf16", ldb=i, ldd=o)))
+            self.p_dx.append(nb.nm_spmm_plan(nb.make_desc(M=i, N=T, K=o, ab_type="bf16", cd_type="bf16", ldb=o, ldd=i)))
+            pdw = nb.nm_spmm_plan(nb.make_desc(M=o, N=i, K=T, mode=nb.NM_SPMM_DENSE_MASKED, ab_type="bf16",
+                                               cd_type="bf16", order_a=nb.NM_COL, order_b=nb.NM_ROW,
+                                               order_cd=nb.NM_ROW, lda=o, ldb=i, ldd=i,
+                                               meta_layout=nb.NM_META_CANONICAL))
+            self.p_dw.append(pdw)
+            wsb = nb.nm_spmm_plan_workspace(pdw)
+            self.ws.append((torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev), wsb))
+
+    def gemm_flops(self, j: int) -> float:
+        _, o, i = self.linears[j]
+        return 2.0 * o * i * self.T
+
+    def flops_per_step(self) -> float:
+        return 3.0 * sum(self.gemm_flops(j) for j in range(len(self.linears))) * len(self.layers)
+
+    def enqueue(self, parts=("prune", "fwd", "dx", "dw"), only=None) -> int:
+        """Launch the step's work on the current stream; returns the number of kernels launched."""
+        nb = self.nb
+        n = 0
+        for lay in self.layers:
+            for j, L in enumerate(lay):
+                if only is not None and j != only:
+                    continue
+                o, i = L["out"], L["inp"]
+                if "prune" in parts:
+                    nb.nm_prune_transposable(L["W"], o, i, i, "bf16", None, 0, L["mask"], L["vals"], L["meta"],
+                                             L["valsT"], L["metaT"], nb.NM_META_TC)
+                    n += 1
+                if "fwd" in parts:
+                    nb.nm_spmm(self.p_fwd[j], 1.0, L["vals"], L["meta"], L["X"], 0.0, None, self.Y[j])
+                    n += 1
+                if "dx" in parts:
+                    nb.nm_spmm(self.p_dx[j], 1.0, L["valsT"], L["metaT"], L["dY"], 0.0, None, self.dX[j])
+                    n += 1
+                if "dw" in parts:
+                    ws, wsb = self.ws[j]
+                    nb.nm_spmm(self.p_dw[j], 1.0, L["dY"], L["mask"], L["X"], 0.0, None, L["dW"], ws if wsb else None,
+                               wsb)
+                    n += 1
+        return n
+
+
+def capture(torch, fn):
+    """CUDA graph of fn's launches (fn runs once untimed first)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_replays(torch, g, reps: int, barrier=None) -> float:
+    """Milliseconds for `reps` back-to-back replays, events on the replay stream."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return a.elapsed_time(b)
+
+
+class Flusher:
+    """Writes a buffer larger than L2 between timed launches."""
+
+    def __init__(self, torch, dev, mib=512):
+        self.buf = torch.empty(mib << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def time_launch(torch, fn, flush, reps=10, warm=3):
+    """Median milliseconds of one launch of fn, L2 flushed before each."""
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+# ------------------------------------------------------------------ rows
+def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
+    flush = Flusher(torch, dev)
+    hbm = peaks["hbm_gbs"]
+    dense_peak = peaks["bf16_tflops"]
+    sparse_peak = dense_peak * SPARSE_RATIO
+    rows = {}
+
+    # S5/S6/S7 per GPT-neo shape, one layer's weights, with cuBLAS on the dense pruned weight
+    L0 = wl.layers[0]
+    for j, (name, o, i) in enumerate(wl.linears):
+        L = L0[j]
+        f = wl.gemm_flops(j)
+        t_fwd = time_launch(torch, lambda: nb.nm_spmm(wl.p_fwd[j], 1.0, L["vals"], L["meta"], L["X"], 0.0, None, wl.Y[j]), flush)
+        t_dx = time_launch(torch, lambda: nb.nm_spmm(wl.p_dx[j], 1.0, L["valsT"], L["metaT"], L["dY"], 0.0, None, wl.dX[j]), flush)
+        ws, wsb = wl.ws[j]
+        t_dw = time_launch(torch, lambda: nb.nm_spmm(wl.p_dw[j], 1.0, L["dY"], L["mask"], L["X"], 0.0, None, L["dW"],
+                                                     ws if wsb else None, wsb), flush)
+        Wd = L["W"]
+        t_cub = time_launch(torch, lambda: torch.matmul(L["X"], Wd.t()), flush)
+        t_cub_dx = time_launch(torch, lambda: torch.matmul(L["dY"], Wd), flush)
+        rows[f"S5_fwd_{name}"] = {"shape_MNK": [o, wl.T, i], "ms": t_fwd, "tflops": f / t_fwd / 1e9,
+                                  "frac_sparse_peak": f / t_fwd / 1e9 / sparse_peak,
+                                  "cublas_dense_tflops": f / t_cub / 1e9, "speedup_vs_cublas": t_cub / t_fwd}
+        rows[f"S6_dx_{name}"] = {"shape_MNK": [i, wl.T, o], "ms": t_dx, "tflops": f / t_dx / 1e9,
+                                 "frac_sparse_peak": f / t_dx / 1e9 / sparse_peak,
+                                 "cublas_dense_tflops": f / t_cub_dx / 1e9, "speedup_vs_cublas": t_cub_dx / t_dx}
+        rows[f"S7_dw_{name}"] = {"shape_MNK": [o, i, wl.T], "ms": t_dw, "tflops": f / t_dw / 1e9,
+                                 "frac_dense_peak": f / t_dw / 1e9 / dense_peak}
+
+    # S3: transposable prune + dual compress, one layer's four weights
+    for j, (name, o, i) in enumerate(wl.linears):
+        L = L0[j]
+        t = time_launch(torch, lambda: nb.nm_prune_transposable(L["W"], o, i, i, "bf16", None, 0, L["mask"], L["vals"],
+                                                                L["meta"], L["valsT"], L["metaT"], nb.NM_META_TC), flush)
+        rows[f"S3_transposable_{name}"] = {"shape": [o, i], "ms": t, "bytes": L["prune_bytes"],
+                                           "gbs": L["prune_bytes"] / t / 1e6, "frac_hbm": L["prune_bytes"] / t / 1e6 / hbm}
+
+    # S1 / S2 / S4 / S8 on the 4096 x 4096 f16 weight
+    M = K = 4096
+    W = inputs.normal((M, K), 0.02, inputs.SEED_W, "f16", device=dev)
+    for layout, lname in ((nb.NM_META_CANONICAL, "canonical"), (nb.NM_META_TC, "tensor_core")):
+        vb, mb = nb.nm_compressed_size(M, K, "f16", 2, 4, layout)
+        vals = torch.empty(vb, dtype=torch.uint8, device=dev)
+        meta = torch.empty(mb, dtype=torch.uint8, device=dev)
+        t = time_launch(torch, lambda: nb.nm_compress(W, M, K, K, "f16", 2, 4, 0, layout, vals, meta), flush)
+        byt = M * K * 2 + vb + mb
+        rows[f"S1_prune_compress_24_{lname}"] = {"shape": [M, K], "ms": t, "bytes": byt, "gbs": byt / t / 1e6,
+                                                 "frac_hbm": byt / t / 1e6 / hbm}
+        Wout = torch.empty_like(W)
+        t = time_launch(torch, lambda: nb.nm_decompress(vals, meta, M, K, "f16", 2, 4, layout, Wout, K), flush)
+        byt = vb + mb + M * K * 2
+        rows[f"S4_decompress_24_{lname}"] = {"ms": t, "bytes": byt, "gbs": byt / t / 1e6, "frac_hbm": byt / t / 1e6 / hbm}
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    t = time_launch(torch, lambda: nb.nm_check(W, M, K, K, "f16", 2, 4, 1, cnt), flush)
+    rows["S4_check_24_transposable"] = {"ms": t, "bytes": M * K * 2 * 2, "gbs": M * K * 4 / t / 1e6,
+                                        "frac_hbm": M * K * 4 / t / 1e6 / hbm}
+    t = time_launch(torch, lambda: nb.nm_prune(W, M, K, K, "f16", 2, 4, W, K, None), flush)
+    rows["S1_prune_inplace_24"] = {"ms": t, "bytes": M * K * 4, "gbs": M * K * 4 / t / 1e6,
+                                   "frac_hbm": M * K * 4 / t / 1e6 / hbm}
+    W = inputs.normal((M, K), 0.02, inputs.SEED_W, "f16", device=dev)
+    for n in (4, 8, 16):
+        vb, mb = nb.nm_compressed_size(M, K, "f16", n, 32)
+        vals = torch.empty(vb, dtype=torch.uint8, device=dev)
+        idx = torch.empty(mb, dtype=torch.uint8, device=dev)
+        t = time_launch(torch, lambda: nb.nm_compress(W, M, K, K, "f16", n, 32, 0, nb.NM_META_CANONICAL, vals, idx), flush)
+        byt = M * K * 2 + vb + mb
+        rows[f"S2_prune_compress_{n}of32"] = {"ms": t, "bytes": byt, "gbs": byt / t / 1e6, "frac_hbm": byt / t / 1e6 / hbm}
+        for b in (1, 8):
+            x = inputs.normal((b, K), 1.0, inputs.SEED_VEC, "f16", device=dev)
+            y = torch.empty((b, M), dtype=torch.float16, device=dev)
+            plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=b, K=K, n=n, m=32, ab_type="f16", cd_type="f16", ldb=K, ldd=M,
+                                                meta_layout=nb.NM_META_CANONICAL))
+            t = time_launch(torch, lambda: nb.nm_spmm(plan, 1.0, vals, idx, x, 0.0, None, y), flush)
+            byt = vb + mb + b * K * 2 + b * M * 2
+            rows[f"S8_gemv_{n}of32_b{b}"] = {"ms": t, "bytes": byt, "gbs": byt / t / 1e6,
+                                             "frac_hbm": byt / t / 1e6 / hbm,
+                                             "gflops": 2.0 * M * (K // 32) * n * b / t / 1e6}
+            plan.destroy()
+
+    # BERT-Large-shaped sparse products (f16) with cuBLAS on the same shapes
+    for (Mb, Nb, Kb) in inputs.BERT_SHAPES:
+        Wb = inputs.normal((Mb, Kb), 0.02, inputs.SEED_W, "f16", device=dev)
+        Xb = inputs.normal((Nb, Kb), 1.0, inputs.SEED_X, "f16", device=dev)
+        vb, mb = nb.nm_compressed_size(Mb, Kb, "f16", 2, 4, nb.NM_META_TC)
+        vals = torch.empty(vb, dtype=torch.uint8, device=dev)
+        meta = torch.empty(mb, dtype=torch.uint8, device=dev)
+        nb.nm_compress(Wb, Mb, Kb, Kb, "f16", 2, 4, 0, nb.NM_META_TC, vals, meta)
+        D = torch.empty((Nb, Mb), dtype=torch.float16, device=dev)
+        plan = nb.nm_spmm_plan(nb.make_desc(M=Mb, N=Nb, K=Kb, ab_type="f16", cd_type="f16", ldb=Kb, ldd=Mb))
+        t = time_launch(torch, lambda: nb.nm_spmm(plan, 1.0, vals, meta, Xb, 0.0, None, D), flush)
+        tc = time_launch(torch, lambda: torch.matmul(Xb, Wb.t()), flush)
+        f = 2.0 * Mb * Nb * Kb
+        rows[f"S5_bert_{Mb}x{Nb}x{Kb}_f16"] = {"ms": t, "tflops": f / t / 1e9, "frac_sparse_peak": f / t / 1e9 / sparse_peak,
+                                                "cublas_dense_tflops": f / tc / 1e9, "speedup_vs_cublas": tc / t}
+        plan.destroy()
+    rows["_peaks"] = {"sparse_tflops": sparse_peak, "dense_tflops": dense_peak, "hbm_gbs": hbm,
+                      "note": "burst peaks (isolated launches, L2 flushed before each)"}
+    return rows
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample_step(inputs, layers: int, tokens: int, seed_base: int = 0):
+    """One bounded sample of the step on the CPU oracle; returns (seconds, dense-equivalent flops)."""
+    import numpy as np
+
+    import oracle as o
+
+    flops = 0.0
+    data = []
+    for l in range(layers):
+        for j, (_, out_f, in_f) in enumerate(inputs.GPTNEO_LINEARS):
+            W = inputs.as_numpy_bits(inputs.normal((out_f, in_f), 0.02, inputs.gptneo_seed(l, j, 0) + seed_base, "bf16"))
+            X = inputs.as_numpy_bits(inputs.normal((tokens, in_f), 1.0, inputs.gptneo_seed(l, j, 1) + seed_base, "bf16"))
+            dY = inputs.as_numpy_bits(inputs.normal((tokens, out_f), 1.0, inputs.gptneo_seed(l, j, 2) + seed_base, "bf16"))
+            data.append((W, X, dY, out_f, in_f))
+    t0 = time.perf_counter()
+    for (W, X, dY, out_f, in_f) in data:
+        pruned, mask, (v, m), (vT, mT) = o.nm_prune_transposable(W, "bf16")
+        o.meta_to_tc_layout(m, out_f, in_f)
+        o.meta_to_tc_layout(mT, in_f, out_f)
+        Xd, dYd = o.decode(X, "bf16"), o.decode(dY, "bf16")
+        A = o.decode(o.nm_decompress(v, m, out_f, in_f, 2, 4), "bf16")
+        AT = o.decode(o.nm_decompress(vT, mT, in_f, out_f, 2, 4), "bf16")
+        o.spmm(1.0, A, Xd.T)       # Y^T
+        o.spmm(1.0, AT, dYd.T)     # dX^T
+        o.masked_weight_grad(dYd, Xd, mask)
+        flops += 3 * 2.0 * out_f * in_f * tokens
+    return time.perf_counter() - t0, flops
+
+
+def cpu_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+ORACLE_SAMPLE = (1, 8192)  # layers, tokens per sample step
+
+
+def cpu_baseline(inputs):
+    layers, tokens = ORACLE_SAMPLE
+    secs, flops = oracle_sample_step(inputs, layers, tokens)
+    return {"value": flops / secs / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{layers} layer(s) x 4 linears, {tokens} of 16384 tokens (fwd, dX, masked dW in float64 "
+                      f"numpy/BLAS; transposable prune, compress, decompress), {secs:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from structured_sparse_gemm_nm_gb300 import inputs
+
+    layers, tokens = ORACLE_SAMPLE
+    for _ in range(args.warmup):
+        oracle_sample_step(inputs, layers, tokens)
+    secs, flops = 0.0, 0.0
+    for k in range(args.steps):
+        s, f = oracle_sample_step(inputs, layers, tokens, seed_base=k)
+        secs += s
+        flops += f
+    value = flops / secs / 1e12
+    sample = f"{layers} layer(s) x 4 linears, {tokens} of 16384 tokens per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ native arm
+def aggregate_over_ranks(torch, dist, elapsed_ms: float) -> float:
+    """Max of a per-rank elapsed time over all ranks (plain value when not distributed)."""
+    if dist is None:
+        return elapsed_ms
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_native(args):
+    import torch
+
+    from structured_sparse_gemm_nm_gb300 import binding as nb
+    from structured_sparse_gemm_nm_gb300 import inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        torch.cuda.set_device(local)
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    barrier = dist.barrier if dist else None
+    peaks, peak_kind = load_peaks()
+    nb.lib()
+
+    wl = GptNeoTrain(torch, nb, inputs, dev, inputs.GPTNEO_LAYERS, inputs.GPTNEO_TOKENS)
+    launches_per_step = [0]
+
+    def step():
+        launches_per_step[0] = wl.enqueue()
+
+    g_step = capture(torch, step)
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ms = time_replays(torch, g_step, args.steps, barrier)
+    sampler.mark(t0, time.time())
+    ms = aggregate_over_ranks(torch, dist, ms)
+    ms_step = ms / args.steps
+    flops = wl.flops_per_step()
+    value = flops * world / (ms_step * 1e-3) / 1e12
+
+    # per-class graphs: the roofline of the dominant kernel and the split of the step
+    classes = {}
+    for cls, parts in (("spmm_tc_sparse", ("fwd", "dx")), ("spmm_tc_dense_masked", ("dw",)),
+                       ("transposable", ("prune",))):
+        cnt = [0]
+
+        def f(parts=parts, cnt=cnt):
+            cnt[0] = wl.enqueue(parts)
+
+        g = capture(torch, f)
+        t0 = time.time()
+        cms = time_replays(torch, g, args.steps, barrier)
+        sampler.mark(t0, time.time())
+        classes[cls] = {"ms_per_step": cms / args.steps, "launches_per_step": cnt[0]}
+        del g
+    sparse_flops = 2 * sum(wl.gemm_flops(j) for j in range(4)) * len(wl.layers)
+    dense_flops = sum(wl.gemm_flops(j) for j in range(4)) * len(wl.layers)
+    prune_bytes = sum(L["prune_bytes"] for lay in wl.layers for L in lay)
+    classes["spmm_tc_sparse"]["tflops"] = sparse_flops / classes["spmm_tc_sparse"]["ms_per_step"] / 1e9
+    classes["spmm_tc_dense_masked"]["tflops"] = dense_flops / classes["spmm_tc_dense_masked"]["ms_per_step"] / 1e9
+    classes["transposable"]["gbs"] = prune_bytes / classes["transposable"]["ms_per_step"] / 1e6
+    dominant = max(classes, key=lambda c: classes[c]["ms_per_step"])
+    c = classes[dominant]
+    sustained = peaks["bf16_tflops_sustained"]
+    if dominant == "transposable":
+        achieved, peak, unit, bound = c["gbs"], peaks["hbm_gbs"], "GB/s", "hbm"
+        per_launch_alg = prune_bytes / c["launches_per_step"]
+        pnote = f"HBM copy bandwidth ({peak_kind})"
+    else:
+        achieved = c["tflops"]
+        sparse = dominant == "spmm_tc_sparse"
+        peak = sustained * (SPARSE_RATIO if sparse else 1.0)
+        unit, bound = "TFLOP/s", "tensor"
+        per_launch_alg = (sparse_flops if sparse else dense_flops) / c["launches_per_step"]
+        pnote = (f"{peak_kind} sustained bf16 dense" + (" x 2 (nominal 2:4 sparse ratio)" if sparse else ""))
+    tr = recorded_traffic(dominant)
+    roofline = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": tr["bytes_per_launch"] if tr else None,
+                "algorithmic_per_launch": per_launch_alg, "peak_source": pnote,
+                "traffic_source": tr["workload"] if tr else "no ncu capture of the current kernel source"}
+
+    # end to end: inputs from pinned host memory, dW back to the host, every step
+    e2e = None
+    if not args.no_e2e:
+        host_in, host_out = [], []
+        for lay in wl.layers:
+            for L in lay:
+                for key in ("W", "X", "dY"):
+                    h = torch.empty(L[key].shape, dtype=L[key].dtype, pin_memory=True)
+                    h.copy_(L[key])
+                    host_in.append((h, L[key]))
+                host_out.append((torch.empty(L["dW"].shape, dtype=L["dW"].dtype, pin_memory=True), L["dW"]))
+        h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+        d2h = sum(h.numel() * h.element_size() for h, _ in host_out)
+
+        def e2e_step():
+            for h, d in host_in:
+                d.copy_(h, non_blocking=True)
+            g_step.replay()
+            for h, d in host_out:
+                h.copy_(d, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        reps = max(1, min(args.steps, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if barrier:
+            barrier()
+        t0 = time.time()
+        a.record()
+        for _ in range(reps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        sampler.mark(t0, time.time())
+        ems = aggregate_over_ranks(torch, dist, a.elapsed_time(b)) / reps
+        e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems,
+               "path": "pinned host -> device copies of W, X, dY of every linear, the step through the C ABI, "
+                       "dW of every linear back to pinned host memory, one stream"}
+        del host_in, host_out
+    clocks = sampler.stop()
+
+    rows = None
+    if rank == 0 and not args.no_rows:
+        rows = measure_rows(torch, nb, inputs, dev, wl, peaks)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(inputs)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_tokens": inputs.GPTNEO_TOKENS * world,
+                       "l2": "inputs larger than L2: 4.8 GB of distinct per-linear activations per step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "graph": "one CUDA graph per step"},
+            "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": launches_per_step[0] * args.steps,
+            "step_split_ms": {k: v["ms_per_step"] for k, v in classes.items()},
+            "classes": classes, "rows": rows,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+# ------------------------------------------------------------------ single-kernel cases (ncu captures)
+KERNEL_CASES = ("sparse_fc1_fwd", "sparse_fc2_dx", "dense_fc1_dw", "transposable_fc1", "prune24_4096",
+                "prune_8of32_4096", "gemv_8of32_b8")
+
+
+def run_kernel_case(name: str, reps: int = 3):
+    """Runs one kernel of the hot path `reps` times on inputs larger than L2 (for profiler captures)."""
+    import torch
+
+    from structured_sparse_gemm_nm_gb300 import binding as nb
+    from structured_sparse_gemm_nm_gb300 import inputs
+
+    dev = torch.device("cuda", 0)
+    nb.lib()
+    T = inputs.GPTNEO_TOKENS
+    if name in ("sparse_fc1_fwd", "sparse_fc2_dx", "dense_fc1_dw", "transposable_fc1"):
+        o, i = 3072, 768  # FC1 weight (out x in); FC2 dX has the same M, K
+        W = inputs.normal((o, i), 0.02, 1, "bf16", device=dev)
+        vb, mb = nb.nm_compressed_size(o, i, "bf16", 2, 4, nb.NM_META_TC)
+        vals, meta = (torch.empty(vb, dtype=torch.uint8, device=dev), torch.empty(mb, dtype=torch.uint8, device=dev))
+        mask = torch.empty(o * i // 32, dtype=torch.int32, device=dev)
+        nb.nm_prune_transposable(W, o, i, i, "bf16", None, 0, mask, vals, meta, None, None, nb.NM_META_TC)
+        if name == "transposable_fc1":
+            Ws = [inputs.normal((o, i), 0.02, 10 + r, "bf16", device=dev) for r in range(reps)]
+            vbT, mbT = nb.nm_compressed_size(i, o, "bf16", 2, 4, nb.NM_META_TC)
+            valsT, metaT = (torch.empty(vbT, dtype=torch.uint8, device=dev), torch.empty(mbT, dtype=torch.uint8, device=dev))
+            fn = [lambda Wr=Wr: nb.nm_prune_transposable(Wr, o, i, i, "bf16", None, 0, mask, vals, meta, valsT, metaT,
+                                                         nb.NM_META_TC) for Wr in Ws]
+        elif name == "dense_fc1_dw":
+            dY = inputs.normal((T, o), 1.0, 2, "bf16", device=dev)
+            X = inputs.normal((T, i), 1.0, 3, "bf16", device=dev)
+            dW = torch.empty((o, i), dtype=torch.bfloat16, device=dev)
+            plan = nb.nm_spmm_plan(nb.make_desc(M=o, N=i, K=T, mode=nb.NM_SPMM_DENSE_MASKED, ab_type="bf16",
+                                                cd_type="bf16", order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_ROW,
+                                                lda=o, ldb=i, ldd=i, meta_layout=nb.NM_META_CANONICAL))
+            wsb = nb.nm_spmm_plan_workspace(plan)
+            ws = torch.empty(max(16, wsb), dtype=torch.uint8, device=dev)
+            fn = [lambda: nb.nm_spmm(plan, 1.0, dY, mask, X, 0.0, None, dW, ws if wsb else None, wsb)]
+        else:
+            X = inputs.normal((T, i), 1.0, 2, "bf16", device=dev)
+            Y = torch.empty((T, o), dtype=torch.bfloat16, device=dev)
+            plan = nb.nm_spmm_plan(nb.make_desc(M=o, N=T, K=i, ab_type="bf16", cd_type="bf16", ldb=i, ldd=o))
+            fn = [lambda: nb.nm_spmm(plan, 1.0, vals, meta, X, 0.0, None, Y)]
+    elif name in ("prune24_4096", "prune_8of32_4096", "gemv_8of32_b8"):
+        M = K = 4096
+        n, m = (2, 4) if name == "prune24_4096" else (8, 32)
+        layout = nb.NM_META_TC if m == 4 else nb.NM_META_CANONICAL
+        Ws = [inputs.normal((M, K), 0.02, 20 + r, "f16", device=dev) for r in range(max(reps, 5))]
+        vb, mb = nb.nm_compressed_size(M, K, "f16", n, m, layout)
+        vals, meta = (torch.empty(vb, dtype=torch.uint8, device=dev), torch.empty(mb, dtype=torch.uint8, device=dev))
+        if name == "gemv_8of32_b8":
+            nb.nm_compress(Ws[0], M, K, K, "f16", n, m, 0, layout, vals, meta)
+            x = inputs.normal((8, K), 1.0, 4, "f16", device=dev)
+            y = torch.empty((8, M), dtype=torch.float16, device=dev)
+            plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=8, K=K, n=n, m=m, ab_type="f16", cd_type="f16", ldb=K, ldd=M,
+                                                meta_layout=nb.NM_META_CANONICAL))
+            fn = [lambda: nb.nm_spmm(plan, 1.0, vals, meta, x, 0.0, None, y)]
+        else:
+            fn = [lambda Wr=Wr: nb.nm_compress(Wr, M, K, K, "f16", n, m, 0, layout, vals, meta) for Wr in Ws]
+    else:
+        raise SystemExit(f"unknown kernel case {name}; one of {KERNEL_CASES}")
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for r in range(reps):
+        fn[r % len(fn)]()
+    b.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"kernel_case": name, "reps": reps, "ms_per_launch": a.elapsed_time(b) / reps}), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-rows", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--kernel-case", choices=KERNEL_CASES, help="run one kernel a few times (profiler captures)")
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args(argv)
+    if args.kernel_case:
+        return run_kernel_case(args.kernel_case, args.reps)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

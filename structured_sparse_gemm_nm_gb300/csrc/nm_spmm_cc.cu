@@ -12,6 +12,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "nm_device.cuh"
 #include "nm_internal.h"
 
@@ -104,8 +106,16 @@ cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s) {
   const size_t smem = (size_t)d.K * kBatch * 2;
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    // set once per device to the largest size this kernel may take
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    if (cudaError_t e = cudaGetDevice(&dev)) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(done_mask.load() & bit)) {
+      cudaError_t e = cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e != cudaSuccess) return e;
+      done_mask.fetch_or(bit);
+    }
   }
   const int threads = 256;
   int64_t blocks = (d.M + 7) / 8;

@@ -9,13 +9,14 @@
 //                   sparsity pattern.  Issued as dense tcgen05.mma.
 //
 // One persistent CTA per SM walks output tiles of 128 x 128.  Warp roles:
-//   warp 0      TMA producer: fills a ring of shared-memory stages
-//               (A, B and, for SPARSE, the metadata of 128 dense K per stage)
+//   warp 0      TMA producer: fills a ring of shared-memory stages of 64
+//               dense K (A, B and, for SPARSE, the metadata of two k-steps)
 //   warp 1      owns tensor memory; one lane issues tcgen05.cp (metadata
 //               into TMEM) and tcgen05.mma, committing to mbarriers
-//   warps 2..5  epilogue: tcgen05.ld the FP32 accumulator, alpha/beta, mask,
-//               convert and store; the accumulator is double buffered so the
-//               epilogue of one tile overlaps the main loop of the next.
+//   warps 2..5  epilogue: tcgen05.ld the FP32 accumulator, alpha, mask,
+//               convert, stage 32 x 32 blocks in shared memory and write them
+//               with TMA bulk stores; the accumulator is double buffered so
+//               the epilogue of one tile overlaps the main loop of the next.
 // Every mbarrier wait is bounded; a wait that gives up sets an abort flag
 // and NM_ERR_TIMEOUT in the caller's status word, the roles drain their
 // outstanding asynchronous work and the CTA frees its tensor memory.
@@ -36,25 +37,31 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = 2 * BN;     // two accumulator buffers
-// Metadata of one k-step occupies one TMEM column; the sparse MMA needs that
-// column 64-aligned, so the four k-steps of a stage use columns 256, 320, 384
-// and 448 (each filled by its own tcgen05.cp of 128 lanes x 128 bits).
+constexpr int kAccCols = 2 * BN;  // two accumulator buffers
+// The metadata of one MMA k-step (32 dense K) occupies one TMEM column; the
+// sparse MMA accepts it only at a 64-aligned column, so k-steps rotate
+// through the four columns 256, 320, 384 and 448, each filled by its own
+// tcgen05.cp of 128 lanes x 128 bits (the other three columns of a copy are
+// filler).
 constexpr int kMetaCol = kAccCols;
 constexpr int kMetaColStride = 64;
-constexpr int kATileBytes = BM * 128;  // 128 rows x 128 B (one 128B-swizzle atom wide)
-constexpr int kBChunkBytes = BN * 128; // BN rows x 128 B
+constexpr int kMetaSlots = 4;
 constexpr int kMetaStepBytes = BM * 16;  // one k-step: 128 slot rows x 16 B
-constexpr int kMetaBytes = 4 * kMetaStepBytes;
+constexpr int kKPerStage = 64;           // dense-equivalent K per stage
+constexpr int kBTileBytes = BN * 128;    // BN rows x 64 elements (128B swizzle)
+constexpr int kEpiBufBytes = 32 * 32 * 2;  // one 32 x 32 output block
 
 template <bool SPARSE>
 struct Cfg {
-  static constexpr int kBChunks = SPARSE ? 2 : 1;  // 64-element chunks of B per stage
-  static constexpr int kStageBytes = kATileBytes + kBChunks * kBChunkBytes + (SPARSE ? kMetaBytes : 0);
-  static constexpr int kStages = SPARSE ? 4 : 6;
-  static constexpr int kKPerStage = SPARSE ? 128 : 64;  // dense-equivalent K per stage
-  static constexpr int kBarOffset = kStages * kStageBytes;
+  // SPARSE: A = 128 rows x 32 compressed values (64B swizzle); DENSE: 128 x 64 (128B swizzle).
+  static constexpr int kATileBytes = SPARSE ? BM * 64 : BM * 128;
+  static constexpr int kMetaBytes = SPARSE ? 2 * kMetaStepBytes : 0;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes + kMetaBytes;
+  static constexpr int kStages = SPARSE ? 7 : 6;
+  static constexpr int kEpiOffset = kStages * kStageBytes;
+  static constexpr int kBarOffset = kEpiOffset + kEpiWarps * 2 * kEpiBufBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
 };
 
@@ -62,6 +69,8 @@ struct Params {
   int M, N, K;
   int num_m_blk, num_n_blk, num_k_stages;
   int num_k_steps;  // SPARSE: K / 32 MMA k-steps
+  const uint8_t* meta;  // SPARSE: tensor-core metadata, [k-step][meta_slots][16 B]
+  int64_t meta_slots;
   int a_mn, b_mn;   // DENSE_MASKED operand majors (1 = M/N contiguous)
   int bf16;         // element type: 0 f16, 1 bf16
   float alpha, beta;
@@ -69,6 +78,7 @@ struct Params {
   void* D;
   int64_t ldc, ldd;
   int cd_col;       // 1: D[n * ldd + m]; 0: D[m * ldd + n]
+  int tma_store;    // 1: D written by TMA bulk stores (C not read)
   const uint32_t* mask;
   int64_t mask_words;
   int32_t* status;
@@ -97,6 +107,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait with a suspend-time hint (ns): the thread may sleep until the phase completes.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
 
 // Bounded wait: false if the budget ran out (then the status word and the
 // CTA's abort flag are set) or another role already aborted.
@@ -105,7 +125,7 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try(bar, parity)) return true;
+    if (mbar_try_sleep(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > budget) {
       *abort_flag = 1;
@@ -122,7 +142,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
-
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -130,6 +149,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// Plain bulk copy of `bytes` contiguous bytes (16-byte aligned, multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+               "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Shared-memory matrix descriptor (tcgen05): start, leading/stride byte
 // offsets (16-byte units), fixed version bit 46, swizzle mode in bits 61..63.
@@ -137,7 +174,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swizzle << 61);
 }
-constexpr uint32_t kSwizzle128 = 2, kSwizzleNone = 0;
+constexpr uint32_t kSwizzle128 = 2, kSwizzle64 = 4, kSwizzleNone = 0;
 
 // Instruction descriptor for kind::f16: D = F32, A/B = F16 or BF16.
 __device__ __forceinline__ uint32_t idesc_f16(int bf16, int a_mn, int b_mn, bool sparse) {
@@ -185,12 +222,15 @@ __device__ __forceinline__ float load_cd(const void* base, int64_t off, int bf16
 __device__ __forceinline__ uint16_t to_cd(float x, int bf16) {
   return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
 }
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
+  return (uint32_t)to_cd(lo, bf16) | ((uint32_t)to_cd(hi, bf16) << 16);
+}
 
 // ----------------------------------------------------------------- kernel
 template <bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmE, const Params p) {
+                   const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmD, const Params p) {
   using C = Cfg<SPARSE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -212,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_tfull, 1);
     mbar_init(bar_tfull + 8, 1);
-    mbar_init(bar_tempty, 4);
-    mbar_init(bar_tempty + 8, 4);
+    mbar_init(bar_tempty, kEpiWarps);
+    mbar_init(bar_tempty + 8, kEpiWarps);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -233,7 +273,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
-      if (SPARSE) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmE) : "memory");
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;  // per-stage bits for the drain at the end
@@ -247,23 +286,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb = bar_full + 8 * stage;
           const uint32_t sA = smem_u32(smem + stage * C::kStageBytes);
-          const uint32_t sB = sA + kATileBytes;
-          mbar_expect_tx(fb, C::kStageBytes);
+          const uint32_t sB = sA + C::kATileBytes;
           if constexpr (SPARSE) {
-            tma_load_2d(sA, &tmA, fb, ks * 64, m0);
-            tma_load_2d(sB, &tmB, fb, ks * 128, n0);
-            tma_load_2d(sB + kBChunkBytes, &tmB, fb, ks * 128 + 64, n0);
-            tma_load_3d(sB + 2 * kBChunkBytes, &tmE, fb, 0, m0, ks * 4);
+            // the 128 slot rows of one k-step are 2 KB of contiguous memory: one bulk copy each
+            const int steps = min(2, p.num_k_steps - 2 * ks);
+            mbar_expect_tx(fb, C::kATileBytes + kBTileBytes + steps * kMetaStepBytes);
+            tma_load_2d(sA, &tmA, fb, ks * 32, m0);
+            tma_load_2d(sB, &tmB, fb, ks * 64, n0);
+            for (int j = 0; j < steps; ++j)
+              bulk_load(sB + kBTileBytes + j * kMetaStepBytes,
+                        p.meta + ((int64_t)(2 * ks + j) * p.meta_slots + m0) * 16, kMetaStepBytes, fb);
           } else {
+            mbar_expect_tx(fb, C::kStageBytes);
             if (p.a_mn) {
               tma_load_2d(sA, &tmA, fb, m0, ks * 64);
-              tma_load_2d(sA + kATileBytes / 2, &tmA, fb, m0 + 64, ks * 64);
+              tma_load_2d(sA + C::kATileBytes / 2, &tmA, fb, m0 + 64, ks * 64);
             } else {
               tma_load_2d(sA, &tmA, fb, ks * 64, m0);
             }
             if (p.b_mn) {
               tma_load_2d(sB, &tmB, fb, n0, ks * 64);
-              tma_load_2d(sB + kBChunkBytes / 2, &tmB, fb, n0 + 64, ks * 64);
+              tma_load_2d(sB + kBTileBytes / 2, &tmB, fb, n0 + 64, ks * 64);
             } else {
               tma_load_2d(sB, &tmB, fb, ks * 64, n0);
             }
@@ -293,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      uint32_t meta_slot = 0;  // running k-step count modulo the slot ring
       bool ok = true;
       if (p.fault_test) ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);  // nothing arrives: runs out
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
@@ -306,24 +350,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + stage * C::kStageBytes);
-          const uint32_t sB = sA + kATileBytes;
+          const uint32_t sB = sA + C::kATileBytes;
           if constexpr (SPARSE) {
-            const int steps = min(4, p.num_k_steps - 4 * ks);  // no MMA past K
+            const int steps = min(2, p.num_k_steps - 2 * ks);  // no MMA past K
             for (int j = 0; j < steps; ++j) {
-              const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * j;
+              const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * meta_slot;
+              meta_slot = (meta_slot + 1) & (kMetaSlots - 1);
               // k-step j: 128 slot rows x 16 B, rows contiguous (8-row core matrices 128 B apart)
-              const uint64_t md = sdesc(sB + 2 * kBChunkBytes + j * kMetaStepBytes, 16, 128, kSwizzleNone);
+              const uint64_t md = sdesc(sB + kBTileBytes + j * kMetaStepBytes, 16, 128, kSwizzleNone);
               asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(tmeta), "l"(md));
-              const uint64_t ad = sdesc(sA + 32 * j, 16, 1024, kSwizzle128);
-              const uint64_t bd = sdesc(sB + (j >> 1) * kBChunkBytes + 64 * (j & 1), 16, 1024, kSwizzle128);
+              // A: 128 rows x 64 B (64B swizzle, 8-row groups 512 B apart), 16 values = 32 B per k-step
+              const uint64_t ad = sdesc(sA + 32 * j, 16, 512, kSwizzle64);
+              // B: BN rows x 128 B (128B swizzle), 32 values = 64 B per k-step
+              const uint64_t bd = sdesc(sB + 64 * j, 16, 1024, kSwizzle128);
               mma_sparse(tacc, ad, bd, tmeta, idesc, (ks > 0 || j > 0) ? 1u : 0u);
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const uint64_t ad = p.a_mn ? sdesc(sA + 2048 * j, kATileBytes / 2, 1024, kSwizzle128)
+              const uint64_t ad = p.a_mn ? sdesc(sA + 2048 * j, C::kATileBytes / 2, 1024, kSwizzle128)
                                          : sdesc(sA + 32 * j, 16, 1024, kSwizzle128);
-              const uint64_t bd = p.b_mn ? sdesc(sB + 2048 * j, kBChunkBytes / 2, 1024, kSwizzle128)
+              const uint64_t bd = p.b_mn ? sdesc(sB + 2048 * j, kBTileBytes / 2, 1024, kSwizzle128)
                                          : sdesc(sB + 32 * j, 16, 1024, kSwizzle128);
               mma_dense(tacc, ad, bd, idesc, (ks > 0 || j > 0) ? 1u : 0u);
             }
@@ -348,72 +395,94 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int ew = warp - 2;
+    uint8_t* ebuf = smem + C::kEpiOffset + ew * 2 * kEpiBufBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
+    int nbuf = 0;  // stores issued by this warp (selects the staging buffer)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.wait_budget, p.status)) break;
       tc_fence_after();
       const int m0 = (tile % p.num_m_blk) * BM, n0 = (tile / p.num_m_blk) * BN;
-      const int row = m0 + 32 * q + lane;
+      const int mq = m0 + 32 * q;
+      const int row = mq + lane;
       const bool row_ok = row < p.M;
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
+        __syncwarp();  // tcgen05.ld is warp-collective: reconverge after any per-lane skip
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * BN + ch * 32, v);
+        if (ch == BN / 32 - 1) {
+          // the accumulator buffer is drained: the next tile's MMAs may reuse it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+        }
         const int nb = n0 + ch * 32;
-        if (!row_ok || nb >= p.N) continue;
+        if (mq >= p.M || nb >= p.N) continue;
         uint32_t mword = 0xFFFFFFFFu;
-        if (!SPARSE && p.mask != nullptr) mword = p.mask[(int64_t)row * p.mask_words + nb / 32];
-        const int cnt = min(32, p.N - nb);
-        if (p.cd_col) {
+        if (!SPARSE && p.mask != nullptr && row_ok) mword = p.mask[(int64_t)row * p.mask_words + nb / 32];
+        if (p.tma_store) {
+          uint8_t* buf = ebuf + (nbuf & 1) * kEpiBufBytes;
+          if (nbuf >= 2) {
+            if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+            __syncwarp();
+          }
+          if (p.cd_col) {
+            // block [32 n][32 m], 64-byte rows: element (n, m) at (n * 32 + m) * 2
+            uint16_t* b16 = reinterpret_cast<uint16_t*>(buf);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
+              b16[j * 32 + lane] = to_cd(x, p.bf16);
+            }
+          } else {
+            // block [32 m][32 n], 64-byte rows in the 64B-swizzled order the store map expects:
+            // 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
+            uint4* b4 = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t w[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int j = 8 * c + 2 * t;
+                const float x0 = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
+                const float x1 = ((mword >> (j + 1)) & 1u) ? __uint_as_float(v[j + 1]) * p.alpha : 0.0f;
+                w[t] = pack2(x0, x1, p.bf16);
+              }
+              b4[c ^ ((lane >> 1) & 3)] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            if (p.cd_col)
+              tma_store_2d(&tmD, smem_u32(buf), mq, nb);
+            else
+              tma_store_2d(&tmD, smem_u32(buf), nb, mq);
+            bulk_commit();
+          }
+          ++nbuf;
+        } else {
+          if (!row_ok) continue;
+          const int cnt = min(32, p.N - nb);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (j >= cnt) break;
             float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) : 0.0f;
             x *= p.alpha;
-            const int64_t off = (int64_t)(nb + j) * p.ldd + row;
-            if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, (int64_t)(nb + j) * p.ldc + row, p.bf16), x);
-            reinterpret_cast<uint16_t*>(p.D)[off] = to_cd(x, p.bf16);
-          }
-        } else {
-          uint16_t* drow = reinterpret_cast<uint16_t*>(p.D) + (int64_t)row * p.ldd + nb;
-          const int64_t coff = (int64_t)row * p.ldc + nb;
-          if (cnt == 32) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float x0 = ((mword >> j) & 1u) ? __uint_as_float(v[j]) : 0.0f;
-              float x1 = ((mword >> (j + 1)) & 1u) ? __uint_as_float(v[j + 1]) : 0.0f;
-              x0 *= p.alpha;
-              x1 *= p.alpha;
-              if (p.C != nullptr) {
-                x0 = fmaf(p.beta, load_cd(p.C, coff + j, p.bf16), x0);
-                x1 = fmaf(p.beta, load_cd(p.C, coff + j + 1, p.bf16), x1);
-              }
-              packed[j / 2] = (uint32_t)to_cd(x0, p.bf16) | ((uint32_t)to_cd(x1, p.bf16) << 16);
-            }
-            uint4* d4 = reinterpret_cast<uint4*>(drow);
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-              d4[t] = make_uint4(packed[4 * t], packed[4 * t + 1], packed[4 * t + 2], packed[4 * t + 3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j >= cnt) break;
-              float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) : 0.0f;
-              x *= p.alpha;
-              if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, coff + j, p.bf16), x);
-              drow[j] = to_cd(x, p.bf16);
-            }
+            const int64_t doff = p.cd_col ? (int64_t)(nb + j) * p.ldd + row : (int64_t)row * p.ldd + nb + j;
+            const int64_t coff = p.cd_col ? (int64_t)(nb + j) * p.ldc + row : (int64_t)row * p.ldc + nb + j;
+            if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, coff, p.bf16), x);
+            reinterpret_cast<uint16_t*>(p.D)[doff] = to_cd(x, p.bf16);
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (lane == 0) bulk_wait_all();  // staging buffers stay valid until the stores are done
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -486,10 +555,19 @@ int num_sms() {
   return v;
 }
 
+// The shared-memory opt-in is set once per device (and so never during a
+// stream capture that replays the launches later).
 template <bool SPARSE>
 cudaError_t set_smem_attr() {
-  // Per device the attribute must be set once; the call is cheap, so it is repeated.
-  return cudaFuncSetAttribute(spmm_tc_kernel<SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<SPARSE>::kSmemBytes);
+  static std::atomic<uint64_t> done_mask{0};
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done_mask.load() & bit) return cudaSuccess;
+  cudaError_t e =
+      cudaFuncSetAttribute(spmm_tc_kernel<SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<SPARSE>::kSmemBytes);
+  if (e == cudaSuccess) done_mask.fetch_or(bit);
+  return e;
 }
 
 long long default_budget() { return 1ll << 32; }  // about two seconds at 2 GHz
@@ -503,7 +581,7 @@ cudaError_t launch_k0(const SpmmLaunch& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-Params base_params(const SpmmLaunch& a, int k_per_stage) {
+Params base_params(const SpmmLaunch& a) {
   const nm_spmm_desc_t& d = a.d;
   Params p{};
   p.M = (int)d.M;
@@ -511,7 +589,7 @@ Params base_params(const SpmmLaunch& a, int k_per_stage) {
   p.K = (int)d.K;
   p.num_m_blk = (int)((d.M + BM - 1) / BM);
   p.num_n_blk = (int)((d.N + BN - 1) / BN);
-  p.num_k_stages = (int)((d.K + k_per_stage - 1) / k_per_stage);
+  p.num_k_stages = (int)((d.K + kKPerStage - 1) / kKPerStage);
   p.bf16 = d.ab_type == NM_BF16;
   p.alpha = a.alpha_f;
   p.beta = a.beta_f;
@@ -520,9 +598,21 @@ Params base_params(const SpmmLaunch& a, int k_per_stage) {
   p.ldc = d.ldc;
   p.ldd = d.ldd;
   p.cd_col = d.order_cd == NM_COL;
+  p.tma_store = a.C == nullptr;
   p.status = a.d_status;
   p.wait_budget = default_budget();
   return p;
+}
+
+// Store map over D in 32 x 32 blocks: column-major D (m contiguous) is
+// staged [n][m] unswizzled; row-major D (n contiguous) is staged [m][n] with
+// the 64-byte swizzle so that each lane's 64-byte row write is bank-conflict free.
+bool make_store_map(CUtensorMap* map, const nm_spmm_desc_t& d, void* D) {
+  if (d.order_cd == NM_COL)
+    return make_map(map, D, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)d.M, (uint64_t)d.N, (uint64_t)(d.ldd * 2), 32, 32,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+  return make_map(map, D, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)d.N, (uint64_t)d.M, (uint64_t)(d.ldd * 2), 32, 32,
+                  CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 }  // namespace tc
@@ -531,26 +621,24 @@ cudaError_t spmm_tc_sparse_impl(const SpmmLaunch& a, cudaStream_t s, int fault_t
   using namespace tc;
   const nm_spmm_desc_t& d = a.d;
   if (d.K == 0) return launch_k0(a, s);
-  Params p = base_params(a, Cfg<true>::kKPerStage);
+  Params p = base_params(a);
   p.fault_test = fault_test;
   if (budget > 0) p.wait_budget = budget;
   const CUtensorMapDataType u16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
-  CUtensorMap mA, mB, mE;
+  CUtensorMap mA, mB, mD;
   const int64_t kc = d.K / 2;  // compressed values per row, packed
-  const int64_t nslots = tc_slots(d.M);
   p.num_k_steps = (int)(d.K / 32);
-  const uint64_t edims[3] = {4, (uint64_t)nslots, (uint64_t)(d.K / 32)};
-  const uint64_t epitch[2] = {16, (uint64_t)(nslots * 16)};
-  const uint32_t ebox[3] = {4, (uint32_t)BM, 4};
-  if (!make_map(&mA, a.A, u16, (uint64_t)kc, (uint64_t)d.M, (uint64_t)(kc * 2), 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  p.meta = static_cast<const uint8_t*>(a.A_meta);
+  p.meta_slots = tc_slots(d.M);
+  if (!make_map(&mA, a.A, u16, (uint64_t)kc, (uint64_t)d.M, (uint64_t)(kc * 2), 32, BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, BN,
                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_3d(&mE, a.A_meta, CU_TENSOR_MAP_DATA_TYPE_UINT32, edims, epitch, ebox))
+      !make_store_map(&mD, d, a.D))
     return cudaErrorInvalidValue;
   if (cudaError_t e = set_smem_attr<true>()) return e;
   const int tiles = p.num_m_blk * p.num_n_blk;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  spmm_tc_kernel<true><<<grid, kThreads, Cfg<true>::kSmemBytes, s>>>(mA, mB, mE, p);
+  spmm_tc_kernel<true><<<grid, kThreads, Cfg<true>::kSmemBytes, s>>>(mA, mB, mA, mD, p);
   return cudaGetLastError();
 }
 
@@ -563,13 +651,13 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int /*split_k*/, cu
   using namespace tc;
   const nm_spmm_desc_t& d = a.d;
   if (d.K == 0) return launch_k0(a, s);
-  Params p = base_params(a, Cfg<false>::kKPerStage);
+  Params p = base_params(a);
   p.a_mn = d.order_a == NM_COL;
   p.b_mn = d.order_b == NM_ROW;
   p.mask = static_cast<const uint32_t*>(a.A_meta);
   p.mask_words = (d.N + 31) / 32;
   const CUtensorMapDataType u16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mD;
   bool ok;
   if (p.a_mn)
     ok = make_map(&mA, a.A, u16, (uint64_t)d.M, (uint64_t)d.K, (uint64_t)(d.lda * 2), 64, 64,
@@ -585,11 +673,12 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int /*split_k*/, cu
       ok = make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  if (ok) ok = make_store_map(&mD, d, a.D);
   if (!ok) return cudaErrorInvalidValue;
   if (cudaError_t e = set_smem_attr<false>()) return e;
   const int tiles = p.num_m_blk * p.num_n_blk;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  spmm_tc_kernel<false><<<grid, kThreads, Cfg<false>::kSmemBytes, s>>>(mA, mB, mA, p);
+  spmm_tc_kernel<false><<<grid, kThreads, Cfg<false>::kSmemBytes, s>>>(mA, mB, mA, mD, p);
   return cudaGetLastError();
 }
 

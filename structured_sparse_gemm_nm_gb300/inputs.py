@@ -41,15 +41,18 @@ BERT_SHAPES = ((1024, 4096, 1024), (4096, 4096, 1024), (1024, 4096, 4096))
 _TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return g
 
 
-def normal(shape, std: float, seed: int, dtype: str = "f16") -> torch.Tensor:
-    """N(0, std) drawn in float32, cast to ``dtype`` (f16, bf16 or f32)."""
-    x = torch.randn(*shape, generator=_gen(seed), dtype=torch.float32) * float(std)
+def normal(shape, std: float, seed: int, dtype: str = "f16", device="cpu") -> torch.Tensor:
+    """N(0, std) drawn in float32, cast to ``dtype`` (f16, bf16 or f32).
+
+    ``device`` selects where the numbers are drawn (large benchmark inputs are
+    drawn on the GPU; CPU and GPU draws of one seed differ)."""
+    x = torch.randn(*shape, generator=_gen(seed, device), dtype=torch.float32, device=device) * float(std)
     return x.to(_TORCH_DT[dtype])
 
 

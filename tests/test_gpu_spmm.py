@@ -48,6 +48,8 @@ SPARSE_CASES = [
     (136, 72, 96, "f16", nb.NM_ROW, 2.0, 0.5, False),      # row-major D, alpha/beta
     (384, 264, 640, "bf16", nb.NM_ROW, -0.5, 1.0, False),
     (128, 128, 32, "f16", nb.NM_COL, 1.0, 0.25, False),    # a single MMA k-step
+    (264, 200, 160, "f16", nb.NM_ROW, 1.5, 0.0, False),    # row-major D through the bulk-store path
+    (96, 40, 32, "bf16", nb.NM_COL, 1.0, 0.0, False),      # one partial tile, one k-step
     (1024, 4096, 1024, "f16", nb.NM_COL, 1.0, 0.0, True),  # BERT-Large shapes
     (4096, 4096, 1024, "f16", nb.NM_COL, 1.0, 0.0, True),
     (1024, 4096, 4096, "f16", nb.NM_COL, 1.0, 0.0, True),
@@ -106,34 +108,38 @@ def test_sparse_backward_uses_transposable_compressed_wt():
 
 
 DENSE_CASES = [
-    # M (out), N (in), K (tokens), dtype, sampled
-    (256, 512, 4096, "f16", False),    # SparseLinear 512 -> 256 weight gradient
-    (104, 200, 96, "bf16", False),     # ragged
-    (136, 72, 1000, "f16", False),     # K not a multiple of the stage
-    (3072, 768, 16384, "bf16", True),  # GPT-neo FC1 dW
-    (768, 3072, 16384, "bf16", True),  # GPT-neo FC2 dW
+    # M (out), N (in), K (tokens), dtype, sampled, alpha, beta
+    (256, 512, 4096, "f16", False, 1.0, 0.0),    # SparseLinear 512 -> 256 weight gradient
+    (104, 200, 96, "bf16", False, 1.0, 0.0),     # ragged
+    (136, 72, 1000, "f16", False, 1.0, 0.0),     # K not a multiple of the stage
+    (136, 72, 1000, "f16", False, 0.5, -1.0),    # gradient accumulation into C
+    (3072, 768, 16384, "bf16", True, 1.0, 0.0),  # GPT-neo FC1 dW
+    (768, 3072, 16384, "bf16", True, 1.0, 0.0),  # GPT-neo FC2 dW
 ]
 
 
-@pytest.mark.parametrize("M,N,K,dtype,sampled", DENSE_CASES)
-def test_masked_weight_grad_matches_oracle(M, N, K, dtype, sampled):
+@pytest.mark.parametrize("M,N,K,dtype,sampled,alpha,beta", DENSE_CASES)
+def test_masked_weight_grad_matches_oracle(M, N, K, dtype, sampled, alpha, beta):
     dY = inputs.normal((K, M), 1.0, inputs.SEED_DY + K, dtype)   # tokens x out
     X = inputs.normal((K, N), 1.0, inputs.SEED_X + K, dtype)     # tokens x in
     W = inputs.normal((M, N), 0.02, inputs.SEED_W, dtype)
     pruned, mask_ref = o.nm_prune(inputs.as_numpy_bits(W), dtype, 2, 4)
     bits = torch.from_numpy(o.mask_to_bits(mask_ref).view(np.int32)).to(DEV)
     dW = torch.empty((M, N), dtype=dY.dtype, device=DEV)
+    C = inputs.normal((M, N), 1.0, inputs.SEED_C, dtype) if beta != 0 else None
     plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, mode=nb.NM_SPMM_DENSE_MASKED, ab_type=dtype, cd_type=dtype,
                                         order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_ROW, lda=M, ldb=N,
-                                        ldd=N, meta_layout=nb.NM_META_CANONICAL))
+                                        ldc=N if C is not None else 0, ldd=N, meta_layout=nb.NM_META_CANONICAL))
     ws_bytes = nb.nm_spmm_plan_workspace(plan)
     ws = dev_bytes(ws_bytes) if ws_bytes else None
-    nb.nm_spmm(plan, 1.0, dY.to(DEV), bits, X.to(DEV), 0.0, None, dW, ws, ws_bytes)
+    nb.nm_spmm(plan, alpha, dY.to(DEV), bits, X.to(DEV), beta, C.to(DEV) if C is not None else None, dW, ws, ws_bytes)
     torch.cuda.synchronize()
     rows = sample_rows(M, 128, seed=K) if sampled else np.arange(M)
     dYm = o.decode(inputs.as_numpy_bits(dY), dtype)
     Xm = o.decode(inputs.as_numpy_bits(X), dtype)
-    ref = o.masked_weight_grad(dYm[:, rows], Xm, mask_ref[rows])
+    ref = alpha * o.masked_weight_grad(dYm[:, rows], Xm, mask_ref[rows])
+    if C is not None:
+        ref = ref + beta * o.decode(inputs.as_numpy_bits(C), dtype)[rows]
     assert_gemm_close(dW.cpu().double().numpy()[rows], ref, f"dW {M}x{N}x{K}")
 
 
