@@ -235,13 +235,16 @@ def time_replays(torch, g, reps: int, barrier=None) -> float:
 
 
 class Flusher:
-    """Writes a buffer larger than L2 between timed launches."""
+    """Evicts L2 between timed launches: writes a buffer larger than L2, then reads
+    it back, so the dirty lines of the write are written back to HBM before the
+    timed launch starts instead of during it."""
 
     def __init__(self, torch, dev, mib=512):
-        self.buf = torch.empty(mib << 20, dtype=torch.uint8, device=dev)
+        self.buf = torch.empty(mib << 19, dtype=torch.int16, device=dev)
 
     def __call__(self):
         self.buf.fill_(1)
+        self.buf.max()
 
 
 def time_launch(torch, fn, flush, reps=10, warm=3):

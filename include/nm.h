@@ -34,12 +34,12 @@
  *   - 2:4 tensor-core metadata (NM_META_TC): the order in which the sparse
  *     tensor core reads metadata for 128-row tiles of 16-bit operands, one
  *     block per k-step of 32 columns.  It is a uint32 array of shape
- *     [cols/32][S][4], S = ceil(rows/128)*128 slot rows of 16 bytes.  Word 0
- *     of slot row 16b + 8h + i in block s holds, in its low 16 bits, the four
- *     codes of row 16b+i for columns 32s+16h .. 32s+16h+15 and, in its high
- *     16 bits, the same codes of row 16b+8+i.  Words 1..3 of every slot row
- *     and the codes of rows past `rows` are 0x4 (positions 0 and 1), so the
- *     tensor core only ever reads valid codes.  Needs cols % 32 == 0.
+ *     [cols/32][S], S = ceil(rows/128)*128 slots.  Word [s][16b + 8h + i]
+ *     holds, in its low 16 bits, the four codes of row 16b+i for columns
+ *     32s+16h .. 32s+16h+15 and, in its high 16 bits, the same codes of row
+ *     16b+8+i.  Codes of rows past `rows` are 0x4 (positions 0 and 1), so the
+ *     tensor core only ever reads valid codes.  Same size as the canonical
+ *     layout (up to the row padding).  Needs cols % 32 == 0.
  *   - N:M metadata for (n, m) != (2, 4): one uint8 position (0..m-1) per kept
  *     value, in the same order as the values (NM_META_CANONICAL only).
  *   - Compressed values: rows x (cols/m*n) elements, packed, kept entries in

@@ -371,26 +371,24 @@ def block_wise_compress(W: np.ndarray, mask: np.ndarray, bh: int = 32, bw: int =
 #   k-step).  Rows are handled in blocks of 16; slot ``16b + 8h + i`` of block
 #   ``b`` holds, in its low half, the four codes of row ``16b + i`` for
 #   columns ``32s + 16h .. 32s + 16h + 15`` and, in its high half, the same
-#   four codes of row ``16b + 8 + i``.  Each k-step's words form their own
-#   block of 16-byte slot rows (the word, then three filler words), so that a
-#   128-row block of one k-step can be copied to tensor memory by itself.
-#   It is the canonical metadata with its 16-bit words permuted and padded.
+#   four codes of row ``16b + 8 + i``.  Words are stored k-step by k-step, so
+#   that the 128 words of one k-step and one tile are contiguous.  It is the
+#   canonical metadata with its 16-bit words permuted, nothing else.
 # --------------------------------------------------------------------------
 def tc_meta_slot_rows(rows: int) -> int:
     """Slot rows: rows rounded up to a multiple of 128 (whole tensor-core tiles)."""
     return ((rows + 127) // 128) * 128
 
 
-# Filler for codes of groups that do not exist (rows past the matrix) and for
-# the three unused words of a slot row: code 0x4 = keep positions 0 and 1.
+# Filler for the codes of rows past the matrix: code 0x4 = keep positions 0 and 1.
 TC_PAD_CODE_WORD = 0x44444444
 
 
 def meta_to_tc_layout(meta: np.ndarray, rows: int, cols: int) -> np.ndarray:
     """Canonical 2:4 metadata (rows x ceil(cols/16) uint16) -> tensor-core order.
 
-    Output: uint32 array of shape (cols/32, tc_meta_slot_rows(rows), 4); entry
-    [s, slot, 0] is the code word, entries [s, slot, 1:] are filler."""
+    Output: uint32 array of shape (cols/32, tc_meta_slot_rows(rows)); codes of
+    rows past ``rows`` are the filler 0x4."""
     if cols % 32:
         raise ValueError("tensor-core metadata needs cols % 32 == 0")
     S = cols // 32
@@ -400,10 +398,7 @@ def meta_to_tc_layout(meta: np.ndarray, rows: int, cols: int) -> np.ndarray:
     canon[:rows] = meta[:, : 2 * S].astype(np.uint32)
     C = canon.reshape(nb, 2, 8, S, 2)  # [block][row half][i][s][h]
     word = C[:, 0] | (C[:, 1] << np.uint32(16))  # [block][i][s][h]
-    slots = word.transpose(2, 0, 3, 1).reshape(S, nslots)  # [s][slot 16b + 8h + i]
-    out = np.full((S, nslots, 4), TC_PAD_CODE_WORD, dtype=np.uint32)
-    out[:, :, 0] = slots
-    return out
+    return word.transpose(2, 0, 3, 1).reshape(S, nslots)  # [s][slot 16b + 8h + i]
 
 
 def meta_from_tc_layout(tc: np.ndarray, rows: int, cols: int) -> np.ndarray:
@@ -411,7 +406,7 @@ def meta_from_tc_layout(tc: np.ndarray, rows: int, cols: int) -> np.ndarray:
     S = cols // 32
     nslots = tc_meta_slot_rows(rows)
     nb = nslots // 16
-    slots = tc.reshape(S, nslots, 4)[:, :, 0].reshape(S, nb, 2, 8)  # [s][block][h][i]
+    slots = tc.reshape(S, nslots).reshape(S, nb, 2, 8)  # [s][block][h][i]
     word = slots.transpose(1, 3, 0, 2)  # [block][i][s][h]
     lo = word & np.uint32(0xFFFF)
     hi = word >> np.uint32(16)
@@ -419,3 +414,30 @@ def meta_from_tc_layout(tc: np.ndarray, rows: int, cols: int) -> np.ndarray:
     out = np.zeros((rows, meta_words_per_row(cols)), dtype=np.uint16)
     out[:, : 2 * S] = canon.astype(np.uint16)
     return out
+
+
+# --------------------------------------------------------------------------
+# compressed (CSR) form of vector-wise and block-wise masks
+#   The kept vectors (blocks) of each row (block row) in ascending column
+#   order: an int32 array of row pointers (rows + 1, or block rows + 1)
+#   followed by one column index per kept vector (vector column c covers
+#   columns v*c .. v*c + v - 1; block column j covers bw*j .. bw*j + bw - 1),
+#   and the kept values in the same order.
+# --------------------------------------------------------------------------
+def vector_wise_csr(W: np.ndarray, mask: np.ndarray, v: int = 32):
+    rows, cols = W.shape
+    kept = mask.reshape(rows, cols // v, v)[:, :, 0]
+    row_ptr = np.concatenate([[0], np.cumsum(kept.sum(axis=1))]).astype(np.int32)
+    r_idx, c_idx = np.nonzero(kept)  # row-major order = ascending within each row
+    vals = W.reshape(rows, cols // v, v)[r_idx, c_idx]
+    return np.concatenate([row_ptr, c_idx.astype(np.int32)]), vals
+
+
+def block_wise_csr(W: np.ndarray, mask: np.ndarray, bh: int = 32, bw: int = 32):
+    rows, cols = W.shape
+    bm, bn = rows // bh, cols // bw
+    kept = mask[::bh, ::bw]
+    row_ptr = np.concatenate([[0], np.cumsum(kept.sum(axis=1))]).astype(np.int32)
+    i_idx, j_idx = np.nonzero(kept)
+    blocks = W.reshape(bm, bh, bn, bw).transpose(0, 2, 1, 3)[i_idx, j_idx]  # kept x bh x bw
+    return np.concatenate([row_ptr, j_idx.astype(np.int32)]), blocks

@@ -38,7 +38,7 @@ nm_status_t check_matrix(const void* p, int64_t rows, int64_t cols, int64_t ld, 
 }
 
 size_t tc_meta_bytes(int64_t rows, int64_t cols) {
-  return (size_t)((cols / 32) * (((rows + 127) / 128) * 128) * 16);
+  return (size_t)((cols / 32) * (((rows + 127) / 128) * 128) * 4);
 }
 
 }  // namespace
@@ -240,7 +240,8 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
       } else {
         if (d.meta_layout != NM_META_CANONICAL) return NM_ERR_UNSUPPORTED;
         if (d.K % 64) return NM_ERR_UNSUPPORTED;
-        return NM_ERR_UNSUPPORTED;  // int8 kernel not built yet
+        if (d.K == 0) return NM_ERR_UNSUPPORTED;
+        kind = 3;
       }
     } else {
       if (d.meta_layout != NM_META_CANONICAL || !fp) return NM_ERR_UNSUPPORTED;

@@ -41,30 +41,18 @@ __device__ __forceinline__ float mag_f32(uint16_t v, int dt) {
   return (f != f) ? __int_as_float(0x7F800000) : f;
 }
 
-// Tensor-core order of 2:4 metadata: for each k-step s (32 columns) a block of
-// `nslots` 16-byte slot rows; word 0 of slot row 16b + 8h + i holds the codes of
-// row 16b+i (low half) and row 16b+8+i (high half) for columns 32s+16h..+15,
-// words 1..3 are filler (code 0x4).  Byte offset of the 16-bit half that holds
-// 16-column segment k of row r:
+// Tensor-core order of 2:4 metadata: for each k-step s (32 columns) `nslots`
+// uint32 words; word s * nslots + (16b + 8h + i) holds the codes of row 16b+i
+// (low half) and row 16b+8+i (high half) for columns 32s+16h .. 32s+16h+15.
+// Byte offset of the 16-bit half that holds 16-column segment k of row r:
 __host__ __device__ __forceinline__ int64_t tc_half_offset(int64_t r, int64_t k, int64_t nslots) {
   const int64_t slot = (r & ~int64_t(15)) + 8 * (k & 1) + (r & 7);
-  return ((k >> 1) * nslots + slot) * 16 + ((r >> 3) & 1) * 2;
+  return ((k >> 1) * nslots + slot) * 4 + ((r >> 3) & 1) * 2;
 }
-constexpr uint32_t kTcFiller = 0x44444444u;
 inline int64_t tc_slots(int64_t rows) { return ((rows + 127) / 128) * 128; }
 
-// Writes segment k of row r into the tensor-core metadata (and the slot row's
-// filler words when this row supplies the low half).
 __device__ __forceinline__ void tc_store(void* meta, int64_t r, int64_t k, int64_t nslots, uint32_t code16) {
-  const int64_t off = tc_half_offset(r, k, nslots);
-  char* base = reinterpret_cast<char*>(meta);
-  *reinterpret_cast<uint16_t*>(base + off) = (uint16_t)code16;
-  if (((r >> 3) & 1) == 0) {
-    uint32_t* f = reinterpret_cast<uint32_t*>(base + off + 4);
-    f[0] = kTcFiller;
-    f[1] = kTcFiller;
-    f[2] = kTcFiller;
-  }
+  *reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(meta) + tc_half_offset(r, k, nslots)) = (uint16_t)code16;
 }
 
 // Grid size for grid-stride loops: enough CTAs to fill 152 SMs several times.

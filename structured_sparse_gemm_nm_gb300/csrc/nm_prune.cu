@@ -12,6 +12,7 @@
 // metadata word), one 16-bit half of a mask word.  For aligned 16-bit data
 // the segment is two 128-bit loads and the eight kept values one 128-bit
 // store.  Other N:M shapes give each thread one group.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "nm_device.cuh"
@@ -227,6 +228,149 @@ __global__ void __launch_bounds__(256) prune_nm_kernel(const typename Elem<DT>::
   }
 }
 
+// n:32 for 16-bit types (apex PR #1631: "Normally we set M = 32"), one thread
+// per group, aligned rows.  The sign-cleared bit patterns of f16/bf16 order
+// exactly like the magnitudes when compared as half/bfloat16 values (for groups
+// without NaN), so the n-th largest key T is found by a 15-step MSB-first
+// search whose counts use packed compares (two elements per instruction).  The
+// kept set is every key > T plus the lowest-position keys == T.  Kept values are
+// gathered through a padded shared-memory copy of the group.  Groups holding a
+// NaN take an exact scalar path (composite keys), so NaN still ranks first.
+template <int DT> struct Pair;
+template <> struct Pair<kF16> {
+  using T2 = __half2;
+  static constexpr uint32_t kInf = 0x7C00u;
+  __device__ __forceinline__ static T2 as(uint32_t w) { return *reinterpret_cast<const __half2*>(&w); }
+  __device__ __forceinline__ static T2 zero() { return __float2half2_rn(0.0f); }
+  __device__ __forceinline__ static int total(T2 a) { return (int)(__low2float(a) + __high2float(a)); }
+};
+template <> struct Pair<kBF16> {
+  using T2 = __nv_bfloat162;
+  static constexpr uint32_t kInf = 0x7F80u;
+  __device__ __forceinline__ static T2 as(uint32_t w) { return *reinterpret_cast<const __nv_bfloat162*>(&w); }
+  __device__ __forceinline__ static T2 zero() { return __float2bfloat162_rn(0.0f); }
+  __device__ __forceinline__ static int total(T2 a) { return (int)(__low2float(a) + __high2float(a)); }
+};
+
+template <int DT, int N>
+__global__ void __launch_bounds__(128) prune32_kernel(const uint16_t* __restrict__ W, int64_t rows, int64_t cols,
+                                                      int64_t ld, uint16_t* W_out, int64_t ld_out,
+                                                      uint32_t* __restrict__ mask_bits, uint16_t* __restrict__ vals,
+                                                      uint8_t* __restrict__ meta) {
+  using P = Pair<DT>;
+  __shared__ uint4 srow4[128][5];  // the thread's group (64 B) at an 80-byte pitch: conflict-free
+  const int64_t gpr = cols / 32;
+  const int64_t total = rows * gpr;
+  uint4* mine = srow4[threadIdx.x];
+  const uint16_t* mine16 = reinterpret_cast<const uint16_t*>(mine);
+  for (int64_t gidx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gidx < total;
+       gidx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = gidx / gpr;
+    const int64_t gi = gidx - r * gpr;
+    const uint4* src = reinterpret_cast<const uint4*>(W + r * ld + gi * 32);
+    uint32_t w[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 q = __ldg(src + c);
+      mine[c] = q;
+      w[4 * c] = q.x;
+      w[4 * c + 1] = q.y;
+      w[4 * c + 2] = q.z;
+      w[4 * c + 3] = q.w;
+    }
+    uint32_t k[16];
+    bool nan = false;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      k[i] = w[i] & 0x7FFF7FFFu;
+      nan |= ((k[i] & 0xFFFFu) > P::kInf) || ((k[i] >> 16) > P::kInf);
+    }
+    uint32_t kept = 0;
+    if (!nan) {
+      uint32_t T = 0;
+#pragma unroll 1
+      for (int b = 14; b >= 0; --b) {
+        const uint32_t cand = T | (1u << b);
+        const typename P::T2 c2 = P::as(cand | (cand << 16));
+        typename P::T2 acc = P::zero();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc = __hadd2(acc, __hge2(P::as(k[i]), c2));
+        if (P::total(acc) >= N) T = cand;
+      }
+      uint32_t gtm = 0, eqm = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t lo = k[i] & 0xFFFFu, hi = k[i] >> 16;
+        gtm |= ((uint32_t)(lo > T) | ((uint32_t)(hi > T) << 1)) << (2 * i);
+        eqm |= ((uint32_t)(lo == T) | ((uint32_t)(hi == T) << 1)) << (2 * i);
+      }
+      kept = gtm;
+      const int need = N - __popc(gtm);
+      for (int j = 0; j < need; ++j) {  // lowest positions among the ties
+        kept |= eqm & (0u - eqm);
+        eqm &= eqm - 1u;
+      }
+    } else {
+      // exact path: composite keys (key << 5 | (31 - position)), NaN above everything
+#pragma unroll 1
+      for (int e = 0; e < 32; ++e) {
+        const uint32_t ke = (min((uint32_t)mine16[e] & 0x7FFFu, P::kInf + 1u) << 5) | (uint32_t)(31 - e);
+        int rank = 0;
+#pragma unroll 1
+        for (int f = 0; f < 32; ++f)
+          rank += ((min((uint32_t)mine16[f] & 0x7FFFu, P::kInf + 1u) << 5) | (uint32_t)(31 - f)) > ke;
+        if (rank < N) kept |= 1u << e;
+      }
+    }
+    // compressed values and positions, ascending position order
+    uint32_t ov[N / 2], oi[N / 4];
+    uint32_t rem = kept;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      const uint32_t pos = (uint32_t)(__ffs(rem) - 1);
+      rem &= rem - 1u;
+      const uint32_t val = mine16[pos];
+      if (j % 2 == 0) ov[j / 2] = val; else ov[j / 2] |= val << 16;
+      if (j % 4 == 0) oi[j / 4] = pos; else oi[j / 4] |= pos << (8 * (j % 4));
+    }
+    if (vals != nullptr) {
+      uint16_t* vo = vals + gidx * N;
+      if constexpr (N == 4) {
+        *reinterpret_cast<uint2*>(vo) = make_uint2(ov[0], ov[1]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < N / 8; ++c)
+          reinterpret_cast<uint4*>(vo)[c] = make_uint4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
+      }
+    }
+    if (meta != nullptr) {
+      uint8_t* mo = meta + gidx * N;
+      if constexpr (N == 4) {
+        *reinterpret_cast<uint32_t*>(mo) = oi[0];
+      } else if constexpr (N == 8) {
+        *reinterpret_cast<uint2*>(mo) = make_uint2(oi[0], oi[1]);
+      } else {
+        *reinterpret_cast<uint4*>(mo) = make_uint4(oi[0], oi[1], oi[2], oi[3]);
+      }
+    }
+    if (mask_bits != nullptr) mask_bits[r * gpr + gi] = kept;
+    if (W_out != nullptr) {
+      uint4* dst = reinterpret_cast<uint4*>(W_out + r * ld_out + gi * 32);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int e = 8 * c + 2 * t;
+          const uint32_t m2 = ((kept >> e) & 1u ? 0x0000FFFFu : 0u) | ((kept >> (e + 1)) & 1u ? 0xFFFF0000u : 0u);
+          o[t] = w[4 * c + t] & m2;
+        }
+        dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+}
+
 // ---- decompression -------------------------------------------------------
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(256) decompress24_kernel(const typename Elem<DT>::T* __restrict__ vals,
@@ -352,7 +496,7 @@ cudaError_t prune_dt(const PruneLaunch& a, cudaStream_t s) {
       // slot rows of rows past the matrix hold the valid code 0x4 (positions 0 and 1)
       const int64_t slots = tc_slots(a.rowsL);
       if (slots != a.rowsL) {
-        cudaError_t e = cudaMemsetAsync(a.meta, 0x44, (size_t)((a.colsL / 32) * slots * 16), s);
+        cudaError_t e = cudaMemsetAsync(a.meta, 0x44, (size_t)((a.colsL / 32) * slots * 4), s);
         if (e != cudaSuccess) return e;
       }
     }
@@ -369,6 +513,25 @@ cudaError_t prune_dt(const PruneLaunch& a, cudaStream_t s) {
       prune24_kernel<DT, false, true><<<grid, threads, 0, s>>>(W, a.rowsL, a.colsL, a.ld, nullptr, 0, nullptr,
                                                                 vals, a.meta, a.meta_tc);
     return cudaGetLastError();
+  }
+  if constexpr (sizeof(T) == 2) {
+    const bool fast = !a.trans && a.m == 32 && (a.n == 4 || a.n == 8 || a.n == 16) && (a.ld % 8) == 0 &&
+                      aligned16(W) && (W_out == nullptr || ((a.ld_out % 8) == 0 && aligned16(W_out))) &&
+                      aligned16(vals) && aligned16(a.meta);
+    if (fast) {
+      const unsigned grid = grid_for(a.rowsL * (a.colsL / 32), 128, 16);
+      const uint16_t* W16 = reinterpret_cast<const uint16_t*>(W);
+      uint16_t* Wo16 = reinterpret_cast<uint16_t*>(W_out);
+      uint16_t* v16 = reinterpret_cast<uint16_t*>(vals);
+      uint8_t* m8 = static_cast<uint8_t*>(a.meta);
+      if (a.n == 4)
+        prune32_kernel<DT, 4><<<grid, 128, 0, s>>>(W16, a.rowsL, a.colsL, a.ld, Wo16, a.ld_out, a.mask_bits, v16, m8);
+      else if (a.n == 8)
+        prune32_kernel<DT, 8><<<grid, 128, 0, s>>>(W16, a.rowsL, a.colsL, a.ld, Wo16, a.ld_out, a.mask_bits, v16, m8);
+      else
+        prune32_kernel<DT, 16><<<grid, 128, 0, s>>>(W16, a.rowsL, a.colsL, a.ld, Wo16, a.ld_out, a.mask_bits, v16, m8);
+      return cudaGetLastError();
+    }
   }
   if (a.mask_bits != nullptr && !a.trans) {
     const size_t bytes = (size_t)a.rowsL * (size_t)((a.colsL + 31) / 32) * 4;

@@ -128,6 +128,175 @@ cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_spmm_i8(const SpmmLaunch&, cudaStream_t) { return cudaErrorNotSupported; }
+// ---------------------------------------------------------------------------
+// 2:4 sparse INT8 product with INT32 accumulation (cuSPARSELt blog, "key
+// features": INT8 inputs, INT32 Tensor Core accumulation).  The tcgen05 MMA
+// has no int8 kind on sm_103a, so this uses the warp-level sparse MMA
+// m16n8k64 (s8 x s8 -> s32) with the canonical metadata: lane 4g+t supplies
+// the 32-bit word of row g + 8*(t&1) covering columns 32*(t>>1) .. +31 of the
+// 64-column k-step, which is exactly two consecutive uint16 words of the
+// canonical layout.
+//
+// CTA tile 128 x 128, 8 warps (4 along M x 2 along N, 32 x 64 each), stages of
+// 128 dense K loaded with cp.async into padded shared memory.
+namespace {
+
+constexpr int I8_BM = 128, I8_BN = 128, I8_BK = 128, I8_STAGES = 3;
+constexpr int I8_APITCH = 80;   // 64 compressed bytes + 16 pad: conflict-free fragment loads
+constexpr int I8_BPITCH = 144;  // 128 bytes + 16 pad
+constexpr int I8_MPITCH = 16;   // 8 uint16 metadata words per row per stage
+constexpr int I8_ABYTES = I8_BM * I8_APITCH, I8_BBYTES = I8_BN * I8_BPITCH, I8_MBYTES = I8_BM * I8_MPITCH;
+constexpr int I8_STAGE_BYTES = I8_ABYTES + I8_BBYTES + I8_MBYTES;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const int8_t* __restrict__ A, const uint16_t* __restrict__ meta,
+                                                      const int8_t* __restrict__ B, const int32_t* __restrict__ C,
+                                                      int32_t* __restrict__ D, int M, int N, int K, int64_t ldb,
+                                                      int64_t ldc, int64_t ldd, int cd_col, int32_t alpha,
+                                                      int32_t beta) {
+  extern __shared__ uint4 smem4[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(smem4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int wm = warp & 3, wn = warp >> 2;
+  const int m0 = blockIdx.y * I8_BM, n0 = blockIdx.x * I8_BN;
+  const int64_t kc = K / 2;         // compressed bytes per A row
+  const int64_t mrow = K / 16;      // uint16 metadata words per row
+  const int kstages = (K + I8_BK - 1) / I8_BK;
+  const int ksteps = K / 64;        // MMA k-steps in K
+
+  auto load_stage = [&](int ks, int buf) {
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem + buf * I8_STAGE_BYTES);
+    // A: 128 rows x 64 bytes = 512 chunks of 16 B
+    for (int c = tid; c < I8_BM * 4; c += 256) {
+      const int r = c >> 2, ch = c & 3;
+      const int64_t kb = (int64_t)ks * 64 + ch * 16;
+      const bool ok = (m0 + r < M) && (kb < kc);
+      cp_async16(base + r * I8_APITCH + ch * 16, ok ? (const void*)(A + (int64_t)(m0 + r) * kc + kb) : (const void*)A, ok);
+    }
+    // B: 128 rows (columns of D) x 128 bytes = 1024 chunks
+    for (int c = tid; c < I8_BN * 8; c += 256) {
+      const int r = c >> 3, ch = c & 7;
+      const int64_t kb = (int64_t)ks * 128 + ch * 16;
+      const bool ok = (n0 + r < N) && (kb < K);
+      cp_async16(base + I8_ABYTES + r * I8_BPITCH + ch * 16,
+                 ok ? (const void*)(B + (int64_t)(n0 + r) * ldb + kb) : (const void*)B, ok);
+    }
+    // metadata: 128 rows x 16 bytes; rows past M (or a K tail) get the valid code 0x4
+    if (tid < I8_BM * 2) {
+      const int r = tid >> 1, h = tid & 1;
+      const int64_t w = (int64_t)ks * 8 + h * 4;
+      const uint32_t dst = base + I8_ABYTES + I8_BBYTES + r * I8_MPITCH + h * 8;
+      if (m0 + r < M && w < mrow) {
+        cp_async8(dst, meta + (int64_t)(m0 + r) * mrow + w);
+      } else {
+        asm volatile("st.shared.v2.u32 [%0], {%1, %1};" ::"r"(dst), "r"(0x44444444u) : "memory");
+      }
+    }
+  };
+
+  int32_t acc[2][8][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[i][j][r] = 0;
+
+  for (int s = 0; s < I8_STAGES - 1; ++s) {
+    if (s < kstages) load_stage(s, s);
+    cp_commit();
+  }
+  for (int ks = 0; ks < kstages; ++ks) {
+    cp_wait<I8_STAGES - 2>();
+    __syncthreads();
+    const int nxt = ks + I8_STAGES - 1;
+    if (nxt < kstages) load_stage(nxt, nxt % I8_STAGES);
+    cp_commit();
+    const uint8_t* sa = smem + (ks % I8_STAGES) * I8_STAGE_BYTES;
+    const uint8_t* sb = sa + I8_ABYTES;
+    const uint8_t* sm = sb + I8_BBYTES;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      if (ks * 2 + kk >= ksteps) break;  // no MMA past K
+      uint32_t bf[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const uint8_t* rowp = sb + (wn * 64 + nt * 8 + g) * I8_BPITCH + kk * 64 + t * 4;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) bf[nt][r] = *reinterpret_cast<const uint32_t*>(rowp + 16 * r);
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int rb = wm * 32 + mt * 16;
+        uint32_t af[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          af[r] = *reinterpret_cast<const uint32_t*>(sa + (rb + g + 8 * (r & 1)) * I8_APITCH + kk * 32 + t * 4 +
+                                                     16 * (r >> 1));
+        const uint32_t e =
+            *reinterpret_cast<const uint32_t*>(sm + (rb + g + 8 * (t & 1)) * I8_MPITCH + kk * 8 + (t >> 1) * 4);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          asm volatile(
+              "mma.sp::ordered_metadata.sync.aligned.m16n8k64.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+              "{%8,%9,%10,%11}, {%0,%1,%2,%3}, %12, 0x0;"
+              : "+r"(acc[mt][nt][0]), "+r"(acc[mt][nt][1]), "+r"(acc[mt][nt][2]), "+r"(acc[mt][nt][3])
+              : "r"(af[0]), "r"(af[1]), "r"(af[2]), "r"(af[3]), "r"(bf[nt][0]), "r"(bf[nt][1]), "r"(bf[nt][2]),
+                "r"(bf[nt][3]), "r"(e));
+        }
+      }
+    }
+  }
+  cp_wait<0>();
+  // epilogue: D = alpha * acc + beta * C in int32 arithmetic modulo 2^32
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = m0 + wm * 32 + mt * 16 + g + 8 * (r >> 1);
+        const int col = n0 + wn * 64 + nt * 8 + 2 * t + (r & 1);
+        if (row >= M || col >= N) continue;
+        uint32_t x = (uint32_t)alpha * (uint32_t)acc[mt][nt][r];
+        if (C != nullptr) x += (uint32_t)beta * (uint32_t)C[cd_col ? (int64_t)col * ldc + row : (int64_t)row * ldc + col];
+        D[cd_col ? (int64_t)col * ldd + row : (int64_t)row * ldd + col] = (int32_t)x;
+      }
+}
+
+}  // namespace
+
+cudaError_t launch_spmm_i8(const SpmmLaunch& a, cudaStream_t s) {
+  const nm_spmm_desc_t& d = a.d;
+  if (d.K == 0) return cudaErrorInvalidValue;  // rejected by the plan
+  const int smem = I8_STAGES * I8_STAGE_BYTES;
+  static std::atomic<uint64_t> done_mask{0};
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(done_mask.load() & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(spmm_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    done_mask.fetch_or(bit);
+  }
+  dim3 grid((unsigned)((d.N + I8_BN - 1) / I8_BN), (unsigned)((d.M + I8_BM - 1) / I8_BM));
+  spmm_i8_kernel<<<grid, 256, smem, s>>>(static_cast<const int8_t*>(a.A), static_cast<const uint16_t*>(a.A_meta),
+                                          static_cast<const int8_t*>(a.B), static_cast<const int32_t*>(a.C),
+                                          static_cast<int32_t*>(a.D), (int)d.M, (int)d.N, (int)d.K, d.ldb, d.ldc,
+                                          d.ldd, d.order_cd == NM_COL, a.alpha_i, a.beta_i);
+  return cudaGetLastError();
+}
 
 }  // namespace nmk

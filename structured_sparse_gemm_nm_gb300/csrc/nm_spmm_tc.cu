@@ -6,17 +6,24 @@
 //                   tcgen05.mma.sp with the metadata in tensor memory.
 //  * DENSE_MASKED:  A and B dense, D = alpha * (mask .* (A B)) + beta * C, the
 //                   weight gradient of a layer whose weight keeps a fixed
-//                   sparsity pattern.  Issued as dense tcgen05.mma.
+//                   sparsity pattern.  Issued as dense tcgen05.mma; K may be
+//                   split across CTAs (fp32 partials in the workspace, summed
+//                   by a finalize kernel) when the output has few tiles.
 //
-// One persistent CTA per SM walks output tiles of 128 x 128.  Warp roles:
-//   warp 0      TMA producer: fills a ring of shared-memory stages of 64
-//               dense K (A, B and, for SPARSE, the metadata of two k-steps)
-//   warp 1      owns tensor memory; one lane issues tcgen05.cp (metadata
-//               into TMEM) and tcgen05.mma, committing to mbarriers
-//   warps 2..5  epilogue: tcgen05.ld the FP32 accumulator, alpha, mask,
-//               convert, stage 32 x 32 blocks in shared memory and write them
-//               with TMA bulk stores; the accumulator is double buffered so
-//               the epilogue of one tile overlaps the main loop of the next.
+// A persistent CTA per SM computes 128 x 256 output tiles.  Two CTAs of a
+// cluster work on neighbouring 128-row blocks of the same 256-column block:
+// each fetches half of the shared B tile and multicasts it to both, which
+// halves the L2 traffic of B.  Warp roles per CTA:
+//   warp 0       TMA producer: A and (its half of) B for stages of 64 dense K
+//   warp 1       owns tensor memory; one lane issues tcgen05.mma
+//   warps 2..5   SPARSE metadata: each warp loads one 32-bit code word per
+//                lane (row slot) and k-step from global memory and writes it
+//                with tcgen05.st into one of four 64-column-aligned TMEM
+//                slots (the sparse MMA accepts its metadata only there); this
+//                keeps metadata movement out of the tensor pipe
+//   warps 6..13  epilogue: drain the FP32 accumulator (alpha, mask) into
+//                packed registers, release it, then stage 32 x 32 blocks in
+//                shared memory and write them with TMA bulk stores
 // Every mbarrier wait is bounded; a wait that gives up sets an abort flag
 // and NM_ERR_TIMEOUT in the caller's status word, the roles drain their
 // outstanding asynchronous work and the CTA frees its tensor memory.
@@ -35,52 +42,49 @@ namespace nmk {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
+constexpr int BN = 256;
+constexpr int kKPerStage = 64;  // dense-equivalent K per stage
+constexpr int kMetaWarp0 = 2, kMetaWarps = 4;
+constexpr int kEpiWarp0 = 6, kEpiWarps = 8;
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = 2 * BN;  // two accumulator buffers
-// The metadata of one MMA k-step (32 dense K) occupies one TMEM column; the
-// sparse MMA accepts it only at a 64-aligned column, so k-steps rotate
-// through the four columns 256, 320, 384 and 448, each filled by its own
-// tcgen05.cp of 128 lanes x 128 bits (the other three columns of a copy are
-// filler).
-constexpr int kMetaCol = kAccCols;
-constexpr int kMetaColStride = 64;
-constexpr int kMetaSlots = 4;
-constexpr int kMetaStepBytes = BM * 16;  // one k-step: 128 slot rows x 16 B
-constexpr int kKPerStage = 64;           // dense-equivalent K per stage
-constexpr int kBTileBytes = BN * 128;    // BN rows x 64 elements (128B swizzle)
+constexpr int kMetaCol = 256, kMetaColStride = 64, kMetaSlots = 4;
 constexpr int kEpiBufBytes = 32 * 32 * 2;  // one 32 x 32 output block
 
 template <bool SPARSE>
 struct Cfg {
-  // SPARSE: A = 128 rows x 32 compressed values (64B swizzle); DENSE: 128 x 64 (128B swizzle).
+  // SPARSE A: 128 rows x 32 compressed values (64B swizzle); dense A: 128 x 64 (128B swizzle).
   static constexpr int kATileBytes = SPARSE ? BM * 64 : BM * 128;
-  static constexpr int kMetaBytes = SPARSE ? 2 * kMetaStepBytes : 0;
-  static constexpr int kStageBytes = kATileBytes + kBTileBytes + kMetaBytes;
-  static constexpr int kStages = SPARSE ? 7 : 6;
+  static constexpr int kBTileBytes = BN * 128;  // 256 rows x 64 elements (128B swizzle)
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kStages = SPARSE ? 5 : 4;
+  static constexpr int kAcc = SPARSE ? 1 : 2;  // 256-column accumulator buffers
   static constexpr int kEpiOffset = kStages * kStageBytes;
-  static constexpr int kBarOffset = kEpiOffset + kEpiWarps * 2 * kEpiBufBytes;
-  static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
+  static constexpr int kBarOffset = kEpiOffset + kEpiWarps * kEpiBufBytes;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + 512;
 };
 
 struct Params {
   int M, N, K;
-  int num_m_blk, num_n_blk, num_k_stages;
-  int num_k_steps;  // SPARSE: K / 32 MMA k-steps
-  const uint8_t* meta;  // SPARSE: tensor-core metadata, [k-step][meta_slots][16 B]
+  int num_m_blk, num_n_blk;
+  int k_stages;          // stages over the whole K
+  int split_k;           // DENSE: number of K splits (1 = direct epilogue)
+  int stages_per_split;
+  int num_units;         // (pair-)tiles x splits
+  int num_k_steps;       // SPARSE: K / 32
+  const uint32_t* meta;  // SPARSE: tensor-core metadata [K/32][meta_slots]
   int64_t meta_slots;
-  int a_mn, b_mn;   // DENSE_MASKED operand majors (1 = M/N contiguous)
-  int bf16;         // element type: 0 f16, 1 bf16
+  int a_mn, b_mn;        // DENSE operand majors (1 = M/N contiguous)
+  int bf16;
   float alpha, beta;
   const void* C;
   void* D;
   int64_t ldc, ldd;
-  int cd_col;       // 1: D[n * ldd + m]; 0: D[m * ldd + n]
-  int tma_store;    // 1: D written by TMA bulk stores (C not read)
+  int cd_col;     // 1: D[n * ldd + m]; 0: D[m * ldd + n]
+  int tma_store;  // 1: D written by TMA bulk stores (C not read)
   const uint32_t* mask;
   int64_t mask_words;
+  float* partial;  // DENSE split-K: [split][M][N]
   int32_t* status;
   long long wait_budget;  // cycles
   int fault_test;         // 1: the MMA lane waits on a barrier nothing arrives at
@@ -107,16 +111,6 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// try_wait with a suspend-time hint (ns): the thread may sleep until the phase completes.
-__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(20000u)
-      : "memory");
-  return ok != 0;
-}
 
 // Bounded wait: false if the budget ran out (then the status word and the
 // CTA's abort flag are set) or another role already aborted.
@@ -125,7 +119,7 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_sleep(bar, parity)) return true;
+    if (mbar_try(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > budget) {
       *abort_flag = 1;
@@ -135,13 +129,6 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   }
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
-          "r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -149,11 +136,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-// Plain bulk copy of `bytes` contiguous bytes (16-byte aligned, multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
+// The same box lands at the same offset in the shared memory of every CTA in
+// `mask`, each completing bytes on its own barrier at offset `bar`.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
 }
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
@@ -161,12 +152,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until at most N committed bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
 
 // Shared-memory matrix descriptor (tcgen05): start, leading/stride byte
 // offsets (16-byte units), fixed version bit 46, swizzle mode in bits 61..63.
@@ -174,9 +170,9 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swizzle << 61);
 }
-constexpr uint32_t kSwizzle128 = 2, kSwizzle64 = 4, kSwizzleNone = 0;
+constexpr uint32_t kSwizzle128 = 2, kSwizzle64 = 4;
 
-// Instruction descriptor for kind::f16: D = F32, A/B = F16 or BF16.
+// Instruction descriptor for kind::f16: D = F32, A/B = F16 or BF16, M = 128, N = 256.
 __device__ __forceinline__ uint32_t idesc_f16(int bf16, int a_mn, int b_mn, bool sparse) {
   uint32_t d = (1u << 4) | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10) | ((uint32_t)a_mn << 15) |
                ((uint32_t)b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
@@ -200,6 +196,13 @@ __device__ __forceinline__ void mma_sparse(uint32_t tmem_d, uint64_t a, uint64_t
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+// Arrives on the barrier at the same offset in every CTA of `mask` once the prior MMAs complete.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -214,6 +217,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ float load_cd(const void* base, int64_t off, int bf16) {
   const uint16_t b = reinterpret_cast<const uint16_t*>(base)[off];
@@ -226,34 +232,58 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
   return (uint32_t)to_cd(lo, bf16) | ((uint32_t)to_cd(hi, bf16) << 16);
 }
 
+// Work unit u -> 128-row block, 256-column block and K split.  In a cluster
+// of two, CTA rank r takes row block 2 * (pair index) + r.
+struct Unit {
+  int m0, n0, kbeg, kend, split;
+};
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u, int cl, int rank) {
+  Unit t;
+  const int mcount = p.num_m_blk / cl;
+  const int mi = u % mcount;
+  const int rest = u / mcount;
+  t.n0 = (rest % p.num_n_blk) * BN;
+  t.split = rest / p.num_n_blk;
+  t.m0 = (mi * cl + rank) * BM;
+  t.kbeg = t.split * p.stages_per_split;
+  t.kend = min(p.k_stages, t.kbeg + p.stages_per_split);
+  return t;
+}
+
 // ----------------------------------------------------------------- kernel
-template <bool SPARSE>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool SPARSE, int CL>
+__global__ void __maxnreg__(144)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmD, const Params p) {
+                   const __grid_constant__ CUtensorMap tmD, const Params p) {
   using C = Cfg<SPARSE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  // bars: full[S], empty[S], tfull[2], tempty[2], mfull[4], mfree[4], drain
   const uint32_t bar_full = smem_u32(bars), bar_empty = smem_u32(bars + C::kStages);
-  const uint32_t bar_tfull = smem_u32(bars + 2 * C::kStages), bar_tempty = smem_u32(bars + 2 * C::kStages + 2);
-  const uint32_t bar_drain = smem_u32(bars + 2 * C::kStages + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5);
+  const uint32_t bar_tfull = smem_u32(bars + 2 * C::kStages), bar_tempty = bar_tfull + 16;
+  const uint32_t bar_mfull = bar_tempty + 16, bar_mfree = bar_mfull + 8 * kMetaSlots;
+  const uint32_t bar_drain = bar_mfree + 8 * kMetaSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5 + 2 * kMetaSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = p.num_m_blk * p.num_n_blk;
+  const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
+  const int cluster_id = blockIdx.x / CL, num_clusters = gridDim.x / CL;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, CL);  // released by the MMA of every CTA that reads the stage
     }
-    mbar_init(bar_tfull, 1);
-    mbar_init(bar_tfull + 8, 1);
-    mbar_init(bar_tempty, kEpiWarps);
-    mbar_init(bar_tempty + 8, kEpiWarps);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, kEpiWarps);
+    }
+    for (int s = 0; s < kMetaSlots; ++s) {
+      mbar_init(bar_mfull + 8 * s, kMetaWarps);
+      mbar_init(bar_mfree + 8 * s, 1);
+    }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -265,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -277,9 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;  // per-stage bits for the drain at the end
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m0 = (tile % p.num_m_blk) * BM, n0 = (tile / p.num_m_blk) * BN;
-        for (int ks = 0; ks < p.num_k_stages; ++ks) {
+      for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+        const Unit t = decode_unit(p, u, CL, rank);
+        for (int ks = t.kbeg; ks < t.kend; ++ks) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_budget, p.status)) {
             ok = false;
             break;
@@ -287,29 +318,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = bar_full + 8 * stage;
           const uint32_t sA = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t sB = sA + C::kATileBytes;
+          mbar_expect_tx(fb, C::kStageBytes);
           if constexpr (SPARSE) {
-            // the 128 slot rows of one k-step are 2 KB of contiguous memory: one bulk copy each
-            const int steps = min(2, p.num_k_steps - 2 * ks);
-            mbar_expect_tx(fb, C::kATileBytes + kBTileBytes + steps * kMetaStepBytes);
-            tma_load_2d(sA, &tmA, fb, ks * 32, m0);
-            tma_load_2d(sB, &tmB, fb, ks * 64, n0);
-            for (int j = 0; j < steps; ++j)
-              bulk_load(sB + kBTileBytes + j * kMetaStepBytes,
-                        p.meta + ((int64_t)(2 * ks + j) * p.meta_slots + m0) * 16, kMetaStepBytes, fb);
+            tma_load_2d(sA, &tmA, fb, ks * 32, t.m0);
+          } else if (p.a_mn) {
+            tma_load_2d(sA, &tmA, fb, t.m0, ks * 64);
+            tma_load_2d(sA + C::kATileBytes / 2, &tmA, fb, t.m0 + 64, ks * 64);
           } else {
-            mbar_expect_tx(fb, C::kStageBytes);
-            if (p.a_mn) {
-              tma_load_2d(sA, &tmA, fb, m0, ks * 64);
-              tma_load_2d(sA + C::kATileBytes / 2, &tmA, fb, m0 + 64, ks * 64);
-            } else {
-              tma_load_2d(sA, &tmA, fb, ks * 64, m0);
+            tma_load_2d(sA, &tmA, fb, ks * 64, t.m0);
+          }
+          // B: this CTA fetches 256 / CL rows (columns of D) and, in a cluster, multicasts them
+          const int nb = t.n0 + (BN / CL) * (int)rank;
+          const uint32_t sBh = sB + (C::kBTileBytes / CL) * rank;
+          if (!SPARSE && p.b_mn) {
+#pragma unroll
+            for (int h = 0; h < 4 / CL; ++h) {
+              if (CL > 1)
+                tma_load_2d_mc(sBh + 8192 * h, &tmB, fb, nb + 64 * h, ks * 64, (uint16_t)((1u << CL) - 1));
+              else
+                tma_load_2d(sBh + 8192 * h, &tmB, fb, nb + 64 * h, ks * 64);
             }
-            if (p.b_mn) {
-              tma_load_2d(sB, &tmB, fb, n0, ks * 64);
-              tma_load_2d(sB + kBTileBytes / 2, &tmB, fb, n0 + 64, ks * 64);
-            } else {
-              tma_load_2d(sB, &tmB, fb, ks * 64, n0);
-            }
+          } else {
+            if (CL > 1)
+              tma_load_2d_mc(sBh, &tmB, fb, ks * 64, nb, (uint16_t)((1u << CL) - 1));
+            else
+              tma_load_2d(sBh, &tmB, fb, ks * 64, nb);
           }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -319,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Drain: every issued copy must have landed before the CTA may exit.
+      // Drain: every copy into this CTA must have landed before the CTA may exit.
       for (int s = 0; s < C::kStages; ++s)
         if ((issued >> s) & 1u) {
           const uint32_t par = (last_parity >> s) & 1u;
@@ -336,14 +369,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      uint32_t meta_slot = 0;  // running k-step count modulo the slot ring
+      int mslot = 0;
+      uint32_t mphase = 0;
       bool ok = true;
       if (p.fault_test) ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);  // nothing arrives: runs out
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+        const Unit t = decode_unit(p, u, CL, rank);
         if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag, p.wait_budget, p.status)) break;
         tc_fence_after();
         const uint32_t tacc = tmem + acc * BN;
-        for (int ks = 0; ks < p.num_k_stages; ++ks) {
+        int kstep = 0;  // MMA k-steps issued for this tile
+        for (int ks = t.kbeg; ks < t.kend; ++ks) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
             ok = false;
             break;
@@ -354,28 +390,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (SPARSE) {
             const int steps = min(2, p.num_k_steps - 2 * ks);  // no MMA past K
             for (int j = 0; j < steps; ++j) {
-              const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * meta_slot;
-              meta_slot = (meta_slot + 1) & (kMetaSlots - 1);
-              // k-step j: 128 slot rows x 16 B, rows contiguous (8-row core matrices 128 B apart)
-              const uint64_t md = sdesc(sB + kBTileBytes + j * kMetaStepBytes, 16, 128, kSwizzleNone);
-              asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(tmeta), "l"(md));
+              if (!mbar_wait(bar_mfull + 8 * mslot, mphase, abort_flag, p.wait_budget, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
               // A: 128 rows x 64 B (64B swizzle, 8-row groups 512 B apart), 16 values = 32 B per k-step
               const uint64_t ad = sdesc(sA + 32 * j, 16, 512, kSwizzle64);
-              // B: BN rows x 128 B (128B swizzle), 32 values = 64 B per k-step
+              // B: 256 rows x 128 B (128B swizzle), 32 values = 64 B per k-step
               const uint64_t bd = sdesc(sB + 64 * j, 16, 1024, kSwizzle128);
-              mma_sparse(tacc, ad, bd, tmeta, idesc, (ks > 0 || j > 0) ? 1u : 0u);
+              mma_sparse(tacc, ad, bd, tmem + kMetaCol + kMetaColStride * mslot, idesc, kstep > 0 ? 1u : 0u);
+              tc_commit(bar_mfree + 8 * mslot);  // the metadata slot is free once this MMA is done
+              ++kstep;
+              if (++mslot == kMetaSlots) {
+                mslot = 0;
+                mphase ^= 1;
+              }
             }
+            if (!ok) break;
           } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint64_t ad = p.a_mn ? sdesc(sA + 2048 * j, C::kATileBytes / 2, 1024, kSwizzle128)
                                          : sdesc(sA + 32 * j, 16, 1024, kSwizzle128);
-              const uint64_t bd = p.b_mn ? sdesc(sB + 2048 * j, kBTileBytes / 2, 1024, kSwizzle128)
+              const uint64_t bd = p.b_mn ? sdesc(sB + 2048 * j, 8192, 1024, kSwizzle128)
                                          : sdesc(sB + 32 * j, 16, 1024, kSwizzle128);
-              mma_dense(tacc, ad, bd, idesc, (ks > 0 || j > 0) ? 1u : 0u);
+              mma_dense(tacc, ad, bd, idesc, (kstep > 0 || j > 0) ? 1u : 0u);
             }
+            ++kstep;
           }
-          tc_commit(bar_empty + 8 * stage);
+          if (CL > 1)
+            tc_commit_mc(bar_empty + 8 * stage, (uint16_t)((1u << CL) - 1));
+          else
+            tc_commit(bar_empty + 8 * stage);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
@@ -383,8 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc_commit(bar_tfull + 8 * acc);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if (++acc == C::kAcc) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
       // Drain: all issued tensor-core work completes before TMEM is freed.
       tc_commit(bar_drain);
@@ -392,66 +441,138 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (!mbar_try(bar_drain, 0u) && clock64() - t0 < p.wait_budget) {
       }
     }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------- SPARSE metadata
+    if constexpr (SPARSE) {
+      const int q = warp & 3;  // TMEM lane quarter this warp may access
+      int mslot = 0;
+      uint32_t mphase = 0;
+      bool ok = true;
+      for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+        const Unit t = decode_unit(p, u, CL, rank);
+        const uint32_t* src = p.meta + t.m0 + 32 * q + lane;
+        const int S = p.num_k_steps;
+        // code words of four k-steps are loaded one batch ahead of their use
+        uint32_t nxt[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) nxt[i] = i < S ? __ldg(src + (int64_t)i * p.meta_slots) : 0u;
+        for (int s0 = 0; ok && s0 < S; s0 += 4) {
+          uint32_t cur[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            nxt[i] = (s0 + 4 + i < S) ? __ldg(src + (int64_t)(s0 + 4 + i) * p.meta_slots) : 0u;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (s0 + i >= S) break;
+            if (!mbar_wait(bar_mfree + 8 * mslot, mphase ^ 1, abort_flag, p.wait_budget, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            tmem_st1(tmem + ((uint32_t)(32 * q) << 16) + kMetaCol + kMetaColStride * mslot, cur[i]);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_mfull + 8 * mslot);
+            if (++mslot == kMetaSlots) {
+              mslot = 0;
+              mphase ^= 1;
+            }
+          }
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int ew = warp - 2;
-    uint8_t* ebuf = smem + C::kEpiOffset + ew * 2 * kEpiBufBytes;
+    const int ew = warp - kEpiWarp0;
+    const int q = warp & 3;   // TMEM lane quarter this warp may access
+    const int half = ew / 4;  // which 128 of the 256 columns
+    uint8_t* buf = smem + C::kEpiOffset + ew * kEpiBufBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
-    int nbuf = 0;  // stores issued by this warp (selects the staging buffer)
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    bool stored = false;
+    for (int u = cluster_id; u < p.num_units; u += num_clusters) {
+      const Unit t = decode_unit(p, u, CL, rank);
       if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.wait_budget, p.status)) break;
       tc_fence_after();
-      const int m0 = (tile % p.num_m_blk) * BM, n0 = (tile / p.num_m_blk) * BN;
-      const int mq = m0 + 32 * q;
+      const int mq = t.m0 + 32 * q;
       const int row = mq + lane;
       const bool row_ok = row < p.M;
-#pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        __syncwarp();  // tcgen05.ld is warp-collective: reconverge after any per-lane skip
+      const int ncol0 = t.n0 + 128 * half;
+      uint32_t pk[4][16];
+      // drain this warp's 32 x 128 block of the accumulator into packed registers
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * BN + ch * 32, v);
-        if (ch == BN / 32 - 1) {
-          // the accumulator buffer is drained: the next tile's MMAs may reuse it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
-        }
-        const int nb = n0 + ch * 32;
-        if (mq >= p.M || nb >= p.N) continue;
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * BN + 128 * half + 32 * c, v);
+        const int nb = ncol0 + 32 * c;
         uint32_t mword = 0xFFFFFFFFu;
-        if (!SPARSE && p.mask != nullptr && row_ok) mword = p.mask[(int64_t)row * p.mask_words + nb / 32];
-        if (p.tma_store) {
-          uint8_t* buf = ebuf + (nbuf & 1) * kEpiBufBytes;
-          if (nbuf >= 2) {
-            if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+        if (!SPARSE && p.mask != nullptr && row_ok && nb < p.N) mword = p.mask[(int64_t)row * p.mask_words + nb / 32];
+        if (p.split_k > 1) {
+          // fp32 partial of this K split, row-major [split][M][N]
+          if (row_ok && nb < p.N) {
+            float* dst = p.partial + ((int64_t)t.split * p.M + row) * p.N + nb;
+            const int cnt = min(32, p.N - nb);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j >= cnt) break;
+              dst[j] = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
+            }
+          }
+        } else if (p.tma_store) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float x0 = ((mword >> (2 * j)) & 1u) ? __uint_as_float(v[2 * j]) * p.alpha : 0.0f;
+            const float x1 = ((mword >> (2 * j + 1)) & 1u) ? __uint_as_float(v[2 * j + 1]) * p.alpha : 0.0f;
+            pk[c][j] = pack2(x0, x1, p.bf16);
+          }
+        } else if (row_ok && nb < p.N) {
+          const int cnt = min(32, p.N - nb);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j >= cnt) break;
+            float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
+            const int64_t doff = p.cd_col ? (int64_t)(nb + j) * p.ldd + row : (int64_t)row * p.ldd + nb + j;
+            const int64_t coff = p.cd_col ? (int64_t)(nb + j) * p.ldc + row : (int64_t)row * p.ldc + nb + j;
+            if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, coff, p.bf16), x);
+            reinterpret_cast<uint16_t*>(p.D)[doff] = to_cd(x, p.bf16);
+          }
+        }
+      }
+      // the accumulator buffer is drained: the next tile's MMAs may reuse it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+      if (++acc == C::kAcc) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+      if (p.split_k == 1 && p.tma_store && mq < p.M) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int nb = ncol0 + 32 * c;
+          if (nb >= p.N) break;
+          if (stored) {
+            if (lane == 0) bulk_wait_read0();  // the previous store has read the staging block
             __syncwarp();
           }
           if (p.cd_col) {
             // block [32 n][32 m], 64-byte rows: element (n, m) at (n * 32 + m) * 2
             uint16_t* b16 = reinterpret_cast<uint16_t*>(buf);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
-              b16[j * 32 + lane] = to_cd(x, p.bf16);
+            for (int j = 0; j < 16; ++j) {
+              b16[(2 * j) * 32 + lane] = (uint16_t)(pk[c][j] & 0xFFFFu);
+              b16[(2 * j + 1) * 32 + lane] = (uint16_t)(pk[c][j] >> 16);
             }
           } else {
-            // block [32 m][32 n], 64-byte rows in the 64B-swizzled order the store map expects:
-            // 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
+            // block [32 m][32 n], 64-byte rows in the 64B-swizzled order of the store map:
+            // 16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)
             uint4* b4 = reinterpret_cast<uint4*>(buf + lane * 64);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t w[4];
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const int j = 8 * c + 2 * t;
-                const float x0 = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
-                const float x1 = ((mword >> (j + 1)) & 1u) ? __uint_as_float(v[j + 1]) * p.alpha : 0.0f;
-                w[t] = pack2(x0, x1, p.bf16);
-              }
-              b4[c ^ ((lane >> 1) & 3)] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+            for (int k = 0; k < 4; ++k)
+              b4[k ^ ((lane >> 1) & 3)] = make_uint4(pk[c][4 * k], pk[c][4 * k + 1], pk[c][4 * k + 2], pk[c][4 * k + 3]);
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
@@ -462,32 +583,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_store_2d(&tmD, smem_u32(buf), nb, mq);
             bulk_commit();
           }
-          ++nbuf;
-        } else {
-          if (!row_ok) continue;
-          const int cnt = min(32, p.N - nb);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j >= cnt) break;
-            float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) : 0.0f;
-            x *= p.alpha;
-            const int64_t doff = p.cd_col ? (int64_t)(nb + j) * p.ldd + row : (int64_t)row * p.ldd + nb + j;
-            const int64_t coff = p.cd_col ? (int64_t)(nb + j) * p.ldc + row : (int64_t)row * p.ldc + nb + j;
-            if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, coff, p.bf16), x);
-            reinterpret_cast<uint16_t*>(p.D)[doff] = to_cd(x, p.bf16);
-          }
+          stored = true;
         }
       }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
     }
-    if (lane == 0) bulk_wait_all();  // staging buffers stay valid until the stores are done
+    if (lane == 0) bulk_wait_all();  // staging blocks stay valid until the stores are done
     __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  if (CL > 1) cluster_sync();  // no CTA leaves while its peer may still signal it
 }
 
 // D = beta * C (or 0) when K == 0: no product to accumulate.
@@ -498,6 +605,22 @@ __global__ void scale_c_kernel(const uint16_t* C, uint16_t* D, int64_t rows, int
     const int64_t r = i / cols, c = i - r * cols;
     const float x = C != nullptr ? beta * load_cd(C, r * ldc + c, bf16) : 0.0f;
     D[r * ldd + c] = to_cd(x, bf16);
+  }
+}
+
+// Sum of the K splits' fp32 partials (alpha and mask already applied), plus
+// beta * C, converted to D.
+__global__ void finalize_split_kernel(const float* __restrict__ part, int splits, int64_t M, int64_t N,
+                                      const uint16_t* __restrict__ C, uint16_t* __restrict__ D, int64_t ldc,
+                                      int64_t ldd, int cd_col, float beta, int bf16) {
+  const int64_t total = M * N;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / N, n = i - m * N;
+    float x = 0.0f;
+    for (int s = 0; s < splits; ++s) x += part[(int64_t)s * total + i];
+    const int64_t doff = cd_col ? n * ldd + m : m * ldd + n;
+    if (C != nullptr) x = fmaf(beta, load_cd(C, cd_col ? n * ldc + m : m * ldc + n, bf16), x);
+    D[doff] = to_cd(x, bf16);
   }
 }
 
@@ -529,19 +652,6 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_map_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, const uint64_t dims[3],
-                 const uint64_t pitches[2], const uint32_t box[3]) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
-  cuuint64_t st[2] = {pitches[0], pitches[1]};
-  cuuint32_t b[3] = {box[0], box[1], box[2]};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, dt, 3, const_cast<void*>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int num_sms() {
   static std::atomic<int> cached{0};
   int v = cached.load();
@@ -557,15 +667,15 @@ int num_sms() {
 
 // The shared-memory opt-in is set once per device (and so never during a
 // stream capture that replays the launches later).
-template <bool SPARSE>
+template <bool SPARSE, int CL>
 cudaError_t set_smem_attr() {
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (done_mask.load() & bit) return cudaSuccess;
-  cudaError_t e =
-      cudaFuncSetAttribute(spmm_tc_kernel<SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<SPARSE>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(spmm_tc_kernel<SPARSE, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<SPARSE>::kSmemBytes);
   if (e == cudaSuccess) done_mask.fetch_or(bit);
   return e;
 }
@@ -589,7 +699,9 @@ Params base_params(const SpmmLaunch& a) {
   p.K = (int)d.K;
   p.num_m_blk = (int)((d.M + BM - 1) / BM);
   p.num_n_blk = (int)((d.N + BN - 1) / BN);
-  p.num_k_stages = (int)((d.K + kKPerStage - 1) / kKPerStage);
+  p.k_stages = (int)((d.K + kKPerStage - 1) / kKPerStage);
+  p.split_k = 1;
+  p.stages_per_split = p.k_stages;
   p.bf16 = d.ab_type == NM_BF16;
   p.alpha = a.alpha_f;
   p.beta = a.beta_f;
@@ -615,6 +727,42 @@ bool make_store_map(CUtensorMap* map, const nm_spmm_desc_t& d, void* D) {
                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+template <bool SPARSE, int CL>
+cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mD, Params p,
+                          cudaStream_t s) {
+  if (cudaError_t e = set_smem_attr<SPARSE, CL>()) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<SPARSE>::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CL > 1 ? 1 : 0;
+  // persistent grid: as many clusters as can be resident at once (queried once per device)
+  static std::atomic<int> resident{0};
+  int max_clusters = resident.load();
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3((unsigned)(num_sms() / CL * CL));
+    int n = 0;
+    if (CL > 1) {
+      if (cudaOccupancyMaxActiveClusters(&n, spmm_tc_kernel<SPARSE, CL>, &cfg) != cudaSuccess) n = 0;
+      cudaGetLastError();
+    }
+    max_clusters = n > 0 ? n : num_sms() / CL;
+    resident.store(max_clusters);
+  }
+  const int clusters = p.num_units < max_clusters ? p.num_units : max_clusters;
+  cfg.gridDim = dim3((unsigned)(clusters * CL));
+  return cudaLaunchKernelEx(&cfg, spmm_tc_kernel<SPARSE, CL>, mA, mB, mD, p);
+}
+
+// Pairs of CTAs share the B tile when the row blocks come in pairs.
+int cluster_for(int num_m_blk) { return (num_m_blk % 2 == 0) ? 2 : 1; }
+
 }  // namespace tc
 
 cudaError_t spmm_tc_sparse_impl(const SpmmLaunch& a, cudaStream_t s, int fault_test, long long budget) {
@@ -624,30 +772,51 @@ cudaError_t spmm_tc_sparse_impl(const SpmmLaunch& a, cudaStream_t s, int fault_t
   Params p = base_params(a);
   p.fault_test = fault_test;
   if (budget > 0) p.wait_budget = budget;
+  const int cl = cluster_for(p.num_m_blk);
+  p.num_units = (p.num_m_blk / cl) * p.num_n_blk;
+  p.num_k_steps = (int)(d.K / 32);
+  p.meta = static_cast<const uint32_t*>(a.A_meta);
+  p.meta_slots = tc_slots(d.M);
   const CUtensorMapDataType u16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
   CUtensorMap mA, mB, mD;
   const int64_t kc = d.K / 2;  // compressed values per row, packed
-  p.num_k_steps = (int)(d.K / 32);
-  p.meta = static_cast<const uint8_t*>(a.A_meta);
-  p.meta_slots = tc_slots(d.M);
   if (!make_map(&mA, a.A, u16, (uint64_t)kc, (uint64_t)d.M, (uint64_t)(kc * 2), 32, BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, BN,
+      !make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, (uint32_t)(BN / cl),
                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_store_map(&mD, d, a.D))
     return cudaErrorInvalidValue;
-  if (cudaError_t e = set_smem_attr<true>()) return e;
-  const int tiles = p.num_m_blk * p.num_n_blk;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  spmm_tc_kernel<true><<<grid, kThreads, Cfg<true>::kSmemBytes, s>>>(mA, mB, mA, mD, p);
-  return cudaGetLastError();
+  return cl == 2 ? launch_kernel<true, 2>(mA, mB, mD, p, s) : launch_kernel<true, 1>(mA, mB, mD, p, s);
 }
 
 cudaError_t launch_spmm_tc_sparse(const SpmmLaunch& a, cudaStream_t s) { return spmm_tc_sparse_impl(a, s, 0, 0); }
 
-int spmm_tc_dense_masked_split(const nm_spmm_desc_t&) { return 1; }
-size_t spmm_tc_dense_masked_workspace(const nm_spmm_desc_t&, int) { return 0; }
+// K split of the masked dense product: the number of splits that best fills
+// the SMs (fewest waves per unit of K), each split keeping at least 8 stages.
+int spmm_tc_dense_masked_split(const nm_spmm_desc_t& d) {
+  using namespace tc;
+  if (d.K <= 0 || d.M <= 0 || d.N <= 0) return 1;
+  const int64_t tiles = ((d.M + BM - 1) / BM) * ((d.N + BN - 1) / BN);
+  const int64_t stages = (d.K + kKPerStage - 1) / kKPerStage;
+  const int sms = num_sms();
+  int best = 1;
+  double best_cost = 1e30;
+  for (int sk = 1; sk <= 16; ++sk) {
+    if (sk > 1 && stages / sk < 8) break;
+    const int64_t units = tiles * sk;
+    const double waves = (double)((units + sms - 1) / sms);
+    const double cost = waves / sk + 0.02 * (sk - 1);  // partial traffic penalty
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = sk;
+    }
+  }
+  return best;
+}
+size_t spmm_tc_dense_masked_workspace(const nm_spmm_desc_t& d, int split_k) {
+  return split_k > 1 ? (size_t)split_k * (size_t)d.M * (size_t)d.N * sizeof(float) : 0;
+}
 
-cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int /*split_k*/, cudaStream_t s) {
+cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaStream_t s) {
   using namespace tc;
   const nm_spmm_desc_t& d = a.d;
   if (d.K == 0) return launch_k0(a, s);
@@ -656,6 +825,15 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int /*split_k*/, cu
   p.b_mn = d.order_b == NM_ROW;
   p.mask = static_cast<const uint32_t*>(a.A_meta);
   p.mask_words = (d.N + 31) / 32;
+  if (split_k > 1) {
+    if (a.ws == nullptr || a.ws_bytes < spmm_tc_dense_masked_workspace(d, split_k)) return cudaErrorInvalidValue;
+    p.stages_per_split = (p.k_stages + split_k - 1) / split_k;
+    p.split_k = (p.k_stages + p.stages_per_split - 1) / p.stages_per_split;  // splits that are not empty
+    p.partial = static_cast<float*>(a.ws);
+    p.tma_store = 0;
+  }
+  const int cl = cluster_for(p.num_m_blk);
+  p.num_units = (p.num_m_blk / cl) * p.num_n_blk * p.split_k;
   const CUtensorMapDataType u16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
   CUtensorMap mA, mB, mD;
   bool ok;
@@ -670,15 +848,16 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int /*split_k*/, cu
       ok = make_map(&mB, a.B, u16, (uint64_t)d.N, (uint64_t)d.K, (uint64_t)(d.ldb * 2), 64, 64,
                     CU_TENSOR_MAP_SWIZZLE_128B);
     else
-      ok = make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, BN,
+      ok = make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, (uint32_t)(BN / cl),
                     CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (ok) ok = make_store_map(&mD, d, a.D);
   if (!ok) return cudaErrorInvalidValue;
-  if (cudaError_t e = set_smem_attr<false>()) return e;
-  const int tiles = p.num_m_blk * p.num_n_blk;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  spmm_tc_kernel<false><<<grid, kThreads, Cfg<false>::kSmemBytes, s>>>(mA, mB, mA, mD, p);
+  cudaError_t e = cl == 2 ? launch_kernel<false, 2>(mA, mB, mD, p, s) : launch_kernel<false, 1>(mA, mB, mD, p, s);
+  if (e != cudaSuccess || p.split_k == 1) return e;
+  finalize_split_kernel<<<grid_for(d.M * d.N, 256), 256, 0, s>>>(
+      p.partial, p.split_k, d.M, d.N, static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.ldc, d.ldd,
+      d.order_cd == NM_COL, a.beta_f, d.ab_type == NM_BF16);
   return cudaGetLastError();
 }
 

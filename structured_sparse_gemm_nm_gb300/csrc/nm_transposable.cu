@@ -197,14 +197,14 @@ cudaError_t transposable_dt(const TransposableLaunch& a, cudaStream_t s) {
     if (a.meta != nullptr) {
       const int64_t slots = tc_slots(a.rows);
       if (slots != a.rows) {
-        cudaError_t e = cudaMemsetAsync(a.meta, 0x44, (size_t)((a.cols / 32) * slots * 16), s);
+        cudaError_t e = cudaMemsetAsync(a.meta, 0x44, (size_t)((a.cols / 32) * slots * 4), s);
         if (e != cudaSuccess) return e;
       }
     }
     if (a.metaT != nullptr) {
       const int64_t slots = tc_slots(a.cols);
       if (slots != a.cols) {
-        cudaError_t e = cudaMemsetAsync(a.metaT, 0x44, (size_t)((a.rows / 32) * slots * 16), s);
+        cudaError_t e = cudaMemsetAsync(a.metaT, 0x44, (size_t)((a.rows / 32) * slots * 4), s);
         if (e != cudaSuccess) return e;
       }
     }

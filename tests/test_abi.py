@@ -50,9 +50,9 @@ def test_version_and_status_strings(lib):
 
 def test_compressed_size(lib):
     assert nb.nm_compressed_size(64, 128, "f16", 2, 4) == (64 * 64 * 2, 64 * 8 * 2)
-    # tensor-core order: slot rows padded to 128, words per row padded to 4
-    assert nb.nm_compressed_size(64, 128, "f16", 2, 4, nb.NM_META_TC) == (64 * 64 * 2, 4 * 128 * 16)
-    assert nb.nm_compressed_size(300, 96, "bf16", 2, 4, nb.NM_META_TC) == (300 * 48 * 2, 3 * 384 * 16)
+    # tensor-core order: slot rows padded to 128, one word per slot and k-step
+    assert nb.nm_compressed_size(64, 128, "f16", 2, 4, nb.NM_META_TC) == (64 * 64 * 2, 4 * 128 * 4)
+    assert nb.nm_compressed_size(300, 96, "bf16", 2, 4, nb.NM_META_TC) == (300 * 48 * 2, 3 * 384 * 4)
     assert nb.nm_compressed_size(4096, 4096, "f16", 8, 32) == (4096 * 1024 * 2, 4096 * 1024)
     assert nb.nm_compressed_size(8, 64, "i8", 2, 4) == (8 * 32, 8 * 4 * 2)
     assert nb.nm_compressed_size(8, 20, "f16", 2, 4)[1] == 8 * 2 * 2  # ceil(20/16) words per row

@@ -62,7 +62,10 @@ PRUNE_CASES = [
     (4096, 4096, 4096, "f16", 8, 32, "normal"),
     (512, 4096, 4096, "f16", 4, 32, "normal"),
     (512, 4096, 4096, "f16", 16, 32, "normal"),
-    (70, 96, 100, "bf16", 8, 32, "special"),
+    (70, 96, 100, "bf16", 8, 32, "special"),     # generic path (ld not a multiple of 8)
+    (70, 96, 104, "bf16", 8, 32, "special"),     # n:32 fast path with NaN/Inf groups
+    (33, 128, 128, "f16", 16, 32, "special"),
+    (40, 64, 64, "bf16", 4, 32, "normal"),
     (45, 40, 40, "f16", 3, 8, "special"),
     (64, 64, 64, "i8", 1, 4, "normal"),
     (50, 30, 30, "f16", 2, 5, "normal"),
@@ -102,6 +105,8 @@ COMPRESS_CASES = [
     (4096, 4096, "f16", 4, 32, 0, nb.NM_META_CANONICAL),
     (4096, 4096, "f16", 16, 32, 0, nb.NM_META_CANONICAL),
     (64, 96, "bf16", 8, 32, 1, nb.NM_META_CANONICAL),
+    (96, 256, "bf16", 16, 32, 0, nb.NM_META_CANONICAL),
+    (50, 64, "f16", 4, 32, 0, nb.NM_META_CANONICAL),
     (45, 40, "f16", 3, 8, 0, nb.NM_META_CANONICAL),
 ]
 

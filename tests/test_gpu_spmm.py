@@ -215,3 +215,45 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     A = o.decode(o.nm_prune(bits_of(W, "f16", (M, K)), "f16", 2, 4)[0], "f16")
     ref = o.spmm(1.0, A, o.decode(bits_of(X, "f16", (N, K)), "f16").T)
     assert_gemm_close(D.cpu().double().numpy().T, ref, "after timeout")
+
+
+I8_CASES = [
+    # M, N, K, alpha, beta, order_cd, sampled, kind
+    (128, 64, 128, 1, 0, nb.NM_COL, False, "uniform"),
+    (200, 136, 192, 3, -2, nb.NM_ROW, False, "uniform"),      # ragged M/N, K tail of one k-step, alpha/beta
+    (64, 128, 4096, 1, 0, nb.NM_COL, False, "extreme"),       # |products| at the int8 limit over K = 4096
+    (1024, 4096, 1024, 1, 0, nb.NM_COL, True, "uniform"),     # BERT-Large shapes
+    (4096, 4096, 1024, 1, 0, nb.NM_COL, True, "uniform"),
+    (1024, 4096, 4096, 1, 0, nb.NM_COL, True, "uniform"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta,order_cd,sampled,kind", I8_CASES)
+def test_sparse_int8_bit_exact(M, N, K, alpha, beta, order_cd, sampled, kind):
+    if kind == "extreme":
+        W = torch.where(torch.arange(M * K).reshape(M, K) % 3 == 0, -128, 127).to(torch.int8)
+        X = torch.where(torch.arange(N * K).reshape(N, K) % 5 == 0, -128, 127).to(torch.int8)
+    else:
+        W = inputs.uniform_int8((M, K), inputs.SEED_W + M)
+        X = inputs.uniform_int8((N, K), inputs.SEED_X + N)
+    vb, mb = nb.nm_compressed_size(M, K, "i8", 2, 4, nb.NM_META_CANONICAL)
+    vals, meta = dev_bytes(vb), dev_bytes(mb)
+    nb.nm_compress(W.to(DEV), M, K, K, "i8", 2, 4, 0, nb.NM_META_CANONICAL, vals, meta)
+    cd_shape = (M, N) if order_cd == nb.NM_ROW else (N, M)
+    C = torch.randint(-2**31, 2**31 - 1, cd_shape, dtype=torch.int64).to(torch.int32) if beta else None
+    D = torch.full(cd_shape, 7, dtype=torch.int32, device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type="i8", cd_type="i32", ldb=K,
+                                        ldc=cd_shape[1] if beta else 0, ldd=cd_shape[1], order_cd=order_cd,
+                                        meta_layout=nb.NM_META_CANONICAL))
+    nb.nm_spmm(plan, alpha, vals, meta, X.to(DEV), beta, C.to(DEV) if C is not None else None, D)
+    torch.cuda.synchronize()
+    A = o.nm_prune(W.numpy(), "i8", 2, 4)[0]
+    rows = sample_rows(M, 64, seed=M + K) if sampled else np.arange(M)
+    Cm = None
+    if C is not None:
+        Cm = C.numpy() if order_cd == nb.NM_ROW else C.numpy().T
+        Cm = Cm[rows]
+    ref = o.spmm_int(alpha, A[rows], X.numpy().T, beta, Cm)
+    got = D.cpu().numpy()
+    got = got if order_cd == nb.NM_ROW else got.T
+    assert np.array_equal(got[rows], ref)

@@ -378,18 +378,36 @@ def test_tc_layout_round_trip_and_grouping():
     W = f16_bits(rng.standard_normal((40, 96)))
     _, meta = o.nm_compress(W, "f16", 2, 4)
     tc = o.meta_to_tc_layout(meta, 40, 96)
-    assert tc.shape == (3, 128, 4)
+    assert tc.shape == (3, 128)
     assert (o.meta_from_tc_layout(tc, 40, 96) == meta).all()
-    assert (tc[:, :, 1:] == o.TC_PAD_CODE_WORD).all()
     # rows 40..47 are the high halves of slots 32..47; slots 48.. are filler
-    assert (tc[:, 48:, 0] == o.TC_PAD_CODE_WORD).all()
-    assert ((tc[:, 32:48, 0] >> 16) == 0x4444).all()
+    assert (tc[:, 48:] == o.TC_PAD_CODE_WORD).all()
+    assert ((tc[:, 32:48] >> 16) == 0x4444).all()
     # each slot word pairs rows i and i+8 of its 16-row block at the same 16 columns
     for slot in range(40):
         b, j = divmod(slot, 16)
         h, i = divmod(j, 8)
         for s in range(3):
             lo_row, hi_row = 16 * b + i, 16 * b + 8 + i
-            assert int(tc[s, slot, 0]) & 0xFFFF == int(meta[lo_row, 2 * s + h])
+            assert int(tc[s, slot]) & 0xFFFF == int(meta[lo_row, 2 * s + h])
             if hi_row < 40:
-                assert int(tc[s, slot, 0]) >> 16 == int(meta[hi_row, 2 * s + h])
+                assert int(tc[s, slot]) >> 16 == int(meta[hi_row, 2 * s + h])
+
+
+def test_vw_bw_csr_matches_sorted_lists():
+    rng = np.random.default_rng(34)
+    W = (rng.standard_normal((64, 128)) * 0.02).astype(np.float16).view(np.uint16)
+    mv = o.vector_wise_mask(W, "f16", 0.25, 32)
+    csr, vals = o.vector_wise_csr(W, mv, 32)
+    idx, vals2 = o.vector_wise_compress(W, mv, 32)
+    row_ptr, cols_ = csr[:65], csr[65:]
+    assert row_ptr[-1] == len(idx) == int(256 * 0.25)
+    assert (row_ptr[:-1] * 0 + np.diff(row_ptr) >= 0).all()
+    # the CSR order is the ascending global vector order
+    assert (np.repeat(np.arange(64), np.diff(row_ptr)) * 4 + cols_ == idx).all()
+    assert (vals == vals2).all()
+    mb = o.block_wise_mask(W, "f16", 0.25, 32, 32)
+    bcsr, blocks = o.block_wise_csr(W, mb, 32, 32)
+    bidx, bvals = o.block_wise_compress(W, mb, 32, 32)
+    assert (np.repeat(np.arange(2), np.diff(bcsr[:3])) * 4 + bcsr[3:] == bidx).all()
+    assert (blocks == bvals).all()
