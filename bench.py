@@ -343,6 +343,37 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
                                              "gflops": 2.0 * M * (K // 32) * n * b / t / 1e6}
             plan.destroy()
 
+    # S9: vector-wise (1 x 32) and block-wise (32 x 32) selection at density 0.25, then the product
+    W = inputs.normal((M, K), 0.02, inputs.SEED_W, "f16", device=dev)
+    for bh, uname in ((1, "vector_wise"), (32, "block_wise")):
+        keep = (M // bh) * (K // 32) // 4
+        wsb = nb.nm_prune_units_workspace(M, K, bh, 32)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        csr = torch.empty((M // bh + 1 + keep) * 4, dtype=torch.uint8, device=dev)
+        vals = torch.empty(keep * bh * 32 * 2, dtype=torch.uint8, device=dev)
+        if bh == 1:
+            sel = lambda: nb.nm_prune_vector_wise(W, M, K, K, "f16", 32, keep, nb.NM_SCORE_ABS_OF_SUM, csr=csr,
+                                                  vals=vals, workspace=ws, workspace_bytes=wsb)
+        else:
+            sel = lambda: nb.nm_prune_block_wise(W, M, K, K, "f16", 32, 32, keep, csr=csr, vals=vals, workspace=ws,
+                                                 workspace_bytes=wsb)
+        t = time_launch(torch, sel, flush)
+        byt = M * K * 2 + csr.numel() + vals.numel()
+        rows[f"S9_{uname}_select_compress"] = {"shape": [M, K], "kept_units": keep, "ms": t, "bytes": byt,
+                                               "gbs": byt / t / 1e6, "frac_hbm": byt / t / 1e6 / hbm}
+        for b in (1, 8):
+            x = inputs.normal((b, K), 1.0, inputs.SEED_VEC, "f16", device=dev)
+            y = torch.empty((b, M), dtype=torch.float16, device=dev)
+            plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=b, K=K, mode=nb.NM_SPMM_BLOCK_SPARSE_A, n=bh, m=32,
+                                                ab_type="f16", cd_type="f16", ldb=K, ldd=M,
+                                                meta_layout=nb.NM_META_CANONICAL))
+            t = time_launch(torch, lambda: nb.nm_spmm(plan, 1.0, vals, csr, x, 0.0, None, y), flush)
+            byt = vals.numel() + csr.numel() + b * K * 2 + b * M * 2
+            rows[f"S9_{uname}_gemv_b{b}"] = {"ms": t, "bytes": byt, "gbs": byt / t / 1e6,
+                                             "frac_hbm": byt / t / 1e6 / hbm,
+                                             "gflops": 2.0 * keep * bh * 32 * b / t / 1e6}
+            plan.destroy()
+
     # BERT-Large-shaped sparse products (f16) with cuBLAS on the same shapes
     for (Mb, Nb, Kb) in inputs.BERT_SHAPES:
         Wb = inputs.normal((Mb, Kb), 0.02, inputs.SEED_W, "f16", device=dev)

@@ -155,14 +155,66 @@ nm_status_t nm_prune_transposable(const void* W, int64_t rows, int64_t cols, int
                                   void* valsT, void* metaT, nm_meta_layout_t layout, nm_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Vector-wise and block-wise pruning (apex PR #1631 "[sparse] update support
+ * for arbitrary N:M settings sparse", extension 2: unstructured_vector_wise
+ * and unstructured_block_wise).  A unit is a 1 x v vector (v consecutive
+ * elements of a row) or a bh x bw block; units are numbered in row-major
+ * order of their top-left element.  The `keep` units with the largest score
+ * are kept, equal scores going to the lower unit index; everything else is
+ * pruned.  Callers derive keep from a density as floor(units * density).
+ *
+ * Scores are computed exactly (f16 and int8 only): vector-wise by |sum w|
+ * (NM_SCORE_ABS_OF_SUM, the page's rule) or sum |w| (NM_SCORE_SUM_OF_ABS);
+ * block-wise always by sum |w|.  An infinite score ranks above every number,
+ * a NaN score (a NaN element, or +Inf and -Inf in one signed sum) below
+ * every number.
+ *
+ * Outputs, each nullable:
+ *   W_out      pruned copy (kept units copied, the rest +0); may alias W
+ *              with ld_out == ld.
+ *   mask_bits  bit mask of the kept elements (format above).
+ *   csr        int32: unit-row pointers (rows/bh + 1 entries, entry r = kept
+ *              units before unit row r), then one unit-column index per kept
+ *              unit (column c covers W columns bw*c .. bw*c + bw - 1), in
+ *              ascending order within each unit row.  rows/bh + 1 + keep
+ *              entries in all.
+ *   vals       the kept units' elements, unit after unit in the csr order,
+ *              each unit row-major (bh * bw elements); keep * bh * bw
+ *              elements in all.
+ * workspace: device scratch of nm_prune_units_workspace bytes, 16-byte
+ * aligned; its contents are not needed between calls.  Calls that share a
+ * workspace must not overlap on the GPU.
+ * Requirements: dtype NM_F16 or NM_I8 (NM_ERR_UNSUPPORTED otherwise);
+ * v == 32, bh == bw == 32 (NM_ERR_UNSUPPORTED otherwise); cols % bw == 0 and
+ * rows % bh == 0; 0 <= keep <= units < 2^31; W, W_out and vals 16-byte
+ * aligned and ld, ld_out multiples of 16 bytes (NM_ERR_MISALIGNED).
+ * ---------------------------------------------------------------------- */
+typedef enum { NM_SCORE_ABS_OF_SUM = 0, NM_SCORE_SUM_OF_ABS = 1 } nm_score_t;
+
+/* Host-only: workspace bytes for a rows x cols matrix cut into bh x bw units. */
+nm_status_t nm_prune_units_workspace(int64_t rows, int64_t cols, int bh, int bw, size_t* bytes);
+
+/* Vector-wise pruning: units are 1 x v vectors. */
+nm_status_t nm_prune_vector_wise(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int v,
+                                 int64_t keep, nm_score_t score, void* W_out, int64_t ld_out, uint32_t* mask_bits,
+                                 int32_t* csr, void* vals, void* workspace, size_t workspace_bytes,
+                                 nm_stream_t stream);
+
+/* Block-wise pruning: units are bh x bw blocks, scored by sum |w|. */
+nm_status_t nm_prune_block_wise(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int bh,
+                                int bw, int64_t keep, void* W_out, int64_t ld_out, uint32_t* mask_bits, int32_t* csr,
+                                void* vals, void* workspace, size_t workspace_bytes, nm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The product D = alpha * op(A) * op(B) + beta * C  (cuSPARSELt blog, the
  * GEMM paragraph: A is M x K, B is K x N, C and D are M x N; "N" layout =
  * column-major, "T" = row-major; FP16/BF16 inputs accumulate in FP32, INT8
  * inputs in INT32).
  * ---------------------------------------------------------------------- */
 typedef enum {
-  NM_SPMM_SPARSE_A = 0,     /* A is N:M sparse, given compressed (values + metadata)                */
-  NM_SPMM_DENSE_MASKED = 1  /* A and B dense; the product is multiplied by a bit mask of D's shape  */
+  NM_SPMM_SPARSE_A = 0,       /* A is N:M sparse, given compressed (values + metadata)                */
+  NM_SPMM_DENSE_MASKED = 1,   /* A and B dense; the product is multiplied by a bit mask of D's shape  */
+  NM_SPMM_BLOCK_SPARSE_A = 2  /* A is given as its kept n x m units: values + CSR (see below)         */
 } nm_spmm_mode_t;
 
 typedef enum {
@@ -194,7 +246,10 @@ typedef struct nm_spmm_plan_s* nm_spmm_plan_t;
  * Supported: SPARSE_A 2:4 F16/BF16 (tensor cores, B in NM_COL), SPARSE_A 2:4
  * I8 -> I32 (canonical metadata, B in NM_COL), SPARSE_A n:m with m <= 32 and
  * canonical metadata (CUDA-core gather, B in NM_COL), DENSE_MASKED F16/BF16
- * (tensor cores, any orders).
+ * (tensor cores, any orders), BLOCK_SPARSE_A F16/BF16 with units of n x m =
+ * 1 x 32 or 32 x 32 (CUDA cores, B in NM_COL; A = the vals and A_meta = the
+ * csr that nm_prune_vector_wise / nm_prune_block_wise write; K % 32 == 0 and,
+ * for 32 x 32, M % 32 == 0).
  */
 nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc);
 

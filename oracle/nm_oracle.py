@@ -315,7 +315,10 @@ def vector_wise_mask(W: np.ndarray, dtype: str, density: float, v: int = 32, sco
     Vectors are consecutive v-element chunks of the row-major matrix.  The
     page scores a vector by the absolute value of its (signed) sum; the
     alternative ``sum_of_abs`` is offered for comparison.  Ties go to the
-    lower vector index.  Sums are exact in float64 for f16 and int8 inputs."""
+    lower vector index.  Sums are exact in float64 for f16 and int8 inputs.
+    Special values follow float64 arithmetic: an infinite score ranks above
+    every number, a NaN score (a NaN element, or +Inf and -Inf summed) below
+    every number, including 0."""
     if dtype == "bf16":
         raise ValueError("vector-wise scores are exact only for f16 and int8")
     flat = decode(W, dtype).reshape(-1, v)
@@ -332,7 +335,7 @@ def block_wise_mask(W: np.ndarray, dtype: str, density: float, bh: int = 32, bw:
     """Keep the floor(#blocks * density) bh x bw blocks with the largest sum of |w|.
 
     Ties go to the lower row-major block index.  Sums are exact in float64
-    for f16 and int8 inputs."""
+    for f16 and int8 inputs; special values rank as in ``vector_wise_mask``."""
     if dtype == "bf16":
         raise ValueError("block-wise scores are exact only for f16 and int8")
     rows, cols = W.shape

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_HERE, "lib", "libnm.so")
 NM_OK, NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED, NM_ERR_MISALIGNED, NM_ERR_CUDA, NM_ERR_TIMEOUT = range(6)
 NM_F16, NM_BF16, NM_I8, NM_F32, NM_I32 = range(5)
 NM_META_CANONICAL, NM_META_TC = 0, 1
-NM_SPMM_SPARSE_A, NM_SPMM_DENSE_MASKED = 0, 1
+NM_SPMM_SPARSE_A, NM_SPMM_DENSE_MASKED, NM_SPMM_BLOCK_SPARSE_A = 0, 1, 2
+NM_SCORE_ABS_OF_SUM, NM_SCORE_SUM_OF_ABS = 0, 1
 NM_ROW, NM_COL = 0, 1
 
 DTYPE_NAMES = {"f16": NM_F16, "bf16": NM_BF16, "i8": NM_I8, "f32": NM_F32, "i32": NM_I32}
@@ -27,8 +28,8 @@ DTYPE_NAMES = {"f16": NM_F16, "bf16": NM_BF16, "i8": NM_I8, "f32": NM_F32, "i32"
 # Every symbol include/nm.h declares.
 EXPORTED = (
     "nm_status_string", "nm_version", "nm_compressed_size", "nm_prune", "nm_compress", "nm_decompress",
-    "nm_check", "nm_prune_transposable", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy",
-    "nm_spmm",
+    "nm_check", "nm_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
+    "nm_prune_block_wise", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm",
 )
 
 
@@ -73,6 +74,9 @@ def lib() -> ctypes.CDLL:
             "nm_decompress": [vp, vp, i64, i64, i32, i32, i32, i32, vp, i64, vp],
             "nm_check": [vp, i64, i64, i64, i32, i32, i32, i32, vp, vp],
             "nm_prune_transposable": [vp, i64, i64, i64, i32, vp, i64, vp, vp, vp, vp, vp, i32, vp],
+            "nm_prune_units_workspace": [i64, i64, i32, i32, ctypes.POINTER(sz)],
+            "nm_prune_vector_wise": [vp, i64, i64, i64, i32, i32, i64, i32, vp, i64, vp, vp, vp, vp, sz, vp],
+            "nm_prune_block_wise": [vp, i64, i64, i64, i32, i32, i32, i64, vp, i64, vp, vp, vp, vp, sz, vp],
             "nm_spmm_plan": [ctypes.POINTER(vp), ctypes.POINTER(SpmmDesc)],
             "nm_spmm_plan_workspace": [vp, ctypes.POINTER(sz)],
             "nm_spmm_plan_destroy": [vp],
@@ -156,6 +160,26 @@ def nm_prune_transposable(W, rows, cols, ld, dtype, W_out=None, ld_out=0, mask_b
     _check(lib().nm_prune_transposable(_ptr(W), rows, cols, ld, _dt(dtype), _ptr(W_out), ld_out, _ptr(mask_bits),
                                        _ptr(vals), _ptr(meta), _ptr(valsT), _ptr(metaT), layout, _stream(stream)),
            "nm_prune_transposable")
+
+
+def nm_prune_units_workspace(rows, cols, bh, bw) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().nm_prune_units_workspace(rows, cols, bh, bw, ctypes.byref(b)), "nm_prune_units_workspace")
+    return b.value
+
+
+def nm_prune_vector_wise(W, rows, cols, ld, dtype, v, keep, score=NM_SCORE_ABS_OF_SUM, W_out=None, ld_out=0,
+                         mask_bits=None, csr=None, vals=None, workspace=None, workspace_bytes=0, stream=None):
+    _check(lib().nm_prune_vector_wise(_ptr(W), rows, cols, ld, _dt(dtype), v, int(keep), int(score), _ptr(W_out),
+                                      ld_out, _ptr(mask_bits), _ptr(csr), _ptr(vals), _ptr(workspace),
+                                      workspace_bytes, _stream(stream)), "nm_prune_vector_wise")
+
+
+def nm_prune_block_wise(W, rows, cols, ld, dtype, bh, bw, keep, W_out=None, ld_out=0, mask_bits=None, csr=None,
+                        vals=None, workspace=None, workspace_bytes=0, stream=None):
+    _check(lib().nm_prune_block_wise(_ptr(W), rows, cols, ld, _dt(dtype), bh, bw, int(keep), _ptr(W_out), ld_out,
+                                     _ptr(mask_bits), _ptr(csr), _ptr(vals), _ptr(workspace), workspace_bytes,
+                                     _stream(stream)), "nm_prune_block_wise")
 
 
 class SpmmPlan:

@@ -45,7 +45,7 @@ size_t tc_meta_bytes(int64_t rows, int64_t cols) {
 
 struct nm_spmm_plan_s {
   nm_spmm_desc_t d;
-  int kind;  // 0 tc sparse, 1 tc dense masked, 2 gather n:m, 3 int8 mma.sp
+  int kind;  // 0 tc sparse, 1 tc dense masked, 2 gather n:m, 3 int8 mma.sp, 4 vector/block units
   int split_k;
   size_t ws_bytes;
 };
@@ -208,6 +208,83 @@ nm_status_t nm_prune_transposable(const void* W, int64_t rows, int64_t cols, int
   return from_cuda(nmk::launch_transposable(a, (cudaStream_t)stream));
 }
 
+// ------------------------------------------------------- vector/block units
+}  // extern "C"
+
+namespace {
+nm_status_t units_shape(int64_t rows, int64_t cols, int bh, int bw, int64_t* units) {
+  if (rows < 0 || cols < 0 || bh < 1 || bw < 1) return NM_ERR_INVALID_ARG;
+  if (bw != 32 || (bh != 1 && bh != 32)) return NM_ERR_UNSUPPORTED;
+  if (cols % bw || rows % bh) return NM_ERR_INVALID_ARG;
+  *units = (rows / bh) * (cols / bw);
+  if (*units >= (int64_t(1) << 31)) return NM_ERR_UNSUPPORTED;
+  return NM_OK;
+}
+
+nm_status_t prune_units(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int bh, int bw,
+                        int64_t keep, int abs_of_sum, void* W_out, int64_t ld_out, uint32_t* mask_bits,
+                        int32_t* csr, void* vals, void* workspace, size_t workspace_bytes, nm_stream_t stream) {
+  if (!is_elem(dtype)) return NM_ERR_INVALID_ARG;
+  int64_t units = 0;
+  if (nm_status_t st = units_shape(rows, cols, bh, bw, &units)) return st;
+  if (dtype == NM_BF16) return NM_ERR_UNSUPPORTED;
+  if (keep < 0 || keep > units) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_matrix(W, rows, cols, ld, dtype, false)) return st;
+  if (nm_status_t st = check_matrix(W_out, rows, cols, ld_out, dtype, true)) return st;
+  if (W_out == W && W != nullptr && ld_out != ld) return NM_ERR_INVALID_ARG;
+  const int64_t es = elem_size(dtype);
+  if (!aligned(W, 16) || (ld * es) % 16 || !aligned(W_out, 16) || (W_out != nullptr && (ld_out * es) % 16) ||
+      !aligned(vals, 16) || !aligned(csr, 4) || !aligned(mask_bits, 4) || !aligned(workspace, 16))
+    return NM_ERR_MISALIGNED;
+  if (units > 0 && (workspace == nullptr || workspace_bytes < nmk::blocks_workspace(units))) return NM_ERR_INVALID_ARG;
+  nmk::BlocksLaunch a{};
+  a.dt = (int)dtype;
+  a.W = W;
+  a.rows = rows;
+  a.cols = cols;
+  a.ld = ld;
+  a.bh = bh;
+  a.units = units;
+  a.unit_rows = rows / bh;
+  a.keep = keep;
+  a.abs_of_sum = abs_of_sum;
+  a.W_out = W_out;
+  a.ld_out = ld_out;
+  a.mask_bits = mask_bits;
+  a.csr = csr;
+  a.vals = vals;
+  a.ws = workspace;
+  return from_cuda(nmk::launch_blocks(a, (cudaStream_t)stream));
+}
+}  // namespace
+
+extern "C" {
+
+nm_status_t nm_prune_units_workspace(int64_t rows, int64_t cols, int bh, int bw, size_t* bytes) {
+  if (bytes == nullptr) return NM_ERR_INVALID_ARG;
+  int64_t units = 0;
+  if (nm_status_t st = units_shape(rows, cols, bh, bw, &units)) return st;
+  *bytes = units > 0 ? nmk::blocks_workspace(units) : 0;
+  return NM_OK;
+}
+
+nm_status_t nm_prune_vector_wise(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int v,
+                                 int64_t keep, nm_score_t score, void* W_out, int64_t ld_out, uint32_t* mask_bits,
+                                 int32_t* csr, void* vals, void* workspace, size_t workspace_bytes,
+                                 nm_stream_t stream) {
+  if (score != NM_SCORE_ABS_OF_SUM && score != NM_SCORE_SUM_OF_ABS) return NM_ERR_INVALID_ARG;
+  return prune_units(W, rows, cols, ld, dtype, 1, v, keep, score == NM_SCORE_ABS_OF_SUM, W_out, ld_out, mask_bits,
+                     csr, vals, workspace, workspace_bytes, stream);
+}
+
+nm_status_t nm_prune_block_wise(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int bh,
+                                int bw, int64_t keep, void* W_out, int64_t ld_out, uint32_t* mask_bits, int32_t* csr,
+                                void* vals, void* workspace, size_t workspace_bytes, nm_stream_t stream) {
+  if (bh == 1) return NM_ERR_UNSUPPORTED;  // 1 x bw blocks are vectors: nm_prune_vector_wise
+  return prune_units(W, rows, cols, ld, dtype, bh, bw, keep, 0, W_out, ld_out, mask_bits, csr, vals, workspace,
+                     workspace_bytes, stream);
+}
+
 // ------------------------------------------------------------------ products
 nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   if (plan == nullptr || desc == nullptr) return NM_ERR_INVALID_ARG;
@@ -253,6 +330,11 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
     if (d.lda < a_inner || d.lda < 1) return NM_ERR_INVALID_ARG;
     if ((d.lda * es) % 16) return NM_ERR_MISALIGNED;
     kind = 1;
+  } else if (d.mode == NM_SPMM_BLOCK_SPARSE_A) {
+    if (!fp || d.order_b != NM_COL) return NM_ERR_UNSUPPORTED;
+    if (d.m != 32 || (d.n != 1 && d.n != 32)) return NM_ERR_UNSUPPORTED;
+    if (d.K % 32 || d.M % d.n) return NM_ERR_INVALID_ARG;
+    kind = 4;
   } else {
     return NM_ERR_INVALID_ARG;
   }
@@ -296,6 +378,7 @@ nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const
   if (A == nullptr || A_meta == nullptr || B == nullptr || D == nullptr) {
     if (d.K > 0 || D == nullptr) return NM_ERR_INVALID_ARG;
   }
+  if (plan->kind == 4 && A_meta == nullptr) return NM_ERR_INVALID_ARG;
   if (!beta_zero && (C == nullptr || d.ldc == 0)) return NM_ERR_INVALID_ARG;
   if (!aligned(A, 16) || !aligned(A_meta, 16) || !aligned(B, 16) || !aligned(D, 16) ||
       (!beta_zero && !aligned(C, 16)) || (d_status && !aligned(d_status, 4)))
@@ -316,6 +399,7 @@ nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const
     case 1: return from_cuda(nmk::launch_spmm_tc_dense_masked(a, plan->split_k, s));
     case 2: return from_cuda(nmk::launch_spmm_nm_gather(a, s));
     case 3: return from_cuda(nmk::launch_spmm_i8(a, s));
+    case 4: return from_cuda(nmk::launch_spmm_blocks(a, s));
   }
   return NM_ERR_INVALID_ARG;
 }

@@ -1,0 +1,673 @@
+// Vector-wise (1 x 32) and block-wise (32 x 32) pruning and the product over
+// the kept units (apex PR #1631 "[sparse] update support for arbitrary N:M
+// settings sparse", extension 2: unstructured vector-wise and block-wise
+// masks).
+//
+// Selection keeps the `keep` units (1 x 32 vectors or 32 x 32 blocks) with the
+// largest score; equal scores go to the lower unit index (row-major order).
+// Scores are exact integers: an f16 value is a whole number of 2^-24 units
+// below 2^40, so the score of a unit of at most 1024 elements is an integer
+// below 2^51 (int8: below 2^18).  A unit's 64-bit key orders it: 0 for a NaN
+// score, score + 1 for a finite score, 2^62 for an infinite one.
+//
+// Four launches, none of which waits on another CTA:
+//   1. score      key of every unit and a histogram of a log-scale bucket of
+//                 the key (64 buckets per octave); the last CTA to finish
+//                 finds the bucket holding the keep-th largest key.
+//   2. candidates the keys of that bucket are gathered; the last CTA finds the
+//                 exact threshold key T by a radix search over them.
+//   3. count      per chunk of 256 units: keys above T and keys equal to T;
+//                 the last CTA turns the counts into exclusive prefixes.
+//   4. write      kept flag and output position of every unit, then the CSR
+//                 arrays, the packed values, the bit mask and the pruned copy.
+// A unit is kept if its key is above T, or equal to T and among the first
+// `need_eq` such units in index order.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "nm_device.cuh"
+#include "nm_internal.h"
+
+namespace nmk {
+namespace {
+
+constexpr int kUnitW = 32;         // unit width (columns) of both kinds
+constexpr int kBins = 4096;        // log-scale buckets
+constexpr int kChunk = 256;        // units per CTA in the count and write kernels
+constexpr uint64_t kKeyInf = 1ull << 62;
+
+struct Ctl {
+  uint32_t ticket[3];
+  uint32_t cand_count;
+  int32_t bucket;  // bucket to refine, or -1 when T is already final
+  uint32_t pad;
+  uint64_t k_rem;    // keys still to take inside `bucket`
+  uint64_t T;        // threshold key
+  uint64_t need_eq;  // keys equal to T that are kept
+};
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t hist, ctl, keys, cand, cnt_gt, cnt_eq, total;
+};
+WsLayout ws_layout(int64_t units) {
+  const int64_t chunks = (units + kChunk - 1) / kChunk;
+  WsLayout w{};
+  w.hist = 0;
+  w.ctl = align256(kBins * 4);
+  w.keys = w.ctl + align256(sizeof(Ctl));
+  w.cand = w.keys + align256((size_t)units * 8);
+  w.cnt_gt = w.cand + align256((size_t)units * 8);
+  w.cnt_eq = w.cnt_gt + align256((size_t)chunks * 4);
+  w.total = w.cnt_eq + align256((size_t)chunks * 4);
+  return w;
+}
+
+// ---------------------------------------------------------------- scoring
+// Flags: 1 NaN, 2 +Inf, 4 -Inf.
+__device__ __forceinline__ void acc_f16(uint32_t h, int64_t& s, int64_t& a, uint32_t& fl) {
+  const uint32_t e = (h >> 10) & 31u, mnt = h & 1023u;
+  if (e == 31u) {
+    fl |= mnt ? 1u : ((h & 0x8000u) ? 4u : 2u);
+    return;
+  }
+  const int64_t u = e ? (int64_t)(1024u + mnt) << (e - 1) : (int64_t)mnt;
+  s += (h & 0x8000u) ? -u : u;
+  a += u;
+}
+
+// Score contributions of one 16-byte segment (8 f16 or 16 int8 elements).
+template <int DT>
+__device__ __forceinline__ void acc_seg(const uint4 v, int64_t& s, int64_t& a, uint32_t& fl) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (DT == kF16) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc_f16(w[i] & 0xFFFFu, s, a, fl);
+      acc_f16(w[i] >> 16, s, a, fl);
+    }
+  } else {
+    int si = 0, ai = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int x = (int)(int8_t)(w[i] >> (8 * b));
+        si += x;
+        ai += x < 0 ? -x : x;
+      }
+    s += si;
+    a += ai;
+  }
+}
+
+__device__ __forceinline__ uint64_t make_key(int64_t s, int64_t a, uint32_t fl, int abs_of_sum) {
+  if (abs_of_sum) {
+    if ((fl & 1u) || (fl & 6u) == 6u) return 0;
+    if (fl) return kKeyInf;
+    return (uint64_t)(s < 0 ? -s : s) + 1;
+  }
+  if (fl & 1u) return 0;
+  if (fl) return kKeyInf;
+  return (uint64_t)a + 1;
+}
+
+// Monotone log-scale bucket: keys below 128 are their own bucket; above, the
+// leading bit position and the next 6 bits.
+__device__ __forceinline__ int key_bucket(uint64_t k) {
+  if (k < 64) return (int)k;
+  const int lead = 63 - __clzll((long long)k);  // >= 6
+  return (lead - 5) * 64 + (int)((k >> (lead - 6)) & 63);
+}
+
+__device__ __forceinline__ int64_t shfl_xor64(int64_t v, int m) {
+  const int lo = __shfl_xor_sync(0xFFFFFFFFu, (int)(uint32_t)(uint64_t)v, m);
+  const int hi = __shfl_xor_sync(0xFFFFFFFFu, (int)(uint32_t)((uint64_t)v >> 32), m);
+  return (int64_t)(((uint64_t)(uint32_t)hi << 32) | (uint32_t)lo);
+}
+
+// True in every thread of the CTA that finished last; its writes and those of
+// all other CTAs are visible to it afterwards (threadfence + ticket pattern).
+__device__ __forceinline__ bool last_cta(uint32_t* ticket) {
+  __shared__ bool is_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (is_last) __threadfence();
+  return is_last;
+}
+
+// Run by the last score CTA: the bucket that holds the keep-th largest key.
+__device__ void select_bucket(const uint32_t* hist, Ctl* ctl, uint64_t keep) {
+  __shared__ uint64_t part[256];
+  const int t = threadIdx.x;  // 256 threads, 16 bins each, highest bins first
+  constexpr int per = kBins / 256;
+  const int top = kBins - per * t;  // bins [top - per, top)
+  uint64_t sum = 0;
+  for (int b = top - per; b < top; ++b) sum += __ldcg(hist + b);
+  part[t] = sum;
+  __syncthreads();
+  if (t == 0) {
+    if (keep == 0) {
+      ctl->bucket = -1;
+      ctl->T = ~0ull;
+      ctl->need_eq = 0;
+    } else {
+      uint64_t above = 0;
+      int tt = 0;
+      while (above + part[tt] < keep) above += part[tt++];
+      int b = kBins - per * tt - 1;
+      for (;; --b) {
+        const uint64_t h = __ldcg(hist + b);
+        if (above + h >= keep) break;
+        above += h;
+      }
+      const uint64_t k_rem = keep - above;
+      if (b < 128) {  // a single key value
+        ctl->bucket = -1;
+        ctl->T = (uint64_t)b;
+        ctl->need_eq = k_rem;
+      } else {
+        ctl->bucket = b;
+        ctl->k_rem = k_rem;
+      }
+    }
+  }
+}
+
+// Vector-wise keys: a thread scores one 16-byte segment; the segments of a
+// vector sit in consecutive lanes.
+template <int DT>
+__global__ void __launch_bounds__(256) vw_score_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_t cols,
+                                                       int64_t ld_bytes, int abs_of_sum, uint64_t* __restrict__ keys,
+                                                       uint32_t* __restrict__ hist, Ctl* ctl, uint64_t keep) {
+  constexpr int kSegElems = DT == kF16 ? 8 : 16;
+  constexpr int kSpv = kUnitW / kSegElems;  // segments per vector: 4 (f16) or 2 (int8)
+  __shared__ uint32_t sh[kBins];
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  const int64_t spr = cols / kSegElems;
+  const int64_t total = rows * spr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x; g0 < total; g0 += 2 * stride) {
+    uint4 v[2];
+    bool ok[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int64_t g = g0 + j * stride + threadIdx.x;
+      ok[j] = g < total;
+      if (ok[j]) {
+        const int64_t r = g / spr, s = g - r * spr;
+        v[j] = __ldcs(reinterpret_cast<const uint4*>(W + r * ld_bytes + s * 16));
+      } else {
+        v[j] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      int64_t s = 0, a = 0;
+      uint32_t fl = 0;
+      acc_seg<DT>(v[j], s, a, fl);
+#pragma unroll
+      for (int m = 1; m < kSpv; m <<= 1) {
+        s += shfl_xor64(s, m);
+        a += shfl_xor64(a, m);
+        fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, m);
+      }
+      const int64_t g = g0 + j * stride + threadIdx.x;
+      if (ok[j] && (lane % kSpv) == 0) {
+        const uint64_t key = make_key(s, a, fl, abs_of_sum);
+        keys[g / kSpv] = key;
+        atomicAdd(&sh[key_bucket(key)], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x)
+    if (sh[i]) atomicAdd(hist + i, sh[i]);
+  if (last_cta(&ctl->ticket[0])) select_bucket(hist, ctl, keep);
+}
+
+// Block-wise keys: a warp scores one 32 x 32 block (sum of |w|).
+template <int DT>
+__global__ void __launch_bounds__(256) bw_score_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_t cols,
+                                                       int64_t ld_bytes, uint64_t* __restrict__ keys,
+                                                       uint32_t* __restrict__ hist, Ctl* ctl, uint64_t keep) {
+  constexpr int kSegElems = DT == kF16 ? 8 : 16;
+  constexpr int kSpr = kUnitW / kSegElems;  // segments per block row: 4 or 2
+  constexpr int kRowsPer = 32 / kSpr;       // block rows per warp load: 8 or 16
+  constexpr int es = DT == kF16 ? 2 : 1;
+  __shared__ uint32_t sh[kBins];
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  const int64_t bn = cols / kUnitW, units = (rows / 32) * bn;
+  const int lane = threadIdx.x & 31;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += wstride) {
+    const int64_t bi = u / bn, bj = u - bi * bn;
+    const uint8_t* base = W + (bi * 32 + lane / kSpr) * ld_bytes + (bj * kUnitW + (lane % kSpr) * kSegElems) * es;
+    uint4 v[32 / kRowsPer];
+#pragma unroll
+    for (int p = 0; p < 32 / kRowsPer; ++p) v[p] = __ldcs(reinterpret_cast<const uint4*>(base + p * kRowsPer * ld_bytes));
+    int64_t s = 0, a = 0;
+    uint32_t fl = 0;
+#pragma unroll
+    for (int p = 0; p < 32 / kRowsPer; ++p) acc_seg<DT>(v[p], s, a, fl);
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      a += shfl_xor64(a, m);
+      fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, m);
+    }
+    if (lane == 0) {
+      const uint64_t key = make_key(0, a, fl, 0);
+      keys[u] = key;
+      atomicAdd(&sh[key_bucket(key)], 1u);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x)
+    if (sh[i]) atomicAdd(hist + i, sh[i]);
+  if (last_cta(&ctl->ticket[0])) select_bucket(hist, ctl, keep);
+}
+
+// ---------------------------------------------------------------- threshold
+__global__ void __launch_bounds__(256) candidates_kernel(const uint64_t* __restrict__ keys, int64_t units, Ctl* ctl,
+                                                         uint64_t* __restrict__ cand) {
+  const int B = ctl->bucket;
+  if (B < 0) return;  // T already final (uniform across the grid)
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); i0 < units; i0 += stride) {
+    const int64_t i = i0 + lane;
+    const uint64_t key = i < units ? keys[i] : 0;
+    const bool c = i < units && key_bucket(key) == B;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, c);
+    if (bal) {
+      const int leader = __ffs(bal) - 1;
+      uint32_t base = 0;
+      if (lane == leader) base = atomicAdd(&ctl->cand_count, (uint32_t)__popc(bal));
+      base = __shfl_sync(0xFFFFFFFFu, base, leader);
+      if (c) cand[base + __popc(bal & ((1u << lane) - 1u))] = key;
+    }
+  }
+  if (!last_cta(&ctl->ticket[1])) return;
+  // Radix search, 8 bits at a time, over the bits the bucket leaves open.
+  __shared__ uint32_t h[256];
+  __shared__ uint64_t s_prefix, s_k;
+  const uint32_t n = __ldcg(&ctl->cand_count);
+  const int lead = B / 64 + 5;
+  const int hi_bit = lead - 7;  // highest bit not fixed by the bucket (B >= 128 so lead >= 7)
+  if (threadIdx.x == 0) {
+    s_prefix = (uint64_t)(64 + (B & 63)) << (lead - 6);
+    s_k = __ldcg(&ctl->k_rem);
+  }
+  for (int shift = (hi_bit / 8) * 8; shift >= 0; shift -= 8) {
+    h[threadIdx.x] = 0;
+    __syncthreads();
+    const uint64_t want = s_prefix >> (shift + 8);
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint64_t key = __ldcg(cand + i);
+      if ((key >> (shift + 8)) == want) atomicAdd(&h[(key >> shift) & 255], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint64_t k = s_k, above = 0;
+      int d = 255;
+      while (above + h[d] < k) above += h[d--];
+      s_k = k - above;
+      s_prefix = (s_prefix & ~(255ull << shift)) | ((uint64_t)d << shift);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    ctl->T = s_prefix;
+    ctl->need_eq = s_k;
+  }
+}
+
+// ---------------------------------------------------------------- ordering
+// In-place exclusive prefix of a[0..n) by one CTA of 256 threads.
+__device__ void cta_exclusive_scan(uint32_t* a, int64_t n) {
+  __shared__ uint32_t part[256];
+  const int t = threadIdx.x;
+  const int64_t per = (n + 255) / 256;
+  const int64_t lo = t * per, hi = lo + per < n ? lo + per : n;
+  uint32_t s = 0;
+  for (int64_t i = lo; i < hi; ++i) s += __ldcg(a + i);
+  part[t] = s;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    const uint32_t v = t >= off ? part[t - off] : 0u;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  uint32_t run = part[t] - s;
+  for (int64_t i = lo; i < hi; ++i) {
+    const uint32_t c = __ldcg(a + i);
+    a[i] = run;
+    run += c;
+  }
+}
+
+__global__ void __launch_bounds__(kChunk) count_kernel(const uint64_t* __restrict__ keys, int64_t units, Ctl* ctl,
+                                                       uint32_t* __restrict__ cnt_gt, uint32_t* __restrict__ cnt_eq) {
+  const uint64_t T = ctl->T;
+  const int64_t i = (int64_t)blockIdx.x * kChunk + threadIdx.x;
+  const uint64_t key = i < units ? keys[i] : 0;
+  const int gt = __syncthreads_count(i < units && key > T);
+  const int eq = __syncthreads_count(i < units && key == T);
+  if (threadIdx.x == 0) {
+    cnt_gt[blockIdx.x] = (uint32_t)gt;
+    cnt_eq[blockIdx.x] = (uint32_t)eq;
+  }
+  if (!last_cta(&ctl->ticket[2])) return;
+  cta_exclusive_scan(cnt_gt, gridDim.x);
+  __syncthreads();
+  cta_exclusive_scan(cnt_eq, gridDim.x);
+}
+
+// Exclusive prefix of a per-thread flag over the CTA (kChunk threads).
+__device__ __forceinline__ uint32_t cta_rank(bool f, uint32_t* warp_tot) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t bal = __ballot_sync(0xFFFFFFFFu, f);
+  __syncthreads();
+  if (lane == 0) warp_tot[w] = __popc(bal);
+  __syncthreads();
+  uint32_t before = 0;
+  for (int j = 0; j < w; ++j) before += warp_tot[j];
+  return before + __popc(bal & ((1u << lane) - 1u));
+}
+
+template <int DT, bool BLOCK>
+__global__ void __launch_bounds__(kChunk) write_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_t cols,
+                                                       int64_t ld_bytes, const uint64_t* __restrict__ keys,
+                                                       int64_t units, const Ctl* ctl, const uint32_t* __restrict__ pre_gt,
+                                                       const uint32_t* __restrict__ pre_eq, uint8_t* W_out,
+                                                       int64_t ldo_bytes, uint32_t* __restrict__ mask,
+                                                       int32_t* __restrict__ csr, uint8_t* __restrict__ vals) {
+  constexpr int es = DT == kF16 ? 2 : 1;
+  constexpr int kSegElems = 16 / es;
+  constexpr int kSpr = kUnitW / kSegElems;         // segments per unit row
+  constexpr int kUnitRows = BLOCK ? 32 : 1;
+  constexpr int kSpu = kSpr * kUnitRows;           // segments per unit
+  constexpr int kUnitBytes = kUnitW * kUnitRows * es;
+  __shared__ uint32_t warp_tot[kChunk / 32];
+  const uint64_t T = ctl->T, need_eq = ctl->need_eq;
+  const int64_t upr = cols / kUnitW;  // units per unit row
+  const int64_t urows = units / upr;
+  const int64_t i = (int64_t)blockIdx.x * kChunk + threadIdx.x;
+  const bool valid = i < units;
+  const uint64_t key = valid ? keys[i] : 0;
+  const bool gt = valid && key > T, eq = valid && key == T;
+  const uint64_t eq0 = pre_eq[blockIdx.x], gt0 = pre_gt[blockIdx.x];
+  const uint64_t eq_rank = eq0 + cta_rank(eq, warp_tot);
+  const bool kept = gt || (eq && eq_rank < need_eq);
+  const uint64_t before = gt0 + (eq0 < need_eq ? eq0 : need_eq);
+  const int64_t pos = (int64_t)(before + cta_rank(kept, warp_tot));
+  if (csr != nullptr && valid) {
+    const int64_t ur = i / upr, uc = i - ur * upr;
+    if (uc == 0) csr[ur] = (int32_t)pos;
+    if (i == units - 1) csr[urows] = (int32_t)(pos + (kept ? 1 : 0));
+    if (kept) csr[urows + 1 + pos] = (int32_t)uc;
+  }
+  // Data movement: each warp handles its 32 units, 16-byte segments spread
+  // over the lanes.
+  const int lane = threadIdx.x & 31;
+  if (mask != nullptr) {
+    const int64_t mw = cols / 32;  // mask words per row
+    if (!BLOCK) {
+      if (valid) mask[i] = kept ? 0xFFFFFFFFu : 0u;  // a 32-column vector is one mask word
+    } else {
+      for (int k = 0; k < 32; ++k) {
+        const int64_t u = i - lane + k;
+        const bool kv = __shfl_sync(0xFFFFFFFFu, kept, k);
+        if (u < units) {
+          const int64_t bi = u / upr, bj = u - bi * upr;
+          mask[(bi * 32 + lane) * mw + bj] = kv ? 0xFFFFFFFFu : 0u;
+        }
+      }
+    }
+  }
+  if (W_out == nullptr && vals == nullptr) return;
+  if (!BLOCK) {
+#pragma unroll
+    for (int it = 0; it < kSpu; ++it) {
+      const int g = it * 32 + lane;
+      const int k = g / kSpu, part = g % kSpu;
+      const bool kv = __shfl_sync(0xFFFFFFFFu, kept, k);
+      const int64_t kp = (int64_t)__shfl_sync(0xFFFFFFFFu, (long long)pos, k);
+      const int64_t u = i - lane + k;
+      if (u >= units) continue;
+      const int64_t r = u / upr, c = u - r * upr;
+      const int64_t col_b = (c * kUnitW + part * kSegElems) * es;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (kv) v = *reinterpret_cast<const uint4*>(W + r * ld_bytes + col_b);
+      if (W_out != nullptr) *reinterpret_cast<uint4*>(W_out + r * ldo_bytes + col_b) = v;
+      if (kv && vals != nullptr) *reinterpret_cast<uint4*>(vals + kp * kUnitBytes + part * 16) = v;
+    }
+  } else {
+    for (int k = 0; k < 32; ++k) {
+      const bool kv = __shfl_sync(0xFFFFFFFFu, kept, k);
+      const int64_t kp = (int64_t)__shfl_sync(0xFFFFFFFFu, (long long)pos, k);
+      const int64_t u = i - lane + k;
+      if (u >= units) break;  // uniform across the warp
+      if (!kv && W_out == nullptr) continue;
+      const int64_t bi = u / upr, bj = u - bi * upr;
+#pragma unroll
+      for (int it = 0; it < kSpu / 32; ++it) {
+        const int g = it * 32 + lane;
+        const int rr = g / kSpr, part = g % kSpr;
+        const int64_t row = bi * 32 + rr;
+        const int64_t col_b = (bj * kUnitW + part * kSegElems) * es;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (kv) v = *reinterpret_cast<const uint4*>(W + row * ld_bytes + col_b);
+        if (W_out != nullptr) *reinterpret_cast<uint4*>(W_out + row * ldo_bytes + col_b) = v;
+        if (kv && vals != nullptr) *reinterpret_cast<uint4*>(vals + kp * kUnitBytes + g * 16) = v;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- product
+__device__ __forceinline__ float h2f(uint32_t b, int bf16) {
+  return bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((uint16_t)b));
+}
+__device__ __forceinline__ uint16_t f2h(float x, int bf16) {
+  return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
+}
+template <int NB>
+__device__ __forceinline__ void dot8(const uint4 a, const uint16_t* x, int64_t ldb, int nb, int bf16, float* acc) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+  float af[8];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    af[2 * t] = h2f(aw[t] & 0xFFFFu, bf16);
+    af[2 * t + 1] = h2f(aw[t] >> 16, bf16);
+  }
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if (b < nb) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + b * ldb));
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        acc[b] = fmaf(af[2 * t], h2f(xw[t] & 0xFFFFu, bf16), acc[b]);
+        acc[b] = fmaf(af[2 * t + 1], h2f(xw[t] >> 16, bf16), acc[b]);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void store_d(const SpmmLaunch& a, int64_t r, int64_t b, float x, int bf16) {
+  const nm_spmm_desc_t& d = a.d;
+  const bool col = d.order_cd == NM_COL;
+  x *= a.alpha_f;
+  if (a.C != nullptr) {
+    const uint16_t* C = static_cast<const uint16_t*>(a.C);
+    x = fmaf(a.beta_f, h2f(C[col ? b * d.ldc + r : r * d.ldc + b], bf16), x);
+  }
+  static_cast<uint16_t*>(a.D)[col ? b * d.ldd + r : r * d.ldd + b] = f2h(x, bf16);
+}
+
+// Vector-wise: a warp per row; 8 kept vectors per step, 4 lanes per vector.
+template <int NB>
+__global__ void __launch_bounds__(256) vw_spmv_kernel(const SpmmLaunch a) {
+  const nm_spmm_desc_t& d = a.d;
+  const int bf16 = d.ab_type == NM_BF16;
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= d.M) return;
+  const int32_t* csr = static_cast<const int32_t*>(a.A_meta);
+  const int32_t* colidx = csr + d.M + 1;
+  const uint16_t* vals = static_cast<const uint16_t*>(a.A);
+  const uint16_t* B = static_cast<const uint16_t*>(a.B);
+  const int p0 = csr[r], p1 = csr[r + 1];
+  const int q = lane >> 2, part = lane & 3;
+  for (int64_t b0 = 0; b0 < d.N; b0 += NB) {
+    const int nb = (int)(d.N - b0 < NB ? d.N - b0 : NB);
+    float acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
+    for (int p = p0 + q; p < p1; p += 8) {
+      const int64_t c = colidx[p];
+      const uint4 av = __ldcs(reinterpret_cast<const uint4*>(vals + (int64_t)p * kUnitW + part * 8));
+      dot8<NB>(av, B + b0 * d.ldb + c * kUnitW + part * 8, d.ldb, nb, bf16, acc);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) acc[b] += __shfl_xor_sync(0xFFFFFFFFu, acc[b], m);
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      if (lane == b && b < nb) store_d(a, r, b0 + b, acc[b], bf16);
+  }
+}
+
+// Block-wise: a CTA per block row; its 8 warps split the kept blocks.  Lane l
+// covers columns 8*(l%4)..+7 of block rows l/4 + 8j, j = 0..3, so that every
+// warp load reads 512 contiguous bytes of a block.
+template <int NB>
+__global__ void __launch_bounds__(256) bw_spmv_kernel(const SpmmLaunch a) {
+  const nm_spmm_desc_t& d = a.d;
+  const int bf16 = d.ab_type == NM_BF16;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t bi = blockIdx.x;
+  const int64_t brows = d.M / 32;
+  const int32_t* csr = static_cast<const int32_t*>(a.A_meta);
+  const int32_t* colidx = csr + brows + 1;
+  const uint16_t* vals = static_cast<const uint16_t*>(a.A);
+  const uint16_t* B = static_cast<const uint16_t*>(a.B);
+  const int p0 = csr[bi], p1 = csr[bi + 1];
+  const int part = lane & 3, rq = lane >> 2;
+  __shared__ float red[8][32][NB];
+  for (int64_t b0 = 0; b0 < d.N; b0 += NB) {
+    const int nb = (int)(d.N - b0 < NB ? d.N - b0 : NB);
+    float acc[4][NB];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc[j][b] = 0.0f;
+    for (int p = p0 + w; p < p1; p += 8) {
+      const int64_t c = colidx[p];
+      const uint16_t* blk = vals + (int64_t)p * 1024;
+      uint4 av[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) av[j] = __ldcs(reinterpret_cast<const uint4*>(blk + (rq + 8 * j) * 32 + part * 8));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dot8<NB>(av[j], B + b0 * d.ldb + c * kUnitW + part * 8, d.ldb, nb, bf16, acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        float v = acc[j][b];
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+        if (part == 0) red[w][rq + 8 * j][b] = v;
+      }
+    __syncthreads();
+    for (int t = threadIdx.x; t < 32 * NB; t += blockDim.x) {
+      const int row = t / NB, b = t - row * NB;
+      if (b < nb) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s += red[k][row][b];
+        store_d(a, bi * 32 + row, b0 + b, s, bf16);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <int DT>
+cudaError_t launch_blocks_dt(const BlocksLaunch& a, const WsLayout& L, cudaStream_t s) {
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  Ctl* ctl = reinterpret_cast<Ctl*>(ws + L.ctl);
+  uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.keys);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(ws + L.cand);
+  uint32_t* cgt = reinterpret_cast<uint32_t*>(ws + L.cnt_gt);
+  uint32_t* ceq = reinterpret_cast<uint32_t*>(ws + L.cnt_eq);
+  constexpr int es = DT == kF16 ? 2 : 1;
+  const int64_t units = a.units;
+  const int64_t chunks = (units + kChunk - 1) / kChunk;
+  const uint8_t* W = static_cast<const uint8_t*>(a.W);
+  if (cudaError_t e = cudaMemsetAsync(ws, 0, L.keys, s)) return e;  // histogram + control block
+  if (a.bh == 1) {
+    const int64_t segs = a.rows * (a.cols * es / 16);
+    vw_score_kernel<DT><<<grid_for(segs, 256, 4), 256, 0, s>>>(W, a.rows, a.cols, a.ld * es, a.abs_of_sum, keys, hist,
+                                                                ctl, (uint64_t)a.keep);
+  } else {
+    bw_score_kernel<DT><<<grid_for(units * 32, 256, 4), 256, 0, s>>>(W, a.rows, a.cols, a.ld * es, keys, hist, ctl,
+                                                                      (uint64_t)a.keep);
+  }
+  candidates_kernel<<<grid_for(units, 256, 4), 256, 0, s>>>(keys, units, ctl, cand);
+  count_kernel<<<(unsigned)chunks, kChunk, 0, s>>>(keys, units, ctl, cgt, ceq);
+  if (a.bh == 1) {
+    write_kernel<DT, false><<<(unsigned)chunks, kChunk, 0, s>>>(
+        W, a.rows, a.cols, a.ld * es, keys, units, ctl, cgt, ceq, static_cast<uint8_t*>(a.W_out), a.ld_out * es,
+        a.mask_bits, a.csr, static_cast<uint8_t*>(a.vals));
+  } else {
+    write_kernel<DT, true><<<(unsigned)chunks, kChunk, 0, s>>>(
+        W, a.rows, a.cols, a.ld * es, keys, units, ctl, cgt, ceq, static_cast<uint8_t*>(a.W_out), a.ld_out * es,
+        a.mask_bits, a.csr, static_cast<uint8_t*>(a.vals));
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t blocks_workspace(int64_t units) { return ws_layout(units).total; }
+
+cudaError_t launch_blocks(const BlocksLaunch& a, cudaStream_t s) {
+  const WsLayout L = ws_layout(a.units);
+  if (a.units == 0) {
+    if (a.csr != nullptr) return cudaMemsetAsync(a.csr, 0, (size_t)(a.unit_rows + 1) * 4, s);
+    return cudaSuccess;
+  }
+  return a.dt == kF16 ? launch_blocks_dt<kF16>(a, L, s) : launch_blocks_dt<kI8>(a, L, s);
+}
+
+cudaError_t launch_spmm_blocks(const SpmmLaunch& a, cudaStream_t s) {
+  const nm_spmm_desc_t& d = a.d;
+  if (d.n == 1) {
+    const unsigned grid = (unsigned)((d.M + 7) / 8);
+    if (d.N == 1)
+      vw_spmv_kernel<1><<<grid, 256, 0, s>>>(a);
+    else
+      vw_spmv_kernel<8><<<grid, 256, 0, s>>>(a);
+  } else {
+    const unsigned grid = (unsigned)(d.M / 32);
+    if (d.N == 1)
+      bw_spmv_kernel<1><<<grid, 256, 0, s>>>(a);
+    else
+      bw_spmv_kernel<8><<<grid, 256, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace nmk

@@ -58,7 +58,27 @@ struct TransposableLaunch {
 };
 cudaError_t launch_transposable(const TransposableLaunch& a, cudaStream_t s);
 
-// ---- products (nm_spmm_tc.cu, nm_spmm_cc.cu) ---------------------------
+// ---- vector-wise / block-wise selection (nm_blocks.cu) -------------------
+// Units are 1 x 32 vectors (bh = 1) or 32 x 32 blocks (bh = 32) in row-major order.
+struct BlocksLaunch {
+  int dt;  // kF16 or kI8
+  const void* W;
+  int64_t rows, cols, ld;
+  int bh;
+  int64_t units, unit_rows;  // unit_rows = rows / bh
+  int64_t keep;
+  int abs_of_sum;  // vector-wise score: 1 = |sum w|, 0 = sum |w|
+  void* W_out;
+  int64_t ld_out;
+  uint32_t* mask_bits;
+  int32_t* csr;
+  void* vals;
+  void* ws;
+};
+size_t blocks_workspace(int64_t units);
+cudaError_t launch_blocks(const BlocksLaunch& a, cudaStream_t s);
+
+// ---- products (nm_spmm_tc.cu, nm_spmm_cc.cu, nm_blocks.cu) ---------------
 struct SpmmLaunch {
   nm_spmm_desc_t d;
   const void* A;
@@ -82,5 +102,7 @@ int spmm_tc_dense_masked_split(const nm_spmm_desc_t& d);
 // CUDA-core paths: n:m gather (any m <= 32) and 2:4 int8 (mma.sp).
 cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s);
 cudaError_t launch_spmm_i8(const SpmmLaunch& a, cudaStream_t s);
+// CUDA-core product over kept 1 x 32 vectors (n = 1) or 32 x 32 blocks (n = 32).
+cudaError_t launch_spmm_blocks(const SpmmLaunch& a, cudaStream_t s);
 
 }  // namespace nmk

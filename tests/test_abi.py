@@ -105,6 +105,40 @@ def test_other_calls_reject_bad_arguments(lib):
                                     None) == nb.NM_ERR_UNSUPPORTED)
 
 
+def test_unit_pruning_rejects_bad_arguments(lib):
+    L = lib
+    ws = ctypes.c_size_t()
+    assert L.nm_prune_units_workspace(64, 128, 1, 32, ctypes.byref(ws)) == nb.NM_OK and ws.value > 256 * 8
+    assert L.nm_prune_units_workspace(64, 128, 1, 16, ctypes.byref(ws)) == nb.NM_ERR_UNSUPPORTED
+    assert L.nm_prune_units_workspace(48, 128, 32, 32, ctypes.byref(ws)) == nb.NM_ERR_INVALID_ARG  # rows % 32
+    assert L.nm_prune_units_workspace(0, 128, 1, 32, ctypes.byref(ws)) == nb.NM_OK and ws.value == 0
+    big = 1 << 40
+
+    def vw(**kw):
+        a = dict(W=FAKE, rows=64, cols=128, ld=128, dt=nb.NM_F16, v=32, keep=64, score=0, W_out=None, ld_out=0,
+                 mask=None, csr=FAKE, vals=None, ws=FAKE, wsb=big)
+        a.update(kw)
+        return L.nm_prune_vector_wise(a["W"], a["rows"], a["cols"], a["ld"], a["dt"], a["v"], a["keep"], a["score"],
+                                      a["W_out"], a["ld_out"], a["mask"], a["csr"], a["vals"], a["ws"], a["wsb"],
+                                      None)
+
+    assert vw(dt=nb.NM_BF16) == nb.NM_ERR_UNSUPPORTED  # scores would not be exact
+    assert vw(v=64) == nb.NM_ERR_UNSUPPORTED
+    assert vw(cols=112, ld=112) == nb.NM_ERR_INVALID_ARG
+    assert vw(keep=257) == nb.NM_ERR_INVALID_ARG
+    assert vw(keep=-1) == nb.NM_ERR_INVALID_ARG
+    assert vw(score=2) == nb.NM_ERR_INVALID_ARG
+    assert vw(wsb=16) == nb.NM_ERR_INVALID_ARG
+    assert vw(ws=None) == nb.NM_ERR_INVALID_ARG
+    assert vw(ld=132) == nb.NM_ERR_MISALIGNED
+    assert vw(vals=FAKE + 4) == nb.NM_ERR_MISALIGNED
+    assert vw(W_out=FAKE, ld_out=136) == nb.NM_ERR_INVALID_ARG  # aliases W with another ld
+    assert (L.nm_prune_block_wise(FAKE, 64, 128, 128, nb.NM_F16, 1, 32, 1, None, 0, None, None, None, FAKE, big, None)
+            == nb.NM_ERR_UNSUPPORTED)
+    assert (L.nm_prune_block_wise(FAKE, 64, 128, 128, nb.NM_I8, 32, 32, 9, None, 0, None, None, None, FAKE, big, None)
+            == nb.NM_ERR_INVALID_ARG)  # 8 blocks
+
+
 def plan_status(**kw):
     d = nb.make_desc(**kw)
     h = ctypes.c_void_p()
@@ -130,6 +164,13 @@ def test_plan_validation(lib):
     assert plan_status(**{**dense, "lda": 100}) == nb.NM_ERR_INVALID_ARG
     assert plan_status(**{**dense, "mode": 7}) == nb.NM_ERR_INVALID_ARG
     assert plan_status(M=-1, N=1, K=32, ab_type="f16", cd_type="f16", ldb=32, ldd=8) == nb.NM_ERR_INVALID_ARG
+    units = dict(M=256, N=8, K=1024, mode=nb.NM_SPMM_BLOCK_SPARSE_A, n=1, m=32, ab_type="f16", cd_type="f16",
+                 ldb=1024, ldd=256)
+    assert plan_status(**units) == nb.NM_OK
+    assert plan_status(**{**units, "n": 32}) == nb.NM_OK
+    assert plan_status(**{**units, "n": 16}) == nb.NM_ERR_UNSUPPORTED
+    assert plan_status(**{**units, "n": 32, "M": 240}) == nb.NM_ERR_INVALID_ARG
+    assert plan_status(**{**units, "ab_type": "i8", "cd_type": "i32"}) == nb.NM_ERR_UNSUPPORTED
 
 
 def test_spmm_rejects_bad_pointers(lib):

@@ -411,3 +411,36 @@ def test_vw_bw_csr_matches_sorted_lists():
     bidx, bvals = o.block_wise_compress(W, mb, 32, 32)
     assert (np.repeat(np.arange(2), np.diff(bcsr[:3])) * 4 + bcsr[3:] == bidx).all()
     assert (blocks == bvals).all()
+
+
+def test_vw_bw_special_values_rank():
+    # float64 ordering read for the unspecified cases: Inf above every number,
+    # NaN below every number (0 included); ties by the lower index.
+    Z = np.zeros((1, 6 * 32), np.float16)
+    Z[0, 0] = np.nan                       # vector 0: NaN
+    Z[0, 32] = np.inf                      # vector 1: +Inf
+    Z[0, 64], Z[0, 65] = np.inf, -np.inf   # vector 2: +Inf + -Inf = NaN (signed sum) / Inf (sum of |w|)
+    Z[0, 96] = 1.0                         # vector 3: 1
+    Z[0, 128] = -np.inf                    # vector 4: |-Inf| = Inf
+    # vector 5: all zeros, score 0
+    bits = Z.view(np.uint16)
+    kept = lambda m: list(np.nonzero(m.reshape(-1, 32)[:, 0])[0])
+    assert kept(o.vector_wise_mask(bits, "f16", 3 / 6, 32)) == [1, 3, 4]
+    assert kept(o.vector_wise_mask(bits, "f16", 4 / 6, 32)) == [1, 3, 4, 5]
+    assert kept(o.vector_wise_mask(bits, "f16", 5 / 6, 32)) == [0, 1, 3, 4, 5]
+    assert kept(o.vector_wise_mask(bits, "f16", 3 / 6, 32, score="sum_of_abs")) == [1, 2, 4]
+    B = np.zeros((2, 4), np.float16)
+    B[0, 0] = np.nan
+    B[1, 3] = np.inf
+    mb = o.block_wise_mask(B.view(np.uint16), "f16", 2 / 4, 1, 2)
+    assert list(np.nonzero(mb[:, ::2].reshape(-1))[0]) == [1, 3]  # zero block 1 beats the NaN block 0
+
+
+def test_vw_int8_scores():
+    W = np.zeros((1, 96), np.int8)
+    W[0, 0], W[0, 1] = -128, 127           # signed sum -1, sum of |w| 255
+    W[0, 32] = 100                         # 100
+    W[0, 64:66] = -60                      # -120 -> 120
+    kept = lambda m: list(np.nonzero(m.reshape(-1, 32)[:, 0])[0])
+    assert kept(o.vector_wise_mask(W, "i8", 1 / 3, 32)) == [2]
+    assert kept(o.vector_wise_mask(W, "i8", 1 / 3, 32, score="sum_of_abs")) == [0]
