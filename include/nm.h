@@ -79,6 +79,10 @@ const char* nm_status_string(nm_status_t status);
 /* Library ABI version, currently 1. */
 int nm_version(void);
 
+/* Text of the CUDA runtime error behind the calling thread's most recent
+ * NM_ERR_CUDA (static string, never NULL; "no CUDA error" if there was none). */
+const char* nm_last_cuda_error(void);
+
 /*
  * nm_compressed_size - host-only size query (cuSPARSELt blog, code example,
  * cusparseLtSpMMACompressedSize before the compressed buffer is allocated).

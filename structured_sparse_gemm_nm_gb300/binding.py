@@ -27,7 +27,7 @@ DTYPE_NAMES = {"f16": NM_F16, "bf16": NM_BF16, "i8": NM_I8, "f32": NM_F32, "i32"
 
 # Every symbol include/nm.h declares.
 EXPORTED = (
-    "nm_status_string", "nm_version", "nm_compressed_size", "nm_prune", "nm_compress", "nm_decompress",
+    "nm_status_string", "nm_version", "nm_last_cuda_error", "nm_compressed_size", "nm_prune", "nm_compress", "nm_decompress",
     "nm_check", "nm_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
     "nm_prune_block_wise", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm",
 )
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.nm_status_string.argtypes = [i32]
         L.nm_version.restype = i32
         L.nm_version.argtypes = []
+        L.nm_last_cuda_error.restype = ctypes.c_char_p
+        L.nm_last_cuda_error.argtypes = []
         sigs = {
             "nm_compressed_size": [i64, i64, i32, i32, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)],
             "nm_prune": [vp, i64, i64, i64, i32, i32, i32, vp, i64, vp, vp],
@@ -119,6 +121,8 @@ def _dt(d) -> int:
 
 def _check(st: int, where: str) -> None:
     if st != NM_OK:
+        if st == NM_ERR_CUDA:
+            where = f"{where} ({lib().nm_last_cuda_error().decode()})"
         raise NmError(st, where)
 
 

@@ -21,7 +21,14 @@ int64_t elem_size(nm_dtype_t t) {
   return 0;
 }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-nm_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? NM_OK : NM_ERR_CUDA; }
+// The CUDA error behind the calling thread's last NM_ERR_CUDA.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+nm_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return NM_OK;
+  g_last_cuda_error = e;
+  return NM_ERR_CUDA;
+}
 
 nm_status_t check_nm(int n, int m) {
   if (m < 2 || m > 32 || n < 1 || n >= m) return NM_ERR_INVALID_ARG;
@@ -65,6 +72,10 @@ const char* nm_status_string(nm_status_t s) {
 }
 
 int nm_version(void) { return 1; }
+
+const char* nm_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda_error);
+}
 
 nm_status_t nm_compressed_size(int64_t rows, int64_t cols, nm_dtype_t dtype, int n, int m, nm_meta_layout_t layout,
                                size_t* vals_bytes, size_t* meta_bytes) {

@@ -251,8 +251,11 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int cl, int 
 }
 
 // ----------------------------------------------------------------- kernel
+// 14 warps are resident as 16 for register allocation (warps are allocated in
+// groups of four), so 128 registers per thread is the most that still fits
+// the 64K-register file.
 template <bool SPARSE, int CL>
-__global__ void __maxnreg__(144)
+__global__ void __maxnreg__(128)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const Params p) {
   using C = Cfg<SPARSE>;

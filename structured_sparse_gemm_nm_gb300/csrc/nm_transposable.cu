@@ -54,7 +54,62 @@ __device__ __forceinline__ float tile_mag(typename Elem<DT>::T v) {
   }
 }
 
-template <int DT>
+// Four consecutive elements of a tile row in one access (VEC: 8 bytes for
+// 16-bit types, 4 for int8), or element by element.
+template <bool VEC>
+__device__ __forceinline__ void load4(const uint16_t* p, uint16_t (&o)[4]) {
+  if constexpr (VEC) {
+    const uint2 q = *reinterpret_cast<const uint2*>(p);
+    o[0] = (uint16_t)q.x, o[1] = (uint16_t)(q.x >> 16), o[2] = (uint16_t)q.y, o[3] = (uint16_t)(q.y >> 16);
+  } else {
+    for (int c = 0; c < 4; ++c) o[c] = p[c];
+  }
+}
+template <bool VEC>
+__device__ __forceinline__ void load4(const int8_t* p, int8_t (&o)[4]) {
+  if constexpr (VEC) {
+    const uint32_t q = *reinterpret_cast<const uint32_t*>(p);
+    for (int c = 0; c < 4; ++c) o[c] = (int8_t)(q >> (8 * c));
+  } else {
+    for (int c = 0; c < 4; ++c) o[c] = p[c];
+  }
+}
+template <bool VEC>
+__device__ __forceinline__ void store4(uint16_t* p, const uint16_t (&o)[4]) {
+  if constexpr (VEC) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(o[0] | ((uint32_t)o[1] << 16), o[2] | ((uint32_t)o[3] << 16));
+  } else {
+    for (int c = 0; c < 4; ++c) p[c] = o[c];
+  }
+}
+template <bool VEC>
+__device__ __forceinline__ void store4(int8_t* p, const int8_t (&o)[4]) {
+  if constexpr (VEC) {
+    uint32_t q = 0;
+    for (int c = 0; c < 4; ++c) q |= (uint32_t)(uint8_t)o[c] << (8 * c);
+    *reinterpret_cast<uint32_t*>(p) = q;
+  } else {
+    for (int c = 0; c < 4; ++c) p[c] = o[c];
+  }
+}
+template <bool VEC>
+__device__ __forceinline__ void store2(uint16_t* p, uint16_t a, uint16_t b) {
+  if constexpr (VEC) {
+    *reinterpret_cast<uint32_t*>(p) = a | ((uint32_t)b << 16);
+  } else {
+    p[0] = a, p[1] = b;
+  }
+}
+template <bool VEC>
+__device__ __forceinline__ void store2(int8_t* p, int8_t a, int8_t b) {
+  if constexpr (VEC) {
+    *reinterpret_cast<uint16_t*>(p) = (uint16_t)((uint8_t)a | ((uint32_t)(uint8_t)b << 8));
+  } else {
+    p[0] = a, p[1] = b;
+  }
+}
+
+template <int DT, bool VEC>
 __global__ void __launch_bounds__(256) transposable_kernel(const typename Elem<DT>::T* __restrict__ W, int64_t rows,
                                                            int64_t cols, int64_t ld, typename Elem<DT>::T* W_out,
                                                            int64_t ld_out, uint32_t* __restrict__ mask_bits,
@@ -77,9 +132,14 @@ __global__ void __launch_bounds__(256) transposable_kernel(const typename Elem<D
     const bool valid = R0 < rows && C0 < cols;
     T v[4][4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < 4; ++r) {
+      if (valid) {
+        load4<VEC>(W + (R0 + r) * ld + C0, v[r]);
+      } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) v[r][c] = valid ? W[(R0 + r) * ld + C0 + c] : (T)0;
+        for (int c = 0; c < 4; ++c) v[r][c] = (T)0;
+      }
+    }
     float p[4][6];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -118,9 +178,12 @@ __global__ void __launch_bounds__(256) transposable_kernel(const typename Elem<D
     // ---- pruned copy
     if (W_out != nullptr && valid) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < 4; ++r) {
+        T o[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) W_out[(R0 + r) * ld_out + C0 + c] = ((bmask >> (4 * r + c)) & 1u) ? v[r][c] : (T)0;
+        for (int c = 0; c < 4; ++c) o[c] = ((bmask >> (4 * r + c)) & 1u) ? v[r][c] : (T)0;
+        store4<VEC>(W_out + (R0 + r) * ld_out + C0, o);
+      }
     }
     // ---- mask bits: 8 lanes of a tile row form one 32-bit word per row
     if (mask_bits != nullptr) {
@@ -141,9 +204,8 @@ __global__ void __launch_bounds__(256) transposable_kernel(const typename Elem<D
         const uint32_t i0 = (km & 1u) ? 0u : ((km & 2u) ? 1u : 2u);
         const uint32_t i1 = (km & 8u) ? 3u : ((km & 4u) ? 2u : 1u);
         if (vals != nullptr && valid) {
-          T* o = vals + (R0 + r) * (cols / 2) + C0 / 2;
-          o[0] = (km & 1u) ? v[r][0] : ((km & 2u) ? v[r][1] : v[r][2]);
-          o[1] = (km & 8u) ? v[r][3] : ((km & 4u) ? v[r][2] : v[r][1]);
+          store2<VEC>(vals + (R0 + r) * (cols / 2) + C0 / 2, (km & 1u) ? v[r][0] : ((km & 2u) ? v[r][1] : v[r][2]),
+                      (km & 8u) ? v[r][3] : ((km & 4u) ? v[r][2] : v[r][1]));
         }
         if (meta != nullptr) {
           uint32_t code = valid ? (i0 | (i1 << 2)) << (4 * (tcol & 3)) : 0u;
@@ -168,9 +230,8 @@ __global__ void __launch_bounds__(256) transposable_kernel(const typename Elem<D
         const uint32_t i0 = (km & 1u) ? 0u : ((km & 2u) ? 1u : 2u);
         const uint32_t i1 = (km & 8u) ? 3u : ((km & 4u) ? 2u : 1u);
         if (valsT != nullptr && valid) {
-          T* o = valsT + (C0 + c) * (rows / 2) + R0 / 2;
-          o[0] = (km & 1u) ? v[0][c] : ((km & 2u) ? v[1][c] : v[2][c]);
-          o[1] = (km & 8u) ? v[3][c] : ((km & 4u) ? v[2][c] : v[1][c]);
+          store2<VEC>(valsT + (C0 + c) * (rows / 2) + R0 / 2, (km & 1u) ? v[0][c] : ((km & 2u) ? v[1][c] : v[2][c]),
+                      (km & 8u) ? v[3][c] : ((km & 4u) ? v[2][c] : v[1][c]));
         }
         if (metaT != nullptr) {
           // four tile rows of the block share one 16-bit word: lanes tcol, tcol+8, tcol+16, tcol+24
@@ -211,10 +272,21 @@ cudaError_t transposable_dt(const TransposableLaunch& a, cudaStream_t s) {
   }
   const int64_t nblocks = ((a.rows + 15) / 16) * ((a.cols + 31) / 32);
   const unsigned grid = grid_for(nblocks * 32, 256);
-  transposable_kernel<DT><<<grid, 256, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
-                                               static_cast<T*>(a.W_out), a.ld_out, a.mask_bits,
-                                               static_cast<T*>(a.vals), a.meta, static_cast<T*>(a.valsT), a.metaT,
-                                               a.meta_tc);
+  // Vector accesses need 4-element rows aligned (W, W_out) and 2-element pairs aligned (vals, valsT).
+  const uintptr_t a4 = 4 * sizeof(T), a2 = 2 * sizeof(T);
+  const bool vec = (reinterpret_cast<uintptr_t>(a.W) % a4) == 0 && a.ld % 4 == 0 &&
+                   (a.W_out == nullptr || ((reinterpret_cast<uintptr_t>(a.W_out) % a4) == 0 && a.ld_out % 4 == 0)) &&
+                   (reinterpret_cast<uintptr_t>(a.vals) % a2) == 0 && (reinterpret_cast<uintptr_t>(a.valsT) % a2) == 0;
+  if (vec)
+    transposable_kernel<DT, true><<<grid, 256, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
+                                                       static_cast<T*>(a.W_out), a.ld_out, a.mask_bits,
+                                                       static_cast<T*>(a.vals), a.meta, static_cast<T*>(a.valsT),
+                                                       a.metaT, a.meta_tc);
+  else
+    transposable_kernel<DT, false><<<grid, 256, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
+                                                        static_cast<T*>(a.W_out), a.ld_out, a.mask_bits,
+                                                        static_cast<T*>(a.vals), a.meta, static_cast<T*>(a.valsT),
+                                                        a.metaT, a.meta_tc);
   return cudaGetLastError();
 }
 

@@ -68,7 +68,7 @@ def run_units(W, rows, cols, dtype, bh, keep, score="abs_of_sum", ld=None, in_pl
                                csr=csr, vals=vals, workspace=ws, workspace_bytes=wsb)
     torch.cuda.synchronize()
     got_w = bits_of(Wo, dtype, (rows, ld))
-    return dict(W_out=got_w, mask=u32(mask, rows * (cols // 32)).reshape(rows, cols // 32),
+    return dict(W_out=got_w, in_place=in_place, mask=u32(mask, rows * (cols // 32)).reshape(rows, cols // 32),
                 csr=u32(csr, urows + 1 + keep).view(np.int32),
                 vals=bits_of(vals, dtype, (keep * bh * 32,)) if keep else np.zeros(0, W.dtype), pad=pad, units=units)
 
@@ -87,8 +87,13 @@ def check_against_oracle(W, rows, cols, dtype, bh, density, score, got, ld):
     assert (got["csr"] == csr).all(), "csr"
     assert (got["vals"] == vals.reshape(-1)).all(), "vals"
     assert (got["W_out"][:, :cols] == np.where(mask, W, 0)).all(), "pruned copy"
-    if ld > cols:
-        assert (got["W_out"][:, cols:] == got["pad"][:, cols:]).all(), "padding touched"
+    if ld > cols:  # the columns past `cols` keep what was there: W's padding in place, else the 0xAB fill
+        if got["in_place"]:
+            before = got["pad"][:, cols:]
+        else:
+            before = np.full((rows, ld - cols), 0xAB, np.uint8).view(np.int8) if dtype == "i8" else \
+                np.full((rows, ld - cols), 0xABAB, np.uint16)
+        assert (got["W_out"][:, cols:] == before).all(), "padding touched"
 
 
 UNIT_CASES = [
