@@ -272,7 +272,8 @@ nm_status_t nm_spmm_plan_destroy(nm_spmm_plan_t plan);
  * 0).  d_status (nullable, device int32): set to NM_ERR_TIMEOUT if a bounded
  * pipeline wait gave up; it is not cleared by the call.
  * Base pointers must be 16-byte aligned and leading dimensions multiples of
- * 16 bytes (NM_ERR_MISALIGNED).
+ * 16 bytes (NM_ERR_MISALIGNED); for the CUDA-core products (SPARSE_A with
+ * (n, m) != (2, 4), BLOCK_SPARSE_A) C and D need only element alignment.
  */
 nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const void* A_meta, const void* B,
                     const void* beta, const void* C, void* D, void* workspace, size_t workspace_bytes,

@@ -314,7 +314,7 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   const int64_t cd_inner = d.order_cd == NM_ROW ? d.N : d.M;
   if (d.ldb < b_inner || d.ldb < 1 || d.ldc < 0 || d.ldd < cd_inner || d.ldd < 1) return NM_ERR_INVALID_ARG;
   if (d.ldc != 0 && d.ldc < cd_inner) return NM_ERR_INVALID_ARG;
-  if ((d.ldb * es) % 16 || (d.ldd * eo) % 16 || (d.ldc * eo) % 16) return NM_ERR_MISALIGNED;
+  if ((d.ldb * es) % 16) return NM_ERR_MISALIGNED;
   int kind = -1;
   if (d.mode == NM_SPMM_SPARSE_A) {
     if (nm_status_t st = check_nm(d.n, d.m)) return st;
@@ -349,6 +349,10 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   } else {
     return NM_ERR_INVALID_ARG;
   }
+  // The tensor-core and int8 kernels write D (and read C) in 16-byte pieces;
+  // the CUDA-core GEMV kernels (kinds 2 and 4) access them element by element.
+  const bool cd_wide = kind != 2 && kind != 4;
+  if (cd_wide && ((d.ldd * eo) % 16 || (d.ldc * eo) % 16)) return NM_ERR_MISALIGNED;
   nm_spmm_plan_s* p = new (std::nothrow) nm_spmm_plan_s;
   if (p == nullptr) return NM_ERR_INVALID_ARG;
   p->d = d;
@@ -391,8 +395,9 @@ nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const
   }
   if (plan->kind == 4 && A_meta == nullptr) return NM_ERR_INVALID_ARG;
   if (!beta_zero && (C == nullptr || d.ldc == 0)) return NM_ERR_INVALID_ARG;
-  if (!aligned(A, 16) || !aligned(A_meta, 16) || !aligned(B, 16) || !aligned(D, 16) ||
-      (!beta_zero && !aligned(C, 16)) || (d_status && !aligned(d_status, 4)))
+  const uintptr_t cd_align = (plan->kind == 2 || plan->kind == 4) ? (uintptr_t)elem_size(d.cd_type) : 16;
+  if (!aligned(A, 16) || !aligned(A_meta, 16) || !aligned(B, 16) || !aligned(D, cd_align) ||
+      (!beta_zero && !aligned(C, cd_align)) || (d_status && !aligned(d_status, 4)))
     return NM_ERR_MISALIGNED;
   if (workspace_bytes < plan->ws_bytes || (plan->ws_bytes > 0 && workspace == nullptr)) return NM_ERR_INVALID_ARG;
   if (workspace != nullptr && !aligned(workspace, 16)) return NM_ERR_MISALIGNED;
