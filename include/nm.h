@@ -209,6 +209,36 @@ nm_status_t nm_prune_block_wise(const void* W, int64_t rows, int64_t cols, int64
                                 int bw, int64_t keep, void* W_out, int64_t ld_out, uint32_t* mask_bits, int32_t* csr,
                                 void* vals, void* workspace, size_t workspace_bytes, nm_stream_t stream);
 
+/*
+ * nm_prune_vector_wise_noalloc - nm_prune_vector_wise without a workspace
+ * argument, for callers that cannot allocate device memory at the time of the
+ * call: code whose device memory is owned and accounted by someone else (a
+ * framework's caching allocator, an inference server that forbids new
+ * allocations once it has started), and latency-critical loops that cannot
+ * afford cudaMalloc's implicit synchronisation or an out-of-memory failure
+ * at run time.  The pages have no counterpart; it is an addition of this
+ * library.
+ *
+ * The scratch lives in a fixed array of device memory inside the library
+ * (about 8 MiB, held on every device that loads the library until the
+ * process exits), so the call allocates nothing.  It handles at most
+ * NM_NOALLOC_MAX_UNITS vectors (rows * cols / v); larger matrices are
+ * rejected with NM_ERR_UNSUPPORTED before anything runs.  Every other
+ * argument, requirement and output is that of nm_prune_vector_wise.
+ *
+ * The first call on a device does a one-time set-up on the current device
+ * (it looks up the array's device address, which may load the library's
+ * device code); make that first call before any stream capture.  All calls on
+ * a device share the one array and each call clears what must start at zero,
+ * so calls must not overlap on the GPU: two calls in flight at the same time
+ * (on different streams, or from different host threads) race on the
+ * scratch and give wrong results.
+ */
+#define NM_NOALLOC_MAX_UNITS 524288
+nm_status_t nm_prune_vector_wise_noalloc(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype,
+                                         int v, int64_t keep, nm_score_t score, void* W_out, int64_t ld_out,
+                                         uint32_t* mask_bits, int32_t* csr, void* vals, nm_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * The product D = alpha * op(A) * op(B) + beta * C  (cuSPARSELt blog, the
  * GEMM paragraph: A is M x K, B is K x N, C and D are M x N; "N" layout =

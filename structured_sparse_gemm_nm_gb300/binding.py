@@ -29,7 +29,7 @@ DTYPE_NAMES = {"f16": NM_F16, "bf16": NM_BF16, "i8": NM_I8, "f32": NM_F32, "i32"
 EXPORTED = (
     "nm_status_string", "nm_version", "nm_last_cuda_error", "nm_compressed_size", "nm_prune", "nm_compress", "nm_decompress",
     "nm_check", "nm_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
-    "nm_prune_block_wise", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm",
+    "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm",
 )
 
 
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             "nm_prune_units_workspace": [i64, i64, i32, i32, ctypes.POINTER(sz)],
             "nm_prune_vector_wise": [vp, i64, i64, i64, i32, i32, i64, i32, vp, i64, vp, vp, vp, vp, sz, vp],
             "nm_prune_block_wise": [vp, i64, i64, i64, i32, i32, i32, i64, vp, i64, vp, vp, vp, vp, sz, vp],
+            "nm_prune_vector_wise_noalloc": [vp, i64, i64, i64, i32, i32, i64, i32, vp, i64, vp, vp, vp, vp],
             "nm_spmm_plan": [ctypes.POINTER(vp), ctypes.POINTER(SpmmDesc)],
             "nm_spmm_plan_workspace": [vp, ctypes.POINTER(sz)],
             "nm_spmm_plan_destroy": [vp],
@@ -184,6 +185,17 @@ def nm_prune_block_wise(W, rows, cols, ld, dtype, bh, bw, keep, W_out=None, ld_o
     _check(lib().nm_prune_block_wise(_ptr(W), rows, cols, ld, _dt(dtype), bh, bw, int(keep), _ptr(W_out), ld_out,
                                      _ptr(mask_bits), _ptr(csr), _ptr(vals), _ptr(workspace), workspace_bytes,
                                      _stream(stream)), "nm_prune_block_wise")
+
+
+NM_NOALLOC_MAX_UNITS = 524288
+
+
+def nm_prune_vector_wise_noalloc(W, rows, cols, ld, dtype, v, keep, score=NM_SCORE_ABS_OF_SUM, W_out=None, ld_out=0,
+                                 mask_bits=None, csr=None, vals=None, stream=None):
+    """nm_prune_vector_wise with the library's fixed scratch instead of a caller workspace."""
+    _check(lib().nm_prune_vector_wise_noalloc(_ptr(W), rows, cols, ld, _dt(dtype), v, int(keep), int(score),
+                                              _ptr(W_out), ld_out, _ptr(mask_bits), _ptr(csr), _ptr(vals),
+                                              _stream(stream)), "nm_prune_vector_wise_noalloc")
 
 
 class SpmmPlan:

@@ -296,6 +296,25 @@ nm_status_t nm_prune_block_wise(const void* W, int64_t rows, int64_t cols, int64
                      workspace_bytes, stream);
 }
 
+nm_status_t nm_prune_vector_wise_noalloc(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype,
+                                         int v, int64_t keep, nm_score_t score, void* W_out, int64_t ld_out,
+                                         uint32_t* mask_bits, int32_t* csr, void* vals, nm_stream_t stream) {
+  if (score != NM_SCORE_ABS_OF_SUM && score != NM_SCORE_SUM_OF_ABS) return NM_ERR_INVALID_ARG;
+  int64_t units = 0;
+  if (nm_status_t st = units_shape(rows, cols, 1, v, &units)) return st;
+  if (units > nmk::fixed_scratch_units()) return NM_ERR_UNSUPPORTED;
+  // cheap checks first, so that a rejected call touches no CUDA state
+  if (!is_elem(dtype) || keep < 0 || keep > units || (W == nullptr && units > 0)) return NM_ERR_INVALID_ARG;
+  if (dtype == NM_BF16) return NM_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  size_t bytes = 0;
+  if (units > 0) {
+    if (nm_status_t st = from_cuda(nmk::fixed_scratch(&scratch, &bytes))) return st;
+  }
+  return prune_units(W, rows, cols, ld, dtype, 1, v, keep, score == NM_SCORE_ABS_OF_SUM, W_out, ld_out, mask_bits,
+                     csr, vals, scratch, bytes, stream);
+}
+
 // ------------------------------------------------------------------ products
 nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   if (plan == nullptr || desc == nullptr) return NM_ERR_INVALID_ARG;

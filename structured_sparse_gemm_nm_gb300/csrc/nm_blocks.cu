@@ -25,6 +25,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "nm_device.cuh"
 #include "nm_internal.h"
 
@@ -642,6 +644,36 @@ cudaError_t launch_blocks_dt(const BlocksLaunch& a, const WsLayout& L, cudaStrea
 }  // namespace
 
 size_t blocks_workspace(int64_t units) { return ws_layout(units).total; }
+
+// ---------------------------------------------------------------- fixed scratch
+// Scratch for the selection of at most kFixedScratchUnits units, held by every
+// device that loads the library for as long as the process runs (about 8 MiB).
+// Host code must not pass `g_units_scratch` itself to a kernel: on the host it
+// names a host-side shadow, not device memory.  Its device address is looked
+// up once per device below.
+constexpr int64_t kFixedScratchUnits = int64_t(1) << 19;
+constexpr size_t kFixedScratchBytes =
+    align256(kBins * 4) + align256(sizeof(Ctl)) + 2 * align256((size_t)kFixedScratchUnits * 8) +
+    2 * align256((size_t)((kFixedScratchUnits + kChunk - 1) / kChunk) * 4);
+static __device__ __align__(256) uint8_t g_units_scratch[kFixedScratchBytes];
+
+int64_t fixed_scratch_units() { return kFixedScratchUnits; }
+
+cudaError_t fixed_scratch(void** ptr, size_t* bytes) {
+  static std::atomic<void*> addr[64];
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* p = addr[dev].load();
+  if (p == nullptr) {
+    // the current device is `dev`: this resolves the array's address on it
+    if (cudaError_t e = cudaGetSymbolAddress(&p, g_units_scratch)) return e;
+    addr[dev].store(p);
+  }
+  *ptr = p;
+  *bytes = kFixedScratchBytes;
+  return cudaSuccess;
+}
 
 cudaError_t launch_blocks(const BlocksLaunch& a, cudaStream_t s) {
   const WsLayout L = ws_layout(a.units);

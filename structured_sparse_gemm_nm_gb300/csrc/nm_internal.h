@@ -77,6 +77,10 @@ struct BlocksLaunch {
 };
 size_t blocks_workspace(int64_t units);
 cudaError_t launch_blocks(const BlocksLaunch& a, cudaStream_t s);
+// Device address and size of the library's own fixed scratch for the selection
+// (looked up once per device, on the current device).
+int64_t fixed_scratch_units();
+cudaError_t fixed_scratch(void** ptr, size_t* bytes);
 
 // ---- products (nm_spmm_tc.cu, nm_spmm_cc.cu, nm_blocks.cu) ---------------
 struct SpmmLaunch {
