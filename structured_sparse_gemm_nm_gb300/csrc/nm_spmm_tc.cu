@@ -20,7 +20,12 @@
 //                lane (row slot) and k-step from global memory and writes it
 //                with tcgen05.st into one of four 64-column-aligned TMEM
 //                slots (the sparse MMA accepts its metadata only there); this
-//                keeps metadata movement out of the tensor pipe
+//                keeps metadata movement out of the tensor pipe.  The slots
+//                form two pairs used by alternate stages: the metadata warps
+//                refill a pair once the stage that last used it is released
+//                (its `empty` barrier) and then arrive on the new stage's
+//                `full` barrier, so the MMA issuer waits on one barrier per
+//                stage and commits once per stage.
 //   warps 6..13  epilogue: drain the FP32 accumulator (alpha, mask) into
 //                packed registers, release it, then stage 32 x 32 blocks in
 //                shared memory and write them with TMA bulk stores
@@ -45,10 +50,10 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int kKPerStage = 64;  // dense-equivalent K per stage
 constexpr int kMetaWarp0 = 2, kMetaWarps = 4;
-constexpr int kEpiWarp0 = 6, kEpiWarps = 8;
+constexpr int kEpiWarp0 = kMetaWarp0 + kMetaWarps, kEpiWarps = 8;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kTmemCols = 512;
-constexpr int kMetaCol = 256, kMetaColStride = 64, kMetaSlots = 4;
+constexpr int kMetaCol = 256, kMetaColStride = 64;  // four metadata slots: columns 256, 320, 384, 448
 constexpr int kEpiBufBytes = 32 * 32 * 2;  // one 32 x 32 output block
 
 template <bool SPARSE>
@@ -114,9 +119,8 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 
 // Bounded wait: false if the budget ran out (then the status word and the
 // CTA's abort flag are set) or another role already aborted.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long budget,
-                                       int32_t* status) {
-  if (mbar_try(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long budget,
+                                            int32_t* status) {
   const long long t0 = clock64();
   while (true) {
     if (mbar_try(bar, parity)) return true;
@@ -127,6 +131,13 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       return false;
     }
   }
+}
+// The phase is usually complete already: test it inline and only call out to
+// the bounded loop when it is not.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long budget,
+                                          int32_t* status) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, budget, status);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
@@ -262,12 +273,11 @@ __global__ void __maxnreg__(128)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-  // bars: full[S], empty[S], tfull[2], tempty[2], mfull[4], mfree[4], drain
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain
   const uint32_t bar_full = smem_u32(bars), bar_empty = smem_u32(bars + C::kStages);
   const uint32_t bar_tfull = smem_u32(bars + 2 * C::kStages), bar_tempty = bar_tfull + 16;
-  const uint32_t bar_mfull = bar_tempty + 16, bar_mfree = bar_mfull + 8 * kMetaSlots;
-  const uint32_t bar_drain = bar_mfree + 8 * kMetaSlots;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5 + 2 * kMetaSlots);
+  const uint32_t bar_drain = bar_tempty + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -276,16 +286,13 @@ __global__ void __maxnreg__(128)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      // SPARSE: the producer's expect_tx arrival and one arrival per metadata warp
+      mbar_init(bar_full + 8 * s, SPARSE ? 1 + kMetaWarps : 1);
       mbar_init(bar_empty + 8 * s, CL);  // released by the MMA of every CTA that reads the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
       mbar_init(bar_tempty + 8 * a, kEpiWarps);
-    }
-    for (int s = 0; s < kMetaSlots; ++s) {
-      mbar_init(bar_mfull + 8 * s, kMetaWarps);
-      mbar_init(bar_mfree + 8 * s, 1);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -372,8 +379,7 @@ __global__ void __maxnreg__(128)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      int mslot = 0;
-      uint32_t mphase = 0;
+      uint32_t mpair = 0;  // SPARSE: metadata slot pair of the current stage (alternates every stage)
       bool ok = true;
       if (p.fault_test) ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);  // nothing arrives: runs out
       for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
@@ -391,26 +397,17 @@ __global__ void __maxnreg__(128)
           const uint32_t sA = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t sB = sA + C::kATileBytes;
           if constexpr (SPARSE) {
-            const int steps = min(2, p.num_k_steps - 2 * ks);  // no MMA past K
-            for (int j = 0; j < steps; ++j) {
-              if (!mbar_wait(bar_mfull + 8 * mslot, mphase, abort_flag, p.wait_budget, p.status)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              // A: 128 rows x 64 B (64B swizzle, 8-row groups 512 B apart), 16 values = 32 B per k-step
-              const uint64_t ad = sdesc(sA + 32 * j, 16, 512, kSwizzle64);
-              // B: 256 rows x 128 B (128B swizzle), 32 values = 64 B per k-step
-              const uint64_t bd = sdesc(sB + 64 * j, 16, 1024, kSwizzle128);
-              mma_sparse(tacc, ad, bd, tmem + kMetaCol + kMetaColStride * mslot, idesc, kstep > 0 ? 1u : 0u);
-              tc_commit(bar_mfree + 8 * mslot);  // the metadata slot is free once this MMA is done
-              ++kstep;
-              if (++mslot == kMetaSlots) {
-                mslot = 0;
-                mphase ^= 1;
-              }
-            }
-            if (!ok) break;
+            // the full barrier also covers this stage's metadata (slots 2 * mpair + j)
+            const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * 2 * mpair;
+            // A: 128 rows x 64 B (64B swizzle, 8-row groups 512 B apart), 16 values = 32 B per k-step
+            // B: 256 rows x 128 B (128B swizzle), 32 values = 64 B per k-step
+            mma_sparse(tacc, sdesc(sA, 16, 512, kSwizzle64), sdesc(sB, 16, 1024, kSwizzle128), tmeta, idesc,
+                       kstep > 0 ? 1u : 0u);
+            if (2 * ks + 1 < p.num_k_steps)  // no MMA past K
+              mma_sparse(tacc, sdesc(sA + 32, 16, 512, kSwizzle64), sdesc(sB + 64, 16, 1024, kSwizzle128),
+                         tmeta + kMetaColStride, idesc, 1u);
+            ++kstep;
+            mpair ^= 1u;
           } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -448,41 +445,52 @@ __global__ void __maxnreg__(128)
     // ------------------------------------------------------- SPARSE metadata
     if constexpr (SPARSE) {
       const int q = warp & 3;  // TMEM lane quarter this warp may access
-      int mslot = 0;
-      uint32_t mphase = 0;
+      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + kMetaCol;
+      const int S = p.num_k_steps;
+      int g = 0;  // stages handed to the MMA so far, in the order the MMA consumes them
       bool ok = true;
       for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
         const Unit t = decode_unit(p, u, CL, rank);
         const uint32_t* src = p.meta + t.m0 + 32 * q + lane;
-        const int S = p.num_k_steps;
-        // code words of four k-steps are loaded one batch ahead of their use
-        uint32_t nxt[4];
+        auto word = [&](int kstep) -> uint32_t {
+          return kstep < S ? __ldg(src + (int64_t)kstep * p.meta_slots) : 0x44444444u;  // 0x4: a valid code
+        };
+        // the words of the next four stages are loaded ahead of their use
+        uint32_t ring[4][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) nxt[i] = i < S ? __ldg(src + (int64_t)i * p.meta_slots) : 0u;
-        for (int s0 = 0; ok && s0 < S; s0 += 4) {
-          uint32_t cur[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            nxt[i] = (s0 + 4 + i < S) ? __ldg(src + (int64_t)(s0 + 4 + i) * p.meta_slots) : 0u;
+        for (int i = 0; i < 4; ++i) {
+          const int ks = t.kbeg + i;
+          ring[i][0] = ks < t.kend ? word(2 * ks) : 0u;
+          ring[i][1] = ks < t.kend ? word(2 * ks + 1) : 0u;
+        }
+        for (int ks0 = t.kbeg; ok && ks0 < t.kend; ks0 += 4) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            if (s0 + i >= S) break;
-            if (!mbar_wait(bar_mfree + 8 * mslot, mphase ^ 1, abort_flag, p.wait_budget, p.status)) {
-              ok = false;
-              break;
+            const int ks = ks0 + i;
+            if (ks >= t.kend) break;
+            const uint32_t w0 = ring[i][0], w1 = ring[i][1];
+            if (ks + 4 < t.kend) {
+              ring[i][0] = word(2 * (ks + 4));
+              ring[i][1] = word(2 * (ks + 4) + 1);
+            }
+            // slot pair g & 1 was last read by the MMAs of stage g - 2: wait until that stage is released
+            if (g >= 2) {
+              const int h = g - 2;
+              if (!mbar_wait(bar_empty + 8 * (h % C::kStages), (uint32_t)((h / C::kStages) & 1), abort_flag,
+                             p.wait_budget, p.status)) {
+                ok = false;
+                break;
+              }
             }
             tc_fence_after();
-            tmem_st1(tmem + ((uint32_t)(32 * q) << 16) + kMetaCol + kMetaColStride * mslot, cur[i]);
+            const uint32_t ta = tq + kMetaColStride * 2 * (g & 1);
+            tmem_st1(ta, w0);
+            tmem_st1(ta + kMetaColStride, w1);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_mfull + 8 * mslot);
-            if (++mslot == kMetaSlots) {
-              mslot = 0;
-              mphase ^= 1;
-            }
+            if (lane == 0) mbar_arrive(bar_full + 8 * (g % C::kStages));
+            ++g;
           }
         }
       }
