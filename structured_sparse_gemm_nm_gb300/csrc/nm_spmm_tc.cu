@@ -217,16 +217,26 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// Loads and the wait for them sit in one asm statement: the registers are
+// defined only once the data has arrived.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
-        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Two 32-column loads in flight at once.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
+        "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
 }
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
@@ -240,7 +250,13 @@ __device__ __forceinline__ uint16_t to_cd(float x, int bf16) {
   return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
 }
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
-  return (uint32_t)to_cd(lo, bf16) | ((uint32_t)to_cd(hi, bf16) << 16);
+  // one round-to-nearest conversion of the pair; `lo` lands in the low 16 bits
+  if (bf16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Work unit u -> 128-row block, 256-column block and K split.  In a cluster
@@ -380,6 +396,25 @@ __global__ void __maxnreg__(128)
       int acc = 0;
       uint32_t acc_phase = 0;
       uint32_t mpair = 0;  // SPARSE: metadata slot pair of the current stage (alternates every stage)
+      // Shared-memory descriptors of stage 0.  Advancing a descriptor's start address
+      // (bits 0-13, in 16-byte units) by an offset is adding offset >> 4, since every
+      // shared address fits the 14-bit field.
+      //   SPARSE A: 128 rows x 64 B (64B swizzle, 8-row groups 512 B apart), 32 B per k-step
+      //   SPARSE B: 256 rows x 128 B (128B swizzle), 64 B per k-step
+      //   DENSE A/B K-major: 128B swizzle, 32 B per K16 step; MN-major: 2048 B per K16 step
+      constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
+      const uint32_t sA0 = smem_u32(smem), sB0 = sA0 + C::kATileBytes;
+      uint64_t a_desc0, b_desc0;
+      uint32_t a_step = 0, b_step = 0;
+      if constexpr (SPARSE) {
+        a_desc0 = sdesc(sA0, 16, 512, kSwizzle64);
+        b_desc0 = sdesc(sB0, 16, 1024, kSwizzle128);
+      } else {
+        a_desc0 = p.a_mn ? sdesc(sA0, C::kATileBytes / 2, 1024, kSwizzle128) : sdesc(sA0, 16, 1024, kSwizzle128);
+        b_desc0 = p.b_mn ? sdesc(sB0, 8192, 1024, kSwizzle128) : sdesc(sB0, 16, 1024, kSwizzle128);
+        a_step = p.a_mn ? (2048 >> 4) : (32 >> 4);
+        b_step = p.b_mn ? (2048 >> 4) : (32 >> 4);
+      }
       bool ok = true;
       if (p.fault_test) ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);  // nothing arrives: runs out
       for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
@@ -394,29 +429,22 @@ __global__ void __maxnreg__(128)
             break;
           }
           tc_fence_after();
-          const uint32_t sA = smem_u32(smem + stage * C::kStageBytes);
-          const uint32_t sB = sA + C::kATileBytes;
+          // descriptors of this stage: the stage-0 descriptors with the start address advanced
+          const uint64_t ad = a_desc0 + (uint64_t)(stage * kStageUnits);
+          const uint64_t bd = b_desc0 + (uint64_t)(stage * kStageUnits);
           if constexpr (SPARSE) {
             // the full barrier also covers this stage's metadata (slots 2 * mpair + j)
             const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * 2 * mpair;
-            // A: 128 rows x 64 B (64B swizzle, 8-row groups 512 B apart), 16 values = 32 B per k-step
-            // B: 256 rows x 128 B (128B swizzle), 32 values = 64 B per k-step
-            mma_sparse(tacc, sdesc(sA, 16, 512, kSwizzle64), sdesc(sB, 16, 1024, kSwizzle128), tmeta, idesc,
-                       kstep > 0 ? 1u : 0u);
+            mma_sparse(tacc, ad, bd, tmeta, idesc, kstep > 0 ? 1u : 0u);
             if (2 * ks + 1 < p.num_k_steps)  // no MMA past K
-              mma_sparse(tacc, sdesc(sA + 32, 16, 512, kSwizzle64), sdesc(sB + 64, 16, 1024, kSwizzle128),
-                         tmeta + kMetaColStride, idesc, 1u);
+              mma_sparse(tacc, ad + (32 >> 4), bd + (64 >> 4), tmeta + kMetaColStride, idesc, 1u);
             ++kstep;
             mpair ^= 1u;
           } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint64_t ad = p.a_mn ? sdesc(sA + 2048 * j, C::kATileBytes / 2, 1024, kSwizzle128)
-                                         : sdesc(sA + 32 * j, 16, 1024, kSwizzle128);
-              const uint64_t bd = p.b_mn ? sdesc(sB + 2048 * j, 8192, 1024, kSwizzle128)
-                                         : sdesc(sB + 32 * j, 16, 1024, kSwizzle128);
-              mma_dense(tacc, ad, bd, idesc, (kstep > 0 || j > 0) ? 1u : 0u);
-            }
+            for (int j = 0; j < 4; ++j)
+              mma_dense(tacc, ad + (uint64_t)(j * a_step), bd + (uint64_t)(j * b_step), idesc,
+                        (kstep > 0 || j > 0) ? 1u : 0u);
             ++kstep;
           }
           if (CL > 1)
@@ -513,11 +541,38 @@ __global__ void __maxnreg__(128)
       const bool row_ok = row < p.M;
       const int ncol0 = t.n0 + 128 * half;
       uint32_t pk[4][16];
-      // drain this warp's 32 x 128 block of the accumulator into packed registers
+      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + acc * BN + 128 * half;
+      if (p.split_k == 1 && p.tma_store) {
+        // drain this warp's 32 x 128 block two 32-column chunks at a time into packed registers
+#pragma unroll
+        for (int c2 = 0; c2 < 4; c2 += 2) {
+          uint32_t va[32], vb[32];
+          tmem_ld32x2(tq + 32 * c2, tq + 32 * (c2 + 1), va, vb);
+          uint32_t ma = 0xFFFFFFFFu, mb = 0xFFFFFFFFu;
+          if (!SPARSE && p.mask != nullptr && row_ok) {
+            const int na = ncol0 + 32 * c2, nbb = na + 32;
+            if (na < p.N) ma = p.mask[(int64_t)row * p.mask_words + na / 32];
+            if (nbb < p.N) mb = p.mask[(int64_t)row * p.mask_words + nbb / 32];
+          }
+          const float al = p.alpha;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float a0 = ((ma >> (2 * j)) & 1u) ? __uint_as_float(va[2 * j]) * al : 0.0f;
+            const float a1 = ((ma >> (2 * j + 1)) & 1u) ? __uint_as_float(va[2 * j + 1]) * al : 0.0f;
+            pk[c2][j] = pack2(a0, a1, p.bf16);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float b0 = ((mb >> (2 * j)) & 1u) ? __uint_as_float(vb[2 * j]) * al : 0.0f;
+            const float b1 = ((mb >> (2 * j + 1)) & 1u) ? __uint_as_float(vb[2 * j + 1]) * al : 0.0f;
+            pk[c2 + 1][j] = pack2(b0, b1, p.bf16);
+          }
+        }
+      } else {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * BN + 128 * half + 32 * c, v);
+        tmem_ld32(tq + 32 * c, v);
         const int nb = ncol0 + 32 * c;
         uint32_t mword = 0xFFFFFFFFu;
         if (!SPARSE && p.mask != nullptr && row_ok && nb < p.N) mword = p.mask[(int64_t)row * p.mask_words + nb / 32];
@@ -532,13 +587,6 @@ __global__ void __maxnreg__(128)
               dst[j] = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
             }
           }
-        } else if (p.tma_store) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float x0 = ((mword >> (2 * j)) & 1u) ? __uint_as_float(v[2 * j]) * p.alpha : 0.0f;
-            const float x1 = ((mword >> (2 * j + 1)) & 1u) ? __uint_as_float(v[2 * j + 1]) * p.alpha : 0.0f;
-            pk[c][j] = pack2(x0, x1, p.bf16);
-          }
         } else if (row_ok && nb < p.N) {
           const int cnt = min(32, p.N - nb);
 #pragma unroll
@@ -551,6 +599,7 @@ __global__ void __maxnreg__(128)
             reinterpret_cast<uint16_t*>(p.D)[doff] = to_cd(x, p.bf16);
           }
         }
+      }
       }
       // the accumulator buffer is drained: the next tile's MMAs may reuse it
       tc_fence_before();
