@@ -569,7 +569,7 @@ __global__ void __maxnreg__(128)
           }
         }
       } else {
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
         tmem_ld32(tq + 32 * c, v);
@@ -577,15 +577,19 @@ __global__ void __maxnreg__(128)
         uint32_t mword = 0xFFFFFFFFu;
         if (!SPARSE && p.mask != nullptr && row_ok && nb < p.N) mword = p.mask[(int64_t)row * p.mask_words + nb / 32];
         if (p.split_k > 1) {
-          // fp32 partial of this K split, row-major [split][M][N]
-          if (row_ok && nb < p.N) {
-            float* dst = p.partial + ((int64_t)t.split * p.M + row) * p.N + nb;
-            const int cnt = min(32, p.N - nb);
+          // fp32 partial of this K split in the tiled order [split][m block][n block][col / 4][128 rows][4]:
+          // for each group of four columns the 32 lanes write 512 contiguous bytes
+          float4* tile = reinterpret_cast<float4*>(p.partial) +
+                         ((int64_t)(t.split * p.num_m_blk + t.m0 / BM) * p.num_n_blk + t.n0 / BN) * (BM * BN / 4);
+          const int c4_0 = (128 * half + 32 * c) / 4;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j >= cnt) break;
-              dst[j] = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
-            }
+          for (int j4 = 0; j4 < 8; ++j4) {
+            float4 w;
+            w.x = ((mword >> (4 * j4)) & 1u) ? __uint_as_float(v[4 * j4]) * p.alpha : 0.0f;
+            w.y = ((mword >> (4 * j4 + 1)) & 1u) ? __uint_as_float(v[4 * j4 + 1]) * p.alpha : 0.0f;
+            w.z = ((mword >> (4 * j4 + 2)) & 1u) ? __uint_as_float(v[4 * j4 + 2]) * p.alpha : 0.0f;
+            w.w = ((mword >> (4 * j4 + 3)) & 1u) ? __uint_as_float(v[4 * j4 + 3]) * p.alpha : 0.0f;
+            tile[(c4_0 + j4) * BM + 32 * q + lane] = w;
           }
         } else if (row_ok && nb < p.N) {
           const int cnt = min(32, p.N - nb);
@@ -670,17 +674,32 @@ __global__ void scale_c_kernel(const uint16_t* C, uint16_t* D, int64_t rows, int
 
 // Sum of the K splits' fp32 partials (alpha and mask already applied), plus
 // beta * C, converted to D.
-__global__ void finalize_split_kernel(const float* __restrict__ part, int splits, int64_t M, int64_t N,
-                                      const uint16_t* __restrict__ C, uint16_t* __restrict__ D, int64_t ldc,
-                                      int64_t ldd, int cd_col, float beta, int bf16) {
-  const int64_t total = M * N;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t m = i / N, n = i - m * N;
-    float x = 0.0f;
-    for (int s = 0; s < splits; ++s) x += part[(int64_t)s * total + i];
-    const int64_t doff = cd_col ? n * ldd + m : m * ldd + n;
-    if (C != nullptr) x = fmaf(beta, load_cd(C, cd_col ? n * ldc + m : m * ldc + n, bf16), x);
-    D[doff] = to_cd(x, bf16);
+__global__ void finalize_split_kernel(const float4* __restrict__ part, int splits, int num_m_blk, int num_n_blk,
+                                      int64_t M, int64_t N, const uint16_t* __restrict__ C, uint16_t* __restrict__ D,
+                                      int64_t ldc, int64_t ldd, int cd_col, float beta, int bf16) {
+  // one thread per four columns of one row, in the tiled order the product wrote
+  const int64_t per_split = (int64_t)num_m_blk * num_n_blk * (BM * BN / 4);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < per_split;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = i / (BM * BN / 4);
+    const int rem = (int)(i - tile * (BM * BN / 4));
+    const int c4 = rem / BM, r = rem - c4 * BM;
+    const int64_t m = (tile / num_n_blk) * BM + r, n0 = (tile % num_n_blk) * BN + 4 * c4;
+    if (m >= M || n0 >= N) continue;
+    float4 x = part[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 y = part[(int64_t)s * per_split + i];
+      x.x += y.x, x.y += y.y, x.z += y.z, x.w += y.w;
+    }
+    const float v[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t n = n0 + j;
+      if (n >= N) break;
+      float o = v[j];
+      if (C != nullptr) o = fmaf(beta, load_cd(C, cd_col ? n * ldc + m : m * ldc + n, bf16), o);
+      D[cd_col ? n * ldd + m : m * ldd + n] = to_cd(o, bf16);
+    }
   }
 }
 
@@ -873,7 +892,9 @@ int spmm_tc_dense_masked_split(const nm_spmm_desc_t& d) {
   return best;
 }
 size_t spmm_tc_dense_masked_workspace(const nm_spmm_desc_t& d, int split_k) {
-  return split_k > 1 ? (size_t)split_k * (size_t)d.M * (size_t)d.N * sizeof(float) : 0;
+  // whole 128 x 256 tiles per split (the tiled partial order of the product's epilogue)
+  const size_t tiles = (size_t)((d.M + tc::BM - 1) / tc::BM) * (size_t)((d.N + tc::BN - 1) / tc::BN);
+  return split_k > 1 ? (size_t)split_k * tiles * tc::BM * tc::BN * sizeof(float) : 0;
 }
 
 cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaStream_t s) {
@@ -915,9 +936,11 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
   if (!ok) return cudaErrorInvalidValue;
   cudaError_t e = cl == 2 ? launch_kernel<false, 2>(mA, mB, mD, p, s) : launch_kernel<false, 1>(mA, mB, mD, p, s);
   if (e != cudaSuccess || p.split_k == 1) return e;
-  finalize_split_kernel<<<grid_for(d.M * d.N, 256), 256, 0, s>>>(
-      p.partial, p.split_k, d.M, d.N, static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.ldc, d.ldd,
-      d.order_cd == NM_COL, a.beta_f, d.ab_type == NM_BF16);
+  const int64_t groups = (int64_t)p.num_m_blk * p.num_n_blk * (BM * BN / 4);
+  finalize_split_kernel<<<grid_for(groups, 256), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(p.partial), p.split_k, p.num_m_blk, p.num_n_blk, d.M, d.N,
+      static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.ldc, d.ldd, d.order_cd == NM_COL, a.beta_f,
+      d.ab_type == NM_BF16);
   return cudaGetLastError();
 }
 
