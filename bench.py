@@ -263,6 +263,47 @@ def time_launch(torch, fn, flush, reps=10, warm=3):
     return statistics.median(ts)
 
 
+L2_BYTES = 132_000_000  # 126 MiB of L2 on GB300
+
+
+def copies_for(bytes_per_launch: int) -> int:
+    """Independent problem copies whose inputs and outputs together exceed twice the L2."""
+    return max(4, min(32, -(-2 * L2_BYTES // max(1, bytes_per_launch))))
+
+
+def time_stream(torch, fns, reps=3):
+    """Median milliseconds per launch of `fns` run back to back on the stream.
+
+    Every function works on its own buffers and the buffers of all of them
+    together exceed twice the L2, so each launch reads its inputs from HBM,
+    as it does inside a longer sequence of work; launch latency overlaps the
+    previous kernel as it would there."""
+    for f in fns:
+        f()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for f in fns:
+            f()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / len(fns))
+    return statistics.median(ts)
+
+
+def hbm_row(torch, make, byt, hbm, flush, **extra):
+    """Row of an HBM-bound kernel: `make(r)` builds copy r's launch; `byt` = algorithmic bytes per launch."""
+    fns = [make(r) for r in range(copies_for(byt))]
+    t = time_stream(torch, fns)
+    t1 = time_launch(torch, fns[0], flush)
+    row = {"ms": t, "bytes": byt, "gbs": byt / t / 1e6, "frac_hbm": byt / t / 1e6 / hbm, "copies": len(fns),
+           "ms_single": t1, "gbs_single": byt / t1 / 1e6}
+    row.update(extra)
+    return row
+
+
 # ------------------------------------------------------------------ rows
 def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
     flush = Flusher(torch, dev)
@@ -293,86 +334,115 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
         rows[f"S7_dw_{name}"] = {"shape_MNK": [o, i, wl.T], "ms": t_dw, "tflops": f / t_dw / 1e9,
                                  "frac_dense_peak": f / t_dw / 1e9 / dense_peak}
 
-    # S3: transposable prune + dual compress, one layer's four weights
-    for j, (name, o, i) in enumerate(wl.linears):
-        L = L0[j]
-        t = time_launch(torch, lambda: nb.nm_prune_transposable(L["W"], o, i, i, "bf16", None, 0, L["mask"], L["vals"],
-                                                                L["meta"], L["valsT"], L["metaT"], nb.NM_META_TC), flush)
-        rows[f"S3_transposable_{name}"] = {"shape": [o, i], "ms": t, "bytes": L["prune_bytes"],
-                                           "gbs": L["prune_bytes"] / t / 1e6, "frac_hbm": L["prune_bytes"] / t / 1e6 / hbm}
+    # HBM-bound rows: `ms` is the per-launch time of back-to-back launches over
+    # copies whose buffers exceed the L2 (see time_stream); `ms_single` is one
+    # launch after an L2 flush, launch latency included.
+    def empty(nbytes):
+        return torch.empty(max(16, nbytes), dtype=torch.uint8, device=dev)
 
-    # S1 / S2 / S4 / S8 on the 4096 x 4096 f16 weight
+    # S3: transposable prune + dual compress (+ mask) of each GPT-neo weight shape, bf16
+    for j, (name, o, i) in enumerate(wl.linears):
+        vb, mb = nb.nm_compressed_size(o, i, "bf16", 2, 4, nb.NM_META_TC)
+        vbT, mbT = nb.nm_compressed_size(i, o, "bf16", 2, 4, nb.NM_META_TC)
+        byt = o * i * 2 + vb + mb + vbT + mbT + o * i // 8
+
+        def make(r, o=o, i=i, vb=vb, mb=mb, vbT=vbT, mbT=mbT):
+            Wr = inputs.normal((o, i), 0.02, 500 + r, "bf16", device=dev)
+            bufs = [empty(o * i // 8), empty(vb), empty(mb), empty(vbT), empty(mbT)]
+            return lambda: nb.nm_prune_transposable(Wr, o, i, i, "bf16", None, 0, bufs[0], bufs[1], bufs[2], bufs[3],
+                                                    bufs[4], nb.NM_META_TC)
+        rows[f"S3_transposable_{name}"] = hbm_row(torch, make, byt, hbm, flush, shape=[o, i])
+
+    # S1 / S2 / S4 / S8 on 4096 x 4096 f16 weights
     M = K = 4096
-    W = inputs.normal((M, K), 0.02, inputs.SEED_W, "f16", device=dev)
+
+    def weight(r):
+        return inputs.normal((M, K), 0.02, inputs.SEED_W + 100 * r, "f16", device=dev)
+
     for layout, lname in ((nb.NM_META_CANONICAL, "canonical"), (nb.NM_META_TC, "tensor_core")):
         vb, mb = nb.nm_compressed_size(M, K, "f16", 2, 4, layout)
-        vals = torch.empty(vb, dtype=torch.uint8, device=dev)
-        meta = torch.empty(mb, dtype=torch.uint8, device=dev)
-        t = time_launch(torch, lambda: nb.nm_compress(W, M, K, K, "f16", 2, 4, 0, layout, vals, meta), flush)
-        byt = M * K * 2 + vb + mb
-        rows[f"S1_prune_compress_24_{lname}"] = {"shape": [M, K], "ms": t, "bytes": byt, "gbs": byt / t / 1e6,
-                                                 "frac_hbm": byt / t / 1e6 / hbm}
-        Wout = torch.empty_like(W)
-        t = time_launch(torch, lambda: nb.nm_decompress(vals, meta, M, K, "f16", 2, 4, layout, Wout, K), flush)
-        byt = vb + mb + M * K * 2
-        rows[f"S4_decompress_24_{lname}"] = {"ms": t, "bytes": byt, "gbs": byt / t / 1e6, "frac_hbm": byt / t / 1e6 / hbm}
-    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
-    t = time_launch(torch, lambda: nb.nm_check(W, M, K, K, "f16", 2, 4, 1, cnt), flush)
-    rows["S4_check_24_transposable"] = {"ms": t, "bytes": M * K * 2 * 2, "gbs": M * K * 4 / t / 1e6,
-                                        "frac_hbm": M * K * 4 / t / 1e6 / hbm}
-    t = time_launch(torch, lambda: nb.nm_prune(W, M, K, K, "f16", 2, 4, W, K, None), flush)
-    rows["S1_prune_inplace_24"] = {"ms": t, "bytes": M * K * 4, "gbs": M * K * 4 / t / 1e6,
-                                   "frac_hbm": M * K * 4 / t / 1e6 / hbm}
-    W = inputs.normal((M, K), 0.02, inputs.SEED_W, "f16", device=dev)
+
+        def make(r, vb=vb, mb=mb, layout=layout):
+            Wr, v, m = weight(r), empty(vb), empty(mb)
+            return lambda: nb.nm_compress(Wr, M, K, K, "f16", 2, 4, 0, layout, v, m)
+        rows[f"S1_prune_compress_24_{lname}"] = hbm_row(torch, make, M * K * 2 + vb + mb, hbm, flush, shape=[M, K])
+
+        def make(r, vb=vb, mb=mb, layout=layout):
+            Wr, v, m = weight(r), empty(vb), empty(mb)
+            nb.nm_compress(Wr, M, K, K, "f16", 2, 4, 0, layout, v, m)
+            return lambda: nb.nm_decompress(v, m, M, K, "f16", 2, 4, layout, Wr, K)
+        rows[f"S4_decompress_24_{lname}"] = hbm_row(torch, make, vb + mb + M * K * 2, hbm, flush)
+
+    def make(r):
+        Wr, cnt = weight(r), torch.zeros(4, dtype=torch.int32, device=dev)
+        return lambda: nb.nm_check(Wr, M, K, K, "f16", 2, 4, 1, cnt)
+    rows["S4_check_24_transposable"] = hbm_row(torch, make, M * K * 2, hbm, flush)
+
+    def make(r):
+        Wr, mask = weight(r), empty(M * K // 8)
+        return lambda: nb.nm_prune(Wr, M, K, K, "f16", 2, 4, Wr, K, mask)
+    rows["S1_prune_inplace_24_mask"] = hbm_row(torch, make, M * K * 4 + M * K // 8, hbm, flush)
+
     for n in (4, 8, 16):
         vb, mb = nb.nm_compressed_size(M, K, "f16", n, 32)
-        vals = torch.empty(vb, dtype=torch.uint8, device=dev)
-        idx = torch.empty(mb, dtype=torch.uint8, device=dev)
-        t = time_launch(torch, lambda: nb.nm_compress(W, M, K, K, "f16", n, 32, 0, nb.NM_META_CANONICAL, vals, idx), flush)
-        byt = M * K * 2 + vb + mb
-        rows[f"S2_prune_compress_{n}of32"] = {"ms": t, "bytes": byt, "gbs": byt / t / 1e6, "frac_hbm": byt / t / 1e6 / hbm}
+
+        def make(r, n=n, vb=vb, mb=mb):
+            Wr, v, m = weight(r), empty(vb), empty(mb)
+            return lambda: nb.nm_compress(Wr, M, K, K, "f16", n, 32, 0, nb.NM_META_CANONICAL, v, m)
+        rows[f"S2_prune_compress_{n}of32"] = hbm_row(torch, make, M * K * 2 + vb + mb, hbm, flush)
         for b in (1, 8):
-            x = inputs.normal((b, K), 1.0, inputs.SEED_VEC, "f16", device=dev)
-            y = torch.empty((b, M), dtype=torch.float16, device=dev)
             plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=b, K=K, n=n, m=32, ab_type="f16", cd_type="f16", ldb=K, ldd=M,
                                                 meta_layout=nb.NM_META_CANONICAL))
-            t = time_launch(torch, lambda: nb.nm_spmm(plan, 1.0, vals, idx, x, 0.0, None, y), flush)
+
+            def make(r, n=n, vb=vb, mb=mb, b=b, plan=plan):
+                Wr, v, m = weight(r % 4), empty(vb), empty(mb)
+                nb.nm_compress(Wr, M, K, K, "f16", n, 32, 0, nb.NM_META_CANONICAL, v, m)
+                x = inputs.normal((b, K), 1.0, inputs.SEED_VEC + r, "f16", device=dev)
+                y = torch.empty((b, M), dtype=torch.float16, device=dev)
+                return lambda: nb.nm_spmm(plan, 1.0, v, m, x, 0.0, None, y)
             byt = vb + mb + b * K * 2 + b * M * 2
-            rows[f"S8_gemv_{n}of32_b{b}"] = {"ms": t, "bytes": byt, "gbs": byt / t / 1e6,
-                                             "frac_hbm": byt / t / 1e6 / hbm,
-                                             "gflops": 2.0 * M * (K // 32) * n * b / t / 1e6}
+            row = hbm_row(torch, make, byt, hbm, flush)
+            row["gflops"] = 2.0 * M * (K // 32) * n * b / row["ms"] / 1e6
+            rows[f"S8_gemv_{n}of32_b{b}"] = row
             plan.destroy()
 
     # S9: vector-wise (1 x 32) and block-wise (32 x 32) selection at density 0.25, then the product
-    W = inputs.normal((M, K), 0.02, inputs.SEED_W, "f16", device=dev)
     for bh, uname in ((1, "vector_wise"), (32, "block_wise")):
         keep = (M // bh) * (K // 32) // 4
         wsb = nb.nm_prune_units_workspace(M, K, bh, 32)
-        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-        csr = torch.empty((M // bh + 1 + keep) * 4, dtype=torch.uint8, device=dev)
-        vals = torch.empty(keep * bh * 32 * 2, dtype=torch.uint8, device=dev)
-        if bh == 1:
-            sel = lambda: nb.nm_prune_vector_wise(W, M, K, K, "f16", 32, keep, nb.NM_SCORE_ABS_OF_SUM, csr=csr,
-                                                  vals=vals, workspace=ws, workspace_bytes=wsb)
-        else:
-            sel = lambda: nb.nm_prune_block_wise(W, M, K, K, "f16", 32, 32, keep, csr=csr, vals=vals, workspace=ws,
-                                                 workspace_bytes=wsb)
-        t = time_launch(torch, sel, flush)
-        byt = M * K * 2 + csr.numel() + vals.numel()
-        rows[f"S9_{uname}_select_compress"] = {"shape": [M, K], "kept_units": keep, "ms": t, "bytes": byt,
-                                               "gbs": byt / t / 1e6, "frac_hbm": byt / t / 1e6 / hbm}
+        csr_b, vals_b = (M // bh + 1 + keep) * 4, keep * bh * 32 * 2
+
+        def make(r, bh=bh, keep=keep, wsb=wsb, csr_b=csr_b, vals_b=vals_b):
+            Wr, ws, csr, vals = weight(r), empty(wsb), empty(csr_b), empty(vals_b)
+            if bh == 1:
+                return lambda: nb.nm_prune_vector_wise(Wr, M, K, K, "f16", 32, keep, nb.NM_SCORE_ABS_OF_SUM, csr=csr,
+                                                       vals=vals, workspace=ws, workspace_bytes=wsb)
+            return lambda: nb.nm_prune_block_wise(Wr, M, K, K, "f16", 32, 32, keep, csr=csr, vals=vals, workspace=ws,
+                                                  workspace_bytes=wsb)
+        rows[f"S9_{uname}_select_compress"] = hbm_row(torch, make, M * K * 2 + csr_b + vals_b, hbm, flush,
+                                                      kept_units=keep)
         for b in (1, 8):
-            x = inputs.normal((b, K), 1.0, inputs.SEED_VEC, "f16", device=dev)
-            y = torch.empty((b, M), dtype=torch.float16, device=dev)
             plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=b, K=K, mode=nb.NM_SPMM_BLOCK_SPARSE_A, n=bh, m=32,
                                                 ab_type="f16", cd_type="f16", ldb=K, ldd=M,
                                                 meta_layout=nb.NM_META_CANONICAL))
-            t = time_launch(torch, lambda: nb.nm_spmm(plan, 1.0, vals, csr, x, 0.0, None, y), flush)
-            byt = vals.numel() + csr.numel() + b * K * 2 + b * M * 2
-            rows[f"S9_{uname}_gemv_b{b}"] = {"ms": t, "bytes": byt, "gbs": byt / t / 1e6,
-                                             "frac_hbm": byt / t / 1e6 / hbm,
-                                             "gflops": 2.0 * keep * bh * 32 * b / t / 1e6}
+
+            def make(r, bh=bh, keep=keep, wsb=wsb, csr_b=csr_b, vals_b=vals_b, b=b, plan=plan):
+                Wr, ws, csr, vals = weight(r % 4), empty(wsb), empty(csr_b), empty(vals_b)
+                if bh == 1:
+                    nb.nm_prune_vector_wise(Wr, M, K, K, "f16", 32, keep, nb.NM_SCORE_ABS_OF_SUM, csr=csr, vals=vals,
+                                            workspace=ws, workspace_bytes=wsb)
+                else:
+                    nb.nm_prune_block_wise(Wr, M, K, K, "f16", 32, 32, keep, csr=csr, vals=vals, workspace=ws,
+                                           workspace_bytes=wsb)
+                x = inputs.normal((b, K), 1.0, inputs.SEED_VEC + r, "f16", device=dev)
+                y = torch.empty((b, M), dtype=torch.float16, device=dev)
+                return lambda: nb.nm_spmm(plan, 1.0, vals, csr, x, 0.0, None, y)
+            byt = vals_b + csr_b + b * K * 2 + b * M * 2
+            row = hbm_row(torch, make, byt, hbm, flush)
+            row["gflops"] = 2.0 * keep * bh * 32 * b / row["ms"] / 1e6
+            rows[f"S9_{uname}_gemv_b{b}"] = row
             plan.destroy()
+        torch.cuda.empty_cache()
 
     # BERT-Large-shaped sparse products (f16) with cuBLAS on the same shapes
     for (Mb, Nb, Kb) in inputs.BERT_SHAPES:
@@ -391,7 +461,8 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
                                                 "cublas_dense_tflops": f / tc / 1e9, "speedup_vs_cublas": tc / t}
         plan.destroy()
     rows["_peaks"] = {"sparse_tflops": sparse_peak, "dense_tflops": dense_peak, "hbm_gbs": hbm,
-                      "note": "burst peaks (isolated launches, L2 flushed before each)"}
+                      "note": "tensor rows: one launch after an L2 flush, burst peaks; HBM rows: back-to-back "
+                              "launches over copies larger than L2 (ms), and one flushed launch (ms_single)"}
     return rows
 
 

@@ -172,6 +172,113 @@ __global__ void __launch_bounds__(256) prune24_kernel(const typename Elem<DT>::T
   }
 }
 
+// 2:4 selection of one 16-element segment: kept values in position order,
+// 16-bit keep mask and 16-bit canonical code word.
+template <int DT>
+__device__ __forceinline__ void select24(const typename Elem<DT>::T (&v)[16], typename Elem<DT>::T (&kv)[8],
+                                         uint32_t& keep, uint32_t& code) {
+  keep = 0;
+  code = 0;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const typename Elem<DT>::T* e = v + 4 * g;
+    const uint32_t km = keep2of4(Elem<DT>::key(e[0]), Elem<DT>::key(e[1]), Elem<DT>::key(e[2]), Elem<DT>::key(e[3]));
+    const uint32_t i0 = (km & 1u) ? 0u : ((km & 2u) ? 1u : 2u);
+    const uint32_t i1 = (km & 8u) ? 3u : ((km & 4u) ? 2u : 1u);
+    kv[2 * g] = (km & 1u) ? e[0] : ((km & 2u) ? e[1] : e[2]);
+    kv[2 * g + 1] = (km & 8u) ? e[3] : ((km & 4u) ? e[2] : e[1]);
+    keep |= km << (4 * g);
+    code |= (i0 | (i1 << 2)) << (4 * g);
+  }
+}
+
+template <typename T, int NW>
+__device__ __forceinline__ void unpack_words(const uint32_t (&w)[NW], T (&v)[4 * NW / sizeof(T)]) {
+#pragma unroll
+  for (int j = 0; j < 4 * NW / (int)sizeof(T); ++j) {
+    if constexpr (sizeof(T) == 2)
+      v[j] = (T)(w[j / 2] >> (16 * (j % 2)));
+    else
+      v[j] = (T)(int8_t)(w[j / 4] >> (8 * (j % 4)));
+  }
+}
+template <typename T, int NW>
+__device__ __forceinline__ void pack_words(const T (&v)[4 * NW / sizeof(T)], uint32_t (&w)[NW]) {
+#pragma unroll
+  for (int i = 0; i < NW; ++i) w[i] = 0;
+#pragma unroll
+  for (int j = 0; j < 4 * NW / (int)sizeof(T); ++j) {
+    if constexpr (sizeof(T) == 2)
+      w[j / 2] |= (uint32_t)(uint16_t)v[j] << (16 * (j % 2));
+    else
+      w[j / 4] |= (uint32_t)(uint8_t)v[j] << (8 * (j % 4));
+  }
+}
+
+// 2:4 for aligned rows whose length is a multiple of 32: one thread per 32
+// columns (two segments), all loads of the pair issued before any selection,
+// one mask word and one 32-bit canonical metadata word per thread; the grid
+// covers the matrix in a single pass.
+template <int DT>
+__global__ void __launch_bounds__(256) prune24_pair_kernel(const typename Elem<DT>::T* __restrict__ W, int64_t rows,
+                                                           int64_t cols, int64_t ld, typename Elem<DT>::T* W_out,
+                                                           int64_t ld_out, uint32_t* __restrict__ mask_bits,
+                                                           typename Elem<DT>::T* __restrict__ vals,
+                                                           void* __restrict__ meta, int meta_tc) {
+  using T = typename Elem<DT>::T;
+  constexpr int kWords = 16 * (int)sizeof(T) / 4;  // 32-bit words of one segment: 8 or 4
+  const int64_t ppr = cols / 32;                   // pairs per row
+  const int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (idx >= rows * ppr) return;
+  const int64_t r = idx / ppr, p = idx - r * ppr;
+  const uint4* src = reinterpret_cast<const uint4*>(W + r * ld + p * 32);
+  uint32_t w[2][kWords];
+#pragma unroll
+  for (int q = 0; q < kWords / 2; ++q) {  // 16-byte loads: 4 (16-bit) or 2 (int8) per pair
+    const uint4 a = __ldcs(src + q);
+    const int h = (4 * q) / kWords, o = (4 * q) % kWords;
+    w[h][o] = a.x, w[h][o + 1] = a.y, w[h][o + 2] = a.z, w[h][o + 3] = a.w;
+  }
+  uint32_t keep[2], code[2];
+  T kv[2][8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    T v[16];
+    unpack_words<T, kWords>(w[h], v);
+    select24<DT>(v, kv[h], keep[h], code[h]);
+    if (W_out != nullptr) {
+      T o[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j] = ((keep[h] >> j) & 1u) ? v[j] : (T)0;
+      uint32_t ow[kWords];
+      pack_words<T, kWords>(o, ow);
+      uint4* dst = reinterpret_cast<uint4*>(W_out + r * ld_out + p * 32 + 16 * h);
+#pragma unroll
+      for (int q = 0; q < kWords / 4; ++q) dst[q] = make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
+    }
+  }
+  if (vals != nullptr) {
+    T all[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) all[j] = kv[0][j], all[8 + j] = kv[1][j];
+    uint32_t vw[kWords];
+    pack_words<T, kWords>(all, vw);
+    uint4* vo = reinterpret_cast<uint4*>(vals + r * (cols / 2) + p * 16);
+#pragma unroll
+    for (int q = 0; q < kWords / 4; ++q) vo[q] = make_uint4(vw[4 * q], vw[4 * q + 1], vw[4 * q + 2], vw[4 * q + 3]);
+  }
+  if (meta != nullptr) {
+    if (meta_tc) {
+      const int64_t nslots = ((rows + 127) / 128) * 128;
+      tc_store(meta, r, 2 * p, nslots, code[0]);
+      tc_store(meta, r, 2 * p + 1, nslots, code[1]);
+    } else {
+      reinterpret_cast<uint32_t*>(meta)[r * ppr + p] = code[0] | (code[1] << 16);
+    }
+  }
+  if (mask_bits != nullptr) mask_bits[r * ppr + p] = keep[0] | (keep[1] << 16);
+}
+
 // General n:m (m <= 32), one thread per group.  Composite keys (key << 5 |
 // (31 - position)) are all distinct; an element is kept when fewer than n
 // composite keys of its group exceed its own.
@@ -503,7 +610,11 @@ cudaError_t prune_dt(const PruneLaunch& a, cudaStream_t s) {
     const int64_t es = (int64_t)sizeof(T);
     const bool vec = !a.trans && (a.colsL % 16 == 0) && (a.ld * es) % 16 == 0 && aligned16(W) &&
                      (W_out == nullptr || ((a.ld_out * es) % 16 == 0 && aligned16(W_out))) && aligned16(vals);
-    if (vec)
+    if (vec && a.colsL % 32 == 0) {
+      const int64_t pairs = a.rowsL * (a.colsL / 32);
+      prune24_pair_kernel<DT><<<(unsigned)((pairs + threads - 1) / threads), threads, 0, s>>>(
+          W, a.rowsL, a.colsL, a.ld, W_out, a.ld_out, a.mask_bits, vals, a.meta, a.meta_tc);
+    } else if (vec)
       prune24_kernel<DT, true, false><<<grid, threads, 0, s>>>(W, a.rowsL, a.colsL, a.ld, W_out, a.ld_out,
                                                                 a.mask_bits, vals, a.meta, a.meta_tc);
     else if (!a.trans)

@@ -29,36 +29,57 @@ __device__ __forceinline__ uint16_t from_f(float x, int bf16) {
   return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
 }
 
+// NB = batch columns per pass (1 or 8).  x is staged in shared memory as
+// [k][NB]; the staging reads B with 16-byte loads when rows of B allow it.
+template <int NB>
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ vals, const uint8_t* __restrict__ idx,
                                                      const uint16_t* __restrict__ B, const uint16_t* __restrict__ C,
                                                      uint16_t* __restrict__ D, int64_t M, int64_t N, int64_t K, int n,
                                                      int m, int64_t ldb, int64_t ldc, int64_t ldd, int cd_col,
                                                      float alpha, float beta, int bf16) {
-  extern __shared__ uint4 xs4[];  // K x kBatch halves, [k][b]
+  extern __shared__ uint4 xs4[];  // K x NB halves, [k][b]
   uint16_t* xs = reinterpret_cast<uint16_t*>(xs4);
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const int64_t kc = (K / m) * n;  // kept values per row
   const bool vec = (kc % 8 == 0);
-  for (int64_t b0 = 0; b0 < N; b0 += kBatch) {
-    const int nb = (int)(N - b0 < kBatch ? N - b0 : kBatch);
+  const bool vstage = (K % 8 == 0);
+  for (int64_t b0 = 0; b0 < N; b0 += NB) {
+    const int nb = (int)(N - b0 < NB ? N - b0 : NB);
     __syncthreads();
-    for (int64_t i = threadIdx.x; i < K * kBatch; i += blockDim.x) {
-      const int64_t k = i / kBatch;
-      const int b = (int)(i - k * kBatch);
-      xs[i] = (b < nb) ? B[(b0 + b) * ldb + k] : (uint16_t)0;
+    if (vstage) {
+      const int64_t k8 = K / 8;
+      for (int64_t i = threadIdx.x; i < k8 * NB; i += blockDim.x) {
+        const int b = (int)(i / k8);
+        const int64_t kk = (i - (int64_t)b * k8) * 8;
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (b < nb) q = __ldg(reinterpret_cast<const uint4*>(B + (b0 + b) * ldb + kk));
+        if constexpr (NB == 1) {
+          reinterpret_cast<uint4*>(xs)[i] = q;
+        } else {
+          const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int t = 0; t < 8; ++t) xs[(kk + t) * NB + b] = (uint16_t)(qw[t / 2] >> (16 * (t % 2)));
+        }
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < K * NB; i += blockDim.x) {
+        const int64_t k = i / NB;
+        const int b = (int)(i - k * NB);
+        xs[i] = (b < nb) ? B[(b0 + b) * ldb + k] : (uint16_t)0;
+      }
     }
     __syncthreads();
     for (int64_t r = blockIdx.x * (int64_t)warps + (threadIdx.x >> 5); r < M; r += (int64_t)gridDim.x * warps) {
-      float acc[kBatch];
+      float acc[NB];
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) acc[b] = 0.0f;
+      for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
       const uint16_t* vr = vals + r * kc;
       const uint8_t* ir = idx + r * kc;
       if (vec) {
         for (int64_t j0 = (int64_t)lane * 8; j0 < kc; j0 += 256) {
-          const uint4 v4 = *reinterpret_cast<const uint4*>(vr + j0);
-          const uint2 i2 = *reinterpret_cast<const uint2*>(ir + j0);
+          const uint4 v4 = __ldcs(reinterpret_cast<const uint4*>(vr + j0));
+          const uint2 i2 = __ldcs(reinterpret_cast<const uint2*>(ir + j0));
           const uint32_t vw[4] = {v4.x, v4.y, v4.z, v4.w};
           const uint32_t iw[2] = {i2.x, i2.y};
 #pragma unroll
@@ -66,10 +87,14 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
             const int64_t j = j0 + t;
             const int64_t k = (j / n) * m + min((iw[t / 4] >> (8 * (t % 4))) & 0xFFu, (uint32_t)(m - 1));
             const float a = to_f((uint16_t)(vw[t / 2] >> (16 * (t % 2))), bf16);
-            const uint4 x4 = *reinterpret_cast<const uint4*>(xs + k * kBatch);
-            const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
+            if constexpr (NB == 1) {
+              acc[0] = fmaf(a, to_f(xs[k], bf16), acc[0]);
+            } else {
+              const uint4 x4 = *reinterpret_cast<const uint4*>(xs + k * NB);
+              const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-            for (int b = 0; b < kBatch; ++b) acc[b] = fmaf(a, to_f((uint16_t)(xw[b / 2] >> (16 * (b % 2))), bf16), acc[b]);
+              for (int b = 0; b < NB; ++b) acc[b] = fmaf(a, to_f((uint16_t)(xw[b / 2] >> (16 * (b % 2))), bf16), acc[b]);
+            }
           }
         }
       } else {
@@ -77,17 +102,17 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
           const int64_t k = (j / n) * m + min((int)ir[j], m - 1);
           const float a = to_f(vr[j], bf16);
 #pragma unroll
-          for (int b = 0; b < kBatch; ++b) acc[b] = fmaf(a, to_f(xs[k * kBatch + b], bf16), acc[b]);
+          for (int b = 0; b < NB; ++b) acc[b] = fmaf(a, to_f(xs[k * NB + b], bf16), acc[b]);
         }
       }
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b)
+      for (int b = 0; b < NB; ++b)
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc[b] += __shfl_xor_sync(0xFFFFFFFFu, acc[b], off);
       if (lane < nb) {
         float x = 0.0f;
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b)
+        for (int b = 0; b < NB; ++b)
           if (b == lane) x = acc[b];
         x *= alpha;
         const int64_t bb = b0 + lane;
@@ -99,11 +124,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
   }
 }
 
-}  // namespace
-
-cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s) {
+template <int NB>
+cudaError_t gather_launch(const SpmmLaunch& a, cudaStream_t s) {
   const nm_spmm_desc_t& d = a.d;
-  const size_t smem = (size_t)d.K * kBatch * 2;
+  const size_t smem = (size_t)d.K * NB * 2;
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     // set once per device to the largest size this kernel may take
@@ -112,7 +136,7 @@ cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s) {
     if (cudaError_t e = cudaGetDevice(&dev)) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(done_mask.load() & bit)) {
-      cudaError_t e = cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      cudaError_t e = cudaFuncSetAttribute(gather_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
       if (e != cudaSuccess) return e;
       done_mask.fetch_or(bit);
     }
@@ -121,11 +145,17 @@ cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s) {
   int64_t blocks = (d.M + 7) / 8;
   if (blocks > 152 * 2) blocks = 152 * 2;
   if (blocks < 1) blocks = 1;
-  gather_kernel<<<(unsigned)blocks, threads, smem, s>>>(
+  gather_kernel<NB><<<(unsigned)blocks, threads, smem, s>>>(
       static_cast<const uint16_t*>(a.A), static_cast<const uint8_t*>(a.A_meta), static_cast<const uint16_t*>(a.B),
       static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.M, d.N, d.K, d.n, d.m, d.ldb, d.ldc, d.ldd,
       d.order_cd == NM_COL, a.alpha_f, a.beta_f, d.ab_type == NM_BF16);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s) {
+  return a.d.N == 1 ? gather_launch<1>(a, s) : gather_launch<kBatch>(a, s);
 }
 
 // ---------------------------------------------------------------------------
