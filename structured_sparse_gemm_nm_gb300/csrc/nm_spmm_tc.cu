@@ -15,7 +15,8 @@
 // each fetches half of the shared B tile and multicasts it to both, which
 // halves the L2 traffic of B.  Warp roles per CTA:
 //   warp 0       TMA producer: A and (its half of) B for stages of 64 dense K
-//   warp 1       owns tensor memory; one lane issues tcgen05.mma
+//   warp 1       owns tensor memory; one lane issues the tcgen05.mma of
+//                columns 0..127 of the tile (M128 N128 per instruction)
 //   warps 2..5   SPARSE metadata: each warp loads one 32-bit code word per
 //                lane (row slot) and k-step from global memory and writes it
 //                with tcgen05.st into one of four 64-column-aligned TMEM
@@ -29,6 +30,10 @@
 //   warps 6..13  epilogue: drain the FP32 accumulator (alpha, mask) into
 //                packed registers, release it, then stage 32 x 32 blocks in
 //                shared memory and write them with TMA bulk stores
+//   warp 14      one lane issues the tcgen05.mma of columns 128..255; an MMA
+//                holds its issuing thread for about its execution time, so two
+//                issuers keep the tensor pipe busy through each other's
+//                barrier waits, commits and loop overhead
 // Every mbarrier wait is bounded; a wait that gives up sets an abort flag
 // and NM_ERR_TIMEOUT in the caller's status word, the roles drain their
 // outstanding asynchronous work and the CTA frees its tensor memory.
@@ -51,7 +56,8 @@ constexpr int BN = 256;
 constexpr int kKPerStage = 64;  // dense-equivalent K per stage
 constexpr int kMetaWarp0 = 2, kMetaWarps = 4;
 constexpr int kEpiWarp0 = kMetaWarp0 + kMetaWarps, kEpiWarps = 8;
-constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kMmaWarpB = kEpiWarp0 + kEpiWarps;  // second MMA issuer (columns 128..255)
+constexpr int kThreads = 32 * (kMmaWarpB + 1);
 constexpr int kTmemCols = 512;
 constexpr int kMetaCol = 256, kMetaColStride = 64;  // four metadata slots: columns 256, 320, 384, 448
 constexpr int kEpiBufBytes = 32 * 32 * 2;  // one 32 x 32 output block
@@ -183,10 +189,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
 }
 constexpr uint32_t kSwizzle128 = 2, kSwizzle64 = 4;
 
-// Instruction descriptor for kind::f16: D = F32, A/B = F16 or BF16, M = 128, N = 256.
+// Instruction descriptor for kind::f16: D = F32, A/B = F16 or BF16, M = 128, N = 128
+// (each of the two issuers computes one 128-column half of the tile).
 __device__ __forceinline__ uint32_t idesc_f16(int bf16, int a_mn, int b_mn, bool sparse) {
   uint32_t d = (1u << 4) | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10) | ((uint32_t)a_mn << 15) |
-               ((uint32_t)b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+               ((uint32_t)b_mn << 16) | ((uint32_t)((BN / 2) >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   if (sparse) d |= 1u << 2;
   return d;
 }
@@ -278,7 +285,7 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int cl, int 
 }
 
 // ----------------------------------------------------------------- kernel
-// 14 warps are resident as 16 for register allocation (warps are allocated in
+// 15 warps are resident as 16 for register allocation (warps are allocated in
 // groups of four), so 128 registers per thread is the most that still fits
 // the 64K-register file.
 template <bool SPARSE, int CL>
@@ -304,13 +311,13 @@ __global__ void __maxnreg__(128)
     for (int s = 0; s < C::kStages; ++s) {
       // SPARSE: the producer's expect_tx arrival and one arrival per metadata warp
       mbar_init(bar_full + 8 * s, SPARSE ? 1 + kMetaWarps : 1);
-      mbar_init(bar_empty + 8 * s, CL);  // released by the MMA of every CTA that reads the stage
+      mbar_init(bar_empty + 8 * s, 2 * CL);  // released by both issuers of every CTA that reads the stage
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tfull + 8 * a, 2);  // both issuers
       mbar_init(bar_tempty + 8 * a, kEpiWarps);
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -387,9 +394,14 @@ __global__ void __maxnreg__(128)
           }
         }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == kMmaWarpB) {
+    // ------------------------------------------------------- MMA issuers
+    // Two single-thread issuers share every stage: warp 1 computes columns
+    // 0..127 and warp kMmaWarpB columns 128..255 of the tile.  An MMA holds
+    // its issuing thread for about its execution time, so while one issuer
+    // waits, commits and loops, the other one keeps the tensor pipe busy.
     if (lane == 0) {
+      const uint32_t nhalf = warp == 1 ? 0u : 1u;
       const uint32_t idesc = idesc_f16(p.bf16, SPARSE ? 0 : p.a_mn, SPARSE ? 0 : p.b_mn, SPARSE);
       int stage = 0;
       uint32_t phase = 0;
@@ -403,7 +415,8 @@ __global__ void __maxnreg__(128)
       //   SPARSE B: 256 rows x 128 B (128B swizzle), 64 B per k-step
       //   DENSE A/B K-major: 128B swizzle, 32 B per K16 step; MN-major: 2048 B per K16 step
       constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
-      const uint32_t sA0 = smem_u32(smem), sB0 = sA0 + C::kATileBytes;
+      // B's second 128 rows (K-major) or second two 64-column atoms (MN-major) start 16 KB in
+      const uint32_t sA0 = smem_u32(smem), sB0 = sA0 + C::kATileBytes + 16384u * nhalf;
       uint64_t a_desc0, b_desc0;
       uint32_t a_step = 0, b_step = 0;
       if constexpr (SPARSE) {
@@ -416,12 +429,13 @@ __global__ void __maxnreg__(128)
         b_step = p.b_mn ? (2048 >> 4) : (32 >> 4);
       }
       bool ok = true;
-      if (p.fault_test) ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);  // nothing arrives: runs out
+      if (p.fault_test && nhalf == 0)  // the drain barrier cannot complete before this issuer commits: runs out
+        ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);
       for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
         const Unit t = decode_unit(p, u, CL, rank);
         if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag, p.wait_budget, p.status)) break;
         tc_fence_after();
-        const uint32_t tacc = tmem + acc * BN;
+        const uint32_t tacc = tmem + acc * BN + (BN / 2) * nhalf;
         int kstep = 0;  // MMA k-steps issued for this tile
         for (int ks = t.kbeg; ks < t.kend; ++ks) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
