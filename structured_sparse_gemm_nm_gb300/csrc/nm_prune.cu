@@ -172,51 +172,35 @@ __global__ void __launch_bounds__(256) prune24_kernel(const typename Elem<DT>::T
   }
 }
 
-// 2:4 selection of one 16-element segment: kept values in position order,
-// 16-bit keep mask and 16-bit canonical code word.
-template <int DT>
-__device__ __forceinline__ void select24(const typename Elem<DT>::T (&v)[16], typename Elem<DT>::T (&kv)[8],
-                                         uint32_t& keep, uint32_t& code) {
-  keep = 0;
-  code = 0;
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const typename Elem<DT>::T* e = v + 4 * g;
-    const uint32_t km = keep2of4(Elem<DT>::key(e[0]), Elem<DT>::key(e[1]), Elem<DT>::key(e[2]), Elem<DT>::key(e[3]));
-    const uint32_t i0 = (km & 1u) ? 0u : ((km & 2u) ? 1u : 2u);
-    const uint32_t i1 = (km & 8u) ? 3u : ((km & 4u) ? 2u : 1u);
-    kv[2 * g] = (km & 1u) ? e[0] : ((km & 2u) ? e[1] : e[2]);
-    kv[2 * g + 1] = (km & 8u) ? e[3] : ((km & 4u) ? e[2] : e[1]);
-    keep |= km << (4 * g);
-    code |= (i0 | (i1 << 2)) << (4 * g);
-  }
+// Positions of the two largest of four keys, lower position first on ties,
+// as the 4-bit code i0 | i1 << 2.  Composite keys (key << 2 | (3 - position))
+// are distinct and order exactly like the rule; the second largest of four is
+// max(min of the two pair maxima, max of the two pair minima).
+__device__ __forceinline__ uint32_t top2of4(uint32_t k0, uint32_t k1, uint32_t k2, uint32_t k3) {
+  const uint32_t c0 = (k0 << 2) | 3u, c1 = (k1 << 2) | 2u, c2 = (k2 << 2) | 1u, c3 = k3 << 2;
+  const uint32_t a = max(c0, c1), b = min(c0, c1), c = max(c2, c3), d = min(c2, c3);
+  const uint32_t first = max(a, c), second = max(min(a, c), max(b, d));
+  const uint32_t t = first & 3u, u = second & 3u;  // 3 - position
+  return (max(t, u) | (min(t, u) << 2)) ^ 15u;
 }
+__device__ __forceinline__ uint32_t keep_of_code(uint32_t code) { return (1u << (code & 3u)) | (1u << (code >> 2)); }
 
-template <typename T, int NW>
-__device__ __forceinline__ void unpack_words(const uint32_t (&w)[NW], T (&v)[4 * NW / sizeof(T)]) {
-#pragma unroll
-  for (int j = 0; j < 4 * NW / (int)sizeof(T); ++j) {
-    if constexpr (sizeof(T) == 2)
-      v[j] = (T)(w[j / 2] >> (16 * (j % 2)));
-    else
-      v[j] = (T)(int8_t)(w[j / 4] >> (8 * (j % 4)));
-  }
+template <int DT>
+__device__ __forceinline__ uint32_t key_lo(uint32_t w) {
+  return min(w & 0x7FFFu, DT == kF16 ? 0x7C01u : 0x7F81u);
 }
-template <typename T, int NW>
-__device__ __forceinline__ void pack_words(const T (&v)[4 * NW / sizeof(T)], uint32_t (&w)[NW]) {
-#pragma unroll
-  for (int i = 0; i < NW; ++i) w[i] = 0;
-#pragma unroll
-  for (int j = 0; j < 4 * NW / (int)sizeof(T); ++j) {
-    if constexpr (sizeof(T) == 2)
-      w[j / 2] |= (uint32_t)(uint16_t)v[j] << (16 * (j % 2));
-    else
-      w[j / 4] |= (uint32_t)(uint8_t)v[j] << (8 * (j % 4));
-  }
+template <int DT>
+__device__ __forceinline__ uint32_t key_hi(uint32_t w) {
+  return min((w >> 16) & 0x7FFFu, DT == kF16 ? 0x7C01u : 0x7F81u);
+}
+__device__ __forceinline__ uint32_t key_i8(uint32_t w, int b) {
+  const int x = (int)(int8_t)(w >> (8 * b));
+  return (uint32_t)(x < 0 ? -x : x);
 }
 
 // 2:4 for aligned rows whose length is a multiple of 32: one thread per 32
 // columns (two segments), all loads of the pair issued before any selection,
+// selection on packed words (one byte permute gathers a group's kept pair),
 // one mask word and one 32-bit canonical metadata word per thread; the grid
 // covers the matrix in a single pass.
 template <int DT>
@@ -226,57 +210,65 @@ __global__ void __launch_bounds__(256) prune24_pair_kernel(const typename Elem<D
                                                            typename Elem<DT>::T* __restrict__ vals,
                                                            void* __restrict__ meta, int meta_tc) {
   using T = typename Elem<DT>::T;
-  constexpr int kWords = 16 * (int)sizeof(T) / 4;  // 32-bit words of one segment: 8 or 4
-  const int64_t ppr = cols / 32;                   // pairs per row
+  constexpr bool k16 = sizeof(T) == 2;
+  constexpr int kWords = k16 ? 16 : 8;  // 32-bit words of the thread's 32 elements
+  const int64_t ppr = cols / 32;        // pairs of segments per row
   const int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (idx >= rows * ppr) return;
   const int64_t r = idx / ppr, p = idx - r * ppr;
   const uint4* src = reinterpret_cast<const uint4*>(W + r * ld + p * 32);
-  uint32_t w[2][kWords];
+  uint32_t w[kWords];
 #pragma unroll
-  for (int q = 0; q < kWords / 2; ++q) {  // 16-byte loads: 4 (16-bit) or 2 (int8) per pair
+  for (int q = 0; q < kWords / 4; ++q) {
     const uint4 a = __ldcs(src + q);
-    const int h = (4 * q) / kWords, o = (4 * q) % kWords;
-    w[h][o] = a.x, w[h][o + 1] = a.y, w[h][o + 2] = a.z, w[h][o + 3] = a.w;
+    w[4 * q] = a.x, w[4 * q + 1] = a.y, w[4 * q + 2] = a.z, w[4 * q + 3] = a.w;
   }
-  uint32_t keep[2], code[2];
-  T kv[2][8];
+  // eight groups of four
+  uint32_t code = 0, keep = 0;
+  uint32_t vw[k16 ? 8 : 4];  // kept values, packed
+  uint32_t ow[kWords];       // pruned copy
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    T v[16];
-    unpack_words<T, kWords>(w[h], v);
-    select24<DT>(v, kv[h], keep[h], code[h]);
-    if (W_out != nullptr) {
-      T o[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) o[j] = ((keep[h] >> j) & 1u) ? v[j] : (T)0;
-      uint32_t ow[kWords];
-      pack_words<T, kWords>(o, ow);
-      uint4* dst = reinterpret_cast<uint4*>(W_out + r * ld_out + p * 32 + 16 * h);
-#pragma unroll
-      for (int q = 0; q < kWords / 4; ++q) dst[q] = make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
+  for (int g = 0; g < 8; ++g) {
+    uint32_t c, km;
+    if constexpr (k16) {
+      const uint32_t w0 = w[2 * g], w1 = w[2 * g + 1];
+      c = top2of4(key_lo<DT>(w0), key_hi<DT>(w0), key_lo<DT>(w1), key_hi<DT>(w1));
+      const uint32_t i0 = c & 3u, i1 = c >> 2;
+      vw[g] = __byte_perm(w0, w1, (i0 * 0x22u + 0x10u) | ((i1 * 0x22u + 0x10u) << 8));
+      km = keep_of_code(c);
+      ow[2 * g] = w0 & ((km & 1u) * 0xFFFFu | (km & 2u) * 0x7FFF8000u);
+      ow[2 * g + 1] = w1 & (((km >> 2) & 1u) * 0xFFFFu | ((km >> 2) & 2u) * 0x7FFF8000u);
+    } else {
+      const uint32_t w0 = w[g];
+      c = top2of4(key_i8(w0, 0), key_i8(w0, 1), key_i8(w0, 2), key_i8(w0, 3));
+      const uint32_t kv = __byte_perm(w0, 0u, (c & 3u) | ((c >> 2) << 4)) & 0xFFFFu;
+      if (g % 2 == 0) vw[g / 2] = kv; else vw[g / 2] |= kv << 16;
+      km = keep_of_code(c);
+      ow[g] = w0 & ((km & 1u) * 0xFFu | (km & 2u) * 0x7F80u | (km & 4u) * 0x3FC000u | (km & 8u) * 0x1FE00000u);
     }
+    code |= c << (4 * g);
+    keep |= km << (4 * g);
+  }
+  if (W_out != nullptr) {
+    uint4* dst = reinterpret_cast<uint4*>(W_out + r * ld_out + p * 32);
+#pragma unroll
+    for (int q = 0; q < kWords / 4; ++q) dst[q] = make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
   }
   if (vals != nullptr) {
-    T all[16];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) all[j] = kv[0][j], all[8 + j] = kv[1][j];
-    uint32_t vw[kWords];
-    pack_words<T, kWords>(all, vw);
     uint4* vo = reinterpret_cast<uint4*>(vals + r * (cols / 2) + p * 16);
 #pragma unroll
-    for (int q = 0; q < kWords / 4; ++q) vo[q] = make_uint4(vw[4 * q], vw[4 * q + 1], vw[4 * q + 2], vw[4 * q + 3]);
+    for (int q = 0; q < (k16 ? 2 : 1); ++q) vo[q] = make_uint4(vw[4 * q], vw[4 * q + 1], vw[4 * q + 2], vw[4 * q + 3]);
   }
   if (meta != nullptr) {
     if (meta_tc) {
       const int64_t nslots = ((rows + 127) / 128) * 128;
-      tc_store(meta, r, 2 * p, nslots, code[0]);
-      tc_store(meta, r, 2 * p + 1, nslots, code[1]);
+      tc_store(meta, r, 2 * p, nslots, code & 0xFFFFu);
+      tc_store(meta, r, 2 * p + 1, nslots, code >> 16);
     } else {
-      reinterpret_cast<uint32_t*>(meta)[r * ppr + p] = code[0] | (code[1] << 16);
+      reinterpret_cast<uint32_t*>(meta)[r * ppr + p] = code;
     }
   }
-  if (mask_bits != nullptr) mask_bits[r * ppr + p] = keep[0] | (keep[1] << 16);
+  if (mask_bits != nullptr) mask_bits[r * ppr + p] = keep;
 }
 
 // General n:m (m <= 32), one thread per group.  Composite keys (key << 5 |
@@ -589,6 +581,74 @@ __global__ void __launch_bounds__(256) check_kernel(const typename Elem<DT>::T* 
 
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Byte-permute selectors that scatter a group's kept pair back to its four
+// positions: for code i0 | i1 << 2, output element t takes the first kept
+// value if t == i0, the second if t == i1, zero otherwise.  16-bit elements:
+// two selectors (elements 0-1, 2-3) in one word; int8: one selector.
+__host__ __device__ constexpr uint32_t scatter_nibble16(uint32_t code, int t) {
+  return (uint32_t)t == (code & 3u) ? 0x10u : ((uint32_t)t == (code >> 2) ? 0x32u : 0x44u);
+}
+__host__ __device__ constexpr uint32_t scatter_sel16(uint32_t code) {
+  return scatter_nibble16(code, 0) | (scatter_nibble16(code, 1) << 8) | (scatter_nibble16(code, 2) << 16) |
+         (scatter_nibble16(code, 3) << 24);
+}
+__host__ __device__ constexpr uint32_t scatter_sel8(uint32_t code) {
+  uint32_t sel = 0;
+  for (int t = 0; t < 4; ++t)
+    sel |= ((uint32_t)t == (code & 3u) ? 0u : ((uint32_t)t == (code >> 2) ? 1u : 4u)) << (4 * t);
+  return sel;
+}
+
+// Decompression for aligned rows whose length is a multiple of 32: one thread
+// per 32 columns; the kept values and codes are loaded as words, each group's
+// four outputs come from byte permutes with a selector looked up by its code.
+template <int DT>
+__global__ void __launch_bounds__(256) decompress24_pair_kernel(const typename Elem<DT>::T* __restrict__ vals,
+                                                                const void* __restrict__ meta, int64_t rows,
+                                                                int64_t cols, int meta_tc,
+                                                                typename Elem<DT>::T* __restrict__ W_out,
+                                                                int64_t ld_out) {
+  using T = typename Elem<DT>::T;
+  constexpr bool k16 = sizeof(T) == 2;
+  __shared__ uint32_t sel[16];
+  if (threadIdx.x < 16) sel[threadIdx.x] = k16 ? scatter_sel16(threadIdx.x) : scatter_sel8(threadIdx.x);
+  __syncthreads();
+  const int64_t ppr = cols / 32;
+  const int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (idx >= rows * ppr) return;
+  const int64_t r = idx / ppr, p = idx - r * ppr;
+  uint32_t code;
+  if (meta_tc) {
+    const int64_t nslots = ((rows + 127) / 128) * 128;
+    const char* mb = reinterpret_cast<const char*>(meta);
+    code = *reinterpret_cast<const uint16_t*>(mb + tc_half_offset(r, 2 * p, nslots)) |
+           ((uint32_t)*reinterpret_cast<const uint16_t*>(mb + tc_half_offset(r, 2 * p + 1, nslots)) << 16);
+  } else {
+    code = __ldcs(reinterpret_cast<const uint32_t*>(meta) + r * ppr + p);
+  }
+  const uint4* vin = reinterpret_cast<const uint4*>(vals + r * (cols / 2) + p * 16);
+  uint32_t kw[k16 ? 8 : 4];
+#pragma unroll
+  for (int q = 0; q < (k16 ? 2 : 1); ++q) {
+    const uint4 a = __ldcs(vin + q);
+    kw[4 * q] = a.x, kw[4 * q + 1] = a.y, kw[4 * q + 2] = a.z, kw[4 * q + 3] = a.w;
+  }
+  uint32_t ow[k16 ? 16 : 8];
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const uint32_t sg = sel[(code >> (4 * g)) & 0xFu];
+    if constexpr (k16) {
+      ow[2 * g] = __byte_perm(kw[g], 0u, sg & 0xFFFFu);
+      ow[2 * g + 1] = __byte_perm(kw[g], 0u, sg >> 16);
+    } else {
+      ow[g] = __byte_perm(kw[g / 2] >> (16 * (g % 2)), 0u, sg);
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(W_out + r * ld_out + p * 32);
+#pragma unroll
+  for (int q = 0; q < (k16 ? 4 : 2); ++q) dst[q] = make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
+}
+
 template <int DT>
 cudaError_t prune_dt(const PruneLaunch& a, cudaStream_t s) {
   using T = typename Elem<DT>::T;
@@ -670,7 +730,13 @@ cudaError_t decompress_dt(const DecompressLaunch& a, cudaStream_t s) {
     const int64_t segs = (a.cols + 15) / 16;
     const unsigned grid = grid_for(a.rows * segs, threads);
     const bool vec = sizeof(T) == 2 && a.cols % 16 == 0 && (a.ld_out * 2) % 16 == 0 && aligned16(W_out);
-    if (vec)
+    const bool pair = a.cols % 32 == 0 && (a.ld_out * (int64_t)sizeof(T)) % 16 == 0 && aligned16(W_out) &&
+                      aligned16(vals) && (a.meta_tc || (reinterpret_cast<uintptr_t>(a.meta) & 3u) == 0);
+    if (pair) {
+      const int64_t pairs = a.rows * (a.cols / 32);
+      decompress24_pair_kernel<DT><<<(unsigned)((pairs + threads - 1) / threads), threads, 0, s>>>(
+          vals, a.meta, a.rows, a.cols, a.meta_tc, W_out, a.ld_out);
+    } else if (vec)
       decompress24_kernel<DT, true><<<grid, threads, 0, s>>>(vals, a.meta, a.rows, a.cols, a.meta_tc, W_out, a.ld_out);
     else
       decompress24_kernel<DT, false><<<grid, threads, 0, s>>>(vals, a.meta, a.rows, a.cols, a.meta_tc, W_out,

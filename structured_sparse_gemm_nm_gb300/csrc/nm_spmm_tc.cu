@@ -62,13 +62,15 @@ constexpr int kTmemCols = 512;
 constexpr int kMetaCol = 256, kMetaColStride = 64;  // four metadata slots: columns 256, 320, 384, 448
 constexpr int kEpiBufBytes = 32 * 32 * 2;  // one 32 x 32 output block
 
-template <bool SPARSE>
+// PAIR: the two CTAs of a cluster run one M256 x N256 product (tcgen05 with
+// cta_group::2); each holds its 128 rows of A and one 128-row half of B.
+template <bool SPARSE, bool PAIR = false>
 struct Cfg {
   // SPARSE A: 128 rows x 32 compressed values (64B swizzle); dense A: 128 x 64 (128B swizzle).
   static constexpr int kATileBytes = SPARSE ? BM * 64 : BM * 128;
-  static constexpr int kBTileBytes = BN * 128;  // 256 rows x 64 elements (128B swizzle)
+  static constexpr int kBTileBytes = (PAIR ? BN / 2 : BN) * 128;  // rows x 64 elements (128B swizzle)
   static constexpr int kStageBytes = kATileBytes + kBTileBytes;
-  static constexpr int kStages = SPARSE ? 5 : 4;
+  static constexpr int kStages = PAIR ? 8 : (SPARSE ? 5 : 4);
   static constexpr int kAcc = SPARSE ? 1 : 2;  // 256-column accumulator buffers
   static constexpr int kEpiOffset = kStages * kStageBytes;
   static constexpr int kBarOffset = kEpiOffset + kEpiWarps * kEpiBufBytes;
@@ -113,23 +115,34 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// CLUSTER: acquire at cluster scope, for barriers the peer CTA arrives on.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (CLUSTER)
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
 // Bounded wait: false if the budget ran out (then the status word and the
 // CTA's abort flag are set) or another role already aborted.
+template <bool CLUSTER = false>
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long budget,
                                             int32_t* status) {
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try(bar, parity)) return true;
+    if (mbar_try<CLUSTER>(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > budget) {
       *abort_flag = 1;
@@ -140,10 +153,11 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
 }
 // The phase is usually complete already: test it inline and only call out to
 // the bounded loop when it is not.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long budget,
                                           int32_t* status) {
-  if (mbar_try(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, budget, status);
+  if (mbar_try<CLUSTER>(bar, parity)) return true;
+  return mbar_wait_slow<CLUSTER>(bar, parity, abort_flag, budget, status);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
@@ -221,6 +235,31 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
       "h"(mask)
       : "memory");
 }
+// cta_group::2 forms: the MMA is issued by the even CTA of the pair and reads
+// the operands of both CTAs at the same shared-memory offsets; the commit
+// arrives on the barrier at the same offset in both CTAs.
+__device__ __forceinline__ void mma_sparse_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t tmem_meta,
+                                                uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %5, 0;\ntcgen05.mma.sp.cta_group::2.kind::f16 [%0], %1, %2, [%3], %4, p;\n}" ::
+          "r"(tmem_d),
+      "l"(a), "l"(b), "r"(tmem_meta), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+// Address of the same shared-memory location in the even CTA of the pair.
+__device__ __forceinline__ uint32_t pair_leader_addr(uint32_t a) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(a));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -288,11 +327,12 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int cl, int 
 // 15 warps are resident as 16 for register allocation (warps are allocated in
 // groups of four), so 128 registers per thread is the most that still fits
 // the 64K-register file.
-template <bool SPARSE, int CL>
+template <bool SPARSE, int CL, bool PAIR>
 __global__ void __maxnreg__(128)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const Params p) {
-  using C = Cfg<SPARSE>;
+  static_assert(!PAIR || (SPARSE && CL == 2), "the paired product is the sparse one on clusters of two");
+  using C = Cfg<SPARSE, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
@@ -309,22 +349,30 @@ __global__ void __maxnreg__(128)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      // SPARSE: the producer's expect_tx arrival and one arrival per metadata warp
-      mbar_init(bar_full + 8 * s, SPARSE ? 1 + kMetaWarps : 1);
-      mbar_init(bar_empty + 8 * s, 2 * CL);  // released by both issuers of every CTA that reads the stage
+      // SPARSE: the producer's expect_tx arrival and one arrival per metadata warp;
+      // PAIR: the leader's barrier also takes the peer's relayed arrival
+      mbar_init(bar_full + 8 * s, (SPARSE ? 1 + kMetaWarps : 1) + (PAIR && rank == 0 ? 1 : 0));
+      // released by both issuers of every CTA that reads the stage (PAIR: the one paired issuer)
+      mbar_init(bar_empty + 8 * s, PAIR ? 1 : 2 * CL);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(bar_tfull + 8 * a, 2);  // both issuers
-      mbar_init(bar_tempty + 8 * a, kEpiWarps);
+      mbar_init(bar_tfull + 8 * a, PAIR ? 1 : 2);
+      mbar_init(bar_tempty + 8 * a, PAIR ? 2 * kEpiWarps : kEpiWarps);  // PAIR: both CTAs' epilogues
     }
-    mbar_init(bar_drain, 2);
+    mbar_init(bar_drain, PAIR ? 1 : 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    if constexpr (PAIR) {  // collective across the pair: both CTAs allocate
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -360,10 +408,13 @@ __global__ void __maxnreg__(128)
           } else {
             tma_load_2d(sA, &tmA, fb, ks * 64, t.m0);
           }
-          // B: this CTA fetches 256 / CL rows (columns of D) and, in a cluster, multicasts them
+          // B: this CTA fetches 256 / CL rows (columns of D) and, in a cluster, multicasts them;
+          // PAIR: each CTA keeps its own half, which the paired MMA reads in place
           const int nb = t.n0 + (BN / CL) * (int)rank;
           const uint32_t sBh = sB + (C::kBTileBytes / CL) * rank;
-          if (!SPARSE && p.b_mn) {
+          if constexpr (PAIR) {
+            tma_load_2d(sB, &tmB, fb, ks * 64, nb);
+          } else if (!SPARSE && p.b_mn) {
 #pragma unroll
             for (int h = 0; h < 4 / CL; ++h) {
               if (CL > 1)
@@ -395,6 +446,76 @@ __global__ void __maxnreg__(128)
         }
     }
   } else if (warp == 1 || warp == kMmaWarpB) {
+    if constexpr (PAIR) {
+      // ----------------------------------------------------- paired issuer / relay
+      // The even CTA issues M256 x N256 MMAs over both CTAs' operands and
+      // commits to both CTAs' barriers; the odd CTA's warp 1 relays "stage
+      // ready" (its own TMA bytes and metadata) to the even CTA's full barrier.
+      if (warp == 1 && lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        if (rank == 0) {
+          const uint32_t idesc = (1u << 4) | ((uint32_t)p.bf16 << 7) | ((uint32_t)p.bf16 << 10) | (1u << 2) |
+                                 ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
+          constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
+          const uint32_t sA0 = smem_u32(smem);
+          const uint64_t a_desc0 = sdesc(sA0, 16, 512, kSwizzle64);
+          const uint64_t b_desc0 = sdesc(sA0 + C::kATileBytes, 16, 1024, kSwizzle128);
+          uint32_t mpair = 0, acc_phase = 0;
+          if (p.fault_test) ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);  // runs out
+          for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+            const Unit t = decode_unit(p, u, CL, rank);
+            if (!mbar_wait<true>(bar_tempty, acc_phase ^ 1, abort_flag, p.wait_budget, p.status)) break;
+            tc_fence_after();
+            int kstep = 0;
+            for (int ks = t.kbeg; ks < t.kend; ++ks) {
+              if (!mbar_wait<true>(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t ad = a_desc0 + (uint64_t)(stage * kStageUnits);
+              const uint64_t bd = b_desc0 + (uint64_t)(stage * kStageUnits);
+              const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * 2 * mpair;
+              mma_sparse_pair(tmem, ad, bd, tmeta, idesc, kstep > 0 ? 1u : 0u);
+              if (2 * ks + 1 < p.num_k_steps)
+                mma_sparse_pair(tmem, ad + (32 >> 4), bd + (64 >> 4), tmeta + kMetaColStride, idesc, 1u);
+              ++kstep;
+              mpair ^= 1u;
+              tc_commit_pair(bar_empty + 8 * stage);
+              if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+            if (!ok) break;
+            tc_commit_pair(bar_tfull);
+            acc_phase ^= 1;
+          }
+          tc_commit_pair(bar_drain);
+        } else {
+          for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+            const Unit t = decode_unit(p, u, CL, rank);
+            for (int ks = t.kbeg; ks < t.kend; ++ks) {
+              if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_remote(pair_leader_addr(bar_full + 8 * stage));
+              if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+          }
+        }
+        // all paired MMAs have completed before either CTA frees its tensor memory
+        const long long t0 = clock64();
+        while (!mbar_try(bar_drain, 0u) && clock64() - t0 < p.wait_budget) {
+        }
+      }
+    } else {
     // ------------------------------------------------------- MMA issuers
     // Two single-thread issuers share every stage: warp 1 computes columns
     // 0..127 and warp kMmaWarpB columns 128..255 of the tile.  An MMA holds
@@ -482,6 +603,7 @@ __global__ void __maxnreg__(128)
       const long long t0 = clock64();
       while (!mbar_try(bar_drain, 0u) && clock64() - t0 < p.wait_budget) {
       }
+    }
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------- SPARSE metadata
@@ -622,7 +744,12 @@ __global__ void __maxnreg__(128)
       // the accumulator buffer is drained: the next tile's MMAs may reuse it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+      if (lane == 0) {
+        if (PAIR && rank == 1)
+          mbar_arrive_remote(pair_leader_addr(bar_tempty + 8 * acc));
+        else
+          mbar_arrive(bar_tempty + 8 * acc);
+      }
       if (++acc == C::kAcc) {
         acc = 0;
         acc_phase ^= 1;
@@ -671,7 +798,12 @@ __global__ void __maxnreg__(128)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  if (warp == 1) {
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
   if (CL > 1) cluster_sync();  // no CTA leaves while its peer may still signal it
 }
 
@@ -760,15 +892,15 @@ int num_sms() {
 
 // The shared-memory opt-in is set once per device (and so never during a
 // stream capture that replays the launches later).
-template <bool SPARSE, int CL>
+template <bool SPARSE, int CL, bool PAIR>
 cudaError_t set_smem_attr() {
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (done_mask.load() & bit) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(spmm_tc_kernel<SPARSE, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<SPARSE>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(spmm_tc_kernel<SPARSE, CL, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<SPARSE, PAIR>::kSmemBytes);
   if (e == cudaSuccess) done_mask.fetch_or(bit);
   return e;
 }
@@ -820,13 +952,13 @@ bool make_store_map(CUtensorMap* map, const nm_spmm_desc_t& d, void* D) {
                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <bool SPARSE, int CL>
+template <bool SPARSE, int CL, bool PAIR>
 cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mD, Params p,
                           cudaStream_t s) {
-  if (cudaError_t e = set_smem_attr<SPARSE, CL>()) return e;
+  if (cudaError_t e = set_smem_attr<SPARSE, CL, PAIR>()) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<SPARSE>::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<SPARSE, PAIR>::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -842,7 +974,7 @@ cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const CU
     cfg.gridDim = dim3((unsigned)(num_sms() / CL * CL));
     int n = 0;
     if (CL > 1) {
-      if (cudaOccupancyMaxActiveClusters(&n, spmm_tc_kernel<SPARSE, CL>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, spmm_tc_kernel<SPARSE, CL, PAIR>, &cfg) != cudaSuccess) n = 0;
       cudaGetLastError();
     }
     max_clusters = n > 0 ? n : num_sms() / CL;
@@ -850,10 +982,11 @@ cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const CU
   }
   const int clusters = p.num_units < max_clusters ? p.num_units : max_clusters;
   cfg.gridDim = dim3((unsigned)(clusters * CL));
-  return cudaLaunchKernelEx(&cfg, spmm_tc_kernel<SPARSE, CL>, mA, mB, mD, p);
+  return cudaLaunchKernelEx(&cfg, spmm_tc_kernel<SPARSE, CL, PAIR>, mA, mB, mD, p);
 }
 
-// Pairs of CTAs share the B tile when the row blocks come in pairs.
+// Pairs of CTAs share the B tile when the row blocks come in pairs (the
+// sparse product then runs as one paired M256 product per cluster).
 int cluster_for(int num_m_blk) { return (num_m_blk % 2 == 0) ? 2 : 1; }
 
 }  // namespace tc
@@ -878,7 +1011,7 @@ cudaError_t spmm_tc_sparse_impl(const SpmmLaunch& a, cudaStream_t s, int fault_t
                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_store_map(&mD, d, a.D))
     return cudaErrorInvalidValue;
-  return cl == 2 ? launch_kernel<true, 2>(mA, mB, mD, p, s) : launch_kernel<true, 1>(mA, mB, mD, p, s);
+  return cl == 2 ? launch_kernel<true, 2, true>(mA, mB, mD, p, s) : launch_kernel<true, 1, false>(mA, mB, mD, p, s);
 }
 
 cudaError_t launch_spmm_tc_sparse(const SpmmLaunch& a, cudaStream_t s) { return spmm_tc_sparse_impl(a, s, 0, 0); }
@@ -948,7 +1081,8 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
   }
   if (ok) ok = make_store_map(&mD, d, a.D);
   if (!ok) return cudaErrorInvalidValue;
-  cudaError_t e = cl == 2 ? launch_kernel<false, 2>(mA, mB, mD, p, s) : launch_kernel<false, 1>(mA, mB, mD, p, s);
+  cudaError_t e =
+      cl == 2 ? launch_kernel<false, 2, false>(mA, mB, mD, p, s) : launch_kernel<false, 1, false>(mA, mB, mD, p, s);
   if (e != cudaSuccess || p.split_k == 1) return e;
   const int64_t groups = (int64_t)p.num_m_blk * p.num_n_blk * (BM * BN / 4);
   finalize_split_kernel<<<grid_for(groups, 256), 256, 0, s>>>(

@@ -194,9 +194,10 @@ def test_k_zero_gives_beta_c():
     assert torch.equal(D, (C.float() * 0.5).half())
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("M", [128, 256])  # one row block (single CTA) and a pair of row blocks (paired CTAs)
+def test_bounded_wait_reports_timeout_and_context_survives(M):
     """A wait nothing completes gives up after its budget: NM_ERR_TIMEOUT, no hang, GPU still usable."""
-    M, N, K = 128, 128, 256
+    N, K = 128, 256
     W = inputs.normal((M, K), 0.5, 1, "f16").to(DEV)
     X = inputs.normal((N, K), 1.0, 2, "f16").to(DEV)
     vals, meta = compress_on_gpu(W, M, K, "f16")
