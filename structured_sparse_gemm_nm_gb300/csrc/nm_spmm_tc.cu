@@ -69,8 +69,10 @@ struct Cfg {
   // SPARSE A: 128 rows x 32 compressed values (64B swizzle); dense A: 128 x 64 (128B swizzle).
   static constexpr int kATileBytes = SPARSE ? BM * 64 : BM * 128;
   static constexpr int kBTileBytes = (PAIR ? BN / 2 : BN) * 128;  // rows x 64 elements (128B swizzle)
-  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
-  static constexpr int kStages = PAIR ? 8 : (SPARSE ? 5 : 4);
+  // PAIR: the stage also carries its two k-steps' metadata, one 16-byte row per row of A
+  static constexpr int kMetaBytes = PAIR ? 2 * BM * 16 : 0;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes + kMetaBytes;
+  static constexpr int kStages = PAIR ? 7 : (SPARSE ? 5 : 4);
   static constexpr int kAcc = SPARSE ? 1 : 2;  // 256-column accumulator buffers
   static constexpr int kEpiOffset = kStages * kStageBytes;
   static constexpr int kBarOffset = kEpiOffset + kEpiWarps * kEpiBufBytes;
@@ -244,6 +246,11 @@ __device__ __forceinline__ void mma_sparse_pair(uint32_t tmem_d, uint64_t a, uin
       "{\n.reg .pred p;\nsetp.ne.b32 p, %5, 0;\ntcgen05.mma.sp.cta_group::2.kind::f16 [%0], %1, %2, [%3], %4, p;\n}" ::
           "r"(tmem_d),
       "l"(a), "l"(b), "r"(tmem_meta), "r"(idesc), "r"(acc));
+}
+// Copies 128 rows x 16 bytes of each CTA's shared memory into its own tensor
+// memory (four columns at `taddr`), in order with the MMAs this thread issues.
+__device__ __forceinline__ void tc_cp_pair(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile(
@@ -462,7 +469,8 @@ __global__ void __maxnreg__(128)
           const uint32_t sA0 = smem_u32(smem);
           const uint64_t a_desc0 = sdesc(sA0, 16, 512, kSwizzle64);
           const uint64_t b_desc0 = sdesc(sA0 + C::kATileBytes, 16, 1024, kSwizzle128);
-          uint32_t mpair = 0, acc_phase = 0;
+          const uint64_t m_desc0 = sdesc(sA0 + C::kATileBytes + C::kBTileBytes, 16, 128, 0);  // 16-byte rows
+          uint32_t mslot = 0, acc_phase = 0;
           if (p.fault_test) ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);  // runs out
           for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
             const Unit t = decode_unit(p, u, CL, rank);
@@ -477,12 +485,17 @@ __global__ void __maxnreg__(128)
               tc_fence_after();
               const uint64_t ad = a_desc0 + (uint64_t)(stage * kStageUnits);
               const uint64_t bd = b_desc0 + (uint64_t)(stage * kStageUnits);
-              const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * 2 * mpair;
-              mma_sparse_pair(tmem, ad, bd, tmeta, idesc, kstep > 0 ? 1u : 0u);
-              if (2 * ks + 1 < p.num_k_steps)
-                mma_sparse_pair(tmem, ad + (32 >> 4), bd + (64 >> 4), tmeta + kMetaColStride, idesc, 1u);
+              const uint64_t md = m_desc0 + (uint64_t)(stage * kStageUnits);
+              // metadata into the next of four 64-column-aligned slots, then the MMA that reads it
+              const int steps = 2 * ks + 1 < p.num_k_steps ? 2 : 1;  // no MMA past K
+              for (int j = 0; j < steps; ++j) {
+                const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * mslot;
+                tc_cp_pair(tmeta, md + (uint64_t)((2048 * j) >> 4));
+                mma_sparse_pair(tmem, ad + (uint64_t)((32 * j) >> 4), bd + (uint64_t)((64 * j) >> 4), tmeta, idesc,
+                                (kstep > 0 || j > 0) ? 1u : 0u);
+                mslot = (mslot + 1) & 3u;
+              }
               ++kstep;
-              mpair ^= 1u;
               tc_commit_pair(bar_empty + 8 * stage);
               if (++stage == C::kStages) {
                 stage = 0;
@@ -636,6 +649,27 @@ __global__ void __maxnreg__(128)
             if (ks + 4 < t.kend) {
               ring[i][0] = word(2 * (ks + 4));
               ring[i][1] = word(2 * (ks + 4) + 1);
+            }
+            if constexpr (PAIR) {
+              // the words go to the stage's metadata rows (copied to tensor memory by the
+              // paired issuer); the stage buffer was last read by the MMAs of stage g - kStages
+              if (g >= C::kStages) {
+                const int h = g - C::kStages;
+                if (!mbar_wait(bar_empty + 8 * (h % C::kStages), (uint32_t)((h / C::kStages) & 1), abort_flag,
+                               p.wait_budget, p.status)) {
+                  ok = false;
+                  break;
+                }
+              }
+              uint8_t* mrow = smem + (g % C::kStages) * C::kStageBytes + C::kATileBytes + C::kBTileBytes +
+                              (32 * q + lane) * 16;
+              *reinterpret_cast<uint32_t*>(mrow) = w0;
+              *reinterpret_cast<uint32_t*>(mrow + BM * 16) = w1;
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_full + 8 * (g % C::kStages));
+              ++g;
+              continue;
             }
             // slot pair g & 1 was last read by the MMAs of stage g - 2: wait until that stage is released
             if (g >= 2) {
