@@ -406,7 +406,7 @@ __global__ void __maxnreg__(128)
           const uint32_t fb = bar_full + 8 * stage;
           const uint32_t sA = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t sB = sA + C::kATileBytes;
-          mbar_expect_tx(fb, C::kStageBytes);
+          mbar_expect_tx(fb, C::kATileBytes + C::kBTileBytes);  // PAIR's metadata rows come from the metadata warps
           if constexpr (SPARSE) {
             tma_load_2d(sA, &tmA, fb, ks * 32, t.m0);
           } else if (p.a_mn) {
