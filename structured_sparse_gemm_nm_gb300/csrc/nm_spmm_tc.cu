@@ -267,6 +267,15 @@ __device__ __forceinline__ uint32_t pair_leader_addr(uint32_t a) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Relaxed remote arrive for "stage ready": the data it announces was written
+// into this CTA's shared memory (TMA, and metadata rows already fenced to the
+// async proxy), completion was observed here, and it is read only through
+// this CTA's shared memory by the paired tensor-core instructions.  A release
+// at cluster scope costs over a thousand cycles per arrive, which would limit
+// the pair to one stage per relay round trip.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -515,7 +524,7 @@ __global__ void __maxnreg__(128)
                 ok = false;
                 break;
               }
-              mbar_arrive_remote(pair_leader_addr(bar_full + 8 * stage));
+              mbar_arrive_remote_relaxed(pair_leader_addr(bar_full + 8 * stage));
               if (++stage == C::kStages) {
                 stage = 0;
                 phase ^= 1;
