@@ -66,13 +66,19 @@ constexpr int kEpiBufBytes = 32 * 32 * 2;  // one 32 x 32 output block
 // cta_group::2); each holds its 128 rows of A and one 128-row half of B.
 template <bool SPARSE, bool PAIR = false>
 struct Cfg {
-  // SPARSE A: 128 rows x 32 compressed values (64B swizzle); dense A: 128 x 64 (128B swizzle).
-  static constexpr int kATileBytes = SPARSE ? BM * 64 : BM * 128;
-  static constexpr int kBTileBytes = (PAIR ? BN / 2 : BN) * 128;  // rows x 64 elements (128B swizzle)
-  // PAIR: the stage also carries its two k-steps' metadata, one 16-byte row per row of A
-  static constexpr int kMetaBytes = PAIR ? 2 * BM * 16 : 0;
+  // dense-equivalent K per stage: 64, or 128 for the paired product (four k-steps per
+  // barrier wait and commit of its single issuer)
+  static constexpr int kKStage = PAIR ? 128 : kKPerStage;
+  static constexpr int kSteps = kKStage / 32;  // SPARSE k-steps per stage
+  // SPARSE A: 128 rows x kKStage/2 compressed values (64B swizzle for 64 B rows, 128B for
+  // 128 B rows); dense A: 128 x 64 (128B swizzle).
+  static constexpr int kATileBytes = SPARSE ? BM * kKStage : BM * 128;
+  // B: rows x 64 elements per 128B-swizzled box; PAIR holds 128 rows and two boxes along K
+  static constexpr int kBTileBytes = PAIR ? (BN / 2) * 256 : BN * 128;
+  // PAIR: the stage also carries its k-steps' metadata, one 16-byte row per row of A
+  static constexpr int kMetaBytes = PAIR ? kSteps * BM * 16 : 0;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes + kMetaBytes;
-  static constexpr int kStages = PAIR ? 7 : (SPARSE ? 5 : 4);
+  static constexpr int kStages = PAIR ? 3 : (SPARSE ? 5 : 4);
   static constexpr int kAcc = SPARSE ? 1 : 2;  // 256-column accumulator buffers
   static constexpr int kEpiOffset = kStages * kStageBytes;
   static constexpr int kBarOffset = kEpiOffset + kEpiWarps * kEpiBufBytes;
@@ -417,7 +423,7 @@ __global__ void __maxnreg__(128)
           const uint32_t sB = sA + C::kATileBytes;
           mbar_expect_tx(fb, C::kATileBytes + C::kBTileBytes);  // PAIR's metadata rows come from the metadata warps
           if constexpr (SPARSE) {
-            tma_load_2d(sA, &tmA, fb, ks * 32, t.m0);
+            tma_load_2d(sA, &tmA, fb, ks * (C::kKStage / 2), t.m0);
           } else if (p.a_mn) {
             tma_load_2d(sA, &tmA, fb, t.m0, ks * 64);
             tma_load_2d(sA + C::kATileBytes / 2, &tmA, fb, t.m0 + 64, ks * 64);
@@ -429,7 +435,8 @@ __global__ void __maxnreg__(128)
           const int nb = t.n0 + (BN / CL) * (int)rank;
           const uint32_t sBh = sB + (C::kBTileBytes / CL) * rank;
           if constexpr (PAIR) {
-            tma_load_2d(sB, &tmB, fb, ks * 64, nb);
+            tma_load_2d(sB, &tmB, fb, ks * 128, nb);
+            tma_load_2d(sB + C::kBTileBytes / 2, &tmB, fb, ks * 128 + 64, nb);
           } else if (!SPARSE && p.b_mn) {
 #pragma unroll
             for (int h = 0; h < 4 / CL; ++h) {
@@ -476,9 +483,11 @@ __global__ void __maxnreg__(128)
                                  ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
           constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
           const uint32_t sA0 = smem_u32(smem);
-          const uint64_t a_desc0 = sdesc(sA0, 16, 512, kSwizzle64);
+          // A: 128 rows x 128 B (128B swizzle), 32 B per k-step; B: two boxes of 128 rows x 128 B,
+          // 64 B per k-step within a box; metadata: 16-byte rows, one block of 128 rows per k-step
+          const uint64_t a_desc0 = sdesc(sA0, 16, 1024, kSwizzle128);
           const uint64_t b_desc0 = sdesc(sA0 + C::kATileBytes, 16, 1024, kSwizzle128);
-          const uint64_t m_desc0 = sdesc(sA0 + C::kATileBytes + C::kBTileBytes, 16, 128, 0);  // 16-byte rows
+          const uint64_t m_desc0 = sdesc(sA0 + C::kATileBytes + C::kBTileBytes, 16, 128, 0);
           uint32_t mslot = 0, acc_phase = 0;
           if (p.fault_test) ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);  // runs out
           for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
@@ -496,12 +505,13 @@ __global__ void __maxnreg__(128)
               const uint64_t bd = b_desc0 + (uint64_t)(stage * kStageUnits);
               const uint64_t md = m_desc0 + (uint64_t)(stage * kStageUnits);
               // metadata into the next of four 64-column-aligned slots, then the MMA that reads it
-              const int steps = 2 * ks + 1 < p.num_k_steps ? 2 : 1;  // no MMA past K
+              const int left = p.num_k_steps - C::kSteps * ks;  // no MMA past K
+              const int steps = left < C::kSteps ? left : C::kSteps;
               for (int j = 0; j < steps; ++j) {
                 const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * mslot;
-                tc_cp_pair(tmeta, md + (uint64_t)((2048 * j) >> 4));
-                mma_sparse_pair(tmem, ad + (uint64_t)((32 * j) >> 4), bd + (uint64_t)((64 * j) >> 4), tmeta, idesc,
-                                (kstep > 0 || j > 0) ? 1u : 0u);
+                tc_cp_pair(tmeta, md + (uint64_t)((BM * 16 * j) >> 4));
+                const uint64_t bj = bd + (uint64_t)(((C::kBTileBytes / 2) * (j / 2) + 64 * (j % 2)) >> 4);
+                mma_sparse_pair(tmem, ad + (uint64_t)((32 * j) >> 4), bj, tmeta, idesc, (kstep > 0 || j > 0) ? 1u : 0u);
                 mslot = (mslot + 1) & 3u;
               }
               ++kstep;
@@ -642,22 +652,25 @@ __global__ void __maxnreg__(128)
           return kstep < S ? __ldg(src + (int64_t)kstep * p.meta_slots) : 0x44444444u;  // 0x4: a valid code
         };
         // the words of the next four stages are loaded ahead of their use
-        uint32_t ring[4][2];
+        constexpr int KS = C::kSteps;
+        uint32_t ring[4][KS];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int ks = t.kbeg + i;
-          ring[i][0] = ks < t.kend ? word(2 * ks) : 0u;
-          ring[i][1] = ks < t.kend ? word(2 * ks + 1) : 0u;
+#pragma unroll
+          for (int j = 0; j < KS; ++j) ring[i][j] = ks < t.kend ? word(KS * ks + j) : 0u;
         }
         for (int ks0 = t.kbeg; ok && ks0 < t.kend; ks0 += 4) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int ks = ks0 + i;
             if (ks >= t.kend) break;
-            const uint32_t w0 = ring[i][0], w1 = ring[i][1];
+            uint32_t w[KS];
+#pragma unroll
+            for (int j = 0; j < KS; ++j) w[j] = ring[i][j];
             if (ks + 4 < t.kend) {
-              ring[i][0] = word(2 * (ks + 4));
-              ring[i][1] = word(2 * (ks + 4) + 1);
+#pragma unroll
+              for (int j = 0; j < KS; ++j) ring[i][j] = word(KS * (ks + 4) + j);
             }
             if constexpr (PAIR) {
               // the words go to the stage's metadata rows (copied to tensor memory by the
@@ -672,8 +685,8 @@ __global__ void __maxnreg__(128)
               }
               uint8_t* mrow = smem + (g % C::kStages) * C::kStageBytes + C::kATileBytes + C::kBTileBytes +
                               (32 * q + lane) * 16;
-              *reinterpret_cast<uint32_t*>(mrow) = w0;
-              *reinterpret_cast<uint32_t*>(mrow + BM * 16) = w1;
+#pragma unroll
+              for (int j = 0; j < KS; ++j) *reinterpret_cast<uint32_t*>(mrow + BM * 16 * j) = w[j];
               asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
               __syncwarp();
               if (lane == 0) mbar_arrive(bar_full + 8 * (g % C::kStages));
@@ -691,8 +704,8 @@ __global__ void __maxnreg__(128)
             }
             tc_fence_after();
             const uint32_t ta = tq + kMetaColStride * 2 * (g & 1);
-            tmem_st1(ta, w0);
-            tmem_st1(ta + kMetaColStride, w1);
+            tmem_st1(ta, w[0]);
+            tmem_st1(ta + kMetaColStride, w[1]);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
@@ -788,8 +801,8 @@ __global__ void __maxnreg__(128)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (PAIR && rank == 1)
-          mbar_arrive_remote(pair_leader_addr(bar_tempty + 8 * acc));
+        if (PAIR && rank == 1)  // the accumulator reads above completed (wait::ld) before this arrive
+          mbar_arrive_remote_relaxed(pair_leader_addr(bar_tempty + 8 * acc));
         else
           mbar_arrive(bar_tempty + 8 * acc);
       }
@@ -1049,7 +1062,14 @@ cudaError_t spmm_tc_sparse_impl(const SpmmLaunch& a, cudaStream_t s, int fault_t
   const CUtensorMapDataType u16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
   CUtensorMap mA, mB, mD;
   const int64_t kc = d.K / 2;  // compressed values per row, packed
-  if (!make_map(&mA, a.A, u16, (uint64_t)kc, (uint64_t)d.M, (uint64_t)(kc * 2), 32, BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  // paired: 128 dense K per stage, so 64 compressed values (128 B, 128B swizzle) per row of A
+  const bool pair = cl == 2;
+  if (pair) {
+    p.k_stages = (int)((d.K + Cfg<true, true>::kKStage - 1) / Cfg<true, true>::kKStage);
+    p.stages_per_split = p.k_stages;
+  }
+  if (!make_map(&mA, a.A, u16, (uint64_t)kc, (uint64_t)d.M, (uint64_t)(kc * 2), pair ? 64 : 32, BM,
+                pair ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, (uint32_t)(BN / cl),
                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_store_map(&mD, d, a.D))
