@@ -333,6 +333,12 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
                                  "cublas_dense_tflops": f / t_cub_dx / 1e9, "speedup_vs_cublas": t_cub_dx / t_dx}
         rows[f"S7_dw_{name}"] = {"shape_MNK": [o, i, wl.T], "ms": t_dw, "tflops": f / t_dw / 1e9,
                                  "frac_dense_peak": f / t_dw / 1e9 / dense_peak}
+        # the same forward product on paired CTAs (algo 1), for comparison with the default
+        pp = nb.nm_spmm_plan(nb.make_desc(M=o, N=wl.T, K=i, ab_type="bf16", cd_type="bf16", ldb=i, ldd=o, algo=1))
+        t_pair = time_launch(torch, lambda: nb.nm_spmm(pp, 1.0, L["vals"], L["meta"], L["X"], 0.0, None, wl.Y[j]), flush)
+        rows[f"S5_fwd_{name}_paired"] = {"shape_MNK": [o, wl.T, i], "ms": t_pair, "tflops": f / t_pair / 1e9,
+                                         "frac_sparse_peak": f / t_pair / 1e9 / sparse_peak}
+        pp.destroy()
 
     # HBM-bound rows: `ms` is the per-launch time of back-to-back launches over
     # copies whose buffers exceed the L2 (see time_stream); `ms_single` is one

@@ -267,6 +267,11 @@ typedef struct {
   nm_order_t order_cd;          /* ROW = C, D stored M x N, COL = stored N x M                */
   int64_t lda, ldb, ldc, ldd;   /* leading dimensions in elements (lda: DENSE_MASKED only)    */
   nm_meta_layout_t meta_layout; /* SPARSE_A 2:4 with F16/BF16 needs NM_META_TC                */
+  int algo;                     /* algorithm selection (cuSPARSELt blog, code example: the    */
+                                /* algorithm-selection step): 0 = the library's default;      */
+                                /* 1 = SPARSE_A 2:4 F16/BF16 on pairs of CTAs (tcgen05 with   */
+                                /* cta_group::2, M256 tiles) when M spans an even number of   */
+                                /* 128-row blocks, else the default                            */
 } nm_spmm_desc_t;
 
 typedef struct nm_spmm_plan_s* nm_spmm_plan_t;

@@ -47,6 +47,7 @@ class SpmmDesc(ctypes.Structure):
         ("order_a", ctypes.c_int), ("order_b", ctypes.c_int), ("order_cd", ctypes.c_int),
         ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64), ("ldd", ctypes.c_int64),
         ("meta_layout", ctypes.c_int),
+        ("algo", ctypes.c_int),
     ]
 
 

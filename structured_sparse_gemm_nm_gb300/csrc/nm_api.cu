@@ -321,6 +321,7 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   *plan = nullptr;
   const nm_spmm_desc_t& d = *desc;
   if (d.M < 0 || d.N < 0 || d.K < 0) return NM_ERR_INVALID_ARG;
+  if (d.algo != 0 && d.algo != 1) return NM_ERR_INVALID_ARG;
   if (!is_elem(d.ab_type)) return NM_ERR_INVALID_ARG;
   const bool fp = d.ab_type != NM_I8;
   if (fp ? d.cd_type != d.ab_type : d.cd_type != NM_I32) return NM_ERR_UNSUPPORTED;

@@ -1041,8 +1041,8 @@ cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const CU
   return cudaLaunchKernelEx(&cfg, spmm_tc_kernel<SPARSE, CL, PAIR>, mA, mB, mD, p);
 }
 
-// Pairs of CTAs share the B tile when the row blocks come in pairs (the
-// sparse product then runs as one paired M256 product per cluster).
+// Pairs of CTAs share the B tile when the row blocks come in pairs (for the
+// sparse product with algo 1 as one paired M256 product per cluster).
 int cluster_for(int num_m_blk) { return (num_m_blk % 2 == 0) ? 2 : 1; }
 
 }  // namespace tc
@@ -1057,13 +1057,16 @@ cudaError_t spmm_tc_sparse_impl(const SpmmLaunch& a, cudaStream_t s, int fault_t
   const int cl = cluster_for(p.num_m_blk);
   p.num_units = (p.num_m_blk / cl) * p.num_n_blk;
   p.num_k_steps = (int)(d.K / 32);
+  // Paired CTAs on request: they halve the shared-memory traffic per SM, but their single
+  // issuer's per-stage work is then exposed; on GB300 the single-CTA kernel with two
+  // issuers was measured faster for the benchmark shapes, so it is the default.
   p.meta = static_cast<const uint32_t*>(a.A_meta);
   p.meta_slots = tc_slots(d.M);
   const CUtensorMapDataType u16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
   CUtensorMap mA, mB, mD;
   const int64_t kc = d.K / 2;  // compressed values per row, packed
   // paired: 128 dense K per stage, so 64 compressed values (128 B, 128B swizzle) per row of A
-  const bool pair = cl == 2;
+  const bool pair = cl == 2 && d.algo == 1;
   if (pair) {
     p.k_stages = (int)((d.K + Cfg<true, true>::kKStage - 1) / Cfg<true, true>::kKStage);
     p.stages_per_split = p.k_stages;
@@ -1074,7 +1077,8 @@ cudaError_t spmm_tc_sparse_impl(const SpmmLaunch& a, cudaStream_t s, int fault_t
                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_store_map(&mD, d, a.D))
     return cudaErrorInvalidValue;
-  return cl == 2 ? launch_kernel<true, 2, true>(mA, mB, mD, p, s) : launch_kernel<true, 1, false>(mA, mB, mD, p, s);
+  if (pair) return launch_kernel<true, 2, true>(mA, mB, mD, p, s);
+  return cl == 2 ? launch_kernel<true, 2, false>(mA, mB, mD, p, s) : launch_kernel<true, 1, false>(mA, mB, mD, p, s);
 }
 
 cudaError_t launch_spmm_tc_sparse(const SpmmLaunch& a, cudaStream_t s) { return spmm_tc_sparse_impl(a, s, 0, 0); }

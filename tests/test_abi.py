@@ -164,6 +164,8 @@ def test_plan_validation(lib):
     assert plan_status(**{**dense, "lda": 100}) == nb.NM_ERR_INVALID_ARG
     assert plan_status(**{**dense, "mode": 7}) == nb.NM_ERR_INVALID_ARG
     assert plan_status(M=-1, N=1, K=32, ab_type="f16", cd_type="f16", ldb=32, ldd=8) == nb.NM_ERR_INVALID_ARG
+    assert plan_status(**{**base, "algo": 1}) == nb.NM_OK
+    assert plan_status(**{**base, "algo": 2}) == nb.NM_ERR_INVALID_ARG
     units = dict(M=256, N=8, K=1024, mode=nb.NM_SPMM_BLOCK_SPARSE_A, n=1, m=32, ab_type="f16", cd_type="f16",
                  ldb=1024, ldd=256)
     assert plan_status(**units) == nb.NM_OK

@@ -58,8 +58,14 @@ SPARSE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("M,N,K,dtype,order_cd,alpha,beta,sampled", SPARSE_CASES)
-def test_sparse_tc_matches_oracle(M, N, K, dtype, order_cd, alpha, beta, sampled):
+# algo 1: paired CTAs (M256 tiles) where M spans an even number of 128-row blocks
+PAIRED_CASES = [c + (1,) for c in SPARSE_CASES if ((c[0] + 127) // 128) % 2 == 0] + \
+    [(264, 200, 160, "f16", nb.NM_ROW, 1.5, 0.0, False, 1), (256, 72, 96, "bf16", nb.NM_ROW, 2.0, 0.5, False, 1)]
+
+
+@pytest.mark.parametrize("M,N,K,dtype,order_cd,alpha,beta,sampled,algo",
+                         [c + (0,) for c in SPARSE_CASES] + PAIRED_CASES)
+def test_sparse_tc_matches_oracle(M, N, K, dtype, order_cd, alpha, beta, sampled, algo):
     std = 0.02 if K >= 512 else 0.5
     W = inputs.normal((M, K), std, inputs.SEED_W + M, dtype)
     X = inputs.normal((N, K), 1.0, inputs.SEED_X + N, dtype)  # B stored N x K
@@ -70,7 +76,7 @@ def test_sparse_tc_matches_oracle(M, N, K, dtype, order_cd, alpha, beta, sampled
     C = inputs.normal(cd_shape, 1.0, inputs.SEED_C, dtype).to(DEV) if beta != 0 else None
     D = torch.full(cd_shape, float("nan"), dtype=C.dtype if C is not None else Wd.dtype, device=DEV)
     plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type=dtype, cd_type=dtype, ldb=K,
-                                        ldc=ld if C is not None else 0, ldd=ld, order_cd=order_cd))
+                                        ldc=ld if C is not None else 0, ldd=ld, order_cd=order_cd, algo=algo))
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     nb.nm_spmm(plan, alpha, vals, meta, Xd, beta, C, D, d_status=status)
     torch.cuda.synchronize()
@@ -194,8 +200,9 @@ def test_k_zero_gives_beta_c():
     assert torch.equal(D, (C.float() * 0.5).half())
 
 
-@pytest.mark.parametrize("M", [128, 256])  # one row block (single CTA) and a pair of row blocks (paired CTAs)
-def test_bounded_wait_reports_timeout_and_context_survives(M):
+# one row block (single CTA), two row blocks (cluster of two), two row blocks on paired CTAs
+@pytest.mark.parametrize("M,algo", [(128, 0), (256, 0), (256, 1)])
+def test_bounded_wait_reports_timeout_and_context_survives(M, algo):
     """A wait nothing completes gives up after its budget: NM_ERR_TIMEOUT, no hang, GPU still usable."""
     N, K = 128, 256
     W = inputs.normal((M, K), 0.5, 1, "f16").to(DEV)
@@ -203,7 +210,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(M):
     vals, meta = compress_on_gpu(W, M, K, "f16")
     D = torch.zeros((N, M), dtype=torch.float16, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    desc = nb.make_desc(M=M, N=N, K=K, ab_type="f16", cd_type="f16", ldb=K, ldd=M)
+    desc = nb.make_desc(M=M, N=N, K=K, ab_type="f16", cd_type="f16", ldb=K, ldd=M, algo=algo)
     nb.nm_test_spmm_wait_timeout(desc, vals, meta, X, D, status, budget_cycles=1 << 22)
     torch.cuda.synchronize()
     assert int(status.item()) == nb.NM_ERR_TIMEOUT
