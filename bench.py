@@ -711,7 +711,7 @@ def run_native(args):
 
 # ------------------------------------------------------------------ single-kernel cases (ncu captures)
 KERNEL_CASES = ("sparse_fc1_fwd", "sparse_fc2_dx", "dense_fc1_dw", "transposable_fc1", "prune24_4096",
-                "prune_8of32_4096", "gemv_8of32_b8")
+                "prune_8of32_4096", "gemv_8of32_b8", "vector_wise_4096")
 
 
 def run_kernel_case(name: str, reps: int = 3):
@@ -768,6 +768,16 @@ def run_kernel_case(name: str, reps: int = 3):
             fn = [lambda: nb.nm_spmm(plan, 1.0, vals, meta, x, 0.0, None, y)]
         else:
             fn = [lambda Wr=Wr: nb.nm_compress(Wr, M, K, K, "f16", n, m, 0, layout, vals, meta) for Wr in Ws]
+    elif name == "vector_wise_4096":
+        M = K = 4096
+        keep = M * (K // 32) // 4
+        Ws = [inputs.normal((M, K), 0.02, 30 + r, "f16", device=dev) for r in range(max(reps, 5))]
+        wsb = nb.nm_prune_units_workspace(M, K, 1, 32)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        csr = torch.empty((M + 1 + keep) * 4, dtype=torch.uint8, device=dev)
+        vals = torch.empty(keep * 64, dtype=torch.uint8, device=dev)
+        fn = [lambda Wr=Wr: nb.nm_prune_vector_wise(Wr, M, K, K, "f16", 32, keep, nb.NM_SCORE_ABS_OF_SUM, csr=csr,
+                                                     vals=vals, workspace=ws, workspace_bytes=wsb) for Wr in Ws]
     else:
         raise SystemExit(f"unknown kernel case {name}; one of {KERNEL_CASES}")
     torch.cuda.synchronize()

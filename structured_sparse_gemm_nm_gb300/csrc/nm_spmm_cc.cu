@@ -32,7 +32,7 @@ __device__ __forceinline__ uint16_t from_f(float x, int bf16) {
 // NB = batch columns per pass (1 or 8).  x is staged in shared memory as
 // [k][NB]; the staging reads B with 16-byte loads when rows of B allow it.
 template <int NB>
-__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ vals, const uint8_t* __restrict__ idx,
+__global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint16_t* __restrict__ vals, const uint8_t* __restrict__ idx,
                                                      const uint16_t* __restrict__ B, const uint16_t* __restrict__ C,
                                                      uint16_t* __restrict__ D, int64_t M, int64_t N, int64_t K, int n,
                                                      int m, int64_t ldb, int64_t ldc, int64_t ldd, int cd_col,
@@ -46,8 +46,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
   const bool vstage = (K % 8 == 0);
   for (int64_t b0 = 0; b0 < N; b0 += NB) {
     const int nb = (int)(N - b0 < NB ? N - b0 : NB);
+    const uint16_t* xg = B + b0 * ldb;  // NB == 1: x is read through the L1 cache, not staged
     __syncthreads();
-    if (vstage) {
+    if (NB == 1) {
+    } else if (vstage) {
       const int64_t k8 = K / 8;
       for (int64_t i = threadIdx.x; i < k8 * NB; i += blockDim.x) {
         const int b = (int)(i / k8);
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
             const int64_t k = (j / n) * m + min((iw[t / 4] >> (8 * (t % 4))) & 0xFFu, (uint32_t)(m - 1));
             const float a = to_f((uint16_t)(vw[t / 2] >> (16 * (t % 2))), bf16);
             if constexpr (NB == 1) {
-              acc[0] = fmaf(a, to_f(xs[k], bf16), acc[0]);
+              acc[0] = fmaf(a, to_f(__ldg(xg + k), bf16), acc[0]);
             } else {
               const uint4 x4 = *reinterpret_cast<const uint4*>(xs + k * NB);
               const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
@@ -101,8 +103,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
         for (int64_t j = lane; j < kc; j += 32) {
           const int64_t k = (j / n) * m + min((int)ir[j], m - 1);
           const float a = to_f(vr[j], bf16);
+          if constexpr (NB == 1) {
+            acc[0] = fmaf(a, to_f(__ldg(xg + k), bf16), acc[0]);
+          } else {
 #pragma unroll
-          for (int b = 0; b < NB; ++b) acc[b] = fmaf(a, to_f(xs[k * NB + b], bf16), acc[b]);
+            for (int b = 0; b < NB; ++b) acc[b] = fmaf(a, to_f(xs[k * NB + b], bf16), acc[b]);
+          }
         }
       }
 #pragma unroll
@@ -127,7 +133,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
 template <int NB>
 cudaError_t gather_launch(const SpmmLaunch& a, cudaStream_t s) {
   const nm_spmm_desc_t& d = a.d;
-  const size_t smem = (size_t)d.K * NB * 2;
+  const size_t smem = NB == 1 ? 0 : (size_t)d.K * NB * 2;
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     // set once per device to the largest size this kernel may take
@@ -141,9 +147,12 @@ cudaError_t gather_launch(const SpmmLaunch& a, cudaStream_t s) {
       done_mask.fetch_or(bit);
     }
   }
-  const int threads = 256;
-  int64_t blocks = (d.M + 7) / 8;
-  if (blocks > 152 * 2) blocks = 152 * 2;
+  // NB == 1: a warp per row, every row in flight at once; NB > 1: x is staged once per
+  // CTA, so one CTA of 32 warps per SM keeps that staging to one copy per SM
+  const int threads = NB == 1 ? 256 : 1024;
+  int64_t blocks = (d.M + threads / 32 - 1) / (threads / 32);
+  const int64_t cap = NB == 1 ? (int64_t)1 << 20 : 152;
+  if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   gather_kernel<NB><<<(unsigned)blocks, threads, smem, s>>>(
       static_cast<const uint16_t*>(a.A), static_cast<const uint8_t*>(a.A_meta), static_cast<const uint16_t*>(a.B),
