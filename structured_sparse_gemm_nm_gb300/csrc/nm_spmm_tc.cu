@@ -306,6 +306,7 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (
       : "r"(ta), "r"(tb)
       : "memory");
 }
+
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
@@ -316,6 +317,60 @@ __device__ __forceinline__ float load_cd(const void* base, int64_t off, int bf16
 }
 __device__ __forceinline__ uint16_t to_cd(float x, int bf16) {
   return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
+}
+// Compile-time form for the drain: one conversion instruction per pair.
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2t(float lo, float hi) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+// One warp's 32 lanes x 64 accumulator columns (two 32-column loads in flight)
+// into packed pairs: alpha applied when SCALE, masked columns zeroed when
+// MASKED (mask words ma, mb for the two 32-column halves).
+template <bool BF16, bool SCALE, bool MASKED>
+__device__ __forceinline__ void drain64(uint32_t taddr, float alpha, uint32_t ma, uint32_t mb, uint32_t (&pa)[16],
+                                        uint32_t (&pb)[16]) {
+  uint32_t va[32], vb[32];
+  tmem_ld32x2(taddr, taddr + 32, va, vb);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float a0 = __uint_as_float(va[2 * j]), a1 = __uint_as_float(va[2 * j + 1]);
+    float b0 = __uint_as_float(vb[2 * j]), b1 = __uint_as_float(vb[2 * j + 1]);
+    if constexpr (SCALE) {
+      a0 *= alpha;
+      a1 *= alpha;
+      b0 *= alpha;
+      b1 *= alpha;
+    }
+    if constexpr (MASKED) {
+      a0 = ((ma >> (2 * j)) & 1u) ? a0 : 0.0f;
+      a1 = ((ma >> (2 * j + 1)) & 1u) ? a1 : 0.0f;
+      b0 = ((mb >> (2 * j)) & 1u) ? b0 : 0.0f;
+      b1 = ((mb >> (2 * j + 1)) & 1u) ? b1 : 0.0f;
+    }
+    pa[j] = pack2t<BF16>(a0, a1);
+    pb[j] = pack2t<BF16>(b0, b1);
+  }
+}
+template <bool MASKED>
+__device__ __forceinline__ void drain64_any(int bf16, bool scale, uint32_t taddr, float alpha, uint32_t ma,
+                                            uint32_t mb, uint32_t (&pa)[16], uint32_t (&pb)[16]) {
+  if (bf16) {
+    if (scale)
+      drain64<true, true, MASKED>(taddr, alpha, ma, mb, pa, pb);
+    else
+      drain64<true, false, MASKED>(taddr, alpha, ma, mb, pa, pb);
+  } else {
+    if (scale)
+      drain64<false, true, MASKED>(taddr, alpha, ma, mb, pa, pb);
+    else
+      drain64<false, false, MASKED>(taddr, alpha, ma, mb, pa, pb);
+  }
 }
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
   // one round-to-nearest conversion of the pair; `lo` lands in the low 16 bits
@@ -358,11 +413,11 @@ __global__ void __maxnreg__(128)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  // bars: full[S], empty[S], tfull[2], tempty[2 buffers][2 column halves], drain
   const uint32_t bar_full = smem_u32(bars), bar_empty = smem_u32(bars + C::kStages);
   const uint32_t bar_tfull = smem_u32(bars + 2 * C::kStages), bar_tempty = bar_tfull + 16;
-  const uint32_t bar_drain = bar_tempty + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5);
+  const uint32_t bar_drain = bar_tempty + 32;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 7);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -377,10 +432,10 @@ __global__ void __maxnreg__(128)
       // released by both issuers of every CTA that reads the stage (PAIR: the one paired issuer)
       mbar_init(bar_empty + 8 * s, PAIR ? 1 : 2 * CL);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(bar_tfull + 8 * a, PAIR ? 1 : 2);
-      mbar_init(bar_tempty + 8 * a, PAIR ? 2 * kEpiWarps : kEpiWarps);  // PAIR: both CTAs' epilogues
-    }
+    for (int a = 0; a < 2; ++a) mbar_init(bar_tfull + 8 * a, PAIR ? 1 : 2);
+    // one arrival per epilogue warp once it has read its columns of that half
+    // (PAIR: a single barrier per buffer, after both halves, from both CTAs' epilogues)
+    for (int a = 0; a < 4; ++a) mbar_init(bar_tempty + 8 * a, PAIR ? 2 * kEpiWarps : kEpiWarps);
     mbar_init(bar_drain, PAIR ? 1 : 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -586,7 +641,9 @@ __global__ void __maxnreg__(128)
         ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);
       for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
         const Unit t = decode_unit(p, u, CL, rank);
-        if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag, p.wait_budget, p.status)) break;
+        // this issuer's column half of the buffer has been read by the epilogue
+        if (!mbar_wait(bar_tempty + 8 * (2 * acc + (int)nhalf), acc_phase ^ 1, abort_flag, p.wait_budget, p.status))
+          break;
         tc_fence_after();
         const uint32_t tacc = tmem + acc * BN + (BN / 2) * nhalf;
         int kstep = 0;  // MMA k-steps issued for this tile
@@ -719,11 +776,28 @@ __global__ void __maxnreg__(128)
     // ------------------------------------------------------- epilogue
     const int ew = warp - kEpiWarp0;
     const int q = warp & 3;   // TMEM lane quarter this warp may access
-    const int half = ew / 4;  // which 128 of the 256 columns
+    const int hw = ew / 4;  // which 64 columns of each 128-column half
     uint8_t* buf = smem + C::kEpiOffset + ew * kEpiBufBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool stored = false;
+    // Hands column half h of the current buffer back to the issuers once this warp has read it.
+    auto release = [&](int h) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR) {
+          if (h == 1) {  // the paired issuer needs both halves: one arrival, after the second
+            if (rank == 1)  // the accumulator reads completed (wait::ld) before this arrive
+              mbar_arrive_remote_relaxed(pair_leader_addr(bar_tempty + 8 * 2 * acc));
+            else
+              mbar_arrive(bar_tempty + 8 * 2 * acc);
+          }
+        } else {
+          mbar_arrive(bar_tempty + 8 * (2 * acc + h));
+        }
+      }
+    };
     for (int u = cluster_id; u < p.num_units; u += num_clusters) {
       const Unit t = decode_unit(p, u, CL, rank);
       if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.wait_budget, p.status)) break;
@@ -731,80 +805,62 @@ __global__ void __maxnreg__(128)
       const int mq = t.m0 + 32 * q;
       const int row = mq + lane;
       const bool row_ok = row < p.M;
-      const int ncol0 = t.n0 + 128 * half;
+      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + acc * BN;
+      // packed chunk c (32 columns) of this warp: tile column 128 * (c / 2) + 64 * hw + 32 * (c % 2)
       uint32_t pk[4][16];
-      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + acc * BN + 128 * half;
+      auto chunk_col = [&](int c) { return 128 * (c >> 1) + 64 * hw + 32 * (c & 1); };
       if (p.split_k == 1 && p.tma_store) {
-        // drain this warp's 32 x 128 block two 32-column chunks at a time into packed registers
+        // half 0 first: once every warp has read its 64 columns of it, the first issuer can
+        // start the next tile while the second half is read
+        const bool scale = p.alpha != 1.0f;
 #pragma unroll
-        for (int c2 = 0; c2 < 4; c2 += 2) {
-          uint32_t va[32], vb[32];
-          tmem_ld32x2(tq + 32 * c2, tq + 32 * (c2 + 1), va, vb);
+        for (int h = 0; h < 2; ++h) {
           uint32_t ma = 0xFFFFFFFFu, mb = 0xFFFFFFFFu;
           if (!SPARSE && p.mask != nullptr && row_ok) {
-            const int na = ncol0 + 32 * c2, nbb = na + 32;
+            const int na = t.n0 + chunk_col(2 * h), nbb = na + 32;
             if (na < p.N) ma = p.mask[(int64_t)row * p.mask_words + na / 32];
             if (nbb < p.N) mb = p.mask[(int64_t)row * p.mask_words + nbb / 32];
           }
-          const float al = p.alpha;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float a0 = ((ma >> (2 * j)) & 1u) ? __uint_as_float(va[2 * j]) * al : 0.0f;
-            const float a1 = ((ma >> (2 * j + 1)) & 1u) ? __uint_as_float(va[2 * j + 1]) * al : 0.0f;
-            pk[c2][j] = pack2(a0, a1, p.bf16);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float b0 = ((mb >> (2 * j)) & 1u) ? __uint_as_float(vb[2 * j]) * al : 0.0f;
-            const float b1 = ((mb >> (2 * j + 1)) & 1u) ? __uint_as_float(vb[2 * j + 1]) * al : 0.0f;
-            pk[c2 + 1][j] = pack2(b0, b1, p.bf16);
-          }
+          drain64_any<!SPARSE>(p.bf16, scale, tq + chunk_col(2 * h), p.alpha, ma, mb, pk[2 * h], pk[2 * h + 1]);
+          release(h);
         }
       } else {
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tq + 32 * c, v);
-        const int nb = ncol0 + 32 * c;
-        uint32_t mword = 0xFFFFFFFFu;
-        if (!SPARSE && p.mask != nullptr && row_ok && nb < p.N) mword = p.mask[(int64_t)row * p.mask_words + nb / 32];
-        if (p.split_k > 1) {
-          // fp32 partial of this K split in the tiled order [split][m block][n block][col / 4][128 rows][4]:
-          // for each group of four columns the 32 lanes write 512 contiguous bytes
-          float4* tile = reinterpret_cast<float4*>(p.partial) +
-                         ((int64_t)(t.split * p.num_m_blk + t.m0 / BM) * p.num_n_blk + t.n0 / BN) * (BM * BN / 4);
-          const int c4_0 = (128 * half + 32 * c) / 4;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tq + chunk_col(c), v);
+          const int nb = t.n0 + chunk_col(c);
+          uint32_t mword = 0xFFFFFFFFu;
+          if (!SPARSE && p.mask != nullptr && row_ok && nb < p.N) mword = p.mask[(int64_t)row * p.mask_words + nb / 32];
+          if (p.split_k > 1) {
+            // fp32 partial of this K split in the tiled order [split][m block][n block][col / 4][128 rows][4]:
+            // for each group of four columns the 32 lanes write 512 contiguous bytes
+            float4* tile = reinterpret_cast<float4*>(p.partial) +
+                           ((int64_t)(t.split * p.num_m_blk + t.m0 / BM) * p.num_n_blk + t.n0 / BN) * (BM * BN / 4);
+            const int c4_0 = chunk_col(c) / 4;
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            float4 w;
-            w.x = ((mword >> (4 * j4)) & 1u) ? __uint_as_float(v[4 * j4]) * p.alpha : 0.0f;
-            w.y = ((mword >> (4 * j4 + 1)) & 1u) ? __uint_as_float(v[4 * j4 + 1]) * p.alpha : 0.0f;
-            w.z = ((mword >> (4 * j4 + 2)) & 1u) ? __uint_as_float(v[4 * j4 + 2]) * p.alpha : 0.0f;
-            w.w = ((mword >> (4 * j4 + 3)) & 1u) ? __uint_as_float(v[4 * j4 + 3]) * p.alpha : 0.0f;
-            tile[(c4_0 + j4) * BM + 32 * q + lane] = w;
-          }
-        } else if (row_ok && nb < p.N) {
-          const int cnt = min(32, p.N - nb);
+            for (int j4 = 0; j4 < 8; ++j4) {
+              float4 w;
+              w.x = ((mword >> (4 * j4)) & 1u) ? __uint_as_float(v[4 * j4]) * p.alpha : 0.0f;
+              w.y = ((mword >> (4 * j4 + 1)) & 1u) ? __uint_as_float(v[4 * j4 + 1]) * p.alpha : 0.0f;
+              w.z = ((mword >> (4 * j4 + 2)) & 1u) ? __uint_as_float(v[4 * j4 + 2]) * p.alpha : 0.0f;
+              w.w = ((mword >> (4 * j4 + 3)) & 1u) ? __uint_as_float(v[4 * j4 + 3]) * p.alpha : 0.0f;
+              tile[(c4_0 + j4) * BM + 32 * q + lane] = w;
+            }
+          } else if (row_ok && nb < p.N) {
+            const int cnt = min(32, p.N - nb);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j >= cnt) break;
-            float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
-            const int64_t doff = p.cd_col ? (int64_t)(nb + j) * p.ldd + row : (int64_t)row * p.ldd + nb + j;
-            const int64_t coff = p.cd_col ? (int64_t)(nb + j) * p.ldc + row : (int64_t)row * p.ldc + nb + j;
-            if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, coff, p.bf16), x);
-            reinterpret_cast<uint16_t*>(p.D)[doff] = to_cd(x, p.bf16);
+            for (int j = 0; j < 32; ++j) {
+              if (j >= cnt) break;
+              float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
+              const int64_t doff = p.cd_col ? (int64_t)(nb + j) * p.ldd + row : (int64_t)row * p.ldd + nb + j;
+              const int64_t coff = p.cd_col ? (int64_t)(nb + j) * p.ldc + row : (int64_t)row * p.ldc + nb + j;
+              if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, coff, p.bf16), x);
+              reinterpret_cast<uint16_t*>(p.D)[doff] = to_cd(x, p.bf16);
+            }
           }
+          if (c & 1) release(c >> 1);  // chunks 0, 1 are this warp's columns of half 0
         }
-      }
-      }
-      // the accumulator buffer is drained: the next tile's MMAs may reuse it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR && rank == 1)  // the accumulator reads above completed (wait::ld) before this arrive
-          mbar_arrive_remote_relaxed(pair_leader_addr(bar_tempty + 8 * acc));
-        else
-          mbar_arrive(bar_tempty + 8 * acc);
       }
       if (++acc == C::kAcc) {
         acc = 0;
@@ -813,8 +869,8 @@ __global__ void __maxnreg__(128)
       if (p.split_k == 1 && p.tma_store && mq < p.M) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int nb = ncol0 + 32 * c;
-          if (nb >= p.N) break;
+          const int nb = t.n0 + chunk_col(c);
+          if (nb >= p.N) continue;
           if (stored) {
             if (lane == 0) bulk_wait_read0();  // the previous store has read the staging block
             __syncwarp();
