@@ -271,25 +271,19 @@ def copies_for(bytes_per_launch: int) -> int:
     return max(4, min(32, -(-2 * L2_BYTES // max(1, bytes_per_launch))))
 
 
-def time_stream(torch, fns, reps=3):
+def time_stream(torch, fns, reps=5):
     """Median milliseconds per launch of `fns` run back to back on the stream.
 
     Every function works on its own buffers and the buffers of all of them
     together exceed twice the L2, so each launch reads its inputs from HBM,
-    as it does inside a longer sequence of work; launch latency overlaps the
-    previous kernel as it would there."""
-    for f in fns:
-        f()
+    as it does inside a longer sequence of work.  The launches are captured
+    once in a CUDA graph and the graph is replayed, as the training step is:
+    the host's per-call work (argument checks, marshalling) then does not
+    stand between the kernels, and launch latency overlaps the previous one."""
+    g = capture(torch, lambda: [f() for f in fns])
+    g.replay()
     torch.cuda.synchronize()
-    ts = []
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for f in fns:
-            f()
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) / len(fns))
+    ts = [time_replays(torch, g, 1) / len(fns) for _ in range(reps)]
     return statistics.median(ts)
 
 

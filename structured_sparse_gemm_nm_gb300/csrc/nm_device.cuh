@@ -55,6 +55,20 @@ __device__ __forceinline__ void tc_store(void* meta, int64_t r, int64_t k, int64
   *reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(meta) + tc_half_offset(r, k, nslots)) = (uint16_t)code16;
 }
 
+// Streaming multiprocessors of the current device (queried once).
+inline int num_sms_cached() {
+  static const int v = [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    return n;
+  }();
+  return v;
+}
+
 // Grid size for grid-stride loops: enough CTAs to fill 152 SMs several times.
 inline unsigned grid_for(int64_t work_items, int threads, int max_ctas_per_sm = 8) {
   int64_t g = (work_items + threads - 1) / threads;

@@ -12,6 +12,8 @@
 // metadata word), one 16-bit half of a mask word.  For aligned 16-bit data
 // the segment is two 128-bit loads and the eight kept values one 128-bit
 // store.  Other N:M shapes give each thread one group.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -269,6 +271,80 @@ __global__ void __launch_bounds__(256) prune24_pair_kernel(const typename Elem<D
     }
   }
   if (mask_bits != nullptr) mask_bits[r * ppr + p] = keep;
+}
+
+// 2:4 for 16-bit rows stored back to back (ld == cols, cols % 32 == 0): the
+// matrix is read as one array of 16-byte words, lane-contiguous, so every warp
+// access covers 512 consecutive bytes; a word holds two groups and yields 8
+// bytes of kept values, one byte of canonical metadata (the two 16-bit halves
+// of a tensor-core metadata word come from a lane and its neighbour) and one
+// byte of the mask.  Every warp of a resident grid takes an equal share of
+// the words (a multiple of 32), four words per lane in flight.
+constexpr int kLaneWords = 4;
+struct LaneSplit {
+  unsigned grid;
+  int64_t per;  // words per warp
+};
+inline LaneSplit lane_split(int64_t words) {
+  LaneSplit s;
+  int64_t g = (int64_t)num_sms_cached() * 5;  // five 256-thread CTAs per SM are resident
+  const int64_t need = (words + 255) / 256;
+  if (need < g) g = need;
+  if (g < 1) g = 1;
+  s.grid = (unsigned)g;
+  const int64_t warps = g * 8;
+  s.per = ((words + warps - 1) / warps + 31) / 32 * 32;
+  return s;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256, 5) prune24_lanes_kernel(const uint4* __restrict__ W, int64_t rows, int64_t cols,
+                                                               int64_t per, uint4* W_out, uint8_t* __restrict__ mask_bytes,
+                                                               uint2* __restrict__ vals, void* __restrict__ meta,
+                                                               int meta_tc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n16 = rows * cols / 8;
+  const int64_t lo = ((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5) * per;
+  const int64_t hi = lo + per < n16 ? lo + per : n16;
+  const int64_t nslots = ((rows + 127) / 128) * 128;
+  for (int64_t base = lo; base < hi; base += 32 * kLaneWords) {
+    uint4 x[kLaneWords];
+#pragma unroll
+    for (int u = 0; u < kLaneWords; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      x[u] = i < hi ? __ldcs(W + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kLaneWords; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      const uint32_t w0 = x[u].x, w1 = x[u].y, w2 = x[u].z, w3 = x[u].w;
+      const uint32_t c0 = top2of4(key_lo<DT>(w0), key_hi<DT>(w0), key_lo<DT>(w1), key_hi<DT>(w1));
+      const uint32_t c1 = top2of4(key_lo<DT>(w2), key_hi<DT>(w2), key_lo<DT>(w3), key_hi<DT>(w3));
+      const uint32_t code = c0 | (c1 << 4);
+      if (meta != nullptr && meta_tc) {  // uniform: the even lane of each pair stores 16 columns' code
+        const uint32_t code_hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+        if (i < hi && (lane & 1) == 0) {
+          const int64_t e = i * 8, r = e / cols;
+          tc_store(meta, r, (e - r * cols) / 16, nslots, code | (code_hi << 8));
+        }
+      }
+      if (i < hi) {
+        if (vals != nullptr)
+          vals[i] = make_uint2(__byte_perm(w0, w1, ((c0 & 3u) * 0x22u + 0x10u) | (((c0 >> 2) * 0x22u + 0x10u) << 8)),
+                               __byte_perm(w2, w3, ((c1 & 3u) * 0x22u + 0x10u) | (((c1 >> 2) * 0x22u + 0x10u) << 8)));
+        if (meta != nullptr && !meta_tc) static_cast<uint8_t*>(meta)[i] = (uint8_t)code;
+        if (W_out != nullptr || mask_bytes != nullptr) {
+          const uint32_t k0 = keep_of_code(c0), k1 = keep_of_code(c1);
+          if (W_out != nullptr)
+            W_out[i] = make_uint4(w0 & ((k0 & 1u) * 0xFFFFu | (k0 & 2u) * 0x7FFF8000u),
+                                  w1 & (((k0 >> 2) & 1u) * 0xFFFFu | ((k0 >> 2) & 2u) * 0x7FFF8000u),
+                                  w2 & ((k1 & 1u) * 0xFFFFu | (k1 & 2u) * 0x7FFF8000u),
+                                  w3 & (((k1 >> 2) & 1u) * 0xFFFFu | ((k1 >> 2) & 2u) * 0x7FFF8000u));
+          if (mask_bytes != nullptr) mask_bytes[i] = (uint8_t)(k0 | (k1 << 4));
+        }
+      }
+    }
+  }
 }
 
 // General n:m (m <= 32), one thread per group.  Composite keys (key << 5 |
@@ -599,6 +675,35 @@ __host__ __device__ constexpr uint32_t scatter_sel8(uint32_t code) {
   return sel;
 }
 
+// Decompression in the same lane-contiguous order and split: 8 bytes of kept
+// values and a canonical metadata byte per 16-byte output word.
+template <int DT>
+__global__ void __launch_bounds__(256, 5) decompress24_lanes_kernel(const uint2* __restrict__ vals,
+                                                                    const uint8_t* __restrict__ meta, int64_t n16,
+                                                                    int64_t per, uint4* __restrict__ W_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t lo = ((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5) * per;
+  const int64_t hi = lo + per < n16 ? lo + per : n16;
+  for (int64_t base = lo; base < hi; base += 32 * kLaneWords) {
+    uint2 v[kLaneWords];
+    uint32_t code[kLaneWords];
+#pragma unroll
+    for (int u = 0; u < kLaneWords; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      v[u] = i < hi ? __ldcs(vals + i) : make_uint2(0u, 0u);
+      code[u] = i < hi ? (uint32_t)__ldcs(meta + i) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kLaneWords; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      if (i >= hi) continue;
+      const uint32_t s0 = scatter_sel16(code[u] & 0xFu), s1 = scatter_sel16((code[u] >> 4) & 0xFu);
+      W_out[i] = make_uint4(__byte_perm(v[u].x, 0u, s0 & 0xFFFFu), __byte_perm(v[u].x, 0u, s0 >> 16),
+                            __byte_perm(v[u].y, 0u, s1 & 0xFFFFu), __byte_perm(v[u].y, 0u, s1 >> 16));
+    }
+  }
+}
+
 // Decompression for aligned rows whose length is a multiple of 32: one thread
 // per 32 columns; the kept values and codes are loaded as words, each group's
 // four outputs come from byte permutes with a selector looked up by its code.
@@ -670,7 +775,17 @@ cudaError_t prune_dt(const PruneLaunch& a, cudaStream_t s) {
     const int64_t es = (int64_t)sizeof(T);
     const bool vec = !a.trans && (a.colsL % 16 == 0) && (a.ld * es) % 16 == 0 && aligned16(W) &&
                      (W_out == nullptr || ((a.ld_out * es) % 16 == 0 && aligned16(W_out))) && aligned16(vals);
-    if (vec && a.colsL % 32 == 0) {
+    const bool lanes = sizeof(T) == 2 && vec && a.colsL % 32 == 0 && a.ld == a.colsL &&
+                       (W_out == nullptr || a.ld_out == a.colsL);
+    if (lanes) {
+      if constexpr (sizeof(T) == 2) {
+        const LaneSplit ls = lane_split(a.rowsL * a.colsL / 8);
+        prune24_lanes_kernel<DT><<<ls.grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(W), a.rowsL, a.colsL, ls.per,
+                                                          reinterpret_cast<uint4*>(W_out),
+                                                          reinterpret_cast<uint8_t*>(a.mask_bits),
+                                                          reinterpret_cast<uint2*>(vals), a.meta, a.meta_tc);
+      }
+    } else if (vec && a.colsL % 32 == 0) {
       const int64_t pairs = a.rowsL * (a.colsL / 32);
       prune24_pair_kernel<DT><<<(unsigned)((pairs + threads - 1) / threads), threads, 0, s>>>(
           W, a.rowsL, a.colsL, a.ld, W_out, a.ld_out, a.mask_bits, vals, a.meta, a.meta_tc);
@@ -732,7 +847,16 @@ cudaError_t decompress_dt(const DecompressLaunch& a, cudaStream_t s) {
     const bool vec = sizeof(T) == 2 && a.cols % 16 == 0 && (a.ld_out * 2) % 16 == 0 && aligned16(W_out);
     const bool pair = a.cols % 32 == 0 && (a.ld_out * (int64_t)sizeof(T)) % 16 == 0 && aligned16(W_out) &&
                       aligned16(vals) && (a.meta_tc || (reinterpret_cast<uintptr_t>(a.meta) & 3u) == 0);
-    if (pair) {
+    // lane order for canonical metadata; tensor-core metadata is stored by row slots, which
+    // the one-thread-per-32-columns kernel reads with fewer scattered accesses
+    if (pair && sizeof(T) == 2 && a.ld_out == a.cols && !a.meta_tc) {
+      if constexpr (sizeof(T) == 2) {
+        const LaneSplit ls = lane_split(a.rows * a.cols / 8);
+        decompress24_lanes_kernel<DT><<<ls.grid, 256, 0, s>>>(reinterpret_cast<const uint2*>(vals),
+                                                               static_cast<const uint8_t*>(a.meta), a.rows * a.cols / 8,
+                                                               ls.per, reinterpret_cast<uint4*>(W_out));
+      }
+    } else if (pair) {
       const int64_t pairs = a.rows * (a.cols / 32);
       decompress24_pair_kernel<DT><<<(unsigned)((pairs + threads - 1) / threads), threads, 0, s>>>(
           vals, a.meta, a.rows, a.cols, a.meta_tc, W_out, a.ld_out);

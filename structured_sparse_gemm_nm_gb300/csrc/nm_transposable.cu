@@ -110,7 +110,7 @@ __device__ __forceinline__ void store2(int8_t* p, int8_t a, int8_t b) {
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(256) transposable_kernel(const typename Elem<DT>::T* __restrict__ W, int64_t rows,
+__global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Elem<DT>::T* __restrict__ W, int64_t rows,
                                                            int64_t cols, int64_t ld, typename Elem<DT>::T* W_out,
                                                            int64_t ld_out, uint32_t* __restrict__ mask_bits,
                                                            typename Elem<DT>::T* __restrict__ vals,
@@ -153,27 +153,47 @@ __global__ void __launch_bounds__(256) transposable_kernel(const typename Elem<D
       p[r][4] = mg[1] + mg[3];
       p[r][5] = mg[2] + mg[3];
     }
-    float best = -1.0f;
-    uint32_t bmask = 0;
+    // The first pattern in (a, b, c) order with the largest score: the best over c for each
+    // (a, b), then over b, then over a, each comparison keeping the earlier pattern on equal
+    // scores; a tree of short chains instead of one chain of 90 dependent comparisons.
+    // Scores are never NaN (magnitudes are >= 0 or +Inf) and a valid pattern scores >= 0.
+    auto keep_first = [](float& s, uint32_t& m, float s2, uint32_t m2) {
+      if (s2 > s) {
+        s = s2;
+        m = m2;
+      }
+    };
+    float sa[6];
+    uint32_t ma[6];
 #pragma unroll
     for (int a = 0; a < 6; ++a) {
+      float sb[6];
+      uint32_t mb[6];
 #pragma unroll
       for (int b = 0; b < 6; ++b) {
         const float s01 = p[0][a] + p[1][b];
+        sb[b] = -1.0f;
+        mb[b] = 0u;
 #pragma unroll
         for (int c = 0; c < 6; ++c) {
           const int d = completion(a, b, c);
-          if (d >= 0) {
-            const float s = (s01 + p[2][c]) + p[3][d];
-            if (s > best) {
-              best = s;
-              bmask = tile_mask(a, b, c, d);
-            }
-          }
+          if (d >= 0) keep_first(sb[b], mb[b], (s01 + p[2][c]) + p[3][d], tile_mask(a, b, c, d));
         }
       }
+      keep_first(sb[0], mb[0], sb[1], mb[1]);
+      keep_first(sb[2], mb[2], sb[3], mb[3]);
+      keep_first(sb[4], mb[4], sb[5], mb[5]);
+      keep_first(sb[0], mb[0], sb[2], mb[2]);
+      keep_first(sb[0], mb[0], sb[4], mb[4]);
+      sa[a] = sb[0];
+      ma[a] = mb[0];
     }
-    if (!valid) bmask = 0;
+    keep_first(sa[0], ma[0], sa[1], ma[1]);
+    keep_first(sa[2], ma[2], sa[3], ma[3]);
+    keep_first(sa[4], ma[4], sa[5], ma[5]);
+    keep_first(sa[0], ma[0], sa[2], ma[2]);
+    keep_first(sa[0], ma[0], sa[4], ma[4]);
+    uint32_t bmask = valid ? ma[0] : 0u;
 
     // ---- pruned copy
     if (W_out != nullptr && valid) {
@@ -271,19 +291,20 @@ cudaError_t transposable_dt(const TransposableLaunch& a, cudaStream_t s) {
     }
   }
   const int64_t nblocks = ((a.rows + 15) / 16) * ((a.cols + 31) / 32);
-  const unsigned grid = grid_for(nblocks * 32, 256);
+  // 128-thread CTAs (four 16 x 32 blocks each) spread small matrices over every SM
+  const unsigned grid = grid_for(nblocks * 32, 128);
   // Vector accesses need 4-element rows aligned (W, W_out) and 2-element pairs aligned (vals, valsT).
   const uintptr_t a4 = 4 * sizeof(T), a2 = 2 * sizeof(T);
   const bool vec = (reinterpret_cast<uintptr_t>(a.W) % a4) == 0 && a.ld % 4 == 0 &&
                    (a.W_out == nullptr || ((reinterpret_cast<uintptr_t>(a.W_out) % a4) == 0 && a.ld_out % 4 == 0)) &&
                    (reinterpret_cast<uintptr_t>(a.vals) % a2) == 0 && (reinterpret_cast<uintptr_t>(a.valsT) % a2) == 0;
   if (vec)
-    transposable_kernel<DT, true><<<grid, 256, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
+    transposable_kernel<DT, true><<<grid, 128, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
                                                        static_cast<T*>(a.W_out), a.ld_out, a.mask_bits,
                                                        static_cast<T*>(a.vals), a.meta, static_cast<T*>(a.valsT),
                                                        a.metaT, a.meta_tc);
   else
-    transposable_kernel<DT, false><<<grid, 256, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
+    transposable_kernel<DT, false><<<grid, 128, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
                                                         static_cast<T*>(a.W_out), a.ld_out, a.mask_bits,
                                                         static_cast<T*>(a.vals), a.meta, static_cast<T*>(a.valsT),
                                                         a.metaT, a.meta_tc);

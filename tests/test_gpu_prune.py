@@ -96,7 +96,9 @@ COMPRESS_CASES = [
     (64, 128, "f16", 2, 4, 0, nb.NM_META_TC),
     (300, 1024, "bf16", 2, 4, 0, nb.NM_META_TC),
     (4096, 4096, "f16", 2, 4, 0, nb.NM_META_TC),
+    (4096, 4096, "bf16", 2, 4, 0, nb.NM_META_CANONICAL),
     (200, 96, "f16", 2, 4, 0, nb.NM_META_TC),
+    (136, 4128, "bf16", 2, 4, 0, nb.NM_META_CANONICAL),  # word count not a multiple of the warp's
     (37, 20, "f16", 2, 4, 0, nb.NM_META_CANONICAL),
     (128, 256, "i8", 2, 4, 0, nb.NM_META_CANONICAL),
     (256, 512, "f16", 2, 4, 1, nb.NM_META_TC),
