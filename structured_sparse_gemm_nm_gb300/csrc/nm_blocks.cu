@@ -67,14 +67,16 @@ WsLayout ws_layout(int64_t units) {
 }
 
 // ---------------------------------------------------------------- scoring
-// Flags: 1 NaN, 2 +Inf, 4 -Inf.
+// Flags: 1 NaN, 2 +Inf, 4 -Inf.  The value of a finite f16 in units of 2^-24 is
+// m << sh with m = mantissa plus the implicit bit (none for subnormals) and
+// sh = max(e - 1, 0): one 32 x 32 -> 64-bit multiply by 2^sh, no branch.
 __device__ __forceinline__ void acc_f16(uint32_t h, int64_t& s, int64_t& a, uint32_t& fl) {
   const uint32_t e = (h >> 10) & 31u, mnt = h & 1023u;
-  if (e == 31u) {
-    fl |= mnt ? 1u : ((h & 0x8000u) ? 4u : 2u);
-    return;
-  }
-  const int64_t u = e ? (int64_t)(1024u + mnt) << (e - 1) : (int64_t)mnt;
+  const bool special = e == 31u;
+  fl |= special ? (mnt ? 1u : ((h & 0x8000u) ? 4u : 2u)) : 0u;
+  const uint32_t m = special ? 0u : (e ? 1024u + mnt : mnt);
+  const uint32_t sh = e ? e - 1u : 0u;
+  const int64_t u = (int64_t)((uint64_t)m * (uint64_t)(1u << (sh & 31u)));
   s += (h & 0x8000u) ? -u : u;
   a += u;
 }

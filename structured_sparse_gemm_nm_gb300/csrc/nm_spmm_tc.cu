@@ -961,6 +961,57 @@ __global__ void finalize_split_kernel(const float4* __restrict__ part, int split
   }
 }
 
+// Row-major D from the tiled partials: one CTA per 128-row x 32-column slab of
+// a tile.  The partials are read in their stored order (consecutive rows for
+// each group of four columns), summed over the splits in split order, turned
+// through shared memory and written along D's rows, eight values per store.
+__global__ void __launch_bounds__(256) finalize_split_rows_kernel(const float4* __restrict__ part, int splits,
+                                                                  int num_m_blk, int num_n_blk, int64_t M, int64_t N,
+                                                                  const uint16_t* __restrict__ C,
+                                                                  uint16_t* __restrict__ D, int64_t ldc, int64_t ldd,
+                                                                  float beta, int bf16) {
+  __shared__ float sm[BM][33];
+  const int64_t tile = blockIdx.x / (BN / 32);
+  const int slab = blockIdx.x - (int)tile * (BN / 32);
+  const int64_t per_split = (int64_t)num_m_blk * num_n_blk * (BM * BN / 4);
+  const float4* src = part + tile * (BM * BN / 4) + (int64_t)slab * 8 * BM;  // column groups 8 slab .. 8 slab + 7
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = threadIdx.x + 256 * k;  // (column group g, row r) = (e / 128, e % 128)
+    float4 x = src[e];
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 y = src[(int64_t)sp * per_split + e];
+      x.x += y.x, x.y += y.y, x.z += y.z, x.w += y.w;
+    }
+    const int g = e / BM, r = e - g * BM;
+    sm[r][4 * g] = x.x, sm[r][4 * g + 1] = x.y, sm[r][4 * g + 2] = x.z, sm[r][4 * g + 3] = x.w;
+  }
+  __syncthreads();
+  const int64_t m0 = (tile / num_n_blk) * BM, n0 = (tile % num_n_blk) * BN + 32 * slab;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int e = threadIdx.x + 256 * k;  // (row r, eight columns q) = (e / 4, e % 4)
+    const int r = e >> 2, q = e & 3;
+    const int64_t m = m0 + r, n = n0 + 8 * q;
+    if (m >= M || n >= N) continue;
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      o[j] = sm[r][8 * q + j];
+      if (C != nullptr && n + j < N) o[j] = fmaf(beta, load_cd(C, m * ldc + n + j, bf16), o[j]);
+    }
+    uint16_t* dst = D + m * ldd + n;
+    if (n + 8 <= N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+      uint4 w;
+      w.x = pack2(o[0], o[1], bf16), w.y = pack2(o[2], o[3], bf16), w.z = pack2(o[4], o[5], bf16),
+      w.w = pack2(o[6], o[7], bf16);
+      *reinterpret_cast<uint4*>(dst) = w;
+    } else {
+      for (int j = 0; j < 8 && n + j < N; ++j) dst[j] = to_cd(o[j], bf16);
+    }
+  }
+}
+
 // ----------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1207,6 +1258,13 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
   cudaError_t e =
       cl == 2 ? launch_kernel<false, 2, false>(mA, mB, mD, p, s) : launch_kernel<false, 1, false>(mA, mB, mD, p, s);
   if (e != cudaSuccess || p.split_k == 1) return e;
+  if (d.order_cd == NM_ROW) {
+    finalize_split_rows_kernel<<<(unsigned)((int64_t)p.num_m_blk * p.num_n_blk * (BN / 32)), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(p.partial), p.split_k, p.num_m_blk, p.num_n_blk, d.M, d.N,
+        static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.ldc, d.ldd, a.beta_f, d.ab_type == NM_BF16);
+    return cudaGetLastError();
+  }
+  // column-major D: the stored order already runs along D's columns
   const int64_t groups = (int64_t)p.num_m_blk * p.num_n_blk * (BM * BN / 4);
   finalize_split_kernel<<<grid_for(groups, 256), 256, 0, s>>>(
       reinterpret_cast<const float4*>(p.partial), p.split_k, p.num_m_blk, p.num_n_blk, d.M, d.N,
