@@ -704,8 +704,10 @@ def run_native(args):
 
 
 # ------------------------------------------------------------------ single-kernel cases (ncu captures)
-KERNEL_CASES = ("sparse_fc1_fwd", "sparse_fc2_dx", "dense_fc1_dw", "transposable_fc1", "prune24_4096",
-                "prune_8of32_4096", "gemv_8of32_b8", "vector_wise_4096")
+LINEARS = {"qkv": (2304, 768), "o": (768, 768), "fc1": (3072, 768), "fc2": (768, 3072)}  # out x in
+SPARSE_CASES = tuple(f"sparse_{lin}_{d}" for lin in LINEARS for d in ("fwd", "dx"))
+KERNEL_CASES = SPARSE_CASES + ("dense_fc1_dw", "transposable_fc1", "prune24_4096", "prune_8of32_4096",
+                               "gemv_8of32_b8", "vector_wise_4096")
 
 
 def run_kernel_case(name: str, reps: int = 3):
@@ -718,7 +720,20 @@ def run_kernel_case(name: str, reps: int = 3):
     dev = torch.device("cuda", 0)
     nb.lib()
     T = inputs.GPTNEO_TOKENS
-    if name in ("sparse_fc1_fwd", "sparse_fc2_dx", "dense_fc1_dw", "transposable_fc1"):
+    if name in SPARSE_CASES:
+        # the step's sparse product of one linear: forward (M = out, K = in) or dX (M = in, K = out)
+        _, lin, d = name.split("_")
+        o, i = LINEARS[lin]
+        M, K = (o, i) if d == "fwd" else (i, o)
+        W = inputs.normal((M, K), 0.02, 1, "bf16", device=dev)
+        vb, mb = nb.nm_compressed_size(M, K, "bf16", 2, 4, nb.NM_META_TC)
+        vals, meta = (torch.empty(vb, dtype=torch.uint8, device=dev), torch.empty(mb, dtype=torch.uint8, device=dev))
+        nb.nm_compress(W, M, K, K, "bf16", 2, 4, 0, nb.NM_META_TC, vals, meta)
+        X = inputs.normal((T, K), 1.0, 2, "bf16", device=dev)
+        Y = torch.empty((T, M), dtype=torch.bfloat16, device=dev)
+        plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=T, K=K, ab_type="bf16", cd_type="bf16", ldb=K, ldd=M))
+        fn = [lambda: nb.nm_spmm(plan, 1.0, vals, meta, X, 0.0, None, Y)]
+    elif name in ("dense_fc1_dw", "transposable_fc1"):
         o, i = 3072, 768  # FC1 weight (out x in); FC2 dX has the same M, K
         W = inputs.normal((o, i), 0.02, 1, "bf16", device=dev)
         vb, mb = nb.nm_compressed_size(o, i, "bf16", 2, 4, nb.NM_META_TC)
@@ -731,7 +746,7 @@ def run_kernel_case(name: str, reps: int = 3):
             valsT, metaT = (torch.empty(vbT, dtype=torch.uint8, device=dev), torch.empty(mbT, dtype=torch.uint8, device=dev))
             fn = [lambda Wr=Wr: nb.nm_prune_transposable(Wr, o, i, i, "bf16", None, 0, mask, vals, meta, valsT, metaT,
                                                          nb.NM_META_TC) for Wr in Ws]
-        elif name == "dense_fc1_dw":
+        else:
             dY = inputs.normal((T, o), 1.0, 2, "bf16", device=dev)
             X = inputs.normal((T, i), 1.0, 3, "bf16", device=dev)
             dW = torch.empty((o, i), dtype=torch.bfloat16, device=dev)
@@ -741,11 +756,6 @@ def run_kernel_case(name: str, reps: int = 3):
             wsb = nb.nm_spmm_plan_workspace(plan)
             ws = torch.empty(max(16, wsb), dtype=torch.uint8, device=dev)
             fn = [lambda: nb.nm_spmm(plan, 1.0, dY, mask, X, 0.0, None, dW, ws if wsb else None, wsb)]
-        else:
-            X = inputs.normal((T, i), 1.0, 2, "bf16", device=dev)
-            Y = torch.empty((T, o), dtype=torch.bfloat16, device=dev)
-            plan = nb.nm_spmm_plan(nb.make_desc(M=o, N=T, K=i, ab_type="bf16", cd_type="bf16", ldb=i, ldd=o))
-            fn = [lambda: nb.nm_spmm(plan, 1.0, vals, meta, X, 0.0, None, Y)]
     elif name in ("prune24_4096", "prune_8of32_4096", "gemv_8of32_b8"):
         M = K = 4096
         n, m = (2, 4) if name == "prune24_4096" else (8, 32)
