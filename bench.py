@@ -176,6 +176,18 @@ class GptNeoTrain:
     def flops_per_step(self) -> float:
         return 3.0 * sum(self.gemm_flops(j) for j in range(len(self.linears))) * len(self.layers)
 
+    def enqueue_one(self, l: int, j: int) -> int:
+        """Launch one linear's work (layer l, linear j) on the current stream; returns the launch count."""
+        nb, L = self.nb, self.layers[l][j]
+        o, i = L["out"], L["inp"]
+        nb.nm_prune_transposable(L["W"], o, i, i, "bf16", None, 0, L["mask"], L["vals"], L["meta"], L["valsT"],
+                                 L["metaT"], nb.NM_META_TC)
+        nb.nm_spmm(self.p_fwd[j], 1.0, L["vals"], L["meta"], L["X"], 0.0, None, self.Y[j])
+        nb.nm_spmm(self.p_dx[j], 1.0, L["valsT"], L["metaT"], L["dY"], 0.0, None, self.dX[j])
+        ws, wsb = self.ws[j]
+        nb.nm_spmm(self.p_dw[j], 1.0, L["dY"], L["mask"], L["X"], 0.0, None, L["dW"], ws if wsb else None, wsb)
+        return 4
+
     def enqueue(self, parts=("prune", "fwd", "dx", "dw"), only=None) -> int:
         """Launch the step's work on the current stream; returns the number of kernels launched."""
         nb = self.nb
@@ -647,12 +659,46 @@ def run_native(args):
         h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
         d2h = sum(h.numel() * h.element_size() for h, _ in host_out)
 
+        # Pipelined: each linear's inputs are copied on one of two copy streams, its work runs on
+        # the compute stream as soon as they have landed, and its dW goes back on a third stream
+        # as soon as it is written.  Across steps, a copy into a buffer waits for the previous
+        # step's reads of it (compute reading W, X, dY; the copy-out reading dW).
+        n_lin = len(host_out)
+        s_c = torch.cuda.current_stream()
+        s_in = [torch.cuda.Stream(), torch.cuda.Stream()]
+        s_out = torch.cuda.Stream()
+        e_in = [torch.cuda.Event() for _ in range(n_lin)]
+        e_done = [torch.cuda.Event() for _ in range(n_lin)]
+        e_out = [torch.cuda.Event() for _ in range(n_lin)]
+        seen = [False]
+
         def e2e_step():
-            for h, d in host_in:
-                d.copy_(h, non_blocking=True)
-            g_step.replay()
-            for h, d in host_out:
-                h.copy_(d, non_blocking=True)
+            for st in s_in + [s_out]:
+                st.wait_stream(s_c)
+            k = 0
+            for l, lay in enumerate(wl.layers):
+                for j, L in enumerate(lay):
+                    si = s_in[k % 2]
+                    with torch.cuda.stream(si):
+                        if seen[0]:
+                            si.wait_event(e_done[k])
+                        for h, d in host_in[3 * k:3 * k + 3]:
+                            d.copy_(h, non_blocking=True)
+                        e_in[k].record(si)
+                    s_c.wait_event(e_in[k])
+                    if seen[0]:
+                        s_c.wait_event(e_out[k])
+                    wl.enqueue_one(l, j)
+                    e_done[k].record(s_c)
+                    with torch.cuda.stream(s_out):
+                        s_out.wait_event(e_done[k])
+                        h, d = host_out[k]
+                        h.copy_(d, non_blocking=True)
+                        e_out[k].record(s_out)
+                    k += 1
+            seen[0] = True
+            for st in s_in + [s_out]:
+                s_c.wait_stream(st)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -670,8 +716,9 @@ def run_native(args):
         ems = aggregate_over_ranks(torch, dist, a.elapsed_time(b)) / reps
         e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems,
-               "path": "pinned host -> device copies of W, X, dY of every linear, the step through the C ABI, "
-                       "dW of every linear back to pinned host memory, one stream"}
+               "path": "pinned host -> device copies of W, X, dY of every linear on two copy streams; each "
+                       "linear's prune, forward, dX and dW through the C ABI on the compute stream once its "
+                       "inputs have landed; each dW back to pinned host memory on a third stream once written"}
         del host_in, host_out
     clocks = sampler.stop()
 
