@@ -67,16 +67,15 @@ WsLayout ws_layout(int64_t units) {
 }
 
 // ---------------------------------------------------------------- scoring
-// Flags: 1 NaN, 2 +Inf, 4 -Inf.  The value of a finite f16 in units of 2^-24 is
-// m << sh with m = mantissa plus the implicit bit (none for subnormals) and
-// sh = max(e - 1, 0): one 32 x 32 -> 64-bit multiply by 2^sh, no branch.
+// Flags: 1 NaN, 2 +Inf, 4 -Inf.  A finite f16 in units of 2^-24: (1024 + mantissa)
+// << (e - 1) for normal numbers, the mantissa for subnormals.
 __device__ __forceinline__ void acc_f16(uint32_t h, int64_t& s, int64_t& a, uint32_t& fl) {
   const uint32_t e = (h >> 10) & 31u, mnt = h & 1023u;
-  const bool special = e == 31u;
-  fl |= special ? (mnt ? 1u : ((h & 0x8000u) ? 4u : 2u)) : 0u;
-  const uint32_t m = special ? 0u : (e ? 1024u + mnt : mnt);
-  const uint32_t sh = e ? e - 1u : 0u;
-  const int64_t u = (int64_t)((uint64_t)m * (uint64_t)(1u << (sh & 31u)));
+  if (e == 31u) {
+    fl |= mnt ? 1u : ((h & 0x8000u) ? 4u : 2u);
+    return;
+  }
+  const int64_t u = e ? (int64_t)(1024u + mnt) << (e - 1) : (int64_t)mnt;
   s += (h & 0x8000u) ? -u : u;
   a += u;
 }
@@ -554,8 +553,12 @@ __global__ void __launch_bounds__(256) vw_spmv_kernel(const SpmmLaunch a) {
 // Block-wise: a CTA per block row; its 8 warps split the kept blocks.  Lane l
 // covers columns 8*(l%4)..+7 of block rows l/4 + 8j, j = 0..3, so that every
 // warp load reads 512 contiguous bytes of a block.
+// One CTA of kBwWarps warps per 32-row block row: each warp takes every kBwWarps-th
+// kept block, so a block row's kept blocks (a quarter of them at the benchmark's
+// density) are all in flight at once.
+constexpr int kBwWarps = 32;
 template <int NB>
-__global__ void __launch_bounds__(256) bw_spmv_kernel(const SpmmLaunch a) {
+__global__ void __launch_bounds__(kBwWarps * 32) bw_spmv_kernel(const SpmmLaunch a) {
   const nm_spmm_desc_t& d = a.d;
   const int bf16 = d.ab_type == NM_BF16;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(256) bw_spmv_kernel(const SpmmLaunch a) {
   const uint16_t* B = static_cast<const uint16_t*>(a.B);
   const int p0 = csr[bi], p1 = csr[bi + 1];
   const int part = lane & 3, rq = lane >> 2;
-  __shared__ float red[8][32][NB];
+  __shared__ float red[kBwWarps][32][NB];
   for (int64_t b0 = 0; b0 < d.N; b0 += NB) {
     const int nb = (int)(d.N - b0 < NB ? d.N - b0 : NB);
     float acc[4][NB];
@@ -575,7 +578,7 @@ __global__ void __launch_bounds__(256) bw_spmv_kernel(const SpmmLaunch a) {
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int b = 0; b < NB; ++b) acc[j][b] = 0.0f;
-    for (int p = p0 + w; p < p1; p += 8) {
+    for (int p = p0 + w; p < p1; p += kBwWarps) {
       const int64_t c = colidx[p];
       const uint16_t* blk = vals + (int64_t)p * 1024;
       uint4 av[4];
@@ -599,7 +602,7 @@ __global__ void __launch_bounds__(256) bw_spmv_kernel(const SpmmLaunch a) {
       if (b < nb) {
         float s = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) s += red[k][row][b];
+        for (int k = 0; k < kBwWarps; ++k) s += red[k][row][b];
         store_d(a, bi * 32 + row, b0 + b, s, bf16);
       }
     }
@@ -697,9 +700,9 @@ cudaError_t launch_spmm_blocks(const SpmmLaunch& a, cudaStream_t s) {
   } else {
     const unsigned grid = (unsigned)(d.M / 32);
     if (d.N == 1)
-      bw_spmv_kernel<1><<<grid, 256, 0, s>>>(a);
+      bw_spmv_kernel<1><<<grid, kBwWarps * 32, 0, s>>>(a);
     else
-      bw_spmv_kernel<8><<<grid, 256, 0, s>>>(a);
+      bw_spmv_kernel<8><<<grid, kBwWarps * 32, 0, s>>>(a);
   }
   return cudaGetLastError();
 }

@@ -50,18 +50,27 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
     __syncthreads();
     if (NB == 1) {
     } else if (vstage) {
+      // a thread takes eight k of all NB (= 8) columns: eight 16-byte loads along B's rows,
+      // a transpose in registers, eight 16-byte stores of one k's NB values each; k's slot
+      // is k ^ ((k >> 3) & 7), so the eight lanes of a store phase hit different banks
+      static_assert(NB == 1 || NB == 8, "x is staged as [k][8]");
       const int64_t k8 = K / 8;
-      for (int64_t i = threadIdx.x; i < k8 * NB; i += blockDim.x) {
-        const int b = (int)(i / k8);
-        const int64_t kk = (i - (int64_t)b * k8) * 8;
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (b < nb) q = __ldg(reinterpret_cast<const uint4*>(B + (b0 + b) * ldb + kk));
-        if constexpr (NB == 1) {
-          reinterpret_cast<uint4*>(xs)[i] = q;
-        } else {
-          const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+      for (int64_t c = threadIdx.x; c < k8; c += blockDim.x) {
+        const int64_t kk = c * 8;
+        uint32_t q[NB][4];
 #pragma unroll
-          for (int t = 0; t < 8; ++t) xs[(kk + t) * NB + b] = (uint16_t)(qw[t / 2] >> (16 * (t % 2)));
+        for (int b = 0; b < NB; ++b) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (b < nb) v = __ldg(reinterpret_cast<const uint4*>(B + (b0 + b) * ldb + kk));
+          q[b][0] = v.x, q[b][1] = v.y, q[b][2] = v.z, q[b][3] = v.w;
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          uint32_t w[4];
+#pragma unroll
+          for (int pr = 0; pr < 4; ++pr)
+            w[pr] = ((q[2 * pr][t / 2] >> (16 * (t % 2))) & 0xFFFFu) | ((q[2 * pr + 1][t / 2] >> (16 * (t % 2))) << 16);
+          xs4[kk + (t ^ (int)(c & 7))] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     } else {
@@ -79,9 +88,25 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
       const uint16_t* vr = vals + r * kc;
       const uint8_t* ir = idx + r * kc;
       if (vec) {
-        for (int64_t j0 = (int64_t)lane * 8; j0 < kc; j0 += 256) {
-          const uint4 v4 = __ldcs(reinterpret_cast<const uint4*>(vr + j0));
-          const uint2 i2 = __ldcs(reinterpret_cast<const uint2*>(ir + j0));
+        // up to CH chunks of 256 kept values per warp with all their loads in flight first
+        constexpr int CH = NB == 1 ? 4 : 2;
+        for (int64_t jb = 0; jb < kc; jb += 256 * CH) {
+          uint4 v4s[CH];
+          uint2 i2s[CH];
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+            const int64_t j0 = jb + 256 * c + (int64_t)lane * 8;
+            if (j0 < kc) {
+              v4s[c] = __ldcs(reinterpret_cast<const uint4*>(vr + j0));
+              i2s[c] = __ldcs(reinterpret_cast<const uint2*>(ir + j0));
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+          const int64_t j0 = jb + 256 * c + (int64_t)lane * 8;
+          if (j0 >= kc) break;
+          const uint4 v4 = v4s[c];
+          const uint2 i2 = i2s[c];
           const uint32_t vw[4] = {v4.x, v4.y, v4.z, v4.w};
           const uint32_t iw[2] = {i2.x, i2.y};
 #pragma unroll
@@ -92,11 +117,12 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
             if constexpr (NB == 1) {
               acc[0] = fmaf(a, to_f(__ldg(xg + k), bf16), acc[0]);
             } else {
-              const uint4 x4 = *reinterpret_cast<const uint4*>(xs + k * NB);
+              const uint4 x4 = xs4[vstage ? (k ^ ((k >> 3) & 7)) : k];
               const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
               for (int b = 0; b < NB; ++b) acc[b] = fmaf(a, to_f((uint16_t)(xw[b / 2] >> (16 * (b % 2))), bf16), acc[b]);
             }
+          }
           }
         }
       } else {
@@ -107,7 +133,8 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
             acc[0] = fmaf(a, to_f(__ldg(xg + k), bf16), acc[0]);
           } else {
 #pragma unroll
-            for (int b = 0; b < NB; ++b) acc[b] = fmaf(a, to_f(xs[k * NB + b], bf16), acc[b]);
+            for (int b = 0; b < NB; ++b)
+              acc[b] = fmaf(a, to_f(xs[(vstage ? (k ^ ((k >> 3) & 7)) : k) * NB + b], bf16), acc[b]);
           }
         }
       }
