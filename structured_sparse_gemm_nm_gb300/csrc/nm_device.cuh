@@ -55,6 +55,32 @@ __device__ __forceinline__ void tc_store(void* meta, int64_t r, int64_t k, int64
   *reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(meta) + tc_half_offset(r, k, nslots)) = (uint16_t)code16;
 }
 
+// Programmatic dependent launch.  A grid launched with launch_pdl may be scheduled
+// while the previous grid of its stream is still finishing: pdl_wait() returns once
+// that grid has completed and its memory operations are visible (at once for a grid
+// launched without the attribute), so every kernel calls it before its first global
+// memory access; pdl_trigger() lets the next grid be scheduled as this one's CTAs
+// exit (called once every CTA of this grid runs, so the next grid never takes the
+// resources a CTA of this one still waits for).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Streaming multiprocessors of the current device (queried once).
 inline int num_sms_cached() {
   static const int v = [] {

@@ -456,6 +456,9 @@ __global__ void __maxnreg__(128)
   if (CL > 1) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // set-up done: from here on global memory may hold the previous grid's results
+  pdl_trigger();
+  pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer
@@ -936,6 +939,8 @@ __global__ void finalize_split_kernel(const float4* __restrict__ part, int split
                                       int64_t M, int64_t N, const uint16_t* __restrict__ C, uint16_t* __restrict__ D,
                                       int64_t ldc, int64_t ldd, int cd_col, float beta, int bf16) {
   // one thread per four columns of one row, in the tiled order the product wrote
+  pdl_trigger();
+  pdl_wait();
   const int64_t per_split = (int64_t)num_m_blk * num_n_blk * (BM * BN / 4);
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < per_split;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -971,6 +976,8 @@ __global__ void __launch_bounds__(256) finalize_split_rows_kernel(const float4* 
                                                                   uint16_t* __restrict__ D, int64_t ldc, int64_t ldd,
                                                                   float beta, int bf16) {
   __shared__ float sm[BM][33];
+  pdl_trigger();
+  pdl_wait();
   const int64_t tile = blockIdx.x / (BN / 32);
   const int slab = blockIdx.x - (int)tile * (BN / 32);
   const int64_t per_split = (int64_t)num_m_blk * num_n_blk * (BM * BN / 4);
@@ -1145,6 +1152,13 @@ cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const CU
   }
   const int clusters = p.num_units < max_clusters ? p.num_units : max_clusters;
   cfg.gridDim = dim3((unsigned)(clusters * CL));
+  // programmatic dependent launch (the kernel waits for the previous grid after its set-up)
+  cudaLaunchAttribute attr2[2];
+  attr2[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr2[0].val.programmaticStreamSerializationAllowed = 1;
+  attr2[1] = attr[0];
+  cfg.attrs = attr2;
+  cfg.numAttrs = CL > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, spmm_tc_kernel<SPARSE, CL, PAIR>, mA, mB, mD, p);
 }
 
@@ -1259,10 +1273,10 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
       cl == 2 ? launch_kernel<false, 2, false>(mA, mB, mD, p, s) : launch_kernel<false, 1, false>(mA, mB, mD, p, s);
   if (e != cudaSuccess || p.split_k == 1) return e;
   if (d.order_cd == NM_ROW) {
-    finalize_split_rows_kernel<<<(unsigned)((int64_t)p.num_m_blk * p.num_n_blk * (BN / 32)), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(p.partial), p.split_k, p.num_m_blk, p.num_n_blk, d.M, d.N,
-        static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.ldc, d.ldd, a.beta_f, d.ab_type == NM_BF16);
-    return cudaGetLastError();
+    return launch_pdl(finalize_split_rows_kernel, dim3((unsigned)((int64_t)p.num_m_blk * p.num_n_blk * (BN / 32))),
+                      dim3(256), 0, s, reinterpret_cast<const float4*>(p.partial), p.split_k, p.num_m_blk,
+                      p.num_n_blk, d.M, d.N, static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.ldc,
+                      d.ldd, a.beta_f, (int)(d.ab_type == NM_BF16));
   }
   // column-major D: the stored order already runs along D's columns
   const int64_t groups = (int64_t)p.num_m_blk * p.num_n_blk * (BM * BN / 4);

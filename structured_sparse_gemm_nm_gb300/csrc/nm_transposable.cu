@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Ele
                                                            typename Elem<DT>::T* __restrict__ valsT,
                                                            void* __restrict__ metaT, int meta_tc) {
   using T = typename Elem<DT>::T;
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int tr = lane >> 3, tcol = lane & 7;
   const int64_t nbr = (rows + 15) / 16, nbc = (cols + 31) / 32;
@@ -298,17 +300,15 @@ cudaError_t transposable_dt(const TransposableLaunch& a, cudaStream_t s) {
   const bool vec = (reinterpret_cast<uintptr_t>(a.W) % a4) == 0 && a.ld % 4 == 0 &&
                    (a.W_out == nullptr || ((reinterpret_cast<uintptr_t>(a.W_out) % a4) == 0 && a.ld_out % 4 == 0)) &&
                    (reinterpret_cast<uintptr_t>(a.vals) % a2) == 0 && (reinterpret_cast<uintptr_t>(a.valsT) % a2) == 0;
+  const T* W = static_cast<const T*>(a.W);
+  T* W_out = static_cast<T*>(a.W_out);
+  T* vals = static_cast<T*>(a.vals);
+  T* valsT = static_cast<T*>(a.valsT);
   if (vec)
-    transposable_kernel<DT, true><<<grid, 128, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
-                                                       static_cast<T*>(a.W_out), a.ld_out, a.mask_bits,
-                                                       static_cast<T*>(a.vals), a.meta, static_cast<T*>(a.valsT),
-                                                       a.metaT, a.meta_tc);
-  else
-    transposable_kernel<DT, false><<<grid, 128, 0, s>>>(static_cast<const T*>(a.W), a.rows, a.cols, a.ld,
-                                                        static_cast<T*>(a.W_out), a.ld_out, a.mask_bits,
-                                                        static_cast<T*>(a.vals), a.meta, static_cast<T*>(a.valsT),
-                                                        a.metaT, a.meta_tc);
-  return cudaGetLastError();
+    return launch_pdl(transposable_kernel<DT, true>, dim3(grid), dim3(128), 0, s, W, a.rows, a.cols, a.ld, W_out,
+                      a.ld_out, a.mask_bits, vals, a.meta, valsT, a.metaT, a.meta_tc);
+  return launch_pdl(transposable_kernel<DT, false>, dim3(grid), dim3(128), 0, s, W, a.rows, a.cols, a.ld, W_out,
+                    a.ld_out, a.mask_bits, vals, a.meta, valsT, a.metaT, a.meta_tc);
 }
 
 }  // namespace
