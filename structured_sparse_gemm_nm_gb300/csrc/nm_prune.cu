@@ -655,6 +655,51 @@ __global__ void __launch_bounds__(256) check_kernel(const typename Elem<DT>::T* 
   if ((threadIdx.x & 31) == 0 && count) atomicAdd(d_violations, count);
 }
 
+// 2:4 check of 16-bit rows in one pass over strips of four rows: a thread reads the
+// same 16-byte word (eight columns) of the strip's four rows, counts the two row
+// groups of each and, for the transposable check, every column of the strip.
+// Nonzero bits: (w & 0x7FFF7FFF) + 0x7FFF7FFF carries into bit 15 / 31 exactly for
+// a half that is not +-0 (no carry crosses the halves).
+__device__ __forceinline__ uint32_t nz8(const uint4 x) {
+  auto h = [](uint32_t w) { return ((w & 0x7FFF7FFFu) + 0x7FFF7FFFu) & 0x80008000u; };
+  const uint32_t a = h(x.x), b = h(x.y), c = h(x.z), d = h(x.w);
+  return ((a >> 15) & 1u) | ((a >> 30) & 2u) | ((b >> 13) & 4u) | ((b >> 28) & 8u) | ((c >> 11) & 16u) |
+         ((c >> 26) & 32u) | ((d >> 9) & 64u) | ((d >> 24) & 128u);
+}
+__global__ void __launch_bounds__(256) check24_strips_kernel(const uint4* __restrict__ W, int64_t rows, int64_t wpr,
+                                                             int64_t ldw, int transposable, int64_t per,
+                                                             int32_t* __restrict__ d_violations) {
+  // every warp takes `per` consecutive items (strip, word), two per lane in flight
+  const int lane = threadIdx.x & 31;
+  const int64_t total = ((rows + 3) / 4) * wpr;
+  const int64_t lo = ((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5) * per;
+  const int64_t hi = lo + per < total ? lo + per : total;
+  int count = 0;
+  for (int64_t base = lo; base < hi; base += 64) {
+    uint32_t m[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t idx = base + 32 * u + lane;
+      const int64_t st = idx / wpr, w = idx - st * wpr;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t r = 4 * st + j;
+        m[u][j] = (idx < hi && r < rows) ? nz8(__ldcs(W + r * ldw + w)) : 0u;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) count += (__popc(m[u][j] & 0xFu) > 2) + (__popc(m[u][j] >> 4) > 2);
+      if (transposable)  // columns with at least three of the strip's four entries nonzero
+        count += __popc((m[u][0] & m[u][1] & (m[u][2] | m[u][3])) | ((m[u][0] | m[u][1]) & m[u][2] & m[u][3]));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) count += __shfl_xor_sync(0xFFFFFFFFu, count, off);
+  if ((threadIdx.x & 31) == 0 && count) atomicAdd(d_violations, count);
+}
+
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Byte-permute selectors that scatter a group's kept pair back to its four
@@ -673,6 +718,73 @@ __host__ __device__ constexpr uint32_t scatter_sel8(uint32_t code) {
   for (int t = 0; t < 4; ++t)
     sel |= ((uint32_t)t == (code & 3u) ? 0u : ((uint32_t)t == (code >> 2) ? 1u : 4u)) << (4 * t);
   return sel;
+}
+
+// 2:4 for 16-bit rows with tensor-core metadata: one CTA per 16-row x 512-column
+// tile.  The selection runs as in the lane kernel (thread (r, g) takes words
+// g, g + 16, g + 32, g + 48 of tile row r, so each row is read in 256-byte runs)
+// and leaves each word's code byte in shared memory; then each thread writes one
+// whole metadata word, the two rows 8 apart that share it, so a k-step's 16 slot
+// words are one 64-byte run.  Slots of rows past the matrix get the valid code 0x4.
+template <int DT>
+__global__ void __launch_bounds__(256) prune24_tc_tile_kernel(const uint4* __restrict__ W, int64_t rows, int64_t cols,
+                                                              int64_t ldw, uint4* W_out, int64_t ldw_out,
+                                                              uint8_t* __restrict__ mask_bytes,
+                                                              uint2* __restrict__ vals, uint32_t* __restrict__ meta) {
+  __shared__ uint8_t codes[16][64];
+  const int64_t wpr = cols / 8;  // 16-byte words per row
+  const int64_t tiles_c = (wpr + 63) / 64, tiles = ((rows + 15) / 16) * tiles_c;
+  const int64_t nslots = ((rows + 127) / 128) * 128;
+  const int tr = threadIdx.x >> 4, g = threadIdx.x & 15;
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t row0 = (tile / tiles_c) * 16, w0 = (tile % tiles_c) * 64;
+    const int64_t r = row0 + tr;
+    uint4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t w = w0 + g + 16 * u;
+      x[u] = (r < rows && w < wpr) ? __ldcs(W + r * ldw + w) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t w = w0 + g + 16 * u;
+      const uint32_t w0_ = x[u].x, w1 = x[u].y, w2 = x[u].z, w3 = x[u].w;
+      const uint32_t c0 = top2of4(key_lo<DT>(w0_), key_hi<DT>(w0_), key_lo<DT>(w1), key_hi<DT>(w1));
+      const uint32_t c1 = top2of4(key_lo<DT>(w2), key_hi<DT>(w2), key_lo<DT>(w3), key_hi<DT>(w3));
+      codes[tr][g + 16 * u] = (uint8_t)(r < rows ? (c0 | (c1 << 4)) : 0x44u);
+      if (r < rows && w < wpr) {
+        const int64_t i = r * wpr + w;  // index in the packed values and mask
+        if (vals != nullptr)
+          vals[i] = make_uint2(
+              __byte_perm(w0_, w1, ((c0 & 3u) * 0x22u + 0x10u) | (((c0 >> 2) * 0x22u + 0x10u) << 8)),
+              __byte_perm(w2, w3, ((c1 & 3u) * 0x22u + 0x10u) | (((c1 >> 2) * 0x22u + 0x10u) << 8)));
+        if (W_out != nullptr || mask_bytes != nullptr) {
+          const uint32_t k0 = keep_of_code(c0), k1 = keep_of_code(c1);
+          if (W_out != nullptr)
+            W_out[r * ldw_out + w] = make_uint4(w0_ & ((k0 & 1u) * 0xFFFFu | (k0 & 2u) * 0x7FFF8000u),
+                                                w1 & (((k0 >> 2) & 1u) * 0xFFFFu | ((k0 >> 2) & 2u) * 0x7FFF8000u),
+                                                w2 & ((k1 & 1u) * 0xFFFFu | (k1 & 2u) * 0x7FFF8000u),
+                                                w3 & (((k1 >> 2) & 1u) * 0xFFFFu | ((k1 >> 2) & 2u) * 0x7FFF8000u));
+          if (mask_bytes != nullptr) mask_bytes[i] = (uint8_t)(k0 | (k1 << 4));
+        }
+      }
+    }
+    __syncthreads();
+    if (meta != nullptr) {
+      // word (k-step j, slot si): rows si & 7 (low half) and (si & 7) + 8 (high half) of the
+      // tile, 16-column segment 2 j + (si >> 3), i.e. code bytes of words 2 seg and 2 seg + 1
+      const int j = threadIdx.x >> 4, si = threadIdx.x & 15;
+      const int64_t kstep = w0 / 4 + j;
+      if (kstep < wpr / 4) {
+        const int lo_r = si & 7, seg = 2 * j + (si >> 3);
+        const uint32_t word = codes[lo_r][2 * seg] | ((uint32_t)codes[lo_r][2 * seg + 1] << 8) |
+                              ((uint32_t)codes[lo_r + 8][2 * seg] << 16) |
+                              ((uint32_t)codes[lo_r + 8][2 * seg + 1] << 24);
+        meta[kstep * nslots + row0 + si] = word;
+      }
+    }
+    __syncthreads();
+  }
 }
 
 // Decompression in the same lane-contiguous order and split: 8 bytes of kept
@@ -777,7 +889,16 @@ cudaError_t prune_dt(const PruneLaunch& a, cudaStream_t s) {
                      (W_out == nullptr || ((a.ld_out * es) % 16 == 0 && aligned16(W_out))) && aligned16(vals);
     const bool lanes = sizeof(T) == 2 && vec && a.colsL % 32 == 0 && a.ld == a.colsL &&
                        (W_out == nullptr || a.ld_out == a.colsL);
-    if (lanes) {
+    if (lanes && a.meta != nullptr && a.meta_tc) {
+      if constexpr (sizeof(T) == 2) {
+        const int64_t tiles = ((a.rowsL + 15) / 16) * ((a.colsL / 8 + 63) / 64);
+        const unsigned g = (unsigned)std::min<int64_t>(tiles, (int64_t)num_sms_cached() * 8);
+        prune24_tc_tile_kernel<DT><<<g, 256, 0, s>>>(
+            reinterpret_cast<const uint4*>(W), a.rowsL, a.colsL, a.ld / 8, reinterpret_cast<uint4*>(W_out),
+            a.ld_out / 8, reinterpret_cast<uint8_t*>(a.mask_bits), reinterpret_cast<uint2*>(vals),
+            static_cast<uint32_t*>(a.meta));
+      }
+    } else if (lanes) {
       if constexpr (sizeof(T) == 2) {
         const LaneSplit ls = lane_split(a.rowsL * a.colsL / 8);
         prune24_lanes_kernel<DT><<<ls.grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(W), a.rowsL, a.colsL, ls.per,
@@ -881,6 +1002,14 @@ cudaError_t check_dt(const void* W, int64_t rows, int64_t cols, int64_t ld, int 
   if (e != cudaSuccess) return e;
   const int64_t work = rows * (cols / m) + (transposable ? (rows / 4) * cols : 0);
   if (work == 0) return cudaSuccess;
+  if (sizeof(T) == 2 && n == 2 && m == 4 && cols % 8 == 0 && ld % 8 == 0 && aligned16(W) &&
+      (!transposable || rows % 4 == 0)) {
+    const int64_t wpr = cols / 8;
+    const LaneSplit ls = lane_split(((rows + 3) / 4) * wpr);
+    check24_strips_kernel<<<ls.grid, 256, 0, s>>>(static_cast<const uint4*>(W), rows, wpr, ld / 8, transposable,
+                                                   ls.per, d_violations);
+    return cudaGetLastError();
+  }
   check_kernel<DT><<<grid_for(work, 256), 256, 0, s>>>(static_cast<const T*>(W), rows, cols, ld, n, m, transposable,
                                                        d_violations);
   return cudaGetLastError();

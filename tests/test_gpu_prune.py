@@ -158,6 +158,19 @@ def test_check_matches_oracle(dtype, n, m, transposable):
         assert int(cnt.item()) == 0
 
 
+@pytest.mark.parametrize("rows,cols,ld,dtype,transposable", [(37, 48, 48, "f16", 0), (36, 40, 56, "bf16", 1),
+                                                            (4096, 4096, 4096, "f16", 1)])
+def test_check_strips_ragged_and_strided(rows, cols, ld, dtype, transposable):
+    a = host_matrix(rows, cols, dtype, seed=rows + cols, kind="special")
+    W, _ = with_ld(a, ld, dtype)
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for mat in (a, o.nm_prune(a, dtype, 2, 4)[0]):
+        Wm, _ = with_ld(mat, ld, dtype)
+        nb.nm_check(Wm, rows, cols, ld, dtype, 2, 4, transposable, cnt)
+        torch.cuda.synchronize()
+        assert int(cnt.item()) == o.nm_check(mat, dtype, 2, 4, transposable=bool(transposable))
+
+
 # ------------------------------------------------------------ transposable
 TRANS_CASES = [
     (256, 512, "f16", nb.NM_META_TC, "normal"),       # SparseLinear 512 -> 256
