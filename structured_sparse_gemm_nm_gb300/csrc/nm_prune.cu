@@ -816,6 +816,55 @@ __global__ void __launch_bounds__(256, 5) decompress24_lanes_kernel(const uint2*
   }
 }
 
+// Decompression with tensor-core metadata in the prune kernel's 16 x 512 tiles: each
+// thread reads one whole metadata word (a k-step's 16 slot words are one 64-byte
+// run) and leaves its four code bytes in shared memory, then thread (r, g) expands
+// words g, g + 16, g + 32, g + 48 of tile row r.
+template <int DT>
+__global__ void __launch_bounds__(256) decompress24_tc_tile_kernel(const uint2* __restrict__ vals,
+                                                                   const uint32_t* __restrict__ meta, int64_t rows,
+                                                                   int64_t cols, uint4* __restrict__ W_out,
+                                                                   int64_t ldw_out) {
+  __shared__ uint8_t codes[16][64];
+  const int64_t wpr = cols / 8;
+  const int64_t tiles_c = (wpr + 63) / 64, tiles = ((rows + 15) / 16) * tiles_c;
+  const int64_t nslots = ((rows + 127) / 128) * 128;
+  const int tr = threadIdx.x >> 4, g = threadIdx.x & 15;
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t row0 = (tile / tiles_c) * 16, w0 = (tile % tiles_c) * 64;
+    {
+      const int j = threadIdx.x >> 4, si = threadIdx.x & 15;
+      const int64_t kstep = w0 / 4 + j;
+      if (kstep < wpr / 4) {
+        const uint32_t word = __ldcs(meta + kstep * nslots + row0 + si);
+        const int lo_r = si & 7, seg = 2 * j + (si >> 3);
+        codes[lo_r][2 * seg] = (uint8_t)word;
+        codes[lo_r][2 * seg + 1] = (uint8_t)(word >> 8);
+        codes[lo_r + 8][2 * seg] = (uint8_t)(word >> 16);
+        codes[lo_r + 8][2 * seg + 1] = (uint8_t)(word >> 24);
+      }
+    }
+    __syncthreads();
+    const int64_t r = row0 + tr;
+    uint2 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t w = w0 + g + 16 * u;
+      v[u] = (r < rows && w < wpr) ? __ldcs(vals + r * wpr + w) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t w = w0 + g + 16 * u;
+      if (r >= rows || w >= wpr) continue;
+      const uint32_t c = codes[tr][g + 16 * u];
+      const uint32_t s0 = scatter_sel16(c & 0xFu), s1 = scatter_sel16((c >> 4) & 0xFu);
+      W_out[r * ldw_out + w] = make_uint4(__byte_perm(v[u].x, 0u, s0 & 0xFFFFu), __byte_perm(v[u].x, 0u, s0 >> 16),
+                                          __byte_perm(v[u].y, 0u, s1 & 0xFFFFu), __byte_perm(v[u].y, 0u, s1 >> 16));
+    }
+    __syncthreads();
+  }
+}
+
 // Decompression for aligned rows whose length is a multiple of 32: one thread
 // per 32 columns; the kept values and codes are loaded as words, each group's
 // four outputs come from byte permutes with a selector looked up by its code.
@@ -976,6 +1025,14 @@ cudaError_t decompress_dt(const DecompressLaunch& a, cudaStream_t s) {
         decompress24_lanes_kernel<DT><<<ls.grid, 256, 0, s>>>(reinterpret_cast<const uint2*>(vals),
                                                                static_cast<const uint8_t*>(a.meta), a.rows * a.cols / 8,
                                                                ls.per, reinterpret_cast<uint4*>(W_out));
+      }
+    } else if (pair && sizeof(T) == 2 && a.meta_tc && (reinterpret_cast<uintptr_t>(a.meta) & 3u) == 0) {
+      if constexpr (sizeof(T) == 2) {
+        const int64_t tiles = ((a.rows + 15) / 16) * ((a.cols / 8 + 63) / 64);
+        const unsigned g = (unsigned)std::min<int64_t>(tiles, (int64_t)num_sms_cached() * 8);
+        decompress24_tc_tile_kernel<DT><<<g, 256, 0, s>>>(reinterpret_cast<const uint2*>(vals),
+                                                           static_cast<const uint32_t*>(a.meta), a.rows, a.cols,
+                                                           reinterpret_cast<uint4*>(W_out), a.ld_out / 8);
       }
     } else if (pair) {
       const int64_t pairs = a.rows * (a.cols / 32);
