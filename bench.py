@@ -152,11 +152,14 @@ class GptNeoTrain:
                     metaT=torch.empty(mbT, dtype=torch.uint8, device=dev),
                     mask=torch.empty(out_f * ((in_f + 31) // 32), dtype=torch.int32, device=dev),
                     dW=torch.empty((out_f, in_f), dtype=tdt, device=dev),
+                    # outputs of the linear's own: work on different linears may overlap
+                    Y=torch.empty((T, out_f), dtype=tdt, device=dev),
+                    dX=torch.empty((T, in_f), dtype=tdt, device=dev),
                     prune_bytes=out_f * in_f * 2 + vb + mb + vbT + mbT + out_f * ((in_f + 31) // 32) * 4,
                 ))
             self.layers.append(lay)
-        self.Y = [torch.empty((T, o), dtype=tdt, device=dev) for (_, o, i) in self.linears]
-        self.dX = [torch.empty((T, i), dtype=tdt, device=dev) for (_, o, i) in self.linears]
+        self.s_prune = torch.cuda.Stream(device=dev)
+        self.s_dw = torch.cuda.Stream(device=dev)
         self.p_fwd, self.p_dx, self.p_dw, self.ws = [], [], [], []
         for (_, o, i) in self.linears:
             self.p_fwd.append(nb.nm_spmm_plan(nb.make_desc(M=o, N=T, K=i, ab_type="bf16", cd_type="bf16", ldb=i, ldd=o)))
@@ -176,42 +179,87 @@ class GptNeoTrain:
     def flops_per_step(self) -> float:
         return 3.0 * sum(self.gemm_flops(j) for j in range(len(self.linears))) * len(self.layers)
 
-    def enqueue_one(self, l: int, j: int) -> int:
-        """Launch one linear's work (layer l, linear j) on the current stream; returns the launch count."""
+    # one library call each; the return value is the number of kernels it launches
+    def prune_one(self, l: int, j: int) -> int:
         nb, L = self.nb, self.layers[l][j]
         o, i = L["out"], L["inp"]
         nb.nm_prune_transposable(L["W"], o, i, i, "bf16", None, 0, L["mask"], L["vals"], L["meta"], L["valsT"],
                                  L["metaT"], nb.NM_META_TC)
-        nb.nm_spmm(self.p_fwd[j], 1.0, L["vals"], L["meta"], L["X"], 0.0, None, self.Y[j])
-        nb.nm_spmm(self.p_dx[j], 1.0, L["valsT"], L["metaT"], L["dY"], 0.0, None, self.dX[j])
+        return 1
+
+    def fwd_one(self, l: int, j: int) -> int:
+        L = self.layers[l][j]
+        self.nb.nm_spmm(self.p_fwd[j], 1.0, L["vals"], L["meta"], L["X"], 0.0, None, L["Y"])
+        return 1
+
+    def dx_one(self, l: int, j: int) -> int:
+        L = self.layers[l][j]
+        self.nb.nm_spmm(self.p_dx[j], 1.0, L["valsT"], L["metaT"], L["dY"], 0.0, None, L["dX"])
+        return 1
+
+    def dw_one(self, l: int, j: int) -> int:
+        L = self.layers[l][j]
         ws, wsb = self.ws[j]
-        nb.nm_spmm(self.p_dw[j], 1.0, L["dY"], L["mask"], L["X"], 0.0, None, L["dW"], ws if wsb else None, wsb)
-        return 4
+        self.nb.nm_spmm(self.p_dw[j], 1.0, L["dY"], L["mask"], L["X"], 0.0, None, L["dW"], ws if wsb else None, wsb)
+        return 2 if wsb else 1  # the K-split product and its finalize
+
+    def enqueue_one(self, l: int, j: int) -> int:
+        """Launch one linear's work (layer l, linear j) on the current stream; returns the launch count."""
+        return self.prune_one(l, j) + self.fwd_one(l, j) + self.dx_one(l, j) + self.dw_one(l, j)
+
+    def enqueue_training_step(self) -> int:
+        """One training step on three streams, with the ordering a real one has: the
+        weights' run-time prune runs ahead on its own stream; the forward products run in
+        layer order, each after its weight's prune; the dX products run in reverse order
+        after them, and each linear's masked dW runs on a third stream once its dX has
+        been issued (its dY is known by then), beside the rest of the dX chain.  The
+        split-K workspace of a linear shape is shared by its dW launches, which stay in
+        order on their stream.  Returns the number of kernels launched."""
+        torch = self.torch
+        main = torch.cuda.current_stream()
+        self.s_prune.wait_stream(main)
+        self.s_dw.wait_stream(main)
+        n = 0
+        pruned = {}
+        with torch.cuda.stream(self.s_prune):
+            for l, lay in enumerate(self.layers):
+                for j in range(len(lay)):
+                    n += self.prune_one(l, j)
+                    e = torch.cuda.Event()
+                    e.record(self.s_prune)
+                    pruned[(l, j)] = e
+        for l, lay in enumerate(self.layers):
+            for j in range(len(lay)):
+                main.wait_event(pruned[(l, j)])
+                n += self.fwd_one(l, j)
+        for l in reversed(range(len(self.layers))):
+            for j in reversed(range(len(self.layers[l]))):
+                n += self.dx_one(l, j)
+                e = torch.cuda.Event()
+                e.record(main)
+                self.s_dw.wait_event(e)
+                with torch.cuda.stream(self.s_dw):
+                    n += self.dw_one(l, j)
+        main.wait_stream(self.s_prune)
+        main.wait_stream(self.s_dw)
+        return n
 
     def enqueue(self, parts=("prune", "fwd", "dx", "dw"), only=None) -> int:
         """Launch the step's work on the current stream; returns the number of kernels launched."""
         nb = self.nb
         n = 0
-        for lay in self.layers:
+        for l, lay in enumerate(self.layers):
             for j, L in enumerate(lay):
                 if only is not None and j != only:
                     continue
-                o, i = L["out"], L["inp"]
                 if "prune" in parts:
-                    nb.nm_prune_transposable(L["W"], o, i, i, "bf16", None, 0, L["mask"], L["vals"], L["meta"],
-                                             L["valsT"], L["metaT"], nb.NM_META_TC)
-                    n += 1
+                    n += self.prune_one(l, j)
                 if "fwd" in parts:
-                    nb.nm_spmm(self.p_fwd[j], 1.0, L["vals"], L["meta"], L["X"], 0.0, None, self.Y[j])
-                    n += 1
+                    n += self.fwd_one(l, j)
                 if "dx" in parts:
-                    nb.nm_spmm(self.p_dx[j], 1.0, L["valsT"], L["metaT"], L["dY"], 0.0, None, self.dX[j])
-                    n += 1
+                    n += self.dx_one(l, j)
                 if "dw" in parts:
-                    ws, wsb = self.ws[j]
-                    nb.nm_spmm(self.p_dw[j], 1.0, L["dY"], L["mask"], L["X"], 0.0, None, L["dW"], ws if wsb else None,
-                               wsb)
-                    n += 1
+                    n += self.dw_one(l, j)
         return n
 
 
@@ -323,8 +371,8 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
     for j, (name, o, i) in enumerate(wl.linears):
         L = L0[j]
         f = wl.gemm_flops(j)
-        t_fwd = time_launch(torch, lambda: nb.nm_spmm(wl.p_fwd[j], 1.0, L["vals"], L["meta"], L["X"], 0.0, None, wl.Y[j]), flush)
-        t_dx = time_launch(torch, lambda: nb.nm_spmm(wl.p_dx[j], 1.0, L["valsT"], L["metaT"], L["dY"], 0.0, None, wl.dX[j]), flush)
+        t_fwd = time_launch(torch, lambda: nb.nm_spmm(wl.p_fwd[j], 1.0, L["vals"], L["meta"], L["X"], 0.0, None, L["Y"]), flush)
+        t_dx = time_launch(torch, lambda: nb.nm_spmm(wl.p_dx[j], 1.0, L["valsT"], L["metaT"], L["dY"], 0.0, None, L["dX"]), flush)
         ws, wsb = wl.ws[j]
         t_dw = time_launch(torch, lambda: nb.nm_spmm(wl.p_dw[j], 1.0, L["dY"], L["mask"], L["X"], 0.0, None, L["dW"],
                                                      ws if wsb else None, wsb), flush)
@@ -341,7 +389,7 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
                                  "frac_dense_peak": f / t_dw / 1e9 / dense_peak}
         # the same forward product on paired CTAs (algo 1), for comparison with the default
         pp = nb.nm_spmm_plan(nb.make_desc(M=o, N=wl.T, K=i, ab_type="bf16", cd_type="bf16", ldb=i, ldd=o, algo=1))
-        t_pair = time_launch(torch, lambda: nb.nm_spmm(pp, 1.0, L["vals"], L["meta"], L["X"], 0.0, None, wl.Y[j]), flush)
+        t_pair = time_launch(torch, lambda: nb.nm_spmm(pp, 1.0, L["vals"], L["meta"], L["X"], 0.0, None, L["Y"]), flush)
         rows[f"S5_fwd_{name}_paired"] = {"shape_MNK": [o, wl.T, i], "ms": t_pair, "tflops": f / t_pair / 1e9,
                                          "frac_sparse_peak": f / t_pair / 1e9 / sparse_peak}
         pp.destroy()
@@ -588,7 +636,7 @@ def run_native(args):
     launches_per_step = [0]
 
     def step():
-        launches_per_step[0] = wl.enqueue()
+        launches_per_step[0] = wl.enqueue_training_step()
 
     g_step = capture(torch, step)
     sampler = ClockSampler(local)
@@ -737,7 +785,8 @@ def run_native(args):
             "config": {"workload": WORKLOAD, "global_tokens": inputs.GPTNEO_TOKENS * world,
                        "l2": "inputs larger than L2: 4.8 GB of distinct per-linear activations per step",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "graph": "one CUDA graph per step"},
+                       "graph": "one CUDA graph per step on three streams: run-time prune ahead, forward chain "
+                                "then dX chain, each dW beside the dX chain"},
             "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
             "gpu_launches": launches_per_step[0] * args.steps,
             "step_split_ms": {k: v["ms_per_step"] for k, v in classes.items()},
