@@ -520,6 +520,30 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
         rows[f"S5_bert_{Mb}x{Nb}x{Kb}_f16"] = {"ms": t, "tflops": f / t / 1e9, "frac_sparse_peak": f / t / 1e9 / sparse_peak,
                                                 "cublas_dense_tflops": f / tc / 1e9, "speedup_vs_cublas": tc / t}
         plan.destroy()
+    # the same shapes in int8 (INT32 accumulation), against torch's int8 matmul of the dense
+    # pruned weight where the installed build has one
+    for (Mb, Nb, Kb) in inputs.BERT_SHAPES:
+        Wi = inputs.uniform_int8((Mb, Kb), inputs.SEED_W + Mb).to(dev)
+        Xi = inputs.uniform_int8((Nb, Kb), inputs.SEED_X + Nb).to(dev)
+        vb, mb = nb.nm_compressed_size(Mb, Kb, "i8", 2, 4, nb.NM_META_CANONICAL)
+        vals = torch.empty(vb, dtype=torch.uint8, device=dev)
+        meta = torch.empty(mb, dtype=torch.uint8, device=dev)
+        nb.nm_compress(Wi, Mb, Kb, Kb, "i8", 2, 4, 0, nb.NM_META_CANONICAL, vals, meta)
+        Di = torch.empty((Nb, Mb), dtype=torch.int32, device=dev)
+        plan = nb.nm_spmm_plan(nb.make_desc(M=Mb, N=Nb, K=Kb, ab_type="i8", cd_type="i32", ldb=Kb, ldd=Mb,
+                                            meta_layout=nb.NM_META_CANONICAL))
+        t = time_launch(torch, lambda: nb.nm_spmm(plan, 1, vals, meta, Xi, 0, None, Di), flush)
+        f = 2.0 * Mb * Nb * Kb
+        row = {"ms": t, "tops": f / t / 1e9, "kernel": "spmm_i8_kernel (warp-level mma.sp m16n8k64)"}
+        try:
+            WiT = Wi.t().contiguous()
+            tq = time_launch(torch, lambda: torch._int_mm(Xi, WiT), flush)
+            row["torch_int8_dense_tops"] = f / tq / 1e9
+            row["speedup_vs_dense_int8"] = tq / t
+        except Exception as e:  # no int8 matmul in this build
+            row["torch_int8_dense"] = f"unavailable: {type(e).__name__}"
+        rows[f"S5_bert_{Mb}x{Nb}x{Kb}_i8"] = row
+        plan.destroy()
     rows["_peaks"] = {"sparse_tflops": sparse_peak, "dense_tflops": dense_peak, "hbm_gbs": hbm,
                       "note": "tensor rows: one launch after an L2 flush, burst peaks; HBM rows: back-to-back "
                               "launches over copies larger than L2 (ms), and one flushed launch (ms_single)"}
