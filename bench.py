@@ -520,6 +520,25 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
         rows[f"S5_bert_{Mb}x{Nb}x{Kb}_f16"] = {"ms": t, "tflops": f / t / 1e9, "frac_sparse_peak": f / t / 1e9 / sparse_peak,
                                                 "cublas_dense_tflops": f / tc / 1e9, "speedup_vs_cublas": tc / t}
         plan.destroy()
+    # the BERT-Large layers of the cuSPARSELt blog's Table 1 (fp16, the same TN layout; the
+    # page's numbers are A100 context: dense / sparse TFLOPS 188/263, 183/242, 196/270, 211/339)
+    for lname, (Mb, Nb, Kb) in (("qkv", (3072, 16384, 1024)), ("proj", (1024, 16384, 1024)),
+                                ("fc1", (4096, 16384, 1024)), ("fc2", (1024, 16384, 4096))):
+        Wb = inputs.normal((Mb, Kb), 0.02, inputs.SEED_W, "f16", device=dev)
+        Xb = inputs.normal((Nb, Kb), 1.0, inputs.SEED_X, "f16", device=dev)
+        vb, mb = nb.nm_compressed_size(Mb, Kb, "f16", 2, 4, nb.NM_META_TC)
+        vals = torch.empty(vb, dtype=torch.uint8, device=dev)
+        meta = torch.empty(mb, dtype=torch.uint8, device=dev)
+        nb.nm_compress(Wb, Mb, Kb, Kb, "f16", 2, 4, 0, nb.NM_META_TC, vals, meta)
+        D = torch.empty((Nb, Mb), dtype=torch.float16, device=dev)
+        plan = nb.nm_spmm_plan(nb.make_desc(M=Mb, N=Nb, K=Kb, ab_type="f16", cd_type="f16", ldb=Kb, ldd=Mb))
+        t = time_launch(torch, lambda: nb.nm_spmm(plan, 1.0, vals, meta, Xb, 0.0, None, D), flush)
+        tc = time_launch(torch, lambda: torch.matmul(Xb, Wb.t()), flush)
+        f = 2.0 * Mb * Nb * Kb
+        rows[f"S5_bert_large_{lname}_{Mb}x{Nb}x{Kb}_f16"] = {
+            "ms": t, "tflops": f / t / 1e9, "frac_sparse_peak": f / t / 1e9 / sparse_peak,
+            "cublas_dense_tflops": f / tc / 1e9, "speedup_vs_cublas": tc / t}
+        plan.destroy()
     # the same shapes in int8 (INT32 accumulation), against torch's int8 matmul of the dense
     # pruned weight where the installed build has one
     for (Mb, Nb, Kb) in inputs.BERT_SHAPES:
