@@ -26,6 +26,7 @@
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <cstring>
 
 #include "nm_device.cuh"
 #include "nm_internal.h"
@@ -36,6 +37,7 @@ namespace {
 constexpr int kUnitW = 32;         // unit width (columns) of both kinds
 constexpr int kBins = 4096;        // log-scale buckets
 constexpr int kChunk = 256;        // units per CTA in the count and write kernels
+constexpr int kCountChunks = 8;    // chunks per CTA of the count kernel (one group)
 constexpr uint64_t kKeyInf = 1ull << 62;
 
 struct Ctl {
@@ -53,67 +55,110 @@ constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct WsLayout {
   size_t hist, ctl, keys, cand, cnt_gt, cnt_eq, total;
 };
-WsLayout ws_layout(int64_t units) {
+// cnt_gt / cnt_eq: one entry per chunk (the prefix within its group) followed by one
+// per group of kCountChunks chunks (the group's prefix).
+constexpr WsLayout ws_layout(int64_t units) {
   const int64_t chunks = (units + kChunk - 1) / kChunk;
+  const int64_t groups = (chunks + kCountChunks - 1) / kCountChunks;
   WsLayout w{};
   w.hist = 0;
   w.ctl = align256(kBins * 4);
   w.keys = w.ctl + align256(sizeof(Ctl));
   w.cand = w.keys + align256((size_t)units * 8);
   w.cnt_gt = w.cand + align256((size_t)units * 8);
-  w.cnt_eq = w.cnt_gt + align256((size_t)chunks * 4);
-  w.total = w.cnt_eq + align256((size_t)chunks * 4);
+  w.cnt_eq = w.cnt_gt + align256((size_t)(chunks + groups) * 4);
+  w.total = w.cnt_eq + align256((size_t)(chunks + groups) * 4);
   return w;
 }
 
 // ---------------------------------------------------------------- scoring
-// Flags: 1 NaN, 2 +Inf, 4 -Inf.  A finite f16 in units of 2^-24: (1024 + mantissa)
-// << (e - 1) for normal numbers, the mantissa for subnormals.
-__device__ __forceinline__ void acc_f16(uint32_t h, int64_t& s, int64_t& a, uint32_t& fl) {
-  const uint32_t e = (h >> 10) & 31u, mnt = h & 1023u;
-  if (e == 31u) {
-    fl |= mnt ? 1u : ((h & 0x8000u) ? 4u : 2u);
-    return;
-  }
-  const int64_t u = e ? (int64_t)(1024u + mnt) << (e - 1) : (int64_t)mnt;
-  s += (h & 0x8000u) ? -u : u;
-  a += u;
-}
+// Exact scores: the sum of a unit's elements (SIGNED) or of their magnitudes, in units
+// of 2^-24 for f16.
+//
+// f16, in fp32 on the FMA pipe: an f16 x converts exactly; adding and then subtracting
+// C = 1.5 * 2^20 rounds it to hi, the nearest multiple of 2^-3 (x + C stays inside
+// [2^20, 2^21), whose spacing is 2^-3), and lo = x - hi is exact, a multiple of 2^-24
+// of magnitude at most 2^-4.  The hi parts of up to 32 elements sum exactly in fp32
+// (below 32 * 65504 * 8 < 2^24 units of 2^-3); the lo parts of one 8-element segment
+// sum exactly (within 2^23 units of 2^-24) and go to a 32-bit integer sum.  The score
+// is hi_sum * 2^21 + lo_int.  (The integer form of the same split, shift-and-add per
+// element, spent twice the issue slots on the half-rate integer pipe.)  An Inf or NaN
+// makes hi_sum non-finite; seg_flags then classifies the unit.
+//
+// int8: a dp4a with ones sums four elements; for magnitudes each byte is multiplied by
+// its sign (+1 or -1 per byte, no carry between bytes).
+struct ScoreAcc {
+  float hs = 0.f;   // f16: exact sum of the hi parts (at most 32 elements)
+  int32_t li = 0;   // f16: sum of the lo parts in units of 2^-24; int8: the sum itself
+};
 
-// Score contributions of one 16-byte segment (8 f16 or 16 int8 elements).
-template <int DT>
-__device__ __forceinline__ void acc_seg(const uint4 v, int64_t& s, int64_t& a, uint32_t& fl) {
+template <int DT, bool SIGNED>
+__device__ __forceinline__ void acc_seg(const uint4 v, ScoreAcc& a) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   if constexpr (DT == kF16) {
+    constexpr float C = 1572864.0f;  // 1.5 * 2^20
+    float ls = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      acc_f16(w[i] & 0xFFFFu, s, a, fl);
-      acc_f16(w[i] >> 16, s, a, fl);
-    }
-  } else {
-    int si = 0, ai = 0;
+      __half2 hh;
+      memcpy(&hh, &w[i], 4);
+      const float2 f2 = __half22float2(hh);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int x = (int)(int8_t)(w[i] >> (8 * b));
-        si += x;
-        ai += x < 0 ? -x : x;
+      for (int j = 0; j < 2; ++j) {
+        const float x = SIGNED ? (j ? f2.y : f2.x) : fabsf(j ? f2.y : f2.x);
+        const float hi = __fsub_rn(__fadd_rn(x, C), C);
+        a.hs = __fadd_rn(a.hs, hi);
+        ls = __fadd_rn(ls, __fsub_rn(x, hi));
       }
-    s += si;
-    a += ai;
+    }
+    a.li += __float2int_rn(ls * 16777216.0f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (SIGNED) {
+        a.li = __dp4a((int)w[i], 0x01010101, a.li);
+      } else {
+        const uint32_t neg = (w[i] >> 7) & 0x01010101u;  // 1 in each negative byte
+        a.li = __dp4a((int)w[i], (int)(0x01010101u + neg * 0xFEu), a.li);
+      }
+    }
   }
 }
 
-__device__ __forceinline__ uint64_t make_key(int64_t s, int64_t a, uint32_t fl, int abs_of_sum) {
-  if (abs_of_sum) {
+// The accumulated score; `special` is set when an f16 Inf or NaN took part.
+template <int DT>
+__device__ __forceinline__ int64_t acc_value(const ScoreAcc& a, bool& special) {
+  if constexpr (DT == kF16) {
+    special = !(fabsf(a.hs) <= 3.0e38f);
+    return (int64_t)__float2int_rn(a.hs * 8.0f) * (1 << 21) + a.li;
+  } else {
+    special = false;
+    return a.li;
+  }
+}
+
+// Flags of the f16 specials in a segment: 1 NaN, 2 +Inf, 4 -Inf.
+__device__ __forceinline__ uint32_t seg_flags(const uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t fl = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t h = (i & 1) ? w[i >> 1] >> 16 : w[i >> 1] & 0xFFFFu;
+    if ((h & 0x7C00u) == 0x7C00u) fl |= (h & 0x3FFu) ? 1u : ((h & 0x8000u) ? 4u : 2u);
+  }
+  return fl;
+}
+
+template <bool SIGNED>
+__device__ __forceinline__ uint64_t make_key(int64_t x, uint32_t fl) {
+  if (SIGNED) {
     if ((fl & 1u) || (fl & 6u) == 6u) return 0;
     if (fl) return kKeyInf;
-    return (uint64_t)(s < 0 ? -s : s) + 1;
+    return (uint64_t)(x < 0 ? -x : x) + 1;
   }
   if (fl & 1u) return 0;
   if (fl) return kKeyInf;
-  return (uint64_t)a + 1;
+  return (uint64_t)x + 1;
 }
 
 // Monotone log-scale bucket: keys below 128 are their own bucket; above, the
@@ -142,88 +187,129 @@ __device__ __forceinline__ bool last_cta(uint32_t* ticket) {
   return is_last;
 }
 
-// Run by the last score CTA: the bucket that holds the keep-th largest key.
-__device__ void select_bucket(const uint32_t* hist, Ctl* ctl, uint64_t keep) {
-  __shared__ uint64_t part[256];
-  const int t = threadIdx.x;  // 256 threads, 16 bins each, highest bins first
-  constexpr int per = kBins / 256;
-  const int top = kBins - per * t;  // bins [top - per, top)
-  uint64_t sum = 0;
-  for (int b = top - per; b < top; ++b) sum += __ldcg(hist + b);
-  part[t] = sum;
+// Inclusive prefix sum over the 256 threads of a CTA (one value each, thread order);
+// `total` receives the sum over the CTA.  Every thread must call it.
+template <typename T>
+__device__ __forceinline__ T cta_inclusive_scan256(T v, T& total) {
+  __shared__ T wsum[8];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T u = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) wsum[w] = v;
   __syncthreads();
-  if (t == 0) {
-    if (keep == 0) {
+  T add = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    add += i < w ? wsum[i] : T(0);
+    tot += wsum[i];
+  }
+  __syncthreads();  // wsum is free again on return
+  total = tot;
+  return v + add;
+}
+
+// Run by the last score CTA: the bucket that holds the keep-th largest key.  Thread t
+// holds 16 bins, highest bins first over t; a prefix sum over the threads finds the one
+// whose bins hold the keep-th key, and that thread walks its bins.
+__device__ void select_bucket(const uint32_t* hist, Ctl* ctl, uint64_t keep) {
+  constexpr int per = kBins / 256;
+  const int top = kBins - per * (int)threadIdx.x;  // bins [top - per, top)
+  uint32_t c[per];
+  unsigned long long sum = 0, total;
+#pragma unroll
+  for (int j = 0; j < per; ++j) {
+    c[j] = __ldcg(hist + top - 1 - j);
+    sum += c[j];
+  }
+  const unsigned long long incl = cta_inclusive_scan256<unsigned long long>(sum, total);
+  const unsigned long long excl = incl - sum;
+  if (keep == 0) {
+    if (threadIdx.x == 0) {
       ctl->bucket = -1;
       ctl->T = ~0ull;
       ctl->need_eq = 0;
-    } else {
-      uint64_t above = 0;
-      int tt = 0;
-      while (above + part[tt] < keep) above += part[tt++];
-      int b = kBins - per * tt - 1;
-      for (;; --b) {
-        const uint64_t h = __ldcg(hist + b);
-        if (above + h >= keep) break;
-        above += h;
-      }
-      const uint64_t k_rem = keep - above;
-      if (b < 128) {  // a single key value
-        ctl->bucket = -1;
-        ctl->T = (uint64_t)b;
-        ctl->need_eq = k_rem;
+    }
+    return;
+  }
+  if (!(excl < keep && keep <= incl)) return;  // exactly one thread goes on (keep <= units)
+  uint64_t above = excl, k_rem = 0;
+  int b = -1;
+#pragma unroll
+  for (int j = 0; j < per; ++j) {
+    if (b < 0) {
+      if (above + c[j] >= keep) {
+        b = top - 1 - j;
+        k_rem = keep - above;
       } else {
-        ctl->bucket = b;
-        ctl->k_rem = k_rem;
+        above += c[j];
       }
     }
   }
+  if (b < 128) {  // a single key value
+    ctl->bucket = -1;
+    ctl->T = (uint64_t)b;
+    ctl->need_eq = k_rem;
+  } else {
+    ctl->bucket = b;
+    ctl->k_rem = k_rem;
+  }
 }
 
-// Vector-wise keys: a thread scores one 16-byte segment; the segments of a
-// vector sit in consecutive lanes.
-template <int DT>
+// Vector-wise keys: a thread scores whole vectors (64 or 32 bytes, loaded as 16-byte
+// segments), two at a time; no cross-lane reduction.
+template <int DT, bool SIGNED>
 __global__ void __launch_bounds__(256) vw_score_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_t cols,
-                                                       int64_t ld_bytes, int abs_of_sum, uint64_t* __restrict__ keys,
+                                                       int64_t ld_bytes, uint64_t* __restrict__ keys,
                                                        uint32_t* __restrict__ hist, Ctl* ctl, uint64_t keep) {
   constexpr int kSegElems = DT == kF16 ? 8 : 16;
   constexpr int kSpv = kUnitW / kSegElems;  // segments per vector: 4 (f16) or 2 (int8)
+  constexpr int kVecBytes = kSpv * 16;
+  constexpr int kVecs = 2;  // vectors in flight per thread
   __shared__ uint32_t sh[kBins];
   for (int i = threadIdx.x; i < kBins; i += blockDim.x) sh[i] = 0;
   __syncthreads();
-  const int64_t spr = cols / kSegElems;
-  const int64_t total = rows * spr;
+  const int64_t vpr = cols / kUnitW;  // vectors per row
+  const int64_t units = rows * vpr;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int lane = threadIdx.x & 31;
-  for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x; g0 < total; g0 += 2 * stride) {
-    uint4 v[2];
-    bool ok[2];
+  // Row and column of the thread's next vector, stepped by `stride` (one division per
+  // thread, not one per vector).
+  const int64_t u_first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t r = u_first / vpr, c = u_first - r * vpr;
+  const int64_t dr = stride / vpr, dc = stride - dr * vpr;
+  for (int64_t u0 = (int64_t)blockIdx.x * blockDim.x; u0 < units; u0 += kVecs * stride) {
+    uint4 v[kVecs][kSpv];
+    bool ok[kVecs];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int64_t g = g0 + j * stride + threadIdx.x;
-      ok[j] = g < total;
-      if (ok[j]) {
-        const int64_t r = g / spr, s = g - r * spr;
-        v[j] = __ldcs(reinterpret_cast<const uint4*>(W + r * ld_bytes + s * 16));
-      } else {
-        v[j] = make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < kVecs; ++j) {
+      ok[j] = u0 + j * stride + threadIdx.x < units;
+      const uint4* p = reinterpret_cast<const uint4*>(W + r * ld_bytes + c * kVecBytes);
+#pragma unroll
+      for (int q = 0; q < kSpv; ++q) v[j][q] = ok[j] ? __ldcs(p + q) : make_uint4(0, 0, 0, 0);
+      c += dc;
+      r += dr;
+      if (c >= vpr) {
+        c -= vpr;
+        ++r;
       }
     }
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      int64_t s = 0, a = 0;
-      uint32_t fl = 0;
-      acc_seg<DT>(v[j], s, a, fl);
+    for (int j = 0; j < kVecs; ++j) {
+      ScoreAcc a;
 #pragma unroll
-      for (int m = 1; m < kSpv; m <<= 1) {
-        s += shfl_xor64(s, m);
-        a += shfl_xor64(a, m);
-        fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, m);
+      for (int q = 0; q < kSpv; ++q) acc_seg<DT, SIGNED>(v[j][q], a);
+      bool sp;
+      const int64_t x = acc_value<DT>(a, sp);
+      uint32_t fl = 0;
+      if (sp) {  // an Inf or NaN in the vector (rare)
+#pragma unroll
+        for (int q = 0; q < kSpv; ++q) fl |= seg_flags(v[j][q]);
       }
-      const int64_t g = g0 + j * stride + threadIdx.x;
-      if (ok[j] && (lane % kSpv) == 0) {
-        const uint64_t key = make_key(s, a, fl, abs_of_sum);
-        keys[g / kSpv] = key;
+      if (ok[j]) {
+        const uint64_t key = make_key<SIGNED>(x, fl);
+        keys[u0 + j * stride + threadIdx.x] = key;
         atomicAdd(&sh[key_bucket(key)], 1u);
       }
     }
@@ -255,17 +341,22 @@ __global__ void __launch_bounds__(256) bw_score_kernel(const uint8_t* __restrict
     uint4 v[32 / kRowsPer];
 #pragma unroll
     for (int p = 0; p < 32 / kRowsPer; ++p) v[p] = __ldcs(reinterpret_cast<const uint4*>(base + p * kRowsPer * ld_bytes));
-    int64_t s = 0, a = 0;
+    ScoreAcc acc;  // a lane's 32 elements (f16) or 32 int8 elements
+#pragma unroll
+    for (int p = 0; p < 32 / kRowsPer; ++p) acc_seg<DT, false>(v[p], acc);
+    bool sp;
+    int64_t a = acc_value<DT>(acc, sp);
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) a += shfl_xor64(a, m);
     uint32_t fl = 0;
+    if (__any_sync(0xFFFFFFFFu, sp)) {  // an Inf or NaN in the block (rare)
 #pragma unroll
-    for (int p = 0; p < 32 / kRowsPer; ++p) acc_seg<DT>(v[p], s, a, fl);
+      for (int p = 0; p < 32 / kRowsPer; ++p) fl |= seg_flags(v[p]);
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-      a += shfl_xor64(a, m);
-      fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, m);
+      for (int m = 1; m < 32; m <<= 1) fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, m);
     }
     if (lane == 0) {
-      const uint64_t key = make_key(0, a, fl, 0);
+      const uint64_t key = make_key<false>(a, fl);
       keys[u] = key;
       atomicAdd(&sh[key_bucket(key)], 1u);
     }
@@ -281,21 +372,50 @@ __global__ void __launch_bounds__(256) candidates_kernel(const uint64_t* __restr
                                                          uint64_t* __restrict__ cand) {
   const int B = ctl->bucket;
   if (B < 0) return;  // T already final (uniform across the grid)
+  // A CTA gathers its candidates in shared memory and claims room for them in the global
+  // array with one atomic (a global atomic per warp serialised thousands of same-address
+  // updates); past the shared buffer's capacity each candidate claims its own slot.
+  constexpr int kCap = 4096;  // also holds all candidates for the radix search when they fit
+  __shared__ uint64_t sc[kCap];
+  __shared__ uint32_t scount, sbase;
+  if (threadIdx.x == 0) scount = 0;
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); i0 < units; i0 += stride) {
-    const int64_t i = i0 + lane;
-    const uint64_t key = i < units ? keys[i] : 0;
-    const bool c = i < units && key_bucket(key) == B;
-    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, c);
-    if (bal) {
-      const int leader = __ffs(bal) - 1;
-      uint32_t base = 0;
-      if (lane == leader) base = atomicAdd(&ctl->cand_count, (uint32_t)__popc(bal));
-      base = __shfl_sync(0xFFFFFFFFu, base, leader);
-      if (c) cand[base + __popc(bal & ((1u << lane) - 1u))] = key;
+  constexpr int kLoads = 4;  // keys in flight per thread
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); i0 < units; i0 += kLoads * stride) {
+    uint64_t k4[kLoads];
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+      const int64_t i = i0 + q * stride + lane;
+      k4[q] = i < units ? keys[i] : 0;
+    }
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+      const int64_t i = i0 + q * stride + lane;
+      const uint64_t key = k4[q];
+      const bool c = i < units && key_bucket(key) == B;
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, c);
+      if (bal) {
+        const int leader = __ffs(bal) - 1;
+        uint32_t base = 0;
+        if (lane == leader) base = atomicAdd(&scount, (uint32_t)__popc(bal));
+        base = __shfl_sync(0xFFFFFFFFu, base, leader);
+        const uint32_t at = base + __popc(bal & ((1u << lane) - 1u));
+        if (c) {
+          if (at < kCap)
+            sc[at] = key;
+          else
+            cand[atomicAdd(&ctl->cand_count, 1u)] = key;
+        }
+      }
     }
   }
+  __syncthreads();
+  const uint32_t mine = scount < kCap ? scount : kCap;
+  if (threadIdx.x == 0) sbase = mine ? atomicAdd(&ctl->cand_count, mine) : 0u;
+  __syncthreads();
+  for (uint32_t t = threadIdx.x; t < mine; t += blockDim.x) cand[sbase + t] = sc[t];
   if (!last_cta(&ctl->ticket[1])) return;
   // Radix search, 8 bits at a time, over the bits the bucket leaves open.
   __shared__ uint32_t h[256];
@@ -307,21 +427,52 @@ __global__ void __launch_bounds__(256) candidates_kernel(const uint64_t* __restr
     s_prefix = (uint64_t)(64 + (B & 63)) << (lead - 6);
     s_k = __ldcg(&ctl->k_rem);
   }
+  // The passes read the candidates from shared memory when they fit (one global read).
+  const bool staged = n <= (uint32_t)kCap;
+  if (staged) {
+    uint32_t i = threadIdx.x;
+    for (; i + 3 * 256 < n; i += 4 * 256) {
+      uint64_t k4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) k4[q] = __ldcg(cand + i + q * 256);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sc[i + q * 256] = k4[q];
+    }
+    for (; i < n; i += 256) sc[i] = __ldcg(cand + i);
+  }
   for (int shift = (hi_bit / 8) * 8; shift >= 0; shift -= 8) {
     h[threadIdx.x] = 0;
     __syncthreads();
     const uint64_t want = s_prefix >> (shift + 8);
-    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+    uint32_t i = threadIdx.x;
+    if (staged) {
+      for (; i < n; i += 256) {
+        const uint64_t key = sc[i];
+        if ((key >> (shift + 8)) == want) atomicAdd(&h[(key >> shift) & 255], 1u);
+      }
+    }
+    for (; i + 3 * 256 < n; i += 4 * 256) {  // four loads in flight per thread
+      uint64_t k4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) k4[q] = __ldcg(cand + i + q * 256);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if ((k4[q] >> (shift + 8)) == want) atomicAdd(&h[(k4[q] >> shift) & 255], 1u);
+    }
+    for (; i < n; i += 256) {
       const uint64_t key = __ldcg(cand + i);
       if ((key >> (shift + 8)) == want) atomicAdd(&h[(key >> shift) & 255], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      uint64_t k = s_k, above = 0;
-      int d = 255;
-      while (above + h[d] < k) above += h[d--];
-      s_k = k - above;
-      s_prefix = (s_prefix & ~(255ull << shift)) | ((uint64_t)d << shift);
+    // Digit of the k-th largest: thread t holds digit 255 - t, prefix over threads.
+    const uint32_t cnt = h[255 - threadIdx.x];
+    uint32_t tot;
+    const uint32_t incl = cta_inclusive_scan256<uint32_t>(cnt, tot);
+    const uint64_t k = s_k;
+    __syncthreads();
+    if ((uint64_t)(incl - cnt) < k && k <= (uint64_t)incl) {
+      s_k = k - (incl - cnt);
+      s_prefix = (s_prefix & ~(255ull << shift)) | ((uint64_t)(255 - threadIdx.x) << shift);
     }
     __syncthreads();
   }
@@ -334,43 +485,65 @@ __global__ void __launch_bounds__(256) candidates_kernel(const uint64_t* __restr
 // ---------------------------------------------------------------- ordering
 // In-place exclusive prefix of a[0..n) by one CTA of 256 threads.
 __device__ void cta_exclusive_scan(uint32_t* a, int64_t n) {
-  __shared__ uint32_t part[256];
-  const int t = threadIdx.x;
-  const int64_t per = (n + 255) / 256;
-  const int64_t lo = t * per, hi = lo + per < n ? lo + per : n;
-  uint32_t s = 0;
-  for (int64_t i = lo; i < hi; ++i) s += __ldcg(a + i);
-  part[t] = s;
-  __syncthreads();
-  for (int off = 1; off < 256; off <<= 1) {
-    const uint32_t v = t >= off ? part[t - off] : 0u;
-    __syncthreads();
-    part[t] += v;
-    __syncthreads();
-  }
-  uint32_t run = part[t] - s;
-  for (int64_t i = lo; i < hi; ++i) {
-    const uint32_t c = __ldcg(a + i);
-    a[i] = run;
-    run += c;
+  constexpr int kPer = 8;  // a thread takes kPer consecutive entries of a 2048-entry tile
+  uint32_t carry = 0;
+  for (int64_t base = 0; base < n; base += 256 * kPer) {
+    const int64_t first = base + (int64_t)threadIdx.x * kPer;
+    uint32_t v[kPer], s = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      v[j] = first + j < n ? __ldcg(a + first + j) : 0u;
+      s += v[j];
+    }
+    uint32_t tile;
+    uint32_t run = carry + cta_inclusive_scan256<uint32_t>(s, tile) - s;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (first + j < n) a[first + j] = run;
+      run += v[j];
+    }
+    carry += tile;
   }
 }
 
+// Counts of keys above and at the threshold per chunk of kChunk keys.  A CTA takes one
+// group of kCountChunks chunks and writes each chunk's prefix within the group and the
+// group's totals; the last CTA turns the group totals into prefixes, so its scan covers
+// groups, not chunks.
 __global__ void __launch_bounds__(kChunk) count_kernel(const uint64_t* __restrict__ keys, int64_t units, Ctl* ctl,
                                                        uint32_t* __restrict__ cnt_gt, uint32_t* __restrict__ cnt_eq) {
   const uint64_t T = ctl->T;
-  const int64_t i = (int64_t)blockIdx.x * kChunk + threadIdx.x;
-  const uint64_t key = i < units ? keys[i] : 0;
-  const int gt = __syncthreads_count(i < units && key > T);
-  const int eq = __syncthreads_count(i < units && key == T);
+  const int64_t chunks = (units + kChunk - 1) / kChunk;
+  const int64_t groups = (chunks + kCountChunks - 1) / kCountChunks;
+  uint64_t key[kCountChunks];
+#pragma unroll
+  for (int q = 0; q < kCountChunks; ++q) {  // every load in flight before the counts
+    const int64_t i = ((int64_t)blockIdx.x * kCountChunks + q) * kChunk + threadIdx.x;
+    key[q] = i < units ? keys[i] : 0;
+  }
+  uint32_t run_gt = 0, run_eq = 0;
+#pragma unroll
+  for (int q = 0; q < kCountChunks; ++q) {
+    const int64_t chunk = (int64_t)blockIdx.x * kCountChunks + q;
+    if (chunk >= chunks) break;  // uniform across the CTA
+    const bool in = chunk * kChunk + threadIdx.x < units;
+    const int gt = __syncthreads_count(in && key[q] > T);
+    const int eq = __syncthreads_count(in && key[q] == T);
+    if (threadIdx.x == 0) {
+      cnt_gt[chunk] = run_gt;
+      cnt_eq[chunk] = run_eq;
+    }
+    run_gt += (uint32_t)gt;
+    run_eq += (uint32_t)eq;
+  }
   if (threadIdx.x == 0) {
-    cnt_gt[blockIdx.x] = (uint32_t)gt;
-    cnt_eq[blockIdx.x] = (uint32_t)eq;
+    cnt_gt[chunks + blockIdx.x] = run_gt;
+    cnt_eq[chunks + blockIdx.x] = run_eq;
   }
   if (!last_cta(&ctl->ticket[2])) return;
-  cta_exclusive_scan(cnt_gt, gridDim.x);
+  cta_exclusive_scan(cnt_gt + chunks, groups);
   __syncthreads();
-  cta_exclusive_scan(cnt_eq, gridDim.x);
+  cta_exclusive_scan(cnt_eq + chunks, groups);
 }
 
 // Exclusive prefix of a per-thread flag over the CTA (kChunk threads).
@@ -406,20 +579,34 @@ __global__ void __launch_bounds__(kChunk) write_kernel(const uint8_t* __restrict
   const bool valid = i < units;
   const uint64_t key = valid ? keys[i] : 0;
   const bool gt = valid && key > T, eq = valid && key == T;
-  const uint64_t eq0 = pre_eq[blockIdx.x], gt0 = pre_gt[blockIdx.x];
+  const int64_t chunks = gridDim.x, grp = chunks + blockIdx.x / kCountChunks;
+  const uint64_t eq0 = pre_eq[blockIdx.x] + pre_eq[grp], gt0 = pre_gt[blockIdx.x] + pre_gt[grp];
   const uint64_t eq_rank = eq0 + cta_rank(eq, warp_tot);
   const bool kept = gt || (eq && eq_rank < need_eq);
   const uint64_t before = gt0 + (eq0 < need_eq ? eq0 : need_eq);
   const int64_t pos = (int64_t)(before + cta_rank(kept, warp_tot));
+  // Unit row and column of unit (warp's first unit) + k, 0 <= k < 32, from one
+  // division per thread (a 64-bit division per segment dominated the issue slots).
+  const int lane = threadIdx.x & 31;
+  const int64_t r0 = (i - lane) / upr, c0 = (i - lane) - r0 * upr;
+  auto unit_at = [&](int k, int64_t& r, int64_t& c) {
+    r = r0;
+    c = c0 + k;
+    if (c >= upr) {
+      const uint32_t q = (uint32_t)c / (uint32_t)upr;  // c < upr + 32
+      r += q;
+      c -= (int64_t)q * upr;
+    }
+  };
   if (csr != nullptr && valid) {
-    const int64_t ur = i / upr, uc = i - ur * upr;
+    int64_t ur, uc;
+    unit_at(lane, ur, uc);
     if (uc == 0) csr[ur] = (int32_t)pos;
     if (i == units - 1) csr[urows] = (int32_t)(pos + (kept ? 1 : 0));
     if (kept) csr[urows + 1 + pos] = (int32_t)uc;
   }
   // Data movement: each warp handles its 32 units, 16-byte segments spread
   // over the lanes.
-  const int lane = threadIdx.x & 31;
   if (mask != nullptr) {
     const int64_t mw = cols / 32;  // mask words per row
     if (!BLOCK) {
@@ -429,28 +616,42 @@ __global__ void __launch_bounds__(kChunk) write_kernel(const uint8_t* __restrict
         const int64_t u = i - lane + k;
         const bool kv = __shfl_sync(0xFFFFFFFFu, kept, k);
         if (u < units) {
-          const int64_t bi = u / upr, bj = u - bi * upr;
+          int64_t bi, bj;
+          unit_at(k, bi, bj);
           mask[(bi * 32 + lane) * mw + bj] = kv ? 0xFFFFFFFFu : 0u;
         }
       }
     }
   }
   if (W_out == nullptr && vals == nullptr) return;
-  if (!BLOCK) {
+  if constexpr (!BLOCK) {
+    // Every load is issued before the first store (W_out may alias W, which would
+    // otherwise order each load after the previous store).  A thread reads and writes
+    // the same addresses, so an in-place call stays correct.
+    uint4 v[kSpu];
+    bool kv[kSpu], in[kSpu];
+    int64_t kp[kSpu], off_w[kSpu], off_o[kSpu];
 #pragma unroll
     for (int it = 0; it < kSpu; ++it) {
       const int g = it * 32 + lane;
       const int k = g / kSpu, part = g % kSpu;
-      const bool kv = __shfl_sync(0xFFFFFFFFu, kept, k);
-      const int64_t kp = (int64_t)__shfl_sync(0xFFFFFFFFu, (long long)pos, k);
+      kv[it] = __shfl_sync(0xFFFFFFFFu, kept, k);
+      kp[it] = (int64_t)__shfl_sync(0xFFFFFFFFu, (long long)pos, k) * kUnitBytes + part * 16;
       const int64_t u = i - lane + k;
-      if (u >= units) continue;
-      const int64_t r = u / upr, c = u - r * upr;
+      in[it] = u < units;
+      int64_t r, c;
+      unit_at(k, r, c);
       const int64_t col_b = (c * kUnitW + part * kSegElems) * es;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (kv) v = *reinterpret_cast<const uint4*>(W + r * ld_bytes + col_b);
-      if (W_out != nullptr) *reinterpret_cast<uint4*>(W_out + r * ldo_bytes + col_b) = v;
-      if (kv && vals != nullptr) *reinterpret_cast<uint4*>(vals + kp * kUnitBytes + part * 16) = v;
+      off_w[it] = r * ld_bytes + col_b;
+      off_o[it] = r * ldo_bytes + col_b;
+      v[it] = make_uint4(0, 0, 0, 0);
+      if (in[it] && kv[it]) v[it] = *reinterpret_cast<const uint4*>(W + off_w[it]);
+    }
+#pragma unroll
+    for (int it = 0; it < kSpu; ++it) {
+      if (!in[it]) continue;
+      if (W_out != nullptr) *reinterpret_cast<uint4*>(W_out + off_o[it]) = v[it];
+      if (kv[it] && vals != nullptr) *reinterpret_cast<uint4*>(vals + kp[it]) = v[it];
     }
   } else {
     for (int k = 0; k < 32; ++k) {
@@ -459,17 +660,24 @@ __global__ void __launch_bounds__(kChunk) write_kernel(const uint8_t* __restrict
       const int64_t u = i - lane + k;
       if (u >= units) break;  // uniform across the warp
       if (!kv && W_out == nullptr) continue;
-      const int64_t bi = u / upr, bj = u - bi * upr;
+      int64_t bi, bj;
+      unit_at(k, bi, bj);
+      constexpr int kIt = kSpu / 32;
+      uint4 v[kIt];
 #pragma unroll
-      for (int it = 0; it < kSpu / 32; ++it) {
+      for (int it = 0; it < kIt; ++it) {  // loads first, as in the vector case
         const int g = it * 32 + lane;
-        const int rr = g / kSpr, part = g % kSpr;
-        const int64_t row = bi * 32 + rr;
-        const int64_t col_b = (bj * kUnitW + part * kSegElems) * es;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (kv) v = *reinterpret_cast<const uint4*>(W + row * ld_bytes + col_b);
-        if (W_out != nullptr) *reinterpret_cast<uint4*>(W_out + row * ldo_bytes + col_b) = v;
-        if (kv && vals != nullptr) *reinterpret_cast<uint4*>(vals + kp * kUnitBytes + g * 16) = v;
+        const int64_t row = bi * 32 + g / kSpr;
+        v[it] = make_uint4(0, 0, 0, 0);
+        if (kv) v[it] = *reinterpret_cast<const uint4*>(W + row * ld_bytes + (bj * kUnitW + (g % kSpr) * kSegElems) * es);
+      }
+#pragma unroll
+      for (int it = 0; it < kIt; ++it) {
+        const int g = it * 32 + lane;
+        const int64_t row = bi * 32 + g / kSpr;
+        const int64_t col_b = (bj * kUnitW + (g % kSpr) * kSegElems) * es;
+        if (W_out != nullptr) *reinterpret_cast<uint4*>(W_out + row * ldo_bytes + col_b) = v[it];
+        if (kv && vals != nullptr) *reinterpret_cast<uint4*>(vals + kp * kUnitBytes + g * 16) = v[it];
       }
     }
   }
@@ -626,14 +834,18 @@ cudaError_t launch_blocks_dt(const BlocksLaunch& a, const WsLayout& L, cudaStrea
   if (cudaError_t e = cudaMemsetAsync(ws, 0, L.keys, s)) return e;  // histogram + control block
   if (a.bh == 1) {
     const int64_t segs = a.rows * (a.cols * es / 16);
-    vw_score_kernel<DT><<<grid_for(segs, 256, 4), 256, 0, s>>>(W, a.rows, a.cols, a.ld * es, a.abs_of_sum, keys, hist,
-                                                                ctl, (uint64_t)a.keep);
+    if (a.abs_of_sum)
+      vw_score_kernel<DT, true><<<grid_for(segs, 256, 4), 256, 0, s>>>(W, a.rows, a.cols, a.ld * es, keys, hist, ctl,
+                                                                       (uint64_t)a.keep);
+    else
+      vw_score_kernel<DT, false><<<grid_for(segs, 256, 4), 256, 0, s>>>(W, a.rows, a.cols, a.ld * es, keys, hist, ctl,
+                                                                        (uint64_t)a.keep);
   } else {
     bw_score_kernel<DT><<<grid_for(units * 32, 256, 4), 256, 0, s>>>(W, a.rows, a.cols, a.ld * es, keys, hist, ctl,
                                                                       (uint64_t)a.keep);
   }
   candidates_kernel<<<grid_for(units, 256, 4), 256, 0, s>>>(keys, units, ctl, cand);
-  count_kernel<<<(unsigned)chunks, kChunk, 0, s>>>(keys, units, ctl, cgt, ceq);
+  count_kernel<<<(unsigned)((chunks + kCountChunks - 1) / kCountChunks), kChunk, 0, s>>>(keys, units, ctl, cgt, ceq);
   if (a.bh == 1) {
     write_kernel<DT, false><<<(unsigned)chunks, kChunk, 0, s>>>(
         W, a.rows, a.cols, a.ld * es, keys, units, ctl, cgt, ceq, static_cast<uint8_t*>(a.W_out), a.ld_out * es,
@@ -657,9 +869,7 @@ size_t blocks_workspace(int64_t units) { return ws_layout(units).total; }
 // names a host-side shadow, not device memory.  Its device address is looked
 // up once per device below.
 constexpr int64_t kFixedScratchUnits = int64_t(1) << 19;
-constexpr size_t kFixedScratchBytes =
-    align256(kBins * 4) + align256(sizeof(Ctl)) + 2 * align256((size_t)kFixedScratchUnits * 8) +
-    2 * align256((size_t)((kFixedScratchUnits + kChunk - 1) / kChunk) * 4);
+constexpr size_t kFixedScratchBytes = ws_layout(kFixedScratchUnits).total;
 static __device__ __align__(256) uint8_t g_units_scratch[kFixedScratchBytes];
 
 int64_t fixed_scratch_units() { return kFixedScratchUnits; }

@@ -35,6 +35,9 @@ def host_matrix(rows, cols, dtype, seed, kind):
         pool = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan], np.float16).view(np.uint16)
         idx = rng.choice(a.size, size=max(1, a.size // 200), replace=False)
         a.reshape(-1)[idx] = rng.choice(pool, size=idx.size)
+    if kind == "mixed":  # every finite exponent (subnormals to 65504) with random signs
+        bits = rng.integers(0, 0x7C00, size=(rows, cols)) | (rng.integers(0, 2, size=(rows, cols)) << 15)
+        return bits.astype(np.uint16)
     if kind == "large":  # magnitudes near the top of the f16 range: the widest exact scores
         a = (rng.uniform(30000, 65504, size=(rows, cols)) * rng.choice([-1, 1], size=(rows, cols)))
         a = a.astype(np.float16).view(np.uint16)
@@ -104,8 +107,13 @@ UNIT_CASES = [
     (33, 256, 256, "i8", 1, 0.5, "abs_of_sum", "normal"),
     (33, 256, 272, "i8", 1, 0.5, "sum_of_abs", "ties"),
     (257, 64, 64, "f16", 1, 0.4, "abs_of_sum", "ties"),
+    (2048, 2048, 2048, "f16", 1, 0.3, "abs_of_sum", "ties"),  # thousands of keys in the threshold bucket
     (128, 128, 128, "f16", 1, 0.5, "abs_of_sum", "zeros"),
     (64, 256, 256, "f16", 1, 0.25, "sum_of_abs", "large"),
+    (64, 256, 256, "f16", 1, 0.25, "abs_of_sum", "large"),
+    (96, 512, 512, "f16", 1, 0.3, "abs_of_sum", "mixed"),
+    (96, 512, 512, "f16", 1, 0.3, "sum_of_abs", "mixed"),
+    (128, 256, 256, "f16", 32, 0.4, "sum_of_abs", "mixed"),
     (64, 64, 64, "f16", 1, 0.0, "abs_of_sum", "normal"),
     (64, 64, 64, "f16", 1, 1.0, "abs_of_sum", "normal"),
     (1, 32, 32, "f16", 1, 1.0, "abs_of_sum", "normal"),
