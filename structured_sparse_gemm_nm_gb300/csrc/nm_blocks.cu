@@ -730,31 +730,32 @@ __global__ void __launch_bounds__(256) vw_spmv_kernel(const SpmmLaunch a) {
   const nm_spmm_desc_t& d = a.d;
   const int bf16 = d.ab_type == NM_BF16;
   const int lane = threadIdx.x & 31;
-  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= d.M) return;
   const int32_t* csr = static_cast<const int32_t*>(a.A_meta);
   const int32_t* colidx = csr + d.M + 1;
   const uint16_t* vals = static_cast<const uint16_t*>(a.A);
   const uint16_t* B = static_cast<const uint16_t*>(a.B);
-  const int p0 = csr[r], p1 = csr[r + 1];
   const int q = lane >> 2, part = lane & 3;
-  for (int64_t b0 = 0; b0 < d.N; b0 += NB) {
-    const int nb = (int)(d.N - b0 < NB ? d.N - b0 : NB);
-    float acc[NB];
+  // rows interleaved over the CTAs of a whole-wave grid (row r to CTA r mod grid)
+  for (int64_t r = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; r < d.M; r += 8 * (int64_t)gridDim.x) {
+    const int p0 = csr[r], p1 = csr[r + 1];
+    for (int64_t b0 = 0; b0 < d.N; b0 += NB) {
+      const int nb = (int)(d.N - b0 < NB ? d.N - b0 : NB);
+      float acc[NB];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
-    for (int p = p0 + q; p < p1; p += 8) {
-      const int64_t c = colidx[p];
-      const uint4 av = __ldcs(reinterpret_cast<const uint4*>(vals + (int64_t)p * kUnitW + part * 8));
-      dot8<NB>(av, B + b0 * d.ldb + c * kUnitW + part * 8, d.ldb, nb, bf16, acc);
+      for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
+      for (int p = p0 + q; p < p1; p += 8) {
+        const int64_t c = colidx[p];
+        const uint4 av = __ldcs(reinterpret_cast<const uint4*>(vals + (int64_t)p * kUnitW + part * 8));
+        dot8<NB>(av, B + b0 * d.ldb + c * kUnitW + part * 8, d.ldb, nb, bf16, acc);
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) acc[b] += __shfl_xor_sync(0xFFFFFFFFu, acc[b], m);
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        if (lane == b && b < nb) store_d(a, r, b0 + b, acc[b], bf16);
     }
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
-#pragma unroll
-      for (int m = 16; m > 0; m >>= 1) acc[b] += __shfl_xor_sync(0xFFFFFFFFu, acc[b], m);
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
-      if (lane == b && b < nb) store_d(a, r, b0 + b, acc[b], bf16);
   }
 }
 
@@ -902,11 +903,15 @@ cudaError_t launch_blocks(const BlocksLaunch& a, cudaStream_t s) {
 cudaError_t launch_spmm_blocks(const SpmmLaunch& a, cudaStream_t s) {
   const nm_spmm_desc_t& d = a.d;
   if (d.n == 1) {
-    const unsigned grid = (unsigned)((d.M + 7) / 8);
+    // whole waves over the SMs; a grid of ceil(M / 8) CTAs left some SMs a CTA short
+    static const int per_sm1 = resident_ctas(vw_spmv_kernel<1>, 256, 0);
+    static const int per_sm8 = resident_ctas(vw_spmv_kernel<8>, 256, 0);
+    int64_t grid = (int64_t)num_sms_cached() * (d.N == 1 ? per_sm1 : per_sm8);
+    if (grid > d.M) grid = d.M;  // a CTA's spare warps exit at once
     if (d.N == 1)
-      vw_spmv_kernel<1><<<grid, 256, 0, s>>>(a);
+      vw_spmv_kernel<1><<<(unsigned)grid, 256, 0, s>>>(a);
     else
-      vw_spmv_kernel<8><<<grid, 256, 0, s>>>(a);
+      vw_spmv_kernel<8><<<(unsigned)grid, 256, 0, s>>>(a);
   } else {
     const unsigned grid = (unsigned)(d.M / 32);
     if (d.N == 1)

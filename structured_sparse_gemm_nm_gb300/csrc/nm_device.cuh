@@ -81,6 +81,18 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// CTAs of `kernel` that fit on one SM at `threads` threads and `smem` dynamic shared bytes
+// (1 if the query fails).
+template <typename Kernel>
+inline int resident_ctas(Kernel kernel, int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  return n;
+}
+
 // Streaming multiprocessors of the current device (queried once).
 inline int num_sms_cached() {
   static const int v = [] {

@@ -438,10 +438,17 @@ __global__ void __launch_bounds__(128) prune32_kernel(const uint16_t* __restrict
   const int64_t total = rows * gpr;
   uint4* mine = srow4[threadIdx.x];
   const uint16_t* mine16 = reinterpret_cast<const uint16_t*>(mine);
-  for (int64_t gidx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gidx < total;
-       gidx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = gidx / gpr;
-    const int64_t gi = gidx - r * gpr;
+  if (total == 0) return;
+  // row and group of gidx, stepped with the grid stride (one 64-bit division per thread)
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t g_first = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t dr = stride / gpr, dg = stride - dr * gpr;
+  int64_t r = g_first / gpr, gi = g_first - r * gpr;
+  for (int64_t gidx = g_first; gidx < total; gidx += stride, r += dr, gi += dg) {
+    if (gi >= gpr) {
+      gi -= gpr;
+      ++r;
+    }
     const uint4* src = reinterpret_cast<const uint4*>(W + r * ld + gi * 32);
     uint32_t w[16];
 #pragma unroll

@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
       }
     }
     __syncthreads();
-    for (int64_t r = blockIdx.x * (int64_t)warps + (threadIdx.x >> 5); r < M; r += (int64_t)gridDim.x * warps) {
+    // rows interleaved over the CTAs (row r to CTA r mod grid), so that with a grid of
+    // whole waves every SM gets within one row per CTA of the same count
+    for (int64_t r = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; r < M; r += (int64_t)gridDim.x * warps) {
       float acc[NB];
 #pragma unroll
       for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
@@ -174,12 +176,14 @@ cudaError_t gather_launch(const SpmmLaunch& a, cudaStream_t s) {
       done_mask.fetch_or(bit);
     }
   }
-  // NB == 1: a warp per row, every row in flight at once; NB > 1: x is staged once per
-  // CTA, so one CTA of 32 warps per SM keeps that staging to one copy per SM
+  // A warp per row.  NB == 1: as many CTAs as fit on every SM at once; NB > 1: x is
+  // staged once per CTA, so one CTA of 32 warps per SM keeps that staging to one copy
+  // per SM.  The grid is whole waves over the SMs (rows are interleaved over CTAs): a
+  // grid of ceil(M / 32) CTAs left 24 of 152 SMs idle at M = 4096.
   const int threads = NB == 1 ? 256 : 1024;
-  int64_t blocks = (d.M + threads / 32 - 1) / (threads / 32);
-  const int64_t cap = NB == 1 ? (int64_t)1 << 20 : 152;
-  if (blocks > cap) blocks = cap;
+  static const int per_sm = NB == 1 ? resident_ctas(gather_kernel<NB>, threads, 0) : 1;
+  int64_t blocks = (int64_t)num_sms_cached() * per_sm;
+  if (blocks > d.M) blocks = d.M;
   if (blocks < 1) blocks = 1;
   gather_kernel<NB><<<(unsigned)blocks, threads, smem, s>>>(
       static_cast<const uint16_t*>(a.A), static_cast<const uint8_t*>(a.A_meta), static_cast<const uint16_t*>(a.B),

@@ -66,6 +66,7 @@ PRUNE_CASES = [
     (70, 96, 104, "bf16", 8, 32, "special"),     # n:32 fast path with NaN/Inf groups
     (33, 128, 128, "f16", 16, 32, "special"),
     (40, 64, 64, "bf16", 4, 32, "normal"),
+    (110000, 96, 96, "f16", 8, 32, "normal"),    # n:32 grid stride over rows of three groups
     (45, 40, 40, "f16", 3, 8, "special"),
     (64, 64, 64, "i8", 1, 4, "normal"),
     (50, 30, 30, "f16", 2, 5, "normal"),

@@ -169,6 +169,25 @@ def test_nm_gather_gemv_matches_oracle(n, batch):
     assert_gemm_close(y.cpu().double().numpy().T, ref, f"gemv n={n} b={batch}")
 
 
+@pytest.mark.parametrize("batch", [1, 8])
+def test_gather_many_rows_per_warp(batch):
+    # more rows than warps in the whole-wave grid: every warp takes several interleaved rows
+    M, K, n, m = 40000 + 3, 64, 8, 32
+    W = inputs.normal((M, K), 0.1, 12, "f16")
+    x = inputs.normal((batch, K), 1.0, 13, "f16")
+    vb, mb = nb.nm_compressed_size(M, K, "f16", n, m)
+    vals, idx = dev_bytes(vb), dev_bytes(mb)
+    nb.nm_compress(W.to(DEV), M, K, K, "f16", n, m, 0, nb.NM_META_CANONICAL, vals, idx)
+    y = torch.empty((batch, M), dtype=torch.float16, device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=batch, K=K, n=n, m=m, ab_type="f16", cd_type="f16", ldb=K, ldd=M,
+                                        meta_layout=nb.NM_META_CANONICAL))
+    nb.nm_spmm(plan, 1.0, vals, idx, x.to(DEV), 0.0, None, y)
+    torch.cuda.synchronize()
+    A = o.decode(o.nm_prune(inputs.as_numpy_bits(W), "f16", n, m)[0], "f16")
+    ref = o.spmm(1.0, A, o.decode(inputs.as_numpy_bits(x), "f16").T)
+    assert_gemm_close(y.cpu().double().numpy().T, ref, f"gather M={M} b={batch}")
+
+
 def test_gather_ragged_and_beta():
     M, K, N, n, m = 77, 96, 11, 3, 8
     W = inputs.normal((M, K), 0.5, 9, "bf16")

@@ -181,6 +181,8 @@ PRODUCT_CASES = [
     (64, 128, 32, 1, "f16", 1.0, 0.0, nb.NM_ROW),
     (128, 256, 32, 8, "bf16", 1.0, 0.0, nb.NM_COL),
     (96, 96, 32, 13, "f16", 2.0, 0.5, nb.NM_ROW),
+    (12000, 64, 1, 1, "f16", 1.0, 0.0, nb.NM_ROW),  # several interleaved rows per warp
+    (12000, 64, 1, 8, "f16", 1.0, 0.0, nb.NM_COL),
     (4096, 4096, 1, 1, "f16", 1.0, 0.0, nb.NM_ROW),
     (4096, 4096, 1, 8, "f16", 1.0, 0.0, nb.NM_ROW),
     (4096, 4096, 32, 1, "f16", 1.0, 0.0, nb.NM_ROW),
