@@ -444,3 +444,45 @@ def test_vw_int8_scores():
     kept = lambda m: list(np.nonzero(m.reshape(-1, 32)[:, 0])[0])
     assert kept(o.vector_wise_mask(W, "i8", 1 / 3, 32)) == [2]
     assert kept(o.vector_wise_mask(W, "i8", 1 / 3, 32, score="sum_of_abs")) == [0]
+
+
+# ------------------------------------------------------- storage formats
+# The header's storage rules, written out by hand for small rows: bit c % 32 of word
+# c / 32 is element c; a 2:4 group g of a row is the 4-bit code i0 | i1 << 2 at bits
+# 4 * (g % 4) of uint16 word g / 4; n:m metadata is one uint8 position per kept value.
+def test_mask_bits_layout_by_hand():
+    mask = np.zeros((2, 70), dtype=bool)
+    mask[0, [0, 5, 31, 32, 63, 64]] = True
+    mask[1, [1, 69]] = True
+    bits = o.mask_to_bits(mask)
+    assert bits.shape == (2, 3) and bits.dtype == np.uint32
+    assert bits[0].tolist() == [0x80000021, 0x80000001, 0x00000001]
+    assert bits[1].tolist() == [0x00000002, 0x00000000, 0x00000020]
+    assert (o.bits_to_mask(bits, 70) == mask).all()
+
+
+def test_canonical_24_metadata_by_hand():
+    row = np.arange(20, dtype=np.uint16) + 100  # five groups of four
+    keep = [(1, 3), (0, 2), (0, 1), (2, 3), (1, 2)]
+    mask = np.zeros((1, 20), dtype=bool)
+    for g, (a, b) in enumerate(keep):
+        mask[0, [4 * g + a, 4 * g + b]] = True
+    vals, meta = o.compress_by_mask(row[None, :], mask, 2, 4)
+    assert vals[0].tolist() == [101, 103, 104, 106, 108, 109, 114, 115, 117, 118]
+    # codes 0xD, 0x8, 0x4, 0xE in word 0 (groups 0..3), 0x9 in word 1 (group 4)
+    assert meta.dtype == np.uint16 and meta[0].tolist() == [0xE48D, 0x0009]
+    assert o.meta_words_per_row(20) == 2 and o.meta_words_per_row(16) == 1 and o.meta_words_per_row(4) == 1
+
+
+def test_nm_position_metadata_by_hand():
+    row = np.arange(16, dtype=np.uint16)  # two groups of eight, three kept in each
+    mask = np.zeros((1, 16), dtype=bool)
+    mask[0, [7, 2, 5]] = True
+    mask[0, [8, 9, 15]] = True
+    vals, meta = o.compress_by_mask(row[None, :], mask, 3, 8)
+    assert vals[0].tolist() == [2, 5, 7, 8, 9, 15]  # ascending position order
+    assert meta.dtype == np.uint8 and meta[0].tolist() == [2, 5, 7, 0, 1, 7]
+
+
+def test_tc_slot_rows_are_whole_tiles():
+    assert [o.tc_meta_slot_rows(r) for r in (1, 127, 128, 129, 256, 300)] == [128, 128, 128, 256, 256, 384]
