@@ -681,17 +681,36 @@ __global__ void __launch_bounds__(256) check24_strips_kernel(const uint4* __rest
   const int64_t total = ((rows + 3) / 4) * wpr;
   const int64_t lo = ((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5) * per;
   const int64_t hi = lo + per < total ? lo + per : total;
+  if (lo >= hi) return;
   int count = 0;
+  // strip and word of the lane's two items, stepped by 64 items per pass (a 64-bit
+  // division per item had cost more issue slots than the check itself)
+  int64_t st[2], wd[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int64_t idx = lo + 32 * u + lane;
+    st[u] = idx / wpr;
+    wd[u] = idx - st[u] * wpr;
+  }
   for (int64_t base = lo; base < hi; base += 64) {
     uint32_t m[2][4];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int64_t idx = base + 32 * u + lane;
-      const int64_t st = idx / wpr, w = idx - st * wpr;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int64_t r = 4 * st + j;
-        m[u][j] = (idx < hi && r < rows) ? nz8(__ldcs(W + r * ldw + w)) : 0u;
+        const int64_t r = 4 * st[u] + j;
+        m[u][j] = (idx < hi && r < rows) ? nz8(__ldcs(W + r * ldw + wd[u])) : 0u;
+      }
+      wd[u] += 64;
+      if (wd[u] >= wpr) {
+        if (wpr >= 64) {
+          wd[u] -= wpr;
+          ++st[u];
+        } else {
+          st[u] += wd[u] / wpr;
+          wd[u] %= wpr;
+        }
       }
     }
 #pragma unroll
