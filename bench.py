@@ -846,7 +846,7 @@ def run_native(args):
 LINEARS = {"qkv": (2304, 768), "o": (768, 768), "fc1": (3072, 768), "fc2": (768, 3072)}  # out x in
 SPARSE_CASES = tuple(f"sparse_{lin}_{d}" for lin in LINEARS for d in ("fwd", "dx"))
 KERNEL_CASES = SPARSE_CASES + ("dense_fc1_dw", "transposable_fc1", "prune24_4096", "prune_8of32_4096",
-                               "gemv_8of32_b8", "vector_wise_4096")
+                               "gemv_8of32_b8", "vector_wise_4096", "check24_4096")
 
 
 def run_kernel_case(name: str, reps: int = 3):
@@ -911,6 +911,11 @@ def run_kernel_case(name: str, reps: int = 3):
             fn = [lambda: nb.nm_spmm(plan, 1.0, vals, meta, x, 0.0, None, y)]
         else:
             fn = [lambda Wr=Wr: nb.nm_compress(Wr, M, K, K, "f16", n, m, 0, layout, vals, meta) for Wr in Ws]
+    elif name == "check24_4096":
+        M = K = 4096
+        Ws = [inputs.normal((M, K), 0.02, 40 + r, "f16", device=dev) for r in range(max(reps, 5))]
+        cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+        fn = [lambda Wr=Wr: nb.nm_check(Wr, M, K, K, "f16", 2, 4, 1, cnt) for Wr in Ws]
     elif name == "vector_wise_4096":
         M = K = 4096
         keep = M * (K // 32) // 4
