@@ -16,8 +16,9 @@
 //                 finds the bucket holding the keep-th largest key.
 //   2. candidates the keys of that bucket are gathered; the last CTA finds the
 //                 exact threshold key T by a radix search over them.
-//   3. count      per chunk of 256 units: keys above T and keys equal to T;
-//                 the last CTA turns the counts into exclusive prefixes.
+//   3. count      per chunk of 256 units: keys above T and keys equal to T,
+//                 as prefixes within groups of 8 chunks plus group totals;
+//                 the last CTA turns the group totals into exclusive prefixes.
 //   4. write      kept flag and output position of every unit, then the CSR
 //                 arrays, the packed values, the bit mask and the pruned copy.
 // A unit is kept if its key is above T, or equal to T and among the first
