@@ -138,6 +138,20 @@ def test_unit_pruning_matches_oracle(rows, cols, ld, dtype, bh, density, score, 
     check_against_oracle(W, rows, cols, dtype, bh, density, score, got, ld)
 
 
+def test_unit_pruning_one_crowded_bucket():
+    # 2.6 M vectors whose scores all fall in one histogram bucket (1.0 everywhere, a tenth
+    # of the elements one ulp higher: 15 distinct scores): every candidates CTA holds
+    # more keys than its shared buffer, the radix search runs over millions of keys in
+    # global memory, and thousands of units tie at the threshold
+    rows, cols = 5120, 16384
+    rng = np.random.default_rng(7)
+    W = np.full((rows, cols), 0x3C00, np.uint16)
+    W[rng.random((rows, cols)) < 0.1] = 0x3C01
+    keep = int(rows * cols // 32 * 0.3)
+    got = run_units(W, rows, cols, "f16", 1, keep, "abs_of_sum")
+    check_against_oracle(W, rows, cols, "f16", 1, 0.3, "abs_of_sum", got, cols)
+
+
 def test_unit_pruning_in_place_and_repeatable():
     rows, cols = 96, 160
     W = host_matrix(rows, cols, "f16", 61, "normal")
