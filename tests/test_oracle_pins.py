@@ -314,6 +314,22 @@ def test_masked_weight_grad_by_loops():
             assert abs(G[i, j] - want) <= 1e-12
 
 
+def test_masked_weight_grad_closed_forms():
+    rng = np.random.default_rng(25)
+    out, inp = 4, 8
+    mask = o.transposable_mask(f16_bits(rng.standard_normal((out, inp))), "f16")
+    # X = identity (tokens = input features): the gradient is the masked transpose of dY
+    dY = rng.standard_normal((inp, out))
+    assert np.array_equal(o.masked_weight_grad(dY, np.eye(inp), mask), np.where(mask, dY.T, 0.0))
+    # rank one: dY[t, i] = a_t b_i and X[t, j] = a_t c_j give (sum a_t^2) b_i c_j on kept entries
+    a = np.array([1.0, -2.0, 0.5, 3.0, 0.25, -1.0])
+    b, c = rng.standard_normal(out), rng.standard_normal(inp)
+    G = o.masked_weight_grad(np.outer(a, b), np.outer(a, c), mask)
+    want = np.where(mask, (a @ a) * np.outer(b, c), 0.0)
+    assert np.allclose(G, want, rtol=1e-13, atol=1e-13)
+    assert G.shape == (out, inp)
+
+
 # ------------------------------------------------- vector- and block-wise masks
 def test_vector_wise_literal_score_and_count():
     rng = np.random.default_rng(31)
