@@ -256,22 +256,31 @@ typedef enum {
   NM_COL = 1  /* column-major: the first index is contiguous */
 } nm_order_t;
 
+/*
+ * Algorithm selection for the tensor-core products (SPARSE_A 2:4 F16/BF16 and
+ * DENSE_MASKED), after the algorithm-selection step of the cuSPARSELt blog's
+ * code example.  Other products have one kernel and ignore the choice.
+ *   NM_ALGO_DEFAULT  the library's choice: paired CTAs when M spans an even
+ *                    number of 128-row blocks, single CTAs otherwise.
+ *   NM_ALGO_PAIRED   two CTAs of a cluster run one M256 x N256 tile with
+ *                    tcgen05 cta_group::2 (each holds 128 rows of A and half
+ *                    of B); falls back to single CTAs for an odd block count.
+ *   NM_ALGO_SINGLE   one CTA per M128 x N256 tile (tcgen05 cta_group::1).
+ */
+typedef enum { NM_ALGO_DEFAULT = 0, NM_ALGO_PAIRED = 1, NM_ALGO_SINGLE = 2 } nm_algo_t;
+
 typedef struct {
   int64_t M, N, K;
   nm_spmm_mode_t mode;
   int n, m;                     /* sparsity of A (SPARSE_A)                                   */
   nm_dtype_t ab_type;           /* F16, BF16 or I8                                            */
-  nm_dtype_t cd_type;           /* = ab_type for F16/BF16; I32 for I8                         */
+  nm_dtype_t cd_type;           /* F16/BF16 in: ab_type, or F32 (tensor-core products); I8: I32 */
   nm_order_t order_a;           /* DENSE_MASKED: ROW = A stored M x K, COL = stored K x M     */
   nm_order_t order_b;           /* ROW = B stored K x N, COL = B stored N x K                 */
   nm_order_t order_cd;          /* ROW = C, D stored M x N, COL = stored N x M                */
   int64_t lda, ldb, ldc, ldd;   /* leading dimensions in elements (lda: DENSE_MASKED only)    */
   nm_meta_layout_t meta_layout; /* SPARSE_A 2:4 with F16/BF16 needs NM_META_TC                */
-  int algo;                     /* algorithm selection (cuSPARSELt blog, code example: the    */
-                                /* algorithm-selection step): 0 = the library's default;      */
-                                /* 1 = SPARSE_A 2:4 F16/BF16 on pairs of CTAs (tcgen05 with   */
-                                /* cta_group::2, M256 tiles) when M spans an even number of   */
-                                /* 128-row blocks, else the default                            */
+  int algo;                     /* an nm_algo_t                                               */
 } nm_spmm_desc_t;
 
 typedef struct nm_spmm_plan_s* nm_spmm_plan_t;

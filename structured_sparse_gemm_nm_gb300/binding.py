@@ -25,12 +25,16 @@ NM_ROW, NM_COL = 0, 1
 
 DTYPE_NAMES = {"f16": NM_F16, "bf16": NM_BF16, "i8": NM_I8, "f32": NM_F32, "i32": NM_I32}
 
+NM_ALGO_DEFAULT, NM_ALGO_PAIRED, NM_ALGO_SINGLE = 0, 1, 2
+
 # Every symbol include/nm.h declares.
 EXPORTED = (
     "nm_status_string", "nm_version", "nm_last_cuda_error", "nm_compressed_size", "nm_prune", "nm_compress", "nm_decompress",
     "nm_check", "nm_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
     "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm",
 )
+# Every symbol include/nm_testing.h declares.
+TESTING_EXPORTED = ("nm_test_spmm_wait_timeout",)
 
 
 class NmError(RuntimeError):

@@ -321,10 +321,10 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   *plan = nullptr;
   const nm_spmm_desc_t& d = *desc;
   if (d.M < 0 || d.N < 0 || d.K < 0) return NM_ERR_INVALID_ARG;
-  if (d.algo != 0 && d.algo != 1) return NM_ERR_INVALID_ARG;
+  if (d.algo != NM_ALGO_DEFAULT && d.algo != NM_ALGO_PAIRED && d.algo != NM_ALGO_SINGLE) return NM_ERR_INVALID_ARG;
   if (!is_elem(d.ab_type)) return NM_ERR_INVALID_ARG;
   const bool fp = d.ab_type != NM_I8;
-  if (fp ? d.cd_type != d.ab_type : d.cd_type != NM_I32) return NM_ERR_UNSUPPORTED;
+  if (fp ? (d.cd_type != d.ab_type && d.cd_type != NM_F32) : d.cd_type != NM_I32) return NM_ERR_UNSUPPORTED;
   if ((d.order_a != NM_ROW && d.order_a != NM_COL) || (d.order_b != NM_ROW && d.order_b != NM_COL) ||
       (d.order_cd != NM_ROW && d.order_cd != NM_COL))
     return NM_ERR_INVALID_ARG;
@@ -369,6 +369,8 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   } else {
     return NM_ERR_INVALID_ARG;
   }
+  // an fp32 C/D only on the tensor-core products
+  if (fp && d.cd_type == NM_F32 && kind != 0 && kind != 1) return NM_ERR_UNSUPPORTED;
   // The tensor-core and int8 kernels write D (and read C) in 16-byte pieces;
   // the CUDA-core GEMV kernels (kinds 2 and 4) access them element by element.
   const bool cd_wide = kind != 2 && kind != 4;

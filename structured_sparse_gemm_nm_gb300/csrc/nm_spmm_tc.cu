@@ -10,32 +10,50 @@
 //                   split across CTAs (fp32 partials in the workspace, summed
 //                   by a finalize kernel) when the output has few tiles.
 //
-// A persistent CTA per SM computes 128 x 256 output tiles.  Two CTAs of a
-// cluster work on neighbouring 128-row blocks of the same 256-column block:
-// each fetches half of the shared B tile and multicasts it to both, which
-// halves the L2 traffic of B.  Warp roles per CTA:
-//   warp 0       TMA producer: A and (its half of) B for stages of 64 dense K
-//   warp 1       owns tensor memory; one lane issues the tcgen05.mma of
-//                columns 0..127 of the tile (M128 N128 per instruction)
-//   warps 2..5   SPARSE metadata: each warp loads one 32-bit code word per
-//                lane (row slot) and k-step from global memory and writes it
-//                with tcgen05.st into one of four 64-column-aligned TMEM
-//                slots (the sparse MMA accepts its metadata only there); this
-//                keeps metadata movement out of the tensor pipe.  The slots
-//                form two pairs used by alternate stages: the metadata warps
-//                refill a pair once the stage that last used it is released
-//                (its `empty` barrier) and then arrive on the new stage's
-//                `full` barrier, so the MMA issuer waits on one barrier per
-//                stage and commits once per stage.
-//   warps 6..13  epilogue: drain the FP32 accumulator (alpha, mask) into
-//                packed registers, release it, then stage 32 x 32 blocks in
-//                shared memory and write them with TMA bulk stores
-//   warp 14      one lane issues the tcgen05.mma of columns 128..255; an MMA
-//                holds its issuing thread for about its execution time, so two
-//                issuers keep the tensor pipe busy through each other's
-//                barrier waits, commits and loop overhead
-// Every mbarrier wait is bounded; a wait that gives up sets an abort flag
-// and NM_ERR_TIMEOUT in the caller's status word, the roles drain their
+// Pairs of CTAs.  A single CTA's M128 x N256 sparse MMA reads its A and B
+// operands from shared memory at 128 bytes per clock (20 KB per K32 step: 160
+// cycles, measured on GB300), more than the 2:4 tensor rate needs.  With
+// cta_group::2 the two CTAs of a cluster run M256 MMAs over both CTAs' shared
+// memory: each CTA stages its own 128 rows of A and one 128-row block of B
+// (tile columns 128 r .. 128 r + 127 for rank r), and a paired sparse K32 step
+// reads 12 KB per SM: measured at 128 cycles for M256 x N256, twice the dense
+// rate.  Every CTA loads only the tiles it holds; no TMA load delivers to
+// more than one CTA.
+//
+// Paired kernel (default when M spans an even number of 128-row blocks),
+// warp roles per CTA:
+//   warp 0       TMA producer (one lane): A, then B in 64-K boxes of 16 KB,
+//                all on the stage's `full` barrier (a warp streams large
+//                boxes grouped per barrier far faster than one box per
+//                barrier); SPARSE stages hold 128 K, DENSE 64 K
+//   warps 1, 14  even CTA: the two MMA issuers, columns 0..127 and 128..255
+//                of the tile as M256 x N128 MMAs.  An MMA holds its issuing
+//                thread until it has nearly completed, so every barrier wait,
+//                commit or loop step of one issuer would leave the tensor pipe
+//                idle; two issuers overlap each other's.  Issuer h reads rows
+//                64 h .. 64 h + 63 of each CTA's B block.
+//                odd CTA: warp 1 relays each completed stage to the even
+//                CTA's `full` barrier
+//   warps 2..5   SPARSE metadata: per pair of k-steps, each warp writes one
+//                32-bit code word per lane (row) and k-step with tcgen05.st
+//                into a pair of the four 64-column-aligned tensor-memory slots
+//                of its own CTA (the sparse MMA reads metadata only there);
+//                the two slot pairs alternate, each with a full/empty barrier
+//                pair shared by both CTAs
+//   warps 6..13  epilogue: drain this CTA's 128 accumulator rows with
+//                tcgen05.ld, first half first, hand each half back to its
+//                issuer, then write D straight from registers (no shared-
+//                memory staging)
+// The accumulator holds 256 columns (SPARSE: one buffer, the metadata slots
+// use the other half of tensor memory; DENSE: two buffers).
+//
+// Single-CTA kernel (an odd number of row blocks, or algo NM_ALGO_SINGLE):
+// M128 x N256 tiles, two MMA issuers of 128 columns each, metadata slot pairs
+// per stage on the stage's `full` barrier, and an epilogue that stages 32 x 32
+// blocks for TMA bulk stores.
+//
+// Every mbarrier wait is bounded; a wait that gives up sets an abort flag and
+// NM_ERR_TIMEOUT in the caller's status word, the roles drain their
 // outstanding asynchronous work and the CTA frees its tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -47,6 +65,7 @@
 
 #include "nm_device.cuh"
 #include "nm_internal.h"
+#include "../../include/nm_testing.h"
 
 namespace nmk {
 namespace tc {
@@ -56,33 +75,37 @@ constexpr int BN = 256;
 constexpr int kKPerStage = 64;  // dense-equivalent K per stage
 constexpr int kMetaWarp0 = 2, kMetaWarps = 4;
 constexpr int kEpiWarp0 = kMetaWarp0 + kMetaWarps, kEpiWarps = 8;
-constexpr int kMmaWarpB = kEpiWarp0 + kEpiWarps;  // second MMA issuer (columns 128..255)
-constexpr int kThreads = 32 * (kMmaWarpB + 1);
+constexpr int kMmaWarpB = kEpiWarp0 + kEpiWarps;  // single CTA: second MMA issuer (columns 128..255)
 constexpr int kTmemCols = 512;
 constexpr int kMetaCol = 256, kMetaColStride = 64;  // four metadata slots: columns 256, 320, 384, 448
-constexpr int kEpiBufBytes = 32 * 32 * 2;  // one 32 x 32 output block
+constexpr int kEpiBufBytes = 32 * 32 * 2;  // single CTA: one 32 x 32 16-bit output block
 
-// PAIR: the two CTAs of a cluster run one M256 x N256 product (tcgen05 with
-// cta_group::2); each holds its 128 rows of A and one 128-row half of B.
-template <bool SPARSE, bool PAIR = false>
+// Output element kinds of C and D.
+constexpr int kCdF16 = 0, kCdBF16 = 1, kCdF32 = 2;
+
+
+template <bool SPARSE, bool PAIR>
 struct Cfg {
-  // dense-equivalent K per stage: 64, or 128 for the paired product (four k-steps per
-  // barrier wait and commit of its single issuer)
-  static constexpr int kKStage = PAIR ? 128 : kKPerStage;
-  static constexpr int kSteps = kKStage / 32;  // SPARSE k-steps per stage
-  // SPARSE A: 128 rows x kKStage/2 compressed values (64B swizzle for 64 B rows, 128B for
-  // 128 B rows); dense A: 128 x 64 (128B swizzle).
+  static constexpr int kWarps = kMmaWarpB + 1;
+  static constexpr int kThreads = 32 * kWarps;
+  // dense-equivalent K per stage: paired SPARSE stages hold 128 K (A 16 KB + B 2 x 16 KB, in large
+  // TMA boxes), the others 64
+  static constexpr int kKStage = (SPARSE && PAIR) ? 128 : kKPerStage;
+  static constexpr int kSubs = kKStage / 64;  // SPARSE: pairs of k-steps per stage
+  // A: SPARSE 128 rows x kKStage / 2 compressed values (64 B rows with the 64B swizzle, 128 B rows
+  // with the 128B swizzle); dense 128 x 64 (128B swizzle)
   static constexpr int kATileBytes = SPARSE ? BM * kKStage : BM * 128;
-  // B: rows x 64 elements per 128B-swizzled box; PAIR holds 128 rows and two boxes along K
-  static constexpr int kBTileBytes = PAIR ? (BN / 2) * 256 : BN * 128;
-  // PAIR: the stage also carries its k-steps' metadata, one 16-byte row per row of A
-  static constexpr int kMetaBytes = PAIR ? kSteps * BM * 16 : 0;
-  static constexpr int kStageBytes = kATileBytes + kBTileBytes + kMetaBytes;
-  static constexpr int kStages = PAIR ? 3 : (SPARSE ? 5 : 4);
+  // B: rows x kKStage (boxes of 64 K with the 128B swizzle); a pair holds one 128-row half of the 256 rows
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;
+  static constexpr int kBTileBytes = kBRows * 2 * kKStage;
+  static constexpr int kTxBytes = kATileBytes + kBTileBytes;  // TMA bytes per stage
+  static constexpr int kStageBytes = kTxBytes;
+  static constexpr int kStages = PAIR ? (SPARSE ? 4 : 6) : (SPARSE ? 5 : 4);
   static constexpr int kAcc = SPARSE ? 1 : 2;  // 256-column accumulator buffers
   static constexpr int kEpiOffset = kStages * kStageBytes;
-  static constexpr int kBarOffset = kEpiOffset + kEpiWarps * kEpiBufBytes;
+  static constexpr int kBarOffset = kEpiOffset + (PAIR ? 0 : kEpiWarps * kEpiBufBytes);
   static constexpr int kSmemBytes = 1024 + kBarOffset + 512;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 struct Params {
@@ -96,16 +119,17 @@ struct Params {
   const uint32_t* meta;  // SPARSE: tensor-core metadata [K/32][meta_slots]
   int64_t meta_slots;
   int a_mn, b_mn;        // DENSE operand majors (1 = M/N contiguous)
-  int bf16;
+  int bf16;              // A, B element type
+  int cd_kind;           // kCdF16, kCdBF16 or kCdF32
   float alpha, beta;
   const void* C;
   void* D;
   int64_t ldc, ldd;
   int cd_col;     // 1: D[n * ldd + m]; 0: D[m * ldd + n]
-  int tma_store;  // 1: D written by TMA bulk stores (C not read)
+  int tma_store;  // single CTA: 1 = D written by TMA bulk stores (16-bit D, C not read)
   const uint32_t* mask;
   int64_t mask_words;
-  float* partial;  // DENSE split-K: [split][M][N]
+  float* partial;  // DENSE split-K: tiled fp32 partials
   int32_t* status;
   long long wait_budget;  // cycles
   int fault_test;         // 1: the MMA lane waits on a barrier nothing arrives at
@@ -123,13 +147,13 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// CLUSTER: acquire at cluster scope, for barriers the peer CTA arrives on.
+// CLUSTER: acquire at cluster scope, for barriers the other CTA of the pair arrives on.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   if constexpr (CLUSTER)
     asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         "selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -167,22 +191,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try<CLUSTER>(bar, parity)) return true;
   return mbar_wait_slow<CLUSTER>(bar, parity, abort_flag, budget, status);
 }
+// Drain wait at the end of a role: bounded, no status (the role already reported any timeout).
+template <bool CLUSTER = false>
+__device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity, long long budget) {
+  const long long t0 = clock64();
+  while (!mbar_try<CLUSTER>(bar, parity) && clock64() - t0 < budget) {
+  }
+}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           dst),
       "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-// The same box lands at the same offset in the shared memory of every CTA in
-// `mask`, each completing bytes on its own barrier at offset `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
-      "%3}], [%4], %5;" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar), "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
@@ -202,6 +223,21 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+// Relaxed remote arrive.  Used where what it announces was completed by the
+// arriving thread itself and is read only through the arriving CTA's own
+// shared or tensor memory (TMA bytes whose completion this thread observed,
+// metadata written with tcgen05.st and waited for, accumulator columns read
+// with tcgen05.ld and waited for).  A release at cluster scope costs over a
+// thousand cycles per arrive on GB300.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 
 // Shared-memory matrix descriptor (tcgen05): start, leading/stride byte
 // offsets (16-byte units), fixed version bit 46, swizzle mode in bits 61..63.
@@ -211,11 +247,10 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
 }
 constexpr uint32_t kSwizzle128 = 2, kSwizzle64 = 4;
 
-// Instruction descriptor for kind::f16: D = F32, A/B = F16 or BF16, M = 128, N = 128
-// (each of the two issuers computes one 128-column half of the tile).
-__device__ __forceinline__ uint32_t idesc_f16(int bf16, int a_mn, int b_mn, bool sparse) {
+// Instruction descriptor for kind::f16: D = F32, A/B = F16 or BF16, shape M x N.
+__device__ __forceinline__ uint32_t idesc_f16(int bf16, int a_mn, int b_mn, bool sparse, int m, int n) {
   uint32_t d = (1u << 4) | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10) | ((uint32_t)a_mn << 15) |
-               ((uint32_t)b_mn << 16) | ((uint32_t)((BN / 2) >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+               ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
   if (sparse) d |= 1u << 2;
   return d;
 }
@@ -236,16 +271,16 @@ __device__ __forceinline__ void mma_sparse(uint32_t tmem_d, uint64_t a, uint64_t
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-// Arrives on the barrier at the same offset in every CTA of `mask` once the prior MMAs complete.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
 // cta_group::2 forms: the MMA is issued by the even CTA of the pair and reads
-// the operands of both CTAs at the same shared-memory offsets; the commit
-// arrives on the barrier at the same offset in both CTAs.
+// the operands of both CTAs at the same shared-memory offsets (and the
+// metadata of both at the same tensor-memory column); a commit arrives on one
+// barrier, in either CTA, once the prior MMAs of the issuing thread complete.
+__device__ __forceinline__ void mma_dense_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
 __device__ __forceinline__ void mma_sparse_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t tmem_meta,
                                                 uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -253,34 +288,14 @@ __device__ __forceinline__ void mma_sparse_pair(uint32_t tmem_d, uint64_t a, uin
           "r"(tmem_d),
       "l"(a), "l"(b), "r"(tmem_meta), "r"(idesc), "r"(acc));
 }
-// Copies 128 rows x 16 bytes of each CTA's shared memory into its own tensor
-// memory (four columns at `taddr`), in order with the MMAs this thread issues.
-__device__ __forceinline__ void tc_cp_pair(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+__device__ __forceinline__ void tc_commit_pair(uint32_t cluster_bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(cluster_bar)
+               : "memory");
 }
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"((uint16_t)3)
-      : "memory");
-}
-// Address of the same shared-memory location in the even CTA of the pair.
-__device__ __forceinline__ uint32_t pair_leader_addr(uint32_t a) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(a));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-// Relaxed remote arrive for "stage ready": the data it announces was written
-// into this CTA's shared memory (TMA, and metadata rows already fenced to the
-// async proxy), completion was observed here, and it is read only through
-// this CTA's shared memory by the paired tensor-core instructions.  A release
-// at cluster scope costs over a thousand cycles per arrive, which would limit
-// the pair to one stage per relay round trip.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// The same barrier offset in both CTAs of the pair.
+__device__ __forceinline__ void tc_commit_both(uint32_t bar) {
+  tc_commit_pair(bar);
+  tc_commit_pair(peer_addr(bar, 1));
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -311,12 +326,19 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ float load_cd(const void* base, int64_t off, int bf16) {
+// C and D elements: f16, bf16 or f32 (cd_kind).
+__device__ __forceinline__ float load_cd(const void* base, int64_t off, int cd_kind) {
+  if (cd_kind == kCdF32) return reinterpret_cast<const float*>(base)[off];
   const uint16_t b = reinterpret_cast<const uint16_t*>(base)[off];
-  return bf16 ? __uint_as_float((uint32_t)b << 16) : __half2float(__ushort_as_half(b));
+  return cd_kind == kCdBF16 ? __uint_as_float((uint32_t)b << 16) : __half2float(__ushort_as_half(b));
 }
-__device__ __forceinline__ uint16_t to_cd(float x, int bf16) {
-  return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
+__device__ __forceinline__ void store_cd(void* base, int64_t off, float x, int cd_kind) {
+  if (cd_kind == kCdF32) {
+    reinterpret_cast<float*>(base)[off] = x;
+    return;
+  }
+  reinterpret_cast<uint16_t*>(base)[off] = cd_kind == kCdBF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x))
+                                                              : __half_as_ushort(__float2half_rn(x));
 }
 // Compile-time form for the drain: one conversion instruction per pair.
 template <bool BF16>
@@ -328,6 +350,10 @@ __device__ __forceinline__ uint32_t pack2t(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
   }
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
+  // one round-to-nearest conversion of the pair; `lo` lands in the low 16 bits
+  return bf16 ? pack2t<true>(lo, hi) : pack2t<false>(lo, hi);
 }
 // One warp's 32 lanes x 64 accumulator columns (two 32-column loads in flight)
 // into packed pairs: alpha applied when SCALE, masked columns zeroed when
@@ -372,18 +398,9 @@ __device__ __forceinline__ void drain64_any(int bf16, bool scale, uint32_t taddr
       drain64<false, false, MASKED>(taddr, alpha, ma, mb, pa, pb);
   }
 }
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
-  // one round-to-nearest conversion of the pair; `lo` lands in the low 16 bits
-  if (bf16) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&h);
-  }
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Work unit u -> 128-row block, 256-column block and K split.  In a cluster
-// of two, CTA rank r takes row block 2 * (pair index) + r.
+// Work unit u -> 128-row block of this CTA, 256-column block and K split.
+// Paired: the pair's 256 rows are row blocks 2 * (pair index) and
+// 2 * (pair index) + 1, the CTA of rank r taking the second index r.
 struct Unit {
   int m0, n0, kbeg, kend, split;
 };
@@ -400,43 +417,88 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int cl, int 
   return t;
 }
 
+// fp32 partial of one K split, in the tiled order
+// [split][m block][n block][col / 4][128 rows][4]: for each group of four
+// columns the 32 lanes of a warp write 512 contiguous bytes.
+__device__ __forceinline__ void store_partial_chunk(const Params& p, const Unit& t, int col, int q, int lane,
+                                                    const uint32_t (&v)[32], uint32_t mword) {
+  float4* tile = reinterpret_cast<float4*>(p.partial) +
+                 ((int64_t)(t.split * p.num_m_blk + t.m0 / BM) * p.num_n_blk + t.n0 / BN) * (BM * BN / 4);
+  const int c4_0 = col / 4;
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) {
+    float4 w;
+    w.x = ((mword >> (4 * j4)) & 1u) ? __uint_as_float(v[4 * j4]) * p.alpha : 0.0f;
+    w.y = ((mword >> (4 * j4 + 1)) & 1u) ? __uint_as_float(v[4 * j4 + 1]) * p.alpha : 0.0f;
+    w.z = ((mword >> (4 * j4 + 2)) & 1u) ? __uint_as_float(v[4 * j4 + 2]) * p.alpha : 0.0f;
+    w.w = ((mword >> (4 * j4 + 3)) & 1u) ? __uint_as_float(v[4 * j4 + 3]) * p.alpha : 0.0f;
+    tile[(c4_0 + j4) * BM + 32 * q + lane] = w;
+  }
+}
+// Element-wise D of one row's 32 columns starting at nb: alpha, mask, beta * C.
+__device__ __forceinline__ void store_chunk_generic(const Params& p, int row, int nb, const uint32_t (&v)[32],
+                                                    uint32_t mword) {
+  const int cnt = min(32, p.N - nb);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j >= cnt) break;
+    float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
+    const int64_t doff = p.cd_col ? (int64_t)(nb + j) * p.ldd + row : (int64_t)row * p.ldd + nb + j;
+    const int64_t coff = p.cd_col ? (int64_t)(nb + j) * p.ldc + row : (int64_t)row * p.ldc + nb + j;
+    if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, coff, p.cd_kind), x);
+    store_cd(p.D, doff, x, p.cd_kind);
+  }
+}
+
 // ----------------------------------------------------------------- kernel
-// 15 warps are resident as 16 for register allocation (warps are allocated in
-// groups of four), so 128 registers per thread is the most that still fits
-// the 64K-register file.
-template <bool SPARSE, int CL, bool PAIR>
+// The warps of a CTA are spread over the SM's four sub-partitions, each with a
+// quarter of the register file: 14 or 15 warps put four on one of them, so
+// 128 registers per thread is the most that fits.
+template <bool SPARSE, bool PAIR>
 __global__ void __maxnreg__(128)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const Params p) {
-  static_assert(!PAIR || (SPARSE && CL == 2), "the paired product is the sparse one on clusters of two");
   using C = Cfg<SPARSE, PAIR>;
+  constexpr int CL = PAIR ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-  // bars: full[S], empty[S], tfull[2], tempty[2 buffers][2 column halves], drain
+  // bars: full[S], empty[S], tfull[2], tempty[4] (single: 2 buffers x 2 column halves; paired: one per
+  // buffer), drain, mfull[2], mempty[2] (paired SPARSE: one pair per metadata slot pair)
   const uint32_t bar_full = smem_u32(bars), bar_empty = smem_u32(bars + C::kStages);
   const uint32_t bar_tfull = smem_u32(bars + 2 * C::kStages), bar_tempty = bar_tfull + 16;
   const uint32_t bar_drain = bar_tempty + 32;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 7);
+  const uint32_t bar_mfull = bar_drain + 8, bar_mempty = bar_mfull + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
   const int cluster_id = blockIdx.x / CL, num_clusters = gridDim.x / CL;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      // SPARSE: the producer's expect_tx arrival and one arrival per metadata warp;
-      // PAIR: the leader's barrier also takes the peer's relayed arrival
-      mbar_init(bar_full + 8 * s, (SPARSE ? 1 + kMetaWarps : 1) + (PAIR && rank == 0 ? 1 : 0));
-      // released by both issuers of every CTA that reads the stage (PAIR: the one paired issuer)
-      mbar_init(bar_empty + 8 * s, PAIR ? 1 : 2 * CL);
+      uint32_t full_count;
+      // single CTA: the producer's expect_tx arrival and (SPARSE) one arrival per metadata warp
+      // once it has written the stage's metadata slot pair; paired: one expect_tx arrival per
+      // producer warp, and on the even CTA the odd CTA's relay
+      if constexpr (PAIR)
+        full_count = 1 + (leader ? 1 : 0);
+      else
+        full_count = 1 + (SPARSE ? kMetaWarps : 0);
+      mbar_init(bar_full + 8 * s, full_count);
+      // released by the commits of the two issuers that read the stage
+      mbar_init(bar_empty + 8 * s, 2);
     }
-    for (int a = 0; a < 2; ++a) mbar_init(bar_tfull + 8 * a, PAIR ? 1 : 2);
-    // one arrival per epilogue warp once it has read its columns of that half
-    // (PAIR: a single barrier per buffer, after both halves, from both CTAs' epilogues)
+    for (int a = 0; a < 2; ++a) mbar_init(bar_tfull + 8 * a, 2);
+    // one arrival per epilogue warp once it has read its columns of that half (paired: from both CTAs)
     for (int a = 0; a < 4; ++a) mbar_init(bar_tempty + 8 * a, PAIR ? 2 * kEpiWarps : kEpiWarps);
-    mbar_init(bar_drain, PAIR ? 1 : 2);
+    mbar_init(bar_drain, 2);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_mfull + 8 * i, 2 * kMetaWarps);  // paired SPARSE: the metadata warps of both CTAs
+      mbar_init(bar_mempty + 8 * i, 2);              // the commits of the two paired issuers
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -453,15 +515,19 @@ __global__ void __maxnreg__(128)
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // set-up done: from here on global memory may hold the previous grid's results
   pdl_trigger();
   pdl_wait();
 
-  if (warp == 0) {
-    // ------------------------------------------------------- TMA producer
+  if (PAIR && warp == 0) {
+    // ------------------------------------------------------- paired TMA producer
+    // This CTA holds 128 rows of A and the 128-row block 128 r .. 128 r + 127 of the
+    // tile's B (r = this CTA's rank).  One lane issues the stage's copies, A then B in
+    // 64-K boxes of 16 KB, on one barrier: measured on GB300, one warp streams large boxes
+    // grouped per barrier at about the L2's rate.
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
@@ -471,43 +537,31 @@ __global__ void __maxnreg__(128)
       bool ok = true;
       for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
         const Unit t = decode_unit(p, u, CL, rank);
+        const int nb = t.n0 + C::kBRows * (int)rank;  // first column of D this CTA's B block holds
         for (int ks = t.kbeg; ks < t.kend; ++ks) {
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_budget, p.status)) {
+          if (!mbar_wait<true>(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_budget, p.status)) {
             ok = false;
             break;
           }
           const uint32_t fb = bar_full + 8 * stage;
           const uint32_t sA = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t sB = sA + C::kATileBytes;
-          mbar_expect_tx(fb, C::kATileBytes + C::kBTileBytes);  // PAIR's metadata rows come from the metadata warps
-          if constexpr (SPARSE) {
+          mbar_expect_tx(fb, C::kTxBytes);
+          if (SPARSE) {
             tma_load_2d(sA, &tmA, fb, ks * (C::kKStage / 2), t.m0);
-          } else if (p.a_mn) {
+          } else if (p.a_mn) {  // two 64-row (M) boxes of 64 K
             tma_load_2d(sA, &tmA, fb, t.m0, ks * 64);
             tma_load_2d(sA + C::kATileBytes / 2, &tmA, fb, t.m0 + 64, ks * 64);
           } else {
             tma_load_2d(sA, &tmA, fb, ks * 64, t.m0);
           }
-          // B: this CTA fetches 256 / CL rows (columns of D) and, in a cluster, multicasts them;
-          // PAIR: each CTA keeps its own half, which the paired MMA reads in place
-          const int nb = t.n0 + (BN / CL) * (int)rank;
-          const uint32_t sBh = sB + (C::kBTileBytes / CL) * rank;
-          if constexpr (PAIR) {
-            tma_load_2d(sB, &tmB, fb, ks * 128, nb);
-            tma_load_2d(sB + C::kBTileBytes / 2, &tmB, fb, ks * 128 + 64, nb);
-          } else if (!SPARSE && p.b_mn) {
-#pragma unroll
-            for (int h = 0; h < 4 / CL; ++h) {
-              if (CL > 1)
-                tma_load_2d_mc(sBh + 8192 * h, &tmB, fb, nb + 64 * h, ks * 64, (uint16_t)((1u << CL) - 1));
-              else
-                tma_load_2d(sBh + 8192 * h, &tmB, fb, nb + 64 * h, ks * 64);
-            }
+          if (!SPARSE && p.b_mn) {  // two 64-row (N) boxes of 64 K
+            tma_load_2d(sB, &tmB, fb, nb, ks * 64);
+            tma_load_2d(sB + 8192, &tmB, fb, nb + 64, ks * 64);
           } else {
-            if (CL > 1)
-              tma_load_2d_mc(sBh, &tmB, fb, ks * 64, nb, (uint16_t)((1u << CL) - 1));
-            else
-              tma_load_2d(sBh, &tmB, fb, ks * 64, nb);
+#pragma unroll
+            for (int kb = 0; kb < C::kKStage / 64; ++kb)  // 128 rows x 64 K per box
+              tma_load_2d(sB + 16384u * (uint32_t)kb, &tmB, fb, ks * C::kKStage + 64 * kb, nb);
           }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -519,187 +573,331 @@ __global__ void __maxnreg__(128)
       }
       // Drain: every copy into this CTA must have landed before the CTA may exit.
       for (int s = 0; s < C::kStages; ++s)
-        if ((issued >> s) & 1u) {
-          const uint32_t par = (last_parity >> s) & 1u;
-          const long long t0 = clock64();
-          while (!mbar_try(bar_full + 8 * s, par) && clock64() - t0 < p.wait_budget) {
-          }
-        }
+        if ((issued >> s) & 1u) mbar_wait_quiet<true>(bar_full + 8 * s, (last_parity >> s) & 1u, p.wait_budget);
     }
+  } else if (!PAIR && warp == 0) {
+    // ------------------------------------------------------- TMA producer
+    // A bulk tensor copy holds the thread that issues it for several hundred cycles
+    // whatever its size, so the stage's copies (A, and B or this CTA's half of it) are
+    // issued by one lane each, in one instruction.
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+    }
+    const int na = (!SPARSE && p.a_mn) ? 2 : 1;                    // copies of A per stage
+    const int nbc = (!SPARSE && p.b_mn) ? C::kBRows / 64 : 1;       // copies of B per stage
+    const bool copier = lane < na + nbc;
+    const bool is_a = lane < na;
+    const int h = is_a ? lane : lane - na;  // which copy of its operand this lane issues
+    const CUtensorMap* map = is_a ? &tmA : &tmB;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, last_parity = 0;  // per-stage bits for the drain at the end
+    bool ok = true;
+    for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+      const Unit t = decode_unit(p, u, CL, rank);
+      const int nb = t.n0 + C::kBRows * (int)rank;  // B: the tile's 256 rows, or this CTA's half of them
+      for (int ks = t.kbeg; ks < t.kend; ++ks) {
+        if (lane == 0) ok = mbar_wait<PAIR>(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_budget, p.status);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        const uint32_t fb = bar_full + 8 * stage;
+        const uint32_t sA = smem_u32(smem + stage * C::kStageBytes);
+        const uint32_t sB = sA + C::kATileBytes;
+        if (lane == 0) mbar_expect_tx(fb, C::kTxBytes);
+        __syncwarp();
+        if (copier) {
+          uint32_t dst;
+          int x, y;
+          if (is_a) {
+            if (SPARSE) {
+              dst = sA, x = ks * (kKPerStage / 2), y = t.m0;
+            } else if (p.a_mn) {  // two 64-row (M) boxes of 64 K
+              dst = sA + (uint32_t)(C::kATileBytes / 2) * (uint32_t)h, x = t.m0 + 64 * h, y = ks * 64;
+            } else {
+              dst = sA, x = ks * 64, y = t.m0;
+            }
+          } else if (!SPARSE && p.b_mn) {  // 64-row (N) boxes of 64 K
+            dst = sB + 8192 * h, x = nb + 64 * h, y = ks * 64;
+          } else {
+            dst = sB, x = ks * 64, y = nb;
+          }
+          tma_load_2d(dst, map, fb, x, y);
+        }
+        issued |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    // Drain: every copy into this CTA must have landed before the CTA may exit.  (The even
+    // CTA's full barrier also counts relay and metadata arrivals; those all come before
+    // the stage's MMAs, so a consumed stage is complete, and an abort ends within the budget.)
+    if (lane == 0)
+      for (int s = 0; s < C::kStages; ++s)
+        if ((issued >> s) & 1u) mbar_wait_quiet<PAIR>(bar_full + 8 * s, (last_parity >> s) & 1u, p.wait_budget);
   } else if (warp == 1 || warp == kMmaWarpB) {
     if constexpr (PAIR) {
-      // ----------------------------------------------------- paired issuer / relay
-      // The even CTA issues M256 x N256 MMAs over both CTAs' operands and
-      // commits to both CTAs' barriers; the odd CTA's warp 1 relays "stage
-      // ready" (its own TMA bytes and metadata) to the even CTA's full barrier.
-      if (warp == 1 && lane == 0) {
+      if (lane == 0 && leader) {
+        // ----------------------------------------------- paired MMA issuers
+        // An MMA holds its issuing thread until it has nearly completed, so every
+        // instruction a single issuer runs between MMAs (barrier waits, commits,
+        // loop work) would leave the tensor pipe idle.  Two issuers, warp 1 for
+        // columns 0..127 of the tile and warp 14 for columns 128..255 (M256 x N128
+        // MMAs), overlap each other's bookkeeping with MMAs.
+        const int h = warp == 1 ? 0 : 1;
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        if (rank == 0) {
-          const uint32_t idesc = (1u << 4) | ((uint32_t)p.bf16 << 7) | ((uint32_t)p.bf16 << 10) | (1u << 2) |
-                                 ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
-          constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
-          const uint32_t sA0 = smem_u32(smem);
-          // A: 128 rows x 128 B (128B swizzle), 32 B per k-step; B: two boxes of 128 rows x 128 B,
-          // 64 B per k-step within a box; metadata: 16-byte rows, one block of 128 rows per k-step
-          const uint64_t a_desc0 = sdesc(sA0, 16, 1024, kSwizzle128);
-          const uint64_t b_desc0 = sdesc(sA0 + C::kATileBytes, 16, 1024, kSwizzle128);
-          const uint64_t m_desc0 = sdesc(sA0 + C::kATileBytes + C::kBTileBytes, 16, 128, 0);
-          uint32_t mslot = 0, acc_phase = 0;
-          if (p.fault_test) ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);  // runs out
-          for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
-            const Unit t = decode_unit(p, u, CL, rank);
-            if (!mbar_wait<true>(bar_tempty, acc_phase ^ 1, abort_flag, p.wait_budget, p.status)) break;
-            tc_fence_after();
-            int kstep = 0;
-            for (int ks = t.kbeg; ks < t.kend; ++ks) {
-              if (!mbar_wait<true>(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint64_t ad = a_desc0 + (uint64_t)(stage * kStageUnits);
-              const uint64_t bd = b_desc0 + (uint64_t)(stage * kStageUnits);
-              const uint64_t md = m_desc0 + (uint64_t)(stage * kStageUnits);
-              // metadata into the next of four 64-column-aligned slots, then the MMA that reads it
-              const int left = p.num_k_steps - C::kSteps * ks;  // no MMA past K
-              const int steps = left < C::kSteps ? left : C::kSteps;
-              for (int j = 0; j < steps; ++j) {
-                const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * mslot;
-                tc_cp_pair(tmeta, md + (uint64_t)((BM * 16 * j) >> 4));
-                const uint64_t bj = bd + (uint64_t)(((C::kBTileBytes / 2) * (j / 2) + 64 * (j % 2)) >> 4);
-                mma_sparse_pair(tmem, ad + (uint64_t)((32 * j) >> 4), bj, tmeta, idesc, (kstep > 0 || j > 0) ? 1u : 0u);
-                mslot = (mslot + 1) & 3u;
-              }
-              ++kstep;
-              tc_commit_pair(bar_empty + 8 * stage);
-              if (++stage == C::kStages) {
-                stage = 0;
-                phase ^= 1;
-              }
+        const uint32_t idesc = idesc_f16(p.bf16, SPARSE ? 0 : p.a_mn, SPARSE ? 0 : p.b_mn, SPARSE, 2 * BM, BN / 2);
+        constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
+        // Issuer h reads rows 64 h .. 64 h + 63 of each CTA's B block: its accumulator columns
+        // 128 h .. 128 h + 63 are tile columns 64 h .. 64 h + 63 (the even CTA's block) and
+        // 128 h + 64 .. 128 h + 127 are tile columns 128 + 64 h .. 128 + 64 h + 63 (the odd CTA's).
+        const uint32_t sA0 = smem_u32(smem), sB0 = sA0 + C::kATileBytes + 8192u * (uint32_t)h;
+        // Stage-0 descriptors; advancing the 14-bit start field by offset >> 4 moves them.
+        //   SPARSE A: 128 rows x 128 B (128B swizzle), 32 B per k-step;
+        //   SPARSE B: 128 rows x 128 B per 64-K box (boxes 16 KB apart), 64 B per k-step in a box
+        //   DENSE K-major: 128B swizzle, 32 B per K16 step; M/N-major: 64-wide atoms 8 KB apart,
+        //   2048 B per K16 step
+        // SPARSE A rows hold kKStage / 2 compressed values: 64 B (64B swizzle, 8-row groups 512 B
+        // apart) or 128 B (128B swizzle)
+        const uint64_t a_desc0 = (!SPARSE && p.a_mn) ? sdesc(sA0, 8192, 1024, kSwizzle128)
+                                 : (SPARSE && C::kKStage == 64) ? sdesc(sA0, 16, 512, kSwizzle64)
+                                                                : sdesc(sA0, 16, 1024, kSwizzle128);
+        const uint64_t b_desc0 = (!SPARSE && p.b_mn) ? sdesc(sB0, 8192, 1024, kSwizzle128)
+                                                     : sdesc(sB0, 16, 1024, kSwizzle128);
+        const uint32_t a_step = (!SPARSE && p.a_mn) ? (2048 >> 4) : (32 >> 4);
+        const uint32_t b_step = SPARSE ? (64 >> 4) : (p.b_mn ? (2048 >> 4) : (32 >> 4));
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t g2 = 0;  // SPARSE: pairs of k-steps issued; pair g2 reads metadata slot pair g2 % 2
+        if (p.fault_test && h == 0)  // the drain barrier cannot complete before this issuer commits: runs out
+          ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);
+        for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+          const Unit t = decode_unit(p, u, CL, rank);
+          // both CTAs' epilogues have read this issuer's column half of the buffer
+          if (!mbar_wait<true>(bar_tempty + 8 * (2 * acc + h), acc_phase ^ 1, abort_flag, p.wait_budget, p.status))
+            break;
+          tc_fence_after();
+          const uint32_t tacc = tmem + acc * BN + (BN / 2) * h;
+          int kstep = 0;
+          for (int ks = t.kbeg; ks < t.kend; ++ks) {
+            if (!mbar_wait<true>(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
+              ok = false;
+              break;
             }
-            if (!ok) break;
-            tc_commit_pair(bar_tfull);
+            tc_fence_after();
+            const uint64_t ad = a_desc0 + (uint64_t)(stage * kStageUnits);
+            const uint64_t bd = b_desc0 + (uint64_t)(stage * kStageUnits);
+            if constexpr (SPARSE) {
+              // four k-steps per stage, in two pairs; each pair waits for its metadata slot pair
+              // (written by both CTAs' metadata warps) and its completion frees the pair
+              for (int sub = 0; sub < C::kSubs; ++sub, ++g2) {
+                const int k0 = 2 * C::kSubs * ks + 2 * sub;
+                if (k0 >= p.num_k_steps) break;  // no MMA past K
+                if (!mbar_wait<true>(bar_mfull + 8 * (g2 & 1u), (g2 >> 1) & 1u, abort_flag, p.wait_budget,
+                                     p.status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * 2 * (g2 & 1u);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  const int i = 2 * sub + j;  // k-step within the stage
+                  if (j == 1 && k0 + 1 >= p.num_k_steps) break;
+                  mma_sparse_pair(tacc, ad + (uint64_t)(i * a_step),
+                                  bd + (uint64_t)(((16384 >> 4) * (i >> 1)) + b_step * (i & 1)),
+                                  tmeta + kMetaColStride * j, idesc, (kstep > 0 || i > 0) ? 1u : 0u);
+                }
+                tc_commit_both(bar_mempty + 8 * (g2 & 1u));
+              }
+              if (!ok) break;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_dense_pair(tacc, ad + (uint64_t)(j * a_step), bd + (uint64_t)(j * b_step), idesc,
+                               (kstep > 0 || j > 0) ? 1u : 0u);
+            }
+            ++kstep;
+            tc_commit_both(bar_empty + 8 * stage);
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          tc_commit_both(bar_tfull + 8 * acc);
+          if (++acc == C::kAcc) {
+            acc = 0;
             acc_phase ^= 1;
           }
-          tc_commit_pair(bar_drain);
-        } else {
-          for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
-            const Unit t = decode_unit(p, u, CL, rank);
-            for (int ks = t.kbeg; ks < t.kend; ++ks) {
-              if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
-                ok = false;
-                break;
-              }
-              mbar_arrive_remote_relaxed(pair_leader_addr(bar_full + 8 * stage));
-              if (++stage == C::kStages) {
-                stage = 0;
-                phase ^= 1;
-              }
+        }
+        tc_commit_both(bar_drain);
+      } else if (lane == 0 && warp == 1) {
+        // ----------------------------------------------- stage relay (odd CTA)
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        const uint32_t lead_full = peer_addr(bar_full, 0);
+        for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+          const Unit t = decode_unit(p, u, CL, rank);
+          for (int ks = t.kbeg; ks < t.kend; ++ks) {
+            if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_remote_relaxed(lead_full + 8 * stage);
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1;
             }
           }
         }
-        // all paired MMAs have completed before either CTA frees its tensor memory
-        const long long t0 = clock64();
-        while (!mbar_try(bar_drain, 0u) && clock64() - t0 < p.wait_budget) {
-        }
       }
+      // all paired MMAs have completed before either CTA frees its tensor memory
+      if (lane == 0 && warp == 1) mbar_wait_quiet<true>(bar_drain, 0u, p.wait_budget);
     } else {
-    // ------------------------------------------------------- MMA issuers
-    // Two single-thread issuers share every stage: warp 1 computes columns
-    // 0..127 and warp kMmaWarpB columns 128..255 of the tile.  An MMA holds
-    // its issuing thread for about its execution time, so while one issuer
-    // waits, commits and loops, the other one keeps the tensor pipe busy.
-    if (lane == 0) {
-      const uint32_t nhalf = warp == 1 ? 0u : 1u;
-      const uint32_t idesc = idesc_f16(p.bf16, SPARSE ? 0 : p.a_mn, SPARSE ? 0 : p.b_mn, SPARSE);
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      uint32_t mpair = 0;  // SPARSE: metadata slot pair of the current stage (alternates every stage)
-      // Shared-memory descriptors of stage 0.  Advancing a descriptor's start address
-      // (bits 0-13, in 16-byte units) by an offset is adding offset >> 4, since every
-      // shared address fits the 14-bit field.
-      //   SPARSE A: 128 rows x 64 B (64B swizzle, 8-row groups 512 B apart), 32 B per k-step
-      //   SPARSE B: 256 rows x 128 B (128B swizzle), 64 B per k-step
-      //   DENSE A/B K-major: 128B swizzle, 32 B per K16 step; MN-major: 2048 B per K16 step
-      constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
-      // B's second 128 rows (K-major) or second two 64-column atoms (MN-major) start 16 KB in
-      const uint32_t sA0 = smem_u32(smem), sB0 = sA0 + C::kATileBytes + 16384u * nhalf;
-      uint64_t a_desc0, b_desc0;
-      uint32_t a_step = 0, b_step = 0;
-      if constexpr (SPARSE) {
-        a_desc0 = sdesc(sA0, 16, 512, kSwizzle64);
-        b_desc0 = sdesc(sB0, 16, 1024, kSwizzle128);
-      } else {
-        a_desc0 = p.a_mn ? sdesc(sA0, C::kATileBytes / 2, 1024, kSwizzle128) : sdesc(sA0, 16, 1024, kSwizzle128);
-        b_desc0 = p.b_mn ? sdesc(sB0, 8192, 1024, kSwizzle128) : sdesc(sB0, 16, 1024, kSwizzle128);
-        a_step = p.a_mn ? (2048 >> 4) : (32 >> 4);
-        b_step = p.b_mn ? (2048 >> 4) : (32 >> 4);
-      }
-      bool ok = true;
-      if (p.fault_test && nhalf == 0)  // the drain barrier cannot complete before this issuer commits: runs out
-        ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);
-      for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
-        const Unit t = decode_unit(p, u, CL, rank);
-        // this issuer's column half of the buffer has been read by the epilogue
-        if (!mbar_wait(bar_tempty + 8 * (2 * acc + (int)nhalf), acc_phase ^ 1, abort_flag, p.wait_budget, p.status))
-          break;
-        tc_fence_after();
-        const uint32_t tacc = tmem + acc * BN + (BN / 2) * nhalf;
-        int kstep = 0;  // MMA k-steps issued for this tile
-        for (int ks = t.kbeg; ks < t.kend; ++ks) {
-          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
-            ok = false;
+      // ----------------------------------------------------- single-CTA MMA issuers
+      // Two single-thread issuers share every stage: warp 1 computes columns
+      // 0..127 and warp kMmaWarpB columns 128..255 of the tile.  An MMA holds
+      // its issuing thread for about its execution time, so while one issuer
+      // waits, commits and loops, the other one keeps the tensor pipe busy.
+      if (lane == 0) {
+        const uint32_t nhalf = warp == 1 ? 0u : 1u;
+        const uint32_t idesc = idesc_f16(p.bf16, SPARSE ? 0 : p.a_mn, SPARSE ? 0 : p.b_mn, SPARSE, BM, BN / 2);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t mpair = 0;  // SPARSE: metadata slot pair of the current stage (alternates every stage)
+        constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
+        // B's second 128 rows (K-major) or second two 64-column atoms (MN-major) start 16 KB in
+        const uint32_t sA0 = smem_u32(smem), sB0 = sA0 + C::kATileBytes + 16384u * nhalf;
+        uint64_t a_desc0, b_desc0;
+        uint32_t a_step = 0, b_step = 0;
+        if constexpr (SPARSE) {
+          a_desc0 = sdesc(sA0, 16, 512, kSwizzle64);
+          b_desc0 = sdesc(sB0, 16, 1024, kSwizzle128);
+        } else {
+          a_desc0 = p.a_mn ? sdesc(sA0, C::kATileBytes / 2, 1024, kSwizzle128) : sdesc(sA0, 16, 1024, kSwizzle128);
+          b_desc0 = p.b_mn ? sdesc(sB0, 8192, 1024, kSwizzle128) : sdesc(sB0, 16, 1024, kSwizzle128);
+          a_step = p.a_mn ? (2048 >> 4) : (32 >> 4);
+          b_step = p.b_mn ? (2048 >> 4) : (32 >> 4);
+        }
+        bool ok = true;
+        if (p.fault_test && nhalf == 0)  // the drain barrier cannot complete before this issuer commits: runs out
+          ok = mbar_wait(bar_drain, 0, abort_flag, p.wait_budget, p.status);
+        for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+          const Unit t = decode_unit(p, u, CL, rank);
+          // this issuer's column half of the buffer has been read by the epilogue
+          if (!mbar_wait(bar_tempty + 8 * (2 * acc + (int)nhalf), acc_phase ^ 1, abort_flag, p.wait_budget, p.status))
             break;
-          }
           tc_fence_after();
-          // descriptors of this stage: the stage-0 descriptors with the start address advanced
-          const uint64_t ad = a_desc0 + (uint64_t)(stage * kStageUnits);
-          const uint64_t bd = b_desc0 + (uint64_t)(stage * kStageUnits);
-          if constexpr (SPARSE) {
-            // the full barrier also covers this stage's metadata (slots 2 * mpair + j)
-            const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * 2 * mpair;
-            mma_sparse(tacc, ad, bd, tmeta, idesc, kstep > 0 ? 1u : 0u);
-            if (2 * ks + 1 < p.num_k_steps)  // no MMA past K
-              mma_sparse(tacc, ad + (32 >> 4), bd + (64 >> 4), tmeta + kMetaColStride, idesc, 1u);
-            ++kstep;
-            mpair ^= 1u;
-          } else {
+          const uint32_t tacc = tmem + acc * BN + (BN / 2) * nhalf;
+          int kstep = 0;  // MMA k-steps issued for this tile
+          for (int ks = t.kbeg; ks < t.kend; ++ks) {
+            if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = a_desc0 + (uint64_t)(stage * kStageUnits);
+            const uint64_t bd = b_desc0 + (uint64_t)(stage * kStageUnits);
+            if constexpr (SPARSE) {
+              // the full barrier also covers this stage's metadata (slots 2 * mpair + j)
+              const uint32_t tmeta = tmem + kMetaCol + kMetaColStride * 2 * mpair;
+              mma_sparse(tacc, ad, bd, tmeta, idesc, kstep > 0 ? 1u : 0u);
+              if (2 * ks + 1 < p.num_k_steps)  // no MMA past K
+                mma_sparse(tacc, ad + (32 >> 4), bd + (64 >> 4), tmeta + kMetaColStride, idesc, 1u);
+              ++kstep;
+              mpair ^= 1u;
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_dense(tacc, ad + (uint64_t)(j * a_step), bd + (uint64_t)(j * b_step), idesc,
-                        (kstep > 0 || j > 0) ? 1u : 0u);
-            ++kstep;
-          }
-          if (CL > 1)
-            tc_commit_mc(bar_empty + 8 * stage, (uint16_t)((1u << CL) - 1));
-          else
+              for (int j = 0; j < 4; ++j)
+                mma_dense(tacc, ad + (uint64_t)(j * a_step), bd + (uint64_t)(j * b_step), idesc,
+                          (kstep > 0 || j > 0) ? 1u : 0u);
+              ++kstep;
+            }
             tc_commit(bar_empty + 8 * stage);
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1;
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          tc_commit(bar_tfull + 8 * acc);
+          if (++acc == C::kAcc) {
+            acc = 0;
+            acc_phase ^= 1;
           }
         }
-        if (!ok) break;
-        tc_commit(bar_tfull + 8 * acc);
-        if (++acc == C::kAcc) {
-          acc = 0;
-          acc_phase ^= 1;
-        }
+        // Drain: all issued tensor-core work completes before TMEM is freed.
+        tc_commit(bar_drain);
+        mbar_wait_quiet(bar_drain, 0u, p.wait_budget);
       }
-      // Drain: all issued tensor-core work completes before TMEM is freed.
-      tc_commit(bar_drain);
-      const long long t0 = clock64();
-      while (!mbar_try(bar_drain, 0u) && clock64() - t0 < p.wait_budget) {
-      }
-    }
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------- SPARSE metadata
-    if constexpr (SPARSE) {
+    if constexpr (SPARSE && PAIR) {
+      // Paired: k-steps in pairs.  Pair g2 goes to slot pair g2 % 2 once the MMAs of pair
+      // g2 - 2 (the last to read it) have completed; this CTA's 128 rows are written with
+      // tcgen05.st and announced on the even CTA's mfull barrier of the slot pair.
+      const int q = warp & 3;  // TMEM lane quarter this warp may access
+      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + kMetaCol;
+      const uint32_t lead_mfull = peer_addr(bar_mfull, 0);
+      const int S = p.num_k_steps;
+      uint32_t g2 = 0;
+      bool ok = true;
+      for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+        const Unit t = decode_unit(p, u, CL, rank);
+        const uint32_t* src = p.meta + t.m0 + 32 * q + lane;
+        auto word = [&](int kstep) -> uint32_t {
+          return kstep < S ? __ldg(src + (int64_t)kstep * p.meta_slots) : 0x44444444u;  // 0x4: a valid code
+        };
+        const int pb = C::kSubs * t.kbeg, pe = min(C::kSubs * t.kend, (S + 1) / 2);  // pairs of k-steps of this unit
+        uint32_t ring[4][2];  // the words of the next four pairs, loaded ahead of their use
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ring[i][0] = pb + i < pe ? word(2 * (pb + i)) : 0u;
+          ring[i][1] = pb + i < pe ? word(2 * (pb + i) + 1) : 0u;
+        }
+        for (int p0 = pb; ok && p0 < pe; p0 += 4) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int pi = p0 + i;
+            if (pi >= pe) break;
+            const uint32_t w0 = ring[i][0], w1 = ring[i][1];
+            if (pi + 4 < pe) {
+              ring[i][0] = word(2 * (pi + 4));
+              ring[i][1] = word(2 * (pi + 4) + 1);
+            }
+            if (!mbar_wait<true>(bar_mempty + 8 * (g2 & 1u), ((g2 >> 1) & 1u) ^ 1u, abort_flag, p.wait_budget,
+                                 p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t ta = tq + kMetaColStride * 2 * (g2 & 1u);
+            tmem_st1(ta, w0);
+            tmem_st1(ta + kMetaColStride, w1);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (leader)
+                mbar_arrive(bar_mfull + 8 * (g2 & 1u));
+              else
+                mbar_arrive_remote_relaxed(lead_mfull + 8 * (g2 & 1u));
+            }
+            ++g2;
+          }
+        }
+      }
+    } else if constexpr (SPARSE) {
       const int q = warp & 3;  // TMEM lane quarter this warp may access
       const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + kMetaCol;
       const int S = p.num_k_steps;
@@ -712,46 +910,22 @@ __global__ void __maxnreg__(128)
           return kstep < S ? __ldg(src + (int64_t)kstep * p.meta_slots) : 0x44444444u;  // 0x4: a valid code
         };
         // the words of the next four stages are loaded ahead of their use
-        constexpr int KS = C::kSteps;
-        uint32_t ring[4][KS];
+        uint32_t ring[4][2];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int ks = t.kbeg + i;
 #pragma unroll
-          for (int j = 0; j < KS; ++j) ring[i][j] = ks < t.kend ? word(KS * ks + j) : 0u;
+          for (int j = 0; j < 2; ++j) ring[i][j] = ks < t.kend ? word(2 * ks + j) : 0u;
         }
         for (int ks0 = t.kbeg; ok && ks0 < t.kend; ks0 += 4) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int ks = ks0 + i;
             if (ks >= t.kend) break;
-            uint32_t w[KS];
-#pragma unroll
-            for (int j = 0; j < KS; ++j) w[j] = ring[i][j];
+            const uint32_t w0 = ring[i][0], w1 = ring[i][1];
             if (ks + 4 < t.kend) {
-#pragma unroll
-              for (int j = 0; j < KS; ++j) ring[i][j] = word(KS * (ks + 4) + j);
-            }
-            if constexpr (PAIR) {
-              // the words go to the stage's metadata rows (copied to tensor memory by the
-              // paired issuer); the stage buffer was last read by the MMAs of stage g - kStages
-              if (g >= C::kStages) {
-                const int h = g - C::kStages;
-                if (!mbar_wait(bar_empty + 8 * (h % C::kStages), (uint32_t)((h / C::kStages) & 1), abort_flag,
-                               p.wait_budget, p.status)) {
-                  ok = false;
-                  break;
-                }
-              }
-              uint8_t* mrow = smem + (g % C::kStages) * C::kStageBytes + C::kATileBytes + C::kBTileBytes +
-                              (32 * q + lane) * 16;
-#pragma unroll
-              for (int j = 0; j < KS; ++j) *reinterpret_cast<uint32_t*>(mrow + BM * 16 * j) = w[j];
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar_full + 8 * (g % C::kStages));
-              ++g;
-              continue;
+              ring[i][0] = word(2 * (ks + 4));
+              ring[i][1] = word(2 * (ks + 4) + 1);
             }
             // slot pair g & 1 was last read by the MMAs of stage g - 2: wait until that stage is released
             if (g >= 2) {
@@ -764,8 +938,8 @@ __global__ void __maxnreg__(128)
             }
             tc_fence_after();
             const uint32_t ta = tq + kMetaColStride * 2 * (g & 1);
-            tmem_st1(ta, w[0]);
-            tmem_st1(ta + kMetaColStride, w[1]);
+            tmem_st1(ta, w0);
+            tmem_st1(ta + kMetaColStride, w1);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
@@ -775,8 +949,113 @@ __global__ void __maxnreg__(128)
         }
       }
     }
+  } else if (warp >= kEpiWarp0 + kEpiWarps) {
+    // (every warp above the epilogue's has a role above)
+  } else if constexpr (PAIR) {
+    // ------------------------------------------------------- paired epilogue
+    // Warp ew reads TMEM lane quarter q (its 32 rows of this CTA's 128) and, of
+    // each 128-column half, the 64 columns 64 hw .. 64 hw + 63.  Half 0 is read
+    // first and handed back to its issuer, which starts the next tile while
+    // half 1 is read.  Common case (16-bit D, C not read, no K split): all four
+    // 32-column chunks are packed in registers before D is written, so the
+    // accumulator is free after the reads alone.  Column-major D: one 2-byte
+    // store per lane and column, 64 contiguous bytes per warp store; row-major
+    // D: a row's 32 columns as four 16-byte stores.
+    const int ew = warp - kEpiWarp0;
+    const int q = warp & 3;
+    const int hw = ew >> 2;
+    const uint32_t lead_tempty = peer_addr(bar_tempty, 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const bool scale = p.alpha != 1.0f;
+    const bool fast = p.split_k == 1 && p.C == nullptr && p.cd_kind != kCdF32;
+    // chunk c (32 columns): accumulator column 128 (c / 2) + 64 hw + 32 (c % 2), which holds tile
+    // column 128 hw + 32 c (see the issuers); chunks 0, 1 lie in the first issuer's half
+    auto chunk_col = [&](int c) { return 128 * (c >> 1) + 64 * hw + 32 * (c & 1); };
+    auto tile_col = [&](int c) { return 128 * hw + 32 * c; };
+    for (int u = cluster_id; u < p.num_units; u += num_clusters) {
+      const Unit t = decode_unit(p, u, CL, rank);
+      if (!mbar_wait<true>(bar_tfull + 8 * acc, acc_phase, abort_flag, p.wait_budget, p.status)) break;
+      tc_fence_after();
+      const int row = t.m0 + 32 * q + lane;
+      const bool row_ok = row < p.M;
+      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + acc * BN;
+      auto mask_word = [&](int c) -> uint32_t {
+        const int nb = t.n0 + tile_col(c);
+        return (!SPARSE && p.mask != nullptr && row_ok && nb < p.N) ? p.mask[(int64_t)row * p.mask_words + nb / 32]
+                                                                      : 0xFFFFFFFFu;
+      };
+      // hands column half h of the current buffer back to its issuer (on the even CTA)
+      auto release = [&](int h) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(bar_tempty + 8 * (2 * acc + h));
+          else
+            mbar_arrive_remote_relaxed(lead_tempty + 8 * (2 * acc + h));
+        }
+      };
+      if (fast) {
+        uint32_t pk[4][16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // two 32-column loads in flight, packed before the next pair
+          drain64_any<!SPARSE>(p.bf16, scale, tq + chunk_col(2 * h), p.alpha, mask_word(2 * h),
+                               mask_word(2 * h + 1), pk[2 * h], pk[2 * h + 1]);
+          release(h);
+        }
+        if (row_ok) {
+          uint16_t* D16 = reinterpret_cast<uint16_t*>(p.D);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int nb = t.n0 + tile_col(c);
+            if (nb >= p.N) continue;
+            const int cnt = min(32, p.N - nb);
+            if (p.cd_col) {
+              uint16_t* dst = D16 + (int64_t)nb * p.ldd + row;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (2 * j < cnt) dst[(int64_t)(2 * j) * p.ldd] = (uint16_t)(pk[c][j] & 0xFFFFu);
+                if (2 * j + 1 < cnt) dst[(int64_t)(2 * j + 1) * p.ldd] = (uint16_t)(pk[c][j] >> 16);
+              }
+            } else {
+              uint16_t* dst = D16 + (int64_t)row * p.ldd + nb;
+              if (cnt == 32) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  d4[k] = make_uint4(pk[c][4 * k], pk[c][4 * k + 1], pk[c][4 * k + 2], pk[c][4 * k + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  if (2 * j < cnt) dst[2 * j] = (uint16_t)(pk[c][j] & 0xFFFFu);
+                  if (2 * j + 1 < cnt) dst[2 * j + 1] = (uint16_t)(pk[c][j] >> 16);
+                }
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tq + chunk_col(c), v);
+          const uint32_t mword = mask_word(c);
+          const int nb = t.n0 + tile_col(c);
+          if (p.split_k > 1)
+            store_partial_chunk(p, t, tile_col(c), q, lane, v, mword);
+          else if (row_ok && nb < p.N)
+            store_chunk_generic(p, row, nb, v, mword);
+          if (c & 1) release(c >> 1);
+        }
+      }
+      if (++acc == C::kAcc) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
   } else {
-    // ------------------------------------------------------- epilogue
+    // ------------------------------------------------------- single-CTA epilogue
     const int ew = warp - kEpiWarp0;
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     const int hw = ew / 4;  // which 64 columns of each 128-column half
@@ -788,18 +1067,7 @@ __global__ void __maxnreg__(128)
     auto release = [&](int h) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR) {
-          if (h == 1) {  // the paired issuer needs both halves: one arrival, after the second
-            if (rank == 1)  // the accumulator reads completed (wait::ld) before this arrive
-              mbar_arrive_remote_relaxed(pair_leader_addr(bar_tempty + 8 * 2 * acc));
-            else
-              mbar_arrive(bar_tempty + 8 * 2 * acc);
-          }
-        } else {
-          mbar_arrive(bar_tempty + 8 * (2 * acc + h));
-        }
-      }
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * (2 * acc + h));
     };
     for (int u = cluster_id; u < p.num_units; u += num_clusters) {
       const Unit t = decode_unit(p, u, CL, rank);
@@ -835,33 +1103,10 @@ __global__ void __maxnreg__(128)
           const int nb = t.n0 + chunk_col(c);
           uint32_t mword = 0xFFFFFFFFu;
           if (!SPARSE && p.mask != nullptr && row_ok && nb < p.N) mword = p.mask[(int64_t)row * p.mask_words + nb / 32];
-          if (p.split_k > 1) {
-            // fp32 partial of this K split in the tiled order [split][m block][n block][col / 4][128 rows][4]:
-            // for each group of four columns the 32 lanes write 512 contiguous bytes
-            float4* tile = reinterpret_cast<float4*>(p.partial) +
-                           ((int64_t)(t.split * p.num_m_blk + t.m0 / BM) * p.num_n_blk + t.n0 / BN) * (BM * BN / 4);
-            const int c4_0 = chunk_col(c) / 4;
-#pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-              float4 w;
-              w.x = ((mword >> (4 * j4)) & 1u) ? __uint_as_float(v[4 * j4]) * p.alpha : 0.0f;
-              w.y = ((mword >> (4 * j4 + 1)) & 1u) ? __uint_as_float(v[4 * j4 + 1]) * p.alpha : 0.0f;
-              w.z = ((mword >> (4 * j4 + 2)) & 1u) ? __uint_as_float(v[4 * j4 + 2]) * p.alpha : 0.0f;
-              w.w = ((mword >> (4 * j4 + 3)) & 1u) ? __uint_as_float(v[4 * j4 + 3]) * p.alpha : 0.0f;
-              tile[(c4_0 + j4) * BM + 32 * q + lane] = w;
-            }
-          } else if (row_ok && nb < p.N) {
-            const int cnt = min(32, p.N - nb);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j >= cnt) break;
-              float x = ((mword >> j) & 1u) ? __uint_as_float(v[j]) * p.alpha : 0.0f;
-              const int64_t doff = p.cd_col ? (int64_t)(nb + j) * p.ldd + row : (int64_t)row * p.ldd + nb + j;
-              const int64_t coff = p.cd_col ? (int64_t)(nb + j) * p.ldc + row : (int64_t)row * p.ldc + nb + j;
-              if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, coff, p.bf16), x);
-              reinterpret_cast<uint16_t*>(p.D)[doff] = to_cd(x, p.bf16);
-            }
-          }
+          if (p.split_k > 1)
+            store_partial_chunk(p, t, chunk_col(c), q, lane, v, mword);
+          else if (row_ok && nb < p.N)
+            store_chunk_generic(p, row, nb, v, mword);
           if (c & 1) release(c >> 1);  // chunks 0, 1 are this warp's columns of half 0
         }
       }
@@ -919,25 +1164,25 @@ __global__ void __maxnreg__(128)
     else
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
   }
-  if (CL > 1) cluster_sync();  // no CTA leaves while its peer may still signal it
+  if constexpr (PAIR) cluster_sync();  // no CTA leaves while the other may still signal it
 }
 
 // D = beta * C (or 0) when K == 0: no product to accumulate.
-__global__ void scale_c_kernel(const uint16_t* C, uint16_t* D, int64_t rows, int64_t cols, int64_t ldc, int64_t ldd,
-                               float beta, int bf16) {
+__global__ void scale_c_kernel(const void* C, void* D, int64_t rows, int64_t cols, int64_t ldc, int64_t ldd,
+                               float beta, int cd_kind) {
   const int64_t total = rows * cols;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / cols, c = i - r * cols;
-    const float x = C != nullptr ? beta * load_cd(C, r * ldc + c, bf16) : 0.0f;
-    D[r * ldd + c] = to_cd(x, bf16);
+    const float x = C != nullptr ? beta * load_cd(C, r * ldc + c, cd_kind) : 0.0f;
+    store_cd(D, r * ldd + c, x, cd_kind);
   }
 }
 
 // Sum of the K splits' fp32 partials (alpha and mask already applied), plus
 // beta * C, converted to D.
 __global__ void finalize_split_kernel(const float4* __restrict__ part, int splits, int num_m_blk, int num_n_blk,
-                                      int64_t M, int64_t N, const uint16_t* __restrict__ C, uint16_t* __restrict__ D,
-                                      int64_t ldc, int64_t ldd, int cd_col, float beta, int bf16) {
+                                      int64_t M, int64_t N, const void* __restrict__ C, void* __restrict__ D,
+                                      int64_t ldc, int64_t ldd, int cd_col, float beta, int cd_kind) {
   // one thread per four columns of one row, in the tiled order the product wrote
   pdl_trigger();
   pdl_wait();
@@ -960,8 +1205,8 @@ __global__ void finalize_split_kernel(const float4* __restrict__ part, int split
       const int64_t n = n0 + j;
       if (n >= N) break;
       float o = v[j];
-      if (C != nullptr) o = fmaf(beta, load_cd(C, cd_col ? n * ldc + m : m * ldc + n, bf16), o);
-      D[cd_col ? n * ldd + m : m * ldd + n] = to_cd(o, bf16);
+      if (C != nullptr) o = fmaf(beta, load_cd(C, cd_col ? n * ldc + m : m * ldc + n, cd_kind), o);
+      store_cd(D, cd_col ? n * ldd + m : m * ldd + n, o, cd_kind);
     }
   }
 }
@@ -972,9 +1217,8 @@ __global__ void finalize_split_kernel(const float4* __restrict__ part, int split
 // through shared memory and written along D's rows, eight values per store.
 __global__ void __launch_bounds__(256) finalize_split_rows_kernel(const float4* __restrict__ part, int splits,
                                                                   int num_m_blk, int num_n_blk, int64_t M, int64_t N,
-                                                                  const uint16_t* __restrict__ C,
-                                                                  uint16_t* __restrict__ D, int64_t ldc, int64_t ldd,
-                                                                  float beta, int bf16) {
+                                                                  const void* __restrict__ C, void* __restrict__ D,
+                                                                  int64_t ldc, int64_t ldd, float beta, int cd_kind) {
   __shared__ float sm[BM][33];
   pdl_trigger();
   pdl_wait();
@@ -1005,16 +1249,27 @@ __global__ void __launch_bounds__(256) finalize_split_rows_kernel(const float4* 
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       o[j] = sm[r][8 * q + j];
-      if (C != nullptr && n + j < N) o[j] = fmaf(beta, load_cd(C, m * ldc + n + j, bf16), o[j]);
+      if (C != nullptr && n + j < N) o[j] = fmaf(beta, load_cd(C, m * ldc + n + j, cd_kind), o[j]);
     }
-    uint16_t* dst = D + m * ldd + n;
+    if (cd_kind == kCdF32) {
+      float* dst = reinterpret_cast<float*>(D) + m * ldd + n;
+      if (n + 8 <= N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+        reinterpret_cast<float4*>(dst)[0] = make_float4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(o[4], o[5], o[6], o[7]);
+      } else {
+        for (int j = 0; j < 8 && n + j < N; ++j) dst[j] = o[j];
+      }
+      continue;
+    }
+    const int bf16 = cd_kind == kCdBF16;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(D) + m * ldd + n;
     if (n + 8 <= N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
       uint4 w;
       w.x = pack2(o[0], o[1], bf16), w.y = pack2(o[2], o[3], bf16), w.z = pack2(o[4], o[5], bf16),
       w.w = pack2(o[6], o[7], bf16);
       *reinterpret_cast<uint4*>(dst) = w;
     } else {
-      for (int j = 0; j < 8 && n + j < N; ++j) dst[j] = to_cd(o[j], bf16);
+      for (int j = 0; j < 8 && n + j < N; ++j) store_cd(D, m * ldd + n + j, o[j], cd_kind);
     }
   }
 }
@@ -1062,14 +1317,14 @@ int num_sms() {
 
 // The shared-memory opt-in is set once per device (and so never during a
 // stream capture that replays the launches later).
-template <bool SPARSE, int CL, bool PAIR>
+template <bool SPARSE, bool PAIR>
 cudaError_t set_smem_attr() {
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (done_mask.load() & bit) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(spmm_tc_kernel<SPARSE, CL, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(spmm_tc_kernel<SPARSE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<SPARSE, PAIR>::kSmemBytes);
   if (e == cudaSuccess) done_mask.fetch_or(bit);
   return e;
@@ -1077,12 +1332,13 @@ cudaError_t set_smem_attr() {
 
 long long default_budget() { return 1ll << 32; }  // about two seconds at 2 GHz
 
+int cd_kind_of(nm_dtype_t t) { return t == NM_F32 ? kCdF32 : (t == NM_BF16 ? kCdBF16 : kCdF16); }
+
 cudaError_t launch_k0(const SpmmLaunch& a, cudaStream_t s) {
   const nm_spmm_desc_t& d = a.d;
   const int64_t rows = d.order_cd == NM_ROW ? d.M : d.N, cols = d.order_cd == NM_ROW ? d.N : d.M;
-  scale_c_kernel<<<grid_for(rows * cols, 256), 256, 0, s>>>(static_cast<const uint16_t*>(a.C),
-                                                            static_cast<uint16_t*>(a.D), rows, cols, d.ldc, d.ldd,
-                                                            a.beta_f, d.ab_type == NM_BF16);
+  scale_c_kernel<<<grid_for(rows * cols, 256), 256, 0, s>>>(a.C, a.D, rows, cols, d.ldc, d.ldd, a.beta_f,
+                                                            cd_kind_of(d.cd_type));
   return cudaGetLastError();
 }
 
@@ -1098,6 +1354,7 @@ Params base_params(const SpmmLaunch& a) {
   p.split_k = 1;
   p.stages_per_split = p.k_stages;
   p.bf16 = d.ab_type == NM_BF16;
+  p.cd_kind = cd_kind_of(d.cd_type);
   p.alpha = a.alpha_f;
   p.beta = a.beta_f;
   p.C = a.C;
@@ -1105,16 +1362,21 @@ Params base_params(const SpmmLaunch& a) {
   p.ldc = d.ldc;
   p.ldd = d.ldd;
   p.cd_col = d.order_cd == NM_COL;
-  p.tma_store = a.C == nullptr;
+  p.tma_store = a.C == nullptr && p.cd_kind != kCdF32;
   p.status = a.d_status;
   p.wait_budget = default_budget();
   return p;
 }
 
-// Store map over D in 32 x 32 blocks: column-major D (m contiguous) is
-// staged [n][m] unswizzled; row-major D (n contiguous) is staged [m][n] with
-// the 64-byte swizzle so that each lane's 64-byte row write is bank-conflict free.
+// Store map over D in 32 x 32 blocks (single-CTA kernel): column-major D (m
+// contiguous) is staged [n][m] unswizzled; row-major D (n contiguous) is
+// staged [m][n] with the 64-byte swizzle so that each lane's 64-byte row write
+// is bank-conflict free.  Not used (and not encoded) for an fp32 D.
 bool make_store_map(CUtensorMap* map, const nm_spmm_desc_t& d, void* D) {
+  if (d.cd_type == NM_F32) {
+    *map = CUtensorMap{};
+    return true;
+  }
   if (d.order_cd == NM_COL)
     return make_map(map, D, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)d.M, (uint64_t)d.N, (uint64_t)(d.ldd * 2), 32, 32,
                     CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -1122,29 +1384,31 @@ bool make_store_map(CUtensorMap* map, const nm_spmm_desc_t& d, void* D) {
                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <bool SPARSE, int CL, bool PAIR>
+template <bool SPARSE, bool PAIR>
 cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mD, Params p,
                           cudaStream_t s) {
-  if (cudaError_t e = set_smem_attr<SPARSE, CL, PAIR>()) return e;
+  using C = Cfg<SPARSE, PAIR>;
+  constexpr int CL = PAIR ? 2 : 1;
+  if (cudaError_t e = set_smem_attr<SPARSE, PAIR>()) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<SPARSE, PAIR>::kSmemBytes;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = CL > 1 ? 1 : 0;
+  cfg.numAttrs = PAIR ? 1 : 0;
   // persistent grid: as many clusters as can be resident at once (queried once per device)
   static std::atomic<int> resident{0};
   int max_clusters = resident.load();
   if (max_clusters == 0) {
     cfg.gridDim = dim3((unsigned)(num_sms() / CL * CL));
     int n = 0;
-    if (CL > 1) {
-      if (cudaOccupancyMaxActiveClusters(&n, spmm_tc_kernel<SPARSE, CL, PAIR>, &cfg) != cudaSuccess) n = 0;
+    if (PAIR) {
+      if (cudaOccupancyMaxActiveClusters(&n, spmm_tc_kernel<SPARSE, PAIR>, &cfg) != cudaSuccess) n = 0;
       cudaGetLastError();
     }
     max_clusters = n > 0 ? n : num_sms() / CL;
@@ -1153,18 +1417,15 @@ cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const CU
   const int clusters = p.num_units < max_clusters ? p.num_units : max_clusters;
   cfg.gridDim = dim3((unsigned)(clusters * CL));
   // programmatic dependent launch (the kernel waits for the previous grid after its set-up)
-  cudaLaunchAttribute attr2[2];
-  attr2[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr2[0].val.programmaticStreamSerializationAllowed = 1;
-  attr2[1] = attr[0];
-  cfg.attrs = attr2;
-  cfg.numAttrs = CL > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, spmm_tc_kernel<SPARSE, CL, PAIR>, mA, mB, mD, p);
+  attr[PAIR ? 1 : 0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[PAIR ? 1 : 0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = PAIR ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, spmm_tc_kernel<SPARSE, PAIR>, mA, mB, mD, p);
 }
 
-// Pairs of CTAs share the B tile when the row blocks come in pairs (for the
-// sparse product with algo 1 as one paired M256 product per cluster).
-int cluster_for(int num_m_blk) { return (num_m_blk % 2 == 0) ? 2 : 1; }
+// Pairs of CTAs when the row blocks come in pairs, unless the plan asks for
+// single CTAs (algo NM_ALGO_SINGLE).
+bool use_pair(int num_m_blk, int algo) { return num_m_blk % 2 == 0 && algo != NM_ALGO_SINGLE; }
 
 }  // namespace tc
 
@@ -1175,31 +1436,29 @@ cudaError_t spmm_tc_sparse_impl(const SpmmLaunch& a, cudaStream_t s, int fault_t
   Params p = base_params(a);
   p.fault_test = fault_test;
   if (budget > 0) p.wait_budget = budget;
-  const int cl = cluster_for(p.num_m_blk);
+  const bool pair = use_pair(p.num_m_blk, d.algo);
+  const int cl = pair ? 2 : 1;
   p.num_units = (p.num_m_blk / cl) * p.num_n_blk;
   p.num_k_steps = (int)(d.K / 32);
-  // Paired CTAs on request: they halve the shared-memory traffic per SM, but their single
-  // issuer's per-stage work is then exposed; on GB300 the single-CTA kernel with two
-  // issuers was measured faster for the benchmark shapes, so it is the default.
   p.meta = static_cast<const uint32_t*>(a.A_meta);
   p.meta_slots = tc_slots(d.M);
   const CUtensorMapDataType u16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
   CUtensorMap mA, mB, mD;
   const int64_t kc = d.K / 2;  // compressed values per row, packed
-  // paired: 128 dense K per stage, so 64 compressed values (128 B, 128B swizzle) per row of A
-  const bool pair = cl == 2 && d.algo == 1;
-  if (pair) {
+  if (pair) {  // 128 dense K per stage: A boxes of 64 compressed values (128 B rows, 128B swizzle)
     p.k_stages = (int)((d.K + Cfg<true, true>::kKStage - 1) / Cfg<true, true>::kKStage);
     p.stages_per_split = p.k_stages;
   }
-  if (!make_map(&mA, a.A, u16, (uint64_t)kc, (uint64_t)d.M, (uint64_t)(kc * 2), pair ? 64 : 32, BM,
-                pair ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
+  constexpr int kPairAStride = Cfg<true, true>::kKStage / 2;  // compressed values per A row and stage (paired)
+  const int a_box = pair ? kPairAStride : 32;
+  if (!make_map(&mA, a.A, u16, (uint64_t)kc, (uint64_t)d.M, (uint64_t)(kc * 2), (uint32_t)a_box, BM,
+                a_box == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, (uint32_t)(BN / cl),
                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_store_map(&mD, d, a.D))
     return cudaErrorInvalidValue;
-  if (pair) return launch_kernel<true, 2, true>(mA, mB, mD, p, s);
-  return cl == 2 ? launch_kernel<true, 2, false>(mA, mB, mD, p, s) : launch_kernel<true, 1, false>(mA, mB, mD, p, s);
+  if (pair) return launch_kernel<true, true>(mA, mB, mD, p, s);
+  return launch_kernel<true, false>(mA, mB, mD, p, s);
 }
 
 cudaError_t launch_spmm_tc_sparse(const SpmmLaunch& a, cudaStream_t s) { return spmm_tc_sparse_impl(a, s, 0, 0); }
@@ -1248,8 +1507,10 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
     p.partial = static_cast<float*>(a.ws);
     p.tma_store = 0;
   }
-  const int cl = cluster_for(p.num_m_blk);
+  const bool pair = use_pair(p.num_m_blk, d.algo);
+  const int cl = pair ? 2 : 1;
   p.num_units = (p.num_m_blk / cl) * p.num_n_blk * p.split_k;
+  const uint32_t b_rows = (uint32_t)(BN / cl);  // paired: this CTA's 128-row block of B
   const CUtensorMapDataType u16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
   CUtensorMap mA, mB, mD;
   bool ok;
@@ -1264,34 +1525,33 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
       ok = make_map(&mB, a.B, u16, (uint64_t)d.N, (uint64_t)d.K, (uint64_t)(d.ldb * 2), 64, 64,
                     CU_TENSOR_MAP_SWIZZLE_128B);
     else
-      ok = make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, (uint32_t)(BN / cl),
+      ok = make_map(&mB, a.B, u16, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)(d.ldb * 2), 64, b_rows,
                     CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (ok) ok = make_store_map(&mD, d, a.D);
   if (!ok) return cudaErrorInvalidValue;
-  cudaError_t e =
-      cl == 2 ? launch_kernel<false, 2, false>(mA, mB, mD, p, s) : launch_kernel<false, 1, false>(mA, mB, mD, p, s);
+  cudaError_t e = pair ? launch_kernel<false, true>(mA, mB, mD, p, s) : launch_kernel<false, false>(mA, mB, mD, p, s);
   if (e != cudaSuccess || p.split_k == 1) return e;
+  const int cdk = cd_kind_of(d.cd_type);
   if (d.order_cd == NM_ROW) {
     return launch_pdl(finalize_split_rows_kernel, dim3((unsigned)((int64_t)p.num_m_blk * p.num_n_blk * (BN / 32))),
                       dim3(256), 0, s, reinterpret_cast<const float4*>(p.partial), p.split_k, p.num_m_blk,
-                      p.num_n_blk, d.M, d.N, static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.ldc,
-                      d.ldd, a.beta_f, (int)(d.ab_type == NM_BF16));
+                      p.num_n_blk, d.M, d.N, a.C, a.D, d.ldc, d.ldd, a.beta_f, cdk);
   }
   // column-major D: the stored order already runs along D's columns
   const int64_t groups = (int64_t)p.num_m_blk * p.num_n_blk * (BM * BN / 4);
-  finalize_split_kernel<<<grid_for(groups, 256), 256, 0, s>>>(
-      reinterpret_cast<const float4*>(p.partial), p.split_k, p.num_m_blk, p.num_n_blk, d.M, d.N,
-      static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.ldc, d.ldd, d.order_cd == NM_COL, a.beta_f,
-      d.ab_type == NM_BF16);
+  finalize_split_kernel<<<grid_for(groups, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(p.partial), p.split_k,
+                                                              p.num_m_blk, p.num_n_blk, d.M, d.N, a.C, a.D, d.ldc,
+                                                              d.ldd, d.order_cd == NM_COL, a.beta_f, cdk);
   return cudaGetLastError();
 }
 
 }  // namespace nmk
 
-// Test hook (not in include/nm.h): runs the sparse kernel with the MMA lane
-// waiting on a barrier nothing arrives at and a short wait budget, so the
-// bounded-wait path can be exercised without hanging or faulting the GPU.
+// Test entry point (declared in include/nm_testing.h): runs the sparse kernel
+// with the MMA lane waiting on a barrier nothing arrives at and a short wait
+// budget, so the bounded-wait path can be exercised without hanging or
+// faulting the GPU.
 extern "C" nm_status_t nm_test_spmm_wait_timeout(nm_spmm_plan_t plan_unused, const nm_spmm_desc_t* desc,
                                                  const void* A, const void* A_meta, const void* B, void* D,
                                                  int32_t* d_status, long long budget_cycles, nm_stream_t stream) {

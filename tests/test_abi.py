@@ -11,6 +11,7 @@ from structured_sparse_gemm_nm_gb300 import binding as nb
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "nm.h")
+TESTING_HEADER = os.path.join(ROOT, "include", "nm_testing.h")
 
 
 @pytest.fixture(scope="module")
@@ -22,22 +23,26 @@ def lib():
     return nb.lib()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(nm_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_binding_names():
     assert declared_functions() == sorted(nb.EXPORTED)
+    assert declared_functions(TESTING_HEADER) == sorted(nb.TESTING_EXPORTED)
 
 
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", nb.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r" T (nm_[a-z0-9_]+)", out))
-    missing = [f for f in declared_functions() if f not in exported]
+    declared = declared_functions() + declared_functions(TESTING_HEADER)
+    missing = [f for f in declared if f not in exported]
     assert not missing, missing
-    for f in declared_functions():
+    # nothing is exported that a header does not declare
+    assert exported == set(declared), sorted(exported - set(declared))
+    for f in declared:
         assert hasattr(lib, f)
 
 
@@ -164,8 +169,17 @@ def test_plan_validation(lib):
     assert plan_status(**{**dense, "lda": 100}) == nb.NM_ERR_INVALID_ARG
     assert plan_status(**{**dense, "mode": 7}) == nb.NM_ERR_INVALID_ARG
     assert plan_status(M=-1, N=1, K=32, ab_type="f16", cd_type="f16", ldb=32, ldd=8) == nb.NM_ERR_INVALID_ARG
-    assert plan_status(**{**base, "algo": 1}) == nb.NM_OK
-    assert plan_status(**{**base, "algo": 2}) == nb.NM_ERR_INVALID_ARG
+    assert plan_status(**{**base, "algo": nb.NM_ALGO_PAIRED}) == nb.NM_OK
+    assert plan_status(**{**base, "algo": nb.NM_ALGO_SINGLE}) == nb.NM_OK
+    assert plan_status(**{**base, "algo": 3}) == nb.NM_ERR_INVALID_ARG
+    # fp32 C/D from 16-bit inputs on the tensor-core products only
+    assert plan_status(**{**base, "cd_type": "f32"}) == nb.NM_OK
+    assert plan_status(**{**base, "cd_type": "f32", "ldd": 258}) == nb.NM_ERR_MISALIGNED  # 1032 bytes
+    assert plan_status(**{**dense, "cd_type": "f32"}) == nb.NM_OK
+    assert plan_status(**{**base, "n": 8, "m": 32, "meta_layout": nb.NM_META_CANONICAL,
+                          "cd_type": "f32"}) == nb.NM_ERR_UNSUPPORTED
+    assert plan_status(**{**base, "ab_type": "i8", "cd_type": "f32",
+                          "meta_layout": nb.NM_META_CANONICAL}) == nb.NM_ERR_UNSUPPORTED
     units = dict(M=256, N=8, K=1024, mode=nb.NM_SPMM_BLOCK_SPARSE_A, n=1, m=32, ab_type="f16", cd_type="f16",
                  ldb=1024, ldd=256)
     assert plan_status(**units) == nb.NM_OK

@@ -16,6 +16,8 @@ from structured_sparse_gemm_nm_gb300 import inputs
 
 from gpu_util import DEV, assert_gemm_close, bits_of, dev_bytes, ensure_lib, to_dev_bits
 
+TORCH_OUT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
 pytestmark = pytest.mark.gpu
 
 
@@ -55,17 +57,29 @@ SPARSE_CASES = [
     (1024, 4096, 4096, "f16", nb.NM_COL, 1.0, 0.0, True),
     (3072, 16384, 768, "bf16", nb.NM_COL, 1.0, 0.0, True),  # GPT-neo FC1 forward
     (768, 16384, 3072, "bf16", nb.NM_COL, 1.0, 0.0, True),  # GPT-neo FC1 backward (dX)
+    (2304, 16384, 768, "bf16", nb.NM_COL, 1.0, 0.0, True),  # GPT-neo QKV forward
+    (768, 16384, 2304, "bf16", nb.NM_COL, 1.0, 0.0, True),  # GPT-neo QKV backward (dX)
+    (768, 16384, 768, "bf16", nb.NM_COL, 1.0, 0.0, True),   # GPT-neo O forward and dX
+]
+
+# Every case runs with the library's default (paired CTAs when M spans an even number of
+# 128-row blocks, else single CTAs); the even-block cases also run on single CTAs.
+SINGLE_CASES = [c for c in SPARSE_CASES if ((c[0] + 127) // 128) % 2 == 0 and not c[7]] + \
+    [(3072, 16384, 768, "bf16", nb.NM_COL, 1.0, 0.0, True)]
+# an fp32 D (and C) from 16-bit inputs
+F32_CASES = [
+    (256, 4096, 512, "bf16", nb.NM_COL, 1.0, 0.0, False, "f32"),
+    (200, 300, 224, "f16", nb.NM_ROW, 0.5, -1.5, False, "f32"),
+    (384, 264, 640, "bf16", nb.NM_COL, 2.0, 1.0, False, "f32"),
 ]
 
 
-# algo 1: paired CTAs (M256 tiles) where M spans an even number of 128-row blocks
-PAIRED_CASES = [c + (1,) for c in SPARSE_CASES if ((c[0] + 127) // 128) % 2 == 0] + \
-    [(264, 200, 160, "f16", nb.NM_ROW, 1.5, 0.0, False, 1), (256, 72, 96, "bf16", nb.NM_ROW, 2.0, 0.5, False, 1)]
-
-
-@pytest.mark.parametrize("M,N,K,dtype,order_cd,alpha,beta,sampled,algo",
-                         [c + (0,) for c in SPARSE_CASES] + PAIRED_CASES)
-def test_sparse_tc_matches_oracle(M, N, K, dtype, order_cd, alpha, beta, sampled, algo):
+@pytest.mark.parametrize("M,N,K,dtype,order_cd,alpha,beta,sampled,algo,cd",
+                         [c + (nb.NM_ALGO_DEFAULT, None) for c in SPARSE_CASES] +
+                         [c + (nb.NM_ALGO_SINGLE, None) for c in SINGLE_CASES] +
+                         [c[:8] + (a, c[8]) for c in F32_CASES for a in (nb.NM_ALGO_DEFAULT, nb.NM_ALGO_SINGLE)])
+def test_sparse_tc_matches_oracle(M, N, K, dtype, order_cd, alpha, beta, sampled, algo, cd):
+    cd = cd or dtype
     std = 0.02 if K >= 512 else 0.5
     W = inputs.normal((M, K), std, inputs.SEED_W + M, dtype)
     X = inputs.normal((N, K), 1.0, inputs.SEED_X + N, dtype)  # B stored N x K
@@ -73,9 +87,9 @@ def test_sparse_tc_matches_oracle(M, N, K, dtype, order_cd, alpha, beta, sampled
     vals, meta = compress_on_gpu(Wd, M, K, dtype)
     cd_shape = (M, N) if order_cd == nb.NM_ROW else (N, M)
     ld = cd_shape[1]
-    C = inputs.normal(cd_shape, 1.0, inputs.SEED_C, dtype).to(DEV) if beta != 0 else None
-    D = torch.full(cd_shape, float("nan"), dtype=C.dtype if C is not None else Wd.dtype, device=DEV)
-    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type=dtype, cd_type=dtype, ldb=K,
+    C = inputs.normal(cd_shape, 1.0, inputs.SEED_C, "f32" if cd == "f32" else dtype).to(DEV) if beta != 0 else None
+    D = torch.full(cd_shape, float("nan"), dtype=TORCH_OUT[cd], device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type=dtype, cd_type=cd, ldb=K,
                                         ldc=ld if C is not None else 0, ldd=ld, order_cd=order_cd, algo=algo))
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     nb.nm_spmm(plan, alpha, vals, meta, Xd, beta, C, D, d_status=status)
@@ -119,23 +133,35 @@ DENSE_CASES = [
     (104, 200, 96, "bf16", False, 1.0, 0.0),     # ragged
     (136, 72, 1000, "f16", False, 1.0, 0.0),     # K not a multiple of the stage
     (136, 72, 1000, "f16", False, 0.5, -1.0),    # gradient accumulation into C
+    (264, 136, 1000, "bf16", False, 0.5, -1.0),  # ragged, even row blocks, accumulation into C
+    (512, 520, 192, "f16", False, 1.0, 0.0),     # no K split, ragged N
     (3072, 768, 16384, "bf16", True, 1.0, 0.0),  # GPT-neo FC1 dW
     (768, 3072, 16384, "bf16", True, 1.0, 0.0),  # GPT-neo FC2 dW
+    (2304, 768, 16384, "bf16", True, 1.0, 0.0),  # GPT-neo QKV dW
+    (768, 768, 16384, "bf16", True, 1.0, 0.0),   # GPT-neo O dW
 ]
+DENSE_SINGLE = [c for c in DENSE_CASES if not c[4]]
 
 
-@pytest.mark.parametrize("M,N,K,dtype,sampled,alpha,beta", DENSE_CASES)
-def test_masked_weight_grad_matches_oracle(M, N, K, dtype, sampled, alpha, beta):
+@pytest.mark.parametrize("M,N,K,dtype,sampled,alpha,beta,algo,cd",
+                         [c + (nb.NM_ALGO_DEFAULT, None) for c in DENSE_CASES] +
+                         [c + (nb.NM_ALGO_SINGLE, None) for c in DENSE_SINGLE] +
+                         [(256, 512, 4096, "bf16", False, 1.0, 0.0, a, "f32") for a in (0, 2)] +
+                         [(264, 136, 1000, "f16", False, 0.5, -1.0, a, "f32") for a in (0, 2)] +
+                         [(512, 520, 192, "bf16", False, 2.0, 0.0, a, "f32") for a in (0, 2)])
+def test_masked_weight_grad_matches_oracle(M, N, K, dtype, sampled, alpha, beta, algo, cd):
+    cd = cd or dtype
     dY = inputs.normal((K, M), 1.0, inputs.SEED_DY + K, dtype)   # tokens x out
     X = inputs.normal((K, N), 1.0, inputs.SEED_X + K, dtype)     # tokens x in
     W = inputs.normal((M, N), 0.02, inputs.SEED_W, dtype)
     pruned, mask_ref = o.nm_prune(inputs.as_numpy_bits(W), dtype, 2, 4)
     bits = torch.from_numpy(o.mask_to_bits(mask_ref).view(np.int32)).to(DEV)
-    dW = torch.empty((M, N), dtype=dY.dtype, device=DEV)
-    C = inputs.normal((M, N), 1.0, inputs.SEED_C, dtype) if beta != 0 else None
-    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, mode=nb.NM_SPMM_DENSE_MASKED, ab_type=dtype, cd_type=dtype,
+    dW = torch.full((M, N), float("nan"), dtype=TORCH_OUT[cd], device=DEV)
+    C = inputs.normal((M, N), 1.0, inputs.SEED_C, cd) if beta != 0 else None
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, mode=nb.NM_SPMM_DENSE_MASKED, ab_type=dtype, cd_type=cd,
                                         order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_ROW, lda=M, ldb=N,
-                                        ldc=N if C is not None else 0, ldd=N, meta_layout=nb.NM_META_CANONICAL))
+                                        ldc=N if C is not None else 0, ldd=N, meta_layout=nb.NM_META_CANONICAL,
+                                        algo=algo))
     ws_bytes = nb.nm_spmm_plan_workspace(plan)
     ws = dev_bytes(ws_bytes) if ws_bytes else None
     nb.nm_spmm(plan, alpha, dY.to(DEV), bits, X.to(DEV), beta, C.to(DEV) if C is not None else None, dW, ws, ws_bytes)
@@ -145,7 +171,7 @@ def test_masked_weight_grad_matches_oracle(M, N, K, dtype, sampled, alpha, beta)
     Xm = o.decode(inputs.as_numpy_bits(X), dtype)
     ref = alpha * o.masked_weight_grad(dYm[:, rows], Xm, mask_ref[rows])
     if C is not None:
-        ref = ref + beta * o.decode(inputs.as_numpy_bits(C), dtype)[rows]
+        ref = ref + beta * C.double().numpy()[rows]
     assert_gemm_close(dW.cpu().double().numpy()[rows], ref, f"dW {M}x{N}x{K}")
 
 
@@ -219,8 +245,8 @@ def test_k_zero_gives_beta_c():
     assert torch.equal(D, (C.float() * 0.5).half())
 
 
-# one row block (single CTA), two row blocks (cluster of two), two row blocks on paired CTAs
-@pytest.mark.parametrize("M,algo", [(128, 0), (256, 0), (256, 1)])
+# one row block (single CTA), two row blocks on paired CTAs (the default), two on single CTAs
+@pytest.mark.parametrize("M,algo", [(128, 0), (256, 0), (256, 2)])
 def test_bounded_wait_reports_timeout_and_context_survives(M, algo):
     """A wait nothing completes gives up after its budget: NM_ERR_TIMEOUT, no hang, GPU still usable."""
     N, K = 128, 256
