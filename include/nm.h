@@ -228,7 +228,10 @@ nm_status_t nm_prune_block_wise(const void* W, int64_t rows, int64_t cols, int64
  *
  * The first call on a device does a one-time set-up on the current device
  * (it looks up the array's device address, which may load the library's
- * device code); make that first call before any stream capture.  All calls on
+ * device code); make that first call before any stream capture.  The address
+ * is kept for the rest of the process, so the device (or its primary context)
+ * must not be reset after the first call.  Every argument is checked before
+ * that set-up: a rejected call touches no CUDA state.  All calls on
  * a device share the one array and each call clears what must start at zero,
  * so calls must not overlap on the GPU: two calls in flight at the same time
  * (on different streams, or from different host threads) race on the

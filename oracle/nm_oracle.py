@@ -24,7 +24,7 @@ Storage conventions (the same bytes the CUDA path reads and writes):
 * Bit masks: row-major, ``ceil(cols / 32)`` uint32 words per row, bit
   ``c % 32`` of word ``c // 32`` is element ``c``.
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent:
 
 * ties in magnitude go to the lower position (``topk``'s tie order is
   unspecified);

@@ -232,21 +232,32 @@ nm_status_t units_shape(int64_t rows, int64_t cols, int bh, int bw, int64_t* uni
   return NM_OK;
 }
 
-nm_status_t prune_units(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int bh, int bw,
-                        int64_t keep, int abs_of_sum, void* W_out, int64_t ld_out, uint32_t* mask_bits,
-                        int32_t* csr, void* vals, void* workspace, size_t workspace_bytes, nm_stream_t stream) {
+// Every check of a unit selection's arguments except the workspace's; touches no CUDA state.
+nm_status_t check_units_args(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int bh, int bw,
+                             int64_t keep, const void* W_out, int64_t ld_out, const uint32_t* mask_bits,
+                             const int32_t* csr, const void* vals, int64_t* units) {
   if (!is_elem(dtype)) return NM_ERR_INVALID_ARG;
-  int64_t units = 0;
-  if (nm_status_t st = units_shape(rows, cols, bh, bw, &units)) return st;
+  if (nm_status_t st = units_shape(rows, cols, bh, bw, units)) return st;
   if (dtype == NM_BF16) return NM_ERR_UNSUPPORTED;
-  if (keep < 0 || keep > units) return NM_ERR_INVALID_ARG;
+  if (keep < 0 || keep > *units) return NM_ERR_INVALID_ARG;
   if (nm_status_t st = check_matrix(W, rows, cols, ld, dtype, false)) return st;
   if (nm_status_t st = check_matrix(W_out, rows, cols, ld_out, dtype, true)) return st;
   if (W_out == W && W != nullptr && ld_out != ld) return NM_ERR_INVALID_ARG;
   const int64_t es = elem_size(dtype);
   if (!aligned(W, 16) || (ld * es) % 16 || !aligned(W_out, 16) || (W_out != nullptr && (ld_out * es) % 16) ||
-      !aligned(vals, 16) || !aligned(csr, 4) || !aligned(mask_bits, 4) || !aligned(workspace, 16))
+      !aligned(vals, 16) || !aligned(csr, 4) || !aligned(mask_bits, 4))
     return NM_ERR_MISALIGNED;
+  return NM_OK;
+}
+
+nm_status_t prune_units(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int bh, int bw,
+                        int64_t keep, int abs_of_sum, void* W_out, int64_t ld_out, uint32_t* mask_bits,
+                        int32_t* csr, void* vals, void* workspace, size_t workspace_bytes, nm_stream_t stream) {
+  int64_t units = 0;
+  if (nm_status_t st = check_units_args(W, rows, cols, ld, dtype, bh, bw, keep, W_out, ld_out, mask_bits, csr, vals,
+                                        &units))
+    return st;
+  if (!aligned(workspace, 16)) return NM_ERR_MISALIGNED;
   if (units > 0 && (workspace == nullptr || workspace_bytes < nmk::blocks_workspace(units))) return NM_ERR_INVALID_ARG;
   nmk::BlocksLaunch a{};
   a.dt = (int)dtype;
@@ -303,9 +314,11 @@ nm_status_t nm_prune_vector_wise_noalloc(const void* W, int64_t rows, int64_t co
   int64_t units = 0;
   if (nm_status_t st = units_shape(rows, cols, 1, v, &units)) return st;
   if (units > nmk::fixed_scratch_units()) return NM_ERR_UNSUPPORTED;
-  // cheap checks first, so that a rejected call touches no CUDA state
-  if (!is_elem(dtype) || keep < 0 || keep > units || (W == nullptr && units > 0)) return NM_ERR_INVALID_ARG;
-  if (dtype == NM_BF16) return NM_ERR_UNSUPPORTED;
+  // every argument is checked before the one-time address lookup, so that a rejected call touches no
+  // CUDA state
+  if (nm_status_t st = check_units_args(W, rows, cols, ld, dtype, 1, v, keep, W_out, ld_out, mask_bits, csr, vals,
+                                        &units))
+    return st;
   void* scratch = nullptr;
   size_t bytes = 0;
   if (units > 0) {

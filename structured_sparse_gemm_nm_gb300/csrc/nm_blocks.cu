@@ -871,6 +871,7 @@ size_t blocks_workspace(int64_t units) { return ws_layout(units).total; }
 // names a host-side shadow, not device memory.  Its device address is looked
 // up once per device below.
 constexpr int64_t kFixedScratchUnits = int64_t(1) << 19;
+static_assert(kFixedScratchUnits == NM_NOALLOC_MAX_UNITS, "the header advertises the fixed scratch's limit");
 constexpr size_t kFixedScratchBytes = ws_layout(kFixedScratchUnits).total;
 static __device__ __align__(256) uint8_t g_units_scratch[kFixedScratchBytes];
 

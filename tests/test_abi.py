@@ -205,3 +205,30 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(nb, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         nb.lib()
+
+
+def test_noalloc_limit_matches_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define NM_NOALLOC_MAX_UNITS (\d+)", text)
+    assert m and int(m.group(1)) == nb.NM_NOALLOC_MAX_UNITS
+
+
+def test_noalloc_rejects_bad_arguments_before_any_cuda_call(lib):
+    # on a machine without a GPU these return their status without touching CUDA
+    L = nb.lib()
+    args = dict(rows=64, cols=128, ld=128, dtype=nb.NM_F16, v=32, keep=4, score=nb.NM_SCORE_ABS_OF_SUM)
+
+    def call(W=FAKE, W_out=None, ld_out=0, mask=None, csr=None, vals=None, **kw):
+        a = {**args, **kw}
+        return L.nm_prune_vector_wise_noalloc(W, a["rows"], a["cols"], a["ld"], a["dtype"], a["v"], a["keep"],
+                                              a["score"], W_out, ld_out, mask, csr, vals, None)
+
+    assert call(W=FAKE + 8) == nb.NM_ERR_MISALIGNED          # W not 16-byte aligned
+    assert call(ld=132) == nb.NM_ERR_MISALIGNED               # row pitch not a multiple of 16 bytes
+    assert call(vals=FAKE + 4) == nb.NM_ERR_MISALIGNED
+    assert call(csr=FAKE + 2) == nb.NM_ERR_MISALIGNED
+    assert call(W_out=FAKE, ld_out=136) == nb.NM_ERR_INVALID_ARG  # aliases W with another ld
+    assert call(keep=10**6) == nb.NM_ERR_INVALID_ARG
+    assert call(dtype=nb.NM_BF16) == nb.NM_ERR_UNSUPPORTED
+    assert call(v=16) == nb.NM_ERR_UNSUPPORTED
+    assert call(rows=4096, cols=4128, ld=4128) == nb.NM_ERR_UNSUPPORTED  # beyond the fixed scratch

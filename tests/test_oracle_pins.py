@@ -171,6 +171,62 @@ def test_check_counts_violations():
     assert o.nm_check(negz, "f16", 2, 4) == 0
 
 
+def test_transposable_check_counts_columns_by_hand():
+    """cuSPARSELt blog, cusparseLtSpMMAPruneCheck; PyTorch issue #126420 (2:4 in both directions).
+
+    Every row group below holds two nonzeros, so only the column count can flag
+    the matrix: column 0 of the first 4-row block holds three nonzeros, column 5
+    of the second block holds four, column 2 of the second block holds three."""
+    nz = np.array([
+        [1, 1, 0, 0, 0, 0, 1, 1],
+        [1, 1, 0, 0, 1, 1, 0, 0],
+        [1, 0, 1, 0, 0, 0, 1, 1],
+        [0, 0, 1, 1, 1, 1, 0, 0],
+        [0, 0, 1, 1, 0, 1, 1, 0],
+        [1, 0, 1, 0, 0, 1, 0, 1],
+        [0, 1, 1, 0, 1, 1, 0, 0],
+        [1, 1, 0, 0, 0, 1, 1, 0],
+    ], dtype=bool)
+    W = f16_bits(np.where(nz, 1.5, 0.0))
+    assert o.nm_check(W, "f16", 2, 4) == 0                         # rows conform
+    assert o.nm_check(W, "f16", 2, 4, transposable=True) == 3      # three column groups do not
+    # rows and columns change roles under transposition
+    WT = np.ascontiguousarray(W.T)
+    assert o.nm_check(WT, "f16", 2, 4) == 3
+    assert o.nm_check(WT, "f16", 2, 4, transposable=True) == 3
+    # a violation in a row group and in a column group at once counts twice
+    W2 = W.copy()
+    W2[0, 2] = f16_bits(2.0)  # row 0's first group gets a third nonzero; column 2, block 0 gets a third
+    assert o.nm_check(W2, "f16", 2, 4) == 1
+    assert o.nm_check(W2, "f16", 2, 4, transposable=True) == 1 + 4
+
+
+def test_transposable_nan_scores_as_infinity():
+    """A NaN magnitude scores +Inf (the reading that NaN ranks above every number):
+    every pattern that keeps a NaN ties at +Inf and the earliest such pattern wins,
+    even against patterns that keep much larger finite values."""
+    t = np.array([
+        [8.0, 8.0, 0.5, np.nan],
+        [8.0, 8.0, np.nan, 0.5],
+        [1.0, 1.0, 2.0, 2.0],
+        [1.0, 1.0, 2.0, 2.0],
+    ])
+    mask = o.transposable_mask(f16_bits(t), "f16")
+    # Canonical order, row 0's pair outermost: row 0 (0,1) with row 1 (0,1) forces rows 2, 3 to
+    # (2,3) and keeps no NaN; row 1 (0,2) is next, keeps the NaN at (1, 2), and rows 2, 3
+    # complete it as (1,3), (2,3).
+    want = np.zeros((4, 4), dtype=bool)
+    for r, pair in enumerate(((0, 1), (0, 2), (1, 3), (2, 3))):
+        want[r, list(pair)] = True
+    assert (mask == want).all()
+    # the finite-only optimum (what a NaN scored as 0 would give) keeps the four 8s instead
+    finite = np.nan_to_num(t, nan=0.0)
+    assert not (o.transposable_mask(f16_bits(finite), "f16") == want).all()
+    # bf16 follows the same rule
+    bf = (np.asarray(t, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert (o.transposable_mask(bf, "bf16") == want).all()
+
+
 # ------------------------------------------------------------ transposable
 def test_ninety_patterns_by_bitmask_enumeration():
     count = 0
