@@ -326,6 +326,26 @@ nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const
                     const void* beta, const void* C, void* D, void* workspace, size_t workspace_bytes,
                     int32_t* d_status, nm_stream_t stream);
 
+/*
+ * nm_spmm_search - algorithm search at plan time (cuSPARSELt blog, code
+ * example: the algorithm-selection step, and the closing paragraph's
+ * performance auto-tuning, cusparseLtMatmulSearch).  For a plan whose
+ * description asked for NM_ALGO_DEFAULT on a tensor-core product (SPARSE_A
+ * 2:4 F16/BF16 or DENSE_MASKED) with M spanning an even number of 128-row
+ * blocks, runs the product with NM_ALGO_PAIRED and with NM_ALGO_SINGLE on the
+ * given operands, `repeats` timed runs each (after one untimed run), timed
+ * with CUDA events on `stream`, and keeps the faster algorithm in the plan.
+ * Other plans keep their kernel and only report it.  *chosen_algo (nullable,
+ * host) receives the algorithm the plan now uses.
+ * Arguments are those of nm_spmm; D (and the workspace) are overwritten with
+ * the product, and with beta != 0 C must not alias D (NM_ERR_INVALID_ARG).
+ * The call synchronises `stream`.  It changes the plan: do not run it while
+ * another thread uses the same plan.  repeats must be 1..1000.
+ */
+nm_status_t nm_spmm_search(nm_spmm_plan_t plan, const void* alpha, const void* A, const void* A_meta, const void* B,
+                           const void* beta, const void* C, void* D, void* workspace, size_t workspace_bytes,
+                           int repeats, int* chosen_algo, nm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ NM_ALGO_DEFAULT, NM_ALGO_PAIRED, NM_ALGO_SINGLE = 0, 1, 2
 EXPORTED = (
     "nm_status_string", "nm_version", "nm_last_cuda_error", "nm_compressed_size", "nm_prune", "nm_compress", "nm_decompress",
     "nm_check", "nm_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
-    "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm",
+    "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm", "nm_spmm_search",
 )
 # Every symbol include/nm_testing.h declares.
 TESTING_EXPORTED = ("nm_test_spmm_wait_timeout",)
@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
             "nm_spmm_plan_workspace": [vp, ctypes.POINTER(sz)],
             "nm_spmm_plan_destroy": [vp],
             "nm_spmm": [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp],
+            "nm_spmm_search": [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i32, ctypes.POINTER(i32), vp],
             "nm_test_spmm_wait_timeout": [vp, ctypes.POINTER(SpmmDesc), vp, vp, vp, vp, vp, ctypes.c_longlong, vp],
         }
         for name, args in sigs.items():
@@ -261,6 +262,18 @@ def nm_spmm(plan: SpmmPlan, alpha, A, A_meta, B, beta, C, D, workspace=None, wor
     a, b = _scalar(alpha, is_int), _scalar(beta, is_int)
     _check(lib().nm_spmm(plan.handle, ctypes.byref(a), _ptr(A), _ptr(A_meta), _ptr(B), ctypes.byref(b), _ptr(C),
                          _ptr(D), _ptr(workspace), workspace_bytes, _ptr(d_status), _stream(stream)), "nm_spmm")
+
+
+def nm_spmm_search(plan: SpmmPlan, alpha, A, A_meta, B, beta, C, D, workspace=None, workspace_bytes=0, repeats=3,
+                   stream=None) -> int:
+    """Times the candidate algorithms on these operands, keeps the fastest in the plan, returns it."""
+    is_int = plan.desc.ab_type == NM_I8
+    a, b = _scalar(alpha, is_int), _scalar(beta, is_int)
+    chosen = ctypes.c_int()
+    _check(lib().nm_spmm_search(plan.handle, ctypes.byref(a), _ptr(A), _ptr(A_meta), _ptr(B), ctypes.byref(b),
+                                _ptr(C), _ptr(D), _ptr(workspace), workspace_bytes, int(repeats),
+                                ctypes.byref(chosen), _stream(stream)), "nm_spmm_search")
+    return chosen.value
 
 
 def nm_test_spmm_wait_timeout(desc: SpmmDesc, A, A_meta, B, D, d_status, budget_cycles: int, stream=None):

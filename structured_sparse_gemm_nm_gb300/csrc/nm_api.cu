@@ -55,6 +55,7 @@ struct nm_spmm_plan_s {
   int kind;  // 0 tc sparse, 1 tc dense masked, 2 gather n:m, 3 int8 mma.sp, 4 vector/block units
   int split_k;
   size_t ws_bytes;
+  bool searchable;  // created with NM_ALGO_DEFAULT and not yet searched
 };
 
 extern "C" {
@@ -394,6 +395,7 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   p->kind = kind;
   p->split_k = kind == 1 ? nmk::spmm_tc_dense_masked_split(d) : 1;
   p->ws_bytes = kind == 1 ? nmk::spmm_tc_dense_masked_workspace(d, p->split_k) : 0;
+  p->searchable = d.algo == NM_ALGO_DEFAULT;
   *plan = p;
   return NM_OK;
 }
@@ -453,6 +455,57 @@ nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const
     case 4: return from_cuda(nmk::launch_spmm_blocks(a, s));
   }
   return NM_ERR_INVALID_ARG;
+}
+
+nm_status_t nm_spmm_search(nm_spmm_plan_t plan, const void* alpha, const void* A, const void* A_meta, const void* B,
+                           const void* beta, const void* C, void* D, void* workspace, size_t workspace_bytes,
+                           int repeats, int* chosen_algo, nm_stream_t stream) {
+  if (plan == nullptr || alpha == nullptr || beta == nullptr || repeats < 1 || repeats > 1000)
+    return NM_ERR_INVALID_ARG;
+  nm_spmm_desc_t& d = plan->d;
+  const bool tc = plan->kind == 0 || plan->kind == 1;
+  const bool even_blocks = ((d.M + 127) / 128) % 2 == 0;
+  if (!tc || !plan->searchable || !even_blocks || d.M == 0 || d.N == 0 || d.K == 0) {
+    if (chosen_algo != nullptr) *chosen_algo = d.algo;
+    return NM_OK;
+  }
+  float beta_f = 0.0f;
+  std::memcpy(&beta_f, beta, 4);
+  if (beta_f != 0.0f && C == D) return NM_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  nm_status_t st = NM_OK;
+  const int cand[2] = {NM_ALGO_PAIRED, NM_ALGO_SINGLE};
+  float best_ms = 0.0f;
+  int best = NM_ALGO_PAIRED;
+  for (int i = 0; i < 2 && st == NM_OK; ++i) {
+    if (ev[0] == nullptr) {
+      if ((st = from_cuda(cudaEventCreate(&ev[0]))) != NM_OK) break;
+      if ((st = from_cuda(cudaEventCreate(&ev[1]))) != NM_OK) break;
+    }
+    d.algo = cand[i];
+    // one untimed run, then the timed ones
+    if ((st = nm_spmm(plan, alpha, A, A_meta, B, beta, C, D, workspace, workspace_bytes, nullptr, stream)) != NM_OK)
+      break;
+    if ((st = from_cuda(cudaEventRecord(ev[0], s))) != NM_OK) break;
+    for (int r = 0; r < repeats && st == NM_OK; ++r)
+      st = nm_spmm(plan, alpha, A, A_meta, B, beta, C, D, workspace, workspace_bytes, nullptr, stream);
+    if (st != NM_OK) break;
+    if ((st = from_cuda(cudaEventRecord(ev[1], s))) != NM_OK) break;
+    if ((st = from_cuda(cudaEventSynchronize(ev[1]))) != NM_OK) break;
+    float ms = 0.0f;
+    if ((st = from_cuda(cudaEventElapsedTime(&ms, ev[0], ev[1]))) != NM_OK) break;
+    if (i == 0 || ms < best_ms) {
+      best_ms = ms;
+      best = cand[i];
+    }
+  }
+  for (cudaEvent_t e : ev)
+    if (e != nullptr) cudaEventDestroy(e);
+  d.algo = st == NM_OK ? best : NM_ALGO_DEFAULT;
+  if (st == NM_OK) plan->searchable = false;
+  if (chosen_algo != nullptr) *chosen_algo = d.algo;
+  return st;
 }
 
 }  // extern "C"

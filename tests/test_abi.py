@@ -232,3 +232,26 @@ def test_noalloc_rejects_bad_arguments_before_any_cuda_call(lib):
     assert call(dtype=nb.NM_BF16) == nb.NM_ERR_UNSUPPORTED
     assert call(v=16) == nb.NM_ERR_UNSUPPORTED
     assert call(rows=4096, cols=4128, ld=4128) == nb.NM_ERR_UNSUPPORTED  # beyond the fixed scratch
+
+
+def test_search_argument_checks_and_fixed_plans(lib):
+    plan = nb.nm_spmm_plan(nb.make_desc(M=256, N=128, K=128, ab_type="f16", cd_type="f16", ldb=128, ldd=256))
+    with pytest.raises(nb.NmError) as e:
+        nb.nm_spmm_search(plan, 1.0, FAKE, FAKE, FAKE, 0.0, None, FAKE, repeats=0, stream=0)
+    assert e.value.status == nb.NM_ERR_INVALID_ARG
+    with pytest.raises(nb.NmError) as e:  # beta != 0 with C aliasing D
+        nb.nm_spmm_search(plan, 1.0, FAKE, FAKE, FAKE, 0.5, FAKE, FAKE, stream=0)
+    assert e.value.status == nb.NM_ERR_INVALID_ARG
+    plan.destroy()
+    # a plan that fixed its algorithm, an odd number of row blocks, or a CUDA-core product: nothing is
+    # run (no GPU needed) and the plan's own choice is reported
+    fixed = nb.nm_spmm_plan(nb.make_desc(M=256, N=128, K=128, ab_type="f16", cd_type="f16", ldb=128, ldd=256,
+                                         algo=nb.NM_ALGO_SINGLE))
+    assert nb.nm_spmm_search(fixed, 1.0, FAKE, FAKE, FAKE, 0.0, None, FAKE, stream=0) == nb.NM_ALGO_SINGLE
+    odd = nb.nm_spmm_plan(nb.make_desc(M=384, N=128, K=128, ab_type="f16", cd_type="f16", ldb=128, ldd=384))
+    assert nb.nm_spmm_search(odd, 1.0, FAKE, FAKE, FAKE, 0.0, None, FAKE, stream=0) == nb.NM_ALGO_DEFAULT
+    gather = nb.nm_spmm_plan(nb.make_desc(M=256, N=8, K=256, n=8, m=32, ab_type="f16", cd_type="f16", ldb=256,
+                                          ldd=256, meta_layout=nb.NM_META_CANONICAL))
+    assert nb.nm_spmm_search(gather, 1.0, FAKE, FAKE, FAKE, 0.0, None, FAKE, stream=0) == nb.NM_ALGO_DEFAULT
+    for p in (fixed, odd, gather):
+        p.destroy()

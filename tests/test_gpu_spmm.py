@@ -310,3 +310,48 @@ def test_sparse_int8_bit_exact(M, N, K, alpha, beta, order_cd, sampled, kind):
     got = D.cpu().numpy()
     got = got if order_cd == nb.NM_ROW else got.T
     assert np.array_equal(got[rows], ref)
+
+
+@pytest.mark.parametrize("mode", ["sparse", "dense"])
+def test_search_keeps_a_correct_algorithm(mode):
+    """Plan-time search (cuSPARSELt blog: algorithm selection, auto-tuning) picks one of the two
+    tensor-core kernels, and the plan then computes the product correctly."""
+    if mode == "sparse":
+        M, N, K = 768, 4096, 768
+        W = inputs.normal((M, K), 0.02, 31, "bf16")
+        X = inputs.normal((N, K), 1.0, 32, "bf16")
+        vals, meta = compress_on_gpu(W.to(DEV), M, K, "bf16")
+        D = torch.empty((N, M), dtype=torch.bfloat16, device=DEV)
+        plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type="bf16", cd_type="bf16", ldb=K, ldd=M))
+        args = (1.0, vals, meta, X.to(DEV), 0.0, None, D)
+        ws, wsb = None, 0
+    else:
+        M, N, K = 768, 768, 4096
+        dY = inputs.normal((K, M), 1.0, 33, "bf16")
+        X = inputs.normal((K, N), 1.0, 34, "bf16")
+        _, mask_ref = o.nm_prune(inputs.as_numpy_bits(inputs.normal((M, N), 0.02, 35, "bf16")), "bf16", 2, 4)
+        bits = torch.from_numpy(o.mask_to_bits(mask_ref).view(np.int32)).to(DEV)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+        plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, mode=nb.NM_SPMM_DENSE_MASKED, ab_type="bf16",
+                                            cd_type="bf16", order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_ROW,
+                                            lda=M, ldb=N, ldd=N, meta_layout=nb.NM_META_CANONICAL))
+        wsb = nb.nm_spmm_plan_workspace(plan)
+        ws = dev_bytes(wsb) if wsb else None
+        args = (1.0, dY.to(DEV), bits, X.to(DEV), 0.0, None, D)
+    chosen = nb.nm_spmm_search(plan, *args, workspace=ws, workspace_bytes=wsb, repeats=2)
+    assert chosen in (nb.NM_ALGO_PAIRED, nb.NM_ALGO_SINGLE)
+    # searched once: a second call reports the same choice
+    assert nb.nm_spmm_search(plan, *args, workspace=ws, workspace_bytes=wsb, repeats=2) == chosen
+    D.fill_(float("nan"))
+    nb.nm_spmm(plan, *args, workspace=ws, workspace_bytes=wsb)
+    torch.cuda.synchronize()
+    if mode == "sparse":
+        A = o.decode(o.nm_prune(inputs.as_numpy_bits(W), "bf16", 2, 4)[0], "bf16")
+        rows = sample_rows(M, 128, seed=5)
+        ref = o.spmm(1.0, A[rows], o.decode(inputs.as_numpy_bits(X), "bf16").T)
+        assert_gemm_close(D.cpu().double().numpy().T[rows], ref, f"searched sparse (algo {chosen})")
+    else:
+        rows = sample_rows(M, 128, seed=6)
+        ref = o.masked_weight_grad(o.decode(inputs.as_numpy_bits(dY), "bf16")[:, rows],
+                                   o.decode(inputs.as_numpy_bits(X), "bf16"), mask_ref[rows])
+        assert_gemm_close(D.cpu().double().numpy()[rows], ref, f"searched dense (algo {chosen})")
