@@ -158,6 +158,26 @@ nm_status_t nm_prune_transposable(const void* W, int64_t rows, int64_t cols, int
                                   void* W_out, int64_t ld_out, uint32_t* mask_bits, void* vals, void* meta,
                                   void* valsT, void* metaT, nm_meta_layout_t layout, nm_stream_t stream);
 
+/*
+ * nm_sgd_prune_transposable - the optimizer's weight write fused with the
+ * run-time re-prune of a 2:4 training layer (PyTorch issue #126420,
+ * maintainer reply: fast sparsification kernels do run-time sparsity for
+ * training, with the 4x4-tile mask that serves W x and W^T dL/dy).  In one
+ * pass over W (rows x cols, leading dimension ld, F16 or BF16, updated in
+ * place) and its gradient dW (leading dimension ld_grad, same type):
+ *   W[i][j] <- round(W[i][j] + round(round(-lr * dW[i][j])))
+ * where the product and the sum are each rounded to float32 (no fused
+ * multiply-add) and the result is rounded to W's type (round to nearest
+ * even); then the updated W is pruned and compressed exactly as
+ * nm_prune_transposable does (mask_bits, vals/meta, valsT/metaT, each
+ * nullable; W itself stays dense: it is the master copy the next step
+ * updates).  Requirements as nm_prune_transposable, plus dW 4-element
+ * aligned (NM_ERR_MISALIGNED); I8 is NM_ERR_UNSUPPORTED; dW must not alias W.
+ */
+nm_status_t nm_sgd_prune_transposable(void* W, const void* dW, float lr, int64_t rows, int64_t cols, int64_t ld,
+                                      int64_t ld_grad, nm_dtype_t dtype, uint32_t* mask_bits, void* vals, void* meta,
+                                      void* valsT, void* metaT, nm_meta_layout_t layout, nm_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Vector-wise and block-wise pruning (apex PR #1631 "[sparse] update support
  * for arbitrary N:M settings sparse", extension 2: unstructured_vector_wise

@@ -262,6 +262,45 @@ def nm_prune_transposable(W: np.ndarray, dtype: str):
 
 
 # --------------------------------------------------------------------------
+# one training step's weight write with the run-time re-prune
+#   PyTorch issue #126420, maintainer reply: fast sparsification kernels do
+#   run-time sparsity for training; the layer keeps a dense master weight,
+#   updates it, and derives the 4x4-tile 2:4 mask and the compressed forms of
+#   W and W^T from the updated weight.
+#   Reading (the pages give no optimizer): plain SGD, w <- w - lr * g, with
+#   the product and the sum each rounded to float32 and the result rounded to
+#   the weight's type (round to nearest even); finite inputs.
+# --------------------------------------------------------------------------
+def encode(x: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 values -> f16 / bf16 bit patterns, rounded to nearest even (finite values)."""
+    x = np.asarray(x, dtype=np.float32)
+    if dtype == "f16":
+        return x.astype(np.float16).view(np.uint16)
+    if dtype == "bf16":
+        b = x.view(np.uint32).astype(np.uint64)
+        rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+        return rounded.astype(np.uint16)
+    raise ValueError(dtype)
+
+
+def sgd_update(W: np.ndarray, dW: np.ndarray, lr: float, dtype: str) -> np.ndarray:
+    """w + (-lr * g): each operation rounded to float32, the result rounded to the element type."""
+    if dtype not in ("f16", "bf16"):
+        raise ValueError("the update is defined for f16 and bf16 weights")
+    w = decode(W, dtype).astype(np.float32)  # exact
+    g = decode(dW, dtype).astype(np.float32)  # exact
+    nlr = -np.float32(lr)
+    t = (nlr * g).astype(np.float32)
+    return encode((w + t).astype(np.float32), dtype)
+
+
+def sgd_prune_transposable(W: np.ndarray, dW: np.ndarray, lr: float, dtype: str):
+    """The updated dense weight, then its transposable prune: (W_new, pruned, mask, (vals, meta), (valsT, metaT))."""
+    W_new = sgd_update(W, dW, lr, dtype)
+    return (W_new,) + tuple(nm_prune_transposable(W_new, dtype))
+
+
+# --------------------------------------------------------------------------
 # the sparse-dense product
 #   cuSPARSELt blog, GEMM paragraph: D = alpha*op(A)*op(B) + beta*C with A
 #   (M x K) the structured sparse operand, B (K x N), C = D (M x N); FP16 and

@@ -30,7 +30,7 @@ NM_ALGO_DEFAULT, NM_ALGO_PAIRED, NM_ALGO_SINGLE = 0, 1, 2
 # Every symbol include/nm.h declares.
 EXPORTED = (
     "nm_status_string", "nm_version", "nm_last_cuda_error", "nm_compressed_size", "nm_prune", "nm_compress", "nm_decompress",
-    "nm_check", "nm_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
+    "nm_check", "nm_prune_transposable", "nm_sgd_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
     "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm", "nm_spmm_search",
 )
 # Every symbol include/nm_testing.h declares.
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
             "nm_decompress": [vp, vp, i64, i64, i32, i32, i32, i32, vp, i64, vp],
             "nm_check": [vp, i64, i64, i64, i32, i32, i32, i32, vp, vp],
             "nm_prune_transposable": [vp, i64, i64, i64, i32, vp, i64, vp, vp, vp, vp, vp, i32, vp],
+            "nm_sgd_prune_transposable": [vp, vp, ctypes.c_float, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, i32,
+                                          vp],
             "nm_prune_units_workspace": [i64, i64, i32, i32, ctypes.POINTER(sz)],
             "nm_prune_vector_wise": [vp, i64, i64, i64, i32, i32, i64, i32, vp, i64, vp, vp, vp, vp, sz, vp],
             "nm_prune_block_wise": [vp, i64, i64, i64, i32, i32, i32, i64, vp, i64, vp, vp, vp, vp, sz, vp],
@@ -171,6 +173,14 @@ def nm_prune_transposable(W, rows, cols, ld, dtype, W_out=None, ld_out=0, mask_b
     _check(lib().nm_prune_transposable(_ptr(W), rows, cols, ld, _dt(dtype), _ptr(W_out), ld_out, _ptr(mask_bits),
                                        _ptr(vals), _ptr(meta), _ptr(valsT), _ptr(metaT), layout, _stream(stream)),
            "nm_prune_transposable")
+
+
+def nm_sgd_prune_transposable(W, dW, lr, rows, cols, ld, ld_grad, dtype, mask_bits=None, vals=None, meta=None,
+                              valsT=None, metaT=None, layout=NM_META_CANONICAL, stream=None):
+    """W <- W - lr * dW (in place), then W's transposable 2:4 mask and compressed forms, in one pass."""
+    _check(lib().nm_sgd_prune_transposable(_ptr(W), _ptr(dW), float(lr), rows, cols, ld, ld_grad, _dt(dtype),
+                                           _ptr(mask_bits), _ptr(vals), _ptr(meta), _ptr(valsT), _ptr(metaT), layout,
+                                           _stream(stream)), "nm_sgd_prune_transposable")
 
 
 def nm_prune_units_workspace(rows, cols, bh, bw) -> int:

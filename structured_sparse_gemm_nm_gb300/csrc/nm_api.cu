@@ -220,6 +220,44 @@ nm_status_t nm_prune_transposable(const void* W, int64_t rows, int64_t cols, int
   return from_cuda(nmk::launch_transposable(a, (cudaStream_t)stream));
 }
 
+nm_status_t nm_sgd_prune_transposable(void* W, const void* dW, float lr, int64_t rows, int64_t cols, int64_t ld,
+                                      int64_t ld_grad, nm_dtype_t dtype, uint32_t* mask_bits, void* vals, void* meta,
+                                      void* valsT, void* metaT, nm_meta_layout_t layout, nm_stream_t stream) {
+  if (!is_elem(dtype)) return NM_ERR_INVALID_ARG;
+  if (dtype == NM_I8) return NM_ERR_UNSUPPORTED;
+  if (layout != NM_META_CANONICAL && layout != NM_META_TC) return NM_ERR_INVALID_ARG;
+  if (rows % 4 || cols % 4) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_matrix(W, rows, cols, ld, dtype, false)) return st;
+  if (nm_status_t st = check_matrix(dW, rows, cols, ld_grad, dtype, false)) return st;
+  if (dW == W && W != nullptr) return NM_ERR_INVALID_ARG;
+  if (layout == NM_META_TC) {
+    if (meta != nullptr && cols % 32) return NM_ERR_UNSUPPORTED;
+    if (metaT != nullptr && rows % 32) return NM_ERR_UNSUPPORTED;
+  }
+  const uintptr_t es = (uintptr_t)elem_size(dtype);
+  if ((vals && !aligned(vals, es)) || (valsT && !aligned(valsT, es)) || (meta && !aligned(meta, 4)) ||
+      (metaT && !aligned(metaT, 4)) || (mask_bits && !aligned(mask_bits, 4)) || !aligned(dW, 4 * es) ||
+      ld_grad % 4)
+    return NM_ERR_MISALIGNED;
+  nmk::TransposableLaunch a{};
+  a.dt = (int)dtype;
+  a.W = W;
+  a.rows = rows;
+  a.cols = cols;
+  a.ld = ld;
+  a.mask_bits = mask_bits;
+  a.vals = vals;
+  a.meta = meta;
+  a.valsT = valsT;
+  a.metaT = metaT;
+  a.meta_tc = layout == NM_META_TC;
+  a.grad = dW;
+  a.ld_grad = ld_grad;
+  a.lr = lr;
+  a.W_upd = W;
+  return from_cuda(nmk::launch_transposable(a, (cudaStream_t)stream));
+}
+
 // ------------------------------------------------------- vector/block units
 }  // extern "C"
 

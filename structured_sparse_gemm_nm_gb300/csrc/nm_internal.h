@@ -55,6 +55,11 @@ struct TransposableLaunch {
   void* valsT;
   void* metaT;
   int meta_tc;
+  // optional SGD update before the prune: W <- round(W - lr * grad), written back to W_upd (= W)
+  const void* grad;
+  int64_t ld_grad;
+  float lr;
+  void* W_upd;
 };
 cudaError_t launch_transposable(const TransposableLaunch& a, cudaStream_t s);
 

@@ -1302,6 +1302,15 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps are encoded through the driver entry point, which needs a context bound to the
+// calling thread.  A thread that has not yet made a runtime call needing one (a framework's
+// worker thread, for example) has none, so the current device's primary context is bound first.
+cudaError_t bind_context() {
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  return cudaSetDevice(dev);
+}
+
 int num_sms() {
   static std::atomic<int> cached{0};
   int v = cached.load();
@@ -1433,6 +1442,7 @@ cudaError_t spmm_tc_sparse_impl(const SpmmLaunch& a, cudaStream_t s, int fault_t
   using namespace tc;
   const nm_spmm_desc_t& d = a.d;
   if (d.K == 0) return launch_k0(a, s);
+  if (cudaError_t e = bind_context()) return e;
   Params p = base_params(a);
   p.fault_test = fault_test;
   if (budget > 0) p.wait_budget = budget;
@@ -1495,6 +1505,7 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
   using namespace tc;
   const nm_spmm_desc_t& d = a.d;
   if (d.K == 0) return launch_k0(a, s);
+  if (cudaError_t e = bind_context()) return e;
   Params p = base_params(a);
   p.a_mn = d.order_a == NM_COL;
   p.b_mn = d.order_b == NM_ROW;

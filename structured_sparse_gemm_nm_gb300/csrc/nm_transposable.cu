@@ -13,6 +13,7 @@
 // row l/8 and tile column l%8 of the block.  Every packed output word (a
 // 32-bit mask word of one row, a 16-bit metadata word of four groups) then
 // comes from lanes of the same warp and is assembled with shuffles.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "nm_device.cuh"
@@ -109,14 +110,37 @@ __device__ __forceinline__ void store2(int8_t* p, int8_t a, int8_t b) {
   }
 }
 
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Elem<DT>::T* __restrict__ W, int64_t rows,
+// One SGD step on a 16-bit element: w + round(-lr * g), both operations rounded to float32
+// separately (no contraction into a fused multiply-add), then rounded to the element type.
+template <int DT>
+__device__ __forceinline__ uint16_t sgd_elem(uint16_t w, uint16_t g, float nlr) {
+  float wf, gf;
+  if constexpr (DT == kBF16) {
+    wf = __uint_as_float((uint32_t)w << 16);
+    gf = __uint_as_float((uint32_t)g << 16);
+  } else {
+    wf = __half2float(__ushort_as_half(w));
+    gf = __half2float(__ushort_as_half(g));
+  }
+  const float x = __fadd_rn(wf, __fmul_rn(nlr, gf));
+  if constexpr (DT == kBF16)
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  else
+    return __half_as_ushort(__float2half_rn(x));
+}
+
+// UPD: the tile is first updated with one SGD step (W <- W - lr * G, written back to W_upd)
+// and the updated values are pruned and compressed.
+template <int DT, bool VEC, bool UPD>
+__global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Elem<DT>::T* W, int64_t rows,
                                                            int64_t cols, int64_t ld, typename Elem<DT>::T* W_out,
                                                            int64_t ld_out, uint32_t* __restrict__ mask_bits,
                                                            typename Elem<DT>::T* __restrict__ vals,
                                                            void* __restrict__ meta,
                                                            typename Elem<DT>::T* __restrict__ valsT,
-                                                           void* __restrict__ metaT, int meta_tc) {
+                                                           void* __restrict__ metaT, int meta_tc,
+                                                           const typename Elem<DT>::T* __restrict__ G, int64_t ld_g,
+                                                           float nlr, typename Elem<DT>::T* W_upd) {
   using T = typename Elem<DT>::T;
   pdl_trigger();
   pdl_wait();
@@ -140,6 +164,20 @@ __global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Ele
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) v[r][c] = (T)0;
+      }
+    }
+    if constexpr (UPD) {
+      if constexpr (DT != kI8) {
+        if (valid) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            T g[4];
+            load4<VEC>(G + (R0 + r) * ld_g + C0, g);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[r][c] = sgd_elem<DT>(v[r][c], g[c], nlr);
+            store4<VEC>(W_upd + (R0 + r) * ld + C0, v[r]);
+          }
+        }
       }
     }
     float p[4][6];
@@ -304,11 +342,26 @@ cudaError_t transposable_dt(const TransposableLaunch& a, cudaStream_t s) {
   T* W_out = static_cast<T*>(a.W_out);
   T* vals = static_cast<T*>(a.vals);
   T* valsT = static_cast<T*>(a.valsT);
+  const T* G = static_cast<const T*>(a.grad);
+  T* W_upd = static_cast<T*>(a.W_upd);
+  const float nlr = -a.lr;
+  if (G != nullptr) {
+    const bool vecg = vec && (reinterpret_cast<uintptr_t>(G) % a4) == 0 && a.ld_grad % 4 == 0;
+    if (vecg)
+      return launch_pdl(transposable_kernel<DT, true, true>, dim3(grid), dim3(128), 0, s, W, a.rows, a.cols, a.ld,
+                        W_out, a.ld_out, a.mask_bits, vals, a.meta, valsT, a.metaT, a.meta_tc, G, a.ld_grad, nlr,
+                        W_upd);
+    return launch_pdl(transposable_kernel<DT, false, true>, dim3(grid), dim3(128), 0, s, W, a.rows, a.cols, a.ld,
+                      W_out, a.ld_out, a.mask_bits, vals, a.meta, valsT, a.metaT, a.meta_tc, G, a.ld_grad, nlr,
+                      W_upd);
+  }
   if (vec)
-    return launch_pdl(transposable_kernel<DT, true>, dim3(grid), dim3(128), 0, s, W, a.rows, a.cols, a.ld, W_out,
-                      a.ld_out, a.mask_bits, vals, a.meta, valsT, a.metaT, a.meta_tc);
-  return launch_pdl(transposable_kernel<DT, false>, dim3(grid), dim3(128), 0, s, W, a.rows, a.cols, a.ld, W_out,
-                    a.ld_out, a.mask_bits, vals, a.meta, valsT, a.metaT, a.meta_tc);
+    return launch_pdl(transposable_kernel<DT, true, false>, dim3(grid), dim3(128), 0, s, W, a.rows, a.cols, a.ld,
+                      W_out, a.ld_out, a.mask_bits, vals, a.meta, valsT, a.metaT, a.meta_tc, (const T*)nullptr,
+                      (int64_t)0, 0.0f, (T*)nullptr);
+  return launch_pdl(transposable_kernel<DT, false, false>, dim3(grid), dim3(128), 0, s, W, a.rows, a.cols, a.ld,
+                    W_out, a.ld_out, a.mask_bits, vals, a.meta, valsT, a.metaT, a.meta_tc, (const T*)nullptr,
+                    (int64_t)0, 0.0f, (T*)nullptr);
 }
 
 }  // namespace
@@ -318,7 +371,7 @@ cudaError_t launch_transposable(const TransposableLaunch& a, cudaStream_t s) {
   switch (a.dt) {
     case kF16: return transposable_dt<kF16>(a, s);
     case kBF16: return transposable_dt<kBF16>(a, s);
-    default: return transposable_dt<kI8>(a, s);
+    default: return a.grad != nullptr ? cudaErrorInvalidValue : transposable_dt<kI8>(a, s);
   }
 }
 

@@ -255,3 +255,31 @@ def test_search_argument_checks_and_fixed_plans(lib):
     assert nb.nm_spmm_search(gather, 1.0, FAKE, FAKE, FAKE, 0.0, None, FAKE, stream=0) == nb.NM_ALGO_DEFAULT
     for p in (fixed, odd, gather):
         p.destroy()
+
+
+def test_sgd_prune_argument_checks(lib):
+    L = nb.lib()
+
+    def call(W=FAKE, dW=FAKE + 4096, dtype=nb.NM_BF16, rows=64, cols=64, ld=64, ld_grad=64):
+        return L.nm_sgd_prune_transposable(W, dW, 0.1, rows, cols, ld, ld_grad, dtype, None, None, None, None, None,
+                                           nb.NM_META_TC, None)
+
+    assert call(dtype=nb.NM_I8) == nb.NM_ERR_UNSUPPORTED
+    assert call(dW=FAKE) == nb.NM_ERR_INVALID_ARG          # the gradient may not alias the weight
+    assert call(dW=FAKE + 4098) == nb.NM_ERR_MISALIGNED    # four-element alignment of dW
+    assert call(ld_grad=66) == nb.NM_ERR_MISALIGNED
+    assert call(rows=62) == nb.NM_ERR_INVALID_ARG
+    assert call(dW=None) == nb.NM_ERR_INVALID_ARG
+
+
+def test_sparse_layer_validates_before_touching_the_device():
+    import torch
+
+    from structured_sparse_gemm_nm_gb300.sparse_linear import SemiStructuredSparseLinear
+
+    with pytest.raises(ValueError):
+        SemiStructuredSparseLinear(100, 64)          # not a multiple of 32
+    with pytest.raises(ValueError):
+        SemiStructuredSparseLinear(64, 64, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        SemiStructuredSparseLinear(64, 64, device="cpu")  # no CPU path

@@ -355,3 +355,33 @@ def test_search_keeps_a_correct_algorithm(mode):
         ref = o.masked_weight_grad(o.decode(inputs.as_numpy_bits(dY), "bf16")[:, rows],
                                    o.decode(inputs.as_numpy_bits(X), "bf16"), mask_ref[rows])
         assert_gemm_close(D.cpu().double().numpy()[rows], ref, f"searched dense (algo {chosen})")
+
+
+def test_first_call_from_a_new_host_thread():
+    """A thread that has made no CUDA call yet (a framework's worker thread) gets a correct product
+    on its first call: the library binds the device's context before encoding tensor maps."""
+    import threading
+
+    M, N, K = 256, 512, 256
+    W = inputs.normal((M, K), 0.05, 51, "f16").to(DEV)
+    X = inputs.normal((N, K), 1.0, 52, "f16").to(DEV)
+    vals, meta = compress_on_gpu(W, M, K, "f16")
+    D = torch.full((N, M), float("nan"), dtype=torch.float16, device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type="f16", cd_type="f16", ldb=K, ldd=M))
+    torch.cuda.synchronize()
+    errors = []
+
+    def run():
+        try:
+            nb.nm_spmm(plan, 1.0, vals, meta, X, 0.0, None, D, stream=0)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    t = threading.Thread(target=run)
+    t.start()
+    t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    A = o.decode(o.nm_prune(bits_of(W, "f16", (M, K)), "f16", 2, 4)[0], "f16")
+    ref = o.spmm(1.0, A, o.decode(bits_of(X, "f16", (N, K)), "f16").T)
+    assert_gemm_close(D.cpu().double().numpy().T, ref, "first call from a new thread")

@@ -558,3 +558,61 @@ def test_nm_position_metadata_by_hand():
 
 def test_tc_slot_rows_are_whole_tiles():
     assert [o.tc_meta_slot_rows(r) for r in (1, 127, 128, 129, 256, 300)] == [128, 128, 128, 256, 256, 384]
+
+
+# ------------------------------------------------------ fused SGD re-prune
+def bf16_bits(a):
+    """float32 values (exactly representable in bf16) as bf16 bit patterns."""
+    return (np.asarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_sgd_update_hand_cases_f16():
+    # exact: 1 - 0.5 * 1 = 0.5; 3 - 2 * 0.25 = 2.5; -2 - 0.25 * (-8) = 0
+    got1 = o.decode(o.sgd_update(f16_bits([[1.0]]), f16_bits([[1.0]]), 0.5, "f16"), "f16")
+    assert got1[0, 0] == 0.5
+    got2 = o.decode(o.sgd_update(f16_bits([[3.0]]), f16_bits([[0.25]]), 2.0, "f16"), "f16")
+    assert got2[0, 0] == 2.5
+    got3 = o.decode(o.sgd_update(f16_bits([[-2.0]]), f16_bits([[-8.0]]), 0.25, "f16"), "f16")
+    assert got3[0, 0] == 0.0
+    # rounding to nearest even in f16 (spacing 2**-11 just below 1.0):
+    # 1 - 2**-11 is representable; 1 - 2**-12 lies halfway between 1 - 2**-11 (odd) and 1.0 (even) -> 1.0;
+    # 1 - 3 * 2**-13 is nearer 1 - 2**-11
+    one = f16_bits([[1.0, 1.0, 1.0]])
+    g = f16_bits([[2.0 ** -11, 2.0 ** -12, 3 * 2.0 ** -13]])
+    got = o.decode(o.sgd_update(one, g, 1.0, "f16"), "f16")[0]
+    assert got.tolist() == [1.0 - 2.0 ** -11, 1.0, 1.0 - 2.0 ** -11]
+
+
+def test_sgd_update_hand_cases_bf16():
+    # bf16 spacing just below 1.0 is 2**-8: 1 - 2**-9 is a tie -> 1.0 (even); 1 - 3 * 2**-10 -> 1 - 2**-8
+    one = bf16_bits([[1.0, 1.0, 1.0, 4.0]])
+    g = bf16_bits([[2.0 ** -9, 3 * 2.0 ** -10, 2.0 ** -8, 1.0]])
+    got = o.decode(o.sgd_update(one, g, 1.0, "bf16"), "bf16")[0]
+    assert got.tolist() == [1.0, 1.0 - 2.0 ** -8, 1.0 - 2.0 ** -8, 3.0]
+
+
+def test_sgd_update_rounds_the_product_to_float32_first():
+    # lr = 0.1 is not a float32 value: -lr rounds to -0.100000001490116..., and the product with g = 3
+    # rounds to float32 before the sum; the result differs from the exactly rounded w - 0.3 in f16
+    # only through those roundings, which the float32 path reproduces: w = 1 gives 0.7 -> f16 0.7001953125
+    got = o.decode(o.sgd_update(f16_bits([[1.0]]), f16_bits([[3.0]]), 0.1, "f16"), "f16")[0, 0]
+    nlr = -np.float32(0.1)
+    assert np.float32(nlr * np.float32(3.0)) == np.float32(-0.3)  # the product rounds to the float32 nearest -0.3
+    assert got == float(np.float16(np.float32(1.0) + np.float32(-0.3)))
+    assert got == 0.7001953125
+
+
+def test_sgd_update_identities_and_composition():
+    rng = np.random.default_rng(41)
+    W = f16_bits(rng.standard_normal((16, 32)) * 0.05 + 0.01)  # no -0
+    G = f16_bits(rng.standard_normal((16, 32)))
+    assert (o.sgd_update(W, G, 0.0, "f16") == W).all()                     # lr = 0
+    assert (o.sgd_update(W, f16_bits(np.zeros((16, 32))), 0.3, "f16") == W).all()  # zero gradient
+    W_new, pruned, mask, (v, m), (vT, mT) = o.sgd_prune_transposable(W, G, 0.01, "f16")
+    # the prune is that of the updated weight, and it is 2:4 in both directions
+    p2, mask2, (v2, m2), (vT2, mT2) = o.nm_prune_transposable(W_new, "f16")
+    assert (mask == mask2).all() and (v == v2).all() and (vT == vT2).all() and (pruned == p2).all()
+    assert o.nm_check(pruned, "f16", 2, 4, transposable=True) == 0
+    # elementwise: the update is w - lr * g up to the two float32 roundings and the final f16 rounding
+    w, gg, wn = o.decode(W, "f16"), o.decode(G, "f16"), o.decode(W_new, "f16")
+    assert np.abs(wn - (w - 0.01 * gg)).max() <= np.abs(w - 0.01 * gg).max() * 2.0 ** -10
