@@ -121,6 +121,19 @@ nm_status_t nm_compress(const void* W, int64_t rows, int64_t cols, int64_t ld, n
                         int transpose, nm_meta_layout_t layout, void* vals, void* meta, nm_stream_t stream);
 
 /*
+ * nm_prune_compress - nm_prune and nm_compress (transpose = 0) in one pass
+ * over W: every output of either, each nullable (W_out, ld_out, mask_bits;
+ * vals, meta in `layout`), from a single read of W.  Meant for operands pruned
+ * at run time, such as activations (PyTorch issue #126420, maintainer reply:
+ * activation sparsity), where a second pass would double the traffic.
+ * Requirements and errors are those of the two calls; W_out may not alias W
+ * here (NM_ERR_INVALID_ARG).
+ */
+nm_status_t nm_prune_compress(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int n, int m,
+                              void* W_out, int64_t ld_out, uint32_t* mask_bits, nm_meta_layout_t layout, void* vals,
+                              void* meta, nm_stream_t stream);
+
+/*
  * nm_decompress - inverse of nm_compress: scatter the values back to their
  * positions, +0 everywhere else.  rows x cols is the dense shape; W_out has
  * leading dimension ld_out.
@@ -334,7 +347,8 @@ nm_status_t nm_spmm_plan_destroy(nm_spmm_plan_t plan);
  * alpha, beta: HOST pointers to float (F16/BF16) or int32 (I8).  beta == 0
  * means C is not read (it may be NULL).  A: compressed values (SPARSE_A) or
  * dense A (DENSE_MASKED).  A_meta: metadata (SPARSE_A) or the bit mask of
- * D's M x N shape in row-major order (DENSE_MASKED).  C may alias D.
+ * D's M x N shape in row-major order (DENSE_MASKED; NULL = no mask, a plain
+ * dense product).  C may alias D.
  * workspace: device buffer of at least nm_spmm_plan_workspace bytes (NULL if
  * 0).  d_status (nullable, device int32): set to NM_ERR_TIMEOUT if a bounded
  * pipeline wait gave up; it is not cleared by the call.

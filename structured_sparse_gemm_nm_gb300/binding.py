@@ -29,7 +29,8 @@ NM_ALGO_DEFAULT, NM_ALGO_PAIRED, NM_ALGO_SINGLE = 0, 1, 2
 
 # Every symbol include/nm.h declares.
 EXPORTED = (
-    "nm_status_string", "nm_version", "nm_last_cuda_error", "nm_compressed_size", "nm_prune", "nm_compress", "nm_decompress",
+    "nm_status_string", "nm_version", "nm_last_cuda_error", "nm_compressed_size", "nm_prune", "nm_compress",
+    "nm_prune_compress", "nm_decompress",
     "nm_check", "nm_prune_transposable", "nm_sgd_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
     "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm", "nm_spmm_search",
 )
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
             "nm_compressed_size": [i64, i64, i32, i32, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)],
             "nm_prune": [vp, i64, i64, i64, i32, i32, i32, vp, i64, vp, vp],
             "nm_compress": [vp, i64, i64, i64, i32, i32, i32, i32, i32, vp, vp, vp],
+            "nm_prune_compress": [vp, i64, i64, i64, i32, i32, i32, vp, i64, vp, i32, vp, vp, vp],
             "nm_decompress": [vp, vp, i64, i64, i32, i32, i32, i32, vp, i64, vp],
             "nm_check": [vp, i64, i64, i64, i32, i32, i32, i32, vp, vp],
             "nm_prune_transposable": [vp, i64, i64, i64, i32, vp, i64, vp, vp, vp, vp, vp, i32, vp],
@@ -156,6 +158,12 @@ def nm_compress(W, rows, cols, ld, dtype, n, m, transpose=0, layout=NM_META_CANO
                 stream=None):
     _check(lib().nm_compress(_ptr(W), rows, cols, ld, _dt(dtype), n, m, int(transpose), layout, _ptr(vals),
                              _ptr(meta), _stream(stream)), "nm_compress")
+
+
+def nm_prune_compress(W, rows, cols, ld, dtype, n, m, W_out=None, ld_out=0, mask_bits=None,
+                      layout=NM_META_CANONICAL, vals=None, meta=None, stream=None):
+    _check(lib().nm_prune_compress(_ptr(W), rows, cols, ld, _dt(dtype), n, m, _ptr(W_out), ld_out, _ptr(mask_bits),
+                                   layout, _ptr(vals), _ptr(meta), _stream(stream)), "nm_prune_compress")
 
 
 def nm_decompress(vals, meta, rows, cols, dtype, n, m, layout, W_out, ld_out, stream=None):

@@ -149,6 +149,38 @@ nm_status_t nm_compress(const void* W, int64_t rows, int64_t cols, int64_t ld, n
   return from_cuda(nmk::launch_prune(a, (cudaStream_t)stream));
 }
 
+nm_status_t nm_prune_compress(const void* W, int64_t rows, int64_t cols, int64_t ld, nm_dtype_t dtype, int n, int m,
+                              void* W_out, int64_t ld_out, uint32_t* mask_bits, nm_meta_layout_t layout, void* vals,
+                              void* meta, nm_stream_t stream) {
+  if (!is_elem(dtype)) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_nm(n, m)) return st;
+  if (cols % m) return NM_ERR_INVALID_ARG;
+  if (nm_status_t st = check_matrix(W, rows, cols, ld, dtype, false)) return st;
+  if (nm_status_t st = check_matrix(W_out, rows, cols, ld_out, dtype, true)) return st;
+  if (W_out == W && W != nullptr) return NM_ERR_INVALID_ARG;
+  size_t vb = 0, mb = 0;
+  if (nm_status_t st = nm_compressed_size(rows, cols, dtype, n, m, layout, &vb, &mb)) return st;
+  if (mask_bits != nullptr && !aligned(mask_bits, 4)) return NM_ERR_MISALIGNED;
+  if (vals != nullptr && !aligned(vals, (uintptr_t)elem_size(dtype))) return NM_ERR_MISALIGNED;
+  if (meta != nullptr && !aligned(meta, 4)) return NM_ERR_MISALIGNED;
+  nmk::PruneLaunch a{};
+  a.dt = (int)dtype;
+  a.W = W;
+  a.rowsL = rows;
+  a.colsL = cols;
+  a.ld = ld;
+  a.trans = 0;
+  a.n = n;
+  a.m = m;
+  a.W_out = W_out;
+  a.ld_out = ld_out;
+  a.mask_bits = mask_bits;
+  a.vals = vals;
+  a.meta = meta;
+  a.meta_tc = layout == NM_META_TC;
+  return from_cuda(nmk::launch_prune(a, (cudaStream_t)stream));
+}
+
 nm_status_t nm_decompress(const void* vals, const void* meta, int64_t rows, int64_t cols, nm_dtype_t dtype, int n,
                           int m, nm_meta_layout_t layout, void* W_out, int64_t ld_out, nm_stream_t stream) {
   if (!is_elem(dtype)) return NM_ERR_INVALID_ARG;
@@ -465,7 +497,9 @@ nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const
   }
   const bool beta_zero = d.ab_type == NM_I8 ? a.beta_i == 0 : a.beta_f == 0.0f;
   if (d.M == 0 || d.N == 0) return NM_OK;
-  if (A == nullptr || A_meta == nullptr || B == nullptr || D == nullptr) {
+  // DENSE_MASKED may run without a mask (a plain dense product)
+  const bool meta_optional = plan->kind == 1;
+  if (A == nullptr || (A_meta == nullptr && !meta_optional) || B == nullptr || D == nullptr) {
     if (d.K > 0 || D == nullptr) return NM_ERR_INVALID_ARG;
   }
   if (plan->kind == 4 && A_meta == nullptr) return NM_ERR_INVALID_ARG;
