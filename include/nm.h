@@ -310,7 +310,8 @@ typedef struct {
   nm_spmm_mode_t mode;
   int n, m;                     /* sparsity of A (SPARSE_A)                                   */
   nm_dtype_t ab_type;           /* F16, BF16 or I8                                            */
-  nm_dtype_t cd_type;           /* F16/BF16 in: ab_type, or F32 (tensor-core products); I8: I32 */
+  nm_dtype_t cd_type;           /* F16/BF16 in: ab_type, or F32 (tensor-core products);       */
+                                /* I8 in (2:4 sparse product): I32, or I8 (see nm_spmm)       */
   nm_order_t order_a;           /* DENSE_MASKED: ROW = A stored M x K, COL = stored K x M     */
   nm_order_t order_b;           /* ROW = B stored K x N, COL = B stored N x K                 */
   nm_order_t order_cd;          /* ROW = C, D stored M x N, COL = stored N x M                */
@@ -344,7 +345,14 @@ nm_status_t nm_spmm_plan_destroy(nm_spmm_plan_t plan);
 
 /*
  * nm_spmm - run a planned product (cuSPARSELt blog, cusparseLtMatmul).
- * alpha, beta: HOST pointers to float (F16/BF16) or int32 (I8).  beta == 0
+ * alpha, beta: HOST pointers to float (F16/BF16 inputs, or I8 inputs with an I8
+ * output) or int32 (I8 inputs with an I32 output).  With an I8 output the
+ * scales are float: D = saturate(round(alpha * acc + beta * C)) where acc is
+ * the exact int32 accumulation, the int32 -> float conversion, each product
+ * and the sum are rounded to float32, the result is rounded to the nearest
+ * integer (ties to even) and clamped to [-128, 127] (cuSPARSELt blog, key
+ * features: INT8 inputs and output; the pages give no scale, this is the
+ * library's definition).  beta == 0
  * means C is not read (it may be NULL).  A: compressed values (SPARSE_A) or
  * dense A (DENSE_MASKED).  A_meta: metadata (SPARSE_A) or the bit mask of
  * D's M x N shape in row-major order (DENSE_MASKED; NULL = no mask, a plain

@@ -329,6 +329,21 @@ def spmm_int(alpha: int, A: np.ndarray, B: np.ndarray, beta: int = 0, C=None) ->
     return _wrap32(D)
 
 
+def spmm_int8_out(alpha: float, A: np.ndarray, B: np.ndarray, beta: float = 0.0, C=None) -> np.ndarray:
+    """int8 D from int8 A (M x K) and B (K x N) with float scales (cuSPARSELt blog, key features: INT8
+    inputs and output; the scale and rounding are this library's reading, the pages give none):
+    acc exact (int64; it must fit int32), converted to float32 (nearest even), alpha * acc and
+    beta * C each rounded to float32, their sum rounded to float32, then to the nearest integer
+    (ties to even) and clamped to [-128, 127]."""
+    acc = A.astype(np.int64) @ B.astype(np.int64)
+    if np.abs(acc).max(initial=0) >= 2 ** 31:
+        raise ValueError("the int32 accumulator would overflow")
+    x = (np.float32(alpha) * acc.astype(np.float32)).astype(np.float32)
+    if C is not None:
+        x = (x + (np.float32(beta) * C.astype(np.float32)).astype(np.float32)).astype(np.float32)
+    return np.clip(np.rint(x), -128, 127).astype(np.int8)
+
+
 def spmm_compressed(alpha: float, vals, meta, dtype: str, M: int, K: int, n: int, m: int, B, beta=0.0, C=None):
     """The product from the compressed form: decompress, then the dense definition."""
     A = decode(nm_decompress(vals, meta, M, K, n, m), dtype)

@@ -276,7 +276,7 @@ def _scalar(x, is_int: bool):
 
 def nm_spmm(plan: SpmmPlan, alpha, A, A_meta, B, beta, C, D, workspace=None, workspace_bytes=0, d_status=None,
             stream=None):
-    is_int = plan.desc.ab_type == NM_I8
+    is_int = plan.desc.ab_type == NM_I8 and plan.desc.cd_type == NM_I32
     a, b = _scalar(alpha, is_int), _scalar(beta, is_int)
     _check(lib().nm_spmm(plan.handle, ctypes.byref(a), _ptr(A), _ptr(A_meta), _ptr(B), ctypes.byref(b), _ptr(C),
                          _ptr(D), _ptr(workspace), workspace_bytes, _ptr(d_status), _stream(stream)), "nm_spmm")
@@ -285,7 +285,7 @@ def nm_spmm(plan: SpmmPlan, alpha, A, A_meta, B, beta, C, D, workspace=None, wor
 def nm_spmm_search(plan: SpmmPlan, alpha, A, A_meta, B, beta, C, D, workspace=None, workspace_bytes=0, repeats=3,
                    stream=None) -> int:
     """Times the candidate algorithms on these operands, keeps the fastest in the plan, returns it."""
-    is_int = plan.desc.ab_type == NM_I8
+    is_int = plan.desc.ab_type == NM_I8 and plan.desc.cd_type == NM_I32
     a, b = _scalar(alpha, is_int), _scalar(beta, is_int)
     chosen = ctypes.c_int()
     _check(lib().nm_spmm_search(plan.handle, ctypes.byref(a), _ptr(A), _ptr(A_meta), _ptr(B), ctypes.byref(b),

@@ -408,7 +408,8 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   if (d.algo != NM_ALGO_DEFAULT && d.algo != NM_ALGO_PAIRED && d.algo != NM_ALGO_SINGLE) return NM_ERR_INVALID_ARG;
   if (!is_elem(d.ab_type)) return NM_ERR_INVALID_ARG;
   const bool fp = d.ab_type != NM_I8;
-  if (fp ? (d.cd_type != d.ab_type && d.cd_type != NM_F32) : d.cd_type != NM_I32) return NM_ERR_UNSUPPORTED;
+  if (fp ? (d.cd_type != d.ab_type && d.cd_type != NM_F32) : (d.cd_type != NM_I32 && d.cd_type != NM_I8))
+    return NM_ERR_UNSUPPORTED;
   if ((d.order_a != NM_ROW && d.order_a != NM_COL) || (d.order_b != NM_ROW && d.order_b != NM_COL) ||
       (d.order_cd != NM_ROW && d.order_cd != NM_COL))
     return NM_ERR_INVALID_ARG;
@@ -453,8 +454,9 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
   } else {
     return NM_ERR_INVALID_ARG;
   }
-  // an fp32 C/D only on the tensor-core products
+  // an fp32 C/D only on the tensor-core products, an int8 C/D only on the int8 sparse product
   if (fp && d.cd_type == NM_F32 && kind != 0 && kind != 1) return NM_ERR_UNSUPPORTED;
+  if (!fp && d.cd_type == NM_I8 && kind != 3) return NM_ERR_UNSUPPORTED;
   // The tensor-core and int8 kernels write D (and read C) in 16-byte pieces;
   // the CUDA-core GEMV kernels (kinds 2 and 4) access them element by element.
   const bool cd_wide = kind != 2 && kind != 4;
@@ -488,14 +490,15 @@ nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const
   const nm_spmm_desc_t& d = plan->d;
   nmk::SpmmLaunch a{};
   a.d = d;
-  if (d.ab_type == NM_I8) {
+  const bool int_scalars = d.ab_type == NM_I8 && d.cd_type == NM_I32;
+  if (int_scalars) {
     std::memcpy(&a.alpha_i, alpha, 4);
     std::memcpy(&a.beta_i, beta, 4);
   } else {
     std::memcpy(&a.alpha_f, alpha, 4);
     std::memcpy(&a.beta_f, beta, 4);
   }
-  const bool beta_zero = d.ab_type == NM_I8 ? a.beta_i == 0 : a.beta_f == 0.0f;
+  const bool beta_zero = int_scalars ? a.beta_i == 0 : a.beta_f == 0.0f;
   if (d.M == 0 || d.N == 0) return NM_OK;
   // DENSE_MASKED may run without a mask (a plain dense product)
   const bool meta_optional = plan->kind == 1;

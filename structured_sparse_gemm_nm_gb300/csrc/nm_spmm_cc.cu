@@ -230,11 +230,14 @@ __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// OUT8: int8 D (and C) with float scales: D = saturate(rne(alpha * acc + beta * C)), each
+// product and the sum rounded to float32; otherwise int32 D = alpha * acc + beta * C modulo 2^32.
+template <bool OUT8>
 __global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const int8_t* __restrict__ A, const uint16_t* __restrict__ meta,
-                                                      const int8_t* __restrict__ B, const int32_t* __restrict__ C,
-                                                      int32_t* __restrict__ D, int M, int N, int K, int64_t ldb,
+                                                      const int8_t* __restrict__ B, const void* __restrict__ Cv,
+                                                      void* __restrict__ Dv, int M, int N, int K, int64_t ldb,
                                                       int64_t ldc, int64_t ldd, int cd_col, int32_t alpha,
-                                                      int32_t beta) {
+                                                      int32_t beta, float alpha_f, float beta_f) {
   extern __shared__ uint4 smem4[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(smem4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -330,7 +333,6 @@ __global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const int8_t* __restric
     }
   }
   cp_wait<0>();
-  // epilogue: D = alpha * acc + beta * C in int32 arithmetic modulo 2^32
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -340,9 +342,19 @@ __global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const int8_t* __restric
         const int row = m0 + wm * 32 + mt * 16 + g + 8 * (r >> 1);
         const int col = n0 + wn * 64 + nt * 8 + 2 * t + (r & 1);
         if (row >= M || col >= N) continue;
-        uint32_t x = (uint32_t)alpha * (uint32_t)acc[mt][nt][r];
-        if (C != nullptr) x += (uint32_t)beta * (uint32_t)C[cd_col ? (int64_t)col * ldc + row : (int64_t)row * ldc + col];
-        D[cd_col ? (int64_t)col * ldd + row : (int64_t)row * ldd + col] = (int32_t)x;
+        const int64_t coff = cd_col ? (int64_t)col * ldc + row : (int64_t)row * ldc + col;
+        const int64_t doff = cd_col ? (int64_t)col * ldd + row : (int64_t)row * ldd + col;
+        if constexpr (OUT8) {
+          float x = __fmul_rn(alpha_f, __int2float_rn(acc[mt][nt][r]));
+          if (Cv != nullptr) x = __fadd_rn(x, __fmul_rn(beta_f, (float)static_cast<const int8_t*>(Cv)[coff]));
+          const int q = __float2int_rn(x);
+          static_cast<int8_t*>(Dv)[doff] = (int8_t)max(-128, min(127, q));
+        } else {
+          // D = alpha * acc + beta * C in int32 arithmetic modulo 2^32
+          uint32_t x = (uint32_t)alpha * (uint32_t)acc[mt][nt][r];
+          if (Cv != nullptr) x += (uint32_t)beta * (uint32_t)static_cast<const int32_t*>(Cv)[coff];
+          static_cast<int32_t*>(Dv)[doff] = (int32_t)x;
+        }
       }
 }
 
@@ -352,20 +364,29 @@ cudaError_t launch_spmm_i8(const SpmmLaunch& a, cudaStream_t s) {
   const nm_spmm_desc_t& d = a.d;
   if (d.K == 0) return cudaErrorInvalidValue;  // rejected by the plan
   const int smem = I8_STAGES * I8_STAGE_BYTES;
+  const bool out8 = d.cd_type == NM_I8;
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(done_mask.load() & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(spmm_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(spmm_i8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(spmm_i8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     done_mask.fetch_or(bit);
   }
   dim3 grid((unsigned)((d.N + I8_BN - 1) / I8_BN), (unsigned)((d.M + I8_BM - 1) / I8_BM));
-  spmm_i8_kernel<<<grid, 256, smem, s>>>(static_cast<const int8_t*>(a.A), static_cast<const uint16_t*>(a.A_meta),
-                                          static_cast<const int8_t*>(a.B), static_cast<const int32_t*>(a.C),
-                                          static_cast<int32_t*>(a.D), (int)d.M, (int)d.N, (int)d.K, d.ldb, d.ldc,
-                                          d.ldd, d.order_cd == NM_COL, a.alpha_i, a.beta_i);
+  if (out8)
+    spmm_i8_kernel<true><<<grid, 256, smem, s>>>(static_cast<const int8_t*>(a.A), static_cast<const uint16_t*>(a.A_meta),
+                                                 static_cast<const int8_t*>(a.B), a.C, a.D, (int)d.M, (int)d.N,
+                                                 (int)d.K, d.ldb, d.ldc, d.ldd, d.order_cd == NM_COL, 0, 0, a.alpha_f,
+                                                 a.beta_f);
+  else
+    spmm_i8_kernel<false><<<grid, 256, smem, s>>>(static_cast<const int8_t*>(a.A), static_cast<const uint16_t*>(a.A_meta),
+                                                  static_cast<const int8_t*>(a.B), a.C, a.D, (int)d.M, (int)d.N,
+                                                  (int)d.K, d.ldb, d.ldc, d.ldd, d.order_cd == NM_COL, a.alpha_i,
+                                                  a.beta_i, 0.0f, 0.0f);
   return cudaGetLastError();
 }
 

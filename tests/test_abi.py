@@ -180,6 +180,10 @@ def test_plan_validation(lib):
                           "cd_type": "f32"}) == nb.NM_ERR_UNSUPPORTED
     assert plan_status(**{**base, "ab_type": "i8", "cd_type": "f32",
                           "meta_layout": nb.NM_META_CANONICAL}) == nb.NM_ERR_UNSUPPORTED
+    # an int8 output on the int8 sparse product only
+    assert plan_status(**{**base, "ab_type": "i8", "cd_type": "i8", "meta_layout": nb.NM_META_CANONICAL}) == nb.NM_OK
+    assert plan_status(**{**base, "ab_type": "i8", "cd_type": "i8", "n": 8, "m": 32,
+                          "meta_layout": nb.NM_META_CANONICAL}) == nb.NM_ERR_UNSUPPORTED
     units = dict(M=256, N=8, K=1024, mode=nb.NM_SPMM_BLOCK_SPARSE_A, n=1, m=32, ab_type="f16", cd_type="f16",
                  ldb=1024, ldd=256)
     assert plan_status(**units) == nb.NM_OK

@@ -385,3 +385,38 @@ def test_first_call_from_a_new_host_thread():
     A = o.decode(o.nm_prune(bits_of(W, "f16", (M, K)), "f16", 2, 4)[0], "f16")
     ref = o.spmm(1.0, A, o.decode(bits_of(X, "f16", (N, K)), "f16").T)
     assert_gemm_close(D.cpu().double().numpy().T, ref, "first call from a new thread")
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta,order_cd", [
+    (128, 64, 128, 0.5, 0.0, nb.NM_COL),
+    (200, 144, 192, 0.03125, 0.75, nb.NM_ROW),   # ragged, with C
+    (1024, 4096, 1024, 0.01, 0.0, nb.NM_COL),    # BERT-shaped
+])
+def test_sparse_int8_output_bit_exact(M, N, K, alpha, beta, order_cd):
+    """INT8 inputs and output (cuSPARSELt blog, key features) with this library's float scale and rounding."""
+    W = inputs.uniform_int8((M, K), 61 + M)
+    X = inputs.uniform_int8((N, K), 62 + N)
+    vb, mb = nb.nm_compressed_size(M, K, "i8", 2, 4, nb.NM_META_CANONICAL)
+    vals, meta = dev_bytes(vb), dev_bytes(mb)
+    nb.nm_compress(W.to(DEV), M, K, K, "i8", 2, 4, 0, nb.NM_META_CANONICAL, vals, meta)
+    cd_shape = (M, N) if order_cd == nb.NM_ROW else (N, M)
+    ld = (cd_shape[1] + 15) // 16 * 16
+    C = inputs.uniform_int8(cd_shape, 63) if beta else None
+    Cp = None
+    if C is not None:
+        Cp = torch.zeros((cd_shape[0], ld), dtype=torch.int8)
+        Cp[:, :cd_shape[1]] = C
+        Cp = Cp.to(DEV)
+    D = torch.full((cd_shape[0], ld), 99, dtype=torch.int8, device=DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type="i8", cd_type="i8", ldb=K, ldc=ld if beta else 0,
+                                        ldd=ld, order_cd=order_cd, meta_layout=nb.NM_META_CANONICAL))
+    nb.nm_spmm(plan, alpha, vals, meta, X.to(DEV), beta, Cp, D)
+    torch.cuda.synchronize()
+    A = o.nm_prune(W.numpy(), "i8", 2, 4)[0]
+    Cm = None
+    if C is not None:
+        Cm = C.numpy() if order_cd == nb.NM_ROW else C.numpy().T
+    ref = o.spmm_int8_out(alpha, A, X.numpy().T, beta, Cm)
+    got = D.cpu().numpy()[:, :cd_shape[1]]
+    got = got if order_cd == nb.NM_ROW else got.T
+    assert np.array_equal(got, ref)

@@ -616,3 +616,25 @@ def test_sgd_update_identities_and_composition():
     # elementwise: the update is w - lr * g up to the two float32 roundings and the final f16 rounding
     w, gg, wn = o.decode(W, "f16"), o.decode(G, "f16"), o.decode(W_new, "f16")
     assert np.abs(wn - (w - 0.01 * gg)).max() <= np.abs(w - 0.01 * gg).max() * 2.0 ** -10
+
+
+def test_int8_output_scale_round_and_saturate():
+    A = np.array([[1, 2, 0, 0], [127, 127, 0, 0], [-128, -128, 0, 0]], dtype=np.int8)
+    B = np.array([[1, 3], [1, -1], [5, 5], [7, 7]], dtype=np.int8)
+    # acc = [[3, 1], [254, 254], [-256, -256]]
+    assert (A.astype(np.int64) @ B.astype(np.int64)).tolist() == [[3, 1], [254, 254], [-256, -256]]
+    got = o.spmm_int8_out(0.5, A, B)
+    # 1.5 -> 2 and 0.5 -> 0 (ties to even); 127 stays; -128 saturates from -128 exactly
+    assert got.tolist() == [[2, 0], [127, 127], [-128, -128]]
+    got = o.spmm_int8_out(1.0, A, B)
+    assert got.tolist() == [[3, 1], [127, 127], [-128, -128]]  # saturation both ways
+    C = np.array([[10, -10], [0, 0], [100, 100]], dtype=np.int8)
+    got = o.spmm_int8_out(0.25, A, B, beta=0.5, C=C)
+    # 0.75 + 5 = 5.75 -> 6; 0.25 - 5 = -4.75 -> -5; 63.5 -> 64 (tie to even); -64 + 50 = -14
+    assert got.tolist() == [[6, -5], [64, 64], [-14, -14]]
+    # above 2**24 the int32 -> float32 conversion rounds to even: 127 * 127 * 1041 = 16790289 -> 16790288,
+    # and 16790288 * 2**-19 = 32.0250244... -> 32
+    A2 = np.full((1, 1041), 127, dtype=np.int8)
+    B2 = np.full((1041, 1), 127, dtype=np.int8)
+    assert float(np.float32(127 * 127 * 1041)) == 16790288.0
+    assert o.spmm_int8_out(2.0 ** -19, A2, B2)[0, 0] == 32
