@@ -340,6 +340,30 @@ def time_launch(torch, fn, flush, reps=10, warm=3):
 L2_BYTES = 132_000_000  # 126 MiB of L2 on GB300
 
 
+def cusparselt_ms(torch, nb, A, B_t, flush, dt="bf16"):
+    """cuSPARSELt's own 2:4 product (torch's private binding, run as a black box) of the 2:4-pruned
+    A (M x K, pruned here by this library's nm_prune) and B_t (N x K, so B = B_t^T), D written N x M
+    as this library's plans write it; the library's best algorithm id from its own search.  Returns
+    (ms, note), ms None where the installed build has no cuSPARSELt."""
+    try:
+        if not torch.backends.cusparselt.is_available():
+            return None, "cuSPARSELt not available in this torch build"
+        M, K = A.shape
+        Ap = torch.empty_like(A)
+        nb.nm_prune(A, M, K, K, dt, 2, 4, Ap, K)
+        Ac = torch._cslt_compress(Ap)
+        try:
+            alg = int(torch._cslt_sparse_mm_search(Ac, B_t.t(), transpose_result=True))
+        except Exception:
+            alg = 0
+        fn = lambda: torch._cslt_sparse_mm(Ac, B_t.t(), transpose_result=True, alg_id=alg)  # noqa: E731
+        fn()
+        torch.cuda.synchronize()
+        return time_launch(torch, fn, flush), f"torch._cslt_sparse_mm, cuSPARSELt {torch.backends.cusparselt.version()}, alg {alg}"
+    except Exception as e:  # a comparator only: the row keeps its own measurement
+        return None, f"cuSPARSELt failed: {type(e).__name__}: {str(e)[:120]}"
+
+
 def copies_for(bytes_per_launch: int) -> int:
     """Independent problem copies whose inputs and outputs together exceed twice the L2."""
     return max(4, min(32, -(-2 * L2_BYTES // max(1, bytes_per_launch))))
@@ -399,6 +423,12 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
         rows[f"S6_dx_{name}"] = {"shape_MNK": [i, wl.T, o], "ms": t_dx, "tflops": f / t_dx / 1e9,
                                  "frac_sparse_peak": f / t_dx / 1e9 / sparse_peak,
                                  "cublas_dense_tflops": f / t_cub_dx / 1e9, "speedup_vs_cublas": t_cub_dx / t_dx}
+        for key, A, Bt, t_own in ((f"S5_fwd_{name}", Wd, L["X"], t_fwd),
+                                  (f"S6_dx_{name}", Wd.t().contiguous(), L["dY"], t_dx)):
+            t_sl, note = cusparselt_ms(torch, nb, A, Bt, flush)
+            rows[key]["cusparselt_tflops"] = f / t_sl / 1e9 if t_sl else None
+            rows[key]["speedup_vs_cusparselt"] = t_sl / t_own if t_sl else None
+            rows[key]["cusparselt_note"] = note
         t_cub_dw = time_launch(torch, lambda: torch.matmul(L["dY"].t(), L["X"]), flush)
         rows[f"S7_dw_{name}"] = {"shape_MNK": [o, i, wl.T], "ms": t_dw, "tflops": f / t_dw / 1e9,
                                  "frac_dense_peak": f / t_dw / 1e9 / dense_peak,
@@ -555,9 +585,12 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
         t = time_launch(torch, lambda: nb.nm_spmm(plan, 1.0, vals, meta, Xb, 0.0, None, D), flush)
         tc = time_launch(torch, lambda: torch.matmul(Xb, Wb.t()), flush)
         f = 2.0 * Mb * Nb * Kb
+        t_sl, note = cusparselt_ms(torch, nb, Wb, Xb, flush, "f16")
         rows[f"S5_bert_large_{lname}_{Mb}x{Nb}x{Kb}_f16"] = {
             "ms": t, "tflops": f / t / 1e9, "frac_sparse_peak": f / t / 1e9 / sparse_peak,
-            "cublas_dense_tflops": f / tc / 1e9, "speedup_vs_cublas": tc / t}
+            "cublas_dense_tflops": f / tc / 1e9, "speedup_vs_cublas": tc / t,
+            "cusparselt_tflops": f / t_sl / 1e9 if t_sl else None,
+            "speedup_vs_cusparselt": t_sl / t if t_sl else None, "cusparselt_note": note}
         plan.destroy()
     # the same shapes in int8 (INT32 accumulation), against torch's int8 matmul of the dense
     # pruned weight where the installed build has one

@@ -32,8 +32,8 @@
 //                commit or loop step of one issuer would leave the tensor pipe
 //                idle; two issuers overlap each other's.  Issuer h reads rows
 //                64 h .. 64 h + 63 of each CTA's B block.
-//                odd CTA: warp 1 relays each completed stage to the even
-//                CTA's `full` barrier
+//                (odd CTA: no issuer; its copies complete on the even CTA's
+//                `full` barrier)
 //   warps 2..5   SPARSE metadata: per pair of k-steps, each warp writes one
 //                32-bit code word per lane (row) and k-step with tcgen05.st
 //                into a pair of the four 64-column-aligned tensor-memory slots
@@ -204,6 +204,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           dst),
       "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// Paired form: the copy lands in this CTA's shared memory and completes its bytes on a
+// barrier that may sit in the other CTA of the pair (here: the even CTA's `full` barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(cluster_bar)
       : "memory");
 }
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
@@ -481,10 +491,11 @@ __global__ void __maxnreg__(128)
     for (int s = 0; s < C::kStages; ++s) {
       uint32_t full_count;
       // single CTA: the producer's expect_tx arrival and (SPARSE) one arrival per metadata warp
-      // once it has written the stage's metadata slot pair; paired: one expect_tx arrival per
-      // producer warp, and on the even CTA the odd CTA's relay
+      // once it has written the stage's metadata slot pair; paired: the even CTA's producer arms
+      // its barrier with both CTAs' bytes, and both CTAs' copies complete on it (the odd CTA's
+      // `full` barriers stay unused)
       if constexpr (PAIR)
-        full_count = 1 + (leader ? 1 : 0);
+        full_count = 1;
       else
         full_count = 1 + (SPARSE ? kMetaWarps : 0);
       mbar_init(bar_full + 8 * s, full_count);
@@ -527,8 +538,14 @@ __global__ void __maxnreg__(128)
     // This CTA holds 128 rows of A and the 128-row block 128 r .. 128 r + 127 of the
     // tile's B (r = this CTA's rank).  One lane issues the stage's copies, A then B in
     // 64-K boxes of 16 KB, on one barrier: measured on GB300, one warp streams large boxes
-    // grouped per barrier at about the L2's rate.
+    // grouped per barrier at about the L2's rate.  Both CTAs' copies complete on the even
+    // CTA's `full` barrier, which its producer arms with the bytes of both; the odd CTA's
+    // bytes may land before that arming, which only makes the transaction count
+    // transiently negative within the phase.  The odd CTA issues a stage only after its
+    // `empty` barrier shows the previous phase consumed, so its bytes never reach an
+    // earlier phase.
     if (lane == 0) {
+      const uint32_t lead_full = peer_addr(bar_full, 0);
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
       int stage = 0;
@@ -543,25 +560,25 @@ __global__ void __maxnreg__(128)
             ok = false;
             break;
           }
-          const uint32_t fb = bar_full + 8 * stage;
+          const uint32_t fb = lead_full + 8 * stage;
           const uint32_t sA = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t sB = sA + C::kATileBytes;
-          mbar_expect_tx(fb, C::kTxBytes);
+          if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * C::kTxBytes);
           if (SPARSE) {
-            tma_load_2d(sA, &tmA, fb, ks * (C::kKStage / 2), t.m0);
+            tma_load_2d_pair(sA, &tmA, fb, ks * (C::kKStage / 2), t.m0);
           } else if (p.a_mn) {  // two 64-row (M) boxes of 64 K
-            tma_load_2d(sA, &tmA, fb, t.m0, ks * 64);
-            tma_load_2d(sA + C::kATileBytes / 2, &tmA, fb, t.m0 + 64, ks * 64);
+            tma_load_2d_pair(sA, &tmA, fb, t.m0, ks * 64);
+            tma_load_2d_pair(sA + C::kATileBytes / 2, &tmA, fb, t.m0 + 64, ks * 64);
           } else {
-            tma_load_2d(sA, &tmA, fb, ks * 64, t.m0);
+            tma_load_2d_pair(sA, &tmA, fb, ks * 64, t.m0);
           }
           if (!SPARSE && p.b_mn) {  // two 64-row (N) boxes of 64 K
-            tma_load_2d(sB, &tmB, fb, nb, ks * 64);
-            tma_load_2d(sB + 8192, &tmB, fb, nb + 64, ks * 64);
+            tma_load_2d_pair(sB, &tmB, fb, nb, ks * 64);
+            tma_load_2d_pair(sB + 8192, &tmB, fb, nb + 64, ks * 64);
           } else {
 #pragma unroll
             for (int kb = 0; kb < C::kKStage / 64; ++kb)  // 128 rows x 64 K per box
-              tma_load_2d(sB + 16384u * (uint32_t)kb, &tmB, fb, ks * C::kKStage + 64 * kb, nb);
+              tma_load_2d_pair(sB + 16384u * (uint32_t)kb, &tmB, fb, ks * C::kKStage + 64 * kb, nb);
           }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -571,9 +588,13 @@ __global__ void __maxnreg__(128)
           }
         }
       }
-      // Drain: every copy into this CTA must have landed before the CTA may exit.
+      // Drain: every copy into this CTA must have landed before the CTA may exit.  The even
+      // CTA waits for its `full` barriers (both CTAs' bytes); the odd CTA, whose copies
+      // complete there, for its `empty` barriers: a stage is released only after the MMAs
+      // that read it, which waited for all its bytes.
       for (int s = 0; s < C::kStages; ++s)
-        if ((issued >> s) & 1u) mbar_wait_quiet<true>(bar_full + 8 * s, (last_parity >> s) & 1u, p.wait_budget);
+        if ((issued >> s) & 1u)
+          mbar_wait_quiet<true>((leader ? bar_full : bar_empty) + 8 * s, (last_parity >> s) & 1u, p.wait_budget);
     }
   } else if (!PAIR && warp == 0) {
     // ------------------------------------------------------- TMA producer
@@ -632,9 +653,9 @@ __global__ void __maxnreg__(128)
         }
       }
     }
-    // Drain: every copy into this CTA must have landed before the CTA may exit.  (The even
-    // CTA's full barrier also counts relay and metadata arrivals; those all come before
-    // the stage's MMAs, so a consumed stage is complete, and an abort ends within the budget.)
+    // Drain: every copy into this CTA must have landed before the CTA may exit.  (The full
+    // barrier also counts the metadata warps' arrivals; those all come before the stage's
+    // MMAs, so a consumed stage is complete, and an abort ends within the budget.)
     if (lane == 0)
       for (int s = 0; s < C::kStages; ++s)
         if ((issued >> s) & 1u) mbar_wait_quiet<PAIR>(bar_full + 8 * s, (last_parity >> s) & 1u, p.wait_budget);
@@ -737,26 +758,6 @@ __global__ void __maxnreg__(128)
           }
         }
         tc_commit_both(bar_drain);
-      } else if (lane == 0 && warp == 1) {
-        // ----------------------------------------------- stage relay (odd CTA)
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        const uint32_t lead_full = peer_addr(bar_full, 0);
-        for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
-          const Unit t = decode_unit(p, u, CL, rank);
-          for (int ks = t.kbeg; ks < t.kend; ++ks) {
-            if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.wait_budget, p.status)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_remote_relaxed(lead_full + 8 * stage);
-            if (++stage == C::kStages) {
-              stage = 0;
-              phase ^= 1;
-            }
-          }
-        }
       }
       // all paired MMAs have completed before either CTA frees its tensor memory
       if (lane == 0 && warp == 1) mbar_wait_quiet<true>(bar_drain, 0u, p.wait_budget);
