@@ -593,7 +593,9 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
             "speedup_vs_cusparselt": t_sl / t if t_sl else None, "cusparselt_note": note}
         plan.destroy()
     # the same shapes in int8 (INT32 accumulation), against torch's int8 matmul of the dense
-    # pruned weight where the installed build has one
+    # pruned weight where the installed build has one, and against the rate of the warp-level
+    # sparse int8 MMA itself, measured now by the library's rate probe (no published figure)
+    i8_peak = nb.nm_test_i8_sparse_mma_rate(20000)
     for (Mb, Nb, Kb) in inputs.BERT_SHAPES:
         Wi = inputs.uniform_int8((Mb, Kb), inputs.SEED_W + Mb).to(dev)
         Xi = inputs.uniform_int8((Nb, Kb), inputs.SEED_X + Nb).to(dev)
@@ -606,7 +608,8 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
                                             meta_layout=nb.NM_META_CANONICAL))
         t = time_launch(torch, lambda: nb.nm_spmm(plan, 1, vals, meta, Xi, 0, None, Di), flush)
         f = 2.0 * Mb * Nb * Kb
-        row = {"ms": t, "tops": f / t / 1e9, "kernel": "spmm_i8_kernel (warp-level mma.sp m16n8k64)"}
+        row = {"ms": t, "tops": f / t / 1e9, "kernel": "spmm_i8_kernel (warp-level mma.sp m16n8k64)",
+               "frac_i8_sparse_mma_peak": f / t / 1e9 / i8_peak}
         try:
             WiT = Wi.t().contiguous()
             tq = time_launch(torch, lambda: torch._int_mm(Xi, WiT), flush)
@@ -617,6 +620,9 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
         rows[f"S5_bert_{Mb}x{Nb}x{Kb}_i8"] = row
         plan.destroy()
     rows["_peaks"] = {"sparse_tflops": sparse_peak, "dense_tflops": dense_peak, "hbm_gbs": hbm,
+                      "i8_sparse_mma_tops": i8_peak,
+                      "i8_note": "nm_test_i8_sparse_mma_rate: mma.sp m16n8k64 s8 on register operands, 8 warps x "
+                                 "4 chains per SM, all SMs, dense-equivalent TOPS",
                       "note": "tensor rows: one launch after an L2 flush, burst peaks; HBM rows: back-to-back "
                               "launches over copies larger than L2 (ms), and one flushed launch (ms_single)"}
     return rows

@@ -35,7 +35,7 @@ EXPORTED = (
     "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm", "nm_spmm_search",
 )
 # Every symbol include/nm_testing.h declares.
-TESTING_EXPORTED = ("nm_test_spmm_wait_timeout",)
+TESTING_EXPORTED = ("nm_test_i8_sparse_mma_rate", "nm_test_spmm_wait_timeout")
 
 
 class NmError(RuntimeError):
@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "nm_spmm": [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp],
             "nm_spmm_search": [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i32, ctypes.POINTER(i32), vp],
             "nm_test_spmm_wait_timeout": [vp, ctypes.POINTER(SpmmDesc), vp, vp, vp, vp, vp, ctypes.c_longlong, vp],
+            "nm_test_i8_sparse_mma_rate": [ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double)],
         }
         for name, args in sigs.items():
             f = getattr(L, name)
@@ -299,3 +300,11 @@ def nm_test_spmm_wait_timeout(desc: SpmmDesc, A, A_meta, B, D, d_status, budget_
     _check(lib().nm_test_spmm_wait_timeout(None, ctypes.byref(desc), _ptr(A), _ptr(A_meta), _ptr(B), _ptr(D),
                                            _ptr(d_status), int(budget_cycles), _stream(stream)),
            "nm_test_spmm_wait_timeout")
+
+
+def nm_test_i8_sparse_mma_rate(iters: int = 20000) -> float:
+    """Measurement hook: the warp-level 2:4 sparse int8 MMA's rate on all SMs, in dense-equivalent TOPS."""
+    ms, ops = ctypes.c_float(), ctypes.c_double()
+    _check(lib().nm_test_i8_sparse_mma_rate(int(iters), ctypes.byref(ms), ctypes.byref(ops)),
+           "nm_test_i8_sparse_mma_rate")
+    return ops.value / ms.value / 1e9

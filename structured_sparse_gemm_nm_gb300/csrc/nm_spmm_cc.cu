@@ -16,6 +16,7 @@
 
 #include "nm_device.cuh"
 #include "nm_internal.h"
+#include "../../include/nm_testing.h"
 
 namespace nmk {
 namespace {
@@ -391,3 +392,52 @@ cudaError_t launch_spmm_i8(const SpmmLaunch& a, cudaStream_t s) {
 }
 
 }  // namespace nmk
+
+namespace {
+// Rate probe: four independent accumulator chains per warp on register operands (metadata
+// code 0x4 = positions 0 and 1 of every group, selector 0), no memory traffic in the loop.
+__global__ void __launch_bounds__(256) i8_sparse_mma_rate_kernel(int iters, int32_t* out, uint32_t seed) {
+  int32_t acc[4][4] = {};
+  const uint32_t a0 = seed * 0x9E3779B9u + threadIdx.x, a1 = a0 ^ 0x55u, a2 = a0 + 7u, a3 = a0 * 3u;
+  const uint32_t b0 = seed + threadIdx.x * 13u, b1 = b0 ^ 0xAAu, b2 = b0 + 5u, b3 = b0 * 5u;
+  const uint32_t e = 0x44444444u;
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      asm volatile(
+          "mma.sp::ordered_metadata.sync.aligned.m16n8k64.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9,%10,%11}, {%0,%1,%2,%3}, %12, 0x0;"
+          : "+r"(acc[c][0]), "+r"(acc[c][1]), "+r"(acc[c][2]), "+r"(acc[c][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(b2), "r"(b3), "r"(e));
+  }
+  int32_t sum = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) sum += acc[c][0] + acc[c][1] + acc[c][2] + acc[c][3];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = sum;  // keeps the chains live
+}
+}  // namespace
+
+extern "C" nm_status_t nm_test_i8_sparse_mma_rate(int iters, float* ms, double* ops) {
+  if (iters < 1 || iters > 1000000 || ms == nullptr || ops == nullptr) return NM_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return NM_ERR_CUDA;
+  constexpr int kThreads = 256;
+  int32_t* out = nullptr;
+  if (cudaMalloc(&out, sizeof(int32_t) * (size_t)sms * kThreads) != cudaSuccess) return NM_ERR_CUDA;
+  cudaEvent_t t0 = nullptr, t1 = nullptr;
+  bool ok = cudaEventCreate(&t0) == cudaSuccess && cudaEventCreate(&t1) == cudaSuccess;
+  if (ok) {
+    i8_sparse_mma_rate_kernel<<<sms, kThreads>>>(iters, out, 1u);  // warm-up
+    ok = cudaEventRecord(t0) == cudaSuccess;
+    i8_sparse_mma_rate_kernel<<<sms, kThreads>>>(iters, out, 2u);
+    ok = ok && cudaGetLastError() == cudaSuccess && cudaEventRecord(t1) == cudaSuccess &&
+         cudaEventSynchronize(t1) == cudaSuccess && cudaEventElapsedTime(ms, t0, t1) == cudaSuccess;
+  }
+  *ops = 2.0 * 16 * 8 * 64 * 4.0 * (double)iters * (kThreads / 32) * sms;
+  if (t0) cudaEventDestroy(t0);
+  if (t1) cudaEventDestroy(t1);
+  const bool freed = cudaFree(out) == cudaSuccess;
+  return ok && freed ? NM_OK : NM_ERR_CUDA;
+}
+

@@ -238,6 +238,15 @@ def test_noalloc_rejects_bad_arguments_before_any_cuda_call(lib):
     assert call(rows=4096, cols=4128, ld=4128) == nb.NM_ERR_UNSUPPORTED  # beyond the fixed scratch
 
 
+def test_i8_rate_probe_rejects_bad_arguments_before_any_cuda_call(lib):
+    import ctypes
+    L = nb.lib()
+    ms, ops = ctypes.c_float(), ctypes.c_double()
+    assert L.nm_test_i8_sparse_mma_rate(0, ctypes.byref(ms), ctypes.byref(ops)) == nb.NM_ERR_INVALID_ARG
+    assert L.nm_test_i8_sparse_mma_rate(10**7, ctypes.byref(ms), ctypes.byref(ops)) == nb.NM_ERR_INVALID_ARG
+    assert L.nm_test_i8_sparse_mma_rate(100, None, ctypes.byref(ops)) == nb.NM_ERR_INVALID_ARG
+
+
 def test_search_argument_checks_and_fixed_plans(lib):
     plan = nb.nm_spmm_plan(nb.make_desc(M=256, N=128, K=128, ab_type="f16", cd_type="f16", ldb=128, ldd=256))
     with pytest.raises(nb.NmError) as e:

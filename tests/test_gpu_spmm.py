@@ -420,3 +420,11 @@ def test_sparse_int8_output_bit_exact(M, N, K, alpha, beta, order_cd):
     got = D.cpu().numpy()[:, :cd_shape[1]]
     got = got if order_cd == nb.NM_ROW else got.T
     assert np.array_equal(got, ref)
+
+
+def test_i8_sparse_mma_rate_probe():
+    """The measurement hook behind the int8 rows' roofline fraction returns a plausible rate."""
+    peak = nb.nm_test_i8_sparse_mma_rate(2000)
+    assert 10.0 < peak < 5000.0
+    with pytest.raises(nb.NmError):
+        nb.nm_test_i8_sparse_mma_rate(0)
