@@ -330,7 +330,8 @@ typedef struct nm_spmm_plan_s* nm_spmm_plan_t;
  * be used from several host threads.
  * Supported: SPARSE_A 2:4 F16/BF16 (tensor cores, B in NM_COL), SPARSE_A 2:4
  * I8 -> I32 (canonical metadata, B in NM_COL), SPARSE_A n:m with m <= 32 and
- * canonical metadata (CUDA-core gather, B in NM_COL), DENSE_MASKED F16/BF16
+ * canonical metadata (CUDA-core gather, B in NM_COL, K < 2^31; with N > 1
+ * also K <= 12800, the batch staged in shared memory), DENSE_MASKED F16/BF16
  * (tensor cores, any orders), BLOCK_SPARSE_A F16/BF16 with units of n x m =
  * 1 x 32 or 32 x 32 (CUDA cores, B in NM_COL; A = the vals and A_meta = the
  * csr that nm_prune_vector_wise / nm_prune_block_wise write; K % 32 == 0 and,

@@ -438,6 +438,8 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc) {
       }
     } else {
       if (d.meta_layout != NM_META_CANONICAL || !fp) return NM_ERR_UNSUPPORTED;
+      // kept-value indices of a row are 32-bit; a batch of B is staged in shared memory
+      if (d.K > 2147483647LL || (d.N > 1 && d.K > 12800)) return NM_ERR_UNSUPPORTED;
       kind = 2;
     }
   } else if (d.mode == NM_SPMM_DENSE_MASKED) {

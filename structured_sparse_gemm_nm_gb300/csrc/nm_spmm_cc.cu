@@ -32,7 +32,9 @@ __device__ __forceinline__ uint16_t from_f(float x, int bf16) {
 
 // NB = batch columns per pass (1 or 8).  x is staged in shared memory as
 // [k][NB]; the staging reads B with 16-byte loads when rows of B allow it.
-template <int NB>
+// NN = n when it is 4, 8 or 16 (the group of a kept value by a shift), 0 for
+// any other n (a 32-bit division per kept value).
+template <int NB, int NN>
 __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint16_t* __restrict__ vals, const uint8_t* __restrict__ idx,
                                                      const uint16_t* __restrict__ B, const uint16_t* __restrict__ C,
                                                      uint16_t* __restrict__ D, int64_t M, int64_t N, int64_t K, int n,
@@ -42,7 +44,9 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
   uint16_t* xs = reinterpret_cast<uint16_t*>(xs4);
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
-  const int64_t kc = (K / m) * n;  // kept values per row
+  const int64_t kc = (K / m) * n;  // kept values per row (below 2^31: K < 2^31)
+  // group of the j-th kept value of a row
+  auto group_of = [&](uint32_t j) -> uint32_t { return NN > 0 ? j / (uint32_t)NN : j / (uint32_t)n; };
   const bool vec = (kc % 8 == 0);
   const bool vstage = (K % 8 == 0);
   for (int64_t b0 = 0; b0 < N; b0 += NB) {
@@ -114,8 +118,9 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
           const uint32_t iw[2] = {i2.x, i2.y};
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
-            const int64_t j = j0 + t;
-            const int64_t k = (j / n) * m + min((iw[t / 4] >> (8 * (t % 4))) & 0xFFu, (uint32_t)(m - 1));
+            const uint32_t j = (uint32_t)j0 + (uint32_t)t;
+            const int64_t k =
+                (int64_t)group_of(j) * m + min((iw[t / 4] >> (8 * (t % 4))) & 0xFFu, (uint32_t)(m - 1));
             const float a = to_f((uint16_t)(vw[t / 2] >> (16 * (t % 2))), bf16);
             if constexpr (NB == 1) {
               acc[0] = fmaf(a, to_f(__ldg(xg + k), bf16), acc[0]);
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
         }
       } else {
         for (int64_t j = lane; j < kc; j += 32) {
-          const int64_t k = (j / n) * m + min((int)ir[j], m - 1);
+          const int64_t k = (int64_t)group_of((uint32_t)j) * m + min((int)ir[j], m - 1);
           const float a = to_f(vr[j], bf16);
           if constexpr (NB == 1) {
             acc[0] = fmaf(a, to_f(__ldg(xg + k), bf16), acc[0]);
@@ -160,7 +165,7 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
   }
 }
 
-template <int NB>
+template <int NB, int NN>
 cudaError_t gather_launch(const SpmmLaunch& a, cudaStream_t s) {
   const nm_spmm_desc_t& d = a.d;
   const size_t smem = NB == 1 ? 0 : (size_t)d.K * NB * 2;
@@ -172,7 +177,7 @@ cudaError_t gather_launch(const SpmmLaunch& a, cudaStream_t s) {
     if (cudaError_t e = cudaGetDevice(&dev)) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(done_mask.load() & bit)) {
-      cudaError_t e = cudaFuncSetAttribute(gather_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      cudaError_t e = cudaFuncSetAttribute(gather_kernel<NB, NN>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
       if (e != cudaSuccess) return e;
       done_mask.fetch_or(bit);
     }
@@ -182,11 +187,11 @@ cudaError_t gather_launch(const SpmmLaunch& a, cudaStream_t s) {
   // per SM.  The grid is whole waves over the SMs (rows are interleaved over CTAs): a
   // grid of ceil(M / 32) CTAs left 24 of 152 SMs idle at M = 4096.
   const int threads = NB == 1 ? 256 : 1024;
-  static const int per_sm = NB == 1 ? resident_ctas(gather_kernel<NB>, threads, 0) : 1;
+  static const int per_sm = NB == 1 ? resident_ctas(gather_kernel<NB, NN>, threads, 0) : 1;
   int64_t blocks = (int64_t)num_sms_cached() * per_sm;
   if (blocks > d.M) blocks = d.M;
   if (blocks < 1) blocks = 1;
-  gather_kernel<NB><<<(unsigned)blocks, threads, smem, s>>>(
+  gather_kernel<NB, NN><<<(unsigned)blocks, threads, smem, s>>>(
       static_cast<const uint16_t*>(a.A), static_cast<const uint8_t*>(a.A_meta), static_cast<const uint16_t*>(a.B),
       static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.M, d.N, d.K, d.n, d.m, d.ldb, d.ldc, d.ldd,
       d.order_cd == NM_COL, a.alpha_f, a.beta_f, d.ab_type == NM_BF16);
@@ -195,8 +200,18 @@ cudaError_t gather_launch(const SpmmLaunch& a, cudaStream_t s) {
 
 }  // namespace
 
+template <int NB>
+cudaError_t gather_launch_n(const SpmmLaunch& a, cudaStream_t s) {
+  switch (a.d.n) {
+    case 4: return gather_launch<NB, 4>(a, s);
+    case 8: return gather_launch<NB, 8>(a, s);
+    case 16: return gather_launch<NB, 16>(a, s);
+    default: return gather_launch<NB, 0>(a, s);
+  }
+}
+
 cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s) {
-  return a.d.N == 1 ? gather_launch<1>(a, s) : gather_launch<kBatch>(a, s);
+  return a.d.N == 1 ? gather_launch_n<1>(a, s) : gather_launch_n<kBatch>(a, s);
 }
 
 // ---------------------------------------------------------------------------
