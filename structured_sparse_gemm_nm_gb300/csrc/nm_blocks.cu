@@ -760,15 +760,18 @@ __global__ void __launch_bounds__(256) vw_spmv_kernel(const SpmmLaunch a) {
   }
 }
 
-// Block-wise: a CTA per block row; its 8 warps split the kept blocks.  Lane l
+// Block-wise: a CTA per block row; its warps split the kept blocks.  Lane l
 // covers columns 8*(l%4)..+7 of block rows l/4 + 8j, j = 0..3, so that every
 // warp load reads 512 contiguous bytes of a block.
-// One CTA of kBwWarps warps per 32-row block row: each warp takes every kBwWarps-th
-// kept block, so a block row's kept blocks (a quarter of them at the benchmark's
-// density) are all in flight at once.
-constexpr int kBwWarps = 32;
+// One CTA of bw_warps(NB) warps per 32-row block row: each warp takes every
+// bw_warps-th kept block, so a block row's kept blocks (a quarter of them at the
+// benchmark's density) are all in flight at once.  Batch 1: 32 warps.  Batch 8:
+// 16 warps, so that a lane has the registers to convert its 32 values of a block
+// and each batch column's 8 values of x once and reuse them across its 4 rows.
+__host__ __device__ constexpr int bw_warps(int nb) { return nb == 1 ? 32 : 16; }
 template <int NB>
-__global__ void __launch_bounds__(kBwWarps * 32) bw_spmv_kernel(const SpmmLaunch a) {
+__global__ void __launch_bounds__(bw_warps(NB) * 32) bw_spmv_kernel(const SpmmLaunch a) {
+  constexpr int kBwWarps = bw_warps(NB);
   const nm_spmm_desc_t& d = a.d;
   const int bf16 = d.ab_type == NM_BF16;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -794,8 +797,39 @@ __global__ void __launch_bounds__(kBwWarps * 32) bw_spmv_kernel(const SpmmLaunch
       uint4 av[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) av[j] = __ldcs(reinterpret_cast<const uint4*>(blk + (rq + 8 * j) * 32 + part * 8));
+      if constexpr (NB == 1) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) dot8<NB>(av[j], B + b0 * d.ldb + c * kUnitW + part * 8, d.ldb, nb, bf16, acc[j]);
+        for (int j = 0; j < 4; ++j) dot8<NB>(av[j], B + b0 * d.ldb + c * kUnitW + part * 8, d.ldb, nb, bf16, acc[j]);
+      } else {
+        float af[4][8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t aw[4] = {av[j].x, av[j].y, av[j].z, av[j].w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            af[j][2 * t] = h2f(aw[t] & 0xFFFFu, bf16);
+            af[j][2 * t + 1] = h2f(aw[t] >> 16, bf16);
+          }
+        }
+        const uint16_t* x = B + b0 * d.ldb + c * kUnitW + part * 8;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (b < nb) {
+            const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + b * d.ldb));
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+            float xf[8];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              xf[2 * t] = h2f(xw[t] & 0xFFFFu, bf16);
+              xf[2 * t + 1] = h2f(xw[t] >> 16, bf16);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[j][b] = fmaf(af[j][e], xf[e], acc[j][b]);
+          }
+        }
+      }
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -917,9 +951,9 @@ cudaError_t launch_spmm_blocks(const SpmmLaunch& a, cudaStream_t s) {
   } else {
     const unsigned grid = (unsigned)(d.M / 32);
     if (d.N == 1)
-      bw_spmv_kernel<1><<<grid, kBwWarps * 32, 0, s>>>(a);
+      bw_spmv_kernel<1><<<grid, bw_warps(1) * 32, 0, s>>>(a);
     else
-      bw_spmv_kernel<8><<<grid, kBwWarps * 32, 0, s>>>(a);
+      bw_spmv_kernel<8><<<grid, bw_warps(8) * 32, 0, s>>>(a);
   }
   return cudaGetLastError();
 }
