@@ -744,10 +744,24 @@ __global__ void __launch_bounds__(256) vw_spmv_kernel(const SpmmLaunch a) {
       float acc[NB];
 #pragma unroll
       for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
-      for (int p = p0 + q; p < p1; p += 8) {
-        const int64_t c = colidx[p];
-        const uint4 av = __ldcs(reinterpret_cast<const uint4*>(vals + (int64_t)p * kUnitW + part * 8));
-        dot8<NB>(av, B + b0 * d.ldb + c * kUnitW + part * 8, d.ldb, nb, bf16, acc);
+      // batch 1: four steps of eight vectors at a time, their column indices and values all
+      // loaded before the first product needs them (7.1 -> 5.1 us at 4096^2, density 0.25);
+      // batch 8 keeps one step at a time (four at once measured 12.6 -> 17.4 us there)
+      constexpr int kSteps = NB == 1 ? 4 : 1;
+      for (int p = p0 + q; p < p1; p += 8 * kSteps) {
+        int64_t cs[kSteps];
+        uint4 avs[kSteps];
+#pragma unroll
+        for (int k = 0; k < kSteps; ++k) {
+          const int pk = p + 8 * k;
+          if (pk < p1) {
+            cs[k] = colidx[pk];
+            avs[k] = __ldcs(reinterpret_cast<const uint4*>(vals + (int64_t)pk * kUnitW + part * 8));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kSteps; ++k)
+          if (p + 8 * k < p1) dot8<NB>(avs[k], B + b0 * d.ldb + cs[k] * kUnitW + part * 8, d.ldb, nb, bf16, acc);
       }
 #pragma unroll
       for (int b = 0; b < NB; ++b)
