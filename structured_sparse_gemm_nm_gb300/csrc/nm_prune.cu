@@ -673,38 +673,39 @@ __device__ __forceinline__ uint32_t nz8(const uint4 x) {
   return ((a >> 15) & 1u) | ((a >> 30) & 2u) | ((b >> 13) & 4u) | ((b >> 28) & 8u) | ((c >> 11) & 16u) |
          ((c >> 26) & 32u) | ((d >> 9) & 64u) | ((d >> 24) & 128u);
 }
+// U items per lane and pass: a warp's `per` items go out in one pass when per <= 32 U.
+template <int U>
 __global__ void __launch_bounds__(256) check24_strips_kernel(const uint4* __restrict__ W, int64_t rows, int64_t wpr,
                                                              int64_t ldw, int transposable, int64_t per,
                                                              int32_t* __restrict__ d_violations) {
-  // every warp takes `per` consecutive items (strip, word), two per lane in flight
+  // every warp takes `per` consecutive items (strip, word), U per lane in flight
   const int lane = threadIdx.x & 31;
   const int64_t total = ((rows + 3) / 4) * wpr;
   const int64_t lo = ((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5) * per;
   const int64_t hi = lo + per < total ? lo + per : total;
-  if (lo >= hi) return;
-  int count = 0;
-  // strip and word of the lane's two items, stepped by 64 items per pass (a 64-bit
+  int count = 0;  // a warp with no items (lo >= hi) skips the loop and adds 0
+  // strip and word of the lane's U items, stepped by 32 U items per pass (a 64-bit
   // division per item had cost more issue slots than the check itself)
-  int64_t st[2], wd[2];
+  int64_t st[U], wd[U];
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
+  for (int u = 0; u < U; ++u) {
     const int64_t idx = lo + 32 * u + lane;
     st[u] = idx / wpr;
     wd[u] = idx - st[u] * wpr;
   }
-  for (int64_t base = lo; base < hi; base += 64) {
-    uint32_t m[2][4];
+  for (int64_t base = lo; base < hi; base += 32 * U) {
+    uint32_t m[U][4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t idx = base + 32 * u + lane;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int64_t r = 4 * st[u] + j;
         m[u][j] = (idx < hi && r < rows) ? nz8(__ldcs(W + r * ldw + wd[u])) : 0u;
       }
-      wd[u] += 64;
+      wd[u] += 32 * U;
       if (wd[u] >= wpr) {
-        if (wpr >= 64) {
+        if (wpr >= 32 * U) {
           wd[u] -= wpr;
           ++st[u];
         } else {
@@ -714,7 +715,7 @@ __global__ void __launch_bounds__(256) check24_strips_kernel(const uint4* __rest
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < U; ++u) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) count += (__popc(m[u][j] & 0xFu) > 2) + (__popc(m[u][j] >> 4) > 2);
       if (transposable)  // columns with at least three of the strip's four entries nonzero
@@ -723,7 +724,17 @@ __global__ void __launch_bounds__(256) check24_strips_kernel(const uint4* __rest
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) count += __shfl_xor_sync(0xFFFFFFFFu, count, off);
-  if ((threadIdx.x & 31) == 0 && count) atomicAdd(d_violations, count);
+  // one atomic per CTA: thousands of same-address atomics, one per warp, had serialised at
+  // the counter when most groups violate
+  __shared__ int warp_count[8];
+  if (lane == 0) warp_count[threadIdx.x >> 5] = count;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int total_count = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) total_count += warp_count[w];
+    if (total_count) atomicAdd(d_violations, total_count);
+  }
 }
 
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -1089,8 +1100,15 @@ cudaError_t check_dt(const void* W, int64_t rows, int64_t cols, int64_t ld, int 
       (!transposable || rows % 4 == 0)) {
     const int64_t wpr = cols / 8;
     const LaneSplit ls = lane_split(((rows + 3) / 4) * wpr);
-    check24_strips_kernel<<<ls.grid, 256, 0, s>>>(static_cast<const uint4*>(W), rows, wpr, ld / 8, transposable,
-                                                   ls.per, d_violations);
+    // one pass per warp when its share is at most 96 items (12 loads of 16 bytes per lane in
+    // flight), else passes of 64
+    const uint4* W4 = static_cast<const uint4*>(W);
+    if (ls.per <= 32)
+      check24_strips_kernel<1><<<ls.grid, 256, 0, s>>>(W4, rows, wpr, ld / 8, transposable, ls.per, d_violations);
+    else if (ls.per <= 96)
+      check24_strips_kernel<3><<<ls.grid, 256, 0, s>>>(W4, rows, wpr, ld / 8, transposable, ls.per, d_violations);
+    else
+      check24_strips_kernel<2><<<ls.grid, 256, 0, s>>>(W4, rows, wpr, ld / 8, transposable, ls.per, d_violations);
     return cudaGetLastError();
   }
   check_kernel<DT><<<grid_for(work, 256), 256, 0, s>>>(static_cast<const T*>(W), rows, cols, ld, n, m, transposable,
