@@ -396,6 +396,127 @@ def hbm_row(torch, make, byt, hbm, flush, **extra):
     return row
 
 
+# ------------------------------------------------------------------ next rows
+def time_steps(torch, fn, reps=10, warm=3):
+    """Median milliseconds of fn in a steady loop (no L2 flush: a training loop's repeated step),
+    timed with CUDA events on the current stream, host work included as a user sees it."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def layer_rows(torch, nb, inputs, dev, flush, sparse_peak):
+    """The built next rows: the 2:4 training layer (forward, backward and the SGD step fused
+    into the transposable re-prune), the activation-sparse layer, and the int8 and fp32
+    outputs of the products, each beside dense PyTorch (cuBLAS) doing the same work."""
+    from structured_sparse_gemm_nm_gb300.sparse_activation import SparseActivationLinear
+    from structured_sparse_gemm_nm_gb300.sparse_linear import SemiStructuredSparseLinear
+
+    F = torch.nn.functional
+    rows = {}
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
+    lr = 1e-3
+    # N1: the MLP workload (512 -> 256, 4096 post-ReLU tokens, fp16) and a GPT-neo FC1 layer (bf16)
+    for name, (T, in_f, out_f, dt) in (("mlp", (4096, 512, 256, "f16")), ("gptneo_fc1", (16384, 768, 3072, "bf16"))):
+        W = inputs.normal((out_f, in_f), 0.05 if name == "mlp" else 0.02, inputs.SEED_W, dt, device=dev)
+        X = (inputs.relu_normal((T, in_f), inputs.SEED_X, dt) if name == "mlp" else
+             inputs.normal((T, in_f), 1.0, inputs.SEED_X, dt)).to(dev).requires_grad_(True)
+        dY = inputs.normal((T, out_f), 0.01 if name == "mlp" else 1.0, inputs.SEED_DY, dt, device=dev)
+        layer = SemiStructuredSparseLinear(in_f, out_f, tdt[dt], dev, weight=W)
+
+        def step(layer=layer, X=X, dY=dY):
+            layer.weight.grad = None
+            X.grad = None
+            layer(X).backward(dY)
+            layer.sgd_step_(lr)
+        t = time_steps(torch, step)
+        Wd = torch.nn.Parameter(W.clone())
+
+        def dense_step(Wd=Wd, X=X, dY=dY):
+            Wd.grad = None
+            X.grad = None
+            F.linear(X, Wd).backward(dY)
+            with torch.no_grad():
+                Wd.add_(Wd.grad, alpha=-lr)
+        td = time_steps(torch, dense_step)
+        f = 3 * 2.0 * T * in_f * out_f
+        rows[f"N1_layer_{name}"] = {
+            "shape_T_in_out": [T, in_f, out_f], "ms": t, "tflops": f / t / 1e9, "dense_torch_ms": td,
+            "speedup_vs_dense": td / t,
+            "note": "SemiStructuredSparseLinear forward, backward (2:4 dX, masked dW) and sgd_step_ (SGD write fused "
+                    "with the transposable re-prune and both compressions), eager on the current stream; dense: "
+                    "F.linear forward, backward and an in-place SGD update"}
+        del layer, X, dY, Wd
+    # N2: activation-sparse GPT-neo FC2 (3072 -> 768, 16384 post-ReLU tokens, bf16)
+    T, in_f, out_f = 16384, 3072, 768
+    W = inputs.normal((out_f, in_f), 0.02, inputs.SEED_W, "bf16", device=dev)
+    X = inputs.relu_normal((T, in_f), inputs.SEED_X, "bf16").to(dev).requires_grad_(True)
+    dY = inputs.normal((T, out_f), 1.0, inputs.SEED_DY, "bf16", device=dev)
+    layer = SparseActivationLinear(in_f, out_f, torch.bfloat16, dev, weight=W)
+
+    def act_step():
+        layer.weight.grad = None
+        X.grad = None
+        layer(X).backward(dY)
+    t = time_steps(torch, act_step)
+    Wd = torch.nn.Parameter(W.clone())
+
+    def act_dense():
+        Wd.grad = None
+        X.grad = None
+        F.linear(X, Wd).backward(dY)
+    td = time_steps(torch, act_dense)
+    f = 3 * 2.0 * T * in_f * out_f
+    rows["N2_activation_gptneo_fc2"] = {
+        "shape_T_in_out": [T, in_f, out_f], "ms": t, "tflops": f / t / 1e9, "dense_torch_ms": td,
+        "speedup_vs_dense": td / t,
+        "note": "SparseActivationLinear forward (one-pass 2:4 prune+compress of X, X as the sparse operand) and "
+                "backward (masked dX, dW on the pruned X), eager; dense: F.linear forward and backward"}
+    del layer, X, dY, Wd
+    # N4: the int8 output of the int8 2:4 product and the fp32 output of the 16-bit one
+    M, N, K = 4096, 4096, 1024
+    Wi = inputs.uniform_int8((M, K), inputs.SEED_W + M).to(dev)
+    Xi = inputs.uniform_int8((N, K), inputs.SEED_X + N).to(dev)
+    vb, mb = nb.nm_compressed_size(M, K, "i8", 2, 4, nb.NM_META_CANONICAL)
+    vals = torch.empty(vb, dtype=torch.uint8, device=dev)
+    meta = torch.empty(mb, dtype=torch.uint8, device=dev)
+    nb.nm_compress(Wi, M, K, K, "i8", 2, 4, 0, nb.NM_META_CANONICAL, vals, meta)
+    Di = torch.empty((N, M), dtype=torch.int8, device=dev)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type="i8", cd_type="i8", ldb=K, ldd=M,
+                                        meta_layout=nb.NM_META_CANONICAL))
+    t = time_launch(torch, lambda: nb.nm_spmm(plan, 0.01, vals, meta, Xi, 0.0, None, Di), flush)
+    rows["N4_int8_out_4096x4096x1024"] = {"ms": t, "tops": 2.0 * M * N * K / t / 1e9,
+                                          "note": "int8 in, int8 out: saturate(rne(alpha * acc)), one launch after an "
+                                                  "L2 flush"}
+    plan.destroy()
+    M, N, K = 3072, 16384, 768
+    W = inputs.normal((M, K), 0.02, inputs.SEED_W, "bf16", device=dev)
+    Xb = inputs.normal((N, K), 1.0, inputs.SEED_X, "bf16", device=dev)
+    vb, mb = nb.nm_compressed_size(M, K, "bf16", 2, 4, nb.NM_META_TC)
+    vals = torch.empty(vb, dtype=torch.uint8, device=dev)
+    meta = torch.empty(mb, dtype=torch.uint8, device=dev)
+    nb.nm_compress(W, M, K, K, "bf16", 2, 4, 0, nb.NM_META_TC, vals, meta)
+    D32 = torch.empty((N, M), dtype=torch.float32, device=dev)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, ab_type="bf16", cd_type="f32", ldb=K, ldd=M))
+    t = time_launch(torch, lambda: nb.nm_spmm(plan, 1.0, vals, meta, Xb, 0.0, None, D32), flush)
+    f = 2.0 * M * N * K
+    rows["N4_f32_out_gptneo_fc1_fwd"] = {"shape_MNK": [M, N, K], "ms": t, "tflops": f / t / 1e9,
+                                         "frac_sparse_peak": f / t / 1e9 / sparse_peak,
+                                         "note": "bf16 in, fp32 D (201 MB written), one launch after an L2 flush"}
+    plan.destroy()
+    torch.cuda.empty_cache()
+    return rows
+
+
 # ------------------------------------------------------------------ rows
 def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
     flush = Flusher(torch, dev)
@@ -619,6 +740,7 @@ def measure_rows(torch, nb, inputs, dev, wl: GptNeoTrain, peaks):
             row["torch_int8_dense"] = f"unavailable: {type(e).__name__}"
         rows[f"S5_bert_{Mb}x{Nb}x{Kb}_i8"] = row
         plan.destroy()
+    rows.update(layer_rows(torch, nb, inputs, dev, flush, sparse_peak))
     rows["_peaks"] = {"sparse_tflops": sparse_peak, "dense_tflops": dense_peak, "hbm_gbs": hbm,
                       "i8_sparse_mma_tops": i8_peak,
                       "i8_note": "nm_test_i8_sparse_mma_rate: mma.sp m16n8k64 s8 on register operands, 8 warps x "
