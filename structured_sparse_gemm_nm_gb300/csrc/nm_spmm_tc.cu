@@ -466,6 +466,31 @@ __device__ __forceinline__ void store_chunk_generic(const Params& p, int row, in
   }
 }
 
+// fp32 D of one row's 32 columns starting at nb (no C, no K split): alpha and the mask applied;
+// column-major D: 32 lanes (rows) write 128 contiguous bytes per column; row-major: 16-byte stores.
+__device__ __forceinline__ void store_chunk_f32(const Params& p, int row, int nb, const uint32_t (&v)[32],
+                                                uint32_t mword, bool scale) {
+  const int cnt = min(32, p.N - nb);
+  float* D32 = reinterpret_cast<float*>(p.D);
+  auto val = [&](int j) -> float {
+    const float x = __uint_as_float(v[j]);
+    return ((mword >> j) & 1u) ? (scale ? x * p.alpha : x) : 0.0f;
+  };
+  if (p.cd_col) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < cnt) D32[(int64_t)(nb + j) * p.ldd + row] = val(j);
+  } else if (cnt == 32) {
+    float4* dst = reinterpret_cast<float4*>(D32 + (int64_t)row * p.ldd + nb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = make_float4(val(4 * k), val(4 * k + 1), val(4 * k + 2), val(4 * k + 3));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < cnt) D32[(int64_t)row * p.ldd + nb + j] = val(j);
+  }
+}
+
 // ----------------------------------------------------------------- kernel
 // The warps of a CTA are spread over the SM's four sub-partitions, each with a
 // quarter of the register file: 14 or 15 warps put four on one of them, so
@@ -1013,6 +1038,7 @@ __global__ void __maxnreg__(128)
     uint32_t acc_phase = 0;
     const bool scale = p.alpha != 1.0f;
     const bool fast = p.split_k == 1 && p.C == nullptr && p.cd_kind != kCdF32;
+    const bool fast32 = p.split_k == 1 && p.C == nullptr && p.cd_kind == kCdF32;
     // chunk c (32 columns): accumulator column 128 (c / 2) + 64 hw + 32 (c % 2), which holds tile
     // column 128 hw + 32 c (see the issuers); chunks 0, 1 lie in the first issuer's half
     auto chunk_col = [&](int c) { return 128 * (c >> 1) + 64 * hw + 32 * (c & 1); };
@@ -1081,6 +1107,17 @@ __global__ void __maxnreg__(128)
               }
             }
           }
+        }
+      } else if (fast32) {
+        // fp32 D: a half's two chunks are loaded, the half is handed back, then stored
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t va[32], vb[32];
+          tmem_ld32x2(tq + chunk_col(2 * h), tq + chunk_col(2 * h) + 32, va, vb);
+          release(h);
+          const int nba = t.n0 + tile_col(2 * h), nbb = t.n0 + tile_col(2 * h + 1);
+          if (row_ok && nba < p.N) store_chunk_f32(p, row, nba, va, mask_word(2 * h), scale);
+          if (row_ok && nbb < p.N) store_chunk_f32(p, row, nbb, vb, mask_word(2 * h + 1), scale);
         }
       } else {
 #pragma unroll 1
