@@ -397,20 +397,22 @@ def hbm_row(torch, make, byt, hbm, flush, **extra):
 
 
 # ------------------------------------------------------------------ next rows
-def time_steps(torch, fn, reps=10, warm=3):
-    """Median milliseconds of fn in a steady loop (no L2 flush: a training loop's repeated step),
-    timed with CUDA events on the current stream, host work included as a user sees it."""
+def time_steps(torch, fn, reps=10, warm=3, trials=3):
+    """Milliseconds per call of fn in a training loop: `reps` calls back to back between two CUDA
+    events on the current stream (the host enqueues ahead of the GPU as a loop does; no L2
+    flush), the median over `trials` such loops."""
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
     ts = []
-    for _ in range(reps):
+    for _ in range(trials):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        fn()
+        for _ in range(reps):
+            fn()
         b.record()
         torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
+        ts.append(a.elapsed_time(b) / reps)
     return statistics.median(ts)
 
 
@@ -453,8 +455,8 @@ def layer_rows(torch, nb, inputs, dev, flush, sparse_peak):
             "shape_T_in_out": [T, in_f, out_f], "ms": t, "tflops": f / t / 1e9, "dense_torch_ms": td,
             "speedup_vs_dense": td / t,
             "note": "SemiStructuredSparseLinear forward, backward (2:4 dX, masked dW) and sgd_step_ (SGD write fused "
-                    "with the transposable re-prune and both compressions), eager on the current stream; dense: "
-                    "F.linear forward, backward and an in-place SGD update"}
+                    "with the transposable re-prune and both compressions), eager, steps back to back on the current "
+                    "stream; dense: F.linear forward, backward and an in-place SGD update"}
         del layer, X, dY, Wd
     # N2: activation-sparse GPT-neo FC2 (3072 -> 768, 16384 post-ReLU tokens, bf16)
     T, in_f, out_f = 16384, 3072, 768

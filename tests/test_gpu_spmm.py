@@ -71,6 +71,10 @@ F32_CASES = [
     (256, 4096, 512, "bf16", nb.NM_COL, 1.0, 0.0, False, "f32"),
     (200, 300, 224, "f16", nb.NM_ROW, 0.5, -1.5, False, "f32"),
     (384, 264, 640, "bf16", nb.NM_COL, 2.0, 1.0, False, "f32"),
+    # beta = 0 on paired CTAs: the fp32 epilogue that hands each half back before storing,
+    # row-major (16-byte row stores, ragged N) and column-major with a ragged tail
+    (256, 200, 224, "bf16", nb.NM_ROW, 0.5, 0.0, False, "f32"),
+    (512, 328, 96, "f16", nb.NM_COL, -1.0, 0.0, False, "f32"),
 ]
 
 
