@@ -416,6 +416,21 @@ def time_steps(torch, fn, reps=10, warm=3, trials=3):
     return statistics.median(ts)
 
 
+def time_graph(torch, fn, reps=10, warm=3, trials=3):
+    """Milliseconds per replay of fn captured once in a CUDA graph (warmed up on the capture
+    stream first): the step's GPU time without the host's per-call work."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(warm):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    return time_steps(torch, g.replay, reps=reps, warm=1, trials=trials)
+
+
 def layer_rows(torch, nb, inputs, dev, flush, sparse_peak):
     """The built next rows: the 2:4 training layer (forward, backward and the SGD step fused
     into the transposable re-prune), the activation-sparse layer, and the int8 and fp32
@@ -450,13 +465,16 @@ def layer_rows(torch, nb, inputs, dev, flush, sparse_peak):
             with torch.no_grad():
                 Wd.add_(Wd.grad, alpha=-lr)
         td = time_steps(torch, dense_step)
+        tg, tdg = time_graph(torch, step), time_graph(torch, dense_step)
         f = 3 * 2.0 * T * in_f * out_f
         rows[f"N1_layer_{name}"] = {
             "shape_T_in_out": [T, in_f, out_f], "ms": t, "tflops": f / t / 1e9, "dense_torch_ms": td,
-            "speedup_vs_dense": td / t,
+            "speedup_vs_dense": td / t, "ms_graph": tg, "tflops_graph": f / tg / 1e9, "dense_torch_ms_graph": tdg,
+            "speedup_vs_dense_graph": tdg / tg,
             "note": "SemiStructuredSparseLinear forward, backward (2:4 dX, masked dW) and sgd_step_ (SGD write fused "
                     "with the transposable re-prune and both compressions), eager, steps back to back on the current "
-                    "stream; dense: F.linear forward, backward and an in-place SGD update"}
+                    "stream, and the same step captured once in a CUDA graph (_graph keys); dense: F.linear forward, "
+                    "backward and an in-place SGD update, timed the same two ways"}
         del layer, X, dY, Wd
     # N2: activation-sparse GPT-neo FC2 (3072 -> 768, 16384 post-ReLU tokens, bf16)
     T, in_f, out_f = 16384, 3072, 768
@@ -477,12 +495,15 @@ def layer_rows(torch, nb, inputs, dev, flush, sparse_peak):
         X.grad = None
         F.linear(X, Wd).backward(dY)
     td = time_steps(torch, act_dense)
+    tg, tdg = time_graph(torch, act_step), time_graph(torch, act_dense)
     f = 3 * 2.0 * T * in_f * out_f
     rows["N2_activation_gptneo_fc2"] = {
         "shape_T_in_out": [T, in_f, out_f], "ms": t, "tflops": f / t / 1e9, "dense_torch_ms": td,
-        "speedup_vs_dense": td / t,
+        "speedup_vs_dense": td / t, "ms_graph": tg, "tflops_graph": f / tg / 1e9, "dense_torch_ms_graph": tdg,
+        "speedup_vs_dense_graph": tdg / tg,
         "note": "SparseActivationLinear forward (one-pass 2:4 prune+compress of X, X as the sparse operand) and "
-                "backward (masked dX, dW on the pruned X), eager; dense: F.linear forward and backward"}
+                "backward (masked dX, dW on the pruned X), eager and captured in a CUDA graph (_graph keys); "
+                "dense: F.linear forward and backward, timed the same two ways"}
     del layer, X, dY, Wd
     # N4: the int8 output of the int8 2:4 product and the fp32 output of the 16-bit one
     M, N, K = 4096, 4096, 1024
