@@ -103,7 +103,10 @@ struct Cfg {
   static constexpr int kStages = PAIR ? (SPARSE ? 4 : 6) : (SPARSE ? 5 : 4);
   static constexpr int kAcc = SPARSE ? 1 : 2;  // 256-column accumulator buffers
   static constexpr int kEpiOffset = kStages * kStageBytes;
-  static constexpr int kBarOffset = kEpiOffset + (PAIR ? 0 : kEpiWarps * kEpiBufBytes);
+  // 16-bit D staging for the TMA stores: one 32 x 32 block per epilogue warp (two, alternating,
+  // in the paired kernel)
+  static constexpr int kEpiBufs = PAIR ? 2 : 1;
+  static constexpr int kBarOffset = kEpiOffset + kEpiWarps * kEpiBufs * kEpiBufBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 512;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
@@ -223,6 +226,7 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -1027,9 +1031,12 @@ __global__ void __maxnreg__(128)
     // first and handed back to its issuer, which starts the next tile while
     // half 1 is read.  Common case (16-bit D, C not read, no K split): all four
     // 32-column chunks are packed in registers before D is written, so the
-    // accumulator is free after the reads alone.  Column-major D: one 2-byte
-    // store per lane and column, 64 contiguous bytes per warp store; row-major
-    // D: a row's 32 columns as four 16-byte stores.
+    // accumulator is free after the reads alone; each chunk is then staged as a
+    // 32 x 32 block in shared memory (two per warp, alternating) and written by
+    // one TMA store.  Column-major D is staged [n][m]: lane pairs swap halves
+    // so that each lane writes 4 bytes (rows 2i, 2i + 1 of one column), an even
+    // lane's column 2j and an odd lane's column 2j + 1 filling one 128-byte line
+    // per instruction; row-major D is staged [m][n] in the 64-byte swizzle.
     const int ew = warp - kEpiWarp0;
     const int q = warp & 3;
     const int hw = ew >> 2;
@@ -1043,11 +1050,14 @@ __global__ void __maxnreg__(128)
     // column 128 hw + 32 c (see the issuers); chunks 0, 1 lie in the first issuer's half
     auto chunk_col = [&](int c) { return 128 * (c >> 1) + 64 * hw + 32 * (c & 1); };
     auto tile_col = [&](int c) { return 128 * hw + 32 * c; };
+    uint8_t* const stage0 = smem + C::kEpiOffset + ew * (2 * kEpiBufBytes);
+    int n_stored = 0;  // TMA stores this warp has issued (lane 0 commits each as a group)
     for (int u = cluster_id; u < p.num_units; u += num_clusters) {
       const Unit t = decode_unit(p, u, CL, rank);
       if (!mbar_wait<true>(bar_tfull + 8 * acc, acc_phase, abort_flag, p.wait_budget, p.status)) break;
       tc_fence_after();
-      const int row = t.m0 + 32 * q + lane;
+      const int mq = t.m0 + 32 * q;
+      const int row = mq + lane;
       const bool row_ok = row < p.M;
       const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + acc * BN;
       auto mask_word = [&](int c) -> uint32_t {
@@ -1077,35 +1087,46 @@ __global__ void __maxnreg__(128)
           pack64_any<!SPARSE>(p.bf16, scale, va, vb, p.alpha, mask_word(2 * h), mask_word(2 * h + 1), pk[2 * h],
                               pk[2 * h + 1]);
         }
-        if (row_ok) {
-          uint16_t* D16 = reinterpret_cast<uint16_t*>(p.D);
+        if (mq < p.M) {
+          const bool odd = lane & 1;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int nb = t.n0 + tile_col(c);
             if (nb >= p.N) continue;
-            const int cnt = min(32, p.N - nb);
+            uint8_t* buf = stage0 + (n_stored & 1) * kEpiBufBytes;
+            if (n_stored >= 2) {
+              if (lane == 0) bulk_wait_read1();  // the store before last has read this block
+              __syncwarp();
+            }
             if (p.cd_col) {
-              uint16_t* dst = D16 + (int64_t)nb * p.ldd + row;
+              // block [32 n][32 m], 64-byte rows: element (n, m) at (n * 32 + m) * 2
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                if (2 * j < cnt) dst[(int64_t)(2 * j) * p.ldd] = (uint16_t)(pk[c][j] & 0xFFFFu);
-                if (2 * j + 1 < cnt) dst[(int64_t)(2 * j + 1) * p.ldd] = (uint16_t)(pk[c][j] >> 16);
+                const uint32_t own = pk[c][j];
+                const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, own, 1);
+                // even lane: column 2j of rows lane, lane + 1; odd lane: column 2j + 1 of rows lane - 1, lane
+                const uint32_t w = odd ? __byte_perm(other, own, 0x7632) : __byte_perm(own, other, 0x5410);
+                *reinterpret_cast<uint32_t*>(buf + (2 * j + (odd ? 1 : 0)) * 64 + (lane & ~1) * 2) = w;
               }
             } else {
-              uint16_t* dst = D16 + (int64_t)row * p.ldd + nb;
-              if (cnt == 32) {
-                uint4* d4 = reinterpret_cast<uint4*>(dst);
+              // block [32 m][32 n], 64-byte rows in the 64B-swizzled order of the store map:
+              // 16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)
+              uint4* b4 = reinterpret_cast<uint4*>(buf + lane * 64);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  d4[k] = make_uint4(pk[c][4 * k], pk[c][4 * k + 1], pk[c][4 * k + 2], pk[c][4 * k + 3]);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  if (2 * j < cnt) dst[2 * j] = (uint16_t)(pk[c][j] & 0xFFFFu);
-                  if (2 * j + 1 < cnt) dst[2 * j + 1] = (uint16_t)(pk[c][j] >> 16);
-                }
-              }
+              for (int k = 0; k < 4; ++k)
+                b4[k ^ ((lane >> 1) & 3)] =
+                    make_uint4(pk[c][4 * k], pk[c][4 * k + 1], pk[c][4 * k + 2], pk[c][4 * k + 3]);
             }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              if (p.cd_col)
+                tma_store_2d(&tmD, smem_u32(buf), mq, nb);
+              else
+                tma_store_2d(&tmD, smem_u32(buf), nb, mq);
+              bulk_commit();
+            }
+            ++n_stored;
           }
         }
       } else if (fast32) {
@@ -1138,6 +1159,8 @@ __global__ void __maxnreg__(128)
         acc_phase ^= 1;
       }
     }
+    if (lane == 0) bulk_wait_all();  // staging blocks stay valid until the stores are done
+    __syncwarp();
   } else {
     // ------------------------------------------------------- single-CTA epilogue
     const int ew = warp - kEpiWarp0;
