@@ -52,6 +52,10 @@ SPARSE_CASES = [
     (128, 128, 32, "f16", nb.NM_COL, 1.0, 0.25, False),    # a single MMA k-step
     (264, 200, 160, "f16", nb.NM_ROW, 1.5, 0.0, False),    # row-major D through the bulk-store path
     (96, 40, 32, "bf16", nb.NM_COL, 1.0, 0.0, False),      # one partial tile, one k-step
+    # paired CTAs, row-major 16-bit D without C: 32 x 32 blocks staged for TMA stores
+    (256, 200, 224, "bf16", nb.NM_ROW, 0.5, 0.0, False),   # ragged N, alpha applied
+    (200, 328, 96, "f16", nb.NM_ROW, 1.0, 0.0, False),     # ragged M inside the pair
+    (512, 4096, 512, "bf16", nb.NM_ROW, 1.0, 0.0, False),  # several tiles per cluster
     (1024, 4096, 1024, "f16", nb.NM_COL, 1.0, 0.0, True),  # BERT-Large shapes
     (4096, 4096, 1024, "f16", nb.NM_COL, 1.0, 0.0, True),
     (1024, 4096, 4096, "f16", nb.NM_COL, 1.0, 0.0, True),
