@@ -934,8 +934,13 @@ def run_native(args):
 
     wl = GptNeoTrain(torch, nb, inputs, dev, inputs.GPTNEO_LAYERS, inputs.GPTNEO_TOKENS)
     # the native arm's algorithm search (its tensor-core products keep whichever of the paired and
-    # single-CTA kernels measured faster on each shape)
-    wl.search_plans()
+    # single-CTA kernels measured faster on each shape); --no-search keeps the library's default
+    # (paired CTAs where M spans an even number of 128-row blocks), e.g. for profiler runs, where
+    # the search would time its candidates through the profiler
+    if args.no_search:
+        wl.algos = {name: {"fwd": "default", "dx": "default", "dw": "default"} for (name, _, _) in wl.linears}
+    else:
+        wl.search_plans()
     torch.cuda.synchronize()
     launches_per_step = [0]
 
@@ -1215,6 +1220,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-search", action="store_true", help="keep each plan's default kernel (no plan-time search)")
     ap.add_argument("--kernel-case", choices=KERNEL_CASES, help="run one kernel a few times (profiler captures)")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)

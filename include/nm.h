@@ -376,8 +376,10 @@ nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const
  * description asked for NM_ALGO_DEFAULT on a tensor-core product (SPARSE_A
  * 2:4 F16/BF16 or DENSE_MASKED) with M spanning an even number of 128-row
  * blocks, runs the product with NM_ALGO_PAIRED and with NM_ALGO_SINGLE on the
- * given operands, `repeats` timed runs each (after one untimed run), timed
- * with CUDA events on `stream`, and keeps the faster algorithm in the plan.
+ * given operands in three rounds that alternate the two, each round `repeats`
+ * timed runs per algorithm (after one untimed run), timed with CUDA events on
+ * `stream`; the plan keeps NM_ALGO_SINGLE only if its fastest round is at
+ * least 2% faster than the paired algorithm's, else NM_ALGO_PAIRED.
  * Other plans keep their kernel and only report it.  *chosen_algo (nullable,
  * host) receives the algorithm the plan now uses.
  * Arguments are those of nm_spmm; D (and the workspace) are overwritten with
