@@ -359,7 +359,10 @@ nm_status_t nm_spmm_plan_destroy(nm_spmm_plan_t plan);
  * D's M x N shape in row-major order (DENSE_MASKED; NULL = no mask, a plain
  * dense product).  C may alias D.
  * workspace: device buffer of at least nm_spmm_plan_workspace bytes (NULL if
- * 0).  d_status (nullable, device int32): set to NM_ERR_TIMEOUT if a bounded
+ * 0); its contents need no initialisation (a DENSE_MASKED product split
+ * along K keeps fp32 partials there and, with two splits on paired CTAs,
+ * per-launch arrival words through which the product sums the splits
+ * itself); calls that may run at the same time must not share one.  d_status (nullable, device int32): set to NM_ERR_TIMEOUT if a bounded
  * pipeline wait gave up; it is not cleared by the call.
  * Base pointers must be 16-byte aligned and leading dimensions multiples of
  * 16 bytes (NM_ERR_MISALIGNED); for the CUDA-core products (SPARSE_A with

@@ -133,6 +133,11 @@ struct Params {
   const uint32_t* mask;
   int64_t mask_words;
   float* partial;  // DENSE split-K: tiled fp32 partials
+  // DENSE split-K summed in the product (paired, two splits): per epilogue warp and tile, a
+  // 64-bit word (launch token << 32 | arrivals); the warp that arrives last sums the splits
+  int fuse_split;
+  uint32_t split_token;
+  unsigned long long* split_cnt;
   int32_t* status;
   long long wait_budget;  // cycles
   int fault_test;         // 1: the MMA lane waits on a barrier nothing arrives at
@@ -467,6 +472,78 @@ __device__ __forceinline__ void store_chunk_generic(const Params& p, int row, in
     const int64_t coff = p.cd_col ? (int64_t)(nb + j) * p.ldc + row : (int64_t)row * p.ldc + nb + j;
     if (p.C != nullptr) x = fmaf(p.beta, load_cd(p.C, coff, p.cd_kind), x);
     store_cd(p.D, doff, x, p.cd_kind);
+  }
+}
+
+// Split-K summed in the product: the arrival of one epilogue warp at its region of a tile, after
+// its partial stores (this launch's token in the high word; a stale token restarts the count).
+// Returns true for the warp that arrives last; its later reads of the other splits' partials
+// are ordered after their writers' fences by the atomic and the fence that follows it.
+__device__ __forceinline__ bool split_arrive_last(const Params& p, int64_t idx, int lane) {
+  __threadfence();  // this lane's partial stores before the arrival
+  __syncwarp();
+  uint32_t last = 0;
+  if (lane == 0) {
+    unsigned long long* w = p.split_cnt + idx;
+    const unsigned long long tok = (unsigned long long)p.split_token << 32;
+    unsigned long long old = atomicAdd(w, 0ull), nw;
+    while (true) {
+      nw = (old & 0xFFFFFFFF00000000ull) == tok ? old + 1ull : tok | 1ull;
+      const unsigned long long prev = atomicCAS(w, old, nw);
+      if (prev == old) break;
+      old = prev;
+    }
+    last = (uint32_t)nw == (uint32_t)p.split_k ? 1u : 0u;
+    __threadfence();
+  }
+  return __shfl_sync(0xFFFFFFFFu, last, 0) != 0;
+}
+// The sum over the splits (in split order) of one row's 32 columns of a tile's partials, then
+// beta * C, stored to D; the same arithmetic as the separate finalize.
+__device__ __forceinline__ void store_split_sum_chunk(const Params& p, const Unit& t, int col, int q, int lane,
+                                                      int row, int nb) {
+  const int64_t per_split = (int64_t)p.num_m_blk * p.num_n_blk * (BM * BN / 4);
+  const float4* src = reinterpret_cast<const float4*>(p.partial) +
+                      ((int64_t)(t.m0 / BM) * p.num_n_blk + t.n0 / BN) * (BM * BN / 4) + (col / 4) * BM + 32 * q + lane;
+  float x[32];
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) {
+    const float4 w = __ldcg(src + j4 * BM);
+    x[4 * j4] = w.x, x[4 * j4 + 1] = w.y, x[4 * j4 + 2] = w.z, x[4 * j4 + 3] = w.w;
+  }
+  for (int sp = 1; sp < p.split_k; ++sp) {
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+      const float4 w = __ldcg(src + sp * per_split + j4 * BM);
+      x[4 * j4] += w.x, x[4 * j4 + 1] += w.y, x[4 * j4 + 2] += w.z, x[4 * j4 + 3] += w.w;
+    }
+  }
+  if (row >= p.M || nb >= p.N) return;
+  const int cnt = min(32, p.N - nb);
+  if (p.C != nullptr) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j >= cnt) break;
+      const int64_t coff = p.cd_col ? (int64_t)(nb + j) * p.ldc + row : (int64_t)row * p.ldc + nb + j;
+      x[j] = fmaf(p.beta, load_cd(p.C, coff, p.cd_kind), x[j]);
+    }
+  }
+  if (!p.cd_col && cnt == 32 && p.cd_kind != kCdF32) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + (int64_t)row * p.ldd + nb;
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = pack2(x[2 * j], x[2 * j + 1], p.cd_kind == kCdBF16);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) reinterpret_cast<uint4*>(dst)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+      return;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j >= cnt) break;
+    const int64_t doff = p.cd_col ? (int64_t)(nb + j) * p.ldd + row : (int64_t)row * p.ldd + nb + j;
+    store_cd(p.D, doff, x[j], p.cd_kind);
   }
 }
 
@@ -1153,6 +1230,13 @@ __global__ void __maxnreg__(128)
             store_chunk_generic(p, row, nb, v, mword);
           if (c & 1) release(c >> 1);
         }
+        if (!SPARSE && p.fuse_split) {  // the split that arrives last at this warp's region sums them
+          const int64_t idx = ((int64_t)(t.m0 / BM) * p.num_n_blk + t.n0 / BN) * kEpiWarps + ew;
+          if (split_arrive_last(p, idx, lane)) {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) store_split_sum_chunk(p, t, tile_col(c), q, lane, row, t.n0 + tile_col(c));
+          }
+        }
       }
       if (++acc == C::kAcc) {
         acc = 0;
@@ -1603,9 +1687,10 @@ int spmm_tc_dense_masked_split(const nm_spmm_desc_t& d) {
   return best;
 }
 size_t spmm_tc_dense_masked_workspace(const nm_spmm_desc_t& d, int split_k) {
-  // whole 128 x 256 tiles per split (the tiled partial order of the product's epilogue)
+  // whole 128 x 256 tiles per split (the tiled partial order of the product's epilogue), then
+  // one 64-bit arrival word per tile and epilogue warp (splits summed in the product)
   const size_t tiles = (size_t)((d.M + tc::BM - 1) / tc::BM) * (size_t)((d.N + tc::BN - 1) / tc::BN);
-  return split_k > 1 ? (size_t)split_k * tiles * tc::BM * tc::BN * sizeof(float) : 0;
+  return split_k > 1 ? (size_t)split_k * tiles * tc::BM * tc::BN * sizeof(float) + tiles * tc::kEpiWarps * 8 : 0;
 }
 
 cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaStream_t s) {
@@ -1626,6 +1711,18 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
     p.tma_store = 0;
   }
   const bool pair = use_pair(p.num_m_blk, d.algo);
+  if (pair && p.split_k == 2) {
+    // two splits are summed by the paired product itself: the warp that finishes a tile's region
+    // last adds the other split's partial (in split order, as the finalize would) and writes D
+    static std::atomic<uint32_t> launches{0x5A170000u};
+    uint32_t token = ++launches;
+    if (token == 0) token = ++launches;
+    const size_t tiles = (size_t)p.num_m_blk * (size_t)p.num_n_blk;
+    p.fuse_split = 1;
+    p.split_token = token;
+    p.split_cnt = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.ws) +
+                                                       (size_t)split_k * tiles * BM * BN * sizeof(float));
+  }
   const int cl = pair ? 2 : 1;
   p.num_units = (p.num_m_blk / cl) * p.num_n_blk * p.split_k;
   const uint32_t b_rows = (uint32_t)(BN / cl);  // paired: this CTA's 128-row block of B
@@ -1649,7 +1746,7 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
   if (ok) ok = make_store_map(&mD, d, a.D);
   if (!ok) return cudaErrorInvalidValue;
   cudaError_t e = pair ? launch_kernel<false, true>(mA, mB, mD, p, s) : launch_kernel<false, false>(mA, mB, mD, p, s);
-  if (e != cudaSuccess || p.split_k == 1) return e;
+  if (e != cudaSuccess || p.split_k == 1 || p.fuse_split) return e;
   const int cdk = cd_kind_of(d.cd_type);
   if (d.order_cd == NM_ROW) {
     return launch_pdl(finalize_split_rows_kernel, dim3((unsigned)((int64_t)p.num_m_blk * p.num_n_blk * (BN / 32))),

@@ -156,6 +156,8 @@ DENSE_SINGLE = [c for c in DENSE_CASES if not c[4]]
                          [c + (nb.NM_ALGO_SINGLE, None) for c in DENSE_SINGLE] +
                          [(256, 512, 4096, "bf16", False, 1.0, 0.0, a, "f32") for a in (0, 2)] +
                          [(264, 136, 1000, "f16", False, 0.5, -1.0, a, "f32") for a in (0, 2)] +
+                         # two K splits on paired CTAs: summed in the product, fp32 D with C
+                         [(136, 72, 1000, "bf16", False, 0.5, -1.0, 0, "f32")] +
                          [(512, 520, 192, "bf16", False, 2.0, 0.0, a, "f32") for a in (0, 2)])
 def test_masked_weight_grad_matches_oracle(M, N, K, dtype, sampled, alpha, beta, algo, cd):
     cd = cd or dtype
@@ -181,6 +183,34 @@ def test_masked_weight_grad_matches_oracle(M, N, K, dtype, sampled, alpha, beta,
     if C is not None:
         ref = ref + beta * C.double().numpy()[rows]
     assert_gemm_close(dW.cpu().double().numpy()[rows], ref, f"dW {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,beta", [(136, 72, 1000, 0.0), (136, 72, 1000, 2.0), (768, 768, 16384, 0.0)])
+def test_masked_weight_grad_column_major(M, N, K, beta):
+    """Column-major dW: two K splits summed in the paired product (with and without C), and the
+    O dW shape's eight splits summed by the separate finalize."""
+    dtype = "bf16"
+    dY = inputs.normal((K, M), 1.0, inputs.SEED_DY + K, dtype)
+    X = inputs.normal((K, N), 1.0, inputs.SEED_X + K, dtype)
+    W = inputs.normal((M, N), 0.02, inputs.SEED_W, dtype)
+    _, mask_ref = o.nm_prune(inputs.as_numpy_bits(W), dtype, 2, 4)
+    bits = torch.from_numpy(o.mask_to_bits(mask_ref).view(np.int32)).to(DEV)
+    dWt = torch.full((N, M), float("nan"), dtype=torch.bfloat16, device=DEV)  # dW column-major: [N][M]
+    C = inputs.normal((N, M), 1.0, inputs.SEED_C, dtype) if beta != 0 else None
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, mode=nb.NM_SPMM_DENSE_MASKED, ab_type=dtype, cd_type=dtype,
+                                        order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_COL, lda=M, ldb=N,
+                                        ldc=M if C is not None else 0, ldd=M, meta_layout=nb.NM_META_CANONICAL))
+    ws_bytes = nb.nm_spmm_plan_workspace(plan)
+    ws = dev_bytes(ws_bytes) if ws_bytes else None
+    nb.nm_spmm(plan, 1.0, dY.to(DEV), bits, X.to(DEV), beta, C.to(DEV) if C is not None else None, dWt, ws, ws_bytes)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, 128, seed=K) if M > 512 else np.arange(M)
+    dYm = o.decode(inputs.as_numpy_bits(dY), dtype)
+    Xm = o.decode(inputs.as_numpy_bits(X), dtype)
+    ref = o.masked_weight_grad(dYm[:, rows], Xm, mask_ref[rows])
+    if C is not None:
+        ref = ref + beta * C.double().numpy().T[rows]
+    assert_gemm_close(dWt.cpu().double().numpy().T[rows], ref, f"dW col-major {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("n", [4, 8, 16])
