@@ -302,6 +302,8 @@ __global__ void __launch_bounds__(256, 5) prune24_lanes_kernel(const uint4* __re
                                                                int64_t per, uint4* W_out, uint8_t* __restrict__ mask_bytes,
                                                                uint2* __restrict__ vals, void* __restrict__ meta,
                                                                int meta_tc) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t n16 = rows * cols / 8;
   const int64_t lo = ((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5) * per;
@@ -768,6 +770,8 @@ __global__ void __launch_bounds__(256) prune24_tc_tile_kernel(const uint4* __res
                                                               int64_t ldw, uint4* W_out, int64_t ldw_out,
                                                               uint8_t* __restrict__ mask_bytes,
                                                               uint2* __restrict__ vals, uint32_t* __restrict__ meta) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint8_t codes[16][64];
   const int64_t wpr = cols / 8;  // 16-byte words per row
   const int64_t tiles_c = (wpr + 63) / 64, tiles = ((rows + 15) / 16) * tiles_c;
@@ -830,6 +834,8 @@ template <int DT>
 __global__ void __launch_bounds__(256, 5) decompress24_lanes_kernel(const uint2* __restrict__ vals,
                                                                     const uint8_t* __restrict__ meta, int64_t n16,
                                                                     int64_t per, uint4* __restrict__ W_out) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t lo = ((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5) * per;
   const int64_t hi = lo + per < n16 ? lo + per : n16;
@@ -862,6 +868,8 @@ __global__ void __launch_bounds__(256) decompress24_tc_tile_kernel(const uint2* 
                                                                    const uint32_t* __restrict__ meta, int64_t rows,
                                                                    int64_t cols, uint4* __restrict__ W_out,
                                                                    int64_t ldw_out) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint8_t codes[16][64];
   const int64_t wpr = cols / 8;
   const int64_t tiles_c = (wpr + 63) / 64, tiles = ((rows + 15) / 16) * tiles_c;
@@ -979,18 +987,21 @@ cudaError_t prune_dt(const PruneLaunch& a, cudaStream_t s) {
       if constexpr (sizeof(T) == 2) {
         const int64_t tiles = ((a.rowsL + 15) / 16) * ((a.colsL / 8 + 63) / 64);
         const unsigned g = (unsigned)std::min<int64_t>(tiles, (int64_t)num_sms_cached() * 8);
-        prune24_tc_tile_kernel<DT><<<g, 256, 0, s>>>(
-            reinterpret_cast<const uint4*>(W), a.rowsL, a.colsL, a.ld / 8, reinterpret_cast<uint4*>(W_out),
-            a.ld_out / 8, reinterpret_cast<uint8_t*>(a.mask_bits), reinterpret_cast<uint2*>(vals),
-            static_cast<uint32_t*>(a.meta));
+        if (cudaError_t e = launch_pdl(prune24_tc_tile_kernel<DT>, dim3(g), dim3(256), 0, s,
+                                       reinterpret_cast<const uint4*>(W), a.rowsL, a.colsL, a.ld / 8,
+                                       reinterpret_cast<uint4*>(W_out), a.ld_out / 8,
+                                       reinterpret_cast<uint8_t*>(a.mask_bits), reinterpret_cast<uint2*>(vals),
+                                       static_cast<uint32_t*>(a.meta)))
+          return e;
       }
     } else if (lanes) {
       if constexpr (sizeof(T) == 2) {
         const LaneSplit ls = lane_split(a.rowsL * a.colsL / 8);
-        prune24_lanes_kernel<DT><<<ls.grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(W), a.rowsL, a.colsL, ls.per,
-                                                          reinterpret_cast<uint4*>(W_out),
-                                                          reinterpret_cast<uint8_t*>(a.mask_bits),
-                                                          reinterpret_cast<uint2*>(vals), a.meta, a.meta_tc);
+        if (cudaError_t e = launch_pdl(prune24_lanes_kernel<DT>, dim3(ls.grid), dim3(256), 0, s,
+                                       reinterpret_cast<const uint4*>(W), a.rowsL, a.colsL, ls.per,
+                                       reinterpret_cast<uint4*>(W_out), reinterpret_cast<uint8_t*>(a.mask_bits),
+                                       reinterpret_cast<uint2*>(vals), a.meta, a.meta_tc))
+          return e;
       }
     } else if (vec && a.colsL % 32 == 0) {
       const int64_t pairs = a.rowsL * (a.colsL / 32);
@@ -1059,17 +1070,19 @@ cudaError_t decompress_dt(const DecompressLaunch& a, cudaStream_t s) {
     if (pair && sizeof(T) == 2 && a.ld_out == a.cols && !a.meta_tc) {
       if constexpr (sizeof(T) == 2) {
         const LaneSplit ls = lane_split(a.rows * a.cols / 8);
-        decompress24_lanes_kernel<DT><<<ls.grid, 256, 0, s>>>(reinterpret_cast<const uint2*>(vals),
-                                                               static_cast<const uint8_t*>(a.meta), a.rows * a.cols / 8,
-                                                               ls.per, reinterpret_cast<uint4*>(W_out));
+        if (cudaError_t e = launch_pdl(decompress24_lanes_kernel<DT>, dim3(ls.grid), dim3(256), 0, s,
+                                       reinterpret_cast<const uint2*>(vals), static_cast<const uint8_t*>(a.meta),
+                                       a.rows * a.cols / 8, ls.per, reinterpret_cast<uint4*>(W_out)))
+          return e;
       }
     } else if (pair && sizeof(T) == 2 && a.meta_tc && (reinterpret_cast<uintptr_t>(a.meta) & 3u) == 0) {
       if constexpr (sizeof(T) == 2) {
         const int64_t tiles = ((a.rows + 15) / 16) * ((a.cols / 8 + 63) / 64);
         const unsigned g = (unsigned)std::min<int64_t>(tiles, (int64_t)num_sms_cached() * 8);
-        decompress24_tc_tile_kernel<DT><<<g, 256, 0, s>>>(reinterpret_cast<const uint2*>(vals),
-                                                           static_cast<const uint32_t*>(a.meta), a.rows, a.cols,
-                                                           reinterpret_cast<uint4*>(W_out), a.ld_out / 8);
+        if (cudaError_t e = launch_pdl(decompress24_tc_tile_kernel<DT>, dim3(g), dim3(256), 0, s,
+                                       reinterpret_cast<const uint2*>(vals), static_cast<const uint32_t*>(a.meta),
+                                       a.rows, a.cols, reinterpret_cast<uint4*>(W_out), a.ld_out / 8))
+          return e;
       }
     } else if (pair) {
       const int64_t pairs = a.rows * (a.cols / 32);
