@@ -265,6 +265,8 @@ template <int DT, bool SIGNED>
 __global__ void __launch_bounds__(256) vw_score_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_t cols,
                                                        int64_t ld_bytes, uint64_t* __restrict__ keys,
                                                        uint32_t* __restrict__ hist, Ctl* ctl, uint64_t keep) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int kSegElems = DT == kF16 ? 8 : 16;
   constexpr int kSpv = kUnitW / kSegElems;  // segments per vector: 4 (f16) or 2 (int8)
   constexpr int kVecBytes = kSpv * 16;
@@ -326,6 +328,8 @@ template <int DT>
 __global__ void __launch_bounds__(256) bw_score_kernel(const uint8_t* __restrict__ W, int64_t rows, int64_t cols,
                                                        int64_t ld_bytes, uint64_t* __restrict__ keys,
                                                        uint32_t* __restrict__ hist, Ctl* ctl, uint64_t keep) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int kSegElems = DT == kF16 ? 8 : 16;
   constexpr int kSpr = kUnitW / kSegElems;  // segments per block row: 4 or 2
   constexpr int kRowsPer = 32 / kSpr;       // block rows per warp load: 8 or 16
@@ -371,6 +375,8 @@ __global__ void __launch_bounds__(256) bw_score_kernel(const uint8_t* __restrict
 // ---------------------------------------------------------------- threshold
 __global__ void __launch_bounds__(256) candidates_kernel(const uint64_t* __restrict__ keys, int64_t units, Ctl* ctl,
                                                          uint64_t* __restrict__ cand) {
+  pdl_trigger();
+  pdl_wait();
   const int B = ctl->bucket;
   if (B < 0) return;  // T already final (uniform across the grid)
   // A CTA gathers its candidates in shared memory and claims room for them in the global
@@ -513,6 +519,8 @@ __device__ void cta_exclusive_scan(uint32_t* a, int64_t n) {
 // groups, not chunks.
 __global__ void __launch_bounds__(kChunk) count_kernel(const uint64_t* __restrict__ keys, int64_t units, Ctl* ctl,
                                                        uint32_t* __restrict__ cnt_gt, uint32_t* __restrict__ cnt_eq) {
+  pdl_trigger();
+  pdl_wait();
   const uint64_t T = ctl->T;
   const int64_t chunks = (units + kChunk - 1) / kChunk;
   const int64_t groups = (chunks + kCountChunks - 1) / kCountChunks;
@@ -566,6 +574,8 @@ __global__ void __launch_bounds__(kChunk) write_kernel(const uint8_t* __restrict
                                                        const uint32_t* __restrict__ pre_eq, uint8_t* W_out,
                                                        int64_t ldo_bytes, uint32_t* __restrict__ mask,
                                                        int32_t* __restrict__ csr, uint8_t* __restrict__ vals) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int es = DT == kF16 ? 2 : 1;
   constexpr int kSegElems = 16 / es;
   constexpr int kSpr = kUnitW / kSegElems;         // segments per unit row
@@ -882,30 +892,35 @@ cudaError_t launch_blocks_dt(const BlocksLaunch& a, const WsLayout& L, cudaStrea
   const int64_t chunks = (units + kChunk - 1) / kChunk;
   const uint8_t* W = static_cast<const uint8_t*>(a.W);
   if (cudaError_t e = cudaMemsetAsync(ws, 0, L.keys, s)) return e;  // histogram + control block
+  cudaError_t e_;
   if (a.bh == 1) {
     const int64_t segs = a.rows * (a.cols * es / 16);
     if (a.abs_of_sum)
-      vw_score_kernel<DT, true><<<grid_for(segs, 256, 4), 256, 0, s>>>(W, a.rows, a.cols, a.ld * es, keys, hist, ctl,
-                                                                       (uint64_t)a.keep);
+      e_ = launch_pdl(vw_score_kernel<DT, true>, dim3(grid_for(segs, 256, 4)), dim3(256), 0, s, W, a.rows, a.cols,
+                      a.ld * es, keys, hist, ctl, (uint64_t)a.keep);
     else
-      vw_score_kernel<DT, false><<<grid_for(segs, 256, 4), 256, 0, s>>>(W, a.rows, a.cols, a.ld * es, keys, hist, ctl,
-                                                                        (uint64_t)a.keep);
+      e_ = launch_pdl(vw_score_kernel<DT, false>, dim3(grid_for(segs, 256, 4)), dim3(256), 0, s, W, a.rows, a.cols,
+                      a.ld * es, keys, hist, ctl, (uint64_t)a.keep);
   } else {
-    bw_score_kernel<DT><<<grid_for(units * 32, 256, 4), 256, 0, s>>>(W, a.rows, a.cols, a.ld * es, keys, hist, ctl,
-                                                                      (uint64_t)a.keep);
+    e_ = launch_pdl(bw_score_kernel<DT>, dim3(grid_for(units * 32, 256, 4)), dim3(256), 0, s, W, a.rows, a.cols,
+                    a.ld * es, keys, hist, ctl, (uint64_t)a.keep);
   }
-  candidates_kernel<<<grid_for(units, 256, 4), 256, 0, s>>>(keys, units, ctl, cand);
-  count_kernel<<<(unsigned)((chunks + kCountChunks - 1) / kCountChunks), kChunk, 0, s>>>(keys, units, ctl, cgt, ceq);
+  if (e_ != cudaSuccess) return e_;
+  e_ = launch_pdl(candidates_kernel, dim3(grid_for(units, 256, 4)), dim3(256), 0, s, keys, units, ctl, cand);
+  if (e_ != cudaSuccess) return e_;
+  e_ = launch_pdl(count_kernel, dim3((unsigned)((chunks + kCountChunks - 1) / kCountChunks)), dim3(kChunk), 0, s, keys,
+                  units, ctl, cgt, ceq);
+  if (e_ != cudaSuccess) return e_;
   if (a.bh == 1) {
-    write_kernel<DT, false><<<(unsigned)chunks, kChunk, 0, s>>>(
-        W, a.rows, a.cols, a.ld * es, keys, units, ctl, cgt, ceq, static_cast<uint8_t*>(a.W_out), a.ld_out * es,
-        a.mask_bits, a.csr, static_cast<uint8_t*>(a.vals));
+    e_ = launch_pdl(write_kernel<DT, false>, dim3((unsigned)chunks), dim3(kChunk), 0, s, W, a.rows, a.cols, a.ld * es,
+                    keys, units, ctl, cgt, ceq, static_cast<uint8_t*>(a.W_out), a.ld_out * es, a.mask_bits, a.csr,
+                    static_cast<uint8_t*>(a.vals));
   } else {
-    write_kernel<DT, true><<<(unsigned)chunks, kChunk, 0, s>>>(
-        W, a.rows, a.cols, a.ld * es, keys, units, ctl, cgt, ceq, static_cast<uint8_t*>(a.W_out), a.ld_out * es,
-        a.mask_bits, a.csr, static_cast<uint8_t*>(a.vals));
+    e_ = launch_pdl(write_kernel<DT, true>, dim3((unsigned)chunks), dim3(kChunk), 0, s, W, a.rows, a.cols, a.ld * es,
+                    keys, units, ctl, cgt, ceq, static_cast<uint8_t*>(a.W_out), a.ld_out * es, a.mask_bits, a.csr,
+                    static_cast<uint8_t*>(a.vals));
   }
-  return cudaGetLastError();
+  return e_;
 }
 
 }  // namespace

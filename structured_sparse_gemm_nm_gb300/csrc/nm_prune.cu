@@ -434,6 +434,8 @@ __global__ void __launch_bounds__(128) prune32_kernel(const uint16_t* __restrict
                                                       int64_t ld, uint16_t* W_out, int64_t ld_out,
                                                       uint32_t* __restrict__ mask_bits, uint16_t* __restrict__ vals,
                                                       uint8_t* __restrict__ meta) {
+  pdl_trigger();
+  pdl_wait();
   using P = Pair<DT>;
   __shared__ uint4 srow4[128][5];  // the thread's group (64 B) at an 80-byte pitch: conflict-free
   const int64_t gpr = cols / 32;
@@ -680,6 +682,8 @@ template <int U>
 __global__ void __launch_bounds__(256) check24_strips_kernel(const uint4* __restrict__ W, int64_t rows, int64_t wpr,
                                                              int64_t ldw, int transposable, int64_t per,
                                                              int32_t* __restrict__ d_violations) {
+  pdl_trigger();
+  pdl_wait();
   // every warp takes `per` consecutive items (strip, word), U per lane in flight
   const int lane = threadIdx.x & 31;
   const int64_t total = ((rows + 3) / 4) * wpr;
@@ -1028,13 +1032,17 @@ cudaError_t prune_dt(const PruneLaunch& a, cudaStream_t s) {
       uint16_t* Wo16 = reinterpret_cast<uint16_t*>(W_out);
       uint16_t* v16 = reinterpret_cast<uint16_t*>(vals);
       uint8_t* m8 = static_cast<uint8_t*>(a.meta);
+      cudaError_t e_;
       if (a.n == 4)
-        prune32_kernel<DT, 4><<<grid, 128, 0, s>>>(W16, a.rowsL, a.colsL, a.ld, Wo16, a.ld_out, a.mask_bits, v16, m8);
+        e_ = launch_pdl(prune32_kernel<DT, 4>, dim3(grid), dim3(128), 0, s, W16, a.rowsL, a.colsL, a.ld, Wo16, a.ld_out,
+                        a.mask_bits, v16, m8);
       else if (a.n == 8)
-        prune32_kernel<DT, 8><<<grid, 128, 0, s>>>(W16, a.rowsL, a.colsL, a.ld, Wo16, a.ld_out, a.mask_bits, v16, m8);
+        e_ = launch_pdl(prune32_kernel<DT, 8>, dim3(grid), dim3(128), 0, s, W16, a.rowsL, a.colsL, a.ld, Wo16, a.ld_out,
+                        a.mask_bits, v16, m8);
       else
-        prune32_kernel<DT, 16><<<grid, 128, 0, s>>>(W16, a.rowsL, a.colsL, a.ld, Wo16, a.ld_out, a.mask_bits, v16, m8);
-      return cudaGetLastError();
+        e_ = launch_pdl(prune32_kernel<DT, 16>, dim3(grid), dim3(128), 0, s, W16, a.rowsL, a.colsL, a.ld, Wo16,
+                        a.ld_out, a.mask_bits, v16, m8);
+      return e_;
     }
   }
   if (a.mask_bits != nullptr && !a.trans) {
@@ -1116,13 +1124,17 @@ cudaError_t check_dt(const void* W, int64_t rows, int64_t cols, int64_t ld, int 
     // one pass per warp when its share is at most 96 items (12 loads of 16 bytes per lane in
     // flight), else passes of 64
     const uint4* W4 = static_cast<const uint4*>(W);
+    cudaError_t e_;
     if (ls.per <= 32)
-      check24_strips_kernel<1><<<ls.grid, 256, 0, s>>>(W4, rows, wpr, ld / 8, transposable, ls.per, d_violations);
+      e_ = launch_pdl(check24_strips_kernel<1>, dim3(ls.grid), dim3(256), 0, s, W4, rows, wpr, ld / 8, transposable,
+                      ls.per, d_violations);
     else if (ls.per <= 96)
-      check24_strips_kernel<3><<<ls.grid, 256, 0, s>>>(W4, rows, wpr, ld / 8, transposable, ls.per, d_violations);
+      e_ = launch_pdl(check24_strips_kernel<3>, dim3(ls.grid), dim3(256), 0, s, W4, rows, wpr, ld / 8, transposable,
+                      ls.per, d_violations);
     else
-      check24_strips_kernel<2><<<ls.grid, 256, 0, s>>>(W4, rows, wpr, ld / 8, transposable, ls.per, d_violations);
-    return cudaGetLastError();
+      e_ = launch_pdl(check24_strips_kernel<2>, dim3(ls.grid), dim3(256), 0, s, W4, rows, wpr, ld / 8, transposable,
+                      ls.per, d_violations);
+    return e_;
   }
   check_kernel<DT><<<grid_for(work, 256), 256, 0, s>>>(static_cast<const T*>(W), rows, cols, ld, n, m, transposable,
                                                        d_violations);

@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(NB == 1 ? 256 : 1024) gather_kernel(const uint
                                                      uint16_t* __restrict__ D, int64_t M, int64_t N, int64_t K, int n,
                                                      int m, int64_t ldb, int64_t ldc, int64_t ldd, int cd_col,
                                                      float alpha, float beta, int bf16) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint4 xs4[];  // K x NB halves, [k][b]
   uint16_t* xs = reinterpret_cast<uint16_t*>(xs4);
   const int lane = threadIdx.x & 31;
@@ -191,11 +193,12 @@ cudaError_t gather_launch(const SpmmLaunch& a, cudaStream_t s) {
   int64_t blocks = (int64_t)num_sms_cached() * per_sm;
   if (blocks > d.M) blocks = d.M;
   if (blocks < 1) blocks = 1;
-  gather_kernel<NB, NN><<<(unsigned)blocks, threads, smem, s>>>(
-      static_cast<const uint16_t*>(a.A), static_cast<const uint8_t*>(a.A_meta), static_cast<const uint16_t*>(a.B),
-      static_cast<const uint16_t*>(a.C), static_cast<uint16_t*>(a.D), d.M, d.N, d.K, d.n, d.m, d.ldb, d.ldc, d.ldd,
-      d.order_cd == NM_COL, a.alpha_f, a.beta_f, d.ab_type == NM_BF16);
-  return cudaGetLastError();
+  const cudaError_t e_ = launch_pdl(gather_kernel<NB, NN>, dim3((unsigned)blocks), dim3(threads), smem, s,
+                                    static_cast<const uint16_t*>(a.A), static_cast<const uint8_t*>(a.A_meta),
+                                    static_cast<const uint16_t*>(a.B), static_cast<const uint16_t*>(a.C),
+                                    static_cast<uint16_t*>(a.D), d.M, d.N, d.K, d.n, d.m, d.ldb, d.ldc, d.ldd,
+                                    d.order_cd == NM_COL, a.alpha_f, a.beta_f, d.ab_type == NM_BF16);
+  return e_;
 }
 
 }  // namespace
