@@ -215,7 +215,8 @@ class GptNeoTrain:
         L = self.layers[l][j]
         ws, wsb = self.ws[j]
         self.nb.nm_spmm(self.p_dw[j], 1.0, L["dY"], L["mask"], L["X"], 0.0, None, L["dW"], ws if wsb else None, wsb)
-        return 2 if wsb else 1  # the K-split product and its finalize
+        # the product, and the finalize when a K split is not summed inside the product
+        return self.nb.nm_spmm_plan_launches(self.p_dw[j])
 
     def enqueue_one(self, l: int, j: int) -> int:
         """Launch one linear's work (layer l, linear j) on the current stream; returns the launch count."""

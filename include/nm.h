@@ -342,6 +342,15 @@ nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc);
 /* Device workspace bytes nm_spmm needs with this plan (may be 0). */
 nm_status_t nm_spmm_plan_workspace(nm_spmm_plan_t plan, size_t* bytes);
 
+/*
+ * Host-only: the number of kernels one nm_spmm call with this plan launches on
+ * its stream (*launches, host): 0 for an empty D, else 1, or 2 for a
+ * DENSE_MASKED product split along K whose splits a separate kernel sums (the
+ * paired kernel sums two splits itself).  Reflects the plan's algorithm as
+ * chosen by nm_spmm_search when that has run.
+ */
+nm_status_t nm_spmm_plan_launches(nm_spmm_plan_t plan, int* launches);
+
 nm_status_t nm_spmm_plan_destroy(nm_spmm_plan_t plan);
 
 /*

@@ -32,7 +32,8 @@ EXPORTED = (
     "nm_status_string", "nm_version", "nm_last_cuda_error", "nm_compressed_size", "nm_prune", "nm_compress",
     "nm_prune_compress", "nm_decompress",
     "nm_check", "nm_prune_transposable", "nm_sgd_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
-    "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace", "nm_spmm_plan_destroy", "nm_spmm", "nm_spmm_search",
+    "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace",
+    "nm_spmm_plan_launches", "nm_spmm_plan_destroy", "nm_spmm", "nm_spmm_search",
 )
 # Every symbol include/nm_testing.h declares.
 TESTING_EXPORTED = ("nm_test_i8_sparse_mma_rate", "nm_test_spmm_wait_timeout")
@@ -91,6 +92,7 @@ def lib() -> ctypes.CDLL:
             "nm_prune_vector_wise_noalloc": [vp, i64, i64, i64, i32, i32, i64, i32, vp, i64, vp, vp, vp, vp],
             "nm_spmm_plan": [ctypes.POINTER(vp), ctypes.POINTER(SpmmDesc)],
             "nm_spmm_plan_workspace": [vp, ctypes.POINTER(sz)],
+            "nm_spmm_plan_launches": [vp, ctypes.POINTER(i32)],
             "nm_spmm_plan_destroy": [vp],
             "nm_spmm": [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp],
             "nm_spmm_search": [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i32, ctypes.POINTER(i32), vp],
@@ -273,6 +275,12 @@ def nm_spmm_plan_workspace(plan: SpmmPlan) -> int:
     b = ctypes.c_size_t()
     _check(lib().nm_spmm_plan_workspace(plan.handle, ctypes.byref(b)), "nm_spmm_plan_workspace")
     return b.value
+
+
+def nm_spmm_plan_launches(plan: SpmmPlan) -> int:
+    n = ctypes.c_int32()
+    _check(lib().nm_spmm_plan_launches(plan.handle, ctypes.byref(n)), "nm_spmm_plan_launches")
+    return n.value
 
 
 def nm_spmm_plan_destroy(plan: SpmmPlan) -> None:

@@ -480,6 +480,13 @@ nm_status_t nm_spmm_plan_workspace(nm_spmm_plan_t plan, size_t* bytes) {
   return NM_OK;
 }
 
+nm_status_t nm_spmm_plan_launches(nm_spmm_plan_t plan, int* launches) {
+  if (plan == nullptr || launches == nullptr) return NM_ERR_INVALID_ARG;
+  const nm_spmm_desc_t& d = plan->d;
+  *launches = (d.M == 0 || d.N == 0) ? 0 : plan->kind == 1 ? nmk::spmm_tc_dense_masked_launches(d, plan->split_k) : 1;
+  return NM_OK;
+}
+
 nm_status_t nm_spmm_plan_destroy(nm_spmm_plan_t plan) {
   delete plan;
   return NM_OK;

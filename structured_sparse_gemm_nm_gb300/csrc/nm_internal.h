@@ -106,6 +106,9 @@ struct SpmmLaunch {
 cudaError_t launch_spmm_tc_sparse(const SpmmLaunch& a, cudaStream_t s);
 cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaStream_t s);
 size_t spmm_tc_dense_masked_workspace(const nm_spmm_desc_t& d, int split_k);
+// Kernels one call of the masked dense product launches: the product, and the finalize
+// when it splits K and does not sum the splits itself.
+int spmm_tc_dense_masked_launches(const nm_spmm_desc_t& d, int split_k);
 int spmm_tc_dense_masked_split(const nm_spmm_desc_t& d);
 
 // CUDA-core paths: n:m gather (any m <= 32) and 2:4 int8 (mma.sp).

@@ -1693,6 +1693,18 @@ size_t spmm_tc_dense_masked_workspace(const nm_spmm_desc_t& d, int split_k) {
   return split_k > 1 ? (size_t)split_k * tiles * tc::BM * tc::BN * sizeof(float) + tiles * tc::kEpiWarps * 8 : 0;
 }
 
+int spmm_tc_dense_masked_launches(const nm_spmm_desc_t& d, int split_k) {
+  using namespace tc;
+  if (d.K == 0 || d.M == 0 || d.N == 0 || split_k <= 1) return 1;
+  // the launch's own reduction to the splits that are not empty, and its pairing rule
+  const int64_t k_stages = (d.K + kKPerStage - 1) / kKPerStage;
+  const int64_t per = (k_stages + split_k - 1) / split_k;
+  const int64_t splits = (k_stages + per - 1) / per;
+  if (splits <= 1) return 1;
+  const bool pair = use_pair((int)((d.M + BM - 1) / BM), d.algo);
+  return pair && splits == 2 ? 1 : 2;
+}
+
 cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaStream_t s) {
   using namespace tc;
   const nm_spmm_desc_t& d = a.d;

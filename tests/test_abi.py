@@ -296,3 +296,24 @@ def test_sparse_layer_validates_before_touching_the_device():
         SemiStructuredSparseLinear(64, 64, dtype=torch.float32)
     with pytest.raises(ValueError):
         SemiStructuredSparseLinear(64, 64, device="cpu")  # no CPU path
+
+
+def test_plan_launches(lib):
+    """Kernels one nm_spmm call launches: the masked dW sums two K splits inside the paired
+    product (one launch), more splits or single CTAs add the finalize; other products launch one."""
+    def dw_plan(o, i, T, algo=nb.NM_ALGO_DEFAULT):
+        return nb.nm_spmm_plan(nb.make_desc(M=o, N=i, K=T, mode=nb.NM_SPMM_DENSE_MASKED, ab_type="bf16",
+                                            cd_type="bf16", order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_ROW,
+                                            lda=o, ldb=i, ldd=i, meta_layout=nb.NM_META_CANONICAL, algo=algo))
+    cases = [(dw_plan(3072, 768, 16384), 1),                      # two splits, paired
+             (dw_plan(3072, 768, 16384, nb.NM_ALGO_SINGLE), 2),   # two splits, single CTAs: finalize
+             (dw_plan(768, 768, 16384), 2),                       # eight splits: finalize
+             (dw_plan(512, 520, 192), 1),                         # no K split
+             (nb.nm_spmm_plan(nb.make_desc(M=3072, N=16384, K=768, ab_type="bf16", cd_type="bf16", ldb=768,
+                                           ldd=3072)), 1),
+             (nb.nm_spmm_plan(nb.make_desc(M=0, N=16, K=32, ab_type="f16", cd_type="f16", ldb=32, ldd=8)), 0)]
+    for plan, want in cases:
+        assert nb.nm_spmm_plan_launches(plan) == want
+        plan.destroy()
+    with pytest.raises(nb.NmError):
+        nb._check(lib.nm_spmm_plan_launches(None, None), "nm_spmm_plan_launches")
