@@ -878,6 +878,14 @@ __global__ void __launch_bounds__(bw_warps(NB) * 32) bw_spmv_kernel(const SpmmLa
   }
 }
 
+// The histogram and control block set to zero in the launch chain (a memset node would end
+// the chain of dependent launches before the scoring kernel).
+__global__ void __launch_bounds__(256) zero_words_kernel(uint4* __restrict__ p, int64_t n16) {
+  pdl_trigger();
+  pdl_wait();
+  for (int64_t i = threadIdx.x; i < n16; i += blockDim.x) p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 template <int DT>
 cudaError_t launch_blocks_dt(const BlocksLaunch& a, const WsLayout& L, cudaStream_t s) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
@@ -891,7 +899,10 @@ cudaError_t launch_blocks_dt(const BlocksLaunch& a, const WsLayout& L, cudaStrea
   const int64_t units = a.units;
   const int64_t chunks = (units + kChunk - 1) / kChunk;
   const uint8_t* W = static_cast<const uint8_t*>(a.W);
-  if (cudaError_t e = cudaMemsetAsync(ws, 0, L.keys, s)) return e;  // histogram + control block
+  // histogram + control block (L.keys bytes, a multiple of 256)
+  if (cudaError_t e = launch_pdl(zero_words_kernel, dim3(1), dim3(256), 0, s, reinterpret_cast<uint4*>(ws),
+                                 (int64_t)(L.keys / 16)))
+    return e;
   cudaError_t e_;
   if (a.bh == 1) {
     const int64_t segs = a.rows * (a.cols * es / 16);

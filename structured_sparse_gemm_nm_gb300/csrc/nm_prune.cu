@@ -285,9 +285,9 @@ struct LaneSplit {
   unsigned grid;
   int64_t per;  // words per warp
 };
-inline LaneSplit lane_split(int64_t words) {
+inline LaneSplit lane_split(int64_t words, int ctas_per_sm = 5) {
   LaneSplit s;
-  int64_t g = (int64_t)num_sms_cached() * 5;  // five 256-thread CTAs per SM are resident
+  int64_t g = (int64_t)num_sms_cached() * ctas_per_sm;  // up to five 256-thread CTAs per SM are resident
   const int64_t need = (words + 255) / 256;
   if (need < g) g = need;
   if (g < 1) g = 1;
@@ -677,6 +677,14 @@ __device__ __forceinline__ uint32_t nz8(const uint4 x) {
   return ((a >> 15) & 1u) | ((a >> 30) & 2u) | ((b >> 13) & 4u) | ((b >> 28) & 8u) | ((c >> 11) & 16u) |
          ((c >> 26) & 32u) | ((d >> 9) & 64u) | ((d >> 24) & 128u);
 }
+// The check's counter set to zero in the launch chain (a memset node would end the chain of
+// dependent launches before the check).
+__global__ void zero_count_kernel(int32_t* __restrict__ d_violations) {
+  pdl_trigger();
+  pdl_wait();
+  *d_violations = 0;
+}
+
 // U items per lane and pass: a warp's `per` items go out in one pass when per <= 32 U.
 template <int U>
 __global__ void __launch_bounds__(256) check24_strips_kernel(const uint4* __restrict__ W, int64_t rows, int64_t wpr,
@@ -1113,7 +1121,7 @@ template <int DT>
 cudaError_t check_dt(const void* W, int64_t rows, int64_t cols, int64_t ld, int n, int m, int transposable,
                      int32_t* d_violations, cudaStream_t s) {
   using T = typename Elem<DT>::T;
-  cudaError_t e = cudaMemsetAsync(d_violations, 0, sizeof(int32_t), s);
+  cudaError_t e = launch_pdl(zero_count_kernel, dim3(1), dim3(32), 0, s, d_violations);
   if (e != cudaSuccess) return e;
   const int64_t work = rows * (cols / m) + (transposable ? (rows / 4) * cols : 0);
   if (work == 0) return cudaSuccess;

@@ -36,7 +36,14 @@ def test_one_layer_of_the_bench_step_matches_oracle():
     torch.cuda.synchronize()
     launches = wl.enqueue_training_step()
     torch.cuda.synchronize()
-    assert launches == 4 + 4 + 4 + sum(2 if wl.ws[j][1] else 1 for j in range(4))
+    # prune, forward and dX: one kernel each; dW: the product, plus the finalize where its K
+    # splits are not summed inside it (as the plan reports)
+    dw = [nb.nm_spmm_plan_launches(wl.p_dw[j]) for j in range(4)]
+    assert launches == 4 + 4 + 4 + sum(dw)
+    if all(wl.algos[name]["dw"] == "paired" for (name, _, _) in wl.linears):
+        # FC1 and FC2 dW split K in two and sum the splits inside the paired product; QKV (five
+        # splits) and O (seven) keep the finalize
+        assert dw == [2, 2, 1, 1]
     rng = np.random.default_rng(17)
     for j, (name, out_f, in_f) in enumerate(wl.linears):
         L = wl.layers[0][j]
