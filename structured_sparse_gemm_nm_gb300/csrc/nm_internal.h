@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/nm.h"
@@ -116,5 +117,13 @@ cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s);
 cudaError_t launch_spmm_i8(const SpmmLaunch& a, cudaStream_t s);
 // CUDA-core product over kept 1 x 32 vectors (n = 1) or 32 x 32 blocks (n = 32).
 cudaError_t launch_spmm_blocks(const SpmmLaunch& a, cudaStream_t s);
+
+namespace tc {
+// A 2-D tiled tensor map (the driver's encoder; false if it rejects the arguments) and the
+// binding of the current device's primary context that encoding needs.
+bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer,
+              uint64_t pitch_bytes, uint32_t inner_box, uint32_t outer_box, CUtensorMapSwizzle sw);
+cudaError_t bind_context();
+}  // namespace tc
 
 }  // namespace nmk

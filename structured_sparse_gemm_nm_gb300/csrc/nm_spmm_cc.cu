@@ -226,20 +226,22 @@ cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s) {
 // 64-column k-step, which is exactly two consecutive uint16 words of the
 // canonical layout.
 //
-// CTA tile 128 x 128, 8 warps (4 along M x 2 along N, 32 x 64 each), stages of
-// 128 dense K loaded with cp.async into padded shared memory.
+// CTA tile 128 x 128, 8 warps (4 along M x 2 along N, 32 x 64 each), four stages of 128
+// dense K.  A (128 rows x 64 compressed bytes) and B (128 rows x 128 bytes) arrive by TMA
+// in the 64-byte and 128-byte swizzles, which keep the fragment loads free of bank
+// conflicts; the metadata (128 rows x 16 bytes) by cp.async, so that rows past M and a K
+// tail can hold the valid code 0x4 instead of TMA's zero fill.
 namespace {
 
-constexpr int I8_BM = 128, I8_BN = 128, I8_BK = 128, I8_STAGES = 3;
-constexpr int I8_APITCH = 80;   // 64 compressed bytes + 16 pad: conflict-free fragment loads
-constexpr int I8_BPITCH = 144;  // 128 bytes + 16 pad
-constexpr int I8_MPITCH = 16;   // 8 uint16 metadata words per row per stage
-constexpr int I8_ABYTES = I8_BM * I8_APITCH, I8_BBYTES = I8_BN * I8_BPITCH, I8_MBYTES = I8_BM * I8_MPITCH;
-constexpr int I8_STAGE_BYTES = I8_ABYTES + I8_BBYTES + I8_MBYTES;
+constexpr int I8_BM = 128, I8_BN = 128, I8_BK = 128, I8_STAGES = 4;
+constexpr int I8_BBYTES = I8_BN * 128;  // stage offset 0 (1024-byte aligned for the 128-byte swizzle)
+constexpr int I8_ABYTES = I8_BM * 64;   // at 16384 (512-byte aligned for the 64-byte swizzle)
+constexpr int I8_MPITCH = 16;           // 8 uint16 metadata words per row per stage
+constexpr int I8_MBYTES = I8_BM * I8_MPITCH;
+constexpr int I8_STAGE_BYTES = I8_BBYTES + I8_ABYTES + I8_MBYTES;  // 26 KB, a multiple of 1024
+constexpr int I8_TX_BYTES = I8_BBYTES + I8_ABYTES;
+static_assert(I8_STAGE_BYTES % 1024 == 0, "stage alignment");
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -248,48 +250,69 @@ template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+__device__ __forceinline__ void i8_tma_load(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool i8_mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 // OUT8: int8 D (and C) with float scales: D = saturate(rne(alpha * acc + beta * C)), each
 // product and the sum rounded to float32; otherwise int32 D = alpha * acc + beta * C modulo 2^32.
+// A stage barrier that has not completed within `budget` cycles writes NM_ERR_TIMEOUT to
+// *status (nullable) and the CTA stops issuing MMAs (D is then not defined).
 template <bool OUT8>
-__global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const int8_t* __restrict__ A, const uint16_t* __restrict__ meta,
-                                                      const int8_t* __restrict__ B, const void* __restrict__ Cv,
-                                                      void* __restrict__ Dv, int M, int N, int K, int64_t ldb,
-                                                      int64_t ldc, int64_t ldd, int cd_col, int32_t alpha,
-                                                      int32_t beta, float alpha_f, float beta_f) {
+__global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                      const __grid_constant__ CUtensorMap tmB,
+                                                      const uint16_t* __restrict__ meta, const void* __restrict__ Cv,
+                                                      void* __restrict__ Dv, int M, int N, int K, int64_t ldc,
+                                                      int64_t ldd, int cd_col, int32_t alpha, int32_t beta,
+                                                      float alpha_f, float beta_f, int32_t* status, long long budget) {
   extern __shared__ uint4 smem4[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(smem4);
+  __shared__ __align__(8) uint64_t full[I8_STAGES];
+  __shared__ int abort_flag;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int wm = warp & 3, wn = warp >> 2;
   const int m0 = blockIdx.y * I8_BM, n0 = blockIdx.x * I8_BN;
-  const int64_t kc = K / 2;         // compressed bytes per A row
   const int64_t mrow = K / 16;      // uint16 metadata words per row
   const int kstages = (K + I8_BK - 1) / I8_BK;
   const int ksteps = K / 64;        // MMA k-steps in K
+  const uint32_t smem_base = (uint32_t)__cvta_generic_to_shared(smem);
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < I8_STAGES; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(&full[i])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
 
+  int issued = 0;  // stages whose copies have been issued (the same count in every thread)
   auto load_stage = [&](int ks, int buf) {
-    const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem + buf * I8_STAGE_BYTES);
-    // A: 128 rows x 64 bytes = 512 chunks of 16 B
-    for (int c = tid; c < I8_BM * 4; c += 256) {
-      const int r = c >> 2, ch = c & 3;
-      const int64_t kb = (int64_t)ks * 64 + ch * 16;
-      const bool ok = (m0 + r < M) && (kb < kc);
-      cp_async16(base + r * I8_APITCH + ch * 16, ok ? (const void*)(A + (int64_t)(m0 + r) * kc + kb) : (const void*)A, ok);
-    }
-    // B: 128 rows (columns of D) x 128 bytes = 1024 chunks
-    for (int c = tid; c < I8_BN * 8; c += 256) {
-      const int r = c >> 3, ch = c & 7;
-      const int64_t kb = (int64_t)ks * 128 + ch * 16;
-      const bool ok = (n0 + r < N) && (kb < K);
-      cp_async16(base + I8_ABYTES + r * I8_BPITCH + ch * 16,
-                 ok ? (const void*)(B + (int64_t)(n0 + r) * ldb + kb) : (const void*)B, ok);
+    ++issued;
+    const uint32_t base = smem_base + buf * I8_STAGE_BYTES;
+    if (tid == 0) {
+      const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&full[buf]);
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(I8_TX_BYTES) : "memory");
+      i8_tma_load(base, &tmB, bar, ks * 128, n0);
+      i8_tma_load(base + I8_BBYTES, &tmA, bar, ks * 64, m0);
     }
     // metadata: 128 rows x 16 bytes; rows past M (or a K tail) get the valid code 0x4
     if (tid < I8_BM * 2) {
       const int r = tid >> 1, h = tid & 1;
       const int64_t w = (int64_t)ks * 8 + h * 4;
-      const uint32_t dst = base + I8_ABYTES + I8_BBYTES + r * I8_MPITCH + h * 8;
+      const uint32_t dst = base + I8_BBYTES + I8_ABYTES + r * I8_MPITCH + h * 8;
       if (m0 + r < M && w < mrow) {
         cp_async8(dst, meta + (int64_t)(m0 + r) * mrow + w);
       } else {
@@ -310,33 +333,56 @@ __global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const int8_t* __restric
     if (s < kstages) load_stage(s, s);
     cp_commit();
   }
+  bool ok = true;
   for (int ks = 0; ks < kstages; ++ks) {
-    cp_wait<I8_STAGES - 2>();
-    __syncthreads();
+    const int buf = ks % I8_STAGES;
+    cp_wait<I8_STAGES - 2>();  // this thread's metadata copies of stage ks
+    if (ok) {                  // the stage's A and B boxes (bounded wait)
+      const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&full[buf]);
+      const uint32_t parity = (uint32_t)(ks / I8_STAGES) & 1u;
+      if (!i8_mbar_try(bar, parity)) {
+        const long long t0 = clock64();
+        while (!i8_mbar_try(bar, parity)) {
+          if (abort_flag || clock64() - t0 > budget) {
+            if (!abort_flag && status != nullptr) atomicExch(status, (int)NM_ERR_TIMEOUT);
+            abort_flag = 1;
+            ok = false;
+            break;
+          }
+        }
+      }
+    }
+    __syncthreads();  // every thread's metadata copies, and the buffer of stage ks - 1 is free
+    if (abort_flag) ok = false;
     const int nxt = ks + I8_STAGES - 1;
-    if (nxt < kstages) load_stage(nxt, nxt % I8_STAGES);
+    if (ok && nxt < kstages) load_stage(nxt, nxt % I8_STAGES);
     cp_commit();
-    const uint8_t* sa = smem + (ks % I8_STAGES) * I8_STAGE_BYTES;
-    const uint8_t* sb = sa + I8_ABYTES;
-    const uint8_t* sm = sb + I8_BBYTES;
+    if (!ok) continue;
+    const uint8_t* sb = smem + buf * I8_STAGE_BYTES;
+    const uint8_t* sa = sb + I8_BBYTES;
+    const uint8_t* sm = sa + I8_ABYTES;
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       if (ks * 2 + kk >= ksteps) break;  // no MMA past K
       uint32_t bf[8][4];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        const uint8_t* rowp = sb + (wn * 64 + nt * 8 + g) * I8_BPITCH + kk * 64 + t * 4;
+        // 128-byte rows in the 128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)
+        const int rn = wn * 64 + nt * 8 + g;
+        const uint8_t* rowp = sb + rn * 128 + t * 4;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) bf[nt][r] = *reinterpret_cast<const uint32_t*>(rowp + 16 * r);
+        for (int r = 0; r < 4; ++r) bf[nt][r] = *reinterpret_cast<const uint32_t*>(rowp + (((4 * kk + r) ^ (rn & 7)) << 4));
       }
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int rb = wm * 32 + mt * 16;
         uint32_t af[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-          af[r] = *reinterpret_cast<const uint32_t*>(sa + (rb + g + 8 * (r & 1)) * I8_APITCH + kk * 32 + t * 4 +
-                                                     16 * (r >> 1));
+        for (int r = 0; r < 4; ++r) {
+          // 64-byte rows in the 64-byte swizzle: 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)
+          const int ra = rb + g + 8 * (r & 1);
+          af[r] = *reinterpret_cast<const uint32_t*>(sa + ra * 64 + (((2 * kk + (r >> 1)) ^ ((ra >> 1) & 3)) << 4) + t * 4);
+        }
         const uint32_t e =
             *reinterpret_cast<const uint32_t*>(sm + (rb + g + 8 * (t & 1)) * I8_MPITCH + kk * 8 + (t >> 1) * 4);
 #pragma unroll
@@ -352,6 +398,16 @@ __global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const int8_t* __restric
     }
   }
   cp_wait<0>();
+  if (!ok && tid == 0) {
+    // copies still in flight land before the CTA's shared memory is released (bounded): the
+    // last I8_STAGES stages issued use distinct barriers, each with one pending phase at most
+    for (int k = issued > I8_STAGES ? issued - I8_STAGES : 0; k < issued; ++k) {
+      const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&full[k % I8_STAGES]);
+      const long long t0 = clock64();
+      while (!i8_mbar_try(bar, (uint32_t)(k / I8_STAGES) & 1u) && clock64() - t0 < budget) {
+      }
+    }
+  }
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -382,7 +438,8 @@ __global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const int8_t* __restric
 cudaError_t launch_spmm_i8(const SpmmLaunch& a, cudaStream_t s) {
   const nm_spmm_desc_t& d = a.d;
   if (d.K == 0) return cudaErrorInvalidValue;  // rejected by the plan
-  const int smem = I8_STAGES * I8_STAGE_BYTES;
+  if (cudaError_t e = tc::bind_context()) return e;
+  const int smem = I8_STAGES * I8_STAGE_BYTES + 1024;  // + alignment of the stages to 1024 bytes
   const bool out8 = d.cd_type == NM_I8;
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
@@ -395,17 +452,23 @@ cudaError_t launch_spmm_i8(const SpmmLaunch& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     done_mask.fetch_or(bit);
   }
+  // A: M rows of K / 2 compressed bytes; B: N rows (columns of D) of K bytes, ldb apart
+  CUtensorMap mA, mB;
+  if (!tc::make_map(&mA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)(d.K / 2), (uint64_t)d.M, (uint64_t)(d.K / 2),
+                    64, I8_BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !tc::make_map(&mB, a.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)d.K, (uint64_t)d.N, (uint64_t)d.ldb, 128, I8_BN,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const long long budget = 1ll << 32;  // cycles, about two seconds
   dim3 grid((unsigned)((d.N + I8_BN - 1) / I8_BN), (unsigned)((d.M + I8_BM - 1) / I8_BM));
   if (out8)
-    spmm_i8_kernel<true><<<grid, 256, smem, s>>>(static_cast<const int8_t*>(a.A), static_cast<const uint16_t*>(a.A_meta),
-                                                 static_cast<const int8_t*>(a.B), a.C, a.D, (int)d.M, (int)d.N,
-                                                 (int)d.K, d.ldb, d.ldc, d.ldd, d.order_cd == NM_COL, 0, 0, a.alpha_f,
-                                                 a.beta_f);
+    spmm_i8_kernel<true><<<grid, 256, smem, s>>>(mA, mB, static_cast<const uint16_t*>(a.A_meta), a.C, a.D, (int)d.M,
+                                                 (int)d.N, (int)d.K, d.ldc, d.ldd, d.order_cd == NM_COL, 0, 0,
+                                                 a.alpha_f, a.beta_f, a.d_status, budget);
   else
-    spmm_i8_kernel<false><<<grid, 256, smem, s>>>(static_cast<const int8_t*>(a.A), static_cast<const uint16_t*>(a.A_meta),
-                                                  static_cast<const int8_t*>(a.B), a.C, a.D, (int)d.M, (int)d.N,
-                                                  (int)d.K, d.ldb, d.ldc, d.ldd, d.order_cd == NM_COL, a.alpha_i,
-                                                  a.beta_i, 0.0f, 0.0f);
+    spmm_i8_kernel<false><<<grid, 256, smem, s>>>(mA, mB, static_cast<const uint16_t*>(a.A_meta), a.C, a.D, (int)d.M,
+                                                  (int)d.N, (int)d.K, d.ldc, d.ldd, d.order_cd == NM_COL, a.alpha_i,
+                                                  a.beta_i, 0.0f, 0.0f, a.d_status, budget);
   return cudaGetLastError();
 }
 
