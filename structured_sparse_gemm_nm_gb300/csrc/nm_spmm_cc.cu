@@ -257,6 +257,13 @@ __device__ __forceinline__ void i8_tma_load(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// Four 8 x 16-byte matrices: lanes 8i .. 8i + 7 give the row addresses of matrix i, and lane
+// (g, t) receives bytes 4t .. 4t + 3 of row g of matrix i in register i.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
 __device__ __forceinline__ bool i8_mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -361,27 +368,28 @@ __global__ void __launch_bounds__(256, 1) spmm_i8_kernel(const __grid_constant__
     const uint8_t* sb = smem + buf * I8_STAGE_BYTES;
     const uint8_t* sa = sb + I8_BBYTES;
     const uint8_t* sm = sa + I8_ABYTES;
+    const uint32_t sb_u = smem_base + buf * I8_STAGE_BYTES, sa_u = sb_u + I8_BBYTES;
+    const int li = lane & 7, lm = lane >> 3;  // ldmatrix: this lane's row within matrix lm
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       if (ks * 2 + kk >= ksteps) break;  // no MMA past K
       uint32_t bf[8][4];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        // 128-byte rows in the 128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)
-        const int rn = wn * 64 + nt * 8 + g;
-        const uint8_t* rowp = sb + rn * 128 + t * 4;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) bf[nt][r] = *reinterpret_cast<const uint32_t*>(rowp + (((4 * kk + r) ^ (rn & 7)) << 4));
+        // matrix r: the eight B rows (columns of D) of this n-tile, 16-byte chunk 4 kk + r; 128-byte
+        // rows in the 128-byte swizzle: chunk c of row n at chunk c ^ (n & 7)
+        const int rn = wn * 64 + nt * 8 + li;
+        ldsm_x4(sb_u + rn * 128 + (((4 * kk + lm) ^ (rn & 7)) << 4), bf[nt]);
       }
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int rb = wm * 32 + mt * 16;
         uint32_t af[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          // 64-byte rows in the 64-byte swizzle: 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)
-          const int ra = rb + g + 8 * (r & 1);
-          af[r] = *reinterpret_cast<const uint32_t*>(sa + ra * 64 + (((2 * kk + (r >> 1)) ^ ((ra >> 1) & 3)) << 4) + t * 4);
+        {
+          // matrix r: A rows rb + 8 (r & 1) .. + 7, 16-byte chunk 2 kk + (r >> 1); 64-byte rows in the
+          // 64-byte swizzle: chunk c of row m at chunk c ^ ((m >> 1) & 3)
+          const int ra = rb + 8 * (lm & 1) + li;
+          ldsm_x4(sa_u + ra * 64 + (((2 * kk + (lm >> 1)) ^ ((ra >> 1) & 3)) << 4), af);
         }
         const uint32_t e =
             *reinterpret_cast<const uint32_t*>(sm + (rb + g + 8 * (t & 1)) * I8_MPITCH + kk * 8 + (t >> 1) * 4);
