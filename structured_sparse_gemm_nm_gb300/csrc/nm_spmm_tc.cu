@@ -61,6 +61,7 @@
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "nm_device.cuh"
@@ -477,8 +478,9 @@ __device__ __forceinline__ void store_chunk_generic(const Params& p, int row, in
 
 // Split-K summed in the product: the arrival of one epilogue warp at its region of a tile, after
 // its partial stores (this launch's token in the high word; a stale token restarts the count).
-// Returns true for the warp that arrives last; its later reads of the other splits' partials
-// are ordered after their writers' fences by the atomic and the fence that follows it.
+// Returns true for the warp that arrives last (which resets the word); its later reads of the
+// other splits' partials are ordered after their writers' fences by the atomic and the fence
+// that follows it.
 __device__ __forceinline__ bool split_arrive_last(const Params& p, int64_t idx, int lane) {
   __threadfence();  // this lane's partial stores before the arrival
   __syncwarp();
@@ -494,6 +496,9 @@ __device__ __forceinline__ bool split_arrive_last(const Params& p, int64_t idx, 
       old = prev;
     }
     last = (uint32_t)nw == (uint32_t)p.split_k ? 1u : 0u;
+    // every split has arrived: the word returns to 0, which no launch's token equals, so a
+    // workspace that outlives this launch (or this process) holds no count of it
+    if (last) atomicExch(w, 0ull);
     __threadfence();
   }
   return __shfl_sync(0xFFFFFFFFu, last, 0) != 0;
@@ -1726,7 +1731,10 @@ cudaError_t launch_spmm_tc_dense_masked(const SpmmLaunch& a, int split_k, cudaSt
   if (pair && p.split_k == 2) {
     // two splits are summed by the paired product itself: the warp that finishes a tile's region
     // last adds the other split's partial (in split order, as the finalize would) and writes D
-    static std::atomic<uint32_t> launches{0x5A170000u};
+    // tokens differ between launches of this process and, from a per-process start, most
+    // likely from those of another process that used the same memory; never 0
+    static std::atomic<uint32_t> launches{(uint32_t)std::chrono::steady_clock::now().time_since_epoch().count() *
+                                          2654435761u};
     uint32_t token = ++launches;
     if (token == 0) token = ++launches;
     const size_t tiles = (size_t)p.num_m_blk * (size_t)p.num_n_blk;

@@ -466,3 +466,36 @@ def test_i8_sparse_mma_rate_probe():
     assert 10.0 < peak < 5000.0
     with pytest.raises(nb.NmError):
         nb.nm_test_i8_sparse_mma_rate(0)
+
+
+def test_masked_weight_grad_fused_splits_workspace():
+    """Two K splits summed in the paired product: a workspace of garbage works, its arrival
+    words (the last tiles x 8 warps x 8 bytes) are 0 after the call, and a second call on the
+    same workspace gives the same D."""
+    M, N, K, dtype = 3072, 768, 16384, "bf16"
+    dY = inputs.normal((K, M), 1.0, inputs.SEED_DY + K, dtype)
+    X = inputs.normal((K, N), 1.0, inputs.SEED_X + K, dtype)
+    W = inputs.normal((M, N), 0.02, inputs.SEED_W, dtype)
+    _, mask_ref = o.nm_prune(inputs.as_numpy_bits(W), dtype, 2, 4)
+    bits = torch.from_numpy(o.mask_to_bits(mask_ref).view(np.int32)).to(DEV)
+    plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=N, K=K, mode=nb.NM_SPMM_DENSE_MASKED, ab_type=dtype, cd_type=dtype,
+                                        order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_ROW, lda=M, ldb=N,
+                                        ldd=N, meta_layout=nb.NM_META_CANONICAL))
+    assert nb.nm_spmm_plan_launches(plan) == 1
+    ws_bytes = nb.nm_spmm_plan_workspace(plan)
+    ws = torch.full((ws_bytes,), 0xA5, dtype=torch.uint8, device=DEV)
+    words = ((M + 127) // 128) * ((N + 255) // 256) * 8 * 8
+    dYd, Xd = dY.to(DEV), X.to(DEV)
+    outs = []
+    for _ in range(2):
+        dW = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+        nb.nm_spmm(plan, 1.0, dYd, bits, Xd, 0.0, None, dW, ws, ws_bytes)
+        torch.cuda.synchronize()
+        assert int(ws[ws_bytes - words:].count_nonzero().item()) == 0
+        outs.append(dW.view(torch.int16).clone())
+    assert torch.equal(outs[0], outs[1])
+    rows = sample_rows(M, 64, seed=5)
+    ref = o.masked_weight_grad(o.decode(inputs.as_numpy_bits(dY), dtype)[:, rows],
+                               o.decode(inputs.as_numpy_bits(X), dtype), mask_ref[rows])
+    got = outs[0].view(torch.bfloat16).cpu().double().numpy()[rows]
+    assert_gemm_close(got, ref, "fused dW")
