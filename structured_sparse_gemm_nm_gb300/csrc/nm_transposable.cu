@@ -132,7 +132,7 @@ __device__ __forceinline__ uint16_t sgd_elem(uint16_t w, uint16_t g, float nlr) 
 // UPD: the tile is first updated with one SGD step (W <- W - lr * G, written back to W_upd)
 // and the updated values are pruned and compressed.
 template <int DT, bool VEC, bool UPD>
-__global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Elem<DT>::T* W, int64_t rows,
+__global__ void __launch_bounds__(128, 7) transposable_kernel(const typename Elem<DT>::T* W, int64_t rows,
                                                            int64_t cols, int64_t ld, typename Elem<DT>::T* W_out,
                                                            int64_t ld_out, uint32_t* __restrict__ mask_bits,
                                                            typename Elem<DT>::T* __restrict__ vals,
@@ -180,6 +180,20 @@ __global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Ele
         }
       }
     }
+    // the tile packed into 32-bit words (two 16-bit or four 8-bit elements each) while the
+    // patterns are scored
+    constexpr int kEB = 8 * (int)sizeof(T), kWords = (4 * kEB) / 32;
+    uint32_t vw[4][kWords];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+#pragma unroll
+      for (int w = 0; w < kWords; ++w) vw[r][w] = 0u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        vw[r][(c * kEB) >> 5] |= (uint32_t)(sizeof(T) == 2 ? (uint32_t)(uint16_t)v[r][c] : (uint32_t)(uint8_t)v[r][c])
+                                 << ((c * kEB) & 31);
+    }
+    auto elem = [&](int r, int c) -> T { return (T)(vw[r][(c * kEB) >> 5] >> ((c * kEB) & 31)); };
     float p[4][6];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -193,47 +207,34 @@ __global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Ele
       p[r][4] = mg[1] + mg[3];
       p[r][5] = mg[2] + mg[3];
     }
-    // The first pattern in (a, b, c) order with the largest score: the best over c for each
-    // (a, b), then over b, then over a, each comparison keeping the earlier pattern on equal
-    // scores; a tree of short chains instead of one chain of 90 dependent comparisons.
-    // Scores are never NaN (magnitudes are >= 0 or +Inf) and a valid pattern scores >= 0.
+    // The first pattern in (a, b, c) order with the largest score: one chain per row-0 pair a
+    // over its 15 patterns, then the chains in a order, each comparison keeping the earlier
+    // pattern on equal scores.  Scores are never NaN (magnitudes are >= 0 or +Inf) and a valid
+    // pattern scores >= 0.
     auto keep_first = [](float& s, uint32_t& m, float s2, uint32_t m2) {
       if (s2 > s) {
         s = s2;
         m = m2;
       }
     };
-    float sa[6];
-    uint32_t ma[6];
+    float s_best = -1.0f;
+    uint32_t m_best = 0u;
 #pragma unroll
     for (int a = 0; a < 6; ++a) {
-      float sb[6];
-      uint32_t mb[6];
+      float sa = -1.0f;
+      uint32_t ma = 0u;
 #pragma unroll
       for (int b = 0; b < 6; ++b) {
         const float s01 = p[0][a] + p[1][b];
-        sb[b] = -1.0f;
-        mb[b] = 0u;
 #pragma unroll
         for (int c = 0; c < 6; ++c) {
           const int d = completion(a, b, c);
-          if (d >= 0) keep_first(sb[b], mb[b], (s01 + p[2][c]) + p[3][d], tile_mask(a, b, c, d));
+          if (d >= 0) keep_first(sa, ma, (s01 + p[2][c]) + p[3][d], tile_mask(a, b, c, d));
         }
       }
-      keep_first(sb[0], mb[0], sb[1], mb[1]);
-      keep_first(sb[2], mb[2], sb[3], mb[3]);
-      keep_first(sb[4], mb[4], sb[5], mb[5]);
-      keep_first(sb[0], mb[0], sb[2], mb[2]);
-      keep_first(sb[0], mb[0], sb[4], mb[4]);
-      sa[a] = sb[0];
-      ma[a] = mb[0];
+      keep_first(s_best, m_best, sa, ma);
     }
-    keep_first(sa[0], ma[0], sa[1], ma[1]);
-    keep_first(sa[2], ma[2], sa[3], ma[3]);
-    keep_first(sa[4], ma[4], sa[5], ma[5]);
-    keep_first(sa[0], ma[0], sa[2], ma[2]);
-    keep_first(sa[0], ma[0], sa[4], ma[4]);
-    uint32_t bmask = valid ? ma[0] : 0u;
+    uint32_t bmask = valid ? m_best : 0u;
 
     // ---- pruned copy
     if (W_out != nullptr && valid) {
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Ele
       for (int r = 0; r < 4; ++r) {
         T o[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) o[c] = ((bmask >> (4 * r + c)) & 1u) ? v[r][c] : (T)0;
+        for (int c = 0; c < 4; ++c) o[c] = ((bmask >> (4 * r + c)) & 1u) ? elem(r, c) : (T)0;
         store4<VEC>(W_out + (R0 + r) * ld_out + C0, o);
       }
     }
@@ -264,8 +265,8 @@ __global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Ele
         const uint32_t i0 = (km & 1u) ? 0u : ((km & 2u) ? 1u : 2u);
         const uint32_t i1 = (km & 8u) ? 3u : ((km & 4u) ? 2u : 1u);
         if (vals != nullptr && valid) {
-          store2<VEC>(vals + (R0 + r) * (cols / 2) + C0 / 2, (km & 1u) ? v[r][0] : ((km & 2u) ? v[r][1] : v[r][2]),
-                      (km & 8u) ? v[r][3] : ((km & 4u) ? v[r][2] : v[r][1]));
+          store2<VEC>(vals + (R0 + r) * (cols / 2) + C0 / 2, (km & 1u) ? elem(r, 0) : ((km & 2u) ? elem(r, 1) : elem(r, 2)),
+                      (km & 8u) ? elem(r, 3) : ((km & 4u) ? elem(r, 2) : elem(r, 1)));
         }
         if (meta != nullptr) {
           uint32_t code = valid ? (i0 | (i1 << 2)) << (4 * (tcol & 3)) : 0u;
@@ -290,8 +291,8 @@ __global__ void __launch_bounds__(128, 6) transposable_kernel(const typename Ele
         const uint32_t i0 = (km & 1u) ? 0u : ((km & 2u) ? 1u : 2u);
         const uint32_t i1 = (km & 8u) ? 3u : ((km & 4u) ? 2u : 1u);
         if (valsT != nullptr && valid) {
-          store2<VEC>(valsT + (C0 + c) * (rows / 2) + R0 / 2, (km & 1u) ? v[0][c] : ((km & 2u) ? v[1][c] : v[2][c]),
-                      (km & 8u) ? v[3][c] : ((km & 4u) ? v[2][c] : v[1][c]));
+          store2<VEC>(valsT + (C0 + c) * (rows / 2) + R0 / 2, (km & 1u) ? elem(0, c) : ((km & 2u) ? elem(1, c) : elem(2, c)),
+                      (km & 8u) ? elem(3, c) : ((km & 4u) ? elem(2, c) : elem(1, c)));
         }
         if (metaT != nullptr) {
           // four tile rows of the block share one 16-bit word: lanes tcol, tcol+8, tcol+16, tcol+24

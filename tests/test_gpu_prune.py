@@ -24,6 +24,13 @@ def host_matrix(rows, cols, dtype, seed, kind="normal"):
         return inputs.as_numpy_bits(inputs.uniform_int8((rows, cols), seed, -128, 127))
     if kind == "uniform":
         return inputs.as_numpy_bits(inputs.uniform((rows, cols), -1.0, 1.0, seed, dtype))
+    if kind == "ties":  # few distinct magnitudes: most tiles hold several best patterns
+        rng = np.random.default_rng(seed)
+        pool = np.array([0.0, 0.25, -0.25, 0.5, -0.5, 1.0, -1.0], dtype=np.float32)
+        vals = rng.choice(pool, size=(rows, cols))
+        if dtype == "f16":
+            return vals.astype(np.float16).view(np.uint16)
+        return (vals.view(np.uint32) >> 16).astype(np.uint16)
     a = inputs.as_numpy_bits(inputs.normal((rows, cols), 0.02, seed, dtype)).copy()
     if kind == "special":
         rng = np.random.default_rng(seed)
@@ -182,6 +189,8 @@ TRANS_CASES = [
     (44, 20, "f16", nb.NM_META_CANONICAL, "special"),
     (96, 160, "bf16", nb.NM_META_TC, "special"),
     (64, 96, "i8", nb.NM_META_CANONICAL, "normal"),
+    (512, 512, "f16", nb.NM_META_TC, "ties"),         # equal scores: the first pattern must win
+    (68, 200, "bf16", nb.NM_META_CANONICAL, "ties"),
 ]
 
 
