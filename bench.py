@@ -184,7 +184,8 @@ class GptNeoTrain:
             b = self.nb.nm_spmm_search(self.p_dx[j], 1.0, L["valsT"], L["metaT"], L["dY"], 0.0, None, L["dX"])
             c = self.nb.nm_spmm_search(self.p_dw[j], 1.0, L["dY"], L["mask"], L["X"], 0.0, None, L["dW"],
                                        ws if wsb else None, wsb)
-            self.algos[name] = {"fwd": names.get(a, a), "dx": names.get(b, b), "dw": names.get(c, c)}
+            self.algos[name] = {"fwd": names.get(a, a), "dx": names.get(b, b), "dw": names.get(c, c),
+                                "dw_split_k": self.nb.nm_spmm_plan_split_k(self.p_dw[j])}
 
     def gemm_flops(self, j: int) -> float:
         _, o, i = self.linears[j]
@@ -935,11 +936,13 @@ def run_native(args):
 
     wl = GptNeoTrain(torch, nb, inputs, dev, inputs.GPTNEO_LAYERS, inputs.GPTNEO_TOKENS)
     # the native arm's algorithm search (its tensor-core products keep whichever of the paired and
-    # single-CTA kernels measured faster on each shape); --no-search keeps the library's default
+    # single-CTA kernels measured faster on each shape, the dW products also the fastest of the
+    # K splits near the planned one); --no-search keeps the library's default
     # (paired CTAs where M spans an even number of 128-row blocks), e.g. for profiler runs, where
     # the search would time its candidates through the profiler
     if args.no_search:
-        wl.algos = {name: {"fwd": "default", "dx": "default", "dw": "default"} for (name, _, _) in wl.linears}
+        wl.algos = {name: {"fwd": "default", "dx": "default", "dw": "default",
+                           "dw_split_k": nb.nm_spmm_plan_split_k(wl.p_dw[j])} for j, (name, _, _) in enumerate(wl.linears)}
     else:
         wl.search_plans()
     torch.cuda.synchronize()

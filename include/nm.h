@@ -339,7 +339,9 @@ typedef struct nm_spmm_plan_s* nm_spmm_plan_t;
  */
 nm_status_t nm_spmm_plan(nm_spmm_plan_t* plan, const nm_spmm_desc_t* desc);
 
-/* Device workspace bytes nm_spmm needs with this plan (may be 0). */
+/* Device workspace bytes nm_spmm needs with this plan (may be 0).  After
+ * nm_spmm_search the size of the K split it chose, which never exceeds the
+ * workspace_bytes given to the search. */
 nm_status_t nm_spmm_plan_workspace(nm_spmm_plan_t plan, size_t* bytes);
 
 /*
@@ -350,6 +352,14 @@ nm_status_t nm_spmm_plan_workspace(nm_spmm_plan_t plan, size_t* bytes);
  * chosen by nm_spmm_search when that has run.
  */
 nm_status_t nm_spmm_plan_launches(nm_spmm_plan_t plan, int* launches);
+
+/*
+ * nm_spmm_plan_split_k - the number of parts a DENSE_MASKED plan splits K into
+ * (*split_k, host; 1 = not split), as planned or as nm_spmm_search chose; 1
+ * for every other product.  Splits hold whole 64-K stages; the last may be
+ * shorter.
+ */
+nm_status_t nm_spmm_plan_split_k(nm_spmm_plan_t plan, int* split_k);
 
 nm_status_t nm_spmm_plan_destroy(nm_spmm_plan_t plan);
 
@@ -386,12 +396,16 @@ nm_status_t nm_spmm(nm_spmm_plan_t plan, const void* alpha, const void* A, const
  * example: the algorithm-selection step, and the closing paragraph's
  * performance auto-tuning, cusparseLtMatmulSearch).  For a plan whose
  * description asked for NM_ALGO_DEFAULT on a tensor-core product (SPARSE_A
- * 2:4 F16/BF16 or DENSE_MASKED) with M spanning an even number of 128-row
- * blocks, runs the product with NM_ALGO_PAIRED and with NM_ALGO_SINGLE on the
- * given operands in three rounds that alternate the two, each round `repeats`
- * timed runs per algorithm (after one untimed run), timed with CUDA events on
- * `stream`; the plan keeps NM_ALGO_SINGLE only if its fastest round is at
- * least 2% faster than the paired algorithm's, else NM_ALGO_PAIRED.
+ * 2:4 F16/BF16 or DENSE_MASKED), the candidates are NM_ALGO_PAIRED and
+ * NM_ALGO_SINGLE when M spans an even number of 128-row blocks (else the
+ * single-CTA kernel alone) and, for DENSE_MASKED, the plan's K split s and the
+ * splits s - 1, s - 2 and s + 1 that keep at least 8 stages of 64 K per split
+ * and whose workspace fits in workspace_bytes.  It runs every candidate on the
+ * given operands in three rounds that alternate them, each round `repeats`
+ * timed runs per candidate (after one untimed run), timed with CUDA events on
+ * `stream`, and keeps the fastest candidate's best round if it is at least 2%
+ * faster than the default's (paired where possible, split s); else the
+ * default.  Results of different K splits differ by float32 rounding only.
  * Other plans keep their kernel and only report it.  *chosen_algo (nullable,
  * host) receives the algorithm the plan now uses.
  * Arguments are those of nm_spmm; D (and the workspace) are overwritten with

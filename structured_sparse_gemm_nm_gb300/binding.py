@@ -33,7 +33,7 @@ EXPORTED = (
     "nm_prune_compress", "nm_decompress",
     "nm_check", "nm_prune_transposable", "nm_sgd_prune_transposable", "nm_prune_units_workspace", "nm_prune_vector_wise",
     "nm_prune_block_wise", "nm_prune_vector_wise_noalloc", "nm_spmm_plan", "nm_spmm_plan_workspace",
-    "nm_spmm_plan_launches", "nm_spmm_plan_destroy", "nm_spmm", "nm_spmm_search",
+    "nm_spmm_plan_launches", "nm_spmm_plan_split_k", "nm_spmm_plan_destroy", "nm_spmm", "nm_spmm_search",
 )
 # Every symbol include/nm_testing.h declares.
 TESTING_EXPORTED = ("nm_test_i8_sparse_mma_rate", "nm_test_spmm_wait_timeout")
@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "nm_spmm_plan": [ctypes.POINTER(vp), ctypes.POINTER(SpmmDesc)],
             "nm_spmm_plan_workspace": [vp, ctypes.POINTER(sz)],
             "nm_spmm_plan_launches": [vp, ctypes.POINTER(i32)],
+            "nm_spmm_plan_split_k": [vp, ctypes.POINTER(i32)],
             "nm_spmm_plan_destroy": [vp],
             "nm_spmm": [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp],
             "nm_spmm_search": [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i32, ctypes.POINTER(i32), vp],
@@ -280,6 +281,13 @@ def nm_spmm_plan_workspace(plan: SpmmPlan) -> int:
 def nm_spmm_plan_launches(plan: SpmmPlan) -> int:
     n = ctypes.c_int32()
     _check(lib().nm_spmm_plan_launches(plan.handle, ctypes.byref(n)), "nm_spmm_plan_launches")
+    return n.value
+
+
+def nm_spmm_plan_split_k(plan: SpmmPlan) -> int:
+    """K splits of a DENSE_MASKED plan (1 = not split; 1 for other products)."""
+    n = ctypes.c_int32()
+    _check(lib().nm_spmm_plan_split_k(plan.handle, ctypes.byref(n)), "nm_spmm_plan_split_k")
     return n.value
 
 

@@ -480,6 +480,12 @@ nm_status_t nm_spmm_plan_workspace(nm_spmm_plan_t plan, size_t* bytes) {
   return NM_OK;
 }
 
+nm_status_t nm_spmm_plan_split_k(nm_spmm_plan_t plan, int* split_k) {
+  if (plan == nullptr || split_k == nullptr) return NM_ERR_INVALID_ARG;
+  *split_k = plan->kind == 1 ? plan->split_k : 1;
+  return NM_OK;
+}
+
 nm_status_t nm_spmm_plan_launches(nm_spmm_plan_t plan, int* launches) {
   if (plan == nullptr || launches == nullptr) return NM_ERR_INVALID_ARG;
   const nm_spmm_desc_t& d = plan->d;
@@ -549,7 +555,35 @@ nm_status_t nm_spmm_search(nm_spmm_plan_t plan, const void* alpha, const void* A
   nm_spmm_desc_t& d = plan->d;
   const bool tc = plan->kind == 0 || plan->kind == 1;
   const bool even_blocks = ((d.M + 127) / 128) % 2 == 0;
-  if (!tc || !plan->searchable || !even_blocks || d.M == 0 || d.N == 0 || d.K == 0) {
+  if (!tc || !plan->searchable || d.M == 0 || d.N == 0 || d.K == 0) {
+    if (chosen_algo != nullptr) *chosen_algo = d.algo;
+    return NM_OK;
+  }
+  // Candidates (algorithm, K split): the paired and the single-CTA kernel (paired only when M
+  // spans an even number of 128-row blocks); for DENSE_MASKED also the plan's split's
+  // neighbours h - 1, h - 2 and h + 1 whose workspace fits in the caller's.  Candidate 0,
+  // the plan's default, stays unless another is at least 2% faster.
+  struct Cand {
+    int algo, split;
+  };
+  Cand cand[8];
+  int nc = 0;
+  const int h = plan->split_k;
+  int splits[4] = {h, 0, 0, 0}, ns = 1;
+  if (plan->kind == 1) {
+    for (int sk : {h - 1, h - 2, h + 1})
+      if (nmk::spmm_tc_dense_masked_split_ok(d, sk) && nmk::spmm_tc_dense_masked_workspace(d, sk) <= workspace_bytes)
+        splits[ns++] = sk;
+  }
+  for (int j = 0; j < ns; ++j) {
+    if (even_blocks) {
+      cand[nc++] = {NM_ALGO_PAIRED, splits[j]};
+      cand[nc++] = {NM_ALGO_SINGLE, splits[j]};
+    } else {
+      cand[nc++] = {NM_ALGO_DEFAULT, splits[j]};  // the single-CTA kernel
+    }
+  }
+  if (nc == 1) {
     if (chosen_algo != nullptr) *chosen_algo = d.algo;
     return NM_OK;
   }
@@ -559,20 +593,23 @@ nm_status_t nm_spmm_search(nm_spmm_plan_t plan, const void* alpha, const void* A
   cudaStream_t s = (cudaStream_t)stream;
   cudaEvent_t ev[2] = {nullptr, nullptr};
   nm_status_t st = NM_OK;
-  const int cand[2] = {NM_ALGO_PAIRED, NM_ALGO_SINGLE};
-  // Three rounds, the two candidates alternating within each, keep each candidate's fastest
-  // round: one sample per candidate moved with the clock (power capping) and with the event
-  // timer's granularity.  The single-CTA kernel replaces the paired one only when it is at
-  // least 2% faster.
+  auto use = [&](const Cand& c) {
+    d.algo = c.algo;
+    plan->split_k = c.split;
+    plan->ws_bytes = plan->kind == 1 ? nmk::spmm_tc_dense_masked_workspace(d, c.split) : 0;
+  };
+  // Three rounds, the candidates alternating within each, keep each candidate's fastest round:
+  // one sample per candidate moved with the clock (power capping) and with the event timer's
+  // granularity.
   constexpr int kRounds = 3;
-  float best_ms[2] = {0.0f, 0.0f};
+  float best_ms[8] = {};
   for (int round = 0; round < kRounds && st == NM_OK; ++round) {
-    for (int i = 0; i < 2 && st == NM_OK; ++i) {
+    for (int i = 0; i < nc && st == NM_OK; ++i) {
       if (ev[0] == nullptr) {
         if ((st = from_cuda(cudaEventCreate(&ev[0]))) != NM_OK) break;
         if ((st = from_cuda(cudaEventCreate(&ev[1]))) != NM_OK) break;
       }
-      d.algo = cand[i];
+      use(cand[i]);
       // one untimed run, then the timed ones
       if ((st = nm_spmm(plan, alpha, A, A_meta, B, beta, C, D, workspace, workspace_bytes, nullptr, stream)) != NM_OK)
         break;
@@ -587,11 +624,18 @@ nm_status_t nm_spmm_search(nm_spmm_plan_t plan, const void* alpha, const void* A
       if (round == 0 || ms < best_ms[i]) best_ms[i] = ms;
     }
   }
-  const int best = best_ms[1] < 0.98f * best_ms[0] ? NM_ALGO_SINGLE : NM_ALGO_PAIRED;
+  int best = 0;
+  for (int i = 1; i < nc; ++i)
+    if (best_ms[i] < best_ms[best]) best = i;
+  if (!(best_ms[best] < 0.98f * best_ms[0])) best = 0;
   for (cudaEvent_t e : ev)
     if (e != nullptr) cudaEventDestroy(e);
-  d.algo = st == NM_OK ? best : NM_ALGO_DEFAULT;
-  if (st == NM_OK) plan->searchable = false;
+  if (st == NM_OK) {
+    use(cand[best]);
+    plan->searchable = false;
+  } else {
+    use(Cand{NM_ALGO_DEFAULT, h});
+  }
   if (chosen_algo != nullptr) *chosen_algo = d.algo;
   return st;
 }

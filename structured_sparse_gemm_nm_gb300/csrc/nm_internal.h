@@ -111,6 +111,8 @@ size_t spmm_tc_dense_masked_workspace(const nm_spmm_desc_t& d, int split_k);
 // when it splits K and does not sum the splits itself.
 int spmm_tc_dense_masked_launches(const nm_spmm_desc_t& d, int split_k);
 int spmm_tc_dense_masked_split(const nm_spmm_desc_t& d);
+// A K split the masked dense product accepts: 1, or up to 16 splits of at least 8 stages each.
+bool spmm_tc_dense_masked_split_ok(const nm_spmm_desc_t& d, int split_k);
 
 // CUDA-core paths: n:m gather (any m <= 32) and 2:4 int8 (mma.sp).
 cudaError_t launch_spmm_nm_gather(const SpmmLaunch& a, cudaStream_t s);

@@ -1514,7 +1514,7 @@ int num_sms() {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    if (v <= 0) v = 148;
+    if (v <= 0) v = 152;  // no device visible: GB300's count
     cached.store(v);
   }
   return v;
@@ -1690,6 +1690,11 @@ int spmm_tc_dense_masked_split(const nm_spmm_desc_t& d) {
     }
   }
   return best;
+}
+bool spmm_tc_dense_masked_split_ok(const nm_spmm_desc_t& d, int split_k) {
+  using namespace tc;
+  const int64_t stages = (d.K + kKPerStage - 1) / kKPerStage;
+  return split_k == 1 || (split_k > 1 && split_k <= 16 && stages / split_k >= 8);
 }
 size_t spmm_tc_dense_masked_workspace(const nm_spmm_desc_t& d, int split_k) {
   // whole 128 x 256 tiles per split (the tiled partial order of the product's epilogue), then

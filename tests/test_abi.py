@@ -305,15 +305,18 @@ def test_plan_launches(lib):
         return nb.nm_spmm_plan(nb.make_desc(M=o, N=i, K=T, mode=nb.NM_SPMM_DENSE_MASKED, ab_type="bf16",
                                             cd_type="bf16", order_a=nb.NM_COL, order_b=nb.NM_ROW, order_cd=nb.NM_ROW,
                                             lda=o, ldb=i, ldd=i, meta_layout=nb.NM_META_CANONICAL, algo=algo))
-    cases = [(dw_plan(3072, 768, 16384), 1),                      # two splits, paired
-             (dw_plan(3072, 768, 16384, nb.NM_ALGO_SINGLE), 2),   # two splits, single CTAs: finalize
-             (dw_plan(768, 768, 16384), 2),                       # eight splits: finalize
-             (dw_plan(512, 520, 192), 1),                         # no K split
+    cases = [(dw_plan(3072, 768, 16384), 1, 2),                      # two splits, paired
+             (dw_plan(3072, 768, 16384, nb.NM_ALGO_SINGLE), 2, 2),   # two splits, single CTAs: finalize
+             (dw_plan(768, 768, 16384), 2, 7),                       # seven splits: finalize
+             (dw_plan(512, 520, 192), 1, 1),                         # no K split
              (nb.nm_spmm_plan(nb.make_desc(M=3072, N=16384, K=768, ab_type="bf16", cd_type="bf16", ldb=768,
-                                           ldd=3072)), 1),
-             (nb.nm_spmm_plan(nb.make_desc(M=0, N=16, K=32, ab_type="f16", cd_type="f16", ldb=32, ldd=8)), 0)]
-    for plan, want in cases:
+                                           ldd=3072)), 1, 1),
+             (nb.nm_spmm_plan(nb.make_desc(M=0, N=16, K=32, ab_type="f16", cd_type="f16", ldb=32, ldd=8)), 0, 1)]
+    for plan, want, split in cases:
         assert nb.nm_spmm_plan_launches(plan) == want
+        assert nb.nm_spmm_plan_split_k(plan) == split
         plan.destroy()
+    with pytest.raises(nb.NmError):
+        nb._check(lib.nm_spmm_plan_split_k(None, None), "nm_spmm_plan_split_k")
     with pytest.raises(nb.NmError):
         nb._check(lib.nm_spmm_plan_launches(None, None), "nm_spmm_plan_launches")

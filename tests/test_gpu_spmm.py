@@ -350,7 +350,7 @@ def test_sparse_int8_bit_exact(M, N, K, alpha, beta, order_cd, sampled, kind):
     assert np.array_equal(got[rows], ref)
 
 
-@pytest.mark.parametrize("mode", ["sparse", "dense"])
+@pytest.mark.parametrize("mode", ["sparse", "dense", "dense_odd"])
 def test_search_keeps_a_correct_algorithm(mode):
     """Plan-time search (cuSPARSELt blog: algorithm selection, auto-tuning) picks one of the two
     tensor-core kernels, and the plan then computes the product correctly."""
@@ -364,7 +364,9 @@ def test_search_keeps_a_correct_algorithm(mode):
         args = (1.0, vals, meta, X.to(DEV), 0.0, None, D)
         ws, wsb = None, 0
     else:
-        M, N, K = 768, 768, 4096
+        # dense: 6 row blocks (paired and single, K splits near the plan's); dense_odd: 3 row
+        # blocks (the single-CTA kernel, K splits only)
+        M, N, K = (768, 768, 4096) if mode == "dense" else (384, 512, 8192)
         dY = inputs.normal((K, M), 1.0, 33, "bf16")
         X = inputs.normal((K, N), 1.0, 34, "bf16")
         _, mask_ref = o.nm_prune(inputs.as_numpy_bits(inputs.normal((M, N), 0.02, 35, "bf16")), "bf16", 2, 4)
@@ -377,7 +379,13 @@ def test_search_keeps_a_correct_algorithm(mode):
         ws = dev_bytes(wsb) if wsb else None
         args = (1.0, dY.to(DEV), bits, X.to(DEV), 0.0, None, D)
     chosen = nb.nm_spmm_search(plan, *args, workspace=ws, workspace_bytes=wsb, repeats=2)
-    assert chosen in (nb.NM_ALGO_PAIRED, nb.NM_ALGO_SINGLE)
+    if mode == "dense_odd":
+        assert chosen == nb.NM_ALGO_DEFAULT
+    else:
+        assert chosen in (nb.NM_ALGO_PAIRED, nb.NM_ALGO_SINGLE)
+    # the K split it keeps fits in the workspace it was given
+    assert nb.nm_spmm_plan_workspace(plan) <= wsb
+    assert nb.nm_spmm_plan_launches(plan) in (1, 2)
     # searched once: a second call reports the same choice
     assert nb.nm_spmm_search(plan, *args, workspace=ws, workspace_bytes=wsb, repeats=2) == chosen
     D.fill_(float("nan"))
