@@ -408,9 +408,12 @@ __global__ void __launch_bounds__(256) prune_nm_kernel(const typename Elem<DT>::
 // n:32 for 16-bit types (apex PR #1631: "Normally we set M = 32"), one thread
 // per group, aligned rows.  The sign-cleared bit patterns of f16/bf16 order
 // exactly like the magnitudes when compared as half/bfloat16 values (for groups
-// without NaN), so the n-th largest key T is found by a 15-step MSB-first
-// search whose counts use packed compares (two elements per instruction).  The
-// kept set is every key > T plus the lowest-position keys == T.  Kept values are
+// without NaN), so the n-th largest key T is found with packed (two elements
+// per instruction) min/max: a sorting network orders the 16 keys of each
+// half-stream (even and odd positions) at once, and T is the n-th largest of
+// the two sorted lists' union (about 4x fewer instructions than a 15-step
+// bisection over packed compare counts).  The kept set is every key > T plus
+// the lowest-position keys == T.  Kept values are
 // gathered through a padded shared-memory copy of the group.  Groups holding a
 // NaN take an exact scalar path (composite keys), so NaN still ranks first.
 template <int DT> struct Pair;
@@ -418,16 +421,43 @@ template <> struct Pair<kF16> {
   using T2 = __half2;
   static constexpr uint32_t kInf = 0x7C00u;
   __device__ __forceinline__ static T2 as(uint32_t w) { return *reinterpret_cast<const __half2*>(&w); }
-  __device__ __forceinline__ static T2 zero() { return __float2half2_rn(0.0f); }
-  __device__ __forceinline__ static int total(T2 a) { return (int)(__low2float(a) + __high2float(a)); }
+  __device__ __forceinline__ static uint32_t bits(T2 v) { return *reinterpret_cast<const uint32_t*>(&v); }
 };
 template <> struct Pair<kBF16> {
   using T2 = __nv_bfloat162;
   static constexpr uint32_t kInf = 0x7F80u;
   __device__ __forceinline__ static T2 as(uint32_t w) { return *reinterpret_cast<const __nv_bfloat162*>(&w); }
-  __device__ __forceinline__ static T2 zero() { return __float2bfloat162_rn(0.0f); }
-  __device__ __forceinline__ static int total(T2 a) { return (int)(__low2float(a) + __high2float(a)); }
+  __device__ __forceinline__ static uint32_t bits(T2 v) { return *reinterpret_cast<const uint32_t*>(&v); }
 };
+
+// Batcher's odd-even merge sort of 16 elements: 63 compare-exchanges, built at compile time.
+struct CmpX {
+  int a, b;
+};
+struct Batcher16 {
+  CmpX c[63];
+};
+__host__ __device__ constexpr Batcher16 make_batcher16() {
+  Batcher16 r{};
+  int n = 0;
+  for (int p = 1; p < 16; p <<= 1)
+    for (int k = p; k >= 1; k >>= 1)
+      for (int j = k % p; j + k < 16; j += 2 * k)
+        for (int i = 0; i < k && i < 16 - j - k; ++i)
+          if ((i + j) / (2 * p) == (i + j + k) / (2 * p)) r.c[n++] = CmpX{i + j, i + j + k};
+  return r;
+}
+// Sorts 16 packed pairs descending in each half (two elements per compare-exchange).
+template <typename T2>
+__device__ __forceinline__ void sort16_desc(T2 (&t)[16]) {
+  constexpr Batcher16 kNet = make_batcher16();
+#pragma unroll
+  for (int q = 0; q < 63; ++q) {
+    const T2 a = t[kNet.c[q].a], b = t[kNet.c[q].b];
+    t[kNet.c[q].a] = __hmax2(a, b);
+    t[kNet.c[q].b] = __hmin2(a, b);
+  }
+}
 
 template <int DT, int N>
 __global__ void __launch_bounds__(128) prune32_kernel(const uint16_t* __restrict__ W, int64_t rows, int64_t cols,
@@ -473,16 +503,20 @@ __global__ void __launch_bounds__(128) prune32_kernel(const uint16_t* __restrict
     }
     uint32_t kept = 0;
     if (!nan) {
-      uint32_t T = 0;
-#pragma unroll 1
-      for (int b = 14; b >= 0; --b) {
-        const uint32_t cand = T | (1u << b);
-        const typename P::T2 c2 = P::as(cand | (cand << 16));
-        typename P::T2 acc = P::zero();
+      // t[0] >= t[1] >= ... in each half: the keys of the half-stream of even positions (low
+      // halves) and of odd positions (high halves), sorted
+      typename P::T2 t[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc = __hadd2(acc, __hge2(P::as(k[i]), c2));
-        if (P::total(acc) >= N) T = cand;
-      }
+      for (int i = 0; i < 16; ++i) t[i] = P::as(k[i]);
+      sort16_desc(t);
+      static_assert(N >= 1 && N <= 16, "n of 32");
+      // the N-th largest of the union of the two sorted lists A (low halves) and B (high
+      // halves): the largest of B[N-1], A[N-1] and min(A[i-1], B[N-1-i]) for 0 < i < N
+      auto lo = [&](int j) { return P::bits(t[j]) & 0xFFFFu; };
+      auto hi = [&](int j) { return P::bits(t[j]) >> 16; };
+      uint32_t T = max(lo(N - 1), hi(N - 1));
+#pragma unroll
+      for (int i = 1; i < N; ++i) T = max(T, min(lo(i - 1), hi(N - 1 - i)));
       uint32_t gtm = 0, eqm = 0;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {

@@ -24,6 +24,13 @@ def host_matrix(rows, cols, dtype, seed, kind="normal"):
         return inputs.as_numpy_bits(inputs.uniform_int8((rows, cols), seed, -128, 127))
     if kind == "uniform":
         return inputs.as_numpy_bits(inputs.uniform((rows, cols), -1.0, 1.0, seed, dtype))
+    if kind == "tiny":  # subnormal magnitudes (and a few normals) must order exactly
+        rng = np.random.default_rng(seed)
+        scale = 3e-5 if dtype == "f16" else 1e-38
+        vals = (rng.standard_normal((rows, cols)) * scale).astype(np.float32)
+        if dtype == "f16":
+            return vals.astype(np.float16).view(np.uint16)
+        return (vals.view(np.uint32) >> 16).astype(np.uint16)
     if kind == "ties":  # few distinct magnitudes: most tiles hold several best patterns
         rng = np.random.default_rng(seed)
         pool = np.array([0.0, 0.25, -0.25, 0.5, -0.5, 1.0, -1.0], dtype=np.float32)
@@ -74,6 +81,13 @@ PRUNE_CASES = [
     (33, 128, 128, "f16", 16, 32, "special"),
     (40, 64, 64, "bf16", 4, 32, "normal"),
     (110000, 96, 96, "f16", 8, 32, "normal"),    # n:32 grid stride over rows of three groups
+    (64, 256, 256, "f16", 4, 32, "tiny"),        # n:32 with subnormal keys
+    (64, 256, 256, "bf16", 4, 32, "tiny"),
+    (64, 256, 256, "f16", 8, 32, "tiny"),
+    (64, 256, 256, "bf16", 8, 32, "tiny"),
+    (64, 256, 256, "bf16", 16, 32, "tiny"),
+    (128, 256, 256, "bf16", 4, 32, "ties"),      # n:32 with many equal keys at the threshold
+    (128, 256, 256, "f16", 8, 32, "ties"),
     (45, 40, 40, "f16", 3, 8, "special"),
     (64, 64, 64, "i8", 1, 4, "normal"),
     (50, 30, 30, "f16", 2, 5, "normal"),
