@@ -494,13 +494,16 @@ __global__ void __launch_bounds__(128) prune32_kernel(const uint16_t* __restrict
       w[4 * c + 2] = q.z;
       w[4 * c + 3] = q.w;
     }
+    // sign-cleared keys; a half holds a NaN iff key > kInf, i.e. iff key + (0x7FFF - kInf) sets
+    // its bit 15 (the sum stays below 0x10000, so no carry reaches the other half)
     uint32_t k[16];
-    bool nan = false;
+    uint32_t nan_bits = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       k[i] = w[i] & 0x7FFF7FFFu;
-      nan |= ((k[i] & 0xFFFFu) > P::kInf) || ((k[i] >> 16) > P::kInf);
+      nan_bits |= k[i] + (0x7FFFu - P::kInf) * 0x00010001u;
     }
+    const bool nan = (nan_bits & 0x80008000u) != 0u;
     uint32_t kept = 0;
     if (!nan) {
       // t[0] >= t[1] >= ... in each half: the keys of the half-stream of even positions (low
