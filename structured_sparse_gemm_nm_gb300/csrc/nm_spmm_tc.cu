@@ -1422,16 +1422,25 @@ __global__ void __launch_bounds__(256) finalize_split_rows_kernel(const float4* 
   const int slab = blockIdx.x - (int)tile * (BN / 32);
   const int64_t per_split = (int64_t)num_m_blk * num_n_blk * (BM * BN / 4);
   const float4* src = part + tile * (BM * BN / 4) + (int64_t)slab * 8 * BM;  // column groups 8 slab .. 8 slab + 7
+  // each element summed in split order; a split's four loads per thread are independent, so
+  // they (and, unrolled, the next split's) are in flight together
+  float4 x[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) x[k] = src[threadIdx.x + 256 * k];
+#pragma unroll 2
+  for (int sp = 1; sp < splits; ++sp) {
+    const float4* ps = src + (int64_t)sp * per_split;
+    float4 y[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = ps[threadIdx.x + 256 * k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k].x += y[k].x, x[k].y += y[k].y, x[k].z += y[k].z, x[k].w += y[k].w;
+  }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int e = threadIdx.x + 256 * k;  // (column group g, row r) = (e / 128, e % 128)
-    float4 x = src[e];
-    for (int sp = 1; sp < splits; ++sp) {
-      const float4 y = src[(int64_t)sp * per_split + e];
-      x.x += y.x, x.y += y.y, x.z += y.z, x.w += y.w;
-    }
     const int g = e / BM, r = e - g * BM;
-    sm[r][4 * g] = x.x, sm[r][4 * g + 1] = x.y, sm[r][4 * g + 2] = x.z, sm[r][4 * g + 3] = x.w;
+    sm[r][4 * g] = x[k].x, sm[r][4 * g + 1] = x[k].y, sm[r][4 * g + 2] = x[k].z, sm[r][4 * g + 3] = x[k].w;
   }
   __syncthreads();
   const int64_t m0 = (tile / num_n_blk) * BM, n0 = (tile % num_n_blk) * BN + 32 * slab;
