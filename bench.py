@@ -1121,8 +1121,8 @@ def run_native(args):
 # ------------------------------------------------------------------ single-kernel cases (ncu captures)
 LINEARS = {"qkv": (2304, 768), "o": (768, 768), "fc1": (3072, 768), "fc2": (768, 3072)}  # out x in
 SPARSE_CASES = tuple(f"sparse_{lin}_{d}" for lin in LINEARS for d in ("fwd", "dx"))
-KERNEL_CASES = SPARSE_CASES + ("dense_fc1_dw", "transposable_fc1", "prune24_4096", "prune_8of32_4096",
-                               "gemv_8of32_b8", "vector_wise_4096", "check24_4096")
+KERNEL_CASES = SPARSE_CASES + ("dense_fc1_dw", "dense_o_dw", "transposable_fc1", "prune24_4096",
+                               "prune_8of32_4096", "gemv_8of32_b8", "vector_wise_4096", "check24_4096")
 
 
 def run_kernel_case(name: str, reps: int = 3):
@@ -1148,8 +1148,10 @@ def run_kernel_case(name: str, reps: int = 3):
         Y = torch.empty((T, M), dtype=torch.bfloat16, device=dev)
         plan = nb.nm_spmm_plan(nb.make_desc(M=M, N=T, K=K, ab_type="bf16", cd_type="bf16", ldb=K, ldd=M))
         fn = [lambda: nb.nm_spmm(plan, 1.0, vals, meta, X, 0.0, None, Y)]
-    elif name in ("dense_fc1_dw", "transposable_fc1"):
-        o, i = 3072, 768  # FC1 weight (out x in); FC2 dX has the same M, K
+    elif name in ("dense_fc1_dw", "dense_o_dw", "transposable_fc1"):
+        # FC1 weight (out x in; FC2 dX has the same M, K), or the O weight, whose dW sums seven
+        # K splits in the separate finalize
+        o, i = (768, 768) if name == "dense_o_dw" else (3072, 768)
         W = inputs.normal((o, i), 0.02, 1, "bf16", device=dev)
         vb, mb = nb.nm_compressed_size(o, i, "bf16", 2, 4, nb.NM_META_TC)
         vals, meta = (torch.empty(vb, dtype=torch.uint8, device=dev), torch.empty(mb, dtype=torch.uint8, device=dev))
