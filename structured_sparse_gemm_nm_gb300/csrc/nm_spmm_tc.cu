@@ -1422,19 +1422,31 @@ __global__ void __launch_bounds__(256) finalize_split_rows_kernel(const float4* 
   const int slab = blockIdx.x - (int)tile * (BN / 32);
   const int64_t per_split = (int64_t)num_m_blk * num_n_blk * (BM * BN / 4);
   const float4* src = part + tile * (BM * BN / 4) + (int64_t)slab * 8 * BM;  // column groups 8 slab .. 8 slab + 7
-  // each element summed in split order; a split's four loads per thread are independent, so
-  // they (and, unrolled, the next split's) are in flight together
+  // each element summed in split order; the loads of up to five splits (four float4 each per
+  // thread) are issued before their adds, so five splits cost one round trip to memory
+  constexpr int kChunk = 5;
   float4 x[4];
+  for (int c0 = 0; c0 < splits; c0 += kChunk) {
+    float4 y[kChunk][4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) x[k] = src[threadIdx.x + 256 * k];
-#pragma unroll 2
-  for (int sp = 1; sp < splits; ++sp) {
-    const float4* ps = src + (int64_t)sp * per_split;
-    float4 y[4];
+    for (int j = 0; j < kChunk; ++j) {
+      if (c0 + j >= splits) break;
+      const float4* ps = src + (int64_t)(c0 + j) * per_split;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) y[k] = ps[threadIdx.x + 256 * k];
+      for (int k = 0; k < 4; ++k) y[j][k] = ps[threadIdx.x + 256 * k];
+    }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) x[k].x += y[k].x, x[k].y += y[k].y, x[k].z += y[k].z, x[k].w += y[k].w;
+    for (int j = 0; j < kChunk; ++j) {
+      if (c0 + j >= splits) break;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (c0 + j == 0) {
+          x[k] = y[j][k];
+        } else {
+          x[k].x += y[j][k].x, x[k].y += y[j][k].y, x[k].z += y[j][k].z, x[k].w += y[j][k].w;
+        }
+      }
+    }
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
