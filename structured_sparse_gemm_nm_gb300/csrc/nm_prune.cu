@@ -410,8 +410,9 @@ __global__ void __launch_bounds__(256) prune_nm_kernel(const typename Elem<DT>::
 // exactly like the magnitudes when compared as half/bfloat16 values (for groups
 // without NaN), so the n-th largest key T is found with packed (two elements
 // per instruction) min/max: a sorting network orders the 16 keys of each
-// half-stream (even and odd positions) at once, and T is the n-th largest of
-// the two sorted lists' union (about 4x fewer instructions than a 15-step
+// half-stream (even and odd positions) at once (for n = 4 a selection network
+// that keeps only the 4 largest), and T is the n-th largest of the two sorted
+// lists' union (about 4x fewer instructions than a 15-step
 // bisection over packed compare counts).  The kept set is every key > T plus
 // the lowest-position keys == T.  Kept values are
 // gathered through a padded shared-memory copy of the group.  Groups holding a
@@ -457,6 +458,41 @@ __device__ __forceinline__ void sort16_desc(T2 (&t)[16]) {
     t[kNet.c[q].a] = __hmax2(a, b);
     t[kNet.c[q].b] = __hmin2(a, b);
   }
+}
+
+// The 4 largest of 16 packed pairs, sorted descending in each half, into t[0..3]: each group of
+// four sorted (5 compare-exchanges), then pairs of sorted fours merged by taking
+// max(a[i], b[3 - i]) (the top four, in bitonic order) and a 4-element bitonic sort.
+template <typename T2>
+__device__ __forceinline__ void cmpx_desc(T2& a, T2& b) {
+  const T2 hi = __hmax2(a, b), lo = __hmin2(a, b);
+  a = hi;
+  b = lo;
+}
+template <typename T2>
+__device__ __forceinline__ void top4_desc(T2 (&t)[16]) {
+#pragma unroll
+  for (int o = 0; o < 16; o += 4) {
+    cmpx_desc(t[o], t[o + 1]);
+    cmpx_desc(t[o + 2], t[o + 3]);
+    cmpx_desc(t[o], t[o + 2]);
+    cmpx_desc(t[o + 1], t[o + 3]);
+    cmpx_desc(t[o + 1], t[o + 2]);
+  }
+  auto merge = [&](int oa, int ob) {
+    T2 m[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m[i] = __hmax2(t[oa + i], t[ob + 3 - i]);
+    cmpx_desc(m[0], m[2]);
+    cmpx_desc(m[1], m[3]);
+    cmpx_desc(m[0], m[1]);
+    cmpx_desc(m[2], m[3]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t[oa + i] = m[i];
+  };
+  merge(0, 4);
+  merge(8, 12);
+  merge(0, 8);
 }
 
 template <int DT, int N>
@@ -511,7 +547,10 @@ __global__ void __launch_bounds__(128) prune32_kernel(const uint16_t* __restrict
       typename P::T2 t[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) t[i] = P::as(k[i]);
-      sort16_desc(t);
+      if constexpr (N == 4)
+        top4_desc(t);  // only the 4 largest are needed
+      else
+        sort16_desc(t);
       static_assert(N >= 1 && N <= 16, "n of 32");
       // the N-th largest of the union of the two sorted lists A (low halves) and B (high
       // halves): the largest of B[N-1], A[N-1] and min(A[i-1], B[N-1-i]) for 0 < i < N
